@@ -1,0 +1,175 @@
+"""ORACLE (test infrastructure only).
+
+A plain, slow, single-threaded CPU restatement of the routed-expert MoE FFN
+with a quantized expert cache, used to check the CUDA path.  Only the tests,
+``__graft_entry__.smoke()`` and the benchmark's CPU-baseline leg may import
+it.  It shares no code with the CUDA library, and the library never calls it.
+
+- ``moe_oracle.c``: numerics (top-k, activation quantization, Q4 block dots,
+  SwiGLU, down projection and combine), binary64 with the integer-deciding
+  steps in binary32 (see the header of that file);
+- ``policy.py``: the admission / eviction policy of the expert pools.
+
+Parity pins: every function here is checked by ``tests/test_oracle_*.py``
+against brute force, closed forms, library routines or hand-traced
+sequences; nothing here is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+from .policy import PolicyOracle  # noqa: F401
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.c")
+_OUT = os.path.join(_HERE, "_build", "liboracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle into oracle/_build/liboracle.so (if stale)."""
+    if (not force and os.path.exists(_OUT)
+            and os.path.getmtime(_OUT) >= os.path.getmtime(_SRC)):
+        return _OUT
+    os.makedirs(os.path.dirname(_OUT), exist_ok=True)
+    tmp = _OUT + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
+           _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _OUT)
+    return _OUT
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        L = ctypes.CDLL(build())
+        i32, vp, f32 = ctypes.c_int, ctypes.c_void_p, ctypes.c_float
+        L.orc_h2d.restype = ctypes.c_double
+        L.orc_h2d.argtypes = [ctypes.c_uint16]
+        L.orc_f2h.restype = ctypes.c_uint16
+        L.orc_f2h.argtypes = [f32]
+        L.orc_topk.argtypes = [vp, i32, i32, i32, i32, vp, vp]
+        L.orc_quantize_blocks.argtypes = [vp, i32, vp, vp]
+        L.orc_dequant.argtypes = [vp, i32, vp]
+        L.orc_block_dot.restype = ctypes.c_int32
+        L.orc_block_dot.argtypes = [vp, vp]
+        L.orc_row_dot.restype = ctypes.c_double
+        L.orc_row_dot.argtypes = [vp, vp, vp, i32, vp]
+        L.orc_expert.argtypes = [vp, vp, vp, i32, i32, vp, vp] + [vp] * 8
+        L.orc_down_combine.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]
+        L.orc_layer.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp] + [vp] * 9
+        _lib = L
+    return _lib
+
+
+def _p(a):
+    if a is None:
+        return None
+    assert isinstance(a, np.ndarray) and a.flags["C_CONTIGUOUS"], "needs a C-contiguous array"
+    return a.ctypes.data
+
+
+def h2d(bits: int) -> float:
+    return float(lib().orc_h2d(int(bits)))
+
+
+def f2h(x: float) -> int:
+    return int(lib().orc_f2h(float(x)))
+
+
+def topk(logits: np.ndarray, k: int, renorm: bool = True):
+    logits = np.ascontiguousarray(logits, np.float32)
+    T, E = logits.shape
+    idx = np.empty((T, k), np.int32)
+    w = np.empty((T, k), np.float64)
+    lib().orc_topk(_p(logits), T, E, k, int(renorm), _p(idx), _p(w))
+    return idx, w
+
+
+def quantize(x: np.ndarray):
+    """x fp32 [..., n] (n % 32 == 0) -> (q int8 [..., n], d uint16 [..., n/32])."""
+    x = np.ascontiguousarray(x, np.float32)
+    n = x.size
+    q = np.empty(x.shape, np.int8)
+    d = np.empty(x.shape[:-1] + (x.shape[-1] // 32,), np.uint16)
+    lib().orc_quantize_blocks(_p(x), n, _p(q), _p(d))
+    return q, d
+
+
+def dequant(blocks: np.ndarray) -> np.ndarray:
+    """Canonical Q4 blocks [..., nb, 18] -> float64 [..., nb*32]."""
+    blocks = np.ascontiguousarray(blocks, np.uint8)
+    nb = blocks.size // 18
+    out = np.empty(blocks.shape[:-2] + (blocks.shape[-2] * 32,), np.float64)
+    lib().orc_dequant(_p(blocks), nb, _p(out))
+    return out
+
+
+def block_dot(block: np.ndarray, qa: np.ndarray) -> int:
+    block = np.ascontiguousarray(block, np.uint8)
+    qa = np.ascontiguousarray(qa, np.int8)
+    return int(lib().orc_block_dot(_p(block), _p(qa)))
+
+
+def row_dot(row: np.ndarray, qa: np.ndarray, da: np.ndarray):
+    row = np.ascontiguousarray(row, np.uint8)
+    qa = np.ascontiguousarray(qa, np.int8)
+    da = np.ascontiguousarray(da, np.uint16)
+    a = np.zeros(1, np.float64)
+    r = lib().orc_row_dot(_p(row), _p(qa), _p(da), row.size // 18, _p(a))
+    return float(r), float(a[0])
+
+
+def _expert_ptrs(tensor):
+    """Expert tensor given as an array [E, rows, nb, 18] or a dict {e: [rows, nb, 18]}."""
+    if isinstance(tensor, dict):
+        E = max(tensor) + 1
+        arrs = {e: np.ascontiguousarray(v, np.uint8) for e, v in tensor.items()}
+        ptrs = (ctypes.c_void_p * E)(*[arrs[e].ctypes.data if e in arrs else None for e in range(E)])
+        return ptrs, arrs
+    t = np.ascontiguousarray(tensor, np.uint8)
+    ptrs = (ctypes.c_void_p * t.shape[0])(*[t[e].ctypes.data for e in range(t.shape[0])])
+    return ptrs, t
+
+
+def layer(x, idx, w, gate, up, down, H, F, want_intermediates=False):
+    """Whole layer: y float64 [T,H] (+ intermediates per assignment)."""
+    x = np.ascontiguousarray(x, np.float32)
+    idx = np.ascontiguousarray(idx, np.int32)
+    w = np.ascontiguousarray(w, np.float64)
+    T, k = idx.shape
+    gp, g_keep = _expert_ptrs(gate)
+    upp, u_keep = _expert_ptrs(up)
+    dp, d_keep = _expert_ptrs(down)
+    y = np.empty((T, H), np.float64)
+    out = {}
+    if want_intermediates:
+        A = T * k
+        out = dict(xq=np.empty((T, H), np.int8), xd=np.empty((T, H // 32), np.uint16),
+                   g=np.empty((A, F)), u=np.empty((A, F)), gabs=np.empty((A, F)), uabs=np.empty((A, F)),
+                   h=np.empty((A, F)), hq=np.empty((A, F), np.int8), hd=np.empty((A, F // 32), np.uint16))
+    o = out
+    lib().orc_layer(T, H, F, k, _p(x), _p(idx), _p(w), ctypes.cast(gp, ctypes.c_void_p),
+                    ctypes.cast(upp, ctypes.c_void_p), ctypes.cast(dp, ctypes.c_void_p), _p(y),
+                    _p(o.get("xq")), _p(o.get("xd")), _p(o.get("g")), _p(o.get("u")), _p(o.get("gabs")),
+                    _p(o.get("uabs")), _p(o.get("h")), _p(o.get("hq")), _p(o.get("hd")))
+    del g_keep, u_keep, d_keep
+    return (y, out) if want_intermediates else y
+
+
+def down_combine(idx, w, down, hq, hd, H, F):
+    idx = np.ascontiguousarray(idx, np.int32)
+    w = np.ascontiguousarray(w, np.float64)
+    hq = np.ascontiguousarray(hq, np.int8)
+    hd = np.ascontiguousarray(hd, np.uint16)
+    T, k = idx.shape
+    dp, keep = _expert_ptrs(down)
+    y = np.empty((T, H), np.float64)
+    lib().orc_down_combine(T, H, F, k, _p(idx), _p(w), ctypes.cast(dp, ctypes.c_void_p), _p(hq), _p(hd), _p(y))
+    del keep
+    return y

@@ -1,0 +1,269 @@
+/*
+ * ORACLE for the routed-expert MoE feed-forward with a quantized expert cache.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This is a plain, slow, single-threaded CPU
+ * restatement of what the hot path computes, used to check the CUDA path.
+ * Only the tests, the smoke check and the benchmark's CPU-baseline leg may
+ * load it.  It shares no code, header, table or constant with the CUDA
+ * library, and the CUDA library never calls it.
+ *
+ * Sources (page titles and sections):
+ *  [A2] Zapdev-labs/a6000-custom-kernels -- the pointer-table GEMV diagram
+ *       ("router (top-8 of 512 experts, per layer)", moe_cache_gemv) and the
+ *       paragraph on the MMVQ dot kernels and "the full MMVQ fusion argument
+ *       set (... GLU ...)".
+ *  [M4] mx-llama.cpp FEATURES.md -- activation quantization to q8_1 reused
+ *       by the matmuls that share one input (router and gate/up).
+ *  [S5] mihailescu2m/llama.cpp -- "the graph-shape problem" (top-k of 512
+ *       expert scores).
+ *  Format of the weights: Q4 blocks of 32 weights with one binary16 scale d
+ *  and 4-bit codes q, w = d * (q - 8) (the block-quantized weight format of
+ *  the workloads); byte j of the 16 code bytes holds element j in its low
+ *  nibble and element j+16 in its high nibble (the canonical Q4 block order).
+ *
+ * Readings where the pages are silent (each listed in the design notes):
+ *  - top-k order is (logit descending, expert index ascending): ties go to
+ *    the lower index; -0.0 and +0.0 tie;
+ *  - routing weights are the softmax over the k selected logits
+ *    (renormalized top-k); renorm=0 gives the softmax over all E logits;
+ *  - activation blocks of 32: d = binary16(amax / 127) computed in binary32,
+ *    q_i = clamp(rint(x_i / d), -127, 127) in binary32 with round-half-even,
+ *    using the stored binary16 scale; an all-zero block (d == 0) gives q = 0;
+ *  - SwiGLU: h = silu(gate) * up = g * u / (1 + exp(-g));
+ *  - the expert FFN output is combined as y[t] = sum_j w[t,j] * o[t,j].
+ *
+ * Precision: the exact values of the method are computed in binary64.  The
+ * two places where floating point decides an integer (the code of an
+ * activation element and the binary16 scale of a block) take that decision
+ * in binary32, the precision the CUDA path uses, after rounding the binary64
+ * value of h to binary32.  Compile with -ffp-contract=off.
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <string.h>
+
+#define ORC_BLOCK 32
+#define ORC_BLOCK_BYTES 18
+
+/* ---- binary16 <-> binary64/32 from the IEEE 754 definition ------------- */
+
+/* Value of binary16 bits h: (-1)^s * 2^(e-15) * 1.m for 1 <= e <= 30,
+ * (-1)^s * 2^-14 * 0.m for e = 0, inf/NaN for e = 31. */
+double orc_h2d(uint16_t h) {
+    int s = (h >> 15) & 1, e = (h >> 10) & 31, m = h & 1023;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -24);
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + m), e - 25);
+    return s ? -v : v;
+}
+
+/* binary32 -> binary16, round to nearest, ties to even.  The quantum of the
+ * binade holding |f| is 2^(max(e,-14)-10); |f| divided by it is exact in
+ * binary64, and rounding that quotient to an integer (ties to even) picks the
+ * nearest binary16 value.  A carry to 2048 moves into the next binade, which
+ * the encoding handles by itself. */
+uint16_t orc_f2h(float f) {
+    double v = (double)f;
+    uint16_t sign = signbit(v) ? 0x8000 : 0;
+    double a = fabs(v);
+    if (isnan(v)) return (uint16_t)(sign | 0x7e00);
+    if (a >= 65520.0) return (uint16_t)(sign | 0x7c00);
+    if (a == 0.0) return sign;
+    int ex;
+    frexp(a, &ex); /* a = fr * 2^ex, fr in [0.5, 1) -> binade exponent ex-1 */
+    int e = ex - 1;
+    if (e < -14) e = -14;
+    double quantum = ldexp(1.0, e - 10);
+    double r = nearbyint(a / quantum); /* default rounding: ties to even */
+    uint32_t bits;
+    if (r < 1024.0) /* subnormal: value r * 2^-24, encoding is r */
+        bits = (uint32_t)r;
+    else
+        bits = ((uint32_t)(e + 15) << 10) + ((uint32_t)r - 1024u);
+    return (uint16_t)(sign | bits);
+}
+
+/* ---- [S5]/[A2] router top-k ---------------------------------------------- */
+
+/* For each token t: idx[t][0..k) = the k experts with the largest logits,
+ * in order (logit desc, index asc); w[t][j] = routing weight.  O(k*E). */
+void orc_topk(const float *logits, int T, int E, int k, int renorm, int32_t *idx, double *w) {
+    for (int t = 0; t < T; ++t) {
+        const float *l = logits + (size_t)t * E;
+        int32_t *id = idx + (size_t)t * k;
+        for (int j = 0; j < k; ++j) {
+            int best = -1;
+            for (int e = 0; e < E; ++e) {
+                int taken = 0;
+                for (int i = 0; i < j; ++i)
+                    if (id[i] == e) taken = 1;
+                if (taken) continue;
+                if (best < 0 || l[e] > l[best]) best = e; /* strict: ties keep the lower index */
+            }
+            id[j] = best;
+        }
+        double m = (double)l[id[0]];
+        double den = 0.0;
+        if (renorm) {
+            for (int j = 0; j < k; ++j) den += exp((double)l[id[j]] - m);
+        } else {
+            for (int e = 0; e < E; ++e) den += exp((double)l[e] - m);
+        }
+        for (int j = 0; j < k; ++j) w[(size_t)t * k + j] = exp((double)l[id[j]] - m) / den;
+    }
+}
+
+/* ---- [M4] activation quantization, int8 blocks of 32 + binary16 scale ---- */
+
+void orc_quantize_blocks(const float *x, int n, int8_t *q, uint16_t *d) {
+    for (int b = 0; b < n / ORC_BLOCK; ++b) {
+        const float *xb = x + (size_t)b * ORC_BLOCK;
+        float amax = 0.0f;
+        for (int i = 0; i < ORC_BLOCK; ++i) {
+            float a = fabsf(xb[i]);
+            if (a > amax) amax = a;
+        }
+        float d32 = amax / 127.0f;
+        uint16_t dh = orc_f2h(d32);
+        float dd = (float)orc_h2d(dh);
+        d[b] = dh;
+        for (int i = 0; i < ORC_BLOCK; ++i) {
+            int v = 0;
+            if (dd != 0.0f) {
+                float r = rintf(xb[i] / dd);
+                if (r > 127.0f) r = 127.0f;
+                if (r < -127.0f) r = -127.0f;
+                v = (int)r;
+            }
+            q[(size_t)b * ORC_BLOCK + i] = (int8_t)v;
+        }
+    }
+}
+
+/* ---- Q4 weights ------------------------------------------------------------ */
+
+/* 4-bit code of element i (0..31) of a canonical 18-byte block. */
+static int orc_code(const uint8_t *blk, int i) {
+    const uint8_t *qs = blk + 2;
+    return i < 16 ? (qs[i] & 15) : (qs[i - 16] >> 4);
+}
+
+static uint16_t orc_block_scale(const uint8_t *blk) { return (uint16_t)(blk[0] | (blk[1] << 8)); }
+
+/* Dequantized weights of nb blocks: w = d * (q - 8). */
+void orc_dequant(const uint8_t *blocks, int nb, double *out) {
+    for (int b = 0; b < nb; ++b) {
+        const uint8_t *blk = blocks + (size_t)b * ORC_BLOCK_BYTES;
+        double d = orc_h2d(orc_block_scale(blk));
+        for (int i = 0; i < ORC_BLOCK; ++i) out[(size_t)b * ORC_BLOCK + i] = d * (double)(orc_code(blk, i) - 8);
+    }
+}
+
+/* [A2] integer block dot: sum_i (q_w,i - 8) * q_a,i, exact in int32. */
+int32_t orc_block_dot(const uint8_t *blk, const int8_t *qa) {
+    int32_t s = 0;
+    for (int i = 0; i < ORC_BLOCK; ++i) s += (int32_t)(orc_code(blk, i) - 8) * (int32_t)qa[i];
+    return s;
+}
+
+/* One weight row (nb blocks) against one quantized activation vector:
+ * r = sum_b d_w,b * d_a,b * sumi_b, in binary64, block order.  abs_sum gets
+ * sum_b |d_w,b * d_a,b * sumi_b| (for error bounds), if not NULL. */
+double orc_row_dot(const uint8_t *row, const int8_t *qa, const uint16_t *da, int nb, double *abs_sum) {
+    double acc = 0.0, aacc = 0.0;
+    for (int b = 0; b < nb; ++b) {
+        const uint8_t *blk = row + (size_t)b * ORC_BLOCK_BYTES;
+        int32_t s = orc_block_dot(blk, qa + (size_t)b * ORC_BLOCK);
+        double term = orc_h2d(orc_block_scale(blk)) * orc_h2d(da[b]) * (double)s;
+        acc += term;
+        aacc += fabs(term);
+    }
+    if (abs_sum) *abs_sum = aacc;
+    return acc;
+}
+
+/* ---- [A2] one routed expert on one token: gate/up, SwiGLU, quantize, down --- */
+
+/* gate, up: F rows x (H/32) blocks; down: H rows x (F/32) blocks (canonical).
+ * Outputs (any may be NULL except o): g, u, |terms| sums of g and u, h (binary64),
+ * hq/hd (the quantized h), o (binary64, H values). */
+void orc_expert(const uint8_t *gate, const uint8_t *up, const uint8_t *down, int H, int F, const int8_t *xq,
+                const uint16_t *xd, double *g_out, double *u_out, double *gabs, double *uabs, double *h_out,
+                int8_t *hq_out, uint16_t *hd_out, double *o) {
+    int nbh = H / ORC_BLOCK, nbf = F / ORC_BLOCK;
+    size_t rowh = (size_t)nbh * ORC_BLOCK_BYTES, rowf = (size_t)nbf * ORC_BLOCK_BYTES;
+    float h32[F > 0 ? F : 1];
+    int8_t hq[F > 0 ? F : 1];
+    uint16_t hd[F / ORC_BLOCK > 0 ? F / ORC_BLOCK : 1];
+    for (int r = 0; r < F; ++r) {
+        double ga, ua;
+        double g = orc_row_dot(gate + r * rowh, xq, xd, nbh, &ga);
+        double u = orc_row_dot(up + r * rowh, xq, xd, nbh, &ua);
+        double h = g * u / (1.0 + exp(-g));
+        if (g_out) g_out[r] = g;
+        if (u_out) u_out[r] = u;
+        if (gabs) gabs[r] = ga;
+        if (uabs) uabs[r] = ua;
+        if (h_out) h_out[r] = h;
+        h32[r] = (float)h;
+    }
+    orc_quantize_blocks(h32, F, hq, hd);
+    if (hq_out) memcpy(hq_out, hq, (size_t)F);
+    if (hd_out) memcpy(hd_out, hd, sizeof(uint16_t) * (size_t)nbf);
+    for (int i = 0; i < H; ++i) o[i] = orc_row_dot(down + i * rowf, hq, hd, nbf, NULL);
+}
+
+/* Down projection + combine from given quantized h (one entry per
+ * assignment a = t*k + j): y[t] = sum_j w[t,j] * (W_down[idx[t,j]] . h_a). */
+void orc_down_combine(int T, int H, int F, int k, const int32_t *idx, const double *w,
+                      const uint8_t *const *down, const int8_t *hq, const uint16_t *hd, double *y) {
+    int nbf = F / ORC_BLOCK;
+    size_t rowf = (size_t)nbf * ORC_BLOCK_BYTES;
+    for (int t = 0; t < T; ++t) {
+        double *yt = y + (size_t)t * H;
+        for (int i = 0; i < H; ++i) yt[i] = 0.0;
+        for (int j = 0; j < k; ++j) {
+            size_t a = (size_t)t * k + j;
+            const uint8_t *dn = down[idx[a]];
+            for (int i = 0; i < H; ++i)
+                yt[i] += w[a] * orc_row_dot(dn + i * rowf, hq + a * F, hd + a * nbf, nbf, NULL);
+        }
+    }
+}
+
+/*
+ * A whole MoE FFN layer on T tokens with given routing (idx, w):
+ *   quantize x_t; for each j: expert idx[t,j] -> o; y[t] = sum_j w[t,j] o_j.
+ * Expert tensors are passed as arrays of E pointers (entries not referenced
+ * by idx may be NULL).  Per-assignment outputs (a = t*k + j) are optional.
+ */
+void orc_layer(int T, int H, int F, int k, const float *x, const int32_t *idx, const double *w,
+               const uint8_t *const *gate, const uint8_t *const *up, const uint8_t *const *down, double *y,
+               int8_t *xq_out, uint16_t *xd_out, double *g_out, double *u_out, double *gabs, double *uabs,
+               double *h_out, int8_t *hq_out, uint16_t *hd_out) {
+    int nbh = H / ORC_BLOCK, nbf = F / ORC_BLOCK;
+    int8_t xq[H];
+    uint16_t xd[H / ORC_BLOCK];
+    double o[H];
+    for (int t = 0; t < T; ++t) {
+        orc_quantize_blocks(x + (size_t)t * H, H, xq, xd);
+        if (xq_out) memcpy(xq_out + (size_t)t * H, xq, (size_t)H);
+        if (xd_out) memcpy(xd_out + (size_t)t * nbh, xd, sizeof(uint16_t) * (size_t)nbh);
+        double *yt = y + (size_t)t * H;
+        for (int i = 0; i < H; ++i) yt[i] = 0.0;
+        for (int j = 0; j < k; ++j) {
+            size_t a = (size_t)t * k + j;
+            int e = idx[a];
+            orc_expert(gate[e], up[e], down[e], H, F, xq, xd, g_out ? g_out + a * F : NULL,
+                       u_out ? u_out + a * F : NULL, gabs ? gabs + a * F : NULL, uabs ? uabs + a * F : NULL,
+                       h_out ? h_out + a * F : NULL, hq_out ? hq_out + a * F : NULL,
+                       hd_out ? hd_out + a * nbf : NULL, o);
+            for (int i = 0; i < H; ++i) yt[i] += w[a] * o[i];
+        }
+    }
+}

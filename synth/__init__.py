@@ -1,0 +1,233 @@
+"""Seeded synthetic inputs for the routed-expert MoE FFN workloads.
+
+Shared, as data, by the CPU oracle and the CUDA path.  Nothing here computes
+any step of the method: the module draws random numbers and lays them out in
+the canonical input formats (fp32 activations and logits, canonical 18-byte Q4
+blocks, expert permutations, seeding orders and pool capacities).
+
+The C core (``synth.c``) is compiled on first use with the system C compiler.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import subprocess
+from dataclasses import dataclass, field
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "synth.c")
+_OUT = os.path.join(_HERE, "_build", "libsynth.so")
+_lib = None
+
+# Stream ids of the key tuple (seed, stream, a, b, c).
+STREAM_WEIGHTS = 1
+STREAM_X = 2
+STREAM_LOGITS = 3
+STREAM_PERM = 4
+
+KIND_GATE, KIND_UP, KIND_DOWN = 0, 1, 2
+Q4_BLOCK_BYTES = 18
+
+
+def build(force: bool = False) -> str:
+    """Compile the C generator into synth/_build/libsynth.so (if stale)."""
+    if (not force and os.path.exists(_OUT)
+            and os.path.getmtime(_OUT) >= os.path.getmtime(_SRC)):
+        return _OUT
+    os.makedirs(os.path.dirname(_OUT), exist_ok=True)
+    tmp = _OUT + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared",
+           "-pthread", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _OUT)
+    return _OUT
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        L = ctypes.CDLL(build())
+        u64, i32, sz = ctypes.c_uint64, ctypes.c_int, ctypes.c_size_t
+        vp, dbl = ctypes.c_void_p, ctypes.c_double
+        L.synth_key.restype = u64
+        L.synth_key.argtypes = [u64, u64, u64, u64, u64]
+        L.synth_uniform_f64.argtypes = [u64, vp, sz]
+        L.synth_normal_f32.argtypes = [u64, vp, sz]
+        L.synth_q4_blocks.argtypes = [u64, vp, sz, dbl, dbl]
+        L.synth_q4_experts.argtypes = [u64, u64, i32, i32, sz, vp, dbl, dbl, i32]
+        L.synth_permutation.argtypes = [u64, vp, i32]
+        L.synth_gumbel_logits.argtypes = [u64, vp, i32, i32, vp]
+        _lib = L
+    return _lib
+
+
+def _ptr(a: np.ndarray) -> int:
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data
+
+
+def key(seed: int, stream: int, a: int = 0, b: int = 0, c: int = 0) -> int:
+    return int(lib().synth_key(seed, stream, a, b, c))
+
+
+def uniform(k: int, n: int) -> np.ndarray:
+    out = np.empty(n, np.float64)
+    lib().synth_uniform_f64(k, _ptr(out), n)
+    return out
+
+
+def normal(k: int, shape) -> np.ndarray:
+    out = np.empty(shape, np.float32)
+    lib().synth_normal_f32(k, _ptr(out), out.size)
+    return out
+
+
+def q4_blocks(k: int, n_blocks: int, dlo: float = 0.005, dhi: float = 0.02) -> np.ndarray:
+    out = np.empty((n_blocks, Q4_BLOCK_BYTES), np.uint8)
+    lib().synth_q4_blocks(k, _ptr(out), n_blocks, dlo, dhi)
+    return out
+
+
+def q4_experts(seed: int, tensor_tag: int, e_begin: int, e_end: int, rows: int, cols: int,
+               out: np.ndarray | None = None, dlo: float = 0.005, dhi: float = 0.02,
+               threads: int | None = None) -> np.ndarray:
+    """Canonical Q4 weights of experts [e_begin, e_end) of one expert tensor.
+
+    Shape [n, rows, cols/32, 18] uint8; expert e's bytes do not depend on the
+    range it was generated in, nor on the thread count.
+    """
+    assert cols % 32 == 0
+    n = e_end - e_begin
+    nbe = rows * (cols // 32)
+    if out is None:
+        out = np.empty((n, rows, cols // 32, Q4_BLOCK_BYTES), np.uint8)
+    assert out.nbytes == n * nbe * Q4_BLOCK_BYTES and out.flags["C_CONTIGUOUS"]
+    if threads is None:
+        threads = max(1, min(16, os.cpu_count() or 1))
+    lib().synth_q4_experts(seed, tensor_tag, e_begin, e_end, nbe, _ptr(out), dlo, dhi, threads)
+    return out
+
+
+def permutation(k: int, n: int) -> np.ndarray:
+    out = np.empty(n, np.int32)
+    lib().synth_permutation(k, _ptr(out), n)
+    return out
+
+
+def gumbel_logits(k: int, base: np.ndarray, T: int) -> np.ndarray:
+    base = np.ascontiguousarray(base, np.float64)
+    E = base.shape[0]
+    out = np.empty((T, E), np.float32)
+    lib().synth_gumbel_logits(k, _ptr(base), T, E, _ptr(out))
+    return out
+
+
+def zipf_probs(E: int, s: float) -> np.ndarray:
+    """p(r) proportional to r^-s for ranks r = 1..E."""
+    w = np.arange(1, E + 1, dtype=np.float64) ** (-s)
+    return w / w.sum()
+
+
+# ---------------------------------------------------------------------------
+# Workloads.  Each names its shapes, routing popularity and pool residency.
+# ---------------------------------------------------------------------------
+
+@dataclass
+class Workload:
+    name: str
+    hidden: int
+    n_experts: int
+    top_k: int
+    ffn: int
+    n_layers: int
+    # popularity of the expert ranked r (1-based) under a per-layer
+    # permutation: "normal" (plain N(0,1) logits), "zipf", or "mix".
+    routing: str = "normal"
+    zipf_s: float = 1.1
+    mix_uniform: float = 0.0
+    seed: int = 0
+    # pool slots per layer (same for gate/up/down of a layer); None = all.
+    capacity: list | None = None
+    phases: list = field(default_factory=list)  # (label, n_tokens, n_steps)
+
+    @property
+    def tensor_shapes(self):
+        H, F = self.hidden, self.ffn
+        return {KIND_GATE: (F, H), KIND_UP: (F, H), KIND_DOWN: (H, F)}
+
+    def tensor_tag(self, layer: int, kind: int) -> int:
+        return layer * 3 + kind
+
+    def expert_tensor(self, layer: int, kind: int, e_begin: int = 0, e_end: int | None = None,
+                      out=None, threads=None) -> np.ndarray:
+        rows, cols = self.tensor_shapes[kind]
+        if e_end is None:
+            e_end = self.n_experts
+        return q4_experts(self.seed, self.tensor_tag(layer, kind), e_begin, e_end, rows, cols,
+                          out=out, threads=threads)
+
+    def popularity(self) -> np.ndarray | None:
+        E = self.n_experts
+        if self.routing == "zipf":
+            return zipf_probs(E, self.zipf_s)
+        if self.routing == "mix":
+            return self.mix_uniform / E + (1.0 - self.mix_uniform) * zipf_probs(E, self.zipf_s)
+        return None
+
+    def perm(self, layer: int) -> np.ndarray:
+        """perm[r] = the expert holding popularity rank r+1 in this layer."""
+        return permutation(key(self.seed, STREAM_PERM, layer), self.n_experts)
+
+    def seed_order(self, layer: int) -> np.ndarray:
+        """Synthetic routing-frequency table: experts by expected pick
+        frequency, most frequent first (rank order of the popularity)."""
+        if self.routing == "normal":
+            return np.arange(self.n_experts, dtype=np.int32)
+        return self.perm(layer).astype(np.int32)
+
+    def layer_capacity(self, layer: int) -> int:
+        if self.capacity is None:
+            return self.n_experts
+        return int(self.capacity[layer])
+
+    def x(self, layer: int, step: int, T: int, phase: int = 0) -> np.ndarray:
+        return normal(key(self.seed, STREAM_X, layer, step, phase), (T, self.hidden))
+
+    def logits(self, layer: int, step: int, T: int, phase: int = 0) -> np.ndarray:
+        k = key(self.seed, STREAM_LOGITS, layer, step, phase)
+        p = self.popularity()
+        if p is None:
+            return normal(k, (T, self.n_experts))
+        perm = self.perm(layer)
+        base = np.empty(self.n_experts, np.float64)
+        base[perm] = np.log(p)
+        return gumbel_logits(k, base, T)
+
+    def tensor_bytes(self, kind: int) -> int:
+        rows, cols = self.tensor_shapes[kind]
+        return rows * (cols // 32) * Q4_BLOCK_BYTES
+
+
+def _c1_capacity(L=48, E=512):
+    # 40 layers fully resident, the other 8 hold a 60% hot set.
+    part = int(math.floor(0.6 * E))
+    return [part] * 8 + [E] * (L - 8)
+
+
+WORKLOADS = {
+    "tiny": Workload("tiny", hidden=256, n_experts=8, top_k=2, ffn=512, n_layers=1,
+                     routing="normal", seed=0, phases=[("decode", 4, 1)]),
+    "decode_b1_resident": Workload("decode_b1_resident", 2048, 512, 8, 1152, 48, routing="zipf",
+                                   zipf_s=1.1, capacity=_c1_capacity(), phases=[("decode", 1, 128)]),
+    "decode_b1_pool25": Workload("decode_b1_pool25", 2048, 512, 8, 1152, 48, routing="zipf",
+                                 zipf_s=1.1, capacity=[128] * 48, phases=[("decode", 1, 256)]),
+    "prefill_t4096": Workload("prefill_t4096", 2048, 512, 8, 1152, 48, routing="zipf", zipf_s=1.1,
+                              capacity=[384] * 48, phases=[("prefill", 4096, 1)]),
+    "large_expert": Workload("large_expert", 2880, 128, 4, 2880, 36, routing="mix", zipf_s=0.8,
+                             mix_uniform=0.5, capacity=[64] * 36,
+                             phases=[("prefill", 512, 1), ("prefill", 4096, 1), ("prefill", 12288, 1),
+                                     ("decode", 1, 16), ("decode", 8, 16), ("decode", 32, 16)]),
+}

@@ -1,0 +1,221 @@
+/*
+ * Seeded synthetic inputs for the routed-expert MoE FFN workloads.
+ *
+ * This module only produces input data: pseudo-random streams, normal
+ * deviates, canonical Q4 weight blocks, permutations and Gumbel-perturbed
+ * router logits.  It holds none of the method's arithmetic (no routing,
+ * quantization, dot product or cache policy) and is shared, as data, by the
+ * CPU oracle and by the CUDA path.
+ *
+ * Generators (published definitions, restated here):
+ *   - splitmix64 (Steele, Lea, Flood 2014) to derive stream keys and seeds;
+ *   - xoshiro256** (Blackman, Vigna 2018) as the stream generator;
+ *   - Box-Muller (1958) for N(0,1), in double precision, rounded to float;
+ *   - Gumbel(0,1) as -ln(-ln U).
+ *
+ * Every stream is keyed by a tuple (seed, stream id, a, b, c), so any part
+ * of a workload can be generated on its own, in parallel, in any order.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <string.h>
+
+static uint64_t sm64_next(uint64_t *state) {
+    uint64_t z = (*state += 0x9E3779B97F4A7C15ull);
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+/* Mix a tuple into one 64-bit stream key. */
+uint64_t synth_key(uint64_t seed, uint64_t stream, uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t s = seed;
+    uint64_t k = sm64_next(&s);
+    uint64_t parts[4] = {stream, a, b, c};
+    for (int i = 0; i < 4; ++i) {
+        s = k ^ (parts[i] + 0x632BE59BD9B4E019ull * (uint64_t)(i + 1));
+        k = sm64_next(&s);
+    }
+    return k;
+}
+
+typedef struct {
+    uint64_t s[4];
+} xo_t;
+
+static inline uint64_t rotl64(uint64_t x, int k) { return (x << k) | (x >> (64 - k)); }
+
+static void xo_init(xo_t *g, uint64_t key) {
+    uint64_t s = key;
+    for (int i = 0; i < 4; ++i) g->s[i] = sm64_next(&s);
+}
+
+static inline uint64_t xo_next(xo_t *g) {
+    uint64_t *s = g->s;
+    const uint64_t result = rotl64(s[1] * 5, 7) * 9;
+    const uint64_t t = s[1] << 17;
+    s[2] ^= s[0];
+    s[3] ^= s[1];
+    s[1] ^= s[2];
+    s[0] ^= s[3];
+    s[2] ^= t;
+    s[3] = rotl64(s[3], 45);
+    return result;
+}
+
+/* Uniform in [0,1) with 53 random bits. */
+static inline double xo_unit(xo_t *g) { return (double)(xo_next(g) >> 11) * 0x1.0p-53; }
+/* Uniform in (0,1]. */
+static inline double xo_unit_open(xo_t *g) { return (double)((xo_next(g) >> 11) + 1) * 0x1.0p-53; }
+
+/* float -> IEEE binary16 bits, round to nearest even.  Used only to store the
+ * generated Q4 block scales in their on-disk format. */
+static uint16_t gen_f16_bits(float f) {
+    uint32_t x;
+    memcpy(&x, &f, 4);
+    uint32_t sign = (x >> 16) & 0x8000u;
+    uint32_t ax = x & 0x7fffffffu;
+    if (ax >= 0x7f800000u) return (uint16_t)(sign | 0x7c00u | (ax > 0x7f800000u ? 0x200u : 0u));
+    if (ax >= 0x477ff000u) return (uint16_t)(sign | 0x7c00u); /* >= 65520 rounds to inf */
+    if (ax < 0x38800000u) {                                  /* below 2^-14: subnormal */
+        float v;
+        memcpy(&v, &ax, 4);
+        double r = nearbyint((double)v * 16777216.0);
+        return (uint16_t)(sign | (uint32_t)r);
+    }
+    uint32_t e = (ax >> 23) - 127u + 15u;
+    uint32_t m = ax & 0x7fffffu;
+    uint32_t h = (e << 10) | (m >> 13);
+    uint32_t rem = m & 0x1fffu;
+    if (rem > 0x1000u || (rem == 0x1000u && (h & 1u))) h++;
+    return (uint16_t)(sign | h);
+}
+
+void synth_uniform_f64(uint64_t key, double *out, size_t n) {
+    xo_t g;
+    xo_init(&g, key);
+    for (size_t i = 0; i < n; ++i) out[i] = xo_unit(&g);
+}
+
+/* N(0,1) deviates (Box-Muller, both outputs of each pair used). */
+void synth_normal_f32(uint64_t key, float *out, size_t n) {
+    xo_t g;
+    xo_init(&g, key);
+    const double two_pi = 6.283185307179586476925286766559;
+    size_t i = 0;
+    while (i < n) {
+        double u1 = xo_unit_open(&g);
+        double u2 = xo_unit(&g);
+        double r = sqrt(-2.0 * log(u1));
+        out[i++] = (float)(r * cos(two_pi * u2));
+        if (i < n) out[i++] = (float)(r * sin(two_pi * u2));
+    }
+}
+
+/*
+ * Canonical Q4 blocks of 32 weights, 18 bytes each: a little-endian binary16
+ * scale d ~ U(dlo, dhi) (rounded to binary16), then 16 bytes of 4-bit codes
+ * q ~ U{0..15}.  Byte j holds element j in its low nibble and element j+16 in
+ * its high nibble.  The generator draws the 16 code bytes as two 64-bit words.
+ */
+void synth_q4_blocks(uint64_t key, uint8_t *out, size_t n_blocks, double dlo, double dhi) {
+    xo_t g;
+    xo_init(&g, key);
+    for (size_t b = 0; b < n_blocks; ++b) {
+        uint8_t *blk = out + b * 18;
+        double d = dlo + (dhi - dlo) * xo_unit(&g);
+        uint16_t h = gen_f16_bits((float)d);
+        blk[0] = (uint8_t)(h & 0xff);
+        blk[1] = (uint8_t)(h >> 8);
+        uint64_t w0 = xo_next(&g), w1 = xo_next(&g);
+        for (int j = 0; j < 8; ++j) {
+            blk[2 + j] = (uint8_t)(w0 >> (8 * j));
+            blk[10 + j] = (uint8_t)(w1 >> (8 * j));
+        }
+    }
+}
+
+typedef struct {
+    uint64_t seed, tag;
+    int e0, e1;
+    size_t blocks_per_expert;
+    uint8_t *out;
+    double dlo, dhi;
+} q4_job_t;
+
+static void *q4_worker(void *arg) {
+    q4_job_t *j = (q4_job_t *)arg;
+    for (int e = j->e0; e < j->e1; ++e) {
+        uint64_t key = synth_key(j->seed, 1, j->tag, (uint64_t)e, 0);
+        synth_q4_blocks(key, j->out + (size_t)e * j->blocks_per_expert * 18, j->blocks_per_expert, j->dlo, j->dhi);
+    }
+    return NULL;
+}
+
+/*
+ * All experts of one expert tensor, expert-major: out[e][block] (18 B each).
+ * Expert e is drawn from its own stream keyed by (seed, 1, tensor_tag, e), so
+ * the result does not depend on n_threads and any expert can be regenerated
+ * alone with synth_q4_experts(seed, tag, e, e+1, ...).
+ */
+void synth_q4_experts(uint64_t seed, uint64_t tensor_tag, int e_begin, int e_end, size_t blocks_per_expert,
+                      uint8_t *out, double dlo, double dhi, int n_threads) {
+    int n = e_end - e_begin;
+    if (n <= 0) return;
+    if (n_threads < 1) n_threads = 1;
+    if (n_threads > 64) n_threads = 64;
+    if (n_threads > n) n_threads = n;
+    q4_job_t jobs[64];
+    pthread_t th[64];
+    for (int t = 0; t < n_threads; ++t) {
+        jobs[t].seed = seed;
+        jobs[t].tag = tensor_tag;
+        jobs[t].e0 = e_begin + (int)((long)n * t / n_threads);
+        jobs[t].e1 = e_begin + (int)((long)n * (t + 1) / n_threads);
+        jobs[t].blocks_per_expert = blocks_per_expert;
+        jobs[t].out = out - (size_t)e_begin * blocks_per_expert * 18;
+        jobs[t].dlo = dlo;
+        jobs[t].dhi = dhi;
+    }
+    for (int t = 1; t < n_threads; ++t) pthread_create(&th[t], NULL, q4_worker, &jobs[t]);
+    q4_worker(&jobs[0]);
+    for (int t = 1; t < n_threads; ++t) pthread_join(th[t], NULL);
+}
+
+/* Uniform random permutation of 0..n-1 (Fisher-Yates, Lemire-free modulo with
+ * rejection so every permutation is equally likely). */
+void synth_permutation(uint64_t key, int32_t *perm, int n) {
+    xo_t g;
+    xo_init(&g, key);
+    for (int i = 0; i < n; ++i) perm[i] = i;
+    for (int i = n - 1; i > 0; --i) {
+        uint64_t bound = (uint64_t)(i + 1);
+        uint64_t lim = UINT64_MAX - UINT64_MAX % bound;
+        uint64_t r;
+        do r = xo_next(&g);
+        while (r >= lim);
+        int j = (int)(r % bound);
+        int32_t t = perm[i];
+        perm[i] = perm[j];
+        perm[j] = t;
+    }
+}
+
+/*
+ * Router logits with a given popularity: out[t][e] = base[e] + G[t][e], with
+ * G ~ Gumbel(0,1) i.i.d.  When base[e] = ln p(e), the top-k of a row is a
+ * sample of k experts without replacement from p (the Gumbel-top-k trick,
+ * Kool, van Hoof, Welling 2019), so each token's first pick follows p exactly.
+ */
+void synth_gumbel_logits(uint64_t key, const double *base, int T, int E, float *out) {
+    xo_t g;
+    xo_init(&g, key);
+    for (int t = 0; t < T; ++t)
+        for (int e = 0; e < E; ++e) {
+            double u = xo_unit_open(&g);
+            if (u >= 1.0) u = 0x1.fffffffffffffp-1;
+            out[(size_t)t * E + e] = (float)(base[e] - log(-log(u)));
+        }
+}

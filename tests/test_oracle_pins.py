@@ -1,0 +1,271 @@
+"""Pins of the numeric oracle against things other than itself: the IEEE
+binary16 definition and numpy's independent float16, hand-worked block dots,
+brute force over all codes, numpy stable sorts, scipy closed forms and fp64
+dense matmuls of independently dequantized weights.
+
+Each pin is chosen so that a plausible mistake in the oracle (a dropped
+term, a wrong sign or offset, swapped nibbles, swapped gate/up, a wrong
+index) fails at least one of them.
+"""
+import math
+
+import numpy as np
+import pytest
+from scipy.special import expit, softmax
+
+import oracle
+import synth
+
+RNG = np.random.default_rng(1234)
+
+
+# ---------------------------------------------------------------- binary16
+def test_h2d_golden(golden):
+    for bits, val, _ in golden("f16_values.txt"):
+        got = oracle.h2d(int(bits, 16))
+        assert got == float(val) and math.copysign(1, got) == math.copysign(1, float(val)), bits
+
+
+def test_h2d_all_bit_patterns_vs_numpy():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = np.array([oracle.h2d(int(b)) for b in bits])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan]))
+
+
+def test_f2h_vs_numpy_random_and_ties():
+    # random magnitudes over the whole binary16 range, incl. subnormals/overflow
+    mags = np.exp2(RNG.uniform(-30, 17, 20000)).astype(np.float32)
+    vals = np.concatenate([mags, -mags]).astype(np.float32)
+    # exact midpoints between neighbouring binary16 values (ties to even)
+    h = np.arange(0, 0x7bff, 7, dtype=np.uint16)
+    lo = h.view(np.float16).astype(np.float64)
+    hi = (h + 1).view(np.float16).astype(np.float64)
+    mid = ((lo + hi) / 2).astype(np.float32)
+    assert np.array_equal(mid.astype(np.float64), (lo + hi) / 2)  # exact in binary32
+    vals = np.concatenate([vals, mid, -mid, np.float32([0.0, -0.0, 65504, 65519.99, 65520, 1e-8, 2.0 ** -25])])
+    ref = vals.astype(np.float16).view(np.uint16)
+    got = np.array([oracle.f2h(float(v)) for v in vals], np.uint16)
+    bad = np.nonzero(got != ref)[0]
+    assert bad.size == 0, [(float(vals[i]), hex(got[i]), hex(ref[i])) for i in bad[:5]]
+
+
+# ---------------------------------------------------------------- top-k
+def _stable_topk(logits, k):
+    # numpy's stable sort on -logit keeps index order among equal keys
+    order = np.argsort(-logits.astype(np.float64), axis=1, kind="stable")
+    return order[:, :k]
+
+
+@pytest.mark.parametrize("E,k", [(8, 2), (512, 8), (128, 4), (64, 1), (16, 16)])
+def test_topk_matches_stable_sort(E, k):
+    T = 37
+    logits = RNG.standard_normal((T, E)).astype(np.float32)
+    # force ties: quantize a third of the rows coarsely
+    logits[::3] = np.round(logits[::3] * 2) / 2
+    idx, w = oracle.topk(logits, k)
+    assert np.array_equal(idx, _stable_topk(logits, k))
+
+
+def test_topk_signed_zero_tie_goes_to_lower_index():
+    logits = np.array([[-1.0, 0.0, -0.0, -2.0], [-1.0, -0.0, 0.0, -2.0]], np.float32)
+    idx, _ = oracle.topk(logits, 2)
+    assert idx.tolist() == [[1, 2], [1, 2]]
+
+
+def test_topk_brute_force_subsets():
+    # the chosen set maximizes the sum of logits among all k-subsets (E=8)
+    import itertools
+    logits = RNG.standard_normal((20, 8)).astype(np.float32)
+    idx, _ = oracle.topk(logits, 3)
+    for t in range(20):
+        best = max(itertools.combinations(range(8), 3), key=lambda s: sum(float(logits[t, i]) for i in s))
+        assert sorted(best) == sorted(idx[t].tolist())
+
+
+def test_topk_weights_closed_forms():
+    logits = RNG.standard_normal((50, 64)).astype(np.float32)
+    idx, w = oracle.topk(logits, 6, renorm=True)
+    sel = np.take_along_axis(logits.astype(np.float64), idx, 1)
+    np.testing.assert_allclose(w, softmax(sel, axis=1), rtol=1e-14, atol=0)
+    idx2, w2 = oracle.topk(logits, 6, renorm=False)
+    full = softmax(logits.astype(np.float64), axis=1)
+    np.testing.assert_allclose(w2, np.take_along_axis(full, idx2, 1), rtol=1e-13)
+
+
+# ---------------------------------------------------------------- quantizer
+def _exact_nearest_codes(xb, dd):
+    """Brute force: the code c in [-127,127] minimizing |x - c*d| (exact,
+    ties to the even code), for every element of a block."""
+    cands = np.arange(-127, 128, dtype=np.float64)
+    err = np.abs(xb[:, None].astype(np.float64) - cands[None, :] * dd)
+    best = err.min(axis=1, keepdims=True)
+    ties = err == best
+    out = []
+    for row in ties:
+        cs = cands[row]
+        even = cs[np.mod(cs, 2) == 0]
+        out.append(even[0] if len(cs) > 1 and len(even) else cs[0])
+    return np.array(out)
+
+
+def test_quantizer_brute_force_and_scale():
+    x = (RNG.standard_normal((64, 32)) * np.exp2(RNG.uniform(-6, 6, (64, 1)))).astype(np.float32)
+    x[5] = 0.0
+    x[7, :] = np.float32(0.5)
+    q, d = oracle.quantize(x)
+    for b in range(x.shape[0]):
+        amax = np.float32(np.abs(x[b]).max())
+        d_ref = np.float16(np.float32(amax) / np.float32(127.0)).view(np.uint16)
+        assert d[b, 0] == d_ref
+        dd = float(np.uint16(d[b, 0]).view(np.float16))
+        if dd == 0:
+            assert not q[b].any()
+            continue
+        ref = _exact_nearest_codes(x[b], dd)
+        quot = x[b].astype(np.float64) / dd
+        near_tie = np.abs(np.abs(quot - np.floor(quot)) - 0.5) < 1e-6 * np.maximum(1, np.abs(quot))
+        mism = (q[b] != ref) & ~near_tie
+        assert not mism.any(), (b, q[b][mism], ref[mism])
+        assert np.abs(q[b]).max() <= 127
+        assert np.abs(q[b]).max() >= 126  # the largest element maps to the end of the range
+
+
+def test_quantizer_zero_and_tiny_blocks():
+    x = np.zeros((2, 32), np.float32)
+    x[1, 3] = 1e-30  # scale underflows binary16 -> zero block
+    q, d = oracle.quantize(x)
+    assert not q.any() and not d.any()
+
+
+# ---------------------------------------------------------------- Q4 blocks
+def _np_dequant(blocks):
+    """Independent dequantization of canonical Q4 blocks [..., 18]."""
+    d = blocks[..., 0:2].copy().view(np.float16)[..., 0].astype(np.float64)
+    qs = blocks[..., 2:18]
+    codes = np.concatenate([qs & 15, qs >> 4], axis=-1).astype(np.int64)  # elements 0..15, 16..31
+    return codes, d
+
+
+def test_block_dot_golden(golden):
+    for qs_hex, acts, expect in golden("q4_block_dot.txt"):
+        blk = np.zeros(18, np.uint8)
+        blk[2:] = np.frombuffer(bytes.fromhex(qs_hex), np.uint8)
+        a = np.array([int(v) for v in acts.split(",")], np.int8)
+        assert oracle.block_dot(blk, a) == int(expect)
+
+
+def test_block_dot_brute_force():
+    blocks = synth.q4_blocks(synth.key(7, 99), 500)
+    acts = RNG.integers(-127, 128, (500, 32)).astype(np.int8)
+    codes, _ = _np_dequant(blocks)
+    ref = ((codes - 8) * acts.astype(np.int64)).sum(axis=1)
+    got = np.array([oracle.block_dot(blocks[i], acts[i]) for i in range(500)])
+    assert np.array_equal(got, ref)
+    assert np.abs(ref).max() <= 32512
+
+
+def test_dequant_vs_independent():
+    blocks = synth.q4_blocks(synth.key(7, 100), 300).reshape(10, 30, 18)
+    codes, d = _np_dequant(blocks)
+    ref = (d[..., None] * (codes - 8)).reshape(10, 30 * 32)
+    assert np.array_equal(oracle.dequant(blocks), ref)
+
+
+def test_row_dot_vs_dense_fp64():
+    nb = 64
+    row = synth.q4_blocks(synth.key(7, 101), nb)
+    x = RNG.standard_normal(nb * 32).astype(np.float32)
+    qa, da = oracle.quantize(x)
+    r, abs_sum = oracle.row_dot(row, qa, da)
+    w = oracle.dequant(row)
+    codes, dw = _np_dequant(row)
+    w_ind = (dw[:, None] * (codes - 8)).reshape(-1)
+    a = qa.astype(np.float64) * np.repeat(da.view(np.float16).astype(np.float64), 32)
+    ref = float(np.dot(w_ind, a))
+    assert abs(r - ref) <= 4 * nb * 2.0 ** -52 * abs_sum
+    assert np.array_equal(w, w_ind)
+
+
+# ---------------------------------------------------------------- layer
+def _tiny_layer(seed=0):
+    wl = synth.WORKLOADS["tiny"]
+    H, F, E, k, T = wl.hidden, wl.ffn, wl.n_experts, wl.top_k, 4
+    gate = wl.expert_tensor(0, synth.KIND_GATE)
+    up = wl.expert_tensor(0, synth.KIND_UP)
+    down = wl.expert_tensor(0, synth.KIND_DOWN)
+    x = wl.x(0, 0, T)
+    logits = wl.logits(0, 0, T)
+    return wl, H, F, E, k, T, gate, up, down, x, logits
+
+
+def test_layer_vs_dense_fp64_brute_force():
+    wl, H, F, E, k, T, gate, up, down, x, logits = _tiny_layer()
+    idx, w = oracle.topk(logits, k)
+    y, it = oracle.layer(x, idx, w, gate, up, down, H, F, want_intermediates=True)
+
+    def deq(t):  # [E, rows, nb, 18] -> [E, rows, cols]
+        codes, d = _np_dequant(t)
+        return (d[..., None] * (codes - 8)).reshape(t.shape[0], t.shape[1], -1)
+
+    Wg, Wu, Wd = deq(gate), deq(up), deq(down)
+    # the oracle's quantized x is pinned by the quantizer tests
+    xa = it["xq"].astype(np.float64) * np.repeat(it["xd"].view(np.float16).astype(np.float64), 32, axis=1)
+    y_bf = np.zeros((T, H))
+    for t in range(T):
+        for j in range(k):
+            a = t * k + j
+            e = idx[t, j]
+            g = Wg[e] @ xa[t]
+            u = Wu[e] @ xa[t]
+            np.testing.assert_allclose(it["g"][a], g, rtol=0, atol=1e-12 * np.abs(g).max())
+            np.testing.assert_allclose(it["u"][a], u, rtol=0, atol=1e-12 * np.abs(u).max())
+            h = g * u * expit(g)  # silu(gate) * up
+            np.testing.assert_allclose(it["h"][a], h, rtol=1e-12, atol=1e-12)
+            # quantized h, recomputed through the (pinned) quantizer from binary32 h
+            hq, hd = oracle.quantize(h.astype(np.float32))
+            assert np.array_equal(hq, it["hq"][a]) and np.array_equal(hd, it["hd"][a])
+            ha = hq.astype(np.float64) * np.repeat(hd.view(np.float16).astype(np.float64), 32)
+            y_bf[t] += w[t, j] * (Wd[e] @ ha)
+    np.testing.assert_allclose(y, y_bf, rtol=1e-12, atol=1e-12 * np.abs(y_bf).max())
+    # quantization-error envelope against unquantized activations (reported, loose)
+    y_fp = np.zeros((T, H))
+    for t in range(T):
+        for j in range(k):
+            e = idx[t, j]
+            g = Wg[e] @ x[t].astype(np.float64)
+            u = Wu[e] @ x[t].astype(np.float64)
+            y_fp[t] += w[t, j] * (Wd[e] @ (g * u * expit(g)))
+    rel = np.linalg.norm(y - y_fp) / np.linalg.norm(y_fp)
+    assert rel < 0.05
+
+
+def test_down_combine_matches_layer():
+    wl, H, F, E, k, T, gate, up, down, x, logits = _tiny_layer()
+    idx, w = oracle.topk(logits, k)
+    y, it = oracle.layer(x, idx, w, gate, up, down, H, F, want_intermediates=True)
+    y2 = oracle.down_combine(idx, w, down, it["hq"], it["hd"], H, F)
+    assert np.array_equal(y, y2)
+
+
+def test_layer_experts_as_dict_equal_array():
+    wl, H, F, E, k, T, gate, up, down, x, logits = _tiny_layer()
+    idx, w = oracle.topk(logits, k)
+    y = oracle.layer(x, idx, w, gate, up, down, H, F)
+    used = sorted(set(idx.ravel().tolist()))
+    y2 = oracle.layer(x, idx, w, {e: gate[e] for e in used}, {e: up[e] for e in used},
+                      {e: down[e] for e in used}, H, F)
+    assert np.array_equal(y, y2)
+
+
+def test_generator_determinism():
+    wl = synth.WORKLOADS["decode_b1_pool25"]
+    a = wl.expert_tensor(3, synth.KIND_DOWN, 10, 14, threads=3)
+    b = wl.expert_tensor(3, synth.KIND_DOWN, 12, 13, threads=1)
+    assert np.array_equal(a[2], b[0])
+    codes, d = _np_dequant(a)
+    assert d.min() >= 0.005 - 1e-5 and d.max() <= 0.02 + 1e-5
+    assert codes.min() == 0 and codes.max() == 15
