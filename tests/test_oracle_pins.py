@@ -269,3 +269,18 @@ def test_generator_determinism():
     codes, d = _np_dequant(a)
     assert d.min() >= 0.005 - 1e-5 and d.max() <= 0.02 + 1e-5
     assert codes.min() == 0 and codes.max() == 15
+
+
+def test_quantizer_exact_ties_round_half_even():
+    # d = 2^-4 exactly: amax = 127/16 gives amax/127 = 1/16 (exact in binary16).
+    # Elements at (n + 1/2) * d are exact ties; round-half-even picks the even code.
+    d = 1.0 / 16
+    halves = [0.5, 1.5, 2.5, 3.5, -0.5, -1.5, -2.5, 125.5, -126.5]
+    expect = [0, 2, 2, 4, 0, -2, -2, 126, -126]
+    x = np.zeros(32, np.float32)
+    x[0] = 127 * d
+    x[1:1 + len(halves)] = np.float32(halves) * np.float32(d)
+    q, dd = oracle.quantize(x[None])
+    assert dd[0, 0] == np.float16(d).view(np.uint16)
+    assert q[0, 0] == 127
+    assert q[0, 1:1 + len(halves)].tolist() == expect
