@@ -1,0 +1,444 @@
+#!/usr/bin/env python3
+"""Benchmark of the routed-expert MoE FFN with a quantized HBM expert cache.
+
+Default workload (batch-1 decode through 48 MoE layers): hidden 2048, 512
+experts, top-8, expert FFN 1152 (SwiGLU), Q4 blocks of 32; router logits with
+Zipf(1.1) expert popularity under a per-layer permutation; the HBM pool holds
+all experts of 40 layers and a 60% hot set (seeded from the synthetic
+routing-frequency table) of the other 8; the rest is read zero-copy from
+pinned host memory.  One step = one decoded token: for each of the 48 layers,
+router top-k and the expert FFN (quantize, gate/up mat-vec + SwiGLU +
+quantize h, down mat-vec + combine), then the promotion pass (cache_step).
+
+    python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+
+Prints one JSON line (rank 0).  `value` is whole-job tokens/s with inputs
+resident in HBM; `e2e` is the same through the C ABI with the step's inputs
+copied from pinned host memory and its outputs copied back inside the timed
+region; `roofline` is for the gate/up mat-vec (the dominant kernel) over the
+fully resident layers; `cpu_baseline` is the CPU oracle on a bounded sample.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE expert-layer tokens/s (decode, prefill); achieved GB/s vs HBM/PCIe peak"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=128)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode_b1_resident")
+    ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--cpu-sample-steps", type=int, default=2)
+    return ap.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return PEAKS_FALLBACK, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def src_hash(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def read_traffic(kernel_file, key):
+    """Per-launch DRAM traffic of a kernel from its committed ncu summary,
+    valid only while the kernel source is unchanged since the capture."""
+    p = os.path.join(ROOT, "profiles", kernel_file)
+    if not os.path.exists(p):
+        return None
+    vals = {}
+    with open(p) as f:
+        for line in f:
+            if ":" in line and line.startswith("bench."):
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip()
+    try:
+        if vals.get("bench.source_hash") != src_hash(["quantized_expert_cache_gb300/csrc/kernels_decode.cu",
+                                                      "quantized_expert_cache_gb300/csrc/common.cuh"]):
+            return None
+        return float(vals[key])
+    except (KeyError, ValueError):
+        return None
+
+
+# ----------------------------------------------------------------------------
+# workload setup
+# ----------------------------------------------------------------------------
+
+def register_workload(qec, synth, ctx, wl, log):
+    t0 = time.time()
+    bufs = {}
+    for layer in range(wl.n_layers):
+        order = wl.seed_order(layer)
+        cap = wl.layer_capacity(layer)
+        for kind in range(3):
+            rows, cols = wl.tensor_shapes[kind]
+            key = (rows, cols)
+            if key not in bufs:
+                bufs[key] = np.empty((wl.n_experts, rows, cols // 32, 18), np.uint8)
+            wl.expert_tensor(layer, kind, out=bufs[key])
+            qec.register_expert_tensor(ctx, layer, kind, bufs[key], rows, cols, cap, order, cap)
+    log(f"registered {3 * wl.n_layers} expert tensors in {time.time() - t0:.1f}s")
+
+
+def make_inputs(wl, n_steps, T):
+    X = np.empty((n_steps, wl.n_layers, T, wl.hidden), np.float32)
+    LG = np.empty((n_steps, wl.n_layers, T, wl.n_experts), np.float32)
+    for s in range(n_steps):
+        for l in range(wl.n_layers):
+            X[s, l] = wl.x(l, s, T)
+            LG[s, l] = wl.logits(l, s, T)
+    return X, LG
+
+
+def run_ours(args):
+    import torch
+    import quantized_expert_cache_gb300 as qec
+    import synth
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def log(m):
+        if rank == 0:
+            print(f"[bench] {m}", file=sys.stderr, flush=True)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    qec.load()
+    wl = synth.WORKLOADS[args.workload]
+    label, T, _ = wl.phases[0]
+    if label != "decode":
+        raise SystemExit("bench.py times a decode workload")
+    L, H, E, k, F = wl.n_layers, wl.hidden, wl.n_experts, wl.top_k, wl.ffn
+    spt = max(wl.layer_capacity(l) for l in range(L))
+    stream = torch.cuda.Stream()
+    ctx = qec.moe_layer_init(H, F, E, k, L, spt, T, stream=stream)
+    register_workload(qec, synth, ctx, wl, log)
+
+    S = args.warmup + args.steps
+    t0 = time.time()
+    Xh, LGh = make_inputs(wl, S, T)
+    log(f"inputs for {S} steps in {time.time() - t0:.1f}s")
+    X = torch.from_numpy(Xh).cuda()
+    LG = torch.from_numpy(LGh).cuda()
+    xin = torch.empty((L, T, H), device="cuda")
+    lin = torch.empty((L, T, E), device="cuda")
+    idx = torch.empty((L, T, k), dtype=torch.int32, device="cuda")
+    w = torch.empty((L, T, k), device="cuda")
+    y = torch.empty((L, T, H), device="cuda")
+    sptr = stream.cuda_stream
+
+    def layers():
+        for l in range(L):
+            qec.route_topk(ctx, lin[l], T, E, k, idx[l], w[l], sptr)
+            qec.moe_ffn_forward(ctx, l, xin[l], T, idx[l], w[l], y[l], sptr)
+
+    graph = None
+    if not args.no_graph:
+        # warm the kernels once, then capture the L-layer step
+        with torch.cuda.stream(stream):
+            xin.copy_(X[0])
+            lin.copy_(LG[0])
+        layers()
+        stream.synchronize()
+        qec.miss_drain(ctx)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            layers()
+    launches_per_step = L * 4 + 1  # top-k, plan, gate/up, down per layer + the table update kernel
+
+    def step(s, host_io=None):
+        with torch.cuda.stream(stream):
+            if host_io is None:
+                xin.copy_(X[s])
+                lin.copy_(LG[s])
+            else:
+                xin.copy_(host_io[0][s], non_blocking=True)
+                lin.copy_(host_io[1][s], non_blocking=True)
+            if graph is not None:
+                graph.replay()
+            else:
+                layers()
+        qec.cache_step(ctx, T)
+        if host_io is not None:
+            with torch.cuda.stream(stream):
+                host_io[2].copy_(y, non_blocking=True)
+
+    for s in range(args.warmup):
+        step(s)
+    stream.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for s in range(args.warmup, S):
+        step(s)
+    ev1.record(stream)
+    stream.synchronize()
+    clk = clocks.stop()
+    ms = ev0.elapsed_time(ev1)
+    barrier()
+    torch.cuda.synchronize()
+    ms_max = ms
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    tok_per_s = world * args.steps * T / (ms_max / 1e3)
+    st_main = qec.moe_stats(ctx)
+
+    # end to end: the step's inputs from pinned host memory, outputs back
+    Xp = torch.from_numpy(Xh).pin_memory()
+    LGp = torch.from_numpy(LGh).pin_memory()
+    Yp = torch.empty((L, T, H)).pin_memory()
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for s in range(args.warmup, S):
+        step(s, host_io=(Xp, LGp, Yp))
+    stream.synchronize()
+    e2e_s = time.perf_counter() - t0
+    barrier()
+    e2e_tok = world * args.steps * T / e2e_s
+
+    # roofline of the gate/up mat-vec over the fully resident layers:
+    # per-layer CUDA events around the launches, recaptured into the graph
+    qec.moe_debug_timing(ctx, True)
+    if graph is not None:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            layers()
+    resident = [l for l in range(L) if wl.layer_capacity(l) == E]
+    blob = wl.tensor_bytes(0)
+    gu_ms, dn_ms, gu_bytes, dn_bytes, n_launch = 0.0, 0.0, 0, 0, 0
+    n_roof = min(args.steps, 32)
+    for s in range(args.warmup, args.warmup + n_roof):
+        step(s)
+        g_ms, d_ms = qec.moe_debug_timing_read(ctx, L)
+        uniq = [len(np.unique(LGh[s, l].argsort(axis=1)[:, -k:])) for l in resident]
+        for j, l in enumerate(resident):
+            gu_ms += g_ms[l]
+            dn_ms += d_ms[l]
+            gu_bytes += uniq[j] * 2 * blob + T * H + T * k * F
+            dn_bytes += uniq[j] * blob + T * k * F + T * H * 4
+            n_launch += 1
+    qec.moe_debug_timing(ctx, False)
+    peaks, peak_src = load_peaks()
+    achieved = gu_bytes / (gu_ms / 1e3) / 1e9
+    traffic = read_traffic("gate_up_gemv_decode_b1.txt", "bench.traffic_bytes_per_launch")
+
+    # bytes of the whole step (weights of the unique experts of every layer)
+    step_bytes = 0
+    for l in range(L):
+        u = len(np.unique(LGh[args.warmup, l].argsort(axis=1)[:, -k:]))
+        step_bytes += u * 3 * blob
+    st = qec.moe_stats(ctx)
+    out = {
+        "metric": METRIC, "value": round(tok_per_s, 2), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+        "config": {"workload": f"{wl.name}: {L} MoE layers, hidden {H}, {E} experts, top-{k}, FFN {F} SwiGLU, "
+                               f"Q4 blocks of 32, Zipf({wl.zipf_s}) routing, batch {T} decode, HBM pool "
+                               f"{[wl.layer_capacity(l) for l in range(L)].count(E)} full layers + "
+                               f"{min(wl.layer_capacity(l) for l in range(L))}/{E} hot set on the rest",
+                   "l2": "inputs larger than L2: ~1.5 GB of expert weights per step vs 129 MB L2",
+                   "cuda_graph": graph is not None, "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "kernel": "gate_up_gemv (resident layers)", "achieved": round(achieved, 1),
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                     "peak_source": f"{peak_src} hbm_gbs (copy)", "traffic": traffic,
+                     "algorithmic_bytes_per_launch": round(gu_bytes / max(1, n_launch)),
+                     "avg_launch_us": round(1e3 * gu_ms / max(1, n_launch), 3),
+                     "down_gemv_gbs": round(dn_bytes / (dn_ms / 1e3) / 1e9, 1)},
+        "step_weight_gbs": round(step_bytes / (ms_max / args.steps / 1e3) / 1e9, 1),
+        "cache": {"hits": st_main["hits"], "misses": st_main["misses"], "admissions": st_main["admissions"],
+                  "evictions": st_main["evictions"], "cold_bytes": st_main["cold_bytes"]},
+        "e2e": {"value": round(e2e_tok, 2), "unit": "tokens/s",
+                "h2d_bytes_per_step": int(Xh[0].nbytes + LGh[0].nbytes), "d2h_bytes_per_step": int(L * T * H * 4)},
+        "clocks": clk,
+        "gpu_launches": launches_per_step * args.steps,
+    }
+    qec.moe_destroy(ctx)
+    del X, LG
+    if rank == 0:
+        out["cpu_baseline"] = cpu_baseline(wl, args.cpu_sample_steps, T)
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle (baseline leg and the reference arm)
+# ----------------------------------------------------------------------------
+
+def oracle_layer_token(oracle, wl, layer, step, T, cache):
+    x, lg = wl.x(layer, step, T), wl.logits(layer, step, T)
+    idx, w = oracle.topk(lg, wl.top_k)
+    used = sorted(set(idx.ravel().tolist()))
+    tens = []
+    for kind in range(3):
+        d = {}
+        for e in used:
+            key = (layer, kind, e)
+            if key not in cache:
+                cache[key] = wl.expert_tensor(layer, kind, e, e + 1)[0]
+            d[e] = cache[key]
+        tens.append(d)
+    return x, idx, w, tens
+
+
+def cpu_baseline(wl, n_steps, T):
+    """The oracle as it stands, single-threaded, on a bounded sample: n_steps
+    decode steps through all layers (weights generated outside the timing)."""
+    import oracle
+    cache = {}
+    work = []
+    for s in range(n_steps):
+        for l in range(wl.n_layers):
+            work.append(oracle_layer_token(oracle, wl, l, s, T, cache))
+    t0 = time.perf_counter()
+    for x, idx, w, (g, u, d) in work:
+        oracle.layer(x, idx, w, g, u, d, wl.hidden, wl.ffn)
+    dt = time.perf_counter() - t0
+    return {"value": round(n_steps * T / dt, 4), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n_steps} decode steps x {wl.n_layers} layers (batch {T}), single-threaded C oracle, "
+                      f"{dt:.1f}s"}
+
+
+def run_reference(args):
+    rank, world, local = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    import synth
+    wl = synth.WORKLOADS[args.workload]
+    label, T, _ = wl.phases[0]
+    L = wl.n_layers
+    layers = list(range(0, L, 12))  # bounded sample: 4 of the 48 layers per step
+    cache = {}
+    per_step = []
+    for s in range(args.warmup + args.steps):
+        work = [oracle_layer_token(oracle, wl, l, s, T, cache) for l in layers]
+        t0 = time.perf_counter()
+        for x, idx, w, (g, u, d) in work:
+            oracle.layer(x, idx, w, g, u, d, wl.hidden, wl.ffn)
+        dt = time.perf_counter() - t0
+        if s >= args.warmup:
+            per_step.append(dt * L / len(layers))
+        if len(cache) > 3 * 8 * 64:
+            cache.clear()
+    step_s = float(np.mean(per_step))
+    value = T / step_s
+    out = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+        "config": {"workload": f"{wl.name} (CPU oracle)", "parallelism": "single host core"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": f"each step: layers {layers} of {L} for one token, scaled by {L}/{len(layers)}"},
+        "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    a = parse()
+    if a.impl == "reference":
+        run_reference(a)
+    else:
+        run_ours(a)

@@ -1,0 +1,269 @@
+/*
+ * moe_cache.h -- C ABI of the GB300 routed-expert MoE feed-forward with a
+ * quantized HBM expert cache.
+ *
+ * Every entry point returns an int status (MOE_OK = 0, negative = error;
+ * moe_last_error() gives a message) unless stated otherwise.  No C++
+ * exception crosses this boundary.  A context is not thread-safe: calls on
+ * one context must not overlap.  Device pointers are CUDA device addresses
+ * (or unified addresses) on the context's device; host pointers are plain
+ * process memory.  Streams are cudaStream_t passed as void*; NULL means the
+ * context's own stream.
+ *
+ * Data formats
+ *   Q4 block (canonical, 18 bytes): binary16 scale d (little endian), then
+ *   16 code bytes; byte j holds element j (low nibble) and element j+16
+ *   (high nibble); weight = d * (q - 8), q in 0..15.
+ *   Expert tensor (canonical): [n_experts][rows][cols/32] Q4 blocks,
+ *   expert-major.  gate and up have rows = ffn, cols = hidden; down has
+ *   rows = hidden, cols = ffn.  Tensor id = layer * 3 + kind.
+ *   Miss key: (tensor_id << 12) | expert (uint32).
+ *
+ * Sources (page titles and sections): Zapdev-labs/a6000-custom-kernels (the
+ * pointer-table GEMV diagram and the paragraphs after it: per-tensor d_tbl
+ * with an LSB tag, the HBM pool, zero-copy reads of pinned host memory, the
+ * miss recorder, stamps and the promotion pass between graphs);
+ * neurall/llama.cpp, "How it works" (admission on repeated use within the
+ * last 64 tokens; expert blocks borrowed by the prompt pass and returned);
+ * mx-llama.cpp FEATURES.md (q8_1 activation quantization reused across the
+ * matmuls of one input; planes of quants and scales); mihailescu2m/llama.cpp
+ * (MUL_MAT_ID over used tiles only; top-k of 512 scores).
+ */
+#ifndef MOE_CACHE_H
+#define MOE_CACHE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_OK 0
+#define MOE_ERR_ARG (-1)        /* an argument is out of range or inconsistent */
+#define MOE_ERR_OOM (-2)        /* a device or pinned host allocation failed */
+#define MOE_ERR_CUDA (-3)       /* a CUDA runtime call failed */
+#define MOE_ERR_NOT_PINNED (-4) /* host memory that must be pinned is not */
+#define MOE_ERR_TIMEOUT (-5)    /* a host-side poll limit was exceeded */
+#define MOE_ERR_CAPACITY (-6)   /* an output buffer is too small */
+#define MOE_ERR_STATE (-7)      /* call not valid in the current state */
+#define MOE_ERR_FAULT (-8)      /* an injected (test) upload fault */
+
+#define MOE_KIND_GATE 0
+#define MOE_KIND_UP 1
+#define MOE_KIND_DOWN 2
+
+typedef struct moe_ctx moe_ctx;
+
+/* Configuration of one context (one model's routed-expert FFN stack). */
+typedef struct moe_cfg {
+    int32_t hidden;             /* H: model width, multiple of 32 */
+    int32_t ffn;                /* F: expert FFN width, multiple of 32 */
+    int32_t n_experts;          /* E: experts per layer, 1..4096 (12-bit key) */
+    int32_t top_k;              /* k: experts per token, 1..32, <= E */
+    int32_t n_layers;           /* L: MoE layers; 3*L expert tensors */
+    int32_t slots_per_tensor;   /* HBM pool slots reserved per expert tensor */
+    int32_t max_tokens;         /* largest n_tokens of one forward */
+    int32_t window_tokens;      /* admission window (tokens), e.g. 64 */
+    int32_t max_swaps_per_step; /* admissions per cache_step, 0 = no limit */
+    int32_t renorm_topk;        /* 1: weights = softmax over the k selected */
+    int32_t poll_timeout_ms;    /* host poll limit in cache_step (0 = 10 s) */
+    int32_t device;             /* CUDA device ordinal */
+} moe_cfg;
+
+typedef struct moe_stats_t {
+    uint64_t steps;        /* cache_step calls */
+    uint64_t hits;         /* (tensor, expert) reads served by the pool */
+    uint64_t misses;       /* (tensor, expert) reads served from host memory */
+    uint64_t admissions;   /* experts uploaded into the pool */
+    uint64_t evictions;    /* experts removed from the pool */
+    uint64_t upload_bytes; /* bytes copied host -> pool by cache_step / return */
+    uint64_t cold_bytes;   /* weight bytes the kernels read zero-copy */
+    uint64_t clock;        /* token clock */
+} moe_stats_t;
+
+/*
+ * Create a context on cfg->device.  cuda_stream (cudaStream_t, may be NULL
+ * for a new non-blocking stream owned by the context) is the stream every
+ * forward of this context runs on.  The library allocates and owns: the HBM
+ * expert pool (3*L*slots_per_tensor slots of rows*cols/32*18 bytes), the
+ * pointer tables, stamps, miss log, workspaces, an upload stream and the
+ * pinned host copies of registered tensors.  *out receives the context.
+ * Errors: MOE_ERR_ARG (sizes), MOE_ERR_OOM, MOE_ERR_CUDA.
+ */
+int moe_layer_init(const moe_cfg *cfg, void *cuda_stream, moe_ctx **out);
+
+/*
+ * Register one expert tensor (layer, kind) and seed its pool.
+ * host_q4: canonical Q4 tensor [n_experts][rows][cols/32][18 B], any host
+ *   memory; the library copies it into its own pinned, device-mapped host
+ *   memory in plane layout (all codes, then all scales) and never reads
+ *   host_q4 again, so the caller may free it on return.
+ * capacity: pool slots of this tensor (<= slots_per_tensor).
+ * seed_order: n_experts distinct expert ids, most frequently routed first
+ *   (a routing-frequency table); the first n_seed (<= capacity) are
+ *   uploaded to slots 0..n_seed-1 (stamp 0).  NULL means 0,1,2,...
+ * Every other expert's table entry points at its pinned host copy with the
+ * low bit set.  *tensor_id (may be NULL) receives layer*3 + kind.
+ * Blocking (returns after the seed uploads finished).
+ * Errors: MOE_ERR_ARG (shape, cols % 32, ids out of range or repeated,
+ * already registered), MOE_ERR_OOM, MOE_ERR_CUDA.
+ */
+int register_expert_tensor(moe_ctx *ctx, int layer, int kind, const void *host_q4, int rows, int cols,
+                           int capacity, const int32_t *seed_order, int n_seed, int *tensor_id);
+
+/*
+ * Router top-k (mihailescu2m/llama.cpp, "the graph-shape problem": only the
+ * top entries of the 512 scores are needed).  d_logits: fp32 [n_tokens][E]
+ * device, row-major.  d_idx: int32 [n_tokens][k] device, the k largest
+ * logits per token ordered by (logit desc, expert asc): ties go to the
+ * lower index.  d_w: fp32 [n_tokens][k] device, the routing weights
+ * (softmax over the k selected logits if cfg.renorm_topk, else softmax over
+ * all E, read at the selected experts).  NaN logits give unspecified
+ * choices.  Asynchronous on `stream`; caller-owned buffers.
+ * Errors: MOE_ERR_ARG.
+ */
+int route_topk(moe_ctx *ctx, const float *d_logits, int n_tokens, int n_experts, int k, int32_t *d_idx,
+               float *d_w, void *stream);
+
+/*
+ * One routed-expert FFN layer (Zapdev-labs/a6000-custom-kernels: the
+ * pointer-table mat-vec, MUL_MAT_ID): for each token t and each j < k,
+ * expert e = d_idx[t][j] computes h = silu(gate_e . x_t) * (up_e . x_t)
+ * from int8-quantized x (blocks of 32, binary16 scale), quantizes h the
+ * same way, computes o = down_e . h, and y[t] = sum_j d_w[t][j] * o.
+ * Block dots are exact int32 sums of (q_w - 8) * q_a; each block is scaled
+ * by d_w * d_a in fp32.  Each expert's weights are read through the
+ * tensor's pointer table: pool slot (tag 0, HBM) or pinned host memory
+ * (tag 1, read zero-copy).  Cold reads are logged once per (tensor,
+ * expert) in the miss log; pool hits write the step's clock into the
+ * slot's stamp.  n_tokens <= 32 runs the mat-vec kernels; larger batches
+ * run the grouped per-expert GEMM over tokens sorted by expert.
+ * d_x: fp32 [n_tokens][H] device; d_idx/d_w as produced by route_topk;
+ * d_y: fp32 [n_tokens][H] device, written.  `stream` must be the
+ * context's stream (or NULL).  Asynchronous; capturable in a CUDA graph
+ * for a fixed n_tokens.  Errors: MOE_ERR_ARG, MOE_ERR_STATE (tensors of
+ * the layer not registered).
+ */
+int moe_ffn_forward(moe_ctx *ctx, int layer, const float *d_x, int n_tokens, const int32_t *d_idx,
+                    const float *d_w, float *d_y, void *stream);
+
+/*
+ * Promotion pass between steps (Zapdev-labs/a6000-custom-kernels:
+ * ggml_cuda_moe_cache_step between graphs, never captured; neurall/llama.cpp:
+ * admission after repeated use within the last 64 tokens).  Waits (host
+ * poll, bounded by cfg.poll_timeout_ms) for the forwards issued so far,
+ * advances the clock by n_tokens, reads the miss log and the stamps, and
+ * for each miss in ascending key order: admits the expert when its previous
+ * sighting is less than window_tokens old, into the lowest free slot or
+ * else the slot with the smallest stamp older than this step (ties: lowest
+ * slot), otherwise records the sighting.  Uploads run on the context's
+ * upload stream; the context stream waits for them before its next forward.
+ * While pool slots are borrowed, nothing is admitted.  The miss log is
+ * cleared.  Errors: MOE_ERR_TIMEOUT, MOE_ERR_CUDA, MOE_ERR_FAULT (injected).
+ */
+int cache_step(moe_ctx *ctx, int n_tokens);
+
+/*
+ * Copy the miss keys logged since the last cache_step (or drain) to
+ * host_out, sorted ascending, unique, and clear the log.  *n_out gets the
+ * count even when cap is too small (then MOE_ERR_CAPACITY and the log is
+ * kept).  Synchronizes with the context stream.
+ */
+int miss_drain(moe_ctx *ctx, uint32_t *host_out, size_t cap, size_t *n_out);
+
+/*
+ * Lend n_slots pool slots to a prefill pass (neurall/llama.cpp, "How it
+ * works": the big micro-batch buffer is lent only to the prompt pass).
+ * Global slot g is local slot g / (3L) of tensor g % (3L); the n highest
+ * global slots are taken, their experts evicted (table entries back to
+ * host).  *d_ws gets the device address of the contiguous lent region and
+ * *bytes its size.  Synchronous.  Errors: MOE_ERR_ARG, MOE_ERR_STATE
+ * (already borrowed).
+ */
+int moe_pool_borrow(moe_ctx *ctx, int n_slots, void **d_ws, size_t *bytes);
+
+/*
+ * Give the lent slots back: each returned slot, in ascending global order,
+ * is refilled with its tensor's most frequent non-resident expert by seed
+ * order (stamp = clock).  Synchronous.  Errors: MOE_ERR_STATE.
+ */
+int moe_pool_return(moe_ctx *ctx);
+
+/*
+ * Snapshot of one tensor's cache state (synchronizes with all streams).
+ * Any output may be NULL.  tbl: uint64 [E], the device pointer table as the
+ * kernels read it; slot_of: int32 [E] (-1 = cold); last_seen: int32 [E]
+ * (-1 = no sighting); owner: int32 [slots_per_tensor] (-1 = free or lent);
+ * stamps: uint32 [slots_per_tensor] (device stamp array).
+ */
+int moe_cache_snapshot(moe_ctx *ctx, int tensor_id, uint64_t *tbl, int32_t *slot_of, int32_t *last_seen,
+                       int32_t *owner, uint32_t *stamps);
+
+/* Base addresses used by table entries: the pool and the pinned host copy
+ * of one tensor (expert e of the tensor lives at host_base + e*tensor_slot). */
+int moe_cache_layout(moe_ctx *ctx, int tensor_id, uint64_t *pool_base, uint64_t *host_base,
+                     uint64_t *slot_bytes, int32_t *n_tensors);
+
+int moe_stats(moe_ctx *ctx, moe_stats_t *out);
+
+/* Message of the last error on ctx (or of the last failed moe_layer_init
+ * when ctx is NULL).  Valid until the next call on ctx. */
+const char *moe_last_error(moe_ctx *ctx);
+
+/* Release everything the context owns.  Synchronizes first. */
+void moe_destroy(moe_ctx *ctx);
+
+/* ---- inspection and measurement hooks (tests, benchmark) ---------------- */
+
+/*
+ * Integer block dots of the mat-vec kernels' block-dot routine: out[r][b] =
+ * sum_i (q_w,i - 8) * qa[b*32 + i] for rows row0..row0+n_rows-1 of expert
+ * `expert` of tensor_id, read through the pointer table (pool or host).
+ * d_qa: int8 [cols] device; d_out: int32 [n_rows][cols/32] device.
+ * Synchronous.  Errors: MOE_ERR_ARG.
+ */
+int moe_debug_block_dots(moe_ctx *ctx, int tensor_id, int expert, int row0, int n_rows, const int8_t *d_qa,
+                         int32_t *d_out);
+
+/*
+ * Copy a workspace of the most recent forward to host memory (synchronizes):
+ * what = 0: quantized x codes int8 [n_tokens][H]; 1: x scales binary16
+ * [n_tokens][H/32]; 2: quantized h codes int8 [n_tokens*k][F] (row
+ * a = t*k + j); 3: h scales binary16 [n_tokens*k][F/32].  bytes must
+ * equal the workspace size.  Errors: MOE_ERR_ARG, MOE_ERR_STATE.
+ */
+int moe_debug_read(moe_ctx *ctx, int what, void *host_out, size_t bytes);
+
+/*
+ * Zero-copy read bandwidth of pinned host memory: a kernel streams `bytes`
+ * from host_pinned (device-mapped) with 128-bit loads, `iters` times; *gbs
+ * receives the best GB/s.  Also measures cudaMemcpyAsync H2D into *copy_gbs
+ * when non-NULL.  Synchronous.  host_pinned must come from cudaHostAlloc
+ * (mapped) or be registered; else MOE_ERR_NOT_PINNED.
+ */
+int moe_probe_host_read(const void *host_pinned, size_t bytes, int iters, double *gbs, double *copy_gbs);
+
+/*
+ * Test hook: make the n-th following pool upload (1-based; 0 = off) report
+ * failure; the step rolls that admission back (the expert stays cold, the
+ * victim stays evicted) and returns MOE_ERR_FAULT after finishing the
+ * step consistently.
+ */
+int moe_debug_fail_upload(moe_ctx *ctx, int nth);
+
+/*
+ * Kernel timing (benchmark hook): when enabled, every forward records CUDA
+ * events on the context stream around its gate/up mat-vec and its down
+ * mat-vec launches (also inside a captured graph).  moe_debug_timing_read
+ * synchronizes and writes, per layer, the device time in ms of the most
+ * recent gate/up and down launch of that layer since the last read (0 when
+ * the layer ran no forward); both arrays hold n_layers doubles.
+ */
+int moe_debug_timing(moe_ctx *ctx, int enable);
+int moe_debug_timing_read(moe_ctx *ctx, double *gate_up_ms, double *down_ms);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_CACHE_H */

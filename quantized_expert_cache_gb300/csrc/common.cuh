@@ -1,0 +1,134 @@
+// Device-side building blocks shared by the kernels of the expert-cache
+// library: the Q4 x int8 block dot, the int8 block quantizer, warp
+// reductions, the expert-blob plane layout and the miss / stamp recorder.
+#pragma once
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+constexpr int kBlock = 32;         // weights / activations per quantization block
+constexpr int kBlockBytes = 18;    // canonical Q4 block: binary16 d + 16 code bytes
+constexpr int kWarps = 8;          // warps per CTA of the mat-vec kernels
+constexpr int kMaxChunk = 8;       // tokens per expert handled per weight pass
+
+// Expert blob in the pool and in pinned host memory ("plane" layout, after
+// the repacked quant/scale planes of mx-llama.cpp FEATURES.md):
+//   [codes: rows x nb x 16 B][scales: rows x nb x binary16]
+// Row r's codes are 16*nb contiguous bytes, so 8 lanes reading 16 B each
+// cover 128 contiguous bytes: coalesced 128-bit loads, which the canonical
+// 18-byte blocks (not 16-B aligned) do not allow.
+__host__ __device__ inline size_t blob_scales_offset(int rows, int nb) { return (size_t)rows * nb * 16; }
+__host__ __device__ inline size_t blob_bytes(int rows, int nb) { return (size_t)rows * nb * kBlockBytes; }
+
+// Per-activation-block data kept next to the int8 codes: the binary16 scale
+// (held as the exactly equal fp32 value) and the sum of the 32 codes, so that
+// sum_i (q_w,i - 8) q_a,i = sum_i q_w,i q_a,i - 8 * sum_i q_a,i.
+struct BlockScale {
+    float d;
+    int s;
+};
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ int warp_sum_i(int v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float warp_sum_f(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Quantize one block of 32 values held one per lane: d = binary16(amax/127)
+// in fp32, q = clamp(rint(v / d), -127, 127) with the stored binary16 scale
+// (round-half-even, IEEE division; this translation unit is compiled without
+// fast-math).  An all-zero block (d == 0) gives q = 0.  Lane 0 writes the
+// scale and the code sum.
+__device__ __forceinline__ void quantize_block_warp(float v, int lane, int8_t *q_out, BlockScale *ds_out) {
+    float amax = warp_max(fabsf(v));
+    float d32 = amax / 127.0f;
+    float dd = __half2float(__float2half_rn(d32));
+    int q = 0;
+    if (dd != 0.0f) {
+        float r = rintf(v / dd);
+        r = fminf(fmaxf(r, -127.0f), 127.0f);
+        q = (int)r;
+    }
+    int s = warp_sum_i(q);
+    q_out[lane] = (int8_t)q;
+    if (lane == 0) {
+        ds_out->d = dd;
+        ds_out->s = s;
+    }
+}
+
+// Raw integer dot of one Q4 block (16 code bytes as 4 words) with 32 int8
+// activations (8 words): sum_i q_w,i * q_a,i with q_w in 0..15.  Word i of the
+// codes holds elements 4i..4i+3 in its low nibbles and 4i+16..4i+19 in its
+// high nibbles.  The caller subtracts 8 * sum(q_a).
+__device__ __forceinline__ int q4_dot_raw(const uint4 &w, const int4 &a0, const int4 &a1) {
+    const uint32_t m = 0x0F0F0F0Fu;
+    int s = 0;
+    s = __dp4a((int)(w.x & m), a0.x, s);
+    s = __dp4a((int)(w.y & m), a0.y, s);
+    s = __dp4a((int)(w.z & m), a0.z, s);
+    s = __dp4a((int)(w.w & m), a0.w, s);
+    s = __dp4a((int)((w.x >> 4) & m), a1.x, s);
+    s = __dp4a((int)((w.y >> 4) & m), a1.y, s);
+    s = __dp4a((int)((w.z >> 4) & m), a1.z, s);
+    s = __dp4a((int)((w.w >> 4) & m), a1.w, s);
+    return s;
+}
+
+// Exact int32 block dot sum_i (q_w,i - 8) * q_a,i.
+__device__ __forceinline__ int q4_block_dot(const uint4 &w, const int4 &a0, const int4 &a1, int a_sum) {
+    return q4_dot_raw(w, a0, a1) - 8 * a_sum;
+}
+
+// Streaming 128-bit load of expert weights (read once per pass; works for
+// pool slots in HBM and for pinned host memory mapped into the device).
+__device__ __forceinline__ uint4 ld_weights(const uint4 *p) { return __ldcs(p); }
+
+__device__ __forceinline__ float ld_scale(const __half *p) { return __half2float(__ldcs(p)); }
+
+// Cache-state arrays of one forward: pointer tables, local slots, stamps and
+// the miss log (Zapdev-labs/a6000-custom-kernels, pointer-table GEMV).
+struct CacheView {
+    const uint64_t *tbl;       // [n_tensors][E]: pool address (bit0 = 0) or host address | 1
+    const int32_t *slot;       // [n_tensors][E]: local pool slot or -1
+    uint32_t *stamps;          // [n_tensors][slots_per_tensor]
+    uint32_t *miss_bitmap;     // [n_tensors][ceil(E/32)]
+    uint32_t *miss_list;       // [miss_cap]
+    uint32_t *miss_count;      // [1]
+    const uint32_t *clock;     // [1]: token clock after the last promotion pass
+    unsigned long long *cold_reads;  // [1]: (tensor, expert) zero-copy passes
+    int E, slots_per_tensor, bitmap_words, miss_cap;
+};
+
+// Record one (tensor, expert) read: a cold read sets its bit in the miss
+// bitmap and, when newly set, appends (tensor << 12 | expert) to the miss
+// list; a pool hit writes the step's clock into the slot's stamp.
+__device__ __forceinline__ void record_read(const CacheView &cv, int tid, int e, uint64_t entry, uint32_t step_clock) {
+    if (entry & 1ull) {
+        uint32_t bit = 1u << (e & 31);
+        uint32_t old = atomicOr(&cv.miss_bitmap[(size_t)tid * cv.bitmap_words + (e >> 5)], bit);
+        if (!(old & bit)) {
+            uint32_t pos = atomicAdd(cv.miss_count, 1u);
+            if (pos < (uint32_t)cv.miss_cap) cv.miss_list[pos] = ((uint32_t)tid << 12) | (uint32_t)e;
+        }
+    } else {
+        int s = cv.slot[(size_t)tid * cv.E + e];
+        if (s >= 0) cv.stamps[(size_t)tid * cv.slots_per_tensor + s] = step_clock;
+    }
+}
+
+}  // namespace moe

@@ -1,0 +1,58 @@
+// Internal interface between the C-ABI runtime (moe_cache.cu) and the
+// kernels.  Not part of the public ABI.
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace moe {
+
+struct PlanParams {
+    const float *x;       // [T][H] (quantized when quantize_x)
+    int8_t *xq;           // [T][H]
+    BlockScale *xds;      // [T][H/32]
+    const int32_t *idx;   // [T][k]
+    int32_t *n_uniq;      // [1]
+    int32_t *uniq_e;      // [min(T*k, E)]
+    int32_t *uniq_off;    // [min(T*k, E) + 1]
+    int32_t *assign;      // [T*k]: assignment ids grouped by expert
+    int *error;           // [1]: bit 0 = expert id out of range
+    int T, k, E, H, quantize_x;
+};
+
+struct GemvParams {
+    CacheView cv;
+    int tid_gate, tid_up, tid_down;
+    int n_tokens, k, H, F;
+    const int8_t *xq;
+    const BlockScale *xds;
+    const int32_t *n_uniq, *uniq_e, *uniq_off, *assign;
+    int8_t *hq;           // [T*k][F]
+    BlockScale *hds;      // [T*k][F/32]
+    float *o;             // [T*k][H]
+    unsigned *counters;   // [H / rows per down item], zero between launches
+    const float *w;       // [T][k]
+    float *y;             // [T][H]
+};
+
+// One table / slot / stamp write of the promotion pass.
+struct Update {
+    uint32_t what;   // 0: tbl[index] = value; 1: slot[index] = value; 2: stamps[index] = value
+    uint32_t index;
+    uint64_t value;
+};
+
+int launch_topk(const float *logits, int T, int E, int k, int renorm, int32_t *idx, float *w, cudaStream_t st);
+int launch_quantize(const float *x, int n_blocks, int8_t *q, BlockScale *ds, int n_sm, cudaStream_t st);
+int launch_plan(const PlanParams &p, cudaStream_t st);
+int launch_gemv(const GemvParams &p, int grid_gu, int grid_dn, cudaStream_t st, cudaEvent_t const *ev = nullptr);
+int down_rows_per_item(int F);
+int launch_block_dots(const uint8_t *blob, int rows, int nb, int row0, int n_rows, const int8_t *qa, int32_t *out,
+                      cudaStream_t st);
+int launch_stream_read(const void *src, size_t bytes, uint32_t *sink, int n_sm, cudaStream_t st);
+int launch_apply_updates(const Update *u, int n, uint64_t *tbl, int32_t *slot, uint32_t *stamps, uint32_t *clock,
+                         uint32_t new_clock, cudaStream_t st);
+
+}  // namespace moe

@@ -1,0 +1,525 @@
+// Decode-side kernels of the routed-expert FFN: router top-k, the per-layer
+// plan (activation quantization + grouping of assignments by expert), the
+// pointer-table gate/up mat-vec with fused SwiGLU and h quantization, the
+// down mat-vec with the fused weighted combine, and test/measurement hooks.
+//
+// Sources: Zapdev-labs/a6000-custom-kernels (moe_cache_gemv: one routed
+// expert sourced through d_tbl; cold reads logged to a miss buffer; stamps);
+// mx-llama.cpp FEATURES.md (q8_1 activations quantized once and reused by the
+// matmuls of one input; fused up/gate lanes for narrow batches);
+// mihailescu2m/llama.cpp (work only over (expert, tile) pairs that hold
+// tokens; top-k instead of a full sort of the 512 scores).
+#include "common.cuh"
+#include "kernels.h"
+
+#include <float.h>
+
+namespace moe {
+
+// --------------------------------------------------------------- top-k
+// One warp per token; lane l holds logits l, l+32, ... (V per lane).  k
+// rounds of a warp arg-max over (value desc, index asc).
+template <int V>
+__global__ void __launch_bounds__(256) topk_kernel(const float *__restrict__ logits, int T, int E, int k,
+                                                   int renorm, int32_t *__restrict__ idx, float *__restrict__ w) {
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (t >= T) return;
+    const float *l = logits + (size_t)t * E;
+    float v[V];
+    uint32_t taken[(V + 31) / 32];
+#pragma unroll
+    for (int i = 0; i < (V + 31) / 32; ++i) taken[i] = 0;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+        int e = lane + 32 * i;
+        v[i] = e < E ? l[e] : -INFINITY;
+        if (e >= E) taken[i >> 5] |= 1u << (i & 31);
+    }
+    float my_v = -INFINITY;
+    int my_i = 0x7fffffff;
+    for (int j = 0; j < k; ++j) {
+        float bv = -INFINITY;
+        int bi = 0x7fffffff;
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+            bool free_ = !(taken[i >> 5] & (1u << (i & 31)));
+            int e = lane + 32 * i;
+            if (free_ && (bi == 0x7fffffff || v[i] > bv)) {
+                bv = v[i];
+                bi = e;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (oi != 0x7fffffff && (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi))) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+        if (bi != 0x7fffffff && (bi & 31) == lane) {
+            int i = bi >> 5;
+#pragma unroll
+            for (int ii = 0; ii < V; ++ii)
+                if (ii == i) taken[ii >> 5] |= 1u << (ii & 31);
+        }
+        if (lane == j) {
+            my_v = bv;
+            my_i = bi;
+        }
+    }
+    float m = __shfl_sync(0xffffffffu, my_v, 0);
+    float ej = lane < k ? expf(my_v - m) : 0.0f;
+    float den;
+    if (renorm) {
+        den = warp_sum_f(ej);
+    } else {
+        float s = 0.0f;
+#pragma unroll
+        for (int i = 0; i < V; ++i)
+            if (lane + 32 * i < E) s += expf(v[i] - m);
+        den = warp_sum_f(s);
+    }
+    if (lane < k) {
+        idx[(size_t)t * k + lane] = my_i;
+        w[(size_t)t * k + lane] = ej / den;
+    }
+}
+
+int launch_topk(const float *logits, int T, int E, int k, int renorm, int32_t *idx, float *w, cudaStream_t st) {
+    if (T <= 0) return 0;
+    dim3 block(256), grid((T + 7) / 8);
+    if (E <= 32)
+        topk_kernel<1><<<grid, block, 0, st>>>(logits, T, E, k, renorm, idx, w);
+    else if (E <= 128)
+        topk_kernel<4><<<grid, block, 0, st>>>(logits, T, E, k, renorm, idx, w);
+    else if (E <= 512)
+        topk_kernel<16><<<grid, block, 0, st>>>(logits, T, E, k, renorm, idx, w);
+    else if (E <= 1024)
+        topk_kernel<32><<<grid, block, 0, st>>>(logits, T, E, k, renorm, idx, w);
+    else
+        topk_kernel<128><<<grid, block, 0, st>>>(logits, T, E, k, renorm, idx, w);
+    return (int)cudaGetLastError();
+}
+
+// --------------------------------------------------------------- quantize
+// Warp per block of 32 activations, grid-stride.
+__global__ void __launch_bounds__(256) quantize_kernel(const float *__restrict__ x, int n_blocks,
+                                                       int8_t *__restrict__ q, BlockScale *__restrict__ ds) {
+    const int lane = threadIdx.x & 31;
+    const int nw = (gridDim.x * blockDim.x) >> 5;
+    for (int b = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; b < n_blocks; b += nw)
+        quantize_block_warp(x[(size_t)b * kBlock + lane], lane, q + (size_t)b * kBlock, ds + b);
+}
+
+int launch_quantize(const float *x, int n_blocks, int8_t *q, BlockScale *ds, int n_sm, cudaStream_t st) {
+    if (n_blocks <= 0) return 0;
+    int grid = (n_blocks + 7) / 8;
+    if (grid > n_sm * 8) grid = n_sm * 8;
+    quantize_kernel<<<grid, 256, 0, st>>>(x, n_blocks, q, ds);
+    return (int)cudaGetLastError();
+}
+
+// --------------------------------------------------------------- plan
+// One CTA of 1024 threads: optionally quantize x (small batches), then group
+// the T*k assignments by expert: counts per expert, the ascending list of
+// used experts with the offsets of their assignment lists, and the
+// assignment ids grouped by expert (order within an expert is not fixed and
+// does not change any result: each assignment is computed on its own).
+__device__ __forceinline__ int block_excl_scan(int v, int *warp_tot) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+    }
+    if (lane == 31) warp_tot[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+        int s = lane < nw ? warp_tot[lane] : 0;
+        int si = s;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int n = __shfl_up_sync(0xffffffffu, si, o);
+            if (lane >= o) si += n;
+        }
+        if (lane < nw) warp_tot[lane] = si - s;  // exclusive warp offsets
+        if (lane == nw - 1) warp_tot[32] = si;   // block total
+    }
+    __syncthreads();
+    int r = warp_tot[wid] + incl - v;
+    __syncthreads();
+    return r;
+}
+
+__global__ void __launch_bounds__(1024) plan_kernel(PlanParams p) {
+    extern __shared__ int sm[];
+    int *cnt = sm;            // [E]
+    int *cur = sm + p.E;      // [E]
+    __shared__ int warp_tot[33];
+    const int A = p.T * p.k;
+    const int lane = threadIdx.x & 31;
+    if (p.quantize_x) {
+        const int nbx = p.H / kBlock, nblk = p.T * nbx;
+        for (int b = threadIdx.x >> 5; b < nblk; b += blockDim.x >> 5)
+            quantize_block_warp(p.x[(size_t)b * kBlock + lane], lane, p.xq + (size_t)b * kBlock, p.xds + b);
+    }
+    for (int e = threadIdx.x; e < p.E; e += blockDim.x) cnt[e] = 0;
+    __syncthreads();
+    for (int a = threadIdx.x; a < A; a += blockDim.x) {
+        int e = p.idx[a];
+        if (e < 0 || e >= p.E) {
+            atomicOr(p.error, 1);
+            e = 0;
+        }
+        atomicAdd(&cnt[e], 1);
+    }
+    __syncthreads();
+    // exclusive scans over experts of counts and of "used" flags, in
+    // chunks of blockDim experts.
+    int run_off = 0, run_u = 0;
+    for (int base = 0; base < p.E; base += blockDim.x) {
+        int e = base + threadIdx.x;
+        int c = e < p.E ? cnt[e] : 0;
+        int used = c > 0;
+        int off = block_excl_scan(c, warp_tot);
+        int tot_c = warp_tot[32];
+        __syncthreads();
+        int uix = block_excl_scan(used, warp_tot);
+        int tot_u = warp_tot[32];
+        __syncthreads();
+        if (e < p.E) {
+            cur[e] = run_off + off;
+            if (used) {
+                p.uniq_e[run_u + uix] = e;
+                p.uniq_off[run_u + uix] = run_off + off;
+            }
+        }
+        run_off += tot_c;
+        run_u += tot_u;
+    }
+    if (threadIdx.x == 0) {
+        p.uniq_off[run_u] = A;
+        *p.n_uniq = run_u;
+    }
+    __syncthreads();
+    for (int a = threadIdx.x; a < A; a += blockDim.x) {
+        int e = p.idx[a];
+        if (e < 0 || e >= p.E) e = 0;
+        int pos = atomicAdd(&cur[e], 1);
+        p.assign[pos] = a;
+    }
+}
+
+int launch_plan(const PlanParams &p, cudaStream_t st) {
+    size_t smem = (size_t)2 * p.E * sizeof(int);
+    plan_kernel<<<1, 1024, smem, st>>>(p);
+    return (int)cudaGetLastError();
+}
+
+// --------------------------------------------------------------- gate/up
+// Work item = (used expert u, block of 32 rows of F).  8 warps; each row is
+// split over 8 lanes (lane l of a row reads blocks l, l+8, ...: 8 lanes x 16 B
+// = 128 contiguous bytes per round), so one warp covers 4 rows and the CTA 32
+// rows.  gate row r and up row r are read by the same lanes, which gives
+// h_r = silu(g_r) * u_r in registers; the 32 values of h per token are then
+// quantized by one warp per token.
+constexpr int kGULanes = 8;
+
+__global__ void __launch_bounds__(256) gate_up_kernel(GemvParams p) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int sub = lane % kGULanes, grp = lane / kGULanes;
+    const int rloc = warp * (32 / kGULanes) + grp;  // 0..31
+    const int nbx = p.H / kBlock;
+    const int rgs = p.F / kBlock;
+    const int n_uniq = *p.n_uniq;
+    const int n_items = n_uniq * rgs;
+    const uint32_t step_clock = *p.cv.clock + (uint32_t)p.n_tokens;
+    const size_t scale_off = blob_scales_offset(p.F, nbx);
+    __shared__ float sh_h[kMaxChunk][32];
+
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+        const int u = item / rgs, rg = item - u * rgs;
+        const int e = p.uniq_e[u];
+        const int a0 = p.uniq_off[u], a1 = p.uniq_off[u + 1];
+        const uint64_t eg = p.cv.tbl[(size_t)p.tid_gate * p.cv.E + e];
+        const uint64_t eu = p.cv.tbl[(size_t)p.tid_up * p.cv.E + e];
+        if (rg == 0 && threadIdx.x == 0) {
+            record_read(p.cv, p.tid_gate, e, eg, step_clock);
+            record_read(p.cv, p.tid_up, e, eu, step_clock);
+        }
+        const uint8_t *bg = (const uint8_t *)(uintptr_t)(eg & ~1ull);
+        const uint8_t *bu = (const uint8_t *)(uintptr_t)(eu & ~1ull);
+        const int r = rg * 32 + rloc;
+        const uint4 *qg = (const uint4 *)bg + (size_t)r * nbx;
+        const uint4 *qu = (const uint4 *)bu + (size_t)r * nbx;
+        const __half *dg = (const __half *)(bg + scale_off) + (size_t)r * nbx;
+        const __half *du = (const __half *)(bu + scale_off) + (size_t)r * nbx;
+
+        for (int c0 = a0; c0 < a1; c0 += kMaxChunk) {
+            const int nt = min(kMaxChunk, a1 - c0);
+            int tok[kMaxChunk];
+#pragma unroll
+            for (int t = 0; t < kMaxChunk; ++t) tok[t] = t < nt ? p.assign[c0 + t] / p.k : 0;
+            float ag[kMaxChunk], au[kMaxChunk];
+#pragma unroll
+            for (int t = 0; t < kMaxChunk; ++t) ag[t] = au[t] = 0.0f;
+            for (int b0 = sub; b0 < nbx; b0 += 4 * kGULanes) {
+                uint4 wg4[4], wu4[4];
+                float sg[4], su[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    int b = b0 + i * kGULanes;
+                    if (b < nbx) {
+                        wg4[i] = ld_weights(qg + b);
+                        wu4[i] = ld_weights(qu + b);
+                        sg[i] = ld_scale(dg + b);
+                        su[i] = ld_scale(du + b);
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    int b = b0 + i * kGULanes;
+                    if (b < nbx) {
+#pragma unroll
+                        for (int t = 0; t < kMaxChunk; ++t) {
+                            if (t < nt) {
+                                const int4 *xa = (const int4 *)(p.xq + (size_t)tok[t] * p.H + (size_t)b * kBlock);
+                                int4 x0 = __ldg(xa), x1 = __ldg(xa + 1);
+                                BlockScale xs = p.xds[(size_t)tok[t] * nbx + b];
+                                int ig = q4_block_dot(wg4[i], x0, x1, xs.s);
+                                int iu = q4_block_dot(wu4[i], x0, x1, xs.s);
+                                ag[t] += (float)ig * (sg[i] * xs.d);
+                                au[t] += (float)iu * (su[i] * xs.d);
+                            }
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int t = 0; t < kMaxChunk; ++t) {
+#pragma unroll
+                for (int o = kGULanes / 2; o > 0; o >>= 1) {
+                    ag[t] += __shfl_xor_sync(0xffffffffu, ag[t], o);
+                    au[t] += __shfl_xor_sync(0xffffffffu, au[t], o);
+                }
+            }
+            if (sub == 0) {
+#pragma unroll
+                for (int t = 0; t < kMaxChunk; ++t)
+                    if (t < nt) {
+                        float g = ag[t], uu = au[t];
+                        sh_h[t][rloc] = g * uu / (1.0f + expf(-g));
+                    }
+            }
+            __syncthreads();
+            if (warp < nt) {
+                const int a = p.assign[c0 + warp];
+                quantize_block_warp(sh_h[warp][lane], lane, p.hq + (size_t)a * p.F + (size_t)rg * kBlock,
+                                    p.hds + (size_t)a * rgs + rg);
+            }
+            __syncthreads();
+        }
+    }
+}
+
+// --------------------------------------------------------------- down
+// Work item = (used expert u, block of ROWS rows of H); L lanes per row
+// (blocks of a row: F/32).  Each item writes o[a][rows] for the assignments
+// of u; the last item of a row block to finish (counted with an atomic per
+// row block) sums y[t][rows] = sum_j w[t][j] * o[t*k+j][rows] in j order.
+template <int L>
+__global__ void __launch_bounds__(256) down_kernel(GemvParams p) {
+    constexpr int G = 32 / L;          // rows per warp
+    constexpr int ROWS = kWarps * G;   // rows per item
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int sub = lane % L, grp = lane / L;
+    const int rloc = warp * G + grp;
+    const int nbf = p.F / kBlock;
+    const int n_rb = p.H / ROWS;
+    const int n_uniq = *p.n_uniq;
+    const int n_items = n_uniq * n_rb;
+    const uint32_t step_clock = *p.cv.clock + (uint32_t)p.n_tokens;
+    const size_t scale_off = blob_scales_offset(p.H, nbf);
+    __shared__ int sh_last;
+
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+        const int u = item / n_rb, rb = item - u * n_rb;
+        const int e = p.uniq_e[u];
+        const int a0 = p.uniq_off[u], a1 = p.uniq_off[u + 1];
+        const uint64_t ed = p.cv.tbl[(size_t)p.tid_down * p.cv.E + e];
+        if (rb == 0 && threadIdx.x == 0) record_read(p.cv, p.tid_down, e, ed, step_clock);
+        const uint8_t *bd = (const uint8_t *)(uintptr_t)(ed & ~1ull);
+        const int r = rb * ROWS + rloc;
+        const uint4 *qd = (const uint4 *)bd + (size_t)r * nbf;
+        const __half *dd = (const __half *)(bd + scale_off) + (size_t)r * nbf;
+
+        for (int c0 = a0; c0 < a1; c0 += kMaxChunk) {
+            const int nt = min(kMaxChunk, a1 - c0);
+            int asg[kMaxChunk];
+#pragma unroll
+            for (int t = 0; t < kMaxChunk; ++t) asg[t] = t < nt ? p.assign[c0 + t] : 0;
+            float acc[kMaxChunk];
+#pragma unroll
+            for (int t = 0; t < kMaxChunk; ++t) acc[t] = 0.0f;
+            for (int b0 = sub; b0 < nbf; b0 += 4 * L) {
+                uint4 w4[4];
+                float sw[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    int b = b0 + i * L;
+                    if (b < nbf) {
+                        w4[i] = ld_weights(qd + b);
+                        sw[i] = ld_scale(dd + b);
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    int b = b0 + i * L;
+                    if (b < nbf) {
+#pragma unroll
+                        for (int t = 0; t < kMaxChunk; ++t) {
+                            if (t < nt) {
+                                const int4 *ha = (const int4 *)(p.hq + (size_t)asg[t] * p.F + (size_t)b * kBlock);
+                                int4 h0 = __ldcg(ha), h1 = __ldcg(ha + 1);
+                                BlockScale hs = p.hds[(size_t)asg[t] * nbf + b];
+                                int id = q4_block_dot(w4[i], h0, h1, hs.s);
+                                acc[t] += (float)id * (sw[i] * hs.d);
+                            }
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int t = 0; t < kMaxChunk; ++t) {
+#pragma unroll
+                for (int o = L / 2; o > 0; o >>= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], o);
+            }
+            if (sub == 0) {
+#pragma unroll
+                for (int t = 0; t < kMaxChunk; ++t)
+                    if (t < nt) p.o[(size_t)asg[t] * p.H + r] = acc[t];
+            }
+        }
+        // arrival count of this row block; the last item combines
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            unsigned prev = atomicAdd(&p.counters[rb], 1u);
+            sh_last = (prev == (unsigned)(n_uniq - 1));
+        }
+        __syncthreads();
+        if (sh_last) {
+            __threadfence();
+            const int n_out = p.n_tokens * ROWS;
+            for (int i = threadIdx.x; i < n_out; i += blockDim.x) {
+                const int t = i / ROWS, rr = rb * ROWS + (i - t * ROWS);
+                float y = 0.0f;
+                for (int j = 0; j < p.k; ++j) {
+                    const size_t a = (size_t)t * p.k + j;
+                    y += p.w[a] * __ldcg(p.o + a * p.H + rr);
+                }
+                p.y[(size_t)t * p.H + rr] = y;
+            }
+            if (threadIdx.x == 0) p.counters[rb] = 0u;
+        }
+        __syncthreads();
+    }
+}
+
+int down_rows_per_item(int F) {
+    int nbf = F / kBlock;
+    int L = nbf <= 40 ? 4 : 8;
+    return kWarps * (32 / L);
+}
+
+// ev (optional): 4 events recorded around the gate/up and the down launch.
+int launch_gemv(const GemvParams &p, int grid_gu, int grid_dn, cudaStream_t st, cudaEvent_t const *ev) {
+    if (ev) cudaEventRecord(ev[0], st);
+    gate_up_kernel<<<grid_gu, 256, 0, st>>>(p);
+    if (ev) cudaEventRecord(ev[1], st);
+    int nbf = p.F / kBlock;
+    if (ev) cudaEventRecord(ev[2], st);
+    if (nbf <= 40)
+        down_kernel<4><<<grid_dn, 256, 0, st>>>(p);
+    else
+        down_kernel<8><<<grid_dn, 256, 0, st>>>(p);
+    if (ev) cudaEventRecord(ev[3], st);
+    return (int)cudaGetLastError();
+}
+
+// --------------------------------------------------------------- hooks
+// Block dots of rows row0.. of one expert through the pointer table, with
+// the same routine the mat-vec kernels use.  One warp per (row, 32 blocks).
+__global__ void block_dots_kernel(const uint8_t *blob, int rows, int nb, int row0, int n_rows,
+                                  const int8_t *__restrict__ qa, int32_t *__restrict__ out) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n_rows * nb) return;
+    const int r = row0 + i / nb, b = i % nb;
+    const uint4 w = ld_weights((const uint4 *)blob + (size_t)r * nb + b);
+    const int4 *xa = (const int4 *)(qa + (size_t)b * kBlock);
+    int4 x0 = xa[0], x1 = xa[1];
+    int s = 0;
+    const int8_t *q8 = qa + (size_t)b * kBlock;
+    for (int j = 0; j < kBlock; ++j) s += q8[j];
+    out[i] = q4_block_dot(w, x0, x1, s);
+}
+
+int launch_block_dots(const uint8_t *blob, int rows, int nb, int row0, int n_rows, const int8_t *qa, int32_t *out,
+                      cudaStream_t st) {
+    int n = n_rows * nb;
+    if (n <= 0) return 0;
+    block_dots_kernel<<<(n + 255) / 256, 256, 0, st>>>(blob, rows, nb, row0, n_rows, qa, out);
+    return (int)cudaGetLastError();
+}
+
+// Streams `n16` 16-byte words with 128-bit loads; the xor of everything read
+// goes to *sink so the loads cannot be dropped.
+__global__ void __launch_bounds__(256) stream_read_kernel(const uint4 *__restrict__ src, size_t n16, uint32_t *sink) {
+    uint32_t acc = 0;
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (; i + 3 * stride < n16; i += 4 * stride) {
+        uint4 a = ld_weights(src + i), b = ld_weights(src + i + stride), c = ld_weights(src + i + 2 * stride),
+              d = ld_weights(src + i + 3 * stride);
+        acc ^= a.x ^ a.y ^ a.z ^ a.w ^ b.x ^ b.y ^ b.z ^ b.w ^ c.x ^ c.y ^ c.z ^ c.w ^ d.x ^ d.y ^ d.z ^ d.w;
+    }
+    for (; i < n16; i += stride) {
+        uint4 a = ld_weights(src + i);
+        acc ^= a.x ^ a.y ^ a.z ^ a.w;
+    }
+    if (acc == 0x9e3779b9u) *sink = acc;
+}
+
+int launch_stream_read(const void *src, size_t bytes, uint32_t *sink, int n_sm, cudaStream_t st) {
+    stream_read_kernel<<<n_sm * 8, 256, 0, st>>>((const uint4 *)src, bytes / 16, sink);
+    return (int)cudaGetLastError();
+}
+
+// Table / stamp updates published by the promotion pass.
+__global__ void apply_updates_kernel(const Update *__restrict__ u, int n, uint64_t *tbl, int32_t *slot,
+                                     uint32_t *stamps, uint32_t *clock, uint32_t new_clock) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i == 0) *clock = new_clock;
+    if (i >= n) return;
+    const Update x = u[i];
+    if (x.what == 0)
+        tbl[x.index] = x.value;
+    else if (x.what == 1)
+        slot[x.index] = (int32_t)(int64_t)x.value;
+    else
+        stamps[x.index] = (uint32_t)x.value;
+}
+
+int launch_apply_updates(const Update *u, int n, uint64_t *tbl, int32_t *slot, uint32_t *stamps, uint32_t *clock,
+                         uint32_t new_clock, cudaStream_t st) {
+    int grid = (n + 255) / 256;
+    if (grid < 1) grid = 1;
+    apply_updates_kernel<<<grid, 256, 0, st>>>(u, n, tbl, slot, stamps, clock, new_clock);
+    return (int)cudaGetLastError();
+}
+
+}  // namespace moe

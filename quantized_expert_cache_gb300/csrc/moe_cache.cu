@@ -1,0 +1,857 @@
+// C-ABI runtime of the GB300 routed-expert FFN with a quantized HBM expert
+// cache: context lifetime, registration (plane repack into pinned, device-
+// mapped host memory and pool seeding), forward dispatch, the promotion pass
+// between steps, the miss log, pool borrowing around a prefill pass, and the
+// inspection hooks.  See moe_cache.h for the contract of each entry point.
+//
+// Sources: Zapdev-labs/a6000-custom-kernels (per-tensor d_tbl / pool / stamp
+// array, LSB-tagged host entries, miss buffer, promotion pass between
+// graphs, seeding from a routing-frequency file); neurall/llama.cpp, "How it
+// works" (admission after repeated use within the last 64 tokens; the prompt
+// pass borrows expert blocks and gives them back refilled with hot experts).
+#include "../../include/moe_cache.h"
+#include "kernels.h"
+
+#include <algorithm>
+#include <chrono>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <thread>
+#include <vector>
+
+using moe::BlockScale;
+using moe::Update;
+
+namespace {
+
+thread_local std::string g_init_error;
+
+struct TensorState {
+    bool registered = false;
+    int capacity = 0;
+    uint8_t *home = nullptr;  // pinned, device-mapped: n_experts blobs of slot_stride bytes
+    uint64_t home_dev = 0;
+    std::vector<int32_t> seed_order, slot_of, owner, last_seen;
+    std::vector<uint64_t> tbl;  // host mirror of the device table row
+    std::vector<uint8_t> lent;
+};
+
+}  // namespace
+
+struct moe_ctx {
+    moe_cfg cfg{};
+    int dev = 0, n_sm = 0;
+    int n_tensors = 0, E = 0, spt = 0, H = 0, F = 0, k = 0, M = 0;
+    size_t blob = 0, stride = 0;
+    cudaStream_t stream = nullptr, up = nullptr;
+    bool own_stream = false;
+    cudaEvent_t ev_fwd = nullptr, ev_up = nullptr;
+
+    uint8_t *arena = nullptr;
+    size_t arena_bytes = 0;
+    uint64_t *d_tbl = nullptr;
+    int32_t *d_slot = nullptr;
+    uint32_t *d_stamps = nullptr, *d_bitmap = nullptr, *d_misslog = nullptr, *d_clock = nullptr;
+    unsigned long long *d_cold = nullptr;
+    int miss_cap = 0, bitmap_words = 0;
+
+    int8_t *xq = nullptr, *hq = nullptr;
+    BlockScale *xds = nullptr, *hds = nullptr;
+    int32_t *plan_i = nullptr;  // n_uniq | uniq_e | uniq_off | assign
+    int *d_error = nullptr;
+    float *o = nullptr;
+    unsigned *counters = nullptr;
+    int n_counters = 0;
+
+    uint32_t *h_readback = nullptr;  // pinned: count + miss list
+    uint32_t *h_stamps = nullptr;    // pinned
+    Update *h_upd = nullptr, *d_upd = nullptr;
+    int upd_cap = 0, n_upd = 0;
+
+    std::vector<TensorState> t;
+    uint64_t clock = 0;
+    int n_lent = 0;
+    moe_stats_t stats{};
+    int last_T = -1;
+    int fail_nth = 0;
+    int grid_gu = 0, grid_dn = 0;
+    // kernel timing hook: 4 events per layer, recorded by each forward
+    bool timing = false;
+    std::vector<cudaEvent_t> tev;
+    std::vector<uint8_t> tev_used;
+    std::string err;
+};
+
+namespace {
+
+int fail(moe_ctx *c, int code, const std::string &msg) {
+    if (c)
+        c->err = msg;
+    else
+        g_init_error = msg;
+    return code;
+}
+
+#define CK(call)                                                                                   \
+    do {                                                                                           \
+        cudaError_t e_ = (call);                                                                   \
+        if (e_ != cudaSuccess)                                                                     \
+            return fail(ctx, e_ == cudaErrorMemoryAllocation ? MOE_ERR_OOM : MOE_ERR_CUDA,         \
+                        std::string(#call) + ": " + cudaGetErrorString(e_));                       \
+    } while (0)
+
+inline int32_t *p_n_uniq(moe_ctx *c) { return c->plan_i; }
+inline int32_t *p_uniq_e(moe_ctx *c) { return c->plan_i + 1; }
+inline int32_t *p_uniq_off(moe_ctx *c) { return c->plan_i + 1 + std::min(c->M * c->k, c->E); }
+inline int32_t *p_assign(moe_ctx *c) { return c->plan_i + 2 + 2 * std::min(c->M * c->k, c->E); }
+
+inline uint64_t pool_addr(moe_ctx *c, int tid, int local) {
+    size_t g = (size_t)local * c->n_tensors + tid;
+    return (uint64_t)(uintptr_t)(c->arena + g * c->stride);
+}
+inline uint64_t home_entry(moe_ctx *c, int tid, int e) {
+    return (c->t[tid].home_dev + (uint64_t)e * c->stride) | 1ull;
+}
+
+void push_upd(moe_ctx *c, uint32_t what, size_t index, uint64_t value) {
+    if (c->n_upd < c->upd_cap) c->h_upd[c->n_upd++] = Update{what, (uint32_t)index, value};
+}
+
+void set_entry(moe_ctx *c, int tid, int e, uint64_t entry, int32_t slot) {
+    TensorState &ts = c->t[tid];
+    ts.tbl[e] = entry;
+    ts.slot_of[e] = slot;
+    push_upd(c, 0, (size_t)tid * c->E + e, entry);
+    push_upd(c, 1, (size_t)tid * c->E + e, (uint64_t)(int64_t)slot);
+}
+
+// Publish the queued updates on `st` (table, slots, stamps, clock).
+int publish(moe_ctx *ctx, cudaStream_t st) {
+    if (ctx->n_upd > 0)
+        CK(cudaMemcpyAsync(ctx->d_upd, ctx->h_upd, sizeof(Update) * ctx->n_upd, cudaMemcpyHostToDevice, st));
+    int rc = moe::launch_apply_updates(ctx->d_upd, ctx->n_upd, ctx->d_tbl, ctx->d_slot, ctx->d_stamps, ctx->d_clock,
+                                       (uint32_t)ctx->clock, st);
+    if (rc) return fail(ctx, MOE_ERR_CUDA, std::string("apply_updates: ") + cudaGetErrorString((cudaError_t)rc));
+    ctx->n_upd = 0;
+    return MOE_OK;
+}
+
+int wait_event(moe_ctx *ctx, cudaEvent_t ev) {
+    int limit = ctx->cfg.poll_timeout_ms > 0 ? ctx->cfg.poll_timeout_ms : 10000;
+    auto t0 = std::chrono::steady_clock::now();
+    for (;;) {
+        cudaError_t q = cudaEventQuery(ev);
+        if (q == cudaSuccess) return MOE_OK;
+        if (q != cudaErrorNotReady) return fail(ctx, MOE_ERR_CUDA, std::string("event: ") + cudaGetErrorString(q));
+        double ms = std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t0).count();
+        if (ms > limit) return fail(ctx, MOE_ERR_TIMEOUT, "timed out waiting for the device");
+        std::this_thread::yield();
+    }
+}
+
+int sync_all(moe_ctx *ctx) {
+    CK(cudaStreamSynchronize(ctx->stream));
+    CK(cudaStreamSynchronize(ctx->up));
+    return MOE_OK;
+}
+
+// Repack canonical 18-byte blocks of n_experts experts into plane blobs.
+void repack(const uint8_t *src, uint8_t *dst, int n_experts, int rows, int nb, size_t stride) {
+    const size_t nblk = (size_t)rows * nb;
+    auto work = [&](int e0, int e1) {
+        for (int e = e0; e < e1; ++e) {
+            const uint8_t *s = src + (size_t)e * nblk * 18;
+            uint8_t *q = dst + (size_t)e * stride;
+            uint8_t *d = q + nblk * 16;
+            for (size_t b = 0; b < nblk; ++b) {
+                d[2 * b] = s[18 * b];
+                d[2 * b + 1] = s[18 * b + 1];
+                memcpy(q + 16 * b, s + 18 * b + 2, 16);
+            }
+        }
+    };
+    int nth = (int)std::min<unsigned>(16, std::max(1u, std::thread::hardware_concurrency()));
+    if ((size_t)n_experts * nblk < (1u << 16) || nth == 1) {
+        work(0, n_experts);
+        return;
+    }
+    nth = std::min(nth, n_experts);
+    std::vector<std::thread> th;
+    for (int i = 0; i < nth; ++i) th.emplace_back(work, n_experts * i / nth, n_experts * (i + 1) / nth);
+    for (auto &x : th) x.join();
+}
+
+uint16_t f32_to_half_bits(float v) {
+    __half h = __float2half_rn(v);
+    uint16_t b;
+    memcpy(&b, &h, 2);
+    return b;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_layer_init(const moe_cfg *cfg, void *cuda_stream, moe_ctx **out) {
+    moe_ctx *ctx = nullptr;
+    if (!cfg || !out) return fail(nullptr, MOE_ERR_ARG, "null argument");
+    *out = nullptr;
+    const moe_cfg &c = *cfg;
+    if (c.hidden <= 0 || c.hidden % 32 || c.ffn <= 0 || c.ffn % 32 || c.n_experts < 1 || c.n_experts > 4096 ||
+        c.top_k < 1 || c.top_k > 32 || c.top_k > c.n_experts || c.n_layers < 1 || c.n_layers * 3 > (1 << 20) ||
+        c.slots_per_tensor < 0 || c.slots_per_tensor > c.n_experts || c.max_tokens < 1 || c.window_tokens < 1 ||
+        c.max_swaps_per_step < 0)
+        return fail(nullptr, MOE_ERR_ARG,
+                    "bad cfg: hidden%32, ffn%32, 1<=E<=4096, 1<=k<=min(32,E), layers>=1, 0<=slots<=E, max_tokens>=1");
+    int down_rows = moe::down_rows_per_item(c.ffn);
+    if (c.hidden % down_rows) return fail(nullptr, MOE_ERR_ARG, "hidden must be a multiple of the down row block");
+    ctx = new moe_ctx();
+    ctx->cfg = c;
+    ctx->dev = c.device;
+    ctx->E = c.n_experts;
+    ctx->H = c.hidden;
+    ctx->F = c.ffn;
+    ctx->k = c.top_k;
+    ctx->M = c.max_tokens;
+    ctx->n_tensors = 3 * c.n_layers;
+    ctx->spt = c.slots_per_tensor;
+    ctx->blob = moe::blob_bytes(c.ffn, c.hidden / 32);
+    ctx->stride = (ctx->blob + 255) / 256 * 256;
+    auto cleanup_fail = [&](int rc) {
+        std::string m = ctx->err;
+        moe_destroy(ctx);
+        g_init_error = m;
+        return rc;
+    };
+#define CKI(call)                                                                                  \
+    do {                                                                                           \
+        cudaError_t e_ = (call);                                                                   \
+        if (e_ != cudaSuccess) {                                                                   \
+            ctx->err = std::string(#call) + ": " + cudaGetErrorString(e_);                         \
+            return cleanup_fail(e_ == cudaErrorMemoryAllocation ? MOE_ERR_OOM : MOE_ERR_CUDA);     \
+        }                                                                                          \
+    } while (0)
+    CKI(cudaSetDevice(ctx->dev));
+    CKI(cudaDeviceGetAttribute(&ctx->n_sm, cudaDevAttrMultiProcessorCount, ctx->dev));
+    if (cuda_stream) {
+        ctx->stream = (cudaStream_t)cuda_stream;
+    } else {
+        CKI(cudaStreamCreateWithFlags(&ctx->stream, cudaStreamNonBlocking));
+        ctx->own_stream = true;
+    }
+    CKI(cudaStreamCreateWithFlags(&ctx->up, cudaStreamNonBlocking));
+    CKI(cudaEventCreateWithFlags(&ctx->ev_fwd, cudaEventDisableTiming));
+    CKI(cudaEventCreateWithFlags(&ctx->ev_up, cudaEventDisableTiming));
+
+    const int nt = ctx->n_tensors, E = ctx->E;
+    ctx->arena_bytes = (size_t)nt * ctx->spt * ctx->stride;
+    if (ctx->arena_bytes) CKI(cudaMalloc(&ctx->arena, ctx->arena_bytes));
+    ctx->bitmap_words = (E + 31) / 32;
+    ctx->miss_cap = nt * E;
+    CKI(cudaMalloc(&ctx->d_tbl, sizeof(uint64_t) * nt * E));
+    CKI(cudaMalloc(&ctx->d_slot, sizeof(int32_t) * nt * E));
+    CKI(cudaMemset(ctx->d_slot, 0xff, sizeof(int32_t) * nt * E));
+    CKI(cudaMemset(ctx->d_tbl, 0, sizeof(uint64_t) * nt * E));
+    CKI(cudaMalloc(&ctx->d_stamps, sizeof(uint32_t) * (size_t)nt * std::max(1, ctx->spt)));
+    CKI(cudaMemset(ctx->d_stamps, 0, sizeof(uint32_t) * (size_t)nt * std::max(1, ctx->spt)));
+    CKI(cudaMalloc(&ctx->d_bitmap, sizeof(uint32_t) * (size_t)nt * ctx->bitmap_words));
+    CKI(cudaMemset(ctx->d_bitmap, 0, sizeof(uint32_t) * (size_t)nt * ctx->bitmap_words));
+    CKI(cudaMalloc(&ctx->d_misslog, sizeof(uint32_t) * (1 + (size_t)ctx->miss_cap)));
+    CKI(cudaMemset(ctx->d_misslog, 0, sizeof(uint32_t)));
+    CKI(cudaMalloc(&ctx->d_clock, sizeof(uint32_t)));
+    CKI(cudaMemset(ctx->d_clock, 0, sizeof(uint32_t)));
+    CKI(cudaMalloc(&ctx->d_cold, sizeof(unsigned long long)));
+    CKI(cudaMemset(ctx->d_cold, 0, sizeof(unsigned long long)));
+
+    const size_t M = ctx->M, A = M * ctx->k, U = std::min<size_t>(A, E);
+    CKI(cudaMalloc(&ctx->xq, M * ctx->H));
+    CKI(cudaMalloc(&ctx->xds, sizeof(BlockScale) * M * (ctx->H / 32)));
+    CKI(cudaMalloc(&ctx->plan_i, sizeof(int32_t) * (2 + 2 * U + A)));
+    CKI(cudaMalloc(&ctx->d_error, sizeof(int)));
+    CKI(cudaMemset(ctx->d_error, 0, sizeof(int)));
+    CKI(cudaMalloc(&ctx->hq, A * ctx->F));
+    CKI(cudaMalloc(&ctx->hds, sizeof(BlockScale) * A * (ctx->F / 32)));
+    CKI(cudaMalloc(&ctx->o, sizeof(float) * A * ctx->H));
+    ctx->n_counters = ctx->H / down_rows;
+    CKI(cudaMalloc(&ctx->counters, sizeof(unsigned) * ctx->n_counters));
+    CKI(cudaMemset(ctx->counters, 0, sizeof(unsigned) * ctx->n_counters));
+
+    CKI(cudaHostAlloc(&ctx->h_readback, sizeof(uint32_t) * (1 + (size_t)ctx->miss_cap), cudaHostAllocDefault));
+    CKI(cudaHostAlloc(&ctx->h_stamps, sizeof(uint32_t) * (size_t)nt * std::max(1, ctx->spt), cudaHostAllocDefault));
+    ctx->upd_cap = 6 * nt * E + 64;
+    CKI(cudaHostAlloc(&ctx->h_upd, sizeof(Update) * (size_t)ctx->upd_cap, cudaHostAllocDefault));
+    CKI(cudaMalloc(&ctx->d_upd, sizeof(Update) * (size_t)ctx->upd_cap));
+    CKI(cudaDeviceSynchronize());
+#undef CKI
+    ctx->t.resize(nt);
+    ctx->grid_gu = ctx->n_sm * 4;
+    ctx->grid_dn = ctx->n_sm * 4;
+    *out = ctx;
+    return MOE_OK;
+}
+
+int register_expert_tensor(moe_ctx *ctx, int layer, int kind, const void *host_q4, int rows, int cols, int capacity,
+                           const int32_t *seed_order, int n_seed, int *tensor_id) {
+    if (!ctx) return fail(nullptr, MOE_ERR_ARG, "null ctx");
+    if (layer < 0 || layer >= ctx->cfg.n_layers || kind < 0 || kind > 2 || !host_q4)
+        return fail(ctx, MOE_ERR_ARG, "bad layer/kind/pointer");
+    const int er = kind == MOE_KIND_DOWN ? ctx->H : ctx->F, ec = kind == MOE_KIND_DOWN ? ctx->F : ctx->H;
+    if (rows != er || cols != ec || cols % 32) return fail(ctx, MOE_ERR_ARG, "tensor shape does not match cfg");
+    if (capacity < 0 || capacity > ctx->spt || n_seed < 0 || n_seed > capacity)
+        return fail(ctx, MOE_ERR_ARG, "need 0 <= n_seed <= capacity <= slots_per_tensor");
+    const int tid = layer * 3 + kind, E = ctx->E;
+    TensorState &ts = ctx->t[tid];
+    if (ts.registered) return fail(ctx, MOE_ERR_ARG, "tensor already registered");
+    std::vector<int32_t> order(E);
+    if (seed_order) {
+        std::vector<uint8_t> seen(E, 0);
+        for (int i = 0; i < E; ++i) {
+            int e = seed_order[i];
+            if (e < 0 || e >= E || seen[e]) return fail(ctx, MOE_ERR_ARG, "seed_order must be a permutation of 0..E-1");
+            seen[e] = 1;
+            order[i] = e;
+        }
+    } else {
+        for (int i = 0; i < E; ++i) order[i] = i;
+    }
+    CK(cudaSetDevice(ctx->dev));
+    void *home = nullptr;
+    CK(cudaHostAlloc(&home, ctx->stride * E, cudaHostAllocMapped | cudaHostAllocPortable));
+    void *home_dev = nullptr;
+    cudaError_t ge = cudaHostGetDevicePointer(&home_dev, home, 0);
+    if (ge != cudaSuccess) {
+        cudaFreeHost(home);
+        return fail(ctx, MOE_ERR_CUDA, std::string("cudaHostGetDevicePointer: ") + cudaGetErrorString(ge));
+    }
+    ts.home = (uint8_t *)home;
+    ts.home_dev = (uint64_t)(uintptr_t)home_dev;
+    repack((const uint8_t *)host_q4, ts.home, E, rows, cols / 32, ctx->stride);
+    ts.capacity = capacity;
+    ts.seed_order = order;
+    ts.slot_of.assign(E, -1);
+    ts.owner.assign(ctx->spt, -1);
+    ts.last_seen.assign(E, -1);
+    ts.lent.assign(ctx->spt, 0);
+    ts.tbl.resize(E);
+    for (int e = 0; e < E; ++e) ts.tbl[e] = home_entry(ctx, tid, e);
+    for (int s = 0; s < n_seed; ++s) {
+        int e = order[s];
+        uint64_t dst = pool_addr(ctx, tid, s);
+        CK(cudaMemcpyAsync((void *)(uintptr_t)dst, ts.home + (size_t)e * ctx->stride, ctx->blob,
+                           cudaMemcpyHostToDevice, ctx->up));
+        ts.tbl[e] = dst;
+        ts.slot_of[e] = s;
+        ts.owner[s] = e;
+    }
+    CK(cudaMemcpyAsync(ctx->d_tbl + (size_t)tid * E, ts.tbl.data(), sizeof(uint64_t) * E, cudaMemcpyHostToDevice,
+                       ctx->up));
+    CK(cudaMemcpyAsync(ctx->d_slot + (size_t)tid * E, ts.slot_of.data(), sizeof(int32_t) * E, cudaMemcpyHostToDevice,
+                       ctx->up));
+    CK(cudaStreamSynchronize(ctx->up));
+    ts.registered = true;
+    ctx->stats.upload_bytes += (uint64_t)n_seed * ctx->blob;
+    if (tensor_id) *tensor_id = tid;
+    return MOE_OK;
+}
+
+int route_topk(moe_ctx *ctx, const float *d_logits, int n_tokens, int n_experts, int k, int32_t *d_idx, float *d_w,
+               void *stream) {
+    if (!ctx) return fail(nullptr, MOE_ERR_ARG, "null ctx");
+    if (n_tokens < 0 || n_experts != ctx->E || k != ctx->k || (n_tokens > 0 && (!d_logits || !d_idx || !d_w)))
+        return fail(ctx, MOE_ERR_ARG, "route_topk: bad sizes or pointers");
+    cudaStream_t st = stream ? (cudaStream_t)stream : ctx->stream;
+    int rc = moe::launch_topk(d_logits, n_tokens, n_experts, k, ctx->cfg.renorm_topk, d_idx, d_w, st);
+    if (rc) return fail(ctx, MOE_ERR_CUDA, std::string("topk launch: ") + cudaGetErrorString((cudaError_t)rc));
+    return MOE_OK;
+}
+
+int moe_ffn_forward(moe_ctx *ctx, int layer, const float *d_x, int n_tokens, const int32_t *d_idx, const float *d_w,
+                    float *d_y, void *stream) {
+    if (!ctx) return fail(nullptr, MOE_ERR_ARG, "null ctx");
+    if (layer < 0 || layer >= ctx->cfg.n_layers || n_tokens < 0 || n_tokens > ctx->M)
+        return fail(ctx, MOE_ERR_ARG, "forward: bad layer or n_tokens (> max_tokens?)");
+    if (stream && (cudaStream_t)stream != ctx->stream)
+        return fail(ctx, MOE_ERR_ARG, "forward: stream must be the context stream");
+    for (int kd = 0; kd < 3; ++kd)
+        if (!ctx->t[layer * 3 + kd].registered) return fail(ctx, MOE_ERR_STATE, "forward: layer not registered");
+    if (n_tokens == 0) return MOE_OK;
+    if (!d_x || !d_idx || !d_w || !d_y) return fail(ctx, MOE_ERR_ARG, "forward: null pointer");
+    cudaStream_t st = ctx->stream;
+    const int T = n_tokens, H = ctx->H;
+    const bool small = T <= 32;
+    int rc = 0;
+    if (!small) rc = moe::launch_quantize(d_x, T * (H / 32), ctx->xq, ctx->xds, ctx->n_sm, st);
+    if (rc) return fail(ctx, MOE_ERR_CUDA, "quantize launch failed");
+    moe::PlanParams pp{};
+    pp.x = d_x;
+    pp.xq = ctx->xq;
+    pp.xds = ctx->xds;
+    pp.idx = d_idx;
+    pp.n_uniq = p_n_uniq(ctx);
+    pp.uniq_e = p_uniq_e(ctx);
+    pp.uniq_off = p_uniq_off(ctx);
+    pp.assign = p_assign(ctx);
+    pp.error = ctx->d_error;
+    pp.T = T;
+    pp.k = ctx->k;
+    pp.E = ctx->E;
+    pp.H = H;
+    pp.quantize_x = small ? 1 : 0;
+    rc = moe::launch_plan(pp, st);
+    if (rc) return fail(ctx, MOE_ERR_CUDA, std::string("plan launch: ") + cudaGetErrorString((cudaError_t)rc));
+
+    moe::GemvParams gp{};
+    gp.cv.tbl = ctx->d_tbl;
+    gp.cv.slot = ctx->d_slot;
+    gp.cv.stamps = ctx->d_stamps;
+    gp.cv.miss_bitmap = ctx->d_bitmap;
+    gp.cv.miss_list = ctx->d_misslog + 1;
+    gp.cv.miss_count = ctx->d_misslog;
+    gp.cv.clock = ctx->d_clock;
+    gp.cv.cold_reads = ctx->d_cold;
+    gp.cv.E = ctx->E;
+    gp.cv.slots_per_tensor = std::max(1, ctx->spt);
+    gp.cv.bitmap_words = ctx->bitmap_words;
+    gp.cv.miss_cap = ctx->miss_cap;
+    gp.tid_gate = layer * 3 + 0;
+    gp.tid_up = layer * 3 + 1;
+    gp.tid_down = layer * 3 + 2;
+    gp.n_tokens = T;
+    gp.k = ctx->k;
+    gp.H = H;
+    gp.F = ctx->F;
+    gp.xq = ctx->xq;
+    gp.xds = ctx->xds;
+    gp.n_uniq = p_n_uniq(ctx);
+    gp.uniq_e = p_uniq_e(ctx);
+    gp.uniq_off = p_uniq_off(ctx);
+    gp.assign = p_assign(ctx);
+    gp.hq = ctx->hq;
+    gp.hds = ctx->hds;
+    gp.o = ctx->o;
+    gp.counters = ctx->counters;
+    gp.w = d_w;
+    gp.y = d_y;
+    const int A = T * ctx->k, U = std::min(A, ctx->E);
+    int max_gu = U * (ctx->F / 32), max_dn = U * ctx->n_counters;
+    const cudaEvent_t *ev = nullptr;
+    if (ctx->timing) {
+        ev = ctx->tev.data() + 4 * (size_t)layer;
+        ctx->tev_used[layer] = 1;
+    }
+    rc = moe::launch_gemv(gp, std::min(max_gu, ctx->grid_gu), std::min(max_dn, ctx->grid_dn), st, ev);
+    if (rc) return fail(ctx, MOE_ERR_CUDA, std::string("gemv launch: ") + cudaGetErrorString((cudaError_t)rc));
+    ctx->last_T = T;
+    return MOE_OK;
+}
+
+int cache_step(moe_ctx *ctx, int n_tokens) {
+    if (!ctx) return fail(nullptr, MOE_ERR_ARG, "null ctx");
+    if (n_tokens < 0) return fail(ctx, MOE_ERR_ARG, "cache_step: n_tokens < 0");
+    CK(cudaSetDevice(ctx->dev));
+    const int nt = ctx->n_tensors, spt = std::max(1, ctx->spt);
+    const size_t fast = std::min<size_t>(ctx->miss_cap, 4096);
+    // read back the miss log and the stamps after the forwards issued so far
+    CK(cudaMemcpyAsync(ctx->h_readback, ctx->d_misslog, sizeof(uint32_t) * (1 + fast), cudaMemcpyDeviceToHost,
+                       ctx->stream));
+    CK(cudaMemcpyAsync(ctx->h_stamps, ctx->d_stamps, sizeof(uint32_t) * (size_t)nt * spt, cudaMemcpyDeviceToHost,
+                       ctx->stream));
+    CK(cudaEventRecord(ctx->ev_fwd, ctx->stream));
+    int rc = wait_event(ctx, ctx->ev_fwd);
+    if (rc) return rc;
+    size_t n_miss = std::min<size_t>(ctx->h_readback[0], ctx->miss_cap);
+    if (n_miss > fast) {
+        CK(cudaMemcpy(ctx->h_readback + 1 + fast, ctx->d_misslog + 1 + fast, sizeof(uint32_t) * (n_miss - fast),
+                      cudaMemcpyDeviceToHost));
+    }
+    std::vector<uint32_t> keys(ctx->h_readback + 1, ctx->h_readback + 1 + n_miss);
+    std::sort(keys.begin(), keys.end());
+    keys.erase(std::unique(keys.begin(), keys.end()), keys.end());
+
+    ctx->clock += (uint64_t)n_tokens;
+    const uint64_t clk = ctx->clock;
+    const uint32_t clk32 = (uint32_t)clk;
+    for (int tid = 0; tid < nt; ++tid) {
+        const TensorState &ts = ctx->t[tid];
+        if (!ts.registered) continue;
+        for (int s = 0; s < ts.capacity; ++s)
+            if (ts.owner[s] >= 0 && ctx->h_stamps[(size_t)tid * spt + s] == clk32) ctx->stats.hits++;
+    }
+    ctx->stats.misses += keys.size();
+    ctx->stats.steps++;
+    for (uint32_t key : keys) {
+        int tid = (int)(key >> 12);
+        if (tid < nt && ctx->t[tid].registered) ctx->stats.cold_bytes += ctx->blob;
+    }
+
+    ctx->n_upd = 0;
+    int fault = 0, swaps = 0;
+    if (ctx->n_lent == 0) {
+        for (uint32_t key : keys) {
+            const int tid = (int)(key >> 12), e = (int)(key & 0xfff);
+            if (tid >= nt || e >= ctx->E || !ctx->t[tid].registered) continue;
+            TensorState &ts = ctx->t[tid];
+            const int64_t ls = ts.last_seen[e];
+            if (!(ls >= 0 && (int64_t)clk - ls < (int64_t)ctx->cfg.window_tokens)) {
+                ts.last_seen[e] = (int32_t)clk;
+                continue;
+            }
+            if (ctx->cfg.max_swaps_per_step && swaps >= ctx->cfg.max_swaps_per_step) continue;
+            int slot = -1;
+            for (int s = 0; s < ts.capacity; ++s)
+                if (!ts.lent[s] && ts.owner[s] < 0) {
+                    slot = s;
+                    break;
+                }
+            if (slot < 0) {
+                uint32_t best = 0;
+                for (int s = 0; s < ts.capacity; ++s) {
+                    if (ts.lent[s]) continue;
+                    uint32_t st = ctx->h_stamps[(size_t)tid * spt + s];
+                    if ((uint64_t)st < clk && (slot < 0 || st < best)) {
+                        slot = s;
+                        best = st;
+                    }
+                }
+            }
+            if (slot < 0) continue;
+            const int victim = ts.owner[slot];
+            if (victim >= 0) {
+                set_entry(ctx, tid, victim, home_entry(ctx, tid, victim), -1);
+                ts.last_seen[victim] = -1;
+                ts.owner[slot] = -1;
+                ctx->stats.evictions++;
+            }
+            swaps++;
+            if (ctx->fail_nth > 0 && --ctx->fail_nth == 0) {
+                // injected upload failure: the admission is rolled back, the
+                // slot stays free and the expert stays cold with its sighting
+                fault = 1;
+                continue;
+            }
+            const uint64_t dst = pool_addr(ctx, tid, slot);
+            CK(cudaMemcpyAsync((void *)(uintptr_t)dst, ts.home + (size_t)e * ctx->stride, ctx->blob,
+                               cudaMemcpyHostToDevice, ctx->up));
+            set_entry(ctx, tid, e, dst, slot);
+            ts.owner[slot] = e;
+            ts.last_seen[e] = -1;
+            ctx->h_stamps[(size_t)tid * spt + slot] = clk32;
+            push_upd(ctx, 2, (size_t)tid * spt + slot, clk32);
+            ctx->stats.admissions++;
+            ctx->stats.upload_bytes += ctx->blob;
+        }
+    }
+    rc = publish(ctx, ctx->up);
+    if (rc) return rc;
+    CK(cudaMemsetAsync(ctx->d_bitmap, 0, sizeof(uint32_t) * (size_t)nt * ctx->bitmap_words, ctx->up));
+    CK(cudaMemsetAsync(ctx->d_misslog, 0, sizeof(uint32_t), ctx->up));
+    CK(cudaEventRecord(ctx->ev_up, ctx->up));
+    CK(cudaStreamWaitEvent(ctx->stream, ctx->ev_up, 0));
+    ctx->stats.clock = clk;
+    if (fault) return fail(ctx, MOE_ERR_FAULT, "injected upload failure (admission rolled back)");
+    return MOE_OK;
+}
+
+int miss_drain(moe_ctx *ctx, uint32_t *host_out, size_t cap, size_t *n_out) {
+    if (!ctx) return fail(nullptr, MOE_ERR_ARG, "null ctx");
+    CK(cudaSetDevice(ctx->dev));
+    CK(cudaStreamSynchronize(ctx->stream));
+    uint32_t cnt = 0;
+    CK(cudaMemcpy(&cnt, ctx->d_misslog, sizeof(uint32_t), cudaMemcpyDeviceToHost));
+    size_t n = std::min<size_t>(cnt, ctx->miss_cap);
+    std::vector<uint32_t> keys(n);
+    if (n) CK(cudaMemcpy(keys.data(), ctx->d_misslog + 1, sizeof(uint32_t) * n, cudaMemcpyDeviceToHost));
+    std::sort(keys.begin(), keys.end());
+    keys.erase(std::unique(keys.begin(), keys.end()), keys.end());
+    if (n_out) *n_out = keys.size();
+    if (keys.size() > cap) return fail(ctx, MOE_ERR_CAPACITY, "miss_drain: output too small");
+    if (!keys.empty()) {
+        if (!host_out) return fail(ctx, MOE_ERR_ARG, "miss_drain: null output");
+        memcpy(host_out, keys.data(), sizeof(uint32_t) * keys.size());
+    }
+    CK(cudaMemsetAsync(ctx->d_bitmap, 0, sizeof(uint32_t) * (size_t)ctx->n_tensors * ctx->bitmap_words, ctx->stream));
+    CK(cudaMemsetAsync(ctx->d_misslog, 0, sizeof(uint32_t), ctx->stream));
+    CK(cudaStreamSynchronize(ctx->stream));
+    return MOE_OK;
+}
+
+int moe_pool_borrow(moe_ctx *ctx, int n_slots, void **d_ws, size_t *bytes) {
+    if (!ctx) return fail(nullptr, MOE_ERR_ARG, "null ctx");
+    const int nt = ctx->n_tensors, G = nt * ctx->spt;
+    if (ctx->n_lent) return fail(ctx, MOE_ERR_STATE, "borrow: slots already lent");
+    if (n_slots < 1 || n_slots > G) return fail(ctx, MOE_ERR_ARG, "borrow: n_slots out of range");
+    CK(cudaSetDevice(ctx->dev));
+    int rc = sync_all(ctx);
+    if (rc) return rc;
+    ctx->n_upd = 0;
+    for (int g = G - n_slots; g < G; ++g) {
+        const int tid = g % nt, local = g / nt;
+        TensorState &ts = ctx->t[tid];
+        if (!ts.registered || local >= ts.capacity) continue;
+        const int e = ts.owner[local];
+        if (e >= 0) {
+            set_entry(ctx, tid, e, home_entry(ctx, tid, e), -1);
+            ts.last_seen[e] = -1;
+            ts.owner[local] = -1;
+            ctx->stats.evictions++;
+        }
+        ts.lent[local] = 1;
+    }
+    rc = publish(ctx, ctx->stream);
+    if (rc) return rc;
+    CK(cudaStreamSynchronize(ctx->stream));
+    ctx->n_lent = n_slots;
+    if (d_ws) *d_ws = ctx->arena + (size_t)(G - n_slots) * ctx->stride;
+    if (bytes) *bytes = (size_t)n_slots * ctx->stride;
+    return MOE_OK;
+}
+
+int moe_pool_return(moe_ctx *ctx) {
+    if (!ctx) return fail(nullptr, MOE_ERR_ARG, "null ctx");
+    if (!ctx->n_lent) return fail(ctx, MOE_ERR_STATE, "return: nothing lent");
+    CK(cudaSetDevice(ctx->dev));
+    int rc = sync_all(ctx);
+    if (rc) return rc;
+    const int nt = ctx->n_tensors, G = nt * ctx->spt, spt = std::max(1, ctx->spt);
+    const uint32_t clk32 = (uint32_t)ctx->clock;
+    ctx->n_upd = 0;
+    for (int g = G - ctx->n_lent; g < G; ++g) {
+        const int tid = g % nt, local = g / nt;
+        TensorState &ts = ctx->t[tid];
+        if (!ts.registered || local >= ts.capacity) continue;
+        ts.lent[local] = 0;
+        for (int e : ts.seed_order) {
+            if (ts.slot_of[e] >= 0) continue;
+            const uint64_t dst = pool_addr(ctx, tid, local);
+            CK(cudaMemcpyAsync((void *)(uintptr_t)dst, ts.home + (size_t)e * ctx->stride, ctx->blob,
+                               cudaMemcpyHostToDevice, ctx->stream));
+            set_entry(ctx, tid, e, dst, local);
+            ts.owner[local] = e;
+            ts.last_seen[e] = -1;
+            push_upd(ctx, 2, (size_t)tid * spt + local, clk32);
+            ctx->stats.upload_bytes += ctx->blob;
+            break;
+        }
+    }
+    rc = publish(ctx, ctx->stream);
+    if (rc) return rc;
+    CK(cudaStreamSynchronize(ctx->stream));
+    ctx->n_lent = 0;
+    return MOE_OK;
+}
+
+int moe_cache_snapshot(moe_ctx *ctx, int tensor_id, uint64_t *tbl, int32_t *slot_of, int32_t *last_seen,
+                       int32_t *owner, uint32_t *stamps) {
+    if (!ctx) return fail(nullptr, MOE_ERR_ARG, "null ctx");
+    if (tensor_id < 0 || tensor_id >= ctx->n_tensors || !ctx->t[tensor_id].registered)
+        return fail(ctx, MOE_ERR_ARG, "snapshot: bad tensor id");
+    CK(cudaSetDevice(ctx->dev));
+    int rc = sync_all(ctx);
+    if (rc) return rc;
+    const TensorState &ts = ctx->t[tensor_id];
+    const int E = ctx->E;
+    if (tbl) CK(cudaMemcpy(tbl, ctx->d_tbl + (size_t)tensor_id * E, sizeof(uint64_t) * E, cudaMemcpyDeviceToHost));
+    if (slot_of) memcpy(slot_of, ts.slot_of.data(), sizeof(int32_t) * E);
+    if (last_seen) memcpy(last_seen, ts.last_seen.data(), sizeof(int32_t) * E);
+    if (owner)
+        for (int s = 0; s < ctx->spt; ++s) owner[s] = ts.lent[s] ? -1 : ts.owner[s];
+    if (stamps && ctx->spt)
+        CK(cudaMemcpy(stamps, ctx->d_stamps + (size_t)tensor_id * ctx->spt, sizeof(uint32_t) * ctx->spt,
+                      cudaMemcpyDeviceToHost));
+    return MOE_OK;
+}
+
+int moe_cache_layout(moe_ctx *ctx, int tensor_id, uint64_t *pool_base, uint64_t *host_base, uint64_t *slot_bytes,
+                     int32_t *n_tensors) {
+    if (!ctx) return fail(nullptr, MOE_ERR_ARG, "null ctx");
+    if (tensor_id < 0 || tensor_id >= ctx->n_tensors) return fail(ctx, MOE_ERR_ARG, "layout: bad tensor id");
+    if (pool_base) *pool_base = (uint64_t)(uintptr_t)ctx->arena;
+    if (host_base) *host_base = ctx->t[tensor_id].home_dev;
+    if (slot_bytes) *slot_bytes = ctx->stride;
+    if (n_tensors) *n_tensors = ctx->n_tensors;
+    return MOE_OK;
+}
+
+int moe_stats(moe_ctx *ctx, moe_stats_t *out) {
+    if (!ctx || !out) return fail(ctx, MOE_ERR_ARG, "null argument");
+    *out = ctx->stats;
+    out->clock = ctx->clock;
+    return MOE_OK;
+}
+
+const char *moe_last_error(moe_ctx *ctx) { return ctx ? ctx->err.c_str() : g_init_error.c_str(); }
+
+void moe_destroy(moe_ctx *ctx) {
+    if (!ctx) return;
+    cudaSetDevice(ctx->dev);
+    if (ctx->stream) cudaStreamSynchronize(ctx->stream);
+    if (ctx->up) cudaStreamSynchronize(ctx->up);
+    for (auto &ts : ctx->t)
+        if (ts.home) cudaFreeHost(ts.home);
+    cudaFree(ctx->arena);
+    cudaFree(ctx->d_tbl);
+    cudaFree(ctx->d_slot);
+    cudaFree(ctx->d_stamps);
+    cudaFree(ctx->d_bitmap);
+    cudaFree(ctx->d_misslog);
+    cudaFree(ctx->d_clock);
+    cudaFree(ctx->d_cold);
+    cudaFree(ctx->xq);
+    cudaFree(ctx->xds);
+    cudaFree(ctx->plan_i);
+    cudaFree(ctx->d_error);
+    cudaFree(ctx->hq);
+    cudaFree(ctx->hds);
+    cudaFree(ctx->o);
+    cudaFree(ctx->counters);
+    cudaFree(ctx->d_upd);
+    if (ctx->h_readback) cudaFreeHost(ctx->h_readback);
+    if (ctx->h_stamps) cudaFreeHost(ctx->h_stamps);
+    if (ctx->h_upd) cudaFreeHost(ctx->h_upd);
+    for (cudaEvent_t e : ctx->tev) cudaEventDestroy(e);
+    if (ctx->ev_fwd) cudaEventDestroy(ctx->ev_fwd);
+    if (ctx->ev_up) cudaEventDestroy(ctx->ev_up);
+    if (ctx->up) cudaStreamDestroy(ctx->up);
+    if (ctx->own_stream && ctx->stream) cudaStreamDestroy(ctx->stream);
+    delete ctx;
+}
+
+int moe_debug_block_dots(moe_ctx *ctx, int tensor_id, int expert, int row0, int n_rows, const int8_t *d_qa,
+                         int32_t *d_out) {
+    if (!ctx) return fail(nullptr, MOE_ERR_ARG, "null ctx");
+    if (tensor_id < 0 || tensor_id >= ctx->n_tensors || !ctx->t[tensor_id].registered || expert < 0 ||
+        expert >= ctx->E || !d_qa || !d_out)
+        return fail(ctx, MOE_ERR_ARG, "block_dots: bad arguments");
+    const int kind = tensor_id % 3;
+    const int rows = kind == 2 ? ctx->H : ctx->F, cols = kind == 2 ? ctx->F : ctx->H;
+    if (row0 < 0 || n_rows < 0 || row0 + n_rows > rows) return fail(ctx, MOE_ERR_ARG, "block_dots: bad rows");
+    CK(cudaSetDevice(ctx->dev));
+    int rc = sync_all(ctx);
+    if (rc) return rc;
+    const uint8_t *blob = (const uint8_t *)(uintptr_t)(ctx->t[tensor_id].tbl[expert] & ~1ull);
+    rc = moe::launch_block_dots(blob, rows, cols / 32, row0, n_rows, d_qa, d_out, ctx->stream);
+    if (rc) return fail(ctx, MOE_ERR_CUDA, "block_dots launch failed");
+    CK(cudaStreamSynchronize(ctx->stream));
+    return MOE_OK;
+}
+
+int moe_debug_read(moe_ctx *ctx, int what, void *host_out, size_t bytes) {
+    if (!ctx) return fail(nullptr, MOE_ERR_ARG, "null ctx");
+    if (ctx->last_T < 0) return fail(ctx, MOE_ERR_STATE, "debug_read: no forward yet");
+    CK(cudaSetDevice(ctx->dev));
+    CK(cudaStreamSynchronize(ctx->stream));
+    const size_t T = ctx->last_T, A = T * ctx->k;
+    size_t need = 0;
+    switch (what) {
+        case 0: need = T * ctx->H; break;
+        case 1: need = T * (ctx->H / 32) * 2; break;
+        case 2: need = A * ctx->F; break;
+        case 3: need = A * (ctx->F / 32) * 2; break;
+        default: return fail(ctx, MOE_ERR_ARG, "debug_read: bad what");
+    }
+    if (bytes != need || !host_out) return fail(ctx, MOE_ERR_ARG, "debug_read: wrong size");
+    if (what == 0 || what == 2) {
+        CK(cudaMemcpy(host_out, what == 0 ? (void *)ctx->xq : (void *)ctx->hq, need, cudaMemcpyDeviceToHost));
+        return MOE_OK;
+    }
+    const size_t n = need / 2;
+    std::vector<BlockScale> tmp(n);
+    CK(cudaMemcpy(tmp.data(), what == 1 ? ctx->xds : ctx->hds, sizeof(BlockScale) * n, cudaMemcpyDeviceToHost));
+    uint16_t *o = (uint16_t *)host_out;
+    for (size_t i = 0; i < n; ++i) o[i] = f32_to_half_bits(tmp[i].d);  // exact: d is a binary16 value
+    return MOE_OK;
+}
+
+int moe_probe_host_read(const void *host_pinned, size_t bytes, int iters, double *gbs, double *copy_gbs) {
+    moe_ctx *ctx = nullptr;
+    if (!host_pinned || bytes < 16 || iters < 1 || !gbs) return fail(nullptr, MOE_ERR_ARG, "probe: bad arguments");
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, host_pinned) != cudaSuccess || at.type != cudaMemoryTypeHost) {
+        cudaGetLastError();
+        return fail(nullptr, MOE_ERR_NOT_PINNED, "probe: memory is not pinned host memory");
+    }
+    void *dptr = nullptr;
+    CK(cudaHostGetDevicePointer(&dptr, (void *)host_pinned, 0));
+    int dev = 0, n_sm = 0;
+    CK(cudaGetDevice(&dev));
+    CK(cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev));
+    uint32_t *sink = nullptr;
+    CK(cudaMalloc(&sink, 4));
+    cudaStream_t st;
+    CK(cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking));
+    cudaEvent_t a, b;
+    CK(cudaEventCreate(&a));
+    CK(cudaEventCreate(&b));
+    bytes &= ~(size_t)15;
+    double best = 0;
+    for (int i = 0; i < iters + 1; ++i) {
+        CK(cudaEventRecord(a, st));
+        moe::launch_stream_read(dptr, bytes, sink, n_sm, st);
+        CK(cudaEventRecord(b, st));
+        CK(cudaEventSynchronize(b));
+        float ms = 0;
+        CK(cudaEventElapsedTime(&ms, a, b));
+        if (i > 0) best = std::max(best, bytes / (ms * 1e-3) / 1e9);
+    }
+    *gbs = best;
+    if (copy_gbs) {
+        size_t cb = std::min<size_t>(bytes, (size_t)1 << 30);
+        void *dbuf = nullptr;
+        CK(cudaMalloc(&dbuf, cb));
+        double bc = 0;
+        for (int i = 0; i < iters + 1; ++i) {
+            CK(cudaEventRecord(a, st));
+            CK(cudaMemcpyAsync(dbuf, host_pinned, cb, cudaMemcpyHostToDevice, st));
+            CK(cudaEventRecord(b, st));
+            CK(cudaEventSynchronize(b));
+            float ms = 0;
+            CK(cudaEventElapsedTime(&ms, a, b));
+            if (i > 0) bc = std::max(bc, cb / (ms * 1e-3) / 1e9);
+        }
+        cudaFree(dbuf);
+        *copy_gbs = bc;
+    }
+    cudaEventDestroy(a);
+    cudaEventDestroy(b);
+    cudaStreamDestroy(st);
+    cudaFree(sink);
+    return MOE_OK;
+}
+
+int moe_debug_timing(moe_ctx *ctx, int enable) {
+    if (!ctx) return fail(nullptr, MOE_ERR_ARG, "null ctx");
+    CK(cudaSetDevice(ctx->dev));
+    if (enable && ctx->tev.empty()) {
+        ctx->tev.resize(4 * (size_t)ctx->cfg.n_layers);
+        for (auto &e : ctx->tev) CK(cudaEventCreate(&e));
+        ctx->tev_used.assign(ctx->cfg.n_layers, 0);
+    }
+    ctx->timing = enable != 0;
+    return MOE_OK;
+}
+
+int moe_debug_timing_read(moe_ctx *ctx, double *gate_up_ms, double *down_ms) {
+    if (!ctx) return fail(nullptr, MOE_ERR_ARG, "null ctx");
+    CK(cudaSetDevice(ctx->dev));
+    CK(cudaStreamSynchronize(ctx->stream));
+    for (int l = 0; l < ctx->cfg.n_layers; ++l) {
+        float a = 0, b = 0;
+        if (l < (int)ctx->tev_used.size() && ctx->tev_used[l]) {
+            CK(cudaEventElapsedTime(&a, ctx->tev[4 * l], ctx->tev[4 * l + 1]));
+            CK(cudaEventElapsedTime(&b, ctx->tev[4 * l + 2], ctx->tev[4 * l + 3]));
+            ctx->tev_used[l] = 0;
+        }
+        if (gate_up_ms) gate_up_ms[l] = a;
+        if (down_ms) down_ms[l] = b;
+    }
+    return MOE_OK;
+}
+
+int moe_debug_fail_upload(moe_ctx *ctx, int nth) {
+    if (!ctx || nth < 0) return fail(ctx, MOE_ERR_ARG, "bad argument");
+    ctx->fail_nth = nth;
+    return MOE_OK;
+}
+
+}  // extern "C"

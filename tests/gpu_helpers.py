@@ -1,0 +1,177 @@
+"""Helpers for the GPU parity tests: build a context from a small workload
+spec, run the oracle on the same seeded inputs, and compare.
+
+Tolerances (from the parity contract of the path):
+- bit-exact: top-k indices, quantized x (codes and binary16 scales), int32
+  block dots, miss-log contents (sorted unique), table / stamp / sighting
+  state after every promotion pass;
+- fp32 layer outputs: |y_gpu - y_ref| <= 1e-4 + 2e-3 * |y_ref| elementwise.
+
+Quantized h: h is computed in fp32 in a different summation order (and with
+CUDA's expf) than the oracle's binary64 value, so a code whose value sits
+within rounding error of a half-step may legitimately round either way.
+Such a code is accepted only if it is the rounding of some h' within the
+derived error bound of the oracle's h (below); y is then compared against
+the oracle's down projection and combine applied to the GPU's quantized h
+(when every code matches, that is exactly the oracle's own y).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+import quantized_expert_cache_gb300 as qec
+import synth
+
+U32 = 2.0 ** -24  # unit roundoff of binary32
+RTOL, ATOL = 2e-3, 1e-4
+
+
+def f16(bits):
+    return np.asarray(bits, np.uint16).view(np.float16).astype(np.float64)
+
+
+def h_error_bound(g, u, gabs, uabs, nb):
+    """Bound on |h_gpu - h| for h = silu(g) u, given binary64 g, u and the
+    sums of |terms| of their block sums: fp32 accumulation of nb scaled block
+    terms (one rounding per product and per addition), then a few fp32 ops
+    and expf (<= 2 ulp) for h."""
+    gam = (nb + 2) * U32 * 1.01
+    Eg, Eu = gam * gabs, gam * uabs
+    sg = 1.0 / (1.0 + np.exp(-np.clip(g, -700, 700)))
+    dh_dg = np.abs(u * sg * (1.0 + g * (1.0 - sg))) + np.abs(u) * 1e-30
+    silu = np.abs(g * sg)
+    h = g * u * sg
+    return dh_dg * (Eg + 1e-30) + silu * Eu + 8 * U32 * np.abs(h) + 1e-38
+
+
+def check_h_codes(hq_gpu, hd_gpu, it, nbh):
+    """Validate the GPU's quantized h against the oracle's binary64 h.
+    Returns the number of codes that differ from the oracle's (all valid)."""
+    A, F = it["h"].shape
+    h = it["h"]
+    E = h_error_bound(it["g"], it["u"], it["gabs"], it["uabs"], nbh)
+    hb = h.reshape(A, F // 32, 32)
+    Eb = E.reshape(A, F // 32, 32)
+    amax = np.abs(hb.astype(np.float32).astype(np.float64)).max(axis=2)
+    Ea = np.abs(Eb).max(axis=2)
+    lo = f16(np.float16(np.float32(np.maximum(amax - Ea, 0)) / np.float32(127)).view(np.uint16))
+    hi = f16(np.float16(np.float32(amax + Ea) / np.float32(127)).view(np.uint16))
+    dd = f16(hd_gpu)
+    bad_d = (dd < lo) | (dd > hi)
+    assert not bad_d.any(), f"h scale outside its valid range at {np.argwhere(bad_d)[:5]}"
+    ddb = dd[..., None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        clo = np.where(ddb > 0, np.clip(np.rint((hb - Eb) / ddb), -127, 127), 0)
+        chi = np.where(ddb > 0, np.clip(np.rint((hb + Eb) / ddb), -127, 127), 0)
+    c = hq_gpu.reshape(A, F // 32, 32).astype(np.float64)
+    bad = (c < clo) | (c > chi)
+    assert not bad.any(), f"h code outside its valid range at {np.argwhere(bad)[:5]}"
+    return int((hq_gpu != it["hq"]).sum()) + int((hd_gpu != it["hd"]).sum())
+
+
+def assert_close(y_gpu, y_ref, what="y"):
+    err = np.abs(y_gpu.astype(np.float64) - y_ref)
+    tol = ATOL + RTOL * np.abs(y_ref)
+    bad = err > tol
+    assert not bad.any(), (f"{what}: {bad.sum()} of {bad.size} outside tolerance; worst "
+                           f"{(err / tol).max():.3g}x at {np.unravel_index((err / tol).argmax(), err.shape)}")
+
+
+class Model:
+    """A small stack of expert tensors registered in one context."""
+
+    def __init__(self, H, F, E, k, L, capacity, max_tokens, seed=0, routing="zipf", zipf_s=1.1, window=64,
+                 slots_per_tensor=None, max_swaps=0, stream=None):
+        import torch
+        self.torch = torch
+        self.wl = synth.Workload("test", H, E, k, F, L, routing=routing, zipf_s=zipf_s, seed=seed,
+                                 capacity=[capacity] * L if isinstance(capacity, int) else list(capacity))
+        self.H, self.F, self.E, self.k, self.L = H, F, E, k, L
+        self.spt = slots_per_tensor if slots_per_tensor is not None else max(self.wl.capacity)
+        self.ctx = qec.moe_layer_init(H, F, E, k, L, self.spt, max_tokens, window_tokens=window,
+                                      max_swaps_per_step=max_swaps, stream=stream)
+        self.tensors = {}
+        self.policy = oracle.PolicyOracle(E, window=window, max_swaps_per_step=max_swaps,
+                                          slots_per_tensor=self.spt, n_tensors=3 * L)
+        for layer in range(L):
+            order = self.wl.seed_order(layer)
+            cap = self.wl.layer_capacity(layer)
+            for kind in range(3):
+                t = self.wl.expert_tensor(layer, kind)
+                rows, cols = self.wl.tensor_shapes[kind]
+                tid = qec.register_expert_tensor(self.ctx, layer, kind, t, rows, cols, cap, order, cap)
+                assert tid == layer * 3 + kind
+                self.tensors[tid] = t
+                self.policy.add_tensor(tid, cap, order, cap)
+
+    def close(self):
+        qec.moe_destroy(self.ctx)
+        self.ctx = None
+
+    def tensor(self, layer, kind):
+        return self.tensors[layer * 3 + kind]
+
+    # -- device helpers --------------------------------------------------------
+    def dev(self, a):
+        return self.torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+    def route(self, logits_np):
+        torch = self.torch
+        T = logits_np.shape[0]
+        lg = self.dev(logits_np)
+        idx = torch.empty((T, self.k), dtype=torch.int32, device="cuda")
+        w = torch.empty((T, self.k), dtype=torch.float32, device="cuda")
+        qec.route_topk(self.ctx, lg, T, self.E, self.k, idx, w)
+        torch.cuda.synchronize()
+        return idx, w
+
+    def forward(self, layer, x_np, idx, w):
+        torch = self.torch
+        T = x_np.shape[0]
+        x = self.dev(x_np)
+        y = torch.empty((T, self.H), dtype=torch.float32, device="cuda")
+        qec.moe_ffn_forward(self.ctx, layer, x, T, idx, w, y)
+        return y
+
+    def read_debug(self, T):
+        H, F, k = self.H, self.F, self.k
+        xq = np.empty((T, H), np.int8)
+        xd = np.empty((T, H // 32), np.uint16)
+        hq = np.empty((T * k, F), np.int8)
+        hd = np.empty((T * k, F // 32), np.uint16)
+        for what, arr in ((0, xq), (1, xd), (2, hq), (3, hd)):
+            qec.moe_debug_read(self.ctx, what, arr)
+        return xq, xd, hq, hd
+
+    def expected_tbl(self, tid):
+        lay = qec.moe_cache_layout(self.ctx, tid)
+        snap = self.policy.snapshot(tid)
+        out = np.empty(self.E, np.uint64)
+        for e in range(self.E):
+            s = snap["slot_of"][e]
+            if s >= 0:
+                out[e] = lay["pool_base"] + (s * lay["n_tensors"] + tid) * lay["slot_bytes"]
+            else:
+                out[e] = (lay["host_base"] + e * lay["slot_bytes"]) | 1
+        return out
+
+
+def check_layer_parity(m: Model, layer, x_np, logits_np, y_gpu, idx_gpu, w_gpu):
+    """Full-layer parity of one forward against the oracle."""
+    T = x_np.shape[0]
+    idx_o, w_o = oracle.topk(logits_np, m.k)
+    assert np.array_equal(idx_gpu, idx_o), "top-k indices differ"
+    np.testing.assert_allclose(w_gpu, w_o, rtol=1e-5, atol=1e-7)
+    used = sorted(set(idx_o.ravel().tolist()))
+    g = {e: m.tensor(layer, 0)[e] for e in used}
+    u = {e: m.tensor(layer, 1)[e] for e in used}
+    d = {e: m.tensor(layer, 2)[e] for e in used}
+    y_o, it = oracle.layer(x_np, idx_o, w_o, g, u, d, m.H, m.F, want_intermediates=True)
+    xq, xd, hq, hd = m.read_debug(T)
+    assert np.array_equal(xq, it["xq"]), "quantized x codes differ"
+    assert np.array_equal(xd, it["xd"]), "quantized x scales differ"
+    n_alt = check_h_codes(hq, hd, it, m.H // 32)
+    y_ref = oracle.down_combine(idx_o, w_o, d, hq, hd, m.H, m.F) if n_alt else y_o
+    assert_close(y_gpu, y_ref)
+    return n_alt
