@@ -226,12 +226,12 @@ def test_injected_upload_failure_rolls_back_consistently():
                 snap = qec.moe_cache_snapshot(m.ctx, tid, m.E, m.spt)
                 lay = qec.moe_cache_layout(m.ctx, tid)
                 for e in range(m.E):
-                    s = snap["slot_of"][e]
+                    s = int(snap["slot_of"][e])
                     if s >= 0:
                         assert snap["owner"][s] == e
-                        assert snap["tbl"][e] == lay["pool_base"] + (s * 3 + tid) * lay["slot_bytes"]
+                        assert int(snap["tbl"][e]) == lay["pool_base"] + (s * 3 + tid) * lay["slot_bytes"]
                     else:
-                        assert snap["tbl"][e] == (lay["host_base"] + e * lay["slot_bytes"]) | 1
+                        assert int(snap["tbl"][e]) == (lay["host_base"] + e * lay["slot_bytes"]) | 1
         assert failed
         # outputs after the fault still match the oracle
         x, lg = m.wl.x(0, 99, 1), m.wl.logits(0, 99, 1)
