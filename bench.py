@@ -281,6 +281,7 @@ def run_ours(args):
         ms_max = float(t.item())
     tok_per_s = world * args.steps * T / (ms_max / 1e3)
     st_main = qec.moe_stats(ctx)
+    log(f"timed: {tok_per_s:.1f} tokens/s, {ms_max / args.steps:.4f} ms/step, clocks {clk}")
 
     # end to end: the step's inputs from pinned host memory, outputs back
     Xp = torch.from_numpy(Xh).pin_memory()
@@ -295,6 +296,7 @@ def run_ours(args):
     e2e_s = time.perf_counter() - t0
     barrier()
     e2e_tok = world * args.steps * T / e2e_s
+    log(f"e2e: {e2e_tok:.1f} tokens/s")
 
     # roofline of the gate/up mat-vec over the fully resident layers:
     # per-layer CUDA events around the launches, recaptured into the graph
@@ -327,7 +329,11 @@ def run_ours(args):
     for l in range(L):
         u = len(np.unique(LGh[args.warmup, l].argsort(axis=1)[:, -k:]))
         step_bytes += u * 3 * blob
-    st = qec.moe_stats(ctx)
+    # host link: zero-copy 128-bit reads of pinned host memory and copy-engine H2D
+    probe = torch.empty(2 << 30, dtype=torch.uint8).pin_memory()
+    zc_gbs, ce_gbs = qec.moe_probe_host_read(probe.data_ptr(), probe.numel(), iters=5)
+    del probe
+    log(f"host link: zero-copy read {zc_gbs:.1f} GB/s, copy engine {ce_gbs:.1f} GB/s")
     out = {
         "metric": METRIC, "value": round(tok_per_s, 2), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4), "higher_is_better": True,
@@ -345,6 +351,7 @@ def run_ours(args):
                      "avg_launch_us": round(1e3 * gu_ms / max(1, n_launch), 3),
                      "down_gemv_gbs": round(dn_bytes / (dn_ms / 1e3) / 1e9, 1)},
         "step_weight_gbs": round(step_bytes / (ms_max / args.steps / 1e3) / 1e9, 1),
+        "host_link": {"zero_copy_read_gbs": round(zc_gbs, 1), "copy_engine_h2d_gbs": round(ce_gbs, 1)},
         "cache": {"hits": st_main["hits"], "misses": st_main["misses"], "admissions": st_main["admissions"],
                   "evictions": st_main["evictions"], "cold_bytes": st_main["cold_bytes"]},
         "e2e": {"value": round(e2e_tok, 2), "unit": "tokens/s",

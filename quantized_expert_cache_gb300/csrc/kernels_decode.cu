@@ -438,16 +438,16 @@ int down_rows_per_item(int F) {
 
 // ev (optional): 4 events recorded around the gate/up and the down launch.
 int launch_gemv(const GemvParams &p, int grid_gu, int grid_dn, cudaStream_t st, cudaEvent_t const *ev) {
-    if (ev) cudaEventRecord(ev[0], st);
+    if (ev) cudaEventRecordWithFlags(ev[0], st, cudaEventRecordExternal);
     gate_up_kernel<<<grid_gu, 256, 0, st>>>(p);
-    if (ev) cudaEventRecord(ev[1], st);
+    if (ev) cudaEventRecordWithFlags(ev[1], st, cudaEventRecordExternal);
     int nbf = p.F / kBlock;
-    if (ev) cudaEventRecord(ev[2], st);
+    if (ev) cudaEventRecordWithFlags(ev[2], st, cudaEventRecordExternal);
     if (nbf <= 40)
         down_kernel<4><<<grid_dn, 256, 0, st>>>(p);
     else
         down_kernel<8><<<grid_dn, 256, 0, st>>>(p);
-    if (ev) cudaEventRecord(ev[3], st);
+    if (ev) cudaEventRecordWithFlags(ev[3], st, cudaEventRecordExternal);
     return (int)cudaGetLastError();
 }
 
