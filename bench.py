@@ -298,13 +298,12 @@ def run_ours(args):
     e2e_tok = world * args.steps * T / e2e_s
     log(f"e2e: {e2e_tok:.1f} tokens/s")
 
-    # roofline of the gate/up mat-vec over the fully resident layers:
-    # per-layer CUDA events around the launches, recaptured into the graph
+    # roofline of the gate/up mat-vec over the fully resident layers: CUDA
+    # events on the context stream around each launch, in a pass of eager
+    # steps after the timed one (event nodes inside a graph do not bracket
+    # kernel execution)
     qec.moe_debug_timing(ctx, True)
-    if graph is not None:
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream):
-            layers()
+    graph = None
     resident = [l for l in range(L) if wl.layer_capacity(l) == E]
     blob = wl.tensor_bytes(0)
     gu_ms, dn_ms, gu_bytes, dn_bytes, n_launch = 0.0, 0.0, 0, 0, 0
@@ -362,7 +361,7 @@ def run_ours(args):
     qec.moe_destroy(ctx)
     del X, LG
     if rank == 0:
-        out["cpu_baseline"] = cpu_baseline(wl, args.cpu_sample_steps, T)
+        out["cpu_baseline"] = cpu_baseline(wl, args.cpu_sample_steps, T) if args.cpu_sample_steps > 0 else None
         print(json.dumps(out), flush=True)
     if world > 1:
         import torch.distributed as dist
