@@ -437,17 +437,26 @@ int down_rows_per_item(int F) {
 }
 
 // ev (optional): 4 events recorded around the gate/up and the down launch.
+static void record(cudaEvent_t e, cudaStream_t st) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaStreamIsCapturing(st, &cs);
+    if (cs == cudaStreamCaptureStatusActive)
+        cudaEventRecordWithFlags(e, st, cudaEventRecordExternal);
+    else
+        cudaEventRecord(e, st);
+}
+
 int launch_gemv(const GemvParams &p, int grid_gu, int grid_dn, cudaStream_t st, cudaEvent_t const *ev) {
-    if (ev) cudaEventRecordWithFlags(ev[0], st, cudaEventRecordExternal);
+    if (ev) record(ev[0], st);
     gate_up_kernel<<<grid_gu, 256, 0, st>>>(p);
-    if (ev) cudaEventRecordWithFlags(ev[1], st, cudaEventRecordExternal);
+    if (ev) record(ev[1], st);
     int nbf = p.F / kBlock;
-    if (ev) cudaEventRecordWithFlags(ev[2], st, cudaEventRecordExternal);
+    if (ev) record(ev[2], st);
     if (nbf <= 40)
         down_kernel<4><<<grid_dn, 256, 0, st>>>(p);
     else
         down_kernel<8><<<grid_dn, 256, 0, st>>>(p);
-    if (ev) cudaEventRecordWithFlags(ev[3], st, cudaEventRecordExternal);
+    if (ev) record(ev[3], st);
     return (int)cudaGetLastError();
 }
 
