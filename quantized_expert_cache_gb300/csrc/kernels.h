@@ -5,6 +5,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <cuda.h>
+
 #include "common.cuh"
 
 namespace moe {
@@ -37,6 +39,41 @@ struct GemvParams {
     float *y;             // [T][H]
 };
 
+// One grouped GEMM launch (gate/up with SwiGLU + h quantization, or down).
+struct GemmParams {
+    const int32_t *n_uniq, *uniq_e, *uniq_off, *tile_off, *assign;
+    const uint64_t *tbl[2];     // expert tables of the A operands (gate, up) or (down, -)
+    const float *a_scaleT;      // [K/32][A_pad]: block scales of the sorted activation rows
+    int rows, K;                // weight rows (output features) and reduction length
+    int A, A_pad, k, F_out;
+    __half *hq16;               // gate/up: [A_pad][F] sorted h codes as fp16
+    float *hdT;                 // gate/up: [F/32][A_pad] sorted h scales
+    int8_t *hq;                 // gate/up: [A][F] h codes by assignment
+    BlockScale *hds;            // gate/up: [A][F/32] by assignment
+    float *o;                   // down: [A][H] by assignment
+    int *error;                 // bit set when a bounded wait expires
+};
+
+struct TilingParams {
+    CacheView cv;
+    const int32_t *n_uniq, *uniq_e, *uniq_off;
+    int32_t *tile_off_gu, *tile_off_dn;
+    int tid0, n_tokens, rt_gu, bn_gu, rt_dn, bn_dn;
+};
+
+struct PrefillLaunch {
+    TilingParams tiling;
+    GemmParams gu, dn;
+    CUtensorMap tm_x, tm_h;     // sorted fp16 activations / h codes, 128-B swizzle
+    const int8_t *xq;
+    const BlockScale *xds;
+    __half *xs16;
+    float *xdT;
+    const float *w;
+    float *y;
+    int T, k, H, n_sm;
+};
+
 // One table / slot / stamp write of the promotion pass.
 struct Update {
     uint32_t what;   // 0: tbl[index] = value; 1: slot[index] = value; 2: stamps[index] = value
@@ -52,6 +89,9 @@ int down_rows_per_item(int F);
 int launch_block_dots(const uint8_t *blob, int rows, int nb, int row0, int n_rows, const int8_t *qa, int32_t *out,
                       cudaStream_t st);
 int launch_stream_read(const void *src, size_t bytes, uint32_t *sink, int n_sm, cudaStream_t st);
+int launch_prefill(const PrefillLaunch &L, cudaStream_t st);
+int gemm_configure();
+int gemm_bn(bool dual);
 int launch_apply_updates(const Update *u, int n, uint64_t *tbl, int32_t *slot, uint32_t *stamps, uint32_t *clock,
                          uint32_t new_clock, cudaStream_t st);
 

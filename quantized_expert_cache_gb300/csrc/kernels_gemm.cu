@@ -1,0 +1,598 @@
+// Prefill path of the routed-expert FFN: a grouped per-expert GEMM on the
+// 5th-generation tensor cores (tcgen05, accumulators in TMEM), over tokens
+// sorted by expert, only over (expert, tile) pairs that hold tokens.
+//
+// Sources: mihailescu2m/llama.cpp, Metal kernels ("MUL_MAT_ID over used tiles
+// only": the expert GEMM runs only over the (expert, tile) pairs that hold
+// tokens); neurall/llama.cpp, "How it works" (prompts in few big passes, each
+// expert upload serving many prompt tokens); the Q4 / q8_1 block formats of
+// the mat-vec kernels (Zapdev-labs/a6000-custom-kernels; mx-llama.cpp
+// FEATURES.md).
+//
+// Arithmetic.  sm_103a has no integer tcgen05 MMA (ptxas rejects kind::i8), so
+// the MMA is kind::f16 with integer-valued fp16 operands: weight codes q-8 in
+// [-8, 7] and activation codes in [-127, 127] are exact in fp16, and the fp32
+// sum of the 32 products of one quantization block (|sum| <= 32512) is exact.
+// Each 32-wide K block is accumulated into its own TMEM buffer, so the MMA
+// produces exactly the int32 block dots of the mat-vec path; epilogue warps
+// then add d_w * d_a * sumi in fp32 (fma.rn.f32x2), as the mat-vec does.
+//
+// Tile: M = 128 weight rows (TMEM lanes) x N tokens (TMEM columns), K staged
+// 64 at a time (two quantization blocks = one 128-B swizzle row of fp16).
+// Warp roles (10 warps): 0 TMA producer of the token tile; 1 TMEM owner and
+// MMA issuer; 2-5 weight converters (Q4 codes read through the expert table,
+// from the HBM pool or zero-copy from pinned host memory, turned into fp16
+// and stored in the 128-B swizzled K-major layout); 6-9 epilogue (TMEM lane
+// quarter = warp % 4).  Gate/up tiles hold two A operands (gate rows and up
+// rows) so SwiGLU and the quantization of h happen in the epilogue; the 32
+// rows of one h block are the 32 lanes of one epilogue warp.
+//
+// Every mbarrier wait is bounded (about 2 s of SM clock): on expiry the CTA
+// sets an error bit, all roles leave their loops, in-flight copies and MMAs
+// are drained with bounded waits and TMEM is freed before the CTA exits.
+#include <cuda.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace gemm {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int NWARPS = 10;
+constexpr int NTHREADS = NWARPS * 32;
+constexpr int W_TMA = 0, W_MMA = 1, W_CONV = 2, W_EPI = 6;
+constexpr long long kTimeoutCycles = 4000000000ll;
+
+template <bool DUAL>
+struct Cfg {
+    static constexpr int BN = DUAL ? 64 : 128;
+    static constexpr int NA = DUAL ? 2 : 1;
+    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int STAGE_BYTES = NA * A_BYTES + B_BYTES;
+    static constexpr int TBUF = NA * BN;          // TMEM columns per K-block buffer
+    static constexpr int NTBUF = 512 / TBUF;      // K-block buffers in TMEM
+    static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
+    // barriers: full[S], empty[S], tfull[NT], tempty[NT]; then tmem slot,
+    // abort flag, epilogue scale buffers
+    static constexpr int NBARS = 2 * STAGES + 2 * NTBUF;
+    static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
+    static constexpr int DA_OFF = MISC_OFF + 16;
+    static constexpr int SMEM = DA_OFF + 4 * BN * 4 + 1024;  // + alignment slack
+};
+
+// ---- PTX wrappers -----------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_tx(uint32_t bar, uint32_t tx) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(tx) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n.reg .pred P;\nmbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2;\nselp.u32 %0, 1, 0, P;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait: false when the CTA is aborting or the wait expired (then the
+// abort flag and an error bit are set).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag, int *err,
+                                          int code) {
+    const long long t0 = clock64();
+    while (!mbar_try(bar, parity)) {
+        if (*abort_flag) return false;
+        if (clock64() - t0 > kTimeoutCycles) {
+            *abort_flag = 1;
+            atomicOr(err, code);
+            return false;
+        }
+    }
+    return true;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *tm, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+            "r"(dst),
+        "l"((uint64_t)tm), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major, 128-B swizzle, 8-row groups 1024 B
+// apart (SBO), Blackwell descriptor version 1.
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr) {
+    return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Instruction descriptor, kind::f16: D fp32, A/B fp16, both K-major, N, M.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
+    return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\ntcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(
+            d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// acc{0,1} += p{0,1} * s{0,1}, two IEEE fp32 fused multiply-adds.
+__device__ __forceinline__ void fma2(float &a0, float &a1, float p0, float p1, float s0, float s1) {
+    unsigned long long acc, pp, ss;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(acc) : "f"(a0), "f"(a1));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(pp) : "f"(p0), "f"(p1));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(ss) : "f"(s0), "f"(s1));
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(pp), "l"(ss));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(acc));
+}
+
+// Q4 codes of one row and two quantization blocks (32 B) -> 64 fp16 values
+// (q - 8) in K order, stored as 8 16-byte chunks of the row in the 128-B
+// swizzled layout (chunk c of row r of an 8-row group sits at chunk c ^ r).
+__device__ __forceinline__ uint32_t nib_pair(uint32_t w, int sel, int hi) {
+    // two bytes of w (selected) -> their low (hi=0) or high (hi=1) nibbles as
+    // the fp16 pair (1024 + n0, 1024 + n1), then minus (1032, 1032)
+    uint32_t t = __byte_perm(w, 0, sel);
+    if (hi) t >>= 4;
+    t = (t & 0x000F000Fu) | 0x64006400u;
+    __half2 h = *reinterpret_cast<__half2 *>(&t);
+    h = __hsub2(h, __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408)));
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+__device__ __forceinline__ void convert_store_row(uint8_t *tile, int r, uint4 c0, uint4 c1) {
+    const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+    uint8_t *rowbase = tile + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+    for (int blk = 0; blk < 2; ++blk) {
+        const uint32_t *q = w + 4 * blk;  // 16 code bytes of this block
+#pragma unroll
+        for (int part = 0; part < 4; ++part) {
+            // part 0: elements 0..7 (low nibbles of bytes 0..7), 1: 8..15
+            // (low, bytes 8..15), 2: 16..23 (high, bytes 0..7), 3: 24..31
+            const int hi = part >> 1;
+            const uint32_t wa = q[(part & 1) * 2], wb = q[(part & 1) * 2 + 1];
+            uint4 out;
+            out.x = nib_pair(wa, 0x4140, hi);
+            out.y = nib_pair(wa, 0x4342, hi);
+            out.z = nib_pair(wb, 0x4140, hi);
+            out.w = nib_pair(wb, 0x4342, hi);
+            const int chunk = blk * 4 + part;
+            *reinterpret_cast<uint4 *>(rowbase + ((chunk ^ (r & 7)) << 4)) = out;
+        }
+    }
+}
+
+// tile index -> (used expert u, row tile, token tile); token tile innermost.
+__device__ __forceinline__ void decode_tile(int t, const int32_t *tile_off, int n_uniq, const int32_t *uniq_off,
+                                            int bn, int &u, int &row_tile, int &tok_tile) {
+    int lo = 0, hi = n_uniq - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (tile_off[mid] <= t)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    u = lo;
+    const int n = uniq_off[u + 1] - uniq_off[u];
+    const int ntok = (n + bn - 1) / bn;
+    const int local = t - tile_off[u];
+    row_tile = local / ntok;
+    tok_tile = local - row_tile * ntok;
+}
+
+template <bool DUAL>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmB, GemmParams p) {
+    using C = Cfg<DUAL>;
+    constexpr int BN = C::BN, NA = C::NA, NTBUF = C::NTBUF;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint64_t *bars = (uint64_t *)(smem + C::BAR_OFF);
+    const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * STAGES, tfull0 = empty0 + 8 * STAGES,
+                   tempty0 = tfull0 + 8 * NTBUF;
+    volatile uint32_t *tmem_slot = (volatile uint32_t *)(smem + C::MISC_OFF);
+    volatile int *abort_flag = (volatile int *)(smem + C::MISC_OFF + 4);
+    float *da_ep = (float *)(smem + C::DA_OFF);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full0 + 8 * s, 1 + 4);
+            mbar_init(empty0 + 8 * s, 1);
+        }
+        for (int j = 0; j < NTBUF; ++j) {
+            mbar_init(tfull0 + 8 * j, 1);
+            mbar_init(tempty0 + 8 * j, 4);
+        }
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == W_MMA) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
+                         smem_u32((const void *)tmem_slot))
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    const int n_uniq = *p.n_uniq;
+    const int total = n_uniq > 0 ? p.tile_off[n_uniq] : 0;
+    const int nkt = p.K / BK;
+    const int nbk = p.K / kBlock;
+    const size_t scale_off = blob_scales_offset(p.rows, nbk);
+
+    if (warp == W_TMA) {
+        if (lane == 0) {
+            int it = 0;
+            for (int t = blockIdx.x; t < total; t += gridDim.x) {
+                int u, rt, tt;
+                decode_tile(t, p.tile_off, n_uniq, p.uniq_off, BN, u, rt, tt);
+                const int pos0 = p.uniq_off[u] + tt * BN;
+                for (int kt = 0; kt < nkt; ++kt, ++it) {
+                    const int slot = it % STAGES;
+                    const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+                    if (!mbar_wait(empty0 + 8 * slot, ph ^ 1u, abort_flag, p.error, 2)) goto tma_done;
+                    mbar_arrive_tx(full0 + 8 * slot, C::B_BYTES);
+                    tma_load_2d(smem_u32(smem + slot * C::STAGE_BYTES + NA * C::A_BYTES), &tmB, kt * BK, pos0,
+                                full0 + 8 * slot);
+                }
+            }
+        tma_done:;
+        }
+    } else if (warp == W_MMA) {
+        if (lane == 0) {
+            const uint32_t idesc = idesc_f16(BM, BN);
+            int it = 0, qc = 0;
+            for (int t = blockIdx.x; t < total; t += gridDim.x) {
+                for (int kt = 0; kt < nkt; ++kt, ++it) {
+                    const int slot = it % STAGES;
+                    if (!mbar_wait(full0 + 8 * slot, (uint32_t)(it / STAGES) & 1u, abort_flag, p.error, 4))
+                        goto mma_done;
+                    tc_fence_after();
+                    uint8_t *st = smem + slot * C::STAGE_BYTES;
+                    const uint64_t db = sdesc(smem_u32(st + NA * C::A_BYTES));
+                    for (int blk = 0; blk < 2; ++blk, ++qc) {
+                        const int j = qc % NTBUF;
+                        if (!mbar_wait(tempty0 + 8 * j, ((uint32_t)(qc / NTBUF) & 1u) ^ 1u, abort_flag, p.error, 8))
+                            goto mma_done;
+                        tc_fence_after();
+#pragma unroll
+                        for (int kk = 0; kk < 2; ++kk) {
+                            const uint64_t koff = (uint64_t)((blk * 32 + kk * 16) * 2) >> 4;
+#pragma unroll
+                            for (int a = 0; a < NA; ++a) {
+                                const uint64_t da = sdesc(smem_u32(st + a * C::A_BYTES));
+                                mma_f16(tmem + (uint32_t)(j * C::TBUF + a * BN), da + koff, db + koff, idesc,
+                                        kk > 0 ? 1u : 0u);
+                            }
+                        }
+                        mma_commit(tfull0 + 8 * j);
+                    }
+                    mma_commit(empty0 + 8 * slot);
+                }
+            }
+        mma_done:;
+        }
+    } else if (warp < W_EPI) {
+        // weight converters: thread r converts row r of each A tile
+        const int r = threadIdx.x - W_CONV * 32;
+        int it = 0;
+        for (int t = blockIdx.x; t < total; t += gridDim.x) {
+            int u, rt, tt;
+            decode_tile(t, p.tile_off, n_uniq, p.uniq_off, BN, u, rt, tt);
+            const int e = p.uniq_e[u];
+            const int row = rt * BM + r;
+            const bool valid = row < p.rows;
+            const uint4 *src[NA];
+#pragma unroll
+            for (int a = 0; a < NA; ++a) {
+                const uint64_t ent = p.tbl[a][e];
+                src[a] = (const uint4 *)(uintptr_t)(ent & ~1ull) + (size_t)(valid ? row : 0) * nbk;
+            }
+            for (int kt = 0; kt < nkt; ++kt, ++it) {
+                uint4 c[NA][2];
+#pragma unroll
+                for (int a = 0; a < NA; ++a) {
+                    if (valid) {
+                        c[a][0] = ld_weights(src[a] + 2 * kt);
+                        c[a][1] = ld_weights(src[a] + 2 * kt + 1);
+                    } else {
+                        c[a][0] = c[a][1] = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
+                    }
+                }
+                const int slot = it % STAGES;
+                const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+                bool ok = true;
+                if (lane == 0) ok = mbar_wait(empty0 + 8 * slot, ph ^ 1u, abort_flag, p.error, 16);
+                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                if (!ok) goto conv_done;
+                uint8_t *st = smem + slot * C::STAGE_BYTES;
+#pragma unroll
+                for (int a = 0; a < NA; ++a) convert_store_row(st + a * C::A_BYTES, r, c[a][0], c[a][1]);
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(full0 + 8 * slot);
+            }
+        }
+    conv_done:;
+    } else {
+        // epilogue: TMEM lane quarter = warp % 4; thread = weight row
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;
+        int qc = 0;
+        for (int t = blockIdx.x; t < total; t += gridDim.x) {
+            int u, rt, tt;
+            decode_tile(t, p.tile_off, n_uniq, p.uniq_off, BN, u, rt, tt);
+            const int e = p.uniq_e[u];
+            const int row = rt * BM + r;
+            const bool vrow = row < p.rows;
+            const int pos0 = p.uniq_off[u] + tt * BN;
+            const int pos_end = p.uniq_off[u + 1];
+            const __half *dsc[NA];
+#pragma unroll
+            for (int a = 0; a < NA; ++a) {
+                const uint64_t ent = p.tbl[a][e];
+                dsc[a] = (const __half *)((const uint8_t *)(uintptr_t)(ent & ~1ull) + scale_off) +
+                         (size_t)(vrow ? row : 0) * nbk;
+            }
+            float acc[NA][BN];
+#pragma unroll
+            for (int a = 0; a < NA; ++a)
+#pragma unroll
+                for (int c = 0; c < BN; ++c) acc[a][c] = 0.0f;
+            float *dbuf = da_ep + (warp - W_EPI) * BN;  // this warp's copy of the token scales
+            for (int q = 0; q < nbk; ++q, ++qc) {
+                // activation scales of this K block for the tile's tokens
+                __syncwarp();
+#pragma unroll
+                for (int c = lane; c < BN; c += 32) {
+                    const int pos = pos0 + c;
+                    dbuf[c] = pos < p.A_pad ? p.a_scaleT[(size_t)q * p.A_pad + pos] : 0.0f;
+                }
+                __syncwarp();
+                float dw[NA];
+#pragma unroll
+                for (int a = 0; a < NA; ++a) dw[a] = __half2float(dsc[a][q]);
+                const int j = qc % NTBUF;
+                bool ok = true;
+                if (lane == 0) ok = mbar_wait(tfull0 + 8 * j, (uint32_t)(qc / NTBUF) & 1u, abort_flag, p.error, 32);
+                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                if (!ok) goto epi_done;
+                tc_fence_after();
+                const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(j * C::TBUF);
+#pragma unroll
+                for (int a = 0; a < NA; ++a) {
+#pragma unroll
+                    for (int c0 = 0; c0 < BN; c0 += 16) {
+                        float pv[16];
+                        tmem_ld16(tb + (uint32_t)(a * BN + c0), pv);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int c = 0; c < 16; c += 2) {
+                            const float2 d2 = *reinterpret_cast<const float2 *>(dbuf + c0 + c);
+                            fma2(acc[a][c0 + c], acc[a][c0 + c + 1], pv[c], pv[c + 1], dw[a] * d2.x, dw[a] * d2.y);
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty0 + 8 * j);
+            }
+            // tile outputs
+            if (DUAL) {
+                const int fb = (rt * BM + quarter * 32) / kBlock;  // h block index along F
+                const bool vblk = rt * BM + quarter * 32 < p.rows;
+#pragma unroll
+                for (int c = 0; c < BN; ++c) {
+                    const int pos = pos0 + c;
+                    const float g = acc[0][c], uu = acc[NA - 1][c];
+                    const float h = g * uu / (1.0f + expf(-g));
+                    const float amax = warp_max(fabsf(h));
+                    const float dd = __half2float(__float2half_rn(amax / 127.0f));
+                    int qv = 0;
+                    if (dd != 0.0f) qv = (int)fminf(fmaxf(rintf(h / dd), -127.0f), 127.0f);
+                    const int s = warp_sum_i(qv);
+                    if (vblk && pos < pos_end) {
+                        const int a = p.assign[pos];
+                        p.hq16[(size_t)pos * p.F_out + row] = __int2half_rn(qv);
+                        p.hq[(size_t)a * p.F_out + row] = (int8_t)qv;
+                        if (lane == 0) {
+                            p.hdT[(size_t)fb * p.A_pad + pos] = dd;
+                            p.hds[(size_t)a * (p.F_out / kBlock) + fb] = BlockScale{dd, s};
+                        }
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < BN; ++c) {
+                    const int pos = pos0 + c;
+                    if (vrow && pos < pos_end) p.o[(size_t)p.assign[pos] * p.rows + row] = acc[0][c];
+                }
+            }
+        }
+    epi_done:;
+    }
+
+    // drain: after an abort, give the copies and MMAs this CTA issued a
+    // bounded time (about 10 ms) to land, then free TMEM
+    __syncwarp();
+    __syncthreads();
+    if (*abort_flag) {
+        const long long t0 = clock64();
+        while (clock64() - t0 < 20000000ll) {
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == W_MMA) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem) : "memory");
+}
+
+}  // namespace gemm
+
+// ---------------------------------------------------------------- prefill helpers
+// Per used expert: cumulative tile counts of the gate/up and down GEMMs, and
+// the miss / stamp record of the layer's three tensors.
+__global__ void tiling_kernel(TilingParams p) {
+    __shared__ int warp_tot[33];
+    const int n_uniq = *p.n_uniq;
+    const uint32_t step_clock = *p.cv.clock + (uint32_t)p.n_tokens;
+    for (int u = threadIdx.x; u < n_uniq; u += blockDim.x) {
+        const int e = p.uniq_e[u];
+        for (int kd = 0; kd < 3; ++kd) {
+            const int tid = p.tid0 + kd;
+            record_read(p.cv, tid, e, p.cv.tbl[(size_t)tid * p.cv.E + e], step_clock);
+        }
+    }
+    int run_gu = 0, run_dn = 0;
+    for (int base = 0; base < n_uniq; base += blockDim.x) {
+        const int u = base + threadIdx.x;
+        int tg = 0, td = 0;
+        if (u < n_uniq) {
+            const int n = p.uniq_off[u + 1] - p.uniq_off[u];
+            tg = p.rt_gu * ((n + p.bn_gu - 1) / p.bn_gu);
+            td = p.rt_dn * ((n + p.bn_dn - 1) / p.bn_dn);
+        }
+        // inclusive warp scans then block offsets, for both counts
+        int ig = tg, id = td;
+        const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int a = __shfl_up_sync(0xffffffffu, ig, o), b = __shfl_up_sync(0xffffffffu, id, o);
+            if (lane >= o) {
+                ig += a;
+                id += b;
+            }
+        }
+        __shared__ int wg[32], wd[32];
+        if (lane == 31) {
+            wg[wid] = ig;
+            wd[wid] = id;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            int sg = 0, sd = 0;
+            for (int w = 0; w < nw; ++w) {
+                int a = wg[w], b = wd[w];
+                wg[w] = sg;
+                wd[w] = sd;
+                sg += a;
+                sd += b;
+            }
+            warp_tot[0] = sg;
+            warp_tot[1] = sd;
+        }
+        __syncthreads();
+        if (u < n_uniq) {
+            p.tile_off_gu[u] = run_gu + wg[wid] + ig - tg;
+            p.tile_off_dn[u] = run_dn + wd[wid] + id - td;
+        }
+        run_gu += warp_tot[0];
+        run_dn += warp_tot[1];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        p.tile_off_gu[n_uniq] = run_gu;
+        p.tile_off_dn[n_uniq] = run_dn;
+    }
+}
+
+// Sorted fp16 activation rows and transposed block scales: row pos of expert
+// order = token of assignment assign[pos].
+__global__ void gather_kernel(const int32_t *__restrict__ assign, int A, int k, int H, const int8_t *__restrict__ xq,
+                              const BlockScale *__restrict__ xds, __half *__restrict__ xs16, float *__restrict__ xdT,
+                              int A_pad) {
+    const int nbx = H / kBlock;
+    const size_t n = (size_t)A * (H / 8);
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+        const int pos = (int)(i / (H / 8)), c8 = (int)(i % (H / 8));
+        const int t = assign[pos] / k;
+        const uint2 q = *reinterpret_cast<const uint2 *>(xq + (size_t)t * H + c8 * 8);
+        const int8_t *b = reinterpret_cast<const int8_t *>(&q);
+        __half h[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) h[j] = __int2half_rn(b[j]);
+        *reinterpret_cast<uint4 *>(xs16 + (size_t)pos * H + c8 * 8) = *reinterpret_cast<uint4 *>(h);
+        if ((c8 & 3) == 0) xdT[(size_t)(c8 / 4) * A_pad + pos] = xds[(size_t)t * nbx + c8 / 4].d;
+    }
+}
+
+// y[t][i] = sum_j w[t][j] * o[t*k + j][i], j in order.
+__global__ void combine_kernel(const float *__restrict__ o, const float *__restrict__ w, float *__restrict__ y, int T,
+                               int k, int H) {
+    const size_t n = (size_t)T * H;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+        const int t = (int)(i / H), c = (int)(i % H);
+        float acc = 0.0f;
+        for (int j = 0; j < k; ++j) acc += w[(size_t)t * k + j] * o[((size_t)t * k + j) * H + c];
+        y[i] = acc;
+    }
+}
+
+int gemm_smem_bytes(bool dual) { return dual ? gemm::Cfg<true>::SMEM : gemm::Cfg<false>::SMEM; }
+int gemm_bn(bool dual) { return dual ? gemm::Cfg<true>::BN : gemm::Cfg<false>::BN; }
+
+int gemm_configure() {
+    cudaError_t e1 = cudaFuncSetAttribute(gemm::grouped_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          gemm::Cfg<true>::SMEM);
+    cudaError_t e2 = cudaFuncSetAttribute(gemm::grouped_gemm_kernel<false>,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize, gemm::Cfg<false>::SMEM);
+    return (int)(e1 != cudaSuccess ? e1 : e2);
+}
+
+int launch_prefill(const PrefillLaunch &L, cudaStream_t st) {
+    tiling_kernel<<<1, 1024, 0, st>>>(L.tiling);
+    const int A = L.gu.A;
+    int g = (int)std::min<size_t>(((size_t)A * (L.H / 8) + 255) / 256, (size_t)L.n_sm * 16);
+    if (g > 0) gather_kernel<<<g, 256, 0, st>>>(L.gu.assign, A, L.k, L.H, L.xq, L.xds, L.xs16, L.xdT, L.gu.A_pad);
+    gemm::grouped_gemm_kernel<true><<<L.n_sm, gemm::NTHREADS, gemm::Cfg<true>::SMEM, st>>>(L.tm_x, L.gu);
+    gemm::grouped_gemm_kernel<false><<<L.n_sm, gemm::NTHREADS, gemm::Cfg<false>::SMEM, st>>>(L.tm_h, L.dn);
+    const size_t n = (size_t)L.T * L.H;
+    int gc = (int)std::min<size_t>((n + 255) / 256, (size_t)L.n_sm * 16);
+    combine_kernel<<<gc, 256, 0, st>>>(L.dn.o, L.w, L.y, L.T, L.k, L.H);
+    return (int)cudaGetLastError();
+}
+
+}  // namespace moe

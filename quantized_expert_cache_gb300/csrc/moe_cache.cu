@@ -12,6 +12,8 @@
 #include "../../include/moe_cache.h"
 #include "kernels.h"
 
+#include <cudaTypedefs.h>
+
 #include <algorithm>
 #include <chrono>
 #include <cstdio>
@@ -63,6 +65,13 @@ struct moe_ctx {
     float *o = nullptr;
     unsigned *counters = nullptr;
     int n_counters = 0;
+    // prefill (grouped GEMM) workspaces
+    bool gemm_ok = false;
+    int A_pad = 0;
+    __half *xs16 = nullptr, *hq16 = nullptr;
+    float *xdT = nullptr, *hdT = nullptr;
+    int32_t *tile_off = nullptr;  // [2][U + 1]
+    CUtensorMap tm_x{}, tm_h{};
 
     uint32_t *h_readback = nullptr;  // pinned: count + miss list
     uint32_t *h_stamps = nullptr;    // pinned
@@ -182,6 +191,30 @@ void repack(const uint8_t *src, uint8_t *dst, int n_experts, int rows, int nb, s
     for (auto &x : th) x.join();
 }
 
+// 2-D fp16 tensor map [rows][cols] (row-major), box {64 elements, box_rows},
+// 128-B swizzle, zero fill out of bounds.
+int make_tmap(moe_ctx *ctx, CUtensorMap *tm, void *base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+    static PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+    if (!enc) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn)
+            return fail(ctx, MOE_ERR_CUDA, "cuTensorMapEncodeTiled entry point not found");
+        enc = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+    }
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {64, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(ctx, MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+    return MOE_OK;
+}
+
 uint16_t f32_to_half_bits(float v) {
     __half h = __float2half_rn(v);
     uint16_t b;
@@ -276,6 +309,26 @@ int moe_layer_init(const moe_cfg *cfg, void *cuda_stream, moe_ctx **out) {
     ctx->n_counters = ctx->H / down_rows;
     CKI(cudaMalloc(&ctx->counters, sizeof(unsigned) * ctx->n_counters));
     CKI(cudaMemset(ctx->counters, 0, sizeof(unsigned) * ctx->n_counters));
+
+    // prefill workspaces: sorted fp16 operands of the grouped GEMM
+    if (ctx->M > 32 && ctx->H % 64 == 0 && ctx->F % 64 == 0) {
+        ctx->A_pad = (int)((A + 127) / 128 * 128 + 128);
+        const size_t AP = ctx->A_pad;
+        CKI(cudaMalloc(&ctx->xs16, sizeof(__half) * AP * ctx->H));
+        CKI(cudaMemset(ctx->xs16, 0, sizeof(__half) * AP * ctx->H));
+        CKI(cudaMalloc(&ctx->xdT, sizeof(float) * AP * (ctx->H / 32)));
+        CKI(cudaMemset(ctx->xdT, 0, sizeof(float) * AP * (ctx->H / 32)));
+        CKI(cudaMalloc(&ctx->hq16, sizeof(__half) * AP * ctx->F));
+        CKI(cudaMemset(ctx->hq16, 0, sizeof(__half) * AP * ctx->F));
+        CKI(cudaMalloc(&ctx->hdT, sizeof(float) * AP * (ctx->F / 32)));
+        CKI(cudaMemset(ctx->hdT, 0, sizeof(float) * AP * (ctx->F / 32)));
+        CKI(cudaMalloc(&ctx->tile_off, sizeof(int32_t) * 2 * (U + 1)));
+        if (make_tmap(ctx, &ctx->tm_x, ctx->xs16, AP, ctx->H, (uint32_t)moe::gemm_bn(true)) ||
+            make_tmap(ctx, &ctx->tm_h, ctx->hq16, AP, ctx->F, (uint32_t)moe::gemm_bn(false)))
+            return cleanup_fail(MOE_ERR_CUDA);
+        CKI((cudaError_t)moe::gemm_configure());
+        ctx->gemm_ok = true;
+    }
 
     CKI(cudaHostAlloc(&ctx->h_readback, sizeof(uint32_t) * (1 + (size_t)ctx->miss_cap), cudaHostAllocDefault));
     CKI(cudaHostAlloc(&ctx->h_stamps, sizeof(uint32_t) * (size_t)nt * std::max(1, ctx->spt), cudaHostAllocDefault));
@@ -434,6 +487,68 @@ int moe_ffn_forward(moe_ctx *ctx, int layer, const float *d_x, int n_tokens, con
     gp.w = d_w;
     gp.y = d_y;
     const int A = T * ctx->k, U = std::min(A, ctx->E);
+    if (!small && ctx->gemm_ok) {
+        // prefill: grouped tensor-core GEMM over tokens sorted by expert
+        const int Umax = std::min(ctx->M * ctx->k, ctx->E);
+        moe::PrefillLaunch L{};
+        L.tiling.cv = gp.cv;
+        L.tiling.n_uniq = gp.n_uniq;
+        L.tiling.uniq_e = gp.uniq_e;
+        L.tiling.uniq_off = gp.uniq_off;
+        L.tiling.tile_off_gu = ctx->tile_off;
+        L.tiling.tile_off_dn = ctx->tile_off + Umax + 1;
+        L.tiling.tid0 = layer * 3;
+        L.tiling.n_tokens = T;
+        L.tiling.rt_gu = (ctx->F + 127) / 128;
+        L.tiling.bn_gu = moe::gemm_bn(true);
+        L.tiling.rt_dn = (ctx->H + 127) / 128;
+        L.tiling.bn_dn = moe::gemm_bn(false);
+        moe::GemmParams g{};
+        g.n_uniq = gp.n_uniq;
+        g.uniq_e = gp.uniq_e;
+        g.uniq_off = gp.uniq_off;
+        g.assign = gp.assign;
+        g.A = A;
+        g.A_pad = ctx->A_pad;
+        g.k = ctx->k;
+        g.F_out = ctx->F;
+        g.error = ctx->d_error;
+        L.gu = g;
+        L.gu.tile_off = L.tiling.tile_off_gu;
+        L.gu.tbl[0] = ctx->d_tbl + (size_t)(layer * 3 + 0) * ctx->E;
+        L.gu.tbl[1] = ctx->d_tbl + (size_t)(layer * 3 + 1) * ctx->E;
+        L.gu.a_scaleT = ctx->xdT;
+        L.gu.rows = ctx->F;
+        L.gu.K = H;
+        L.gu.hq16 = ctx->hq16;
+        L.gu.hdT = ctx->hdT;
+        L.gu.hq = ctx->hq;
+        L.gu.hds = ctx->hds;
+        L.dn = g;
+        L.dn.tile_off = L.tiling.tile_off_dn;
+        L.dn.tbl[0] = ctx->d_tbl + (size_t)(layer * 3 + 2) * ctx->E;
+        L.dn.tbl[1] = nullptr;
+        L.dn.a_scaleT = ctx->hdT;
+        L.dn.rows = H;
+        L.dn.K = ctx->F;
+        L.dn.o = ctx->o;
+        L.tm_x = ctx->tm_x;
+        L.tm_h = ctx->tm_h;
+        L.xq = ctx->xq;
+        L.xds = ctx->xds;
+        L.xs16 = ctx->xs16;
+        L.xdT = ctx->xdT;
+        L.w = d_w;
+        L.y = d_y;
+        L.T = T;
+        L.k = ctx->k;
+        L.H = H;
+        L.n_sm = ctx->n_sm;
+        rc = moe::launch_prefill(L, st);
+        if (rc) return fail(ctx, MOE_ERR_CUDA, std::string("prefill launch: ") + cudaGetErrorString((cudaError_t)rc));
+        ctx->last_T = T;
+        return MOE_OK;
+    }
     int max_gu = U * (ctx->F / 32), max_dn = U * ctx->n_counters;
     const cudaEvent_t *ev = nullptr;
     if (ctx->timing) {
@@ -706,6 +821,11 @@ void moe_destroy(moe_ctx *ctx) {
     cudaFree(ctx->o);
     cudaFree(ctx->counters);
     cudaFree(ctx->d_upd);
+    cudaFree(ctx->xs16);
+    cudaFree(ctx->xdT);
+    cudaFree(ctx->hq16);
+    cudaFree(ctx->hdT);
+    cudaFree(ctx->tile_off);
     if (ctx->h_readback) cudaFreeHost(ctx->h_readback);
     if (ctx->h_stamps) cudaFreeHost(ctx->h_stamps);
     if (ctx->h_upd) cudaFreeHost(ctx->h_upd);
