@@ -89,6 +89,9 @@ class Model:
                                  capacity=[capacity] * L if isinstance(capacity, int) else list(capacity))
         self.H, self.F, self.E, self.k, self.L = H, F, E, k, L
         self.spt = slots_per_tensor if slots_per_tensor is not None else max(self.wl.capacity)
+        # one stream for torch's copies / allocations and the library's kernels
+        if stream is None:
+            stream = torch.cuda.current_stream().cuda_stream
         self.ctx = qec.moe_layer_init(H, F, E, k, L, self.spt, max_tokens, window_tokens=window,
                                       max_swaps_per_step=max_swaps, stream=stream)
         self.tensors = {}

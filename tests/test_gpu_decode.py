@@ -22,7 +22,7 @@ def _gpu():
 
 
 def _ctx(E, k, H=256, F=256, L=1, spt=0, M=512):
-    return qec.moe_layer_init(H, F, E, k, L, spt, M)
+    return qec.moe_layer_init(H, F, E, k, L, spt, M, stream=torch.cuda.current_stream().cuda_stream)
 
 
 @pytest.mark.parametrize("E,k,T", [(8, 2, 4), (512, 8, 37), (128, 4, 300), (4096, 8, 5), (64, 32, 9), (1000, 3, 17)])
