@@ -15,8 +15,8 @@ quantize h, down mat-vec + combine), then the promotion pass (cache_step).
 Prints one JSON line (rank 0).  `value` is whole-job tokens/s with inputs
 resident in HBM; `e2e` is the same through the C ABI with the step's inputs
 copied from pinned host memory and its outputs copied back inside the timed
-region; `roofline` is for the gate/up mat-vec (the dominant kernel) over the
-fully resident layers; `cpu_baseline` is the CPU oracle on a bounded sample.
+region; `roofline` is for the fused expert-FFN layer kernel (the dominant
+kernel) over the fully resident layers; `cpu_baseline` is the CPU oracle on a bounded sample.
 """
 from __future__ import annotations
 
@@ -298,7 +298,8 @@ def run_ours(args):
     e2e_tok = world * args.steps * T / e2e_s
     log(f"e2e: {e2e_tok:.1f} tokens/s")
 
-    # roofline of the gate/up mat-vec over the fully resident layers: CUDA
+    # roofline of the fused expert-FFN layer kernel (gate/up + SwiGLU + down +
+    # combine, one launch per layer) over the fully resident layers: CUDA
     # events on the context stream around each launch, in a pass of eager
     # steps after the timed one (event nodes inside a graph do not bracket
     # kernel execution)
@@ -315,13 +316,13 @@ def run_ours(args):
         for j, l in enumerate(resident):
             gu_ms += g_ms[l]
             dn_ms += d_ms[l]
-            gu_bytes += uniq[j] * 2 * blob + T * H + T * k * F
-            dn_bytes += uniq[j] * blob + T * k * F + T * H * 4
+            # weights of the used experts (3 tensors) + x (fp32) + y (fp32)
+            gu_bytes += uniq[j] * 3 * blob + T * H * 4 + T * H * 4
             n_launch += 1
     qec.moe_debug_timing(ctx, False)
     peaks, peak_src = load_peaks()
     achieved = gu_bytes / (gu_ms / 1e3) / 1e9
-    traffic = read_traffic("gate_up_gemv_decode_b1.txt", "bench.traffic_bytes_per_launch")
+    traffic = read_traffic("decode_layer_kernel_decode_b1.txt", "bench.traffic_bytes_per_launch")
 
     # bytes of the whole step (weights of the unique experts of every layer)
     step_bytes = 0
@@ -343,12 +344,12 @@ def run_ours(args):
                                f"{min(wl.layer_capacity(l) for l in range(L))}/{E} hot set on the rest",
                    "l2": "inputs larger than L2: ~1.5 GB of expert weights per step vs 129 MB L2",
                    "cuda_graph": graph is not None, "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "hbm", "kernel": "gate_up_gemv (resident layers)", "achieved": round(achieved, 1),
+        "roofline": {"bound": "hbm", "kernel": "decode_layer_kernel (fused expert FFN, resident layers)",
+                     "achieved": round(achieved, 1),
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                      "peak_source": f"{peak_src} hbm_gbs (copy)", "traffic": traffic,
                      "algorithmic_bytes_per_launch": round(gu_bytes / max(1, n_launch)),
-                     "avg_launch_us": round(1e3 * gu_ms / max(1, n_launch), 3),
-                     "down_gemv_gbs": round(dn_bytes / (dn_ms / 1e3) / 1e9, 1)},
+                     "avg_launch_us": round(1e3 * gu_ms / max(1, n_launch), 3)},
         "step_weight_gbs": round(step_bytes / (ms_max / args.steps / 1e3) / 1e9, 1),
         "host_link": {"zero_copy_read_gbs": round(zc_gbs, 1), "copy_engine_h2d_gbs": round(ce_gbs, 1)},
         "cache": {"hits": st_main["hits"], "misses": st_main["misses"], "admissions": st_main["admissions"],

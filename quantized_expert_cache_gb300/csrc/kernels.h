@@ -37,6 +37,18 @@ struct GemvParams {
     unsigned *counters;   // [H / rows per down item], zero between launches
     const float *w;       // [T][k]
     float *y;             // [T][H]
+    int8_t *xq_out;       // fused path: [T][H] copy of the quantized x
+    BlockScale *xds_out;  // fused path: [T][H/32]
+};
+
+// Fused small-batch layer (cooperative launch).
+struct FusedParams {
+    GemvParams g;
+    const float *x;          // [T][H]
+    const int32_t *idx;      // [T][k]
+    unsigned *done_gu;       // [E]: published gate/up row blocks per expert, zero between launches
+    unsigned *exit_count;    // [1]
+    int *error;
 };
 
 // One grouped GEMM launch (gate/up with SwiGLU + h quantization, or down).
@@ -89,6 +101,9 @@ int down_rows_per_item(int F);
 int launch_block_dots(const uint8_t *blob, int rows, int nb, int row0, int n_rows, const int8_t *qa, int32_t *out,
                       cudaStream_t st);
 int launch_stream_read(const void *src, size_t bytes, uint32_t *sink, int n_sm, cudaStream_t st);
+size_t fused_smem_bytes(int H, int F);
+int fused_configure(int F, size_t smem, int *blocks_per_sm);
+int launch_fused(const FusedParams &p, int grid, size_t smem, cudaStream_t st, cudaEvent_t const *ev);
 int launch_prefill(const PrefillLaunch &L, cudaStream_t st);
 int gemm_configure();
 int gemm_bn(bool dual);

@@ -16,6 +16,16 @@
 
 namespace moe {
 
+static void record(cudaEvent_t e, cudaStream_t st) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaStreamIsCapturing(st, &cs);
+    if (cs == cudaStreamCaptureStatusActive)
+        cudaEventRecordWithFlags(e, st, cudaEventRecordExternal);
+    else
+        cudaEventRecord(e, st);
+}
+
+
 // --------------------------------------------------------------- top-k
 // One warp per token; lane l holds logits l, l+32, ... (V per lane).  k
 // rounds of a warp arg-max over (value desc, index asc).
@@ -437,15 +447,6 @@ int down_rows_per_item(int F) {
 }
 
 // ev (optional): 4 events recorded around the gate/up and the down launch.
-static void record(cudaEvent_t e, cudaStream_t st) {
-    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-    cudaStreamIsCapturing(st, &cs);
-    if (cs == cudaStreamCaptureStatusActive)
-        cudaEventRecordWithFlags(e, st, cudaEventRecordExternal);
-    else
-        cudaEventRecord(e, st);
-}
-
 int launch_gemv(const GemvParams &p, int grid_gu, int grid_dn, cudaStream_t st, cudaEvent_t const *ev) {
     if (ev) record(ev[0], st);
     gate_up_kernel<<<grid_gu, 256, 0, st>>>(p);
@@ -458,6 +459,394 @@ int launch_gemv(const GemvParams &p, int grid_gu, int grid_dn, cudaStream_t st, 
         down_kernel<8><<<grid_dn, 256, 0, st>>>(p);
     if (ev) record(ev[3], st);
     return (int)cudaGetLastError();
+}
+
+// --------------------------------------------------------------- fused layer
+// One cooperative launch per layer for small batches (T*k <= kMaxFusedA).
+// Every CTA derives the same plan from idx in shared memory (used experts
+// ascending, assignments grouped by expert).  Gate/up items (used expert,
+// 32 rows of F) issue all their weight loads first, quantize the x of their
+// tokens into shared memory while the loads are in flight, then compute
+// SwiGLU and quantize h, and publish completion per expert.  Down items
+// (used expert, ROWS rows of H) issue their weight loads, then wait (bounded)
+// until every gate/up row block of their expert is published, read h and
+// write o; the last item of a row block sums y in j order.  Gate/up items
+// never wait, and a cooperative launch keeps every CTA resident, so each wait
+// ends; an expired wait sets an error bit and the item is skipped.
+constexpr int kMaxFusedA = 256;
+constexpr int kGURounds = 8;  // 128-bit loads per lane and tensor issued together
+
+__device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ void fused_plan(const FusedParams &p, int *s_e, int *s_uniq, int *s_off, int *s_asg, int *s_nu,
+                           int *s_cnt, int *s_first) {
+    const int A = p.g.n_tokens * p.g.k;
+    for (int a = threadIdx.x; a < A; a += blockDim.x) {
+        int e = p.idx[a];
+        if (e < 0 || e >= p.g.cv.E) {
+            atomicOr(p.error, 1);
+            e = 0;
+        }
+        s_e[a] = e;
+    }
+    __syncthreads();
+    int n_first = 0;
+    for (int a = threadIdx.x; a < A; a += blockDim.x) {
+        const int e = s_e[a];
+        int first = 1;
+        for (int b = 0; b < a; ++b)
+            if (s_e[b] == e) {
+                first = 0;
+                break;
+            }
+        s_first[a] = first;
+        n_first += first;
+    }
+    (void)n_first;
+    __syncthreads();
+    // rank of each first occurrence among the distinct experts, and its count
+    for (int a = threadIdx.x; a < A; a += blockDim.x) {
+        if (!s_first[a]) continue;
+        const int e = s_e[a];
+        int smaller = 0, cnt = 0;
+        for (int b = 0; b < A; ++b) {
+            const int eb = s_e[b];
+            cnt += eb == e;
+            smaller += (eb < e) && s_first[b];
+        }
+        s_uniq[smaller] = e;
+        s_cnt[smaller] = cnt;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int n = 0, off = 0;
+        for (int a = 0; a < A; ++a) n += s_first[a];
+        for (int u = 0; u < n; ++u) {
+            s_off[u] = off;
+            off += s_cnt[u];
+        }
+        s_off[n] = off;
+        *s_nu = n;
+    }
+    __syncthreads();
+    // assignments grouped by expert, ascending assignment id within an expert
+    for (int a = threadIdx.x; a < A; a += blockDim.x) {
+        const int e = s_e[a];
+        int lo = 0, hi = *s_nu - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (s_uniq[mid] < e)
+                lo = mid + 1;
+            else
+                hi = mid;
+        }
+        int before = 0;
+        for (int b = 0; b < a; ++b) before += s_e[b] == e;
+        s_asg[s_off[lo] + before] = a;
+    }
+    __syncthreads();
+}
+
+template <int LD>
+__global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
+    __shared__ int s_e[kMaxFusedA], s_uniq[kMaxFusedA], s_off[kMaxFusedA + 1], s_asg[kMaxFusedA],
+        s_cnt[kMaxFusedA], s_first[kMaxFusedA];
+    __shared__ int s_nu, s_last;
+    __shared__ float sh_h[kMaxChunk][32];
+    extern __shared__ __align__(16) uint8_t dsm[];
+    const GemvParams &g = p.g;
+    const int H = g.H, F = g.F, k = g.k;
+    const int nbx = H / kBlock, nbf = F / kBlock, rgs = F / kBlock;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t step_clock = *g.cv.clock + (uint32_t)g.n_tokens;
+
+    fused_plan(p, s_e, s_uniq, s_off, s_asg, &s_nu, s_cnt, s_first);
+    const int nu = s_nu;
+
+    // ---------------- gate/up items
+    {
+        int8_t *xq_s = (int8_t *)dsm;                                     // [chunk][H]
+        BlockScale *xds_s = (BlockScale *)(dsm + kMaxChunk * H);          // [chunk][nbx]
+        const int sub = lane % kGULanes, grp = lane / kGULanes;
+        const int rloc = warp * (32 / kGULanes) + grp;
+        const size_t scale_off = blob_scales_offset(F, nbx);
+        const int n_items = nu * rgs;
+        for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+            const int u = item / rgs, rg = item - u * rgs;
+            const int e = s_uniq[u];
+            const int a0 = s_off[u], a1 = s_off[u + 1];
+            const uint64_t eg = g.cv.tbl[(size_t)g.tid_gate * g.cv.E + e];
+            const uint64_t eu = g.cv.tbl[(size_t)g.tid_up * g.cv.E + e];
+            if (rg == 0 && threadIdx.x == 0) {
+                record_read(g.cv, g.tid_gate, e, eg, step_clock);
+                record_read(g.cv, g.tid_up, e, eu, step_clock);
+            }
+            const uint8_t *bg = (const uint8_t *)(uintptr_t)(eg & ~1ull);
+            const uint8_t *bu = (const uint8_t *)(uintptr_t)(eu & ~1ull);
+            const int r = rg * 32 + rloc;
+            const uint4 *qg = (const uint4 *)bg + (size_t)r * nbx;
+            const uint4 *qu = (const uint4 *)bu + (size_t)r * nbx;
+            const __half *dg = (const __half *)(bg + scale_off) + (size_t)r * nbx;
+            const __half *du = (const __half *)(bu + scale_off) + (size_t)r * nbx;
+            for (int c0 = a0; c0 < a1; c0 += kMaxChunk) {
+                const int nt = min(kMaxChunk, a1 - c0);
+                float ag[kMaxChunk], au[kMaxChunk];
+#pragma unroll
+                for (int t = 0; t < kMaxChunk; ++t) ag[t] = au[t] = 0.0f;
+                for (int bb = 0; bb * kGULanes * kGURounds < nbx; ++bb) {
+                    uint4 wg4[kGURounds], wu4[kGURounds];
+                    float sg[kGURounds], su[kGURounds];
+#pragma unroll
+                    for (int i = 0; i < kGURounds; ++i) {
+                        const int b = sub + kGULanes * (bb * kGURounds + i);
+                        if (b < nbx) {
+                            wg4[i] = ld_weights(qg + b);
+                            wu4[i] = ld_weights(qu + b);
+                            sg[i] = ld_scale(dg + b);
+                            su[i] = ld_scale(du + b);
+                        }
+                    }
+                    if (bb == 0) {
+                        // quantize the x rows of this chunk while the loads fly
+                        const int nblk = nt * nbx;
+                        for (int q = warp; q < nblk; q += kWarps) {
+                            const int t = q / nbx, b = q - t * nbx;
+                            const int a = s_asg[c0 + t];
+                            const int tok = a / k;
+                            quantize_block_warp(p.x[(size_t)tok * H + (size_t)b * kBlock + lane], lane,
+                                                xq_s + (size_t)t * H + (size_t)b * kBlock, xds_s + (size_t)t * nbx + b);
+                            if (rg == 0 && (a % k) == 0) {
+                                __syncwarp();
+                                g.xq_out[(size_t)tok * H + (size_t)b * kBlock + lane] =
+                                    xq_s[(size_t)t * H + (size_t)b * kBlock + lane];
+                                if (lane == 0) g.xds_out[(size_t)tok * nbx + b] = xds_s[(size_t)t * nbx + b];
+                            }
+                        }
+                        __syncthreads();
+                    }
+#pragma unroll
+                    for (int i = 0; i < kGURounds; ++i) {
+                        const int b = sub + kGULanes * (bb * kGURounds + i);
+                        if (b < nbx) {
+#pragma unroll
+                            for (int t = 0; t < kMaxChunk; ++t) {
+                                if (t < nt) {
+                                    const int4 *xa = (const int4 *)(xq_s + (size_t)t * H + (size_t)b * kBlock);
+                                    const int4 x0 = xa[0], x1 = xa[1];
+                                    const BlockScale xs = xds_s[(size_t)t * nbx + b];
+                                    ag[t] += (float)q4_block_dot(wg4[i], x0, x1, xs.s) * (sg[i] * xs.d);
+                                    au[t] += (float)q4_block_dot(wu4[i], x0, x1, xs.s) * (su[i] * xs.d);
+                                }
+                            }
+                        }
+                    }
+                }
+#pragma unroll
+                for (int t = 0; t < kMaxChunk; ++t) {
+#pragma unroll
+                    for (int o = kGULanes / 2; o > 0; o >>= 1) {
+                        ag[t] += __shfl_xor_sync(0xffffffffu, ag[t], o);
+                        au[t] += __shfl_xor_sync(0xffffffffu, au[t], o);
+                    }
+                }
+                if (sub == 0) {
+#pragma unroll
+                    for (int t = 0; t < kMaxChunk; ++t)
+                        if (t < nt) sh_h[t][rloc] = ag[t] * au[t] / (1.0f + expf(-ag[t]));
+                }
+                __syncthreads();
+                if (warp < nt) {
+                    const int a = s_asg[c0 + warp];
+                    quantize_block_warp(sh_h[warp][lane], lane, g.hq + (size_t)a * F + (size_t)rg * kBlock,
+                                        g.hds + (size_t)a * rgs + rg);
+                }
+                __syncthreads();
+            }
+            // publish this row block of expert e
+            __threadfence();
+            __syncthreads();
+            if (threadIdx.x == 0) atomicAdd(&p.done_gu[e], 1u);
+        }
+    }
+
+    // ---------------- down items
+    {
+        constexpr int G = 32 / LD, ROWS = kWarps * G;
+        constexpr int RD = 12;  // loads per lane issued together (<= 12 rounds)
+        int8_t *hq_s = (int8_t *)dsm;                                   // [chunk][F]
+        BlockScale *hds_s = (BlockScale *)(dsm + kMaxChunk * F);        // [chunk][nbf]
+        const int sub = lane % LD, grp = lane / LD;
+        const int rloc = warp * G + grp;
+        const int n_rb = H / ROWS;
+        const size_t scale_off = blob_scales_offset(H, nbf);
+        const int n_items = nu * n_rb;
+        for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+            const int u = item / n_rb, rb = item - u * n_rb;
+            const int e = s_uniq[u];
+            const int a0 = s_off[u], a1 = s_off[u + 1];
+            const uint64_t ed = g.cv.tbl[(size_t)g.tid_down * g.cv.E + e];
+            if (rb == 0 && threadIdx.x == 0) record_read(g.cv, g.tid_down, e, ed, step_clock);
+            const uint8_t *bd = (const uint8_t *)(uintptr_t)(ed & ~1ull);
+            const int r = rb * ROWS + rloc;
+            const uint4 *qd = (const uint4 *)bd + (size_t)r * nbf;
+            const __half *dd = (const __half *)(bd + scale_off) + (size_t)r * nbf;
+            bool waited = false;
+            for (int c0 = a0; c0 < a1; c0 += kMaxChunk) {
+                const int nt = min(kMaxChunk, a1 - c0);
+                float acc[kMaxChunk];
+#pragma unroll
+                for (int t = 0; t < kMaxChunk; ++t) acc[t] = 0.0f;
+                for (int bb = 0; bb * LD * RD < nbf; ++bb) {
+                    uint4 w4[RD];
+                    float sw[RD];
+#pragma unroll
+                    for (int i = 0; i < RD; ++i) {
+                        const int b = sub + LD * (bb * RD + i);
+                        if (b < nbf) {
+                            w4[i] = ld_weights(qd + b);
+                            sw[i] = ld_scale(dd + b);
+                        }
+                    }
+                    if (bb == 0) {
+                        if (!waited) {
+                            // wait (bounded) for all gate/up row blocks of expert e
+                            if (threadIdx.x == 0) {
+                                const long long t0 = clock64();
+                                while (ld_acquire(&p.done_gu[e]) < (unsigned)rgs) {
+                                    if (clock64() - t0 > 4000000000ll) {
+                                        atomicOr(p.error, 2);
+                                        break;
+                                    }
+                                    __nanosleep(64);
+                                }
+                            }
+                            __syncthreads();
+                            waited = true;
+                        }
+                        // stage the chunk's h codes and scales
+                        for (int i = threadIdx.x; i < nt * (F / 16); i += blockDim.x) {
+                            const int t = i / (F / 16), c = i - t * (F / 16);
+                            const int a = s_asg[c0 + t];
+                            reinterpret_cast<int4 *>(hq_s + (size_t)t * F)[c] =
+                                __ldcg(reinterpret_cast<const int4 *>(g.hq + (size_t)a * F) + c);
+                        }
+                        for (int i = threadIdx.x; i < nt * nbf; i += blockDim.x) {
+                            const int t = i / nbf, c = i - t * nbf;
+                            const int a = s_asg[c0 + t];
+                            const int2 v = __ldcg(reinterpret_cast<const int2 *>(g.hds + (size_t)a * nbf + c));
+                            hds_s[(size_t)t * nbf + c] = BlockScale{__int_as_float(v.x), v.y};
+                        }
+                        __syncthreads();
+                    }
+#pragma unroll
+                    for (int i = 0; i < RD; ++i) {
+                        const int b = sub + LD * (bb * RD + i);
+                        if (b < nbf) {
+#pragma unroll
+                            for (int t = 0; t < kMaxChunk; ++t) {
+                                if (t < nt) {
+                                    const int4 *ha = (const int4 *)(hq_s + (size_t)t * F + (size_t)b * kBlock);
+                                    const BlockScale hs = hds_s[(size_t)t * nbf + b];
+                                    acc[t] += (float)q4_block_dot(w4[i], ha[0], ha[1], hs.s) * (sw[i] * hs.d);
+                                }
+                            }
+                        }
+                    }
+                }
+#pragma unroll
+                for (int t = 0; t < kMaxChunk; ++t) {
+#pragma unroll
+                    for (int o = LD / 2; o > 0; o >>= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], o);
+                }
+                if (sub == 0) {
+#pragma unroll
+                    for (int t = 0; t < kMaxChunk; ++t)
+                        if (t < nt) g.o[(size_t)s_asg[c0 + t] * H + r] = acc[t];
+                }
+                __syncthreads();
+            }
+            // arrival count of this row block; the last item combines
+            __threadfence();
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                const unsigned prev = atomicAdd(&g.counters[rb], 1u);
+                s_last = (prev == (unsigned)(nu - 1));
+            }
+            __syncthreads();
+            if (s_last) {
+                __threadfence();
+                const int n_out = g.n_tokens * ROWS;
+                for (int i = threadIdx.x; i < n_out; i += blockDim.x) {
+                    const int t = i / ROWS, rr = rb * ROWS + (i - t * ROWS);
+                    float y = 0.0f;
+                    for (int j = 0; j < k; ++j) {
+                        const size_t a = (size_t)t * k + j;
+                        y += g.w[a] * __ldcg(g.o + a * H + rr);
+                    }
+                    g.y[(size_t)t * H + rr] = y;
+                }
+                if (threadIdx.x == 0) g.counters[rb] = 0u;
+            }
+            __syncthreads();
+        }
+    }
+
+    // ---------------- the last CTA to leave resets the per-expert counters
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const unsigned prev = atomicAdd(p.exit_count, 1u);
+        if (prev == gridDim.x - 1) {
+            for (int u = 0; u < nu; ++u) p.done_gu[s_uniq[u]] = 0u;
+            *p.exit_count = 0u;
+            __threadfence();
+        }
+    }
+}
+
+size_t fused_smem_bytes(int H, int F) {
+    const size_t gu = (size_t)kMaxChunk * H + (size_t)kMaxChunk * (H / kBlock) * sizeof(BlockScale);
+    const size_t dn = (size_t)kMaxChunk * F + (size_t)kMaxChunk * (F / kBlock) * sizeof(BlockScale);
+    return gu > dn ? gu : dn;
+}
+
+int fused_down_lanes(int F) { return F / kBlock <= 40 ? 4 : 8; }
+
+int fused_configure(int F, size_t smem, int *blocks_per_sm) {
+    const void *fn = fused_down_lanes(F) == 4 ? (const void *)decode_layer_kernel<4> : (const void *)decode_layer_kernel<8>;
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return (int)e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, fn, 256, smem);
+    return (int)e;
+}
+
+int launch_fused(const FusedParams &p, int grid, size_t smem, cudaStream_t st, cudaEvent_t const *ev) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (ev) record(ev[0], st);
+    cudaError_t e;
+    if (fused_down_lanes(p.g.F) == 4)
+        e = cudaLaunchKernelEx(&cfg, decode_layer_kernel<4>, p);
+    else
+        e = cudaLaunchKernelEx(&cfg, decode_layer_kernel<8>, p);
+    if (ev) {
+        record(ev[1], st);
+        record(ev[2], st);
+        record(ev[3], st);
+    }
+    return (int)e;
 }
 
 // --------------------------------------------------------------- hooks

@@ -72,6 +72,10 @@ struct moe_ctx {
     float *xdT = nullptr, *hdT = nullptr;
     int32_t *tile_off = nullptr;  // [2][U + 1]
     CUtensorMap tm_x{}, tm_h{};
+    // fused small-batch layer kernel
+    unsigned *done_gu = nullptr, *exit_count = nullptr;
+    size_t fused_smem = 0;
+    int fused_blocks = 0;
 
     uint32_t *h_readback = nullptr;  // pinned: count + miss list
     uint32_t *h_stamps = nullptr;    // pinned
@@ -330,6 +334,16 @@ int moe_layer_init(const moe_cfg *cfg, void *cuda_stream, moe_ctx **out) {
         ctx->gemm_ok = true;
     }
 
+    CKI(cudaMalloc(&ctx->done_gu, sizeof(unsigned) * (E + 1)));
+    CKI(cudaMemset(ctx->done_gu, 0, sizeof(unsigned) * (E + 1)));
+    ctx->exit_count = ctx->done_gu + E;
+    ctx->fused_smem = moe::fused_smem_bytes(ctx->H, ctx->F);
+    {
+        int bps = 0;
+        CKI((cudaError_t)moe::fused_configure(ctx->F, ctx->fused_smem, &bps));
+        ctx->fused_blocks = bps * ctx->n_sm;
+    }
+
     CKI(cudaHostAlloc(&ctx->h_readback, sizeof(uint32_t) * (1 + (size_t)ctx->miss_cap), cudaHostAllocDefault));
     CKI(cudaHostAlloc(&ctx->h_stamps, sizeof(uint32_t) * (size_t)nt * std::max(1, ctx->spt), cudaHostAllocDefault));
     ctx->upd_cap = 6 * nt * E + 64;
@@ -434,26 +448,6 @@ int moe_ffn_forward(moe_ctx *ctx, int layer, const float *d_x, int n_tokens, con
     const int T = n_tokens, H = ctx->H;
     const bool small = T <= 32;
     int rc = 0;
-    if (!small) rc = moe::launch_quantize(d_x, T * (H / 32), ctx->xq, ctx->xds, ctx->n_sm, st);
-    if (rc) return fail(ctx, MOE_ERR_CUDA, "quantize launch failed");
-    moe::PlanParams pp{};
-    pp.x = d_x;
-    pp.xq = ctx->xq;
-    pp.xds = ctx->xds;
-    pp.idx = d_idx;
-    pp.n_uniq = p_n_uniq(ctx);
-    pp.uniq_e = p_uniq_e(ctx);
-    pp.uniq_off = p_uniq_off(ctx);
-    pp.assign = p_assign(ctx);
-    pp.error = ctx->d_error;
-    pp.T = T;
-    pp.k = ctx->k;
-    pp.E = ctx->E;
-    pp.H = H;
-    pp.quantize_x = small ? 1 : 0;
-    rc = moe::launch_plan(pp, st);
-    if (rc) return fail(ctx, MOE_ERR_CUDA, std::string("plan launch: ") + cudaGetErrorString((cudaError_t)rc));
-
     moe::GemvParams gp{};
     gp.cv.tbl = ctx->d_tbl;
     gp.cv.slot = ctx->d_slot;
@@ -487,6 +481,48 @@ int moe_ffn_forward(moe_ctx *ctx, int layer, const float *d_x, int n_tokens, con
     gp.w = d_w;
     gp.y = d_y;
     const int A = T * ctx->k, U = std::min(A, ctx->E);
+    gp.xq_out = ctx->xq;
+    gp.xds_out = ctx->xds;
+    if (small && A <= 256 && ctx->fused_blocks > 0) {
+        moe::FusedParams fp{};
+        fp.g = gp;
+        fp.x = d_x;
+        fp.idx = d_idx;
+        fp.done_gu = ctx->done_gu;
+        fp.exit_count = ctx->exit_count;
+        fp.error = ctx->d_error;
+        const int items = U * std::max(ctx->F / 32, ctx->n_counters);
+        const int grid = std::min(items, ctx->fused_blocks);
+        const cudaEvent_t *ev = nullptr;
+        if (ctx->timing) {
+            ev = ctx->tev.data() + 4 * (size_t)layer;
+            ctx->tev_used[layer] = 1;
+        }
+        rc = moe::launch_fused(fp, grid, ctx->fused_smem, st, ev);
+        if (rc) return fail(ctx, MOE_ERR_CUDA, std::string("fused launch: ") + cudaGetErrorString((cudaError_t)rc));
+        ctx->last_T = T;
+        return MOE_OK;
+    }
+    if (!small) rc = moe::launch_quantize(d_x, T * (H / 32), ctx->xq, ctx->xds, ctx->n_sm, st);
+    if (rc) return fail(ctx, MOE_ERR_CUDA, "quantize launch failed");
+    moe::PlanParams pp{};
+    pp.x = d_x;
+    pp.xq = ctx->xq;
+    pp.xds = ctx->xds;
+    pp.idx = d_idx;
+    pp.n_uniq = p_n_uniq(ctx);
+    pp.uniq_e = p_uniq_e(ctx);
+    pp.uniq_off = p_uniq_off(ctx);
+    pp.assign = p_assign(ctx);
+    pp.error = ctx->d_error;
+    pp.T = T;
+    pp.k = ctx->k;
+    pp.E = ctx->E;
+    pp.H = H;
+    pp.quantize_x = small ? 1 : 0;
+    rc = moe::launch_plan(pp, st);
+    if (rc) return fail(ctx, MOE_ERR_CUDA, std::string("plan launch: ") + cudaGetErrorString((cudaError_t)rc));
+
     if (!small && ctx->gemm_ok) {
         // prefill: grouped tensor-core GEMM over tokens sorted by expert
         const int Umax = std::min(ctx->M * ctx->k, ctx->E);
@@ -826,6 +862,7 @@ void moe_destroy(moe_ctx *ctx) {
     cudaFree(ctx->hq16);
     cudaFree(ctx->hdT);
     cudaFree(ctx->tile_off);
+    cudaFree(ctx->done_gu);
     if (ctx->h_readback) cudaFreeHost(ctx->h_readback);
     if (ctx->h_stamps) cudaFreeHost(ctx->h_stamps);
     if (ctx->h_upd) cudaFreeHost(ctx->h_upd);
