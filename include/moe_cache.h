@@ -7,8 +7,8 @@
  * exception crosses this boundary.  A context is not thread-safe: calls on
  * one context must not overlap.  Device pointers are CUDA device addresses
  * (or unified addresses) on the context's device; host pointers are plain
- * process memory.  Streams are cudaStream_t passed as void*; NULL means the
- * context's own stream.
+ * process memory.  Streams are cudaStream_t passed as void*; in route_topk
+ * and moe_ffn_forward NULL means the context's stream.
  *
  * Data formats
  *   Q4 block (canonical, 18 bytes): binary16 scale d (little endian), then
@@ -83,9 +83,9 @@ typedef struct moe_stats_t {
 } moe_stats_t;
 
 /*
- * Create a context on cfg->device.  cuda_stream (cudaStream_t, may be NULL
- * for a new non-blocking stream owned by the context) is the stream every
- * forward of this context runs on.  The library allocates and owns: the HBM
+ * Create a context on cfg->device.  cuda_stream (cudaStream_t; NULL is the
+ * legacy default stream, as everywhere in CUDA) is the stream every forward
+ * of this context runs on; the caller keeps owning it.  The library allocates and owns: the HBM
  * expert pool (3*L*slots_per_tensor slots of rows*cols/32*18 bytes), the
  * pointer tables, stamps, miss log, workspaces, an upload stream and the
  * pinned host copies of registered tensors.  *out receives the context.

@@ -47,7 +47,6 @@ struct moe_ctx {
     int n_tensors = 0, E = 0, spt = 0, H = 0, F = 0, k = 0, M = 0;
     size_t blob = 0, stride = 0;
     cudaStream_t stream = nullptr, up = nullptr;
-    bool own_stream = false;
     cudaEvent_t ev_fwd = nullptr, ev_up = nullptr;
 
     uint8_t *arena = nullptr;
@@ -271,12 +270,7 @@ int moe_layer_init(const moe_cfg *cfg, void *cuda_stream, moe_ctx **out) {
     } while (0)
     CKI(cudaSetDevice(ctx->dev));
     CKI(cudaDeviceGetAttribute(&ctx->n_sm, cudaDevAttrMultiProcessorCount, ctx->dev));
-    if (cuda_stream) {
-        ctx->stream = (cudaStream_t)cuda_stream;
-    } else {
-        CKI(cudaStreamCreateWithFlags(&ctx->stream, cudaStreamNonBlocking));
-        ctx->own_stream = true;
-    }
+    ctx->stream = (cudaStream_t)cuda_stream;  // NULL: the legacy default stream
     CKI(cudaStreamCreateWithFlags(&ctx->up, cudaStreamNonBlocking));
     CKI(cudaEventCreateWithFlags(&ctx->ev_fwd, cudaEventDisableTiming));
     CKI(cudaEventCreateWithFlags(&ctx->ev_up, cudaEventDisableTiming));
@@ -836,7 +830,7 @@ const char *moe_last_error(moe_ctx *ctx) { return ctx ? ctx->err.c_str() : g_ini
 void moe_destroy(moe_ctx *ctx) {
     if (!ctx) return;
     cudaSetDevice(ctx->dev);
-    if (ctx->stream) cudaStreamSynchronize(ctx->stream);
+    cudaStreamSynchronize(ctx->stream);
     if (ctx->up) cudaStreamSynchronize(ctx->up);
     for (auto &ts : ctx->t)
         if (ts.home) cudaFreeHost(ts.home);
@@ -870,7 +864,6 @@ void moe_destroy(moe_ctx *ctx) {
     if (ctx->ev_fwd) cudaEventDestroy(ctx->ev_fwd);
     if (ctx->ev_up) cudaEventDestroy(ctx->ev_up);
     if (ctx->up) cudaStreamDestroy(ctx->up);
-    if (ctx->own_stream && ctx->stream) cudaStreamDestroy(ctx->stream);
     delete ctx;
 }
 
