@@ -207,8 +207,9 @@ int moe_cache_layout(moe_ctx *ctx, int tensor_id, uint64_t *pool_base, uint64_t 
 
 int moe_stats(moe_ctx *ctx, moe_stats_t *out);
 
-/* Message of the last error on ctx (or of the last failed moe_layer_init
- * when ctx is NULL).  Valid until the next call on ctx. */
+/* Message of the last error on ctx (or, when ctx is NULL, of the last failed
+ * call that takes no context: moe_layer_init, moe_probe_host_read,
+ * moe_expert_ffn_noalloc).  Valid until the next such call. */
 const char *moe_last_error(moe_ctx *ctx);
 
 /* Release everything the context owns.  Synchronizes first. */
@@ -262,6 +263,36 @@ int moe_debug_fail_upload(moe_ctx *ctx, int nth);
  */
 int moe_debug_timing(moe_ctx *ctx, int enable);
 int moe_debug_timing_read(moe_ctx *ctx, double *gate_up_ms, double *down_ms);
+
+/*
+ * One routed-expert FFN layer that allocates nothing (no counterpart on the
+ * source pages: this entry point exists for callers that cannot allocate
+ * device memory when they run a layer, such as code running while a CUDA
+ * graph is captured in a mode that forbids allocation, or processes whose
+ * device memory is entirely reserved by another allocator).  It computes what
+ * moe_ffn_forward computes for a small batch, with the caller's expert tables
+ * instead of a context: d_tbl holds 3 rows of n_experts uint64 entries
+ * (gate, up, down), each the device address of one expert blob in the plane
+ * layout the library uses (tag bit 0 clear), or of a device-mapped pinned
+ * host copy with bit 0 set, as moe_cache_snapshot reports them.  d_x, d_idx,
+ * d_w, d_y as in moe_ffn_forward; `stream` is any stream (NULL = legacy
+ * default stream).  No miss log, stamp or clock is kept.
+ * Every intermediate lives in one file-scope device array of 8 MiB held by
+ * every GPU that loads the library until the process exits; a call needs
+ * about T*k*(4*H + F + F/4) + T*(H + H/4) bytes plus small tables and is
+ * rejected with MOE_ERR_CAPACITY (message in moe_last_error(NULL)) when that
+ * exceeds 8 MiB.  Limits: n_tokens <= 32, n_tokens*top_k <= 256, hidden a
+ * multiple of the down row block (64 for ffn/32 <= 40, else 32).  The first
+ * call on a device looks up the array's device address and configures the
+ * kernel (make it before any stream capture); later calls on that device
+ * only clear the parts of the array that must start at zero and launch one
+ * kernel.  All calls share the array and each leaves its contents behind, so
+ * calls that overlap on the GPU (other streams, other host threads) race.
+ * Errors: MOE_ERR_ARG, MOE_ERR_CAPACITY, MOE_ERR_CUDA.
+ */
+int moe_expert_ffn_noalloc(const float *d_x, int n_tokens, const int32_t *d_idx, const float *d_w,
+                           const uint64_t *d_tbl, int hidden, int ffn, int n_experts, int top_k, float *d_y,
+                           void *stream);
 
 #ifdef __cplusplus
 }

@@ -65,6 +65,7 @@ SIGNATURES = {
     "moe_debug_fail_upload": (_i32, [_vp, _i32]),
     "moe_debug_timing": (_i32, [_vp, _i32]),
     "moe_debug_timing_read": (_i32, [_vp, _vp, _vp]),
+    "moe_expert_ffn_noalloc": (_i32, [_vp, _i32, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp]),
 }
 
 
@@ -243,3 +244,9 @@ def moe_debug_timing_read(ctx, n_layers):
     dn = np.zeros(n_layers, np.float64)
     _check(ctx, load().moe_debug_timing_read(ctx, _host(gu), _host(dn)))
     return gu, dn
+
+
+def moe_expert_ffn_noalloc(x, n_tokens, idx, w, tbl, hidden, ffn, n_experts, top_k, y, stream=None):
+    """One layer without any device allocation (scratch in a fixed device array)."""
+    return _check(None, load().moe_expert_ffn_noalloc(_dev(x), n_tokens, _dev(idx), _dev(w), _dev(tbl), hidden, ffn,
+                                                      n_experts, top_k, _dev(y), _stream(stream)))

@@ -227,6 +227,10 @@ uint16_t f32_to_half_bits(float v) {
 
 }  // namespace
 
+namespace moe {
+void set_context_free_error(const std::string &msg) { g_init_error = msg; }
+}  // namespace moe
+
 extern "C" {
 
 int moe_layer_init(const moe_cfg *cfg, void *cuda_stream, moe_ctx **out) {
