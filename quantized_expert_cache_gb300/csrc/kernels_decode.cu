@@ -475,11 +475,28 @@ int launch_gemv(const GemvParams &p, int grid_gu, int grid_dn, cudaStream_t st, 
 // ends; an expired wait sets an error bit and the item is skipped.
 constexpr int kMaxFusedA = 256;
 constexpr int kGURounds = 8;  // 128-bit loads per lane and tensor issued together
+constexpr int kXBatch = 8;    // x blocks per warp loaded before they are quantized
+
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gsrc) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(smem_dst)),
+                 "l"(gsrc)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 __device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
     unsigned v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
+}
+
+// Shared staging of x (gate/up) or h (down) codes for one chunk of tokens,
+// rounded up to 16 B; the down prefetch area follows it.
+__host__ __device__ inline size_t fused_stage_bytes(int H, int F) {
+    const size_t gu = (size_t)kMaxChunk * H + (size_t)kMaxChunk * (H / kBlock) * sizeof(BlockScale);
+    const size_t dn = (size_t)kMaxChunk * F + (size_t)kMaxChunk * (F / kBlock) * sizeof(BlockScale);
+    return ((gu > dn ? gu : dn) + 15) / 16 * 16;
 }
 
 __device__ void fused_plan(const FusedParams &p, int *s_e, int *s_uniq, int *s_off, int *s_asg, int *s_nu,
@@ -567,6 +584,29 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
     fused_plan(p, s_e, s_uniq, s_off, s_asg, &s_nu, s_cnt, s_first);
     const int nu = s_nu;
 
+    // Prefetch this CTA's first down item (codes + scales of ROWS rows) into
+    // shared memory with cp.async, so the down weights stream while the
+    // gate/up item runs.
+    constexpr int DG = 32 / LD, DROWS = kWarps * DG;
+    const int n_rb_all = H / DROWS;
+    uint8_t *dpre = dsm + fused_stage_bytes(H, F);
+    const bool prefetched = (int)blockIdx.x < nu * n_rb_all;
+    if (prefetched) {
+        const int u = blockIdx.x / n_rb_all, rb = blockIdx.x - u * n_rb_all;
+        const uint64_t ed = g.cv.tbl[(size_t)g.tid_down * g.cv.E + s_uniq[u]];
+        const uint8_t *bd = (const uint8_t *)(uintptr_t)(ed & ~1ull);
+        const uint8_t *codes = bd + (size_t)rb * DROWS * nbf * 16;
+        const uint8_t *scales = bd + blob_scales_offset(H, nbf) + (size_t)rb * DROWS * nbf * 2;
+        const int nc = DROWS * nbf, ns = DROWS * nbf * 2 / 16;
+        for (int i = threadIdx.x; i < nc + ns; i += blockDim.x) {
+            if (i < nc)
+                cp_async16(dpre + (size_t)i * 16, codes + (size_t)i * 16);
+            else
+                cp_async16(dpre + (size_t)nc * 16 + (size_t)(i - nc) * 16, scales + (size_t)(i - nc) * 16);
+        }
+        cp_async_commit();
+    }
+
     // ---------------- gate/up items
     {
         int8_t *xq_s = (int8_t *)dsm;                                     // [chunk][H]
@@ -611,19 +651,35 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
                         }
                     }
                     if (bb == 0) {
-                        // quantize the x rows of this chunk while the loads fly
+                        // quantize the x rows of this chunk while the loads fly;
+                        // each warp first loads all of its blocks, then reduces
                         const int nblk = nt * nbx;
-                        for (int q = warp; q < nblk; q += kWarps) {
-                            const int t = q / nbx, b = q - t * nbx;
-                            const int a = s_asg[c0 + t];
-                            const int tok = a / k;
-                            quantize_block_warp(p.x[(size_t)tok * H + (size_t)b * kBlock + lane], lane,
-                                                xq_s + (size_t)t * H + (size_t)b * kBlock, xds_s + (size_t)t * nbx + b);
-                            if (rg == 0 && (a % k) == 0) {
-                                __syncwarp();
-                                g.xq_out[(size_t)tok * H + (size_t)b * kBlock + lane] =
-                                    xq_s[(size_t)t * H + (size_t)b * kBlock + lane];
-                                if (lane == 0) g.xds_out[(size_t)tok * nbx + b] = xds_s[(size_t)t * nbx + b];
+                        for (int q0 = warp; q0 < nblk; q0 += kWarps * kXBatch) {
+                            float xv[kXBatch];
+#pragma unroll
+                            for (int i = 0; i < kXBatch; ++i) {
+                                const int q = q0 + i * kWarps;
+                                if (q < nblk) {
+                                    const int t = q / nbx, b = q - t * nbx;
+                                    const int tok = s_asg[c0 + t] / k;
+                                    xv[i] = __ldg(p.x + (size_t)tok * H + (size_t)b * kBlock + lane);
+                                }
+                            }
+#pragma unroll
+                            for (int i = 0; i < kXBatch; ++i) {
+                                const int q = q0 + i * kWarps;
+                                if (q < nblk) {
+                                    const int t = q / nbx, b = q - t * nbx;
+                                    const int a = s_asg[c0 + t];
+                                    const int tok = a / k;
+                                    quantize_block_warp(xv[i], lane, xq_s + (size_t)t * H + (size_t)b * kBlock,
+                                                        xds_s + (size_t)t * nbx + b);
+                                    if (rg == 0 && (a % k) == 0) {
+                                        g.xq_out[(size_t)tok * H + (size_t)b * kBlock + lane] =
+                                            xq_s[(size_t)t * H + (size_t)b * kBlock + lane];
+                                        if (lane == 0) g.xds_out[(size_t)tok * nbx + b] = xds_s[(size_t)t * nbx + b];
+                                    }
+                                }
                             }
                         }
                         __syncthreads();
@@ -700,18 +756,22 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
                 float acc[kMaxChunk];
 #pragma unroll
                 for (int t = 0; t < kMaxChunk; ++t) acc[t] = 0.0f;
+                const bool from_smem = prefetched && item == (int)blockIdx.x;
                 for (int bb = 0; bb * LD * RD < nbf; ++bb) {
                     uint4 w4[RD];
                     float sw[RD];
+                    if (!from_smem) {
 #pragma unroll
-                    for (int i = 0; i < RD; ++i) {
-                        const int b = sub + LD * (bb * RD + i);
-                        if (b < nbf) {
-                            w4[i] = ld_weights(qd + b);
-                            sw[i] = ld_scale(dd + b);
+                        for (int i = 0; i < RD; ++i) {
+                            const int b = sub + LD * (bb * RD + i);
+                            if (b < nbf) {
+                                w4[i] = ld_weights(qd + b);
+                                sw[i] = ld_scale(dd + b);
+                            }
                         }
                     }
                     if (bb == 0) {
+                        if (from_smem) cp_async_wait_all();
                         if (!waited) {
                             // wait (bounded) for all gate/up row blocks of expert e
                             if (threadIdx.x == 0) {
@@ -741,6 +801,18 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
                             hds_s[(size_t)t * nbf + c] = BlockScale{__int_as_float(v.x), v.y};
                         }
                         __syncthreads();
+                    }
+                    if (from_smem) {
+                        const uint4 *pc = (const uint4 *)dpre + (size_t)rloc * nbf;
+                        const __half *ps = (const __half *)(dpre + (size_t)DROWS * nbf * 16) + (size_t)rloc * nbf;
+#pragma unroll
+                        for (int i = 0; i < RD; ++i) {
+                            const int b = sub + LD * (bb * RD + i);
+                            if (b < nbf) {
+                                w4[i] = pc[b];
+                                sw[i] = __half2float(ps[b]);
+                            }
+                        }
                     }
 #pragma unroll
                     for (int i = 0; i < RD; ++i) {
@@ -809,9 +881,9 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
 }
 
 size_t fused_smem_bytes(int H, int F) {
-    const size_t gu = (size_t)kMaxChunk * H + (size_t)kMaxChunk * (H / kBlock) * sizeof(BlockScale);
-    const size_t dn = (size_t)kMaxChunk * F + (size_t)kMaxChunk * (F / kBlock) * sizeof(BlockScale);
-    return gu > dn ? gu : dn;
+    const int LD = F / kBlock <= 40 ? 4 : 8;
+    const size_t rows = (size_t)kWarps * (32 / LD);
+    return fused_stage_bytes(H, F) + rows * (F / kBlock) * kBlockBytes;
 }
 
 int fused_down_lanes(int F) { return F / kBlock <= 40 ? 4 : 8; }
