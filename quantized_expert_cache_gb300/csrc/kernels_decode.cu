@@ -568,7 +568,206 @@ __device__ void fused_plan(const FusedParams &p, int *s_e, int *s_uniq, int *s_o
     __syncthreads();
 }
 
-template <int LD>
+// One chunk (nt <= NT tokens of one used expert) of a gate/up item: issue
+// the item's weight loads, quantize the chunk's x rows into shared memory
+// while they fly, block dots, SwiGLU, quantize h (one warp per token).
+template <int NT>
+__device__ __forceinline__ void gu_chunk(const FusedParams &p, int c0, int nt, int rg, int rloc, int sub, int lane,
+                                         int warp, const uint4 *qg, const uint4 *qu, const __half *dg,
+                                         const __half *du, int8_t *xq_s, BlockScale *xds_s, float (*sh_h)[32],
+                                         const int *s_asg) {
+    const GemvParams &g = p.g;
+    const int H = g.H, F = g.F, k = g.k;
+    const int nbx = H / kBlock, rgs = F / kBlock;
+    float ag[NT], au[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) ag[t] = au[t] = 0.0f;
+    for (int bb = 0; bb * kGULanes * kGURounds < nbx; ++bb) {
+        uint4 wg4[kGURounds], wu4[kGURounds];
+        float sg[kGURounds], su[kGURounds];
+#pragma unroll
+        for (int i = 0; i < kGURounds; ++i) {
+            const int b = sub + kGULanes * (bb * kGURounds + i);
+            if (b < nbx) {
+                wg4[i] = ld_weights(qg + b);
+                wu4[i] = ld_weights(qu + b);
+                sg[i] = ld_scale(dg + b);
+                su[i] = ld_scale(du + b);
+            }
+        }
+        if (bb == 0) {
+            // quantize the x rows of this chunk while the loads fly; each
+            // warp first loads all of its blocks, then reduces
+            const int nblk = nt * nbx;
+            for (int q0 = warp; q0 < nblk; q0 += kWarps * kXBatch) {
+                float xv[kXBatch];
+#pragma unroll
+                for (int i = 0; i < kXBatch; ++i) {
+                    const int q = q0 + i * kWarps;
+                    if (q < nblk) {
+                        const int t = q / nbx, b = q - t * nbx;
+                        const int tok = s_asg[c0 + t] / k;
+                        xv[i] = __ldg(p.x + (size_t)tok * H + (size_t)b * kBlock + lane);
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < kXBatch; ++i) {
+                    const int q = q0 + i * kWarps;
+                    if (q < nblk) {
+                        const int t = q / nbx, b = q - t * nbx;
+                        const int a = s_asg[c0 + t];
+                        const int tok = a / k;
+                        quantize_block_warp(xv[i], lane, xq_s + (size_t)t * H + (size_t)b * kBlock,
+                                            xds_s + (size_t)t * nbx + b);
+                        if (rg == 0 && (a % k) == 0) {
+                            g.xq_out[(size_t)tok * H + (size_t)b * kBlock + lane] =
+                                xq_s[(size_t)t * H + (size_t)b * kBlock + lane];
+                            if (lane == 0) g.xds_out[(size_t)tok * nbx + b] = xds_s[(size_t)t * nbx + b];
+                        }
+                    }
+                }
+            }
+            __syncthreads();
+        }
+#pragma unroll
+        for (int i = 0; i < kGURounds; ++i) {
+            const int b = sub + kGULanes * (bb * kGURounds + i);
+            if (b < nbx) {
+#pragma unroll
+                for (int t = 0; t < NT; ++t) {
+                    if (NT == 1 || t < nt) {
+                        const int4 *xa = (const int4 *)(xq_s + (size_t)t * H + (size_t)b * kBlock);
+                        const int4 x0 = xa[0], x1 = xa[1];
+                        const BlockScale xs = xds_s[(size_t)t * nbx + b];
+                        ag[t] += (float)q4_block_dot(wg4[i], x0, x1, xs.s) * (sg[i] * xs.d);
+                        au[t] += (float)q4_block_dot(wu4[i], x0, x1, xs.s) * (su[i] * xs.d);
+                    }
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+#pragma unroll
+        for (int o = kGULanes / 2; o > 0; o >>= 1) {
+            ag[t] += __shfl_xor_sync(0xffffffffu, ag[t], o);
+            au[t] += __shfl_xor_sync(0xffffffffu, au[t], o);
+        }
+    }
+    if (sub == 0) {
+#pragma unroll
+        for (int t = 0; t < NT; ++t)
+            if (NT == 1 || t < nt) sh_h[t][rloc] = ag[t] * au[t] / (1.0f + expf(-ag[t]));
+    }
+    __syncthreads();
+    if (warp < nt) {
+        const int a = s_asg[c0 + warp];
+        quantize_block_warp(sh_h[warp][lane], lane, g.hq + (size_t)a * F + (size_t)rg * kBlock,
+                            g.hds + (size_t)a * rgs + rg);
+    }
+    __syncthreads();
+}
+
+// One chunk of a down item: weight loads (or the shared-memory prefetch),
+// a bounded wait for the expert's h (first chunk only), h staged in shared
+// memory, block dots, o written per assignment.
+template <int NT, int LD>
+__device__ __forceinline__ void dn_chunk(const FusedParams &p, int c0, int nt, int e, int r, int rloc, int sub,
+                                         const uint4 *qd, const __half *dd, int8_t *hq_s, BlockScale *hds_s,
+                                         const uint8_t *dpre, bool from_smem, bool waited, const int *s_asg) {
+    constexpr int DG = 32 / LD, DROWS = kWarps * DG;
+    constexpr int RD = 12;  // loads per lane issued together (<= 12 rounds)
+    const GemvParams &g = p.g;
+    const int H = g.H, F = g.F;
+    const int nbf = F / kBlock, rgs = F / kBlock;
+    float acc[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) acc[t] = 0.0f;
+    for (int bb = 0; bb * LD * RD < nbf; ++bb) {
+        uint4 w4[RD];
+        float sw[RD];
+        if (!from_smem) {
+#pragma unroll
+            for (int i = 0; i < RD; ++i) {
+                const int b = sub + LD * (bb * RD + i);
+                if (b < nbf) {
+                    w4[i] = ld_weights(qd + b);
+                    sw[i] = ld_scale(dd + b);
+                }
+            }
+        }
+        if (bb == 0) {
+            if (from_smem) cp_async_wait_all();
+            if (!waited) {
+                // wait (bounded) for all gate/up row blocks of expert e
+                if (threadIdx.x == 0) {
+                    const long long t0 = clock64();
+                    while (ld_acquire(&p.done_gu[e]) < (unsigned)rgs) {
+                        if (clock64() - t0 > 4000000000ll) {
+                            atomicOr(p.error, 2);
+                            break;
+                        }
+                        __nanosleep(64);
+                    }
+                }
+                __syncthreads();
+            }
+            // stage the chunk's h codes and scales
+            for (int i = threadIdx.x; i < nt * (F / 16); i += blockDim.x) {
+                const int t = i / (F / 16), c = i - t * (F / 16);
+                const int a = s_asg[c0 + t];
+                reinterpret_cast<int4 *>(hq_s + (size_t)t * F)[c] =
+                    __ldcg(reinterpret_cast<const int4 *>(g.hq + (size_t)a * F) + c);
+            }
+            for (int i = threadIdx.x; i < nt * nbf; i += blockDim.x) {
+                const int t = i / nbf, c = i - t * nbf;
+                const int a = s_asg[c0 + t];
+                const int2 v = __ldcg(reinterpret_cast<const int2 *>(g.hds + (size_t)a * nbf + c));
+                hds_s[(size_t)t * nbf + c] = BlockScale{__int_as_float(v.x), v.y};
+            }
+            __syncthreads();
+        }
+        if (from_smem) {
+            const uint4 *pc = (const uint4 *)dpre + (size_t)rloc * nbf;
+            const __half *ps = (const __half *)(dpre + (size_t)DROWS * nbf * 16) + (size_t)rloc * nbf;
+#pragma unroll
+            for (int i = 0; i < RD; ++i) {
+                const int b = sub + LD * (bb * RD + i);
+                if (b < nbf) {
+                    w4[i] = pc[b];
+                    sw[i] = __half2float(ps[b]);
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < RD; ++i) {
+            const int b = sub + LD * (bb * RD + i);
+            if (b < nbf) {
+#pragma unroll
+                for (int t = 0; t < NT; ++t) {
+                    if (NT == 1 || t < nt) {
+                        const int4 *ha = (const int4 *)(hq_s + (size_t)t * F + (size_t)b * kBlock);
+                        const BlockScale hs = hds_s[(size_t)t * nbf + b];
+                        acc[t] += (float)q4_block_dot(w4[i], ha[0], ha[1], hs.s) * (sw[i] * hs.d);
+                    }
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+#pragma unroll
+        for (int o = LD / 2; o > 0; o >>= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], o);
+    }
+    if (sub == 0) {
+#pragma unroll
+        for (int t = 0; t < NT; ++t)
+            if (NT == 1 || t < nt) g.o[(size_t)s_asg[c0 + t] * H + r] = acc[t];
+    }
+    __syncthreads();
+}
+
+template <int LD, int NT>
 __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
     __shared__ int s_e[kMaxFusedA], s_uniq[kMaxFusedA], s_off[kMaxFusedA + 1], s_asg[kMaxFusedA],
         s_cnt[kMaxFusedA], s_first[kMaxFusedA];
@@ -632,95 +831,9 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
             const uint4 *qu = (const uint4 *)bu + (size_t)r * nbx;
             const __half *dg = (const __half *)(bg + scale_off) + (size_t)r * nbx;
             const __half *du = (const __half *)(bu + scale_off) + (size_t)r * nbx;
-            for (int c0 = a0; c0 < a1; c0 += kMaxChunk) {
-                const int nt = min(kMaxChunk, a1 - c0);
-                float ag[kMaxChunk], au[kMaxChunk];
-#pragma unroll
-                for (int t = 0; t < kMaxChunk; ++t) ag[t] = au[t] = 0.0f;
-                for (int bb = 0; bb * kGULanes * kGURounds < nbx; ++bb) {
-                    uint4 wg4[kGURounds], wu4[kGURounds];
-                    float sg[kGURounds], su[kGURounds];
-#pragma unroll
-                    for (int i = 0; i < kGURounds; ++i) {
-                        const int b = sub + kGULanes * (bb * kGURounds + i);
-                        if (b < nbx) {
-                            wg4[i] = ld_weights(qg + b);
-                            wu4[i] = ld_weights(qu + b);
-                            sg[i] = ld_scale(dg + b);
-                            su[i] = ld_scale(du + b);
-                        }
-                    }
-                    if (bb == 0) {
-                        // quantize the x rows of this chunk while the loads fly;
-                        // each warp first loads all of its blocks, then reduces
-                        const int nblk = nt * nbx;
-                        for (int q0 = warp; q0 < nblk; q0 += kWarps * kXBatch) {
-                            float xv[kXBatch];
-#pragma unroll
-                            for (int i = 0; i < kXBatch; ++i) {
-                                const int q = q0 + i * kWarps;
-                                if (q < nblk) {
-                                    const int t = q / nbx, b = q - t * nbx;
-                                    const int tok = s_asg[c0 + t] / k;
-                                    xv[i] = __ldg(p.x + (size_t)tok * H + (size_t)b * kBlock + lane);
-                                }
-                            }
-#pragma unroll
-                            for (int i = 0; i < kXBatch; ++i) {
-                                const int q = q0 + i * kWarps;
-                                if (q < nblk) {
-                                    const int t = q / nbx, b = q - t * nbx;
-                                    const int a = s_asg[c0 + t];
-                                    const int tok = a / k;
-                                    quantize_block_warp(xv[i], lane, xq_s + (size_t)t * H + (size_t)b * kBlock,
-                                                        xds_s + (size_t)t * nbx + b);
-                                    if (rg == 0 && (a % k) == 0) {
-                                        g.xq_out[(size_t)tok * H + (size_t)b * kBlock + lane] =
-                                            xq_s[(size_t)t * H + (size_t)b * kBlock + lane];
-                                        if (lane == 0) g.xds_out[(size_t)tok * nbx + b] = xds_s[(size_t)t * nbx + b];
-                                    }
-                                }
-                            }
-                        }
-                        __syncthreads();
-                    }
-#pragma unroll
-                    for (int i = 0; i < kGURounds; ++i) {
-                        const int b = sub + kGULanes * (bb * kGURounds + i);
-                        if (b < nbx) {
-#pragma unroll
-                            for (int t = 0; t < kMaxChunk; ++t) {
-                                if (t < nt) {
-                                    const int4 *xa = (const int4 *)(xq_s + (size_t)t * H + (size_t)b * kBlock);
-                                    const int4 x0 = xa[0], x1 = xa[1];
-                                    const BlockScale xs = xds_s[(size_t)t * nbx + b];
-                                    ag[t] += (float)q4_block_dot(wg4[i], x0, x1, xs.s) * (sg[i] * xs.d);
-                                    au[t] += (float)q4_block_dot(wu4[i], x0, x1, xs.s) * (su[i] * xs.d);
-                                }
-                            }
-                        }
-                    }
-                }
-#pragma unroll
-                for (int t = 0; t < kMaxChunk; ++t) {
-#pragma unroll
-                    for (int o = kGULanes / 2; o > 0; o >>= 1) {
-                        ag[t] += __shfl_xor_sync(0xffffffffu, ag[t], o);
-                        au[t] += __shfl_xor_sync(0xffffffffu, au[t], o);
-                    }
-                }
-                if (sub == 0) {
-#pragma unroll
-                    for (int t = 0; t < kMaxChunk; ++t)
-                        if (t < nt) sh_h[t][rloc] = ag[t] * au[t] / (1.0f + expf(-ag[t]));
-                }
-                __syncthreads();
-                if (warp < nt) {
-                    const int a = s_asg[c0 + warp];
-                    quantize_block_warp(sh_h[warp][lane], lane, g.hq + (size_t)a * F + (size_t)rg * kBlock,
-                                        g.hds + (size_t)a * rgs + rg);
-                }
-                __syncthreads();
+            for (int c0 = a0; c0 < a1; c0 += NT) {
+                const int nt = min(NT, a1 - c0);
+                gu_chunk<NT>(p, c0, nt, rg, rloc, sub, lane, warp, qg, qu, dg, du, xq_s, xds_s, sh_h, s_asg);
             }
             // publish this row block of expert e
             __threadfence();
@@ -751,95 +864,11 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
             const uint4 *qd = (const uint4 *)bd + (size_t)r * nbf;
             const __half *dd = (const __half *)(bd + scale_off) + (size_t)r * nbf;
             bool waited = false;
-            for (int c0 = a0; c0 < a1; c0 += kMaxChunk) {
-                const int nt = min(kMaxChunk, a1 - c0);
-                float acc[kMaxChunk];
-#pragma unroll
-                for (int t = 0; t < kMaxChunk; ++t) acc[t] = 0.0f;
-                const bool from_smem = prefetched && item == (int)blockIdx.x;
-                for (int bb = 0; bb * LD * RD < nbf; ++bb) {
-                    uint4 w4[RD];
-                    float sw[RD];
-                    if (!from_smem) {
-#pragma unroll
-                        for (int i = 0; i < RD; ++i) {
-                            const int b = sub + LD * (bb * RD + i);
-                            if (b < nbf) {
-                                w4[i] = ld_weights(qd + b);
-                                sw[i] = ld_scale(dd + b);
-                            }
-                        }
-                    }
-                    if (bb == 0) {
-                        if (from_smem) cp_async_wait_all();
-                        if (!waited) {
-                            // wait (bounded) for all gate/up row blocks of expert e
-                            if (threadIdx.x == 0) {
-                                const long long t0 = clock64();
-                                while (ld_acquire(&p.done_gu[e]) < (unsigned)rgs) {
-                                    if (clock64() - t0 > 4000000000ll) {
-                                        atomicOr(p.error, 2);
-                                        break;
-                                    }
-                                    __nanosleep(64);
-                                }
-                            }
-                            __syncthreads();
-                            waited = true;
-                        }
-                        // stage the chunk's h codes and scales
-                        for (int i = threadIdx.x; i < nt * (F / 16); i += blockDim.x) {
-                            const int t = i / (F / 16), c = i - t * (F / 16);
-                            const int a = s_asg[c0 + t];
-                            reinterpret_cast<int4 *>(hq_s + (size_t)t * F)[c] =
-                                __ldcg(reinterpret_cast<const int4 *>(g.hq + (size_t)a * F) + c);
-                        }
-                        for (int i = threadIdx.x; i < nt * nbf; i += blockDim.x) {
-                            const int t = i / nbf, c = i - t * nbf;
-                            const int a = s_asg[c0 + t];
-                            const int2 v = __ldcg(reinterpret_cast<const int2 *>(g.hds + (size_t)a * nbf + c));
-                            hds_s[(size_t)t * nbf + c] = BlockScale{__int_as_float(v.x), v.y};
-                        }
-                        __syncthreads();
-                    }
-                    if (from_smem) {
-                        const uint4 *pc = (const uint4 *)dpre + (size_t)rloc * nbf;
-                        const __half *ps = (const __half *)(dpre + (size_t)DROWS * nbf * 16) + (size_t)rloc * nbf;
-#pragma unroll
-                        for (int i = 0; i < RD; ++i) {
-                            const int b = sub + LD * (bb * RD + i);
-                            if (b < nbf) {
-                                w4[i] = pc[b];
-                                sw[i] = __half2float(ps[b]);
-                            }
-                        }
-                    }
-#pragma unroll
-                    for (int i = 0; i < RD; ++i) {
-                        const int b = sub + LD * (bb * RD + i);
-                        if (b < nbf) {
-#pragma unroll
-                            for (int t = 0; t < kMaxChunk; ++t) {
-                                if (t < nt) {
-                                    const int4 *ha = (const int4 *)(hq_s + (size_t)t * F + (size_t)b * kBlock);
-                                    const BlockScale hs = hds_s[(size_t)t * nbf + b];
-                                    acc[t] += (float)q4_block_dot(w4[i], ha[0], ha[1], hs.s) * (sw[i] * hs.d);
-                                }
-                            }
-                        }
-                    }
-                }
-#pragma unroll
-                for (int t = 0; t < kMaxChunk; ++t) {
-#pragma unroll
-                    for (int o = LD / 2; o > 0; o >>= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], o);
-                }
-                if (sub == 0) {
-#pragma unroll
-                    for (int t = 0; t < kMaxChunk; ++t)
-                        if (t < nt) g.o[(size_t)s_asg[c0 + t] * H + r] = acc[t];
-                }
-                __syncthreads();
+            const bool from_smem = prefetched && item == (int)blockIdx.x;
+            for (int c0 = a0; c0 < a1; c0 += NT) {
+                const int nt = min(NT, a1 - c0);
+                dn_chunk<NT, LD>(p, c0, nt, e, r, rloc, sub, qd, dd, hq_s, hds_s, dpre, from_smem, waited, s_asg);
+                waited = true;
             }
             // arrival count of this row block; the last item combines
             __threadfence();
@@ -888,12 +917,37 @@ size_t fused_smem_bytes(int H, int F) {
 
 int fused_down_lanes(int F) { return F / kBlock <= 40 ? 4 : 8; }
 
+static int fused_nt(int T) { return T <= 1 ? 1 : T == 2 ? 2 : T <= 4 ? 4 : 8; }
+
+static const void *fused_fn(int F, int T) {
+    const int ld = fused_down_lanes(F), nt = fused_nt(T);
+    if (ld == 4) {
+        if (nt == 1) return (const void *)decode_layer_kernel<4, 1>;
+        if (nt == 2) return (const void *)decode_layer_kernel<4, 2>;
+        if (nt == 4) return (const void *)decode_layer_kernel<4, 4>;
+        return (const void *)decode_layer_kernel<4, 8>;
+    }
+    if (nt == 1) return (const void *)decode_layer_kernel<8, 1>;
+    if (nt == 2) return (const void *)decode_layer_kernel<8, 2>;
+    if (nt == 4) return (const void *)decode_layer_kernel<8, 4>;
+    return (const void *)decode_layer_kernel<8, 8>;
+}
+
+// Shared-memory opt-in for every token-count variant; *blocks_per_sm gets
+// the smallest resident-CTA count over the variants (a safe cooperative grid).
 int fused_configure(int F, size_t smem, int *blocks_per_sm) {
-    const void *fn = fused_down_lanes(F) == 4 ? (const void *)decode_layer_kernel<4> : (const void *)decode_layer_kernel<8>;
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return (int)e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, fn, 256, smem);
-    return (int)e;
+    int best = 1 << 30;
+    for (int T : {1, 2, 4, 8}) {
+        const void *fn = fused_fn(F, T);
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return (int)e;
+        int b = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, fn, 256, smem);
+        if (e != cudaSuccess) return (int)e;
+        best = b < best ? b : best;
+    }
+    *blocks_per_sm = best;
+    return 0;
 }
 
 int launch_fused(const FusedParams &p, int grid, size_t smem, cudaStream_t st, cudaEvent_t const *ev) {
@@ -908,11 +962,8 @@ int launch_fused(const FusedParams &p, int grid, size_t smem, cudaStream_t st, c
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (ev) record(ev[0], st);
-    cudaError_t e;
-    if (fused_down_lanes(p.g.F) == 4)
-        e = cudaLaunchKernelEx(&cfg, decode_layer_kernel<4>, p);
-    else
-        e = cudaLaunchKernelEx(&cfg, decode_layer_kernel<8>, p);
+    void *args[] = {(void *)&p};
+    cudaError_t e = cudaLaunchKernelExC(&cfg, fused_fn(p.g.F, p.g.n_tokens), args);
     if (ev) {
         record(ev[1], st);
         record(ev[2], st);
