@@ -42,7 +42,6 @@ namespace gemm {
 
 constexpr int BM = 128;
 constexpr int BK = 64;
-constexpr int STAGES = 4;
 constexpr int NWARPS = 10;
 constexpr int NTHREADS = NWARPS * 32;
 constexpr int W_TMA = 0, W_MMA = 1, W_CONV = 2, W_EPI = 6;
@@ -52,18 +51,27 @@ template <bool DUAL>
 struct Cfg {
     static constexpr int BN = DUAL ? 64 : 128;
     static constexpr int NA = DUAL ? 2 : 1;
+    static constexpr int STAGES = DUAL ? 3 : 4;   // A/B pipeline slots
+    static constexpr int RR = 8;                  // raw prefetch ring (converter cp.async)
+    static constexpr int PD = RR - 1;             // prefetch distance in stages
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = BN * BK * 2;
-    static constexpr int STAGE_BYTES = NA * A_BYTES + B_BYTES;
+    // per-slot scales for the epilogue: weight scales [NA][BM][2] fp16 and
+    // activation scales [2][BN] fp32 of the slot's two K blocks
+    static constexpr int WS_BYTES = NA * BM * 2 * 2;
+    static constexpr int AS_BYTES = 2 * BN * 4;
+    static constexpr int SLOT_BYTES = NA * A_BYTES + B_BYTES + WS_BYTES + AS_BYTES;
+    static constexpr int SLOT_STRIDE = (SLOT_BYTES + 1023) / 1024 * 1024;
+    // raw ring entry: codes [NA][BM][32 B], weight scales, activation scales
+    static constexpr int RAW_CODES = NA * BM * 32;
+    static constexpr int RAW_BYTES = RAW_CODES + WS_BYTES + AS_BYTES;
+    static constexpr int RAW_OFF = STAGES * SLOT_STRIDE;
     static constexpr int TBUF = NA * BN;          // TMEM columns per K-block buffer
     static constexpr int NTBUF = 512 / TBUF;      // K-block buffers in TMEM
-    static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
-    // barriers: full[S], empty[S], tfull[NT], tempty[NT]; then tmem slot,
-    // abort flag, epilogue scale buffers
+    static constexpr int BAR_OFF = RAW_OFF + RR * RAW_BYTES;
     static constexpr int NBARS = 2 * STAGES + 2 * NTBUF;
     static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
-    static constexpr int DA_OFF = MISC_OFF + 16;
-    static constexpr int SMEM = DA_OFF + 4 * BN * 4 + 1024;  // + alignment slack
+    static constexpr int SMEM = MISC_OFF + 16 + 1024;  // + alignment slack
 };
 
 // ---- PTX wrappers -----------------------------------------------------------
@@ -111,6 +119,17 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *tm,
         "l"((uint64_t)tm), "r"(x), "r"(y), "r"(bar)
         : "memory");
 }
+
+__device__ __forceinline__ void cp_async(uint32_t dst, const void *src, int bytes, bool valid) {
+    const int n = valid ? bytes : 0;  // 0: zero fill, nothing read
+    if (bytes == 16)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
+    else
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -219,11 +238,36 @@ __device__ __forceinline__ void decode_tile(int t, const int32_t *tile_off, int 
     tok_tile = local - row_tile * ntok;
 }
 
+// Stage cursor over the flattened (tile, K stage) sequence of one CTA.
+struct StageCur {
+    int t, kt, u, rt, tt;
+    bool valid;
+};
+
+template <int BN>
+__device__ __forceinline__ void cur_init(StageCur &c, const GemmParams &p, int n_uniq, int total) {
+    c.t = blockIdx.x;
+    c.kt = 0;
+    c.valid = c.t < total;
+    if (c.valid) decode_tile(c.t, p.tile_off, n_uniq, p.uniq_off, BN, c.u, c.rt, c.tt);
+}
+
+template <int BN>
+__device__ __forceinline__ void cur_next(StageCur &c, const GemmParams &p, int n_uniq, int total, int nkt) {
+    if (!c.valid) return;
+    if (++c.kt == nkt) {
+        c.kt = 0;
+        c.t += gridDim.x;
+        c.valid = c.t < total;
+        if (c.valid) decode_tile(c.t, p.tile_off, n_uniq, p.uniq_off, BN, c.u, c.rt, c.tt);
+    }
+}
+
 template <bool DUAL>
 __global__ void __launch_bounds__(NTHREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmB, GemmParams p) {
     using C = Cfg<DUAL>;
-    constexpr int BN = C::BN, NA = C::NA, NTBUF = C::NTBUF;
+    constexpr int BN = C::BN, NA = C::NA, NTBUF = C::NTBUF, STAGES = C::STAGES;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint64_t *bars = (uint64_t *)(smem + C::BAR_OFF);
@@ -231,13 +275,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                    tempty0 = tfull0 + 8 * NTBUF;
     volatile uint32_t *tmem_slot = (volatile uint32_t *)(smem + C::MISC_OFF);
     volatile int *abort_flag = (volatile int *)(smem + C::MISC_OFF + 4);
-    float *da_ep = (float *)(smem + C::DA_OFF);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full0 + 8 * s, 1 + 4);
-            mbar_init(empty0 + 8 * s, 1);
+            mbar_init(full0 + 8 * s, 1 + 4);   // TMA expect-tx arrive + 4 converter warps
+            mbar_init(empty0 + 8 * s, 1 + 4);  // MMA commit + 4 epilogue warps
         }
         for (int j = 0; j < NTBUF; ++j) {
             mbar_init(tfull0 + 8 * j, 1);
@@ -262,6 +305,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int nkt = p.K / BK;
     const int nbk = p.K / kBlock;
     const size_t scale_off = blob_scales_offset(p.rows, nbk);
+    auto slot_ptr = [&](int slot) { return smem + slot * C::SLOT_STRIDE; };
 
     if (warp == W_TMA) {
         if (lane == 0) {
@@ -275,8 +319,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
                     if (!mbar_wait(empty0 + 8 * slot, ph ^ 1u, abort_flag, p.error, 2)) goto tma_done;
                     mbar_arrive_tx(full0 + 8 * slot, C::B_BYTES);
-                    tma_load_2d(smem_u32(smem + slot * C::STAGE_BYTES + NA * C::A_BYTES), &tmB, kt * BK, pos0,
-                                full0 + 8 * slot);
+                    tma_load_2d(smem_u32(slot_ptr(slot) + NA * C::A_BYTES), &tmB, kt * BK, pos0, full0 + 8 * slot);
                 }
             }
         tma_done:;
@@ -291,7 +334,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     if (!mbar_wait(full0 + 8 * slot, (uint32_t)(it / STAGES) & 1u, abort_flag, p.error, 4))
                         goto mma_done;
                     tc_fence_after();
-                    uint8_t *st = smem + slot * C::STAGE_BYTES;
+                    uint8_t *st = slot_ptr(slot);
                     const uint64_t db = sdesc(smem_u32(st + NA * C::A_BYTES));
                     for (int blk = 0; blk < 2; ++blk, ++qc) {
                         const int j = qc % NTBUF;
@@ -316,109 +359,136 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         mma_done:;
         }
     } else if (warp < W_EPI) {
-        // weight converters: thread r converts row r of each A tile
+        // Converters: thread r owns row r of the A tiles.  Raw Q4 codes and
+        // both scale sets of stage s are fetched with cp.async PD stages ahead
+        // into raw ring entry s % RR; stage s is then converted into its slot.
         const int r = threadIdx.x - W_CONV * 32;
-        int it = 0;
-        for (int t = blockIdx.x; t < total; t += gridDim.x) {
-            int u, rt, tt;
-            decode_tile(t, p.tile_off, n_uniq, p.uniq_off, BN, u, rt, tt);
-            const int e = p.uniq_e[u];
-            const int row = rt * BM + r;
-            const bool valid = row < p.rows;
-            const uint4 *src[NA];
-#pragma unroll
-            for (int a = 0; a < NA; ++a) {
-                const uint64_t ent = p.tbl[a][e];
-                src[a] = (const uint4 *)(uintptr_t)(ent & ~1ull) + (size_t)(valid ? row : 0) * nbk;
-            }
-            for (int kt = 0; kt < nkt; ++kt, ++it) {
-                uint4 c[NA][2];
+        uint8_t *raw = smem + C::RAW_OFF;
+        StageCur fc, cc;  // fetch and convert cursors
+        cur_init<BN>(fc, p, n_uniq, total);
+        cur_init<BN>(cc, p, n_uniq, total);
+        auto fetch = [&](const StageCur &c, int rs) {
+            uint8_t *ent = raw + rs * C::RAW_BYTES;
+            if (c.valid) {
+                const int e = p.uniq_e[c.u];
+                const int row = c.rt * BM + r;
+                const bool vrow = row < p.rows;
+                const int srow = vrow ? row : 0;
 #pragma unroll
                 for (int a = 0; a < NA; ++a) {
-                    if (valid) {
-                        c[a][0] = ld_weights(src[a] + 2 * kt);
-                        c[a][1] = ld_weights(src[a] + 2 * kt + 1);
-                    } else {
-                        c[a][0] = c[a][1] = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
-                    }
+                    const uint8_t *blob = (const uint8_t *)(uintptr_t)(p.tbl[a][e] & ~1ull);
+                    const uint8_t *src = blob + ((size_t)srow * nbk + 2 * c.kt) * 16;
+                    const uint32_t dst = smem_u32(ent + (a * BM + r) * 32);
+                    cp_async(dst, src, 16, vrow);
+                    cp_async(dst + 16, src + 16, 16, vrow);
+                    const uint8_t *ssrc = blob + scale_off + ((size_t)srow * nbk + 2 * c.kt) * 2;
+                    cp_async(smem_u32(ent + C::RAW_CODES + (a * BM + r) * 4), ssrc, 4, vrow);
                 }
-                const int slot = it % STAGES;
-                const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
-                bool ok = true;
-                if (lane == 0) ok = mbar_wait(empty0 + 8 * slot, ph ^ 1u, abort_flag, p.error, 16);
-                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-                if (!ok) goto conv_done;
-                uint8_t *st = smem + slot * C::STAGE_BYTES;
-#pragma unroll
-                for (int a = 0; a < NA; ++a) convert_store_row(st + a * C::A_BYTES, r, c[a][0], c[a][1]);
-                fence_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(full0 + 8 * slot);
+                const int pos0 = p.uniq_off[c.u] + c.tt * BN;
+                for (int i = r; i < 2 * BN; i += 128) {
+                    const int q = i / BN, col = i - q * BN;
+                    const int pos = pos0 + col;
+                    const bool v = pos < p.A_pad;
+                    const float *src = p.a_scaleT + (size_t)(2 * c.kt + q) * p.A_pad + (v ? pos : 0);
+                    cp_async(smem_u32(ent + C::RAW_CODES + C::WS_BYTES + i * 4), src, 4, v);
+                }
             }
+            cp_commit();
+        };
+        for (int i = 0; i < C::PD; ++i) {
+            fetch(fc, i % C::RR);
+            cur_next<BN>(fc, p, n_uniq, total, nkt);
         }
-    conv_done:;
+        int it = 0;
+        while (cc.valid) {
+            fetch(fc, (it + C::PD) % C::RR);
+            cur_next<BN>(fc, p, n_uniq, total, nkt);
+            cp_wait<C::PD>();
+            const uint8_t *ent = raw + (it % C::RR) * C::RAW_BYTES;
+            const int slot = it % STAGES;
+            const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+            bool ok = true;
+            if (lane == 0) ok = mbar_wait(empty0 + 8 * slot, ph ^ 1u, abort_flag, p.error, 16);
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            if (!ok) break;
+            uint8_t *st = slot_ptr(slot);
+#pragma unroll
+            for (int a = 0; a < NA; ++a) {
+                const uint4 *cs = (const uint4 *)(ent + (a * BM + r) * 32);
+                convert_store_row(st + a * C::A_BYTES, r, cs[0], cs[1]);
+                // this row's two weight scales of the stage
+                *(uint32_t *)(st + NA * C::A_BYTES + C::B_BYTES + (a * BM + r) * 4) =
+                    *(const uint32_t *)(ent + C::RAW_CODES + (a * BM + r) * 4);
+            }
+            for (int i = r; i < 2 * BN; i += 128)
+                *(float *)(st + NA * C::A_BYTES + C::B_BYTES + C::WS_BYTES + i * 4) =
+                    *(const float *)(ent + C::RAW_CODES + C::WS_BYTES + i * 4);
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(full0 + 8 * slot);
+            cur_next<BN>(cc, p, n_uniq, total, nkt);
+            ++it;
+        }
+        cp_wait<0>();
     } else {
         // epilogue: TMEM lane quarter = warp % 4; thread = weight row
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;
-        int qc = 0;
+        int qc = 0, it = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
             int u, rt, tt;
             decode_tile(t, p.tile_off, n_uniq, p.uniq_off, BN, u, rt, tt);
-            const int e = p.uniq_e[u];
             const int row = rt * BM + r;
             const bool vrow = row < p.rows;
             const int pos0 = p.uniq_off[u] + tt * BN;
             const int pos_end = p.uniq_off[u + 1];
-            const __half *dsc[NA];
-#pragma unroll
-            for (int a = 0; a < NA; ++a) {
-                const uint64_t ent = p.tbl[a][e];
-                dsc[a] = (const __half *)((const uint8_t *)(uintptr_t)(ent & ~1ull) + scale_off) +
-                         (size_t)(vrow ? row : 0) * nbk;
-            }
             float acc[NA][BN];
 #pragma unroll
             for (int a = 0; a < NA; ++a)
 #pragma unroll
                 for (int c = 0; c < BN; ++c) acc[a][c] = 0.0f;
-            float *dbuf = da_ep + (warp - W_EPI) * BN;  // this warp's copy of the token scales
-            for (int q = 0; q < nbk; ++q, ++qc) {
-                // activation scales of this K block for the tile's tokens
-                __syncwarp();
-#pragma unroll
-                for (int c = lane; c < BN; c += 32) {
-                    const int pos = pos0 + c;
-                    dbuf[c] = pos < p.A_pad ? p.a_scaleT[(size_t)q * p.A_pad + pos] : 0.0f;
-                }
-                __syncwarp();
-                float dw[NA];
-#pragma unroll
-                for (int a = 0; a < NA; ++a) dw[a] = __half2float(dsc[a][q]);
-                const int j = qc % NTBUF;
+            for (int kt = 0; kt < nkt; ++kt, ++it) {
+                const int slot = it % STAGES;
+                const uint8_t *st = slot_ptr(slot);
                 bool ok = true;
-                if (lane == 0) ok = mbar_wait(tfull0 + 8 * j, (uint32_t)(qc / NTBUF) & 1u, abort_flag, p.error, 32);
+                // the slot's scales were written before its full barrier completed
+                if (lane == 0) ok = mbar_wait(full0 + 8 * slot, (uint32_t)(it / STAGES) & 1u, abort_flag, p.error, 64);
                 ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                 if (!ok) goto epi_done;
-                tc_fence_after();
-                const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(j * C::TBUF);
+                __half2 wsc[NA];
 #pragma unroll
-                for (int a = 0; a < NA; ++a) {
+                for (int a = 0; a < NA; ++a)
+                    wsc[a] = *(const __half2 *)(st + NA * C::A_BYTES + C::B_BYTES + (a * BM + r) * 4);
+                const float *asc = (const float *)(st + NA * C::A_BYTES + C::B_BYTES + C::WS_BYTES);
+                for (int blk = 0; blk < 2; ++blk, ++qc) {
+                    const int j = qc % NTBUF;
+                    if (lane == 0) ok = mbar_wait(tfull0 + 8 * j, (uint32_t)(qc / NTBUF) & 1u, abort_flag, p.error, 32);
+                    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                    if (!ok) goto epi_done;
+                    tc_fence_after();
+                    const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(j * C::TBUF);
+                    const float *dq = asc + blk * BN;
 #pragma unroll
-                    for (int c0 = 0; c0 < BN; c0 += 16) {
-                        float pv[16];
-                        tmem_ld16(tb + (uint32_t)(a * BN + c0), pv);
-                        tmem_ld_wait();
+                    for (int a = 0; a < NA; ++a) {
+                        const float dw = blk ? __high2float(wsc[a]) : __low2float(wsc[a]);
 #pragma unroll
-                        for (int c = 0; c < 16; c += 2) {
-                            const float2 d2 = *reinterpret_cast<const float2 *>(dbuf + c0 + c);
-                            fma2(acc[a][c0 + c], acc[a][c0 + c + 1], pv[c], pv[c + 1], dw[a] * d2.x, dw[a] * d2.y);
+                        for (int c0 = 0; c0 < BN; c0 += 16) {
+                            float pv[16];
+                            tmem_ld16(tb + (uint32_t)(a * BN + c0), pv);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int c = 0; c < 16; c += 2) {
+                                const float2 d2 = *reinterpret_cast<const float2 *>(dq + c0 + c);
+                                fma2(acc[a][c0 + c], acc[a][c0 + c + 1], pv[c], pv[c + 1], dw * d2.x, dw * d2.y);
+                            }
                         }
                     }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(tempty0 + 8 * j);
                 }
-                tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(tempty0 + 8 * j);
+                if (lane == 0) mbar_arrive(empty0 + 8 * slot);
             }
             // tile outputs
             if (DUAL) {
