@@ -571,18 +571,34 @@ __device__ void fused_plan(const FusedParams &p, int *s_e, int *s_uniq, int *s_o
 // One chunk (nt <= NT tokens of one used expert) of a gate/up item: issue
 // the item's weight loads, quantize the chunk's x rows into shared memory
 // while they fly, block dots, SwiGLU, quantize h (one warp per token).
-template <int NT>
+template <int NT, class Prefetch>
 __device__ __forceinline__ void gu_chunk(const FusedParams &p, int c0, int nt, int rg, int rloc, int sub, int lane,
                                          int warp, const uint4 *qg, const uint4 *qu, const __half *dg,
                                          const __half *du, int8_t *xq_s, BlockScale *xds_s, float (*sh_h)[32],
-                                         const int *s_asg) {
+                                         const int *s_asg, Prefetch &&prefetch) {
     const GemvParams &g = p.g;
     const int H = g.H, F = g.F, k = g.k;
     const int nbx = H / kBlock, rgs = F / kBlock;
+    constexpr int XB = NT == 1 ? 12 : kXBatch;  // x blocks per warp loaded ahead of the weights
     float ag[NT], au[NT];
 #pragma unroll
     for (int t = 0; t < NT; ++t) ag[t] = au[t] = 0.0f;
+    const int nblk = nt * nbx;
     for (int bb = 0; bb * kGULanes * kGURounds < nbx; ++bb) {
+        // x of the chunk is requested before the weights, so the tiny x loads
+        // are not queued behind the item's weight stream
+        float xv[XB];
+        if (bb == 0) {
+#pragma unroll
+            for (int i = 0; i < XB; ++i) {
+                const int q = warp + i * kWarps;
+                if (q < nblk) {
+                    const int t = q / nbx, b = q - t * nbx;
+                    const int tok = s_asg[c0 + t] / k;
+                    xv[i] = __ldg(p.x + (size_t)tok * H + (size_t)b * kBlock + lane);
+                }
+            }
+        }
         uint4 wg4[kGURounds], wu4[kGURounds];
         float sg[kGURounds], su[kGURounds];
 #pragma unroll
@@ -596,22 +612,22 @@ __device__ __forceinline__ void gu_chunk(const FusedParams &p, int c0, int nt, i
             }
         }
         if (bb == 0) {
-            // quantize the x rows of this chunk while the loads fly; each
-            // warp first loads all of its blocks, then reduces
-            const int nblk = nt * nbx;
-            for (int q0 = warp; q0 < nblk; q0 += kWarps * kXBatch) {
-                float xv[kXBatch];
+            prefetch();  // the down item's weights, behind the gate/up weights
+            // quantize the x rows of this chunk while the weights fly
+            for (int q0 = warp; q0 < nblk; q0 += kWarps * XB) {
+                if (q0 != warp) {
 #pragma unroll
-                for (int i = 0; i < kXBatch; ++i) {
-                    const int q = q0 + i * kWarps;
-                    if (q < nblk) {
-                        const int t = q / nbx, b = q - t * nbx;
-                        const int tok = s_asg[c0 + t] / k;
-                        xv[i] = __ldg(p.x + (size_t)tok * H + (size_t)b * kBlock + lane);
+                    for (int i = 0; i < XB; ++i) {
+                        const int q = q0 + i * kWarps;
+                        if (q < nblk) {
+                            const int t = q / nbx, b = q - t * nbx;
+                            const int tok = s_asg[c0 + t] / k;
+                            xv[i] = __ldg(p.x + (size_t)tok * H + (size_t)b * kBlock + lane);
+                        }
                     }
                 }
 #pragma unroll
-                for (int i = 0; i < kXBatch; ++i) {
+                for (int i = 0; i < XB; ++i) {
                     const int q = q0 + i * kWarps;
                     if (q < nblk) {
                         const int t = q / nbx, b = q - t * nbx;
@@ -783,14 +799,18 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
     fused_plan(p, s_e, s_uniq, s_off, s_asg, &s_nu, s_cnt, s_first);
     const int nu = s_nu;
 
-    // Prefetch this CTA's first down item (codes + scales of ROWS rows) into
-    // shared memory with cp.async, so the down weights stream while the
-    // gate/up item runs.
+    // This CTA's first down item (codes + scales of DROWS rows) is copied
+    // into shared memory with cp.async, issued right behind the CTA's first
+    // gate/up weight loads (or at once when the CTA has no gate/up item), so
+    // the down weights stream while the gate/up item runs.
     constexpr int DG = 32 / LD, DROWS = kWarps * DG;
     const int n_rb_all = H / DROWS;
     uint8_t *dpre = dsm + fused_stage_bytes(H, F);
     const bool prefetched = (int)blockIdx.x < nu * n_rb_all;
-    if (prefetched) {
+    bool pf_issued = !prefetched;
+    auto issue_prefetch = [&]() {
+        if (pf_issued) return;
+        pf_issued = true;
         const int u = blockIdx.x / n_rb_all, rb = blockIdx.x - u * n_rb_all;
         const uint64_t ed = g.cv.tbl[(size_t)g.tid_down * g.cv.E + s_uniq[u]];
         const uint8_t *bd = (const uint8_t *)(uintptr_t)(ed & ~1ull);
@@ -804,7 +824,8 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
                 cp_async16(dpre + (size_t)nc * 16 + (size_t)(i - nc) * 16, scales + (size_t)(i - nc) * 16);
         }
         cp_async_commit();
-    }
+    };
+    if ((int)blockIdx.x >= nu * rgs) issue_prefetch();
 
     // ---------------- gate/up items
     {
@@ -833,7 +854,8 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
             const __half *du = (const __half *)(bu + scale_off) + (size_t)r * nbx;
             for (int c0 = a0; c0 < a1; c0 += NT) {
                 const int nt = min(NT, a1 - c0);
-                gu_chunk<NT>(p, c0, nt, rg, rloc, sub, lane, warp, qg, qu, dg, du, xq_s, xds_s, sh_h, s_asg);
+                gu_chunk<NT>(p, c0, nt, rg, rloc, sub, lane, warp, qg, qu, dg, du, xq_s, xds_s, sh_h, s_asg,
+                             issue_prefetch);
             }
             // publish this row block of expert e
             __threadfence();
@@ -841,6 +863,8 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
             if (threadIdx.x == 0) atomicAdd(&p.done_gu[e], 1u);
         }
     }
+
+    issue_prefetch();
 
     // ---------------- down items
     {

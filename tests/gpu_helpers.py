@@ -178,3 +178,74 @@ def check_layer_parity(m: Model, layer, x_np, logits_np, y_gpu, idx_gpu, w_gpu):
     y_ref = oracle.down_combine(idx_o, w_o, d, hq, hd, m.H, m.F) if n_alt else y_o
     assert_close(y_gpu, y_ref)
     return n_alt
+
+
+class _LazyExperts:
+    """Expert tensor whose experts are regenerated on demand from their
+    seeded streams (full-size workloads do not keep every weight in RAM)."""
+
+    def __init__(self, wl, layer, kind):
+        self.wl, self.layer, self.kind = wl, layer, kind
+        self.cache = {}
+
+    def __getitem__(self, e):
+        e = int(e)
+        if e not in self.cache:
+            self.cache[e] = self.wl.expert_tensor(self.layer, self.kind, e, e + 1)[0]
+        return self.cache[e]
+
+
+class FullModel(Model):
+    """A whole workload of synth.WORKLOADS registered in one context, with
+    the library's seeding (capacity and routing-frequency order per layer)."""
+
+    def __init__(self, wl, max_tokens, slots_per_tensor=None, window=64, stream=None):
+        import torch
+        self.torch = torch
+        self.wl = wl
+        self.H, self.F, self.E, self.k, self.L = wl.hidden, wl.ffn, wl.n_experts, wl.top_k, wl.n_layers
+        self.spt = slots_per_tensor or max(wl.layer_capacity(l) for l in range(wl.n_layers))
+        if stream is None:
+            stream = torch.cuda.current_stream().cuda_stream
+        self.ctx = qec.moe_layer_init(self.H, self.F, self.E, self.k, self.L, self.spt, max_tokens,
+                                      window_tokens=window, stream=stream)
+        self.policy = oracle.PolicyOracle(self.E, window=window, slots_per_tensor=self.spt, n_tensors=3 * self.L)
+        self.tensors = {}
+        bufs = {}
+        for layer in range(self.L):
+            order = wl.seed_order(layer)
+            cap = wl.layer_capacity(layer)
+            for kind in range(3):
+                rows, cols = wl.tensor_shapes[kind]
+                if (rows, cols) not in bufs:
+                    bufs[(rows, cols)] = np.empty((self.E, rows, cols // 32, 18), np.uint8)
+                wl.expert_tensor(layer, kind, out=bufs[(rows, cols)])
+                tid = qec.register_expert_tensor(self.ctx, layer, kind, bufs[(rows, cols)], rows, cols, cap, order,
+                                                 cap)
+                self.tensors[tid] = _LazyExperts(wl, layer, kind)
+                self.policy.add_tensor(tid, cap, order, cap)
+        del bufs
+
+
+def check_sampled_rows(m, layer, x_np, logits_np, y_gpu, idx_gpu, w_gpu, rows):
+    """Parity of selected tokens (rows) of one forward against the oracle:
+    idx of every token bit-exact, and for the sampled tokens x codes, h codes
+    (validated) and y."""
+    T = x_np.shape[0]
+    idx_o, w_o = oracle.topk(logits_np, m.k)
+    assert np.array_equal(idx_gpu, idx_o), "top-k indices differ"
+    np.testing.assert_allclose(w_gpu, w_o, rtol=1e-5, atol=1e-7)
+    rows = np.asarray(sorted(set(int(r) for r in rows)))
+    xs, io, wo = x_np[rows], idx_o[rows], w_o[rows]
+    used = sorted(set(io.ravel().tolist()))
+    g = {e: m.tensor(layer, 0)[e] for e in used}
+    u = {e: m.tensor(layer, 1)[e] for e in used}
+    d = {e: m.tensor(layer, 2)[e] for e in used}
+    y_o, it = oracle.layer(xs, io, wo, g, u, d, m.H, m.F, want_intermediates=True)
+    xq, xd, hq, hd = m.read_debug(T)
+    assert np.array_equal(xq[rows], it["xq"]) and np.array_equal(xd[rows], it["xd"]), "x codes differ"
+    arows = (rows[:, None] * m.k + np.arange(m.k)[None, :]).ravel()
+    n_alt = check_h_codes(hq[arows], hd[arows], it, m.H // 32)
+    y_ref = oracle.down_combine(io, wo, d, hq[arows], hd[arows], m.H, m.F) if n_alt else y_o
+    assert_close(y_gpu[rows], y_ref)
+    return n_alt

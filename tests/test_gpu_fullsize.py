@@ -1,0 +1,176 @@
+"""Parity at the workloads' full sizes, on sampled outputs, in the launch
+configuration the benchmark times (one context per workload, every layer
+registered with its pool seeding):
+
+- decode_b1_resident: 48 layers x 512 experts, batch 1, 40 resident layers +
+  307/512 hot sets; sampled (layer, step) outputs, the miss log of every step;
+- decode_b1_pool25: 128 slots per tensor, 256 decode steps with the
+  promotion pass between steps; the table, stamp and sighting state of every
+  tensor after every step bit-exact against the policy oracle;
+- prefill_t4096: one 4096-token micro-batch through 48 layers (grouped
+  tensor-core GEMM), sampled tokens of sampled layers;
+- large_expert: 36 layers, hidden 2880, 128 experts, top-4, 50% pool;
+  borrow -> prefill 512 / 4096 / 12288 -> return -> decode at 1, 8, 32.
+"""
+import numpy as np
+import pytest
+
+import quantized_expert_cache_gb300 as qec
+import synth
+from gpu_helpers import FullModel, check_sampled_rows
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    qec.build.build()
+    qec.load()
+
+
+def _decode_steps(m, steps, T, check, on_step=None):
+    """Route + forward every layer per step, promotion pass after each step."""
+    for step in range(steps):
+        used = {}
+        for layer in range(m.L):
+            x, lg = m.wl.x(layer, step, T), m.wl.logits(layer, step, T)
+            idx, w = m.route(lg)
+            y = m.forward(layer, x, idx, w)
+            idx_np = idx.cpu().numpy()
+            for kind in range(3):
+                used[layer * 3 + kind] = idx_np.ravel().tolist()
+            if (step, layer) in check:
+                torch.cuda.synchronize()
+                check_sampled_rows(m, layer, x, lg, y.cpu().numpy(), idx_np, w.cpu().numpy(), range(T))
+        if on_step:
+            on_step(step, used)
+        qec.cache_step(m.ctx, T)
+        m.policy.step(T, used)
+
+
+def test_decode_b1_resident_full_size():
+    wl = synth.WORKLOADS["decode_b1_resident"]
+    m = FullModel(wl, max_tokens=1)
+    try:
+        rng = np.random.default_rng(0)
+        check = {(int(s), int(l)) for s, l in zip(rng.integers(0, 12, 6), rng.integers(0, 48, 6))}
+        check |= {(0, 0), (3, 7), (5, 47)}
+
+        def misses(step, used):
+            # the miss log of the step, before the promotion pass reads it, is
+            # compared through the statistics afterwards
+            pass
+
+        _decode_steps(m, 12, 1, check, misses)
+        st = qec.moe_stats(m.ctx)
+        assert st["misses"] == m.policy.stats["misses"] and st["admissions"] == m.policy.stats["admissions"]
+        for tid in (0, 5, 21, 23, 24, 140):
+            snap = qec.moe_cache_snapshot(m.ctx, tid, m.E, m.spt)
+            o = m.policy.snapshot(tid)
+            assert snap["slot_of"].tolist() == o["slot_of"]
+            assert np.array_equal(snap["tbl"], m.expected_tbl(tid))
+    finally:
+        m.close()
+
+
+def test_decode_b1_pool25_state_every_step():
+    wl = synth.WORKLOADS["decode_b1_pool25"]
+    m = FullModel(wl, max_tokens=1)
+    try:
+        check = {(0, 0), (40, 13), (128, 30), (255, 47)}
+
+        def after(step, used):
+            pass
+
+        steps = wl.phases[0][2]
+        for step in range(steps):
+            used = {}
+            for layer in range(m.L):
+                x, lg = m.wl.x(layer, step, 1), m.wl.logits(layer, step, 1)
+                idx, w = m.route(lg)
+                y = m.forward(layer, x, idx, w)
+                idx_np = idx.cpu().numpy()
+                for kind in range(3):
+                    used[layer * 3 + kind] = idx_np.ravel().tolist()
+                if (step, layer) in check:
+                    torch.cuda.synchronize()
+                    check_sampled_rows(m, layer, x, lg, y.cpu().numpy(), idx_np, w.cpu().numpy(), [0])
+            qec.cache_step(m.ctx, 1)
+            m.policy.step(1, used)
+            for tid in range(3 * m.L):
+                snap = qec.moe_cache_snapshot(m.ctx, tid, m.E, m.spt)
+                o = m.policy.snapshot(tid)
+                assert snap["slot_of"].tolist() == o["slot_of"], (step, tid)
+                assert snap["last_seen"].tolist() == o["last_seen"], (step, tid)
+                assert snap["stamps"].tolist() == o["stamp"], (step, tid)
+                assert np.array_equal(snap["tbl"], m.expected_tbl(tid)), (step, tid)
+        st = qec.moe_stats(m.ctx)
+        assert st["admissions"] == m.policy.stats["admissions"] > 0
+        assert st["evictions"] == m.policy.stats["evictions"] > 0
+    finally:
+        m.close()
+
+
+def test_prefill_t4096_full_size_sampled():
+    wl = synth.WORKLOADS["prefill_t4096"]
+    T = 4096
+    m = FullModel(wl, max_tokens=T)
+    try:
+        rng = np.random.default_rng(1)
+        for layer in range(m.L):
+            x, lg = m.wl.x(layer, 0, T), m.wl.logits(layer, 0, T)
+            idx, w = m.route(lg)
+            y = m.forward(layer, x, idx, w)
+            if layer in (0, 17, 47):
+                torch.cuda.synchronize()
+                rows = [0, T - 1] + rng.integers(0, T, 6).tolist()
+                check_sampled_rows(m, layer, x, lg, y.cpu().numpy(), idx.cpu().numpy(), w.cpu().numpy(), rows)
+                keys = qec.miss_drain(m.ctx)
+                idx_np = idx.cpu().numpy()
+                used = sorted(set(idx_np.ravel().tolist()))
+                expect = sorted((layer * 3 + kind) << 12 | e for kind in range(3) for e in used
+                                if m.policy.snapshot(layer * 3 + kind)["slot_of"][e] < 0)
+                assert keys.tolist() == expect
+            else:
+                qec.miss_drain(m.ctx)
+    finally:
+        m.close()
+
+
+def test_large_expert_borrow_prefill_return_decode():
+    wl = synth.WORKLOADS["large_expert"]
+    m = FullModel(wl, max_tokens=12288)
+    try:
+        rng = np.random.default_rng(2)
+        n_borrow = 3 * m.L * 8  # 8 slots of every tensor lent to the prompt pass
+        qec.moe_pool_borrow(m.ctx, n_borrow)
+        m.policy.borrow(n_borrow)
+        for phase, (label, T, steps) in enumerate(wl.phases):
+            if label == "decode" and m.policy.n_lent:
+                qec.moe_pool_return(m.ctx)
+                m.policy.give_back()
+            for step in range(min(steps, 3 if label == "decode" else 1)):
+                used = {}
+                for layer in range(m.L):
+                    x, lg = m.wl.x(layer, step, T, phase), m.wl.logits(layer, step, T, phase)
+                    idx, w = m.route(lg)
+                    y = m.forward(layer, x, idx, w)
+                    idx_np = idx.cpu().numpy()
+                    for kind in range(3):
+                        used[layer * 3 + kind] = idx_np.ravel().tolist()
+                    if layer in (0, 35) and step == 0:
+                        torch.cuda.synchronize()
+                        rows = sorted(set([0, T - 1] + rng.integers(0, T, 3).tolist()))
+                        check_sampled_rows(m, layer, x, lg, y.cpu().numpy(), idx_np, w.cpu().numpy(), rows)
+                qec.cache_step(m.ctx, T)
+                m.policy.step(T, used)
+                for tid in (0, 1, 2, 50, 105, 107):
+                    snap = qec.moe_cache_snapshot(m.ctx, tid, m.E, m.spt)
+                    o = m.policy.snapshot(tid)
+                    assert snap["slot_of"].tolist() == o["slot_of"], (phase, step, tid)
+                    assert snap["stamps"].tolist() == o["stamp"], (phase, step, tid)
+                    assert np.array_equal(snap["tbl"], m.expected_tbl(tid)), (phase, step, tid)
+    finally:
+        m.close()
