@@ -575,11 +575,15 @@ template <int NT, class Prefetch>
 __device__ __forceinline__ void gu_chunk(const FusedParams &p, int c0, int nt, int rg, int rloc, int sub, int lane,
                                          int warp, const uint4 *qg, const uint4 *qu, const __half *dg,
                                          const __half *du, int8_t *xq_s, BlockScale *xds_s, float (*sh_h)[32],
-                                         const int *s_asg, Prefetch &&prefetch) {
+                                         const int *s_asg, Prefetch &&prefetch, bool xpre) {
     const GemvParams &g = p.g;
     const int H = g.H, F = g.F, k = g.k;
     const int nbx = H / kBlock, rgs = F / kBlock;
     constexpr int XB = NT == 1 ? 12 : kXBatch;  // x blocks per warp loaded ahead of the weights
+    // xpre: every token's x is already quantized in xq_s (row = token id)
+    int xrow[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) xrow[t] = xpre ? (t < nt ? s_asg[c0 + t] / k : 0) : t;
     float ag[NT], au[NT];
 #pragma unroll
     for (int t = 0; t < NT; ++t) ag[t] = au[t] = 0.0f;
@@ -588,7 +592,7 @@ __device__ __forceinline__ void gu_chunk(const FusedParams &p, int c0, int nt, i
         // x of the chunk is requested before the weights, so the tiny x loads
         // are not queued behind the item's weight stream
         float xv[XB];
-        if (bb == 0) {
+        if (bb == 0 && !xpre) {
 #pragma unroll
             for (int i = 0; i < XB; ++i) {
                 const int q = warp + i * kWarps;
@@ -611,8 +615,8 @@ __device__ __forceinline__ void gu_chunk(const FusedParams &p, int c0, int nt, i
                 su[i] = ld_scale(du + b);
             }
         }
-        if (bb == 0) {
-            prefetch();  // the down item's weights, behind the gate/up weights
+        if (bb == 0) prefetch();  // the down item's weights, behind the gate/up weights
+        if (bb == 0 && !xpre) {
             // quantize the x rows of this chunk while the weights fly
             for (int q0 = warp; q0 < nblk; q0 += kWarps * XB) {
                 if (q0 != warp) {
@@ -652,9 +656,9 @@ __device__ __forceinline__ void gu_chunk(const FusedParams &p, int c0, int nt, i
 #pragma unroll
                 for (int t = 0; t < NT; ++t) {
                     if (NT == 1 || t < nt) {
-                        const int4 *xa = (const int4 *)(xq_s + (size_t)t * H + (size_t)b * kBlock);
+                        const int4 *xa = (const int4 *)(xq_s + (size_t)xrow[t] * H + (size_t)b * kBlock);
                         const int4 x0 = xa[0], x1 = xa[1];
-                        const BlockScale xs = xds_s[(size_t)t * nbx + b];
+                        const BlockScale xs = xds_s[(size_t)xrow[t] * nbx + b];
                         ag[t] += (float)q4_block_dot(wg4[i], x0, x1, xs.s) * (sg[i] * xs.d);
                         au[t] += (float)q4_block_dot(wu4[i], x0, x1, xs.s) * (su[i] * xs.d);
                     }
@@ -796,8 +800,38 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t step_clock = *g.cv.clock + (uint32_t)g.n_tokens;
 
+    // Small batches: every token's x is quantized into shared memory first
+    // (it does not depend on the routing), overlapping the plan's loads and
+    // ahead of every weight request.
+    const bool xpre = g.n_tokens <= kMaxChunk;
+    if (xpre) {
+        int8_t *xq_s0 = (int8_t *)dsm;
+        BlockScale *xds_s0 = (BlockScale *)(dsm + kMaxChunk * H);
+        const int nblk = g.n_tokens * nbx;
+        for (int q0 = warp; q0 < nblk; q0 += kWarps * 12) {
+            float xv[12];
+#pragma unroll
+            for (int i = 0; i < 12; ++i) {
+                const int q = q0 + i * kWarps;
+                if (q < nblk) xv[i] = __ldg(p.x + (size_t)q * kBlock + lane);
+            }
+#pragma unroll
+            for (int i = 0; i < 12; ++i) {
+                const int q = q0 + i * kWarps;
+                if (q < nblk) quantize_block_warp(xv[i], lane, xq_s0 + (size_t)q * kBlock, xds_s0 + q);
+            }
+        }
+        // (the plan's barriers order these shared-memory writes before use)
+    }
     fused_plan(p, s_e, s_uniq, s_off, s_asg, &s_nu, s_cnt, s_first);
     const int nu = s_nu;
+    if (xpre && blockIdx.x == 0) {
+        // the context's copy of the quantized x (for inspection)
+        const int8_t *xq_s0 = (const int8_t *)dsm;
+        const BlockScale *xds_s0 = (const BlockScale *)(dsm + kMaxChunk * H);
+        for (int i = threadIdx.x; i < g.n_tokens * H; i += blockDim.x) g.xq_out[i] = xq_s0[i];
+        for (int i = threadIdx.x; i < g.n_tokens * nbx; i += blockDim.x) g.xds_out[i] = xds_s0[i];
+    }
 
     // This CTA's first down item (codes + scales of DROWS rows) is copied
     // into shared memory with cp.async, issued right behind the CTA's first
@@ -855,7 +889,7 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
             for (int c0 = a0; c0 < a1; c0 += NT) {
                 const int nt = min(NT, a1 - c0);
                 gu_chunk<NT>(p, c0, nt, rg, rloc, sub, lane, warp, qg, qu, dg, du, xq_s, xds_s, sh_h, s_asg,
-                             issue_prefetch);
+                             issue_prefetch, xpre);
             }
             // publish this row block of expert e
             __threadfence();
