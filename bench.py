@@ -80,7 +80,7 @@ class ClockSampler:
             os.close(fd)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -221,9 +221,10 @@ def run_ours(args):
     sptr = stream.cuda_stream
 
     def layers():
+        # router top-k + expert FFN per layer (one launch per layer for
+        # small batches: every CTA routes the tokens itself)
         for l in range(L):
-            qec.route_topk(ctx, lin[l], T, E, k, idx[l], w[l], sptr)
-            qec.moe_ffn_forward(ctx, l, xin[l], T, idx[l], w[l], y[l], sptr)
+            qec.moe_ffn_forward_routed(ctx, l, xin[l], lin[l], T, idx[l], w[l], y[l], sptr)
 
     graph = None
     if not args.no_graph:
@@ -237,7 +238,7 @@ def run_ours(args):
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=stream):
             layers()
-    launches_per_step = L * 4 + 1  # top-k, plan, gate/up, down per layer + the table update kernel
+    launches_per_step = L * (1 if T * k <= 256 else 4) + 1  # per layer + the table update kernel
 
     def step(s, host_io=None):
         with torch.cuda.stream(stream):
@@ -256,13 +257,16 @@ def run_ours(args):
             with torch.cuda.stream(stream):
                 host_io[2].copy_(y, non_blocking=True)
 
+    # the clock sampler starts before the warm-up so that nvidia-smi's own
+    # start-up does not fall inside the timed region
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(1.0)
     for s in range(args.warmup):
         step(s)
     stream.synchronize()
     barrier()
     torch.cuda.synchronize()
-    clocks = ClockSampler(local)
-    clocks.start()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
     for s in range(args.warmup, S):

@@ -149,6 +149,16 @@ int moe_ffn_forward(moe_ctx *ctx, int layer, const float *d_x, int n_tokens, con
                     const float *d_w, float *d_y, void *stream);
 
 /*
+ * route_topk followed by moe_ffn_forward, as one call: same results (d_idx
+ * and d_w are written as route_topk writes them), and for small batches
+ * (n_tokens <= 32, n_tokens*k <= 256) one kernel launch in which every CTA
+ * routes the tokens itself.  d_logits: fp32 [n_tokens][E] device.
+ * Asynchronous; `stream` as in moe_ffn_forward.  Errors: as the two calls.
+ */
+int moe_ffn_forward_routed(moe_ctx *ctx, int layer, const float *d_x, const float *d_logits, int n_tokens,
+                           int32_t *d_idx, float *d_w, float *d_y, void *stream);
+
+/*
  * Promotion pass between steps (Zapdev-labs/a6000-custom-kernels:
  * ggml_cuda_moe_cache_step between graphs, never captured; neurall/llama.cpp:
  * admission after repeated use within the last 64 tokens).  Waits (host

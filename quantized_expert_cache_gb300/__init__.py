@@ -49,6 +49,7 @@ SIGNATURES = {
     "register_expert_tensor": (_i32, [_vp, _i32, _i32, _vp, _i32, _i32, _i32, _vp, _i32, ctypes.POINTER(_i32)]),
     "route_topk": (_i32, [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp]),
     "moe_ffn_forward": (_i32, [_vp, _i32, _vp, _i32, _vp, _vp, _vp, _vp]),
+    "moe_ffn_forward_routed": (_i32, [_vp, _i32, _vp, _vp, _i32, _vp, _vp, _vp, _vp]),
     "cache_step": (_i32, [_vp, _i32]),
     "miss_drain": (_i32, [_vp, _vp, _sz, ctypes.POINTER(_sz)]),
     "moe_pool_borrow": (_i32, [_vp, _i32, ctypes.POINTER(_vp), ctypes.POINTER(_sz)]),
@@ -155,6 +156,11 @@ def route_topk(ctx, logits, n_tokens, n_experts, k, idx, w, stream=None):
 def moe_ffn_forward(ctx, layer, x, n_tokens, idx, w, y, stream=None):
     return _check(ctx, load().moe_ffn_forward(ctx, layer, _dev(x), n_tokens, _dev(idx), _dev(w), _dev(y),
                                               _stream(stream)))
+
+
+def moe_ffn_forward_routed(ctx, layer, x, logits, n_tokens, idx, w, y, stream=None):
+    return _check(ctx, load().moe_ffn_forward_routed(ctx, layer, _dev(x), _dev(logits), n_tokens, _dev(idx), _dev(w),
+                                                     _dev(y), _stream(stream)))
 
 
 def cache_step(ctx, n_tokens):

@@ -45,7 +45,12 @@ struct GemvParams {
 struct FusedParams {
     GemvParams g;
     const float *x;          // [T][H]
-    const int32_t *idx;      // [T][k]
+    const int32_t *idx;      // [T][k] (when logits is null)
+    const float *logits;     // [T][E]: route in-kernel (top-k + softmax) when not null
+    int32_t *idx_out;        // routed: [T][k] written by CTA 0
+    float *w_out;            // routed: [T][k] written by CTA 0
+    int renorm;
+    int pdl;                 // launched with programmatic stream serialization
     unsigned *done_gu;       // [E]: published gate/up row blocks per expert, zero between launches
     unsigned *exit_count;    // [1]
     int *error;

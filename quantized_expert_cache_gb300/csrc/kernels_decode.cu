@@ -499,16 +499,85 @@ __host__ __device__ inline size_t fused_stage_bytes(int H, int F) {
     return ((gu > dn ? gu : dn) + 15) / 16 * 16;
 }
 
-__device__ void fused_plan(const FusedParams &p, int *s_e, int *s_uniq, int *s_off, int *s_asg, int *s_nu,
-                           int *s_cnt, int *s_first) {
-    const int A = p.g.n_tokens * p.g.k;
-    for (int a = threadIdx.x; a < A; a += blockDim.x) {
-        int e = p.idx[a];
-        if (e < 0 || e >= p.g.cv.E) {
-            atomicOr(p.error, 1);
-            e = 0;
+// Top-k of one logits row by one warp, without a taken mask: round j picks
+// the largest (value, -index) below the previous pick in the order (value
+// desc, index asc), so ties go to the lower index.  Lane j < k returns pick
+// j and its routing weight (softmax over the k picks, or over all E).
+__device__ __forceinline__ void warp_topk_row(const float *l, int E, int k, int renorm, int lane, int &my_e,
+                                              float &my_w) {
+    float lv = INFINITY;
+    int le = -1;
+    my_e = 0;
+    float my_v = -INFINITY;
+    for (int j = 0; j < k; ++j) {
+        float bv = -INFINITY;
+        int bi = 0x7fffffff;
+        for (int e = lane; e < E; e += 32) {
+            const float v = l[e];
+            const bool after = v < lv || (v == lv && e > le);
+            if (after && (bi == 0x7fffffff || v > bv)) {
+                bv = v;
+                bi = e;
+            }
         }
-        s_e[a] = e;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (oi != 0x7fffffff && (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi))) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+        lv = bv;
+        le = bi;
+        if (lane == j) {
+            my_e = bi;
+            my_v = bv;
+        }
+    }
+    const float m = __shfl_sync(0xffffffffu, my_v, 0);
+    const float ej = lane < k ? expf(my_v - m) : 0.0f;
+    float den;
+    if (renorm) {
+        den = warp_sum_f(ej);
+    } else {
+        float sacc = 0.0f;
+        for (int e = lane; e < E; e += 32) sacc += expf(l[e] - m);
+        den = warp_sum_f(sacc);
+    }
+    my_w = ej / den;
+}
+
+__device__ void fused_plan(const FusedParams &p, int *s_e, int *s_uniq, int *s_off, int *s_asg, int *s_nu,
+                           int *s_cnt, int *s_first, float *s_w) {
+    const int A = p.g.n_tokens * p.g.k;
+    if (p.logits) {
+        // route in the CTA: one warp per token
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, k = p.g.k, E = p.g.cv.E;
+        for (int t = warp; t < p.g.n_tokens; t += blockDim.x >> 5) {
+            int me;
+            float mw;
+            warp_topk_row(p.logits + (size_t)t * E, E, k, p.renorm, lane, me, mw);
+            if (lane < k) {
+                s_e[t * k + lane] = me;
+                s_w[t * k + lane] = mw;
+                if (blockIdx.x == 0) {
+                    p.idx_out[t * k + lane] = me;
+                    p.w_out[t * k + lane] = mw;
+                }
+            }
+        }
+    } else {
+        for (int a = threadIdx.x; a < A; a += blockDim.x) {
+            int e = p.idx[a];
+            if (e < 0 || e >= p.g.cv.E) {
+                atomicOr(p.error, 1);
+                e = 0;
+            }
+            s_e[a] = e;
+            s_w[a] = p.g.w[a];
+        }
     }
     __syncthreads();
     int n_first = 0;
@@ -791,6 +860,7 @@ template <int LD, int NT>
 __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
     __shared__ int s_e[kMaxFusedA], s_uniq[kMaxFusedA], s_off[kMaxFusedA + 1], s_asg[kMaxFusedA],
         s_cnt[kMaxFusedA], s_first[kMaxFusedA];
+    __shared__ float s_w[kMaxFusedA];
     __shared__ int s_nu, s_last;
     __shared__ float sh_h[kMaxChunk][32];
     extern __shared__ __align__(16) uint8_t dsm[];
@@ -800,6 +870,12 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t step_clock = *g.cv.clock + (uint32_t)g.n_tokens;
 
+    if (p.pdl) {
+        // programmatic dependent launch: the previous kernel's writes are
+        // visible after this wait; let the next layer's kernel get scheduled
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        asm volatile("griddepcontrol.launch_dependents;");
+    }
     // Small batches: every token's x is quantized into shared memory first
     // (it does not depend on the routing), overlapping the plan's loads and
     // ahead of every weight request.
@@ -823,7 +899,7 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
         }
         // (the plan's barriers order these shared-memory writes before use)
     }
-    fused_plan(p, s_e, s_uniq, s_off, s_asg, &s_nu, s_cnt, s_first);
+    fused_plan(p, s_e, s_uniq, s_off, s_asg, &s_nu, s_cnt, s_first, s_w);
     const int nu = s_nu;
     if (xpre && blockIdx.x == 0) {
         // the context's copy of the quantized x (for inspection)
@@ -944,7 +1020,7 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
                     float y = 0.0f;
                     for (int j = 0; j < k; ++j) {
                         const size_t a = (size_t)t * k + j;
-                        y += g.w[a] * __ldcg(g.o + a * H + rr);
+                        y += s_w[a] * __ldcg(g.o + a * H + rr);
                     }
                     g.y[(size_t)t * H + rr] = y;
                 }
@@ -1014,11 +1090,13 @@ int launch_fused(const FusedParams &p, int grid, size_t smem, cudaStream_t st, c
     cfg.blockDim = dim3(256);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = p.pdl ? 2 : 1;
     if (ev) record(ev[0], st);
     void *args[] = {(void *)&p};
     cudaError_t e = cudaLaunchKernelExC(&cfg, fused_fn(p.g.F, p.g.n_tokens), args);

@@ -75,6 +75,7 @@ struct moe_ctx {
     unsigned *done_gu = nullptr, *exit_count = nullptr;
     size_t fused_smem = 0;
     int fused_blocks = 0;
+    int pdl = 1;  // fused layer kernels use programmatic dependent launch
 
     uint32_t *h_readback = nullptr;  // pinned: count + miss list
     uint32_t *h_stamps = nullptr;    // pinned
@@ -431,8 +432,29 @@ int route_topk(moe_ctx *ctx, const float *d_logits, int n_tokens, int n_experts,
     return MOE_OK;
 }
 
+static int ffn_forward_impl(moe_ctx *ctx, int layer, const float *d_x, int n_tokens, const int32_t *d_idx,
+                            const float *d_w, float *d_y, void *stream, const float *d_logits, int32_t *idx_out,
+                            float *w_out);
+
 int moe_ffn_forward(moe_ctx *ctx, int layer, const float *d_x, int n_tokens, const int32_t *d_idx, const float *d_w,
                     float *d_y, void *stream) {
+    return ffn_forward_impl(ctx, layer, d_x, n_tokens, d_idx, d_w, d_y, stream, nullptr, nullptr, nullptr);
+}
+
+int moe_ffn_forward_routed(moe_ctx *ctx, int layer, const float *d_x, const float *d_logits, int n_tokens,
+                           int32_t *d_idx, float *d_w, float *d_y, void *stream) {
+    if (!ctx) return fail(nullptr, MOE_ERR_ARG, "null ctx");
+    if (n_tokens > 0 && (!d_logits || !d_idx || !d_w)) return fail(ctx, MOE_ERR_ARG, "routed forward: null pointer");
+    if (n_tokens > 0 && n_tokens <= 32 && n_tokens * ctx->k <= 256 && ctx->fused_blocks > 0)
+        return ffn_forward_impl(ctx, layer, d_x, n_tokens, d_idx, d_w, d_y, stream, d_logits, d_idx, d_w);
+    int rc = route_topk(ctx, d_logits, n_tokens, ctx->E, ctx->k, d_idx, d_w, stream);
+    if (rc) return rc;
+    return ffn_forward_impl(ctx, layer, d_x, n_tokens, d_idx, d_w, d_y, stream, nullptr, nullptr, nullptr);
+}
+
+static int ffn_forward_impl(moe_ctx *ctx, int layer, const float *d_x, int n_tokens, const int32_t *d_idx,
+                            const float *d_w, float *d_y, void *stream, const float *d_logits, int32_t *idx_out,
+                            float *w_out) {
     if (!ctx) return fail(nullptr, MOE_ERR_ARG, "null ctx");
     if (layer < 0 || layer >= ctx->cfg.n_layers || n_tokens < 0 || n_tokens > ctx->M)
         return fail(ctx, MOE_ERR_ARG, "forward: bad layer or n_tokens (> max_tokens?)");
@@ -489,6 +511,11 @@ int moe_ffn_forward(moe_ctx *ctx, int layer, const float *d_x, int n_tokens, con
         fp.done_gu = ctx->done_gu;
         fp.exit_count = ctx->exit_count;
         fp.error = ctx->d_error;
+        fp.logits = d_logits;
+        fp.idx_out = idx_out;
+        fp.w_out = w_out;
+        fp.renorm = ctx->cfg.renorm_topk;
+        fp.pdl = ctx->pdl;
         const int items = U * std::max(ctx->F / 32, ctx->n_counters);
         const int grid = std::min(items, ctx->fused_blocks);
         const cudaEvent_t *ev = nullptr;

@@ -251,3 +251,29 @@ def test_probe_host_read_and_not_pinned():
     with pytest.raises(qec.MoeError) as ei:
         qec.moe_probe_host_read(pageable.ctypes.data, pageable.nbytes, iters=1)
     assert ei.value.code == -4
+
+
+@pytest.mark.parametrize("H,F,E,k,T", [(2048, 1152, 512, 8, 1), (512, 384, 64, 4, 3), (640, 1440, 128, 4, 8),
+                                       (512, 384, 128, 4, 32), (256, 512, 8, 2, 40)])
+def test_routed_forward_matches_route_then_forward(H, F, E, k, T):
+    m = Model(H=H, F=F, E=E, k=k, L=1, capacity=E // 2, max_tokens=T, zipf_s=0.8)
+    try:
+        x, lg = m.wl.x(0, 4, T), m.wl.logits(0, 4, T)
+        lg[0, :4] = 1.5  # ties inside the top-k
+        idx_ref, w_ref = m.route(lg)
+        y_ref = m.forward(0, x, idx_ref, w_ref)
+        torch.cuda.synchronize()
+        y_ref = y_ref.cpu().numpy()
+        qec.miss_drain(m.ctx)
+        d_x, d_lg = m.dev(x), m.dev(lg)
+        idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+        w = torch.empty((T, k), device="cuda")
+        y = torch.empty((T, H), device="cuda")
+        qec.moe_ffn_forward_routed(m.ctx, 0, d_x, d_lg, T, idx, w, y)
+        torch.cuda.synchronize()
+        assert torch.equal(idx, idx_ref)
+        np.testing.assert_allclose(w.cpu().numpy(), w_ref.cpu().numpy(), rtol=1e-6, atol=1e-8)
+        check_layer_parity(m, 0, x, lg, y.cpu().numpy(), idx.cpu().numpy(), w.cpu().numpy())
+        np.testing.assert_allclose(y.cpu().numpy(), y_ref, rtol=1e-5, atol=1e-6)
+    finally:
+        m.close()
