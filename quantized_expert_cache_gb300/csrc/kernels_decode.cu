@@ -505,6 +505,7 @@ __host__ __device__ inline size_t fused_stage_bytes(int H, int F) {
 // j and its routing weight (softmax over the k picks, or over all E).
 __device__ __forceinline__ void warp_topk_row(const float *l, int E, int k, int renorm, int lane, int &my_e,
                                               float &my_w) {
+    constexpr int C = 16;  // logits per lane loaded together (one 512-wide chunk per warp)
     float lv = INFINITY;
     int le = -1;
     my_e = 0;
@@ -512,12 +513,21 @@ __device__ __forceinline__ void warp_topk_row(const float *l, int E, int k, int 
     for (int j = 0; j < k; ++j) {
         float bv = -INFINITY;
         int bi = 0x7fffffff;
-        for (int e = lane; e < E; e += 32) {
-            const float v = l[e];
-            const bool after = v < lv || (v == lv && e > le);
-            if (after && (bi == 0x7fffffff || v > bv)) {
-                bv = v;
-                bi = e;
+        for (int e0 = 0; e0 < E; e0 += 32 * C) {
+            float v[C];
+#pragma unroll
+            for (int i = 0; i < C; ++i) {
+                const int e = e0 + lane + 32 * i;
+                v[i] = e < E ? __ldg(l + e) : -INFINITY;
+            }
+#pragma unroll
+            for (int i = 0; i < C; ++i) {
+                const int e = e0 + lane + 32 * i;
+                const bool after = e < E && (v[i] < lv || (v[i] == lv && e > le));
+                if (after && (bi == 0x7fffffff || v[i] > bv)) {
+                    bv = v[i];
+                    bi = e;
+                }
             }
         }
 #pragma unroll
@@ -543,7 +553,16 @@ __device__ __forceinline__ void warp_topk_row(const float *l, int E, int k, int 
         den = warp_sum_f(ej);
     } else {
         float sacc = 0.0f;
-        for (int e = lane; e < E; e += 32) sacc += expf(l[e] - m);
+        for (int e0 = 0; e0 < E; e0 += 32 * C) {
+            float v[C];
+#pragma unroll
+            for (int i = 0; i < C; ++i) {
+                const int e = e0 + lane + 32 * i;
+                v[i] = e < E ? __ldg(l + e) : -INFINITY;
+            }
+#pragma unroll
+            for (int i = 0; i < C; ++i) sacc += e0 + lane + 32 * i < E ? expf(v[i] - m) : 0.0f;
+        }
         den = warp_sum_f(sacc);
     }
     my_w = ej / den;
