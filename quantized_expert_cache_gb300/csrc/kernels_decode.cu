@@ -503,16 +503,24 @@ __host__ __device__ inline size_t fused_stage_bytes(int H, int F) {
 // the largest (value, -index) below the previous pick in the order (value
 // desc, index asc), so ties go to the lower index.  Lane j < k returns pick
 // j and its routing weight (softmax over the k picks, or over all E).
+// Order-preserving unsigned key of a float (-0.0 and +0.0 map to one key).
+__device__ __forceinline__ unsigned fkey(float v) {
+    unsigned u = __float_as_uint(v == 0.0f ? 0.0f : v);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
 __device__ __forceinline__ void warp_topk_row(const float *l, int E, int k, int renorm, int lane, int &my_e,
                                               float &my_w) {
     constexpr int C = 16;  // logits per lane loaded together (one 512-wide chunk per warp)
-    float lv = INFINITY;
+    unsigned lk = 0xffffffffu;  // key of the previous pick (first round: no bound)
     int le = -1;
+    bool first = true;
     my_e = 0;
     float my_v = -INFINITY;
     for (int j = 0; j < k; ++j) {
-        float bv = -INFINITY;
+        unsigned bk = 0;
         int bi = 0x7fffffff;
+        bool have = false;
         for (int e0 = 0; e0 < E; e0 += 32 * C) {
             float v[C];
 #pragma unroll
@@ -523,29 +531,26 @@ __device__ __forceinline__ void warp_topk_row(const float *l, int E, int k, int 
 #pragma unroll
             for (int i = 0; i < C; ++i) {
                 const int e = e0 + lane + 32 * i;
-                const bool after = e < E && (v[i] < lv || (v[i] == lv && e > le));
-                if (after && (bi == 0x7fffffff || v[i] > bv)) {
-                    bv = v[i];
+                const unsigned key = fkey(v[i]);
+                // after the previous pick in the order (value desc, index asc)
+                const bool after = e < E && (first || key < lk || (key == lk && e > le));
+                if (after && (!have || key > bk)) {
+                    bk = key;
                     bi = e;
+                    have = true;
                 }
             }
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (oi != 0x7fffffff && (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi))) {
-                bv = ov;
-                bi = oi;
-            }
-        }
-        lv = bv;
-        le = bi;
-        if (lane == j) {
-            my_e = bi;
-            my_v = bv;
-        }
+        // warp arg-max: largest key, then the lowest index holding it
+        const unsigned mk = __reduce_max_sync(0xffffffffu, have ? bk : 0u);
+        const unsigned cand = (have && bk == mk) ? (unsigned)bi : 0xffffffffu;
+        const int wi = (int)__reduce_min_sync(0xffffffffu, cand);
+        lk = mk;
+        le = wi;
+        first = false;
+        if (lane == j) my_e = wi;
     }
+    if (lane < k) my_v = __ldg(l + my_e);
     const float m = __shfl_sync(0xffffffffu, my_v, 0);
     const float ej = lane < k ? expf(my_v - m) : 0.0f;
     float den;
@@ -571,23 +576,7 @@ __device__ __forceinline__ void warp_topk_row(const float *l, int E, int k, int 
 __device__ void fused_plan(const FusedParams &p, int *s_e, int *s_uniq, int *s_off, int *s_asg, int *s_nu,
                            int *s_cnt, int *s_first, float *s_w) {
     const int A = p.g.n_tokens * p.g.k;
-    if (p.logits) {
-        // route in the CTA: one warp per token
-        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, k = p.g.k, E = p.g.cv.E;
-        for (int t = warp; t < p.g.n_tokens; t += blockDim.x >> 5) {
-            int me;
-            float mw;
-            warp_topk_row(p.logits + (size_t)t * E, E, k, p.renorm, lane, me, mw);
-            if (lane < k) {
-                s_e[t * k + lane] = me;
-                s_w[t * k + lane] = mw;
-                if (blockIdx.x == 0) {
-                    p.idx_out[t * k + lane] = me;
-                    p.w_out[t * k + lane] = mw;
-                }
-            }
-        }
-    } else {
+    if (!p.logits) {
         for (int a = threadIdx.x; a < A; a += blockDim.x) {
             int e = p.idx[a];
             if (e < 0 || e >= p.g.cv.E) {
@@ -895,29 +884,47 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
         asm volatile("griddepcontrol.wait;" ::: "memory");
         asm volatile("griddepcontrol.launch_dependents;");
     }
-    // Small batches: every token's x is quantized into shared memory first
-    // (it does not depend on the routing), overlapping the plan's loads and
-    // ahead of every weight request.
+    // Prologue.  Routed launches: warps 0..T-1 route the tokens (top-k over
+    // the logits) while the remaining warps quantize every token's x (small
+    // batches: x does not depend on the routing); both before any weight
+    // request.
     const bool xpre = g.n_tokens <= kMaxChunk;
-    if (xpre) {
+    const int n_route_warps = !p.logits ? 0 : xpre ? max(1, min(g.n_tokens, kWarps / 2)) : kWarps;
+    if (p.logits && warp < n_route_warps) {
+        const int k_ = g.k, E = g.cv.E;
+        for (int t = warp; t < g.n_tokens; t += n_route_warps) {
+            int me;
+            float mw;
+            warp_topk_row(p.logits + (size_t)t * E, E, k_, p.renorm, lane, me, mw);
+            if (lane < k_) {
+                s_e[t * k_ + lane] = me;
+                s_w[t * k_ + lane] = mw;
+                if (blockIdx.x == 0) {
+                    p.idx_out[t * k_ + lane] = me;
+                    p.w_out[t * k_ + lane] = mw;
+                }
+            }
+        }
+    } else if (xpre) {
         int8_t *xq_s0 = (int8_t *)dsm;
         BlockScale *xds_s0 = (BlockScale *)(dsm + kMaxChunk * H);
         const int nblk = g.n_tokens * nbx;
-        for (int q0 = warp; q0 < nblk; q0 += kWarps * 12) {
+        const int w0 = warp - n_route_warps, nw = kWarps - n_route_warps;
+        for (int q0 = w0; q0 < nblk; q0 += nw * 12) {
             float xv[12];
 #pragma unroll
             for (int i = 0; i < 12; ++i) {
-                const int q = q0 + i * kWarps;
+                const int q = q0 + i * nw;
                 if (q < nblk) xv[i] = __ldg(p.x + (size_t)q * kBlock + lane);
             }
 #pragma unroll
             for (int i = 0; i < 12; ++i) {
-                const int q = q0 + i * kWarps;
+                const int q = q0 + i * nw;
                 if (q < nblk) quantize_block_warp(xv[i], lane, xq_s0 + (size_t)q * kBlock, xds_s0 + q);
             }
         }
-        // (the plan's barriers order these shared-memory writes before use)
     }
+    // (the plan's barriers order these shared-memory writes before any use)
     fused_plan(p, s_e, s_uniq, s_off, s_asg, &s_nu, s_cnt, s_first, s_w);
     const int nu = s_nu;
     if (xpre && blockIdx.x == 0) {
