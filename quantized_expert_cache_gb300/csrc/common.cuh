@@ -54,7 +54,8 @@ __device__ __forceinline__ float warp_sum_f(float v) {
 // fast-math).  An all-zero block (d == 0) gives q = 0.  Lane 0 writes the
 // scale and the code sum.
 __device__ __forceinline__ void quantize_block_warp(float v, int lane, int8_t *q_out, BlockScale *ds_out) {
-    float amax = warp_max(fabsf(v));
+    // max of |v| over the warp: non-negative floats order like their bits
+    const float amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v))));
     float d32 = amax / 127.0f;
     float dd = __half2float(__float2half_rn(d32));
     int q = 0;
@@ -63,7 +64,7 @@ __device__ __forceinline__ void quantize_block_warp(float v, int lane, int8_t *q
         r = fminf(fmaxf(r, -127.0f), 127.0f);
         q = (int)r;
     }
-    int s = warp_sum_i(q);
+    const int s = __reduce_add_sync(0xffffffffu, q);
     q_out[lane] = (int8_t)q;
     if (lane == 0) {
         ds_out->d = dd;

@@ -517,11 +517,33 @@ __device__ __forceinline__ void warp_topk_row(const float *l, int E, int k, int 
     bool first = true;
     my_e = 0;
     float my_v = -INFINITY;
+    // rows of up to 512 logits stay in registers across the k rounds
+    unsigned kr[C];
+    if (E <= 32 * C) {
+#pragma unroll
+        for (int i = 0; i < C; ++i) {
+            const int e = lane + 32 * i;
+            kr[i] = e < E ? fkey(__ldg(l + e)) : 0u;
+        }
+    }
     for (int j = 0; j < k; ++j) {
         unsigned bk = 0;
         int bi = 0x7fffffff;
         bool have = false;
-        for (int e0 = 0; e0 < E; e0 += 32 * C) {
+        if (E <= 32 * C) {
+#pragma unroll
+            for (int i = 0; i < C; ++i) {
+                const int e = lane + 32 * i;
+                const unsigned key = kr[i];
+                const bool after = e < E && (first || key < lk || (key == lk && e > le));
+                if (after && (!have || key > bk)) {
+                    bk = key;
+                    bi = e;
+                    have = true;
+                }
+            }
+        }
+        for (int e0 = 0; E > 32 * C && e0 < E; e0 += 32 * C) {
             float v[C];
 #pragma unroll
             for (int i = 0; i < C; ++i) {
@@ -576,6 +598,57 @@ __device__ __forceinline__ void warp_topk_row(const float *l, int E, int k, int 
 __device__ void fused_plan(const FusedParams &p, int *s_e, int *s_uniq, int *s_off, int *s_asg, int *s_nu,
                            int *s_cnt, int *s_first, float *s_w) {
     const int A = p.g.n_tokens * p.g.k;
+    if (A <= 32) {
+        // one warp: bitonic sort of (expert, assignment) keys, then the
+        // used experts are the positions where the expert changes
+        __syncthreads();  // routing / x prologue writes
+        if (threadIdx.x < 32) {
+            const int lane = threadIdx.x;
+            int e = 0x7fffffff;
+            if (lane < A) {
+                if (p.logits) {
+                    e = s_e[lane];
+                } else {
+                    e = p.idx[lane];
+                    if (e < 0 || e >= p.g.cv.E) {
+                        atomicOr(p.error, 1);
+                        e = 0;
+                    }
+                    s_e[lane] = e;
+                    s_w[lane] = p.g.w[lane];
+                }
+            }
+            unsigned key = lane < A ? ((unsigned)e << 8) | (unsigned)lane : 0xffffffffu;
+#pragma unroll
+            for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+                for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                    const unsigned other = __shfl_xor_sync(0xffffffffu, key, stride);
+                    const bool up = (lane & size) == 0;
+                    const bool lower = (lane & stride) == 0;
+                    const unsigned lo = min(key, other), hi = max(key, other);
+                    key = (lower == up) ? lo : hi;
+                }
+            }
+            const int se = (int)(key >> 8), sa = (int)(key & 0xffu);
+            const int prev = __shfl_up_sync(0xffffffffu, se, 1);
+            const bool head = lane < A && (lane == 0 || prev != se);
+            const unsigned heads = __ballot_sync(0xffffffffu, head);
+            const int u = __popc(heads & ((1u << lane) - 1u)) + (head ? 0 : -1);
+            if (lane < A) s_asg[lane] = sa;
+            if (head) {
+                s_uniq[u] = se;
+                s_off[u] = lane;
+            }
+            if (lane == 0) {
+                const int nu = __popc(heads);
+                s_off[nu] = A;
+                *s_nu = nu;
+            }
+        }
+        __syncthreads();
+        return;
+    }
     if (!p.logits) {
         for (int a = threadIdx.x; a < A; a += blockDim.x) {
             int e = p.idx[a];
