@@ -509,69 +509,58 @@ __device__ __forceinline__ unsigned fkey(float v) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// Top-k of one logits row by one warp.  Each logit is packed with its
+// index into a 64-bit rank r = key(v) << 32 | ~e, so that larger r means
+// (value desc, index asc).  Round j picks the largest r below the previous
+// pick: a local log-depth max over the lane's values, then the warp maximum
+// of the high word and, among the lanes holding it, of the low word.  Lane
+// j < k returns pick j and its routing weight (softmax over the k picks, or
+// over all E logits).
+__device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsigned long long b) {
+    return a > b ? a : b;
+}
+
 __device__ __forceinline__ void warp_topk_row(const float *l, int E, int k, int renorm, int lane, int &my_e,
                                               float &my_w) {
-    constexpr int C = 16;  // logits per lane loaded together (one 512-wide chunk per warp)
-    unsigned lk = 0xffffffffu;  // key of the previous pick (first round: no bound)
-    int le = -1;
-    bool first = true;
+    constexpr int C = 16;  // logits per lane held in registers (one 512-wide chunk per warp)
+    unsigned long long last = ~0ull;  // rank of the previous pick (first round: no bound)
     my_e = 0;
-    float my_v = -INFINITY;
-    // rows of up to 512 logits stay in registers across the k rounds
-    unsigned kr[C];
-    if (E <= 32 * C) {
+    unsigned long long rk[C];
+    const bool resident = E <= 32 * C;
+    if (resident) {
 #pragma unroll
         for (int i = 0; i < C; ++i) {
             const int e = lane + 32 * i;
-            kr[i] = e < E ? fkey(__ldg(l + e)) : 0u;
+            rk[i] = e < E ? ((unsigned long long)fkey(__ldg(l + e)) << 32) | (unsigned)(~(unsigned)e) : 0ull;
         }
     }
     for (int j = 0; j < k; ++j) {
-        unsigned bk = 0;
-        int bi = 0x7fffffff;
-        bool have = false;
-        if (E <= 32 * C) {
+        unsigned long long best = 0ull;
+        for (int e0 = 0; e0 < (resident ? 32 * C : E); e0 += 32 * C) {
+            unsigned long long c[C];
 #pragma unroll
             for (int i = 0; i < C; ++i) {
-                const int e = lane + 32 * i;
-                const unsigned key = kr[i];
-                const bool after = e < E && (first || key < lk || (key == lk && e > le));
-                if (after && (!have || key > bk)) {
-                    bk = key;
-                    bi = e;
-                    have = true;
+                unsigned long long r;
+                if (resident) {
+                    r = rk[i];
+                } else {
+                    const int e = e0 + lane + 32 * i;
+                    r = e < E ? ((unsigned long long)fkey(__ldg(l + e)) << 32) | (unsigned)(~(unsigned)e) : 0ull;
                 }
-            }
-        }
-        for (int e0 = 0; E > 32 * C && e0 < E; e0 += 32 * C) {
-            float v[C];
-#pragma unroll
-            for (int i = 0; i < C; ++i) {
-                const int e = e0 + lane + 32 * i;
-                v[i] = e < E ? __ldg(l + e) : -INFINITY;
+                c[i] = r < last ? r : 0ull;
             }
 #pragma unroll
-            for (int i = 0; i < C; ++i) {
-                const int e = e0 + lane + 32 * i;
-                const unsigned key = fkey(v[i]);
-                // after the previous pick in the order (value desc, index asc)
-                const bool after = e < E && (first || key < lk || (key == lk && e > le));
-                if (after && (!have || key > bk)) {
-                    bk = key;
-                    bi = e;
-                    have = true;
-                }
-            }
+            for (int w = C / 2; w > 0; w >>= 1)
+#pragma unroll
+                for (int i = 0; i < w; ++i) c[i] = umax64(c[i], c[i + w]);
+            best = umax64(best, c[0]);
         }
-        // warp arg-max: largest key, then the lowest index holding it
-        const unsigned mk = __reduce_max_sync(0xffffffffu, have ? bk : 0u);
-        const unsigned cand = (have && bk == mk) ? (unsigned)bi : 0xffffffffu;
-        const int wi = (int)__reduce_min_sync(0xffffffffu, cand);
-        lk = mk;
-        le = wi;
-        first = false;
-        if (lane == j) my_e = wi;
+        const unsigned hi = __reduce_max_sync(0xffffffffu, (unsigned)(best >> 32));
+        const unsigned lo = __reduce_max_sync(0xffffffffu, (unsigned)(best >> 32) == hi ? (unsigned)best : 0u);
+        last = ((unsigned long long)hi << 32) | lo;
+        if (lane == j) my_e = (int)(~lo);
     }
+    float my_v = -INFINITY;
     if (lane < k) my_v = __ldg(l + my_e);
     const float m = __shfl_sync(0xffffffffu, my_v, 0);
     const float ej = lane < k ? expf(my_v - m) : 0.0f;
