@@ -239,6 +239,7 @@ def run_ours(args):
         with torch.cuda.graph(graph, stream=stream):
             layers()
     launches_per_step = L * (1 if T * k <= 256 else 4) + 1  # per layer + the table update kernel
+    used_graph = graph is not None
 
     def step(s, host_io=None):
         with torch.cuda.stream(stream):
@@ -347,7 +348,7 @@ def run_ours(args):
                                f"{[wl.layer_capacity(l) for l in range(L)].count(E)} full layers + "
                                f"{min(wl.layer_capacity(l) for l in range(L))}/{E} hot set on the rest",
                    "l2": "inputs larger than L2: ~1.5 GB of expert weights per step vs 129 MB L2",
-                   "cuda_graph": graph is not None, "parallelism": f"replicas x{world}"},
+                   "cuda_graph": used_graph, "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "kernel": "decode_layer_kernel (fused expert FFN, resident layers)",
                      "achieved": round(achieved, 1),
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),

@@ -91,6 +91,17 @@ struct PrefillLaunch {
     int T, k, H, n_sm;
 };
 
+// Staging of a prefill layer's cold expert tensors into lent pool slots.
+struct StageParams {
+    const uint64_t *tbl;      // [n_tensors][E]
+    uint64_t *etbl;           // [3][E]: effective table rows of the layer
+    const int32_t *n_uniq, *uniq_e;
+    uint64_t *jobs;           // [2 * n_slots]: (source, destination) per staged blob
+    int *n_jobs;
+    uint64_t slot_base, slot_stride;
+    int n_slots, tid0, E;
+};
+
 // One table / slot / stamp write of the promotion pass.
 struct Update {
     uint32_t what;   // 0: tbl[index] = value; 1: slot[index] = value; 2: stamps[index] = value
@@ -110,6 +121,7 @@ size_t fused_smem_bytes(int H, int F);
 int fused_configure(int F, size_t smem, int *blocks_per_sm);
 int launch_fused(const FusedParams &p, int grid, size_t smem, cudaStream_t st, cudaEvent_t const *ev);
 int launch_prefill(const PrefillLaunch &L, cudaStream_t st);
+int launch_stage(const StageParams &p, size_t blob_bytes, int n_sm, cudaStream_t st);
 int gemm_configure();
 int gemm_bn(bool dual);
 int launch_apply_updates(const Update *u, int n, uint64_t *tbl, int32_t *slot, uint32_t *stamps, uint32_t *clock,

@@ -641,6 +641,53 @@ __global__ void combine_kernel(const float *__restrict__ o, const float *__restr
     }
 }
 
+// ---------------------------------------------------------------- staging
+// Cold expert tensors of the layer's used experts are copied once over the
+// host link into the pool slots lent to this prompt pass, and the GEMMs read
+// them from HBM through an effective copy of the layer's three table rows.
+// Assignment is deterministic: used experts ascending, tensors gate/up/down;
+// cold tensors beyond the lent slots stay zero-copy.
+__global__ void stage_plan_kernel(StageParams p) {
+    const int n_uniq = *p.n_uniq;
+    for (int i = threadIdx.x; i < 3 * p.E; i += blockDim.x) p.etbl[i] = p.tbl[(size_t)p.tid0 * p.E + i];
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int n = 0;
+        for (int u = 0; u < n_uniq; ++u) {
+            const int e = p.uniq_e[u];
+            for (int kd = 0; kd < 3; ++kd) {
+                const uint64_t ent = p.tbl[(size_t)(p.tid0 + kd) * p.E + e];
+                if (!(ent & 1ull) || n >= p.n_slots) continue;
+                const uint64_t dst = p.slot_base + (uint64_t)n * p.slot_stride;
+                p.jobs[2 * n] = ent & ~1ull;
+                p.jobs[2 * n + 1] = dst;
+                p.etbl[(size_t)kd * p.E + e] = dst;
+                ++n;
+            }
+        }
+        *p.n_jobs = n;
+    }
+}
+
+// Grid-stride copy of the staging jobs, 128-bit loads from pinned host memory.
+__global__ void __launch_bounds__(256) stage_copy_kernel(const uint64_t *__restrict__ jobs, const int *n_jobs,
+                                                         size_t blob16) {
+    const int nj = *n_jobs;
+    const size_t total = (size_t)nj * blob16;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+        const size_t j = i / blob16, w = i - j * blob16;
+        const uint4 *src = (const uint4 *)(uintptr_t)jobs[2 * j];
+        uint4 *dst = (uint4 *)(uintptr_t)jobs[2 * j + 1];
+        dst[w] = ld_weights(src + w);
+    }
+}
+
+int launch_stage(const StageParams &p, size_t blob_bytes, int n_sm, cudaStream_t st) {
+    stage_plan_kernel<<<1, 256, 0, st>>>(p);
+    stage_copy_kernel<<<n_sm * 8, 256, 0, st>>>(p.jobs, p.n_jobs, blob_bytes / 16);
+    return (int)cudaGetLastError();
+}
+
 int gemm_smem_bytes(bool dual) { return dual ? gemm::Cfg<true>::SMEM : gemm::Cfg<false>::SMEM; }
 int gemm_bn(bool dual) { return dual ? gemm::Cfg<true>::BN : gemm::Cfg<false>::BN; }
 

@@ -71,6 +71,11 @@ struct moe_ctx {
     float *xdT = nullptr, *hdT = nullptr;
     int32_t *tile_off = nullptr;  // [2][U + 1]
     CUtensorMap tm_x{}, tm_h{};
+    // prefill staging of cold experts into lent slots
+    uint64_t *etbl = nullptr;     // [3][E]
+    uint64_t *stage_jobs = nullptr;
+    int *stage_n = nullptr;
+    int stage_cap = 0;
     // fused small-batch layer kernel
     unsigned *done_gu = nullptr, *exit_count = nullptr;
     size_t fused_smem = 0;
@@ -326,6 +331,10 @@ int moe_layer_init(const moe_cfg *cfg, void *cuda_stream, moe_ctx **out) {
         CKI(cudaMalloc(&ctx->hdT, sizeof(float) * AP * (ctx->F / 32)));
         CKI(cudaMemset(ctx->hdT, 0, sizeof(float) * AP * (ctx->F / 32)));
         CKI(cudaMalloc(&ctx->tile_off, sizeof(int32_t) * 2 * (U + 1)));
+        CKI(cudaMalloc(&ctx->etbl, sizeof(uint64_t) * 3 * E));
+        ctx->stage_cap = 3 * E;
+        CKI(cudaMalloc(&ctx->stage_jobs, sizeof(uint64_t) * 2 * ctx->stage_cap));
+        CKI(cudaMalloc(&ctx->stage_n, sizeof(int)));
         if (make_tmap(ctx, &ctx->tm_x, ctx->xs16, AP, ctx->H, (uint32_t)moe::gemm_bn(true)) ||
             make_tmap(ctx, &ctx->tm_h, ctx->hq16, AP, ctx->F, (uint32_t)moe::gemm_bn(false)))
             return cleanup_fail(MOE_ERR_CUDA);
@@ -576,8 +585,29 @@ static int ffn_forward_impl(moe_ctx *ctx, int layer, const float *d_x, int n_tok
         g.error = ctx->d_error;
         L.gu = g;
         L.gu.tile_off = L.tiling.tile_off_gu;
-        L.gu.tbl[0] = ctx->d_tbl + (size_t)(layer * 3 + 0) * ctx->E;
-        L.gu.tbl[1] = ctx->d_tbl + (size_t)(layer * 3 + 1) * ctx->E;
+        // with pool slots lent to this prompt pass, the layer's cold expert
+        // tensors are staged there once and read from HBM by the GEMMs
+        const uint64_t *rows = ctx->d_tbl + (size_t)(layer * 3) * ctx->E;
+        if (ctx->n_lent > 0) {
+            const int nt = ctx->n_tensors, G = nt * ctx->spt;
+            moe::StageParams sp{};
+            sp.tbl = ctx->d_tbl;
+            sp.etbl = ctx->etbl;
+            sp.n_uniq = gp.n_uniq;
+            sp.uniq_e = gp.uniq_e;
+            sp.jobs = ctx->stage_jobs;
+            sp.n_jobs = ctx->stage_n;
+            sp.slot_base = (uint64_t)(uintptr_t)(ctx->arena + (size_t)(G - ctx->n_lent) * ctx->stride);
+            sp.slot_stride = ctx->stride;
+            sp.n_slots = std::min(ctx->n_lent, ctx->stage_cap);
+            sp.tid0 = layer * 3;
+            sp.E = ctx->E;
+            rc = moe::launch_stage(sp, ctx->blob, ctx->n_sm, st);
+            if (rc) return fail(ctx, MOE_ERR_CUDA, "stage launch failed");
+            rows = ctx->etbl;
+        }
+        L.gu.tbl[0] = rows + 0 * (size_t)ctx->E;
+        L.gu.tbl[1] = rows + 1 * (size_t)ctx->E;
         L.gu.a_scaleT = ctx->xdT;
         L.gu.rows = ctx->F;
         L.gu.K = H;
@@ -587,7 +617,7 @@ static int ffn_forward_impl(moe_ctx *ctx, int layer, const float *d_x, int n_tok
         L.gu.hds = ctx->hds;
         L.dn = g;
         L.dn.tile_off = L.tiling.tile_off_dn;
-        L.dn.tbl[0] = ctx->d_tbl + (size_t)(layer * 3 + 2) * ctx->E;
+        L.dn.tbl[0] = rows + 2 * (size_t)ctx->E;
         L.dn.tbl[1] = nullptr;
         L.dn.a_scaleT = ctx->hdT;
         L.dn.rows = H;
@@ -888,6 +918,9 @@ void moe_destroy(moe_ctx *ctx) {
     cudaFree(ctx->hdT);
     cudaFree(ctx->tile_off);
     cudaFree(ctx->done_gu);
+    cudaFree(ctx->etbl);
+    cudaFree(ctx->stage_jobs);
+    cudaFree(ctx->stage_n);
     if (ctx->h_readback) cudaFreeHost(ctx->h_readback);
     if (ctx->h_stamps) cudaFreeHost(ctx->h_stamps);
     if (ctx->h_upd) cudaFreeHost(ctx->h_upd);

@@ -57,13 +57,7 @@ def test_decode_b1_resident_full_size():
         rng = np.random.default_rng(0)
         check = {(int(s), int(l)) for s, l in zip(rng.integers(0, 12, 6), rng.integers(0, 48, 6))}
         check |= {(0, 0), (3, 7), (5, 47)}
-
-        def misses(step, used):
-            # the miss log of the step, before the promotion pass reads it, is
-            # compared through the statistics afterwards
-            pass
-
-        _decode_steps(m, 12, 1, check, misses)
+        _decode_steps(m, 12, 1, check)
         st = qec.moe_stats(m.ctx)
         assert st["misses"] == m.policy.stats["misses"] and st["admissions"] == m.policy.stats["admissions"]
         for tid in (0, 5, 21, 23, 24, 140):
@@ -80,10 +74,6 @@ def test_decode_b1_pool25_state_every_step():
     m = FullModel(wl, max_tokens=1)
     try:
         check = {(0, 0), (40, 13), (128, 30), (255, 47)}
-
-        def after(step, used):
-            pass
-
         steps = wl.phases[0][2]
         for step in range(steps):
             used = {}

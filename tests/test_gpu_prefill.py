@@ -61,3 +61,34 @@ def test_prefill_repeat_is_deterministic():
         assert torch.equal(y1, y2)
     finally:
         m.close()
+
+
+@pytest.mark.parametrize("n_borrow", [2, 7, 30])
+def test_prefill_with_lent_slots_stages_cold_experts(n_borrow):
+    """With pool slots lent to the prompt pass, the layer's cold expert
+    tensors are staged into them (as many as fit) and read from HBM; the
+    result is unchanged and the miss log still lists every cold read."""
+    m = Model(H=512, F=384, E=16, k=2, L=2, capacity=8, max_tokens=600, zipf_s=0.5, slots_per_tensor=8)
+    try:
+        qec.moe_pool_borrow(m.ctx, n_borrow)
+        m.policy.borrow(n_borrow)
+        for layer in range(2):
+            T = 600
+            x, lg = m.wl.x(layer, 5, T), m.wl.logits(layer, 5, T)
+            idx, w = m.route(lg)
+            y = m.forward(layer, x, idx, w)
+            torch.cuda.synchronize()
+            idx_np = idx.cpu().numpy()
+            check_layer_parity(m, layer, x, lg, y.cpu().numpy(), idx_np, w.cpu().numpy())
+            used = sorted(set(idx_np.ravel().tolist()))
+            expect = sorted(((layer * 3 + kd) << 12) | e for kd in range(3) for e in used
+                            if m.policy.snapshot(layer * 3 + kd)["slot_of"][e] < 0)
+            assert qec.miss_drain(m.ctx).tolist() == expect
+        qec.moe_pool_return(m.ctx)
+        m.policy.give_back()
+        for tid in range(6):
+            snap = qec.moe_cache_snapshot(m.ctx, tid, m.E, m.spt)
+            assert snap["slot_of"].tolist() == m.policy.snapshot(tid)["slot_of"]
+            assert np.array_equal(snap["tbl"], m.expected_tbl(tid))
+    finally:
+        m.close()
