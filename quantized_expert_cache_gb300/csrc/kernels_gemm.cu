@@ -42,9 +42,10 @@ namespace gemm {
 
 constexpr int BM = 128;
 constexpr int BK = 64;
-constexpr int NWARPS = 10;
+constexpr int NWARPS = 14;
 constexpr int NTHREADS = NWARPS * 32;
 constexpr int W_TMA = 0, W_MMA = 1, W_CONV = 2, W_EPI = 6;
+constexpr int N_EPI = 8;  // two epilogue warps per TMEM lane quarter, each owning half of the token columns
 constexpr long long kTimeoutCycles = 4000000000ll;
 
 template <bool DUAL>
@@ -279,12 +280,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full0 + 8 * s, 1 + 4);   // TMA expect-tx arrive + 4 converter warps
-            mbar_init(empty0 + 8 * s, 1 + 4);  // MMA commit + 4 epilogue warps
+            mbar_init(full0 + 8 * s, 1 + 4);       // TMA expect-tx arrive + 4 converter warps
+            mbar_init(empty0 + 8 * s, 1 + N_EPI);  // MMA commit + the epilogue warps
         }
         for (int j = 0; j < NTBUF; ++j) {
             mbar_init(tfull0 + 8 * j, 1);
-            mbar_init(tempty0 + 8 * j, 4);
+            mbar_init(tempty0 + 8 * j, N_EPI);
         }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -431,8 +432,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         cp_wait<0>();
     } else {
-        // epilogue: TMEM lane quarter = warp % 4; thread = weight row
+        // epilogue: TMEM lane quarter = warp % 4 (thread = weight row), half =
+        // which BN/2 token columns this warp owns
         const int quarter = warp & 3;
+        const int half = (warp - W_EPI) >> 2;
+        constexpr int HC = BN / 2;  // token columns per epilogue warp
         const int r = quarter * 32 + lane;
         int qc = 0, it = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
@@ -440,13 +444,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             decode_tile(t, p.tile_off, n_uniq, p.uniq_off, BN, u, rt, tt);
             const int row = rt * BM + r;
             const bool vrow = row < p.rows;
-            const int pos0 = p.uniq_off[u] + tt * BN;
+            const int pos0 = p.uniq_off[u] + tt * BN + half * HC;
             const int pos_end = p.uniq_off[u + 1];
-            float acc[NA][BN];
+            float acc[NA][HC];
 #pragma unroll
             for (int a = 0; a < NA; ++a)
 #pragma unroll
-                for (int c = 0; c < BN; ++c) acc[a][c] = 0.0f;
+                for (int c = 0; c < HC; ++c) acc[a][c] = 0.0f;
             for (int kt = 0; kt < nkt; ++kt, ++it) {
                 const int slot = it % STAGES;
                 const uint8_t *st = slot_ptr(slot);
@@ -459,27 +463,30 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                 for (int a = 0; a < NA; ++a)
                     wsc[a] = *(const __half2 *)(st + NA * C::A_BYTES + C::B_BYTES + (a * BM + r) * 4);
-                const float *asc = (const float *)(st + NA * C::A_BYTES + C::B_BYTES + C::WS_BYTES);
+                const float *asc = (const float *)(st + NA * C::A_BYTES + C::B_BYTES + C::WS_BYTES) + half * HC;
                 for (int blk = 0; blk < 2; ++blk, ++qc) {
                     const int j = qc % NTBUF;
                     if (lane == 0) ok = mbar_wait(tfull0 + 8 * j, (uint32_t)(qc / NTBUF) & 1u, abort_flag, p.error, 32);
                     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                     if (!ok) goto epi_done;
                     tc_fence_after();
-                    const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(j * C::TBUF);
+                    const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(j * C::TBUF + half * HC);
                     const float *dq = asc + blk * BN;
 #pragma unroll
                     for (int a = 0; a < NA; ++a) {
+                        // up to 32 columns loaded per wait
+                        constexpr int LC = HC < 32 ? HC : 32;
                         const float dw = blk ? __high2float(wsc[a]) : __low2float(wsc[a]);
 #pragma unroll
-                        for (int c0 = 0; c0 < BN; c0 += 16) {
-                            float pv[16];
-                            tmem_ld16(tb + (uint32_t)(a * BN + c0), pv);
+                        for (int cb = 0; cb < HC; cb += LC) {
+                            float pv[LC];
+#pragma unroll
+                            for (int c0 = 0; c0 < LC; c0 += 16) tmem_ld16(tb + (uint32_t)(a * BN + cb + c0), pv + c0);
                             tmem_ld_wait();
 #pragma unroll
-                            for (int c = 0; c < 16; c += 2) {
-                                const float2 d2 = *reinterpret_cast<const float2 *>(dq + c0 + c);
-                                fma2(acc[a][c0 + c], acc[a][c0 + c + 1], pv[c], pv[c + 1], dw * d2.x, dw * d2.y);
+                            for (int c = 0; c < LC; c += 2) {
+                                const float2 d2 = *reinterpret_cast<const float2 *>(dq + cb + c);
+                                fma2(acc[a][cb + c], acc[a][cb + c + 1], pv[c], pv[c + 1], dw * d2.x, dw * d2.y);
                             }
                         }
                     }
@@ -490,12 +497,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(empty0 + 8 * slot);
             }
-            // tile outputs
+            // tile outputs (this warp's token columns)
             if (DUAL) {
                 const int fb = (rt * BM + quarter * 32) / kBlock;  // h block index along F
                 const bool vblk = rt * BM + quarter * 32 < p.rows;
 #pragma unroll
-                for (int c = 0; c < BN; ++c) {
+                for (int c = 0; c < HC; ++c) {
                     const int pos = pos0 + c;
                     const float g = acc[0][c], uu = acc[NA - 1][c];
                     const float h = g * uu / (1.0f + expf(-g));
@@ -516,7 +523,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
             } else {
 #pragma unroll
-                for (int c = 0; c < BN; ++c) {
+                for (int c = 0; c < HC; ++c) {
                     const int pos = pos0 + c;
                     if (vrow && pos < pos_end) p.o[(size_t)p.assign[pos] * p.rows + row] = acc[0][c];
                 }
