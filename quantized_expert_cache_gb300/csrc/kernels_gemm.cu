@@ -42,10 +42,7 @@ namespace gemm {
 
 constexpr int BM = 128;
 constexpr int BK = 64;
-constexpr int NWARPS = 14;
-constexpr int NTHREADS = NWARPS * 32;
 constexpr int W_TMA = 0, W_MMA = 1, W_CONV = 2, W_EPI = 6;
-constexpr int N_EPI = 8;  // two epilogue warps per TMEM lane quarter, each owning half of the token columns
 constexpr long long kTimeoutCycles = 4000000000ll;
 
 template <bool DUAL>
@@ -73,6 +70,11 @@ struct Cfg {
     static constexpr int NBARS = 2 * STAGES + 2 * NTBUF;
     static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
     static constexpr int SMEM = MISC_OFF + 16 + 1024;  // + alignment slack
+    // epilogue warps: EPI_SPLIT per TMEM lane quarter, each owning BN / EPI_SPLIT
+    // token columns (gate/up: 16 warps; down, one tensor: 8)
+    static constexpr int N_EPI = DUAL ? 16 : 8;
+    static constexpr int EPI_SPLIT = N_EPI / 4;
+    static constexpr int NTHREADS = (W_EPI + N_EPI) * 32;
 };
 
 // ---- PTX wrappers -----------------------------------------------------------
@@ -265,10 +267,11 @@ __device__ __forceinline__ void cur_next(StageCur &c, const GemmParams &p, int n
 }
 
 template <bool DUAL>
-__global__ void __launch_bounds__(NTHREADS, 1)
+__global__ void __launch_bounds__(Cfg<DUAL>::NTHREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmB, GemmParams p) {
     using C = Cfg<DUAL>;
     constexpr int BN = C::BN, NA = C::NA, NTBUF = C::NTBUF, STAGES = C::STAGES;
+    constexpr int N_EPI = C::N_EPI, EPI_SPLIT = C::EPI_SPLIT;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint64_t *bars = (uint64_t *)(smem + C::BAR_OFF);
@@ -435,8 +438,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // epilogue: TMEM lane quarter = warp % 4 (thread = weight row), half =
         // which BN/2 token columns this warp owns
         const int quarter = warp & 3;
-        const int half = (warp - W_EPI) >> 2;
-        constexpr int HC = BN / 2;  // token columns per epilogue warp
+        const int half = (warp - W_EPI) >> 2;  // which column part this warp owns
+        constexpr int HC = BN / EPI_SPLIT;      // token columns per epilogue warp
         const int r = quarter * 32 + lane;
         int qc = 0, it = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
@@ -711,8 +714,8 @@ int launch_prefill(const PrefillLaunch &L, cudaStream_t st) {
     const int A = L.gu.A;
     int g = (int)std::min<size_t>(((size_t)A * (L.H / 8) + 255) / 256, (size_t)L.n_sm * 16);
     if (g > 0) gather_kernel<<<g, 256, 0, st>>>(L.gu.assign, A, L.k, L.H, L.xq, L.xds, L.xs16, L.xdT, L.gu.A_pad);
-    gemm::grouped_gemm_kernel<true><<<L.n_sm, gemm::NTHREADS, gemm::Cfg<true>::SMEM, st>>>(L.tm_x, L.gu);
-    gemm::grouped_gemm_kernel<false><<<L.n_sm, gemm::NTHREADS, gemm::Cfg<false>::SMEM, st>>>(L.tm_h, L.dn);
+    gemm::grouped_gemm_kernel<true><<<L.n_sm, gemm::Cfg<true>::NTHREADS, gemm::Cfg<true>::SMEM, st>>>(L.tm_x, L.gu);
+    gemm::grouped_gemm_kernel<false><<<L.n_sm, gemm::Cfg<false>::NTHREADS, gemm::Cfg<false>::SMEM, st>>>(L.tm_h, L.dn);
     const size_t n = (size_t)L.T * L.H;
     int gc = (int)std::min<size_t>((n + 255) / 256, (size_t)L.n_sm * 16);
     combine_kernel<<<gc, 256, 0, st>>>(L.dn.o, L.w, L.y, L.T, L.k, L.H);
