@@ -46,7 +46,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode_b1_resident")
     ap.add_argument("--no-graph", action="store_true")
-    ap.add_argument("--cpu-sample-steps", type=int, default=2)
+    ap.add_argument("--cpu-sample-steps", type=int, default=6)
     ap.add_argument("--prefill-steps", type=int, default=2)
     ap.add_argument("--prefill-workload", default="prefill_t4096")
     return ap.parse_args()
