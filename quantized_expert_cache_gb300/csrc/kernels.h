@@ -51,9 +51,19 @@ struct FusedParams {
     float *w_out;            // routed: [T][k] written by CTA 0
     int renorm;
     int pdl;                 // launched with programmatic stream serialization
-    unsigned *done_gu;       // [E]: published gate/up row blocks per expert, zero between launches
+    unsigned *done_gu;       // [E]: published gate/up row blocks per expert (row-block mode: per
+                             // used-expert index), zero between launches
     unsigned *exit_count;    // [1]
     int *error;
+    // Row-block down mode (rb_rows > 0): a down item is rb_rows rows of H for
+    // every used expert, so it sums y itself; done_gu is then indexed by the
+    // used-expert index.  pre_off: shared-memory offset of the down prefetch
+    // area.
+    int rb_rows;
+    int pre_off;
+    // One routed token in row-block mode (fused_t1_ok): shared-memory offset
+    // of the layer's gate, up and down table rows (0: the general prologue).
+    int tbl_off;
 };
 
 // One grouped GEMM launch (gate/up with SwiGLU + h quantization, or down).
@@ -119,6 +129,10 @@ int launch_block_dots(const uint8_t *blob, int rows, int nb, int row0, int n_row
 int launch_stream_read(const void *src, size_t bytes, uint32_t *sink, int n_sm, cudaStream_t st);
 size_t fused_smem_bytes(int H, int F);
 int fused_configure(int F, size_t smem, int *blocks_per_sm);
+int fused_rb_rows(int H, int F, int T, int k, int E);
+size_t fused_rb_smem(int H, int F, int T, int k, int E, int rows, int *pre_off);
+bool fused_t1_ok(int E, int k);
+int fused_configure_rb(int F, size_t smem, int *blocks_per_sm);
 int launch_fused(const FusedParams &p, int grid, size_t smem, cudaStream_t st, cudaEvent_t const *ev);
 int launch_prefill(const PrefillLaunch &L, cudaStream_t st);
 int launch_stage(const StageParams &p, size_t blob_bytes, int n_sm, cudaStream_t st);

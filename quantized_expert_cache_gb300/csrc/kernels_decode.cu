@@ -12,6 +12,9 @@
 #include "common.cuh"
 #include "kernels.h"
 
+#include <map>
+#include <mutex>
+
 #include <float.h>
 
 namespace moe {
@@ -474,6 +477,9 @@ int launch_gemv(const GemvParams &p, int grid_gu, int grid_dn, cudaStream_t st, 
 // never wait, and a cooperative launch keeps every CTA resident, so each wait
 // ends; an expired wait sets an error bit and the item is skipped.
 constexpr int kMaxFusedA = 256;
+constexpr int kMaxRbA = 32;     // row-block mode: assignments per launch
+constexpr int kMaxRbRows = 8;   // row-block mode: rows of H per down item
+constexpr int kMaxRbOut = kMaxRbA * kMaxRbRows;
 constexpr int kGURounds = 8;  // 128-bit loads per lane and tensor issued together
 constexpr int kXBatch = 8;    // x blocks per warp loaded before they are quantized
 
@@ -484,6 +490,12 @@ __device__ __forceinline__ void cp_async16(void *smem_dst, const void *gsrc) {
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Publish: a release-ordered add (the warp's prior writes, ordered before
+// lane 0 by __syncwarp, become visible before the count does).
+__device__ __forceinline__ void red_release_add(unsigned *p, unsigned v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 
 __device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
     unsigned v;
@@ -520,11 +532,17 @@ __device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsig
     return a > b ? a : b;
 }
 
+// Inverse of fkey (-0.0 comes back as +0.0, which exp treats alike).
+__device__ __forceinline__ float funkey(unsigned key) {
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+}
+
 __device__ __forceinline__ void warp_topk_row(const float *l, int E, int k, int renorm, int lane, int &my_e,
                                               float &my_w) {
     constexpr int C = 16;  // logits per lane held in registers (one 512-wide chunk per warp)
     unsigned long long last = ~0ull;  // rank of the previous pick (first round: no bound)
     my_e = 0;
+    unsigned my_key = 0u;
     unsigned long long rk[C];
     const bool resident = E <= 32 * C;
     if (resident) {
@@ -558,10 +576,12 @@ __device__ __forceinline__ void warp_topk_row(const float *l, int E, int k, int 
         const unsigned hi = __reduce_max_sync(0xffffffffu, (unsigned)(best >> 32));
         const unsigned lo = __reduce_max_sync(0xffffffffu, (unsigned)(best >> 32) == hi ? (unsigned)best : 0u);
         last = ((unsigned long long)hi << 32) | lo;
-        if (lane == j) my_e = (int)(~lo);
+        if (lane == j) {
+            my_e = (int)(~lo);
+            my_key = hi;
+        }
     }
-    float my_v = -INFINITY;
-    if (lane < k) my_v = __ldg(l + my_e);
+    const float my_v = lane < k ? funkey(my_key) : -INFINITY;
     const float m = __shfl_sync(0xffffffffu, my_v, 0);
     const float ej = lane < k ? expf(my_v - m) : 0.0f;
     float den;
@@ -591,7 +611,18 @@ __device__ void fused_plan(const FusedParams &p, int *s_e, int *s_uniq, int *s_o
         // one warp: bitonic sort of (expert, assignment) keys, then the
         // used experts are the positions where the expert changes
         __syncthreads();  // routing / x prologue writes
-        if (threadIdx.x < 32) {
+        if (p.logits && p.g.n_tokens == 1) {
+            // one routed token: its k picks are distinct experts already
+            if (threadIdx.x < p.g.k) {
+                s_asg[threadIdx.x] = threadIdx.x;
+                s_uniq[threadIdx.x] = s_e[threadIdx.x];
+                s_off[threadIdx.x] = threadIdx.x;
+            }
+            if (threadIdx.x == 0) {
+                s_off[p.g.k] = p.g.k;
+                *s_nu = p.g.k;
+            }
+        } else if (threadIdx.x < 32) {
             const int lane = threadIdx.x;
             int e = 0x7fffffff;
             if (lane < A) {
@@ -823,6 +854,7 @@ __device__ __forceinline__ void gu_chunk(const FusedParams &p, int c0, int nt, i
         const int a = s_asg[c0 + warp];
         quantize_block_warp(sh_h[warp][lane], lane, g.hq + (size_t)a * F + (size_t)rg * kBlock,
                             g.hds + (size_t)a * rgs + rg);
+        __threadfence();  // h is published by the item's counter after the barrier
     }
     __syncthreads();
 }
@@ -926,12 +958,247 @@ __device__ __forceinline__ void dn_chunk(const FusedParams &p, int c0, int nt, i
     __syncthreads();
 }
 
-template <int LD, int NT>
+
+// ------------------------------------------------ one routed token, early start
+// T = 1, routed, row-block mode, E <= kT1MaxE.  Warp 0 routes and publishes
+// each pick the moment it is known; warps 1..7 meanwhile copy the layer's
+// gate and up table rows into shared memory and quantize x.  Gate/up item i
+// is (pick i mod k, row group i / k), so every CTA starts its weight loads as
+// soon as its own pick is out, and the later picks overlap the weight
+// stream.  Rows 0..27 of an item belong to warps 1..7, rows 28..31 to warp
+// 0, which takes them (and issues the CTA's down staging) after routing.
+__device__ __forceinline__ void bar_sync_n(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+__device__ __forceinline__ void bar_arrive_n(int id, int n) { asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+
+__device__ __forceinline__ void t1_route_gate_up(const FusedParams &p, int *s_e, float *s_w, int *s_uniq, int *s_off,
+                                                 int *s_asg, int *s_nu, int *s_npick, float (*sh_h)[32], uint8_t *dsm,
+                                                 uint8_t *dpre, int n_dn_items, uint32_t step_clock) {
+    const GemvParams &g = p.g;
+    const int H = g.H, F = g.F, k = g.k, E = g.cv.E;
+    const int nbx = H / kBlock, nbf = F / kBlock, rgs = F / kBlock;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int R = p.rb_rows;
+    int8_t *xq_s = (int8_t *)dsm;
+    BlockScale *xds_s = (BlockScale *)(dsm + kMaxChunk * H);
+    const uint64_t *s_tg = (const uint64_t *)(dsm + p.tbl_off);  // [gate row E][up row E][down row E]
+    const uint64_t *s_tu = s_tg + E, *s_td = s_tg + 2 * E;
+    volatile int *v_npick = s_npick;
+    volatile int *v_e = s_e;
+    if (warp == 0) {
+        // ---- routing: top-k over packed ranks, each pick published at once
+        const float *l = p.logits;
+        unsigned long long rk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int e = lane + 32 * i;
+            rk[i] = e < E ? ((unsigned long long)fkey(__ldg(l + e)) << 32) | (unsigned)(~(unsigned)e) : 0ull;
+        }
+        unsigned long long last = ~0ull;
+        int my_e = 0;
+        unsigned my_key = 0u;
+        for (int j = 0; j < k; ++j) {
+            unsigned long long c[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) c[i] = rk[i] < last ? rk[i] : 0ull;
+#pragma unroll
+            for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+                for (int i = 0; i < w; ++i) c[i] = umax64(c[i], c[i + w]);
+            const unsigned hi = __reduce_max_sync(0xffffffffu, (unsigned)(c[0] >> 32));
+            const unsigned lo = __reduce_max_sync(0xffffffffu, (unsigned)(c[0] >> 32) == hi ? (unsigned)c[0] : 0u);
+            last = ((unsigned long long)hi << 32) | lo;
+            if (lane == 0) {
+                v_e[j] = (int)(~lo);
+                __threadfence_block();
+                *v_npick = j + 1;
+            }
+            if (lane == j) {
+                my_e = (int)(~lo);
+                my_key = hi;
+            }
+        }
+        const float my_v = lane < k ? funkey(my_key) : -INFINITY;
+        const float m = __shfl_sync(0xffffffffu, my_v, 0);
+        const float ej = lane < k ? expf(my_v - m) : 0.0f;
+        float den;
+        if (p.renorm) {
+            den = warp_sum_f(ej);
+        } else {
+            float sacc = 0.0f;
+            for (int e = lane; e < E; e += 32) sacc += expf(__ldg(l + e) - m);
+            den = warp_sum_f(sacc);
+        }
+        const float my_w = ej / den;
+        if (lane < k) {
+            s_w[lane] = my_w;
+            s_uniq[lane] = my_e;
+            s_off[lane] = lane;
+            s_asg[lane] = lane;
+            if (blockIdx.x == 0) {
+                p.idx_out[lane] = my_e;
+                p.w_out[lane] = my_w;
+            }
+        }
+        if (lane == 0) {
+            s_off[k] = k;
+            *s_nu = k;
+        }
+        bar_sync_n(2, 256);  // x and the table rows are in shared memory
+    } else {
+        // ---- gate, up and down table rows (contiguous: tensor ids 3l .. 3l + 2)
+        {
+            const uint4 *src = reinterpret_cast<const uint4 *>(g.cv.tbl + (size_t)g.tid_gate * E);
+            uint8_t *dst = dsm + p.tbl_off;
+            for (int i = threadIdx.x - 32; i < 3 * E / 2; i += 224) cp_async16(dst + (size_t)i * 16, src + i);
+            cp_async_commit();
+        }
+        // ---- x of the token, quantized into shared memory
+        for (int q0 = warp - 1; q0 < nbx; q0 += 7 * 12) {
+            float xv[12];
+#pragma unroll
+            for (int i = 0; i < 12; ++i) {
+                const int q = q0 + i * 7;
+                if (q < nbx) xv[i] = __ldg(p.x + (size_t)q * kBlock + lane);
+            }
+#pragma unroll
+            for (int i = 0; i < 12; ++i) {
+                const int q = q0 + i * 7;
+                if (q < nbx) quantize_block_warp(xv[i], lane, xq_s + (size_t)q * kBlock, xds_s + q);
+            }
+        }
+        cp_async_wait_all();
+        bar_arrive_n(2, 256);
+        bar_sync_n(1, 224);
+        if (blockIdx.x == 0) {
+            for (int i = threadIdx.x - 32; i < H; i += 224) g.xq_out[i] = xq_s[i];
+            for (int i = threadIdx.x - 32; i < nbx; i += 224) g.xds_out[i] = xds_s[i];
+        }
+    }
+
+    // ---- the CTA's first down item (rows [rb R, rb R + R) of every pick),
+    // staged by warps 1..7 (pick u by warp 1 + u mod 7) once the pick is out
+    auto stage_first_down = [&]() {
+        if (warp == 0 || (int)blockIdx.x >= n_dn_items) return;
+        const int rb = blockIdx.x;
+        const int nc = R * nbf, ns = R * nbf / 8, per = nc + ns;
+        const size_t soff = blob_scales_offset(H, nbf);
+        for (int u = warp - 1; u < k; u += kWarps - 1) {
+            if (lane == 0) {
+                const long long t0 = clock64();
+                while (*v_npick <= u) {
+                    if (clock64() - t0 > 4000000000ll) {
+                        atomicOr(p.error, 4);
+                        break;
+                    }
+                    __nanosleep(20);
+                }
+                __threadfence_block();
+            }
+            __syncwarp();
+            const uint8_t *bd = (const uint8_t *)(uintptr_t)(s_td[v_e[u]] & ~1ull);
+            for (int j = lane; j < per; j += 32) {
+                if (j < nc)
+                    cp_async16(dpre + ((size_t)u * nc + j) * 16, bd + ((size_t)rb * nc + j) * 16);
+                else
+                    cp_async16(dpre + (size_t)k * nc * 16 + ((size_t)u * ns + (j - nc)) * 16,
+                               bd + soff + (size_t)rb * nc * 2 + (size_t)(j - nc) * 16);
+            }
+        }
+        cp_async_commit();
+    };
+
+    // ---- gate/up items: (pick i mod k, row group i / k)
+    const int sub = lane % kGULanes, grp = lane / kGULanes;
+    const int rloc = warp == 0 ? 28 + grp : (warp - 1) * 4 + grp;
+    const size_t scale_off = blob_scales_offset(F, nbx);
+    const int n_items = k * rgs;
+    int m = 0;
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++m) {
+        const int u = item % k, rg = item / k;
+        if (warp != 0 && lane == 0) {
+            const long long t0 = clock64();
+            while (*v_npick <= u) {
+                if (clock64() - t0 > 4000000000ll) {
+                    atomicOr(p.error, 4);
+                    break;
+                }
+                __nanosleep(20);
+            }
+            __threadfence_block();
+        }
+        __syncwarp();
+        const int e = v_e[u];
+        const uint64_t eg = s_tg[e], eu = s_tu[e];
+        if (rg == 0 && threadIdx.x == 32) {
+            record_read(g.cv, g.tid_gate, e, eg, step_clock);
+            record_read(g.cv, g.tid_up, e, eu, step_clock);
+        }
+        const uint8_t *bg = (const uint8_t *)(uintptr_t)(eg & ~1ull);
+        const uint8_t *bu = (const uint8_t *)(uintptr_t)(eu & ~1ull);
+        const int r = rg * 32 + rloc;
+        const uint4 *qg = (const uint4 *)bg + (size_t)r * nbx;
+        const uint4 *qu = (const uint4 *)bu + (size_t)r * nbx;
+        const __half *dg = (const __half *)(bg + scale_off) + (size_t)r * nbx;
+        const __half *du = (const __half *)(bu + scale_off) + (size_t)r * nbx;
+        float ag = 0.0f, au = 0.0f;
+        for (int bb = 0; bb * kGULanes * kGURounds < nbx; ++bb) {
+            uint4 wg4[kGURounds], wu4[kGURounds];
+            float sg[kGURounds], su[kGURounds];
+#pragma unroll
+            for (int i = 0; i < kGURounds; ++i) {
+                const int b = sub + kGULanes * (bb * kGURounds + i);
+                if (b < nbx) {
+                    wg4[i] = ld_weights(qg + b);
+                    wu4[i] = ld_weights(qu + b);
+                    sg[i] = ld_scale(dg + b);
+                    su[i] = ld_scale(du + b);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < kGURounds; ++i) {
+                const int b = sub + kGULanes * (bb * kGURounds + i);
+                if (b < nbx) {
+                    const int4 *xa = (const int4 *)(xq_s + (size_t)b * kBlock);
+                    const int4 x0 = xa[0], x1 = xa[1];
+                    const BlockScale xs = xds_s[b];
+                    ag += (float)q4_block_dot(wg4[i], x0, x1, xs.s) * (sg[i] * xs.d);
+                    au += (float)q4_block_dot(wu4[i], x0, x1, xs.s) * (su[i] * xs.d);
+                }
+            }
+        }
+#pragma unroll
+        for (int o = kGULanes / 2; o > 0; o >>= 1) {
+            ag += __shfl_xor_sync(0xffffffffu, ag, o);
+            au += __shfl_xor_sync(0xffffffffu, au, o);
+        }
+        float *hrow = sh_h[m & 1];
+        if (sub == 0) hrow[rloc] = ag * au / (1.0f + expf(-ag));
+        __syncthreads();
+        if (warp == 0) {
+            // h block rg of assignment u (one token: assignment = pick index)
+            quantize_block_warp(hrow[lane], lane, g.hq + (size_t)u * F + (size_t)rg * kBlock, g.hds + (size_t)u * rgs + rg);
+            __syncwarp();
+            if (lane == 0) red_release_add(&p.done_gu[u], 1u);
+            if (m == 0) bar_arrive_n(3, 256);
+        } else if (m == 0) {
+            // the down rows are requested once this item's gate/up weights
+            // are in and its h block is out, so they compete neither with the
+            // gate/up stream nor with the publish
+            bar_sync_n(3, 256);
+            stage_first_down();
+        }
+    }
+    if (m == 0) stage_first_down();  // a CTA without a gate/up item
+    __syncthreads();  // routing results for CTAs without a gate/up item
+}
+
+template <int LD, int NT, bool RB>
 __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
     __shared__ int s_e[kMaxFusedA], s_uniq[kMaxFusedA], s_off[kMaxFusedA + 1], s_asg[kMaxFusedA],
         s_cnt[kMaxFusedA], s_first[kMaxFusedA];
     __shared__ float s_w[kMaxFusedA];
-    __shared__ int s_nu, s_last;
+    __shared__ float s_o[RB ? kMaxRbOut : 1];  // row-block mode: [assignment][row] down outputs
+    __shared__ int s_nu, s_last, s_npick;
     __shared__ float sh_h[kMaxChunk][32];
     extern __shared__ __align__(16) uint8_t dsm[];
     const GemvParams &g = p.g;
@@ -946,13 +1213,25 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
         asm volatile("griddepcontrol.wait;" ::: "memory");
         asm volatile("griddepcontrol.launch_dependents;");
     }
+    constexpr int DG = 32 / LD, DROWS = kWarps * DG;
+    const int n_rb_all = H / DROWS;
+    const int R = p.rb_rows;
+    uint8_t *dpre = dsm + (RB ? (size_t)p.pre_off : fused_stage_bytes(H, F));
+    const bool t1 = NT == 1 && RB && p.tbl_off > 0;
+    if (t1) {
+        if (threadIdx.x == 0) s_npick = 0;
+        __syncthreads();
+        t1_route_gate_up(p, s_e, s_w, s_uniq, s_off, s_asg, &s_nu, &s_npick, sh_h, dsm, dpre, H / R, step_clock);
+    }
     // Prologue.  Routed launches: warps 0..T-1 route the tokens (top-k over
     // the logits) while the remaining warps quantize every token's x (small
     // batches: x does not depend on the routing); both before any weight
     // request.
     const bool xpre = g.n_tokens <= kMaxChunk;
     const int n_route_warps = !p.logits ? 0 : xpre ? max(1, min(g.n_tokens, kWarps / 2)) : kWarps;
-    if (p.logits && warp < n_route_warps) {
+    if (t1) {
+        // routed and x quantized above
+    } else if (p.logits && warp < n_route_warps) {
         const int k_ = g.k, E = g.cv.E;
         for (int t = warp; t < g.n_tokens; t += n_route_warps) {
             int me;
@@ -987,9 +1266,9 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
         }
     }
     // (the plan's barriers order these shared-memory writes before any use)
-    fused_plan(p, s_e, s_uniq, s_off, s_asg, &s_nu, s_cnt, s_first, s_w);
+    if (!t1) fused_plan(p, s_e, s_uniq, s_off, s_asg, &s_nu, s_cnt, s_first, s_w);
     const int nu = s_nu;
-    if (xpre && blockIdx.x == 0) {
+    if (!t1 && xpre && blockIdx.x == 0) {
         // the context's copy of the quantized x (for inspection)
         const int8_t *xq_s0 = (const int8_t *)dsm;
         const BlockScale *xds_s0 = (const BlockScale *)(dsm + kMaxChunk * H);
@@ -997,18 +1276,39 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
         for (int i = threadIdx.x; i < g.n_tokens * nbx; i += blockDim.x) g.xds_out[i] = xds_s0[i];
     }
 
-    // This CTA's first down item (codes + scales of DROWS rows) is copied
+    // This CTA's first down item (codes + scales of its rows) is copied
     // into shared memory with cp.async, issued right behind the CTA's first
     // gate/up weight loads (or at once when the CTA has no gate/up item), so
-    // the down weights stream while the gate/up item runs.
-    constexpr int DG = 32 / LD, DROWS = kWarps * DG;
-    const int n_rb_all = H / DROWS;
-    uint8_t *dpre = dsm + fused_stage_bytes(H, F);
-    const bool prefetched = (int)blockIdx.x < nu * n_rb_all;
-    bool pf_issued = !prefetched;
+    // the down weights stream while the gate/up item runs.  Row-block mode:
+    // rows [rb R, rb R + R) of every used expert, laid out as codes
+    // [expert][row][block] then scales [expert][row][block].
+    const int n_dn_items = RB ? H / R : nu * n_rb_all;
+    const bool prefetched = (int)blockIdx.x < n_dn_items;
+    bool pf_issued = !prefetched || t1;  // (one routed token: staged during routing)
+    // warp w stages the rows of used experts w, w + 8, ...
+    auto stage_rb = [&](int rb) {
+        const int nc = R * nbf, ns = R * nbf / 8, per = nc + ns;
+        const size_t soff = blob_scales_offset(H, nbf);
+        for (int u = warp; u < nu; u += kWarps) {
+            const uint64_t ed = g.cv.tbl[(size_t)g.tid_down * g.cv.E + s_uniq[u]];
+            const uint8_t *bd = (const uint8_t *)(uintptr_t)(ed & ~1ull);
+            for (int j = lane; j < per; j += 32) {
+                if (j < nc)
+                    cp_async16(dpre + ((size_t)u * nc + j) * 16, bd + ((size_t)rb * nc + j) * 16);
+                else
+                    cp_async16(dpre + (size_t)nu * nc * 16 + ((size_t)u * ns + (j - nc)) * 16,
+                               bd + soff + (size_t)rb * nc * 2 + (size_t)(j - nc) * 16);
+            }
+        }
+        cp_async_commit();
+    };
     auto issue_prefetch = [&]() {
         if (pf_issued) return;
         pf_issued = true;
+        if (RB) {
+            stage_rb(blockIdx.x);
+            return;
+        }
         const int u = blockIdx.x / n_rb_all, rb = blockIdx.x - u * n_rb_all;
         const uint64_t ed = g.cv.tbl[(size_t)g.tid_down * g.cv.E + s_uniq[u]];
         const uint8_t *bd = (const uint8_t *)(uintptr_t)(ed & ~1ull);
@@ -1026,7 +1326,7 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
     if ((int)blockIdx.x >= nu * rgs) issue_prefetch();
 
     // ---------------- gate/up items
-    {
+    if (!t1) {
         int8_t *xq_s = (int8_t *)dsm;                                     // [chunk][H]
         BlockScale *xds_s = (BlockScale *)(dsm + kMaxChunk * H);          // [chunk][nbx]
         const int sub = lane % kGULanes, grp = lane / kGULanes;
@@ -1055,17 +1355,100 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
                 gu_chunk<NT>(p, c0, nt, rg, rloc, sub, lane, warp, qg, qu, dg, du, xq_s, xds_s, sh_h, s_asg,
                              issue_prefetch, xpre);
             }
-            // publish this row block of expert e
-            __threadfence();
-            __syncthreads();
-            if (threadIdx.x == 0) atomicAdd(&p.done_gu[e], 1u);
+            // publish this row block of expert e (the writers fenced h
+            // before the chunk's closing barrier)
+            if (threadIdx.x == 0) atomicAdd(&p.done_gu[RB ? u : e], 1u);
         }
     }
 
     issue_prefetch();
 
     // ---------------- down items
-    {
+    if (RB) {
+        // Row-block mode: item rb = rows [rb R, rb R + R) of H for every used
+        // expert, (expert, row) pairs spread over the CTA's lanes (LD lanes a
+        // pair).  Each warp waits only for the gate/up items of the experts
+        // its pairs touch and reads their h from L2, so the down products of
+        // early experts overlap the gate/up of late ones; each item then sums
+        // y in j order.
+        const int n_items = n_dn_items;
+        if ((int)blockIdx.x < n_items) {
+            constexpr int VP = 256 / LD;  // (expert, row) pairs per pass
+            const int sub = threadIdx.x % LD;
+            cp_async_wait_all();
+            __syncthreads();  // the first item's staged rows
+            for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+                const bool first = item == (int)blockIdx.x;
+                if (!first) {
+                    __syncthreads();  // the previous item's reads of the staged rows and s_o
+                    stage_rb(item);
+                    cp_async_wait_all();
+                    __syncthreads();
+                }
+                if (item == 0 && (int)threadIdx.x < nu) {
+                    const int e = s_uniq[threadIdx.x];
+                    record_read(g.cv, g.tid_down, e, g.cv.tbl[(size_t)g.tid_down * g.cv.E + e], step_clock);
+                }
+                const uint4 *wc0 = (const uint4 *)dpre;
+                const __half *ws0 = (const __half *)(dpre + (size_t)nu * R * nbf * 16);
+                for (int v0 = 0; v0 < nu * R; v0 += VP) {
+                    const int vr = v0 + (int)threadIdx.x / LD;
+                    const bool act = vr < nu * R;
+                    const int u = act ? vr / R : 0, r = vr - u * R;
+                    if (first) {
+                        // bounded wait for the gate/up items of this warp's experts
+                        const int ulo = __shfl_sync(0xffffffffu, u, 0);
+                        const int uhi = __reduce_max_sync(0xffffffffu, act ? u : 0);
+                        if (lane == 0 && v0 + (int)threadIdx.x / LD < nu * R) {
+                            const long long t0 = clock64();
+                            for (int uu = ulo; uu <= uhi; ++uu) {
+                                while (ld_acquire(&p.done_gu[uu]) < (unsigned)rgs) {
+                                    if (clock64() - t0 > 4000000000ll) {
+                                        atomicOr(p.error, 2);
+                                        break;
+                                    }
+                                    __nanosleep(20);
+                                }
+                            }
+                        }
+                        __syncwarp();
+                    }
+                    const int a0 = act ? s_off[u] : 0, cnt = act ? s_off[u + 1] - a0 : 0;
+                    const int mc = __reduce_max_sync(0xffffffffu, cnt);
+                    const uint4 *wc = wc0 + (size_t)vr * nbf;
+                    const __half *ws = ws0 + (size_t)vr * nbf;
+                    for (int sl = 0; sl < mc; ++sl) {
+                        float acc = 0.0f;
+                        int a = 0;
+                        if (sl < cnt) {
+                            a = s_asg[a0 + sl];
+                            // h of assignment a from L2 (written by other CTAs of this launch)
+                            const int4 *ha = reinterpret_cast<const int4 *>(g.hq + (size_t)a * F);
+                            const int2 *hs = reinterpret_cast<const int2 *>(g.hds + (size_t)a * nbf);
+#pragma unroll 4
+                            for (int b = sub; b < nbf; b += LD) {
+                                const int4 h0 = __ldcg(ha + 2 * b), h1 = __ldcg(ha + 2 * b + 1);
+                                const int2 hsc = __ldcg(hs + b);
+                                const uint4 w4 = wc[b];
+                                acc += (float)q4_block_dot(w4, h0, h1, hsc.y) *
+                                       (__half2float(ws[b]) * __int_as_float(hsc.x));
+                            }
+                        }
+#pragma unroll
+                        for (int o = LD / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+                        if (sl < cnt && sub == 0) s_o[a * R + r] = acc;
+                    }
+                }
+                __syncthreads();
+                for (int i = threadIdx.x; i < g.n_tokens * R; i += blockDim.x) {
+                    const int t = i / R, r = i - t * R;
+                    float y = 0.0f;
+                    for (int j = 0; j < k; ++j) y += s_w[t * k + j] * s_o[(t * k + j) * R + r];
+                    g.y[(size_t)t * H + (size_t)item * R + r] = y;
+                }
+            }
+        }
+    } else {
         constexpr int G = 32 / LD, ROWS = kWarps * G;
         constexpr int RD = 12;  // loads per lane issued together (<= 12 rounds)
         int8_t *hq_s = (int8_t *)dsm;                                   // [chunk][F]
@@ -1124,7 +1507,7 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
         __threadfence();
         const unsigned prev = atomicAdd(p.exit_count, 1u);
         if (prev == gridDim.x - 1) {
-            for (int u = 0; u < nu; ++u) p.done_gu[s_uniq[u]] = 0u;
+            for (int u = 0; u < nu; ++u) p.done_gu[RB ? u : s_uniq[u]] = 0u;
             *p.exit_count = 0u;
             __threadfence();
         }
@@ -1141,36 +1524,87 @@ int fused_down_lanes(int F) { return F / kBlock <= 40 ? 4 : 8; }
 
 static int fused_nt(int T) { return T <= 1 ? 1 : T == 2 ? 2 : T <= 4 ? 4 : 8; }
 
-static const void *fused_fn(int F, int T) {
+template <bool RB>
+static const void *fused_fn_t(int F, int T) {
     const int ld = fused_down_lanes(F), nt = fused_nt(T);
     if (ld == 4) {
-        if (nt == 1) return (const void *)decode_layer_kernel<4, 1>;
-        if (nt == 2) return (const void *)decode_layer_kernel<4, 2>;
-        if (nt == 4) return (const void *)decode_layer_kernel<4, 4>;
-        return (const void *)decode_layer_kernel<4, 8>;
+        if (nt == 1) return (const void *)decode_layer_kernel<4, 1, RB>;
+        if (nt == 2) return (const void *)decode_layer_kernel<4, 2, RB>;
+        if (nt == 4) return (const void *)decode_layer_kernel<4, 4, RB>;
+        return (const void *)decode_layer_kernel<4, 8, RB>;
     }
-    if (nt == 1) return (const void *)decode_layer_kernel<8, 1>;
-    if (nt == 2) return (const void *)decode_layer_kernel<8, 2>;
-    if (nt == 4) return (const void *)decode_layer_kernel<8, 4>;
-    return (const void *)decode_layer_kernel<8, 8>;
+    if (nt == 1) return (const void *)decode_layer_kernel<8, 1, RB>;
+    if (nt == 2) return (const void *)decode_layer_kernel<8, 2, RB>;
+    if (nt == 4) return (const void *)decode_layer_kernel<8, 4, RB>;
+    return (const void *)decode_layer_kernel<8, 8, RB>;
 }
 
-// Shared-memory opt-in for every token-count variant; *blocks_per_sm gets
-// the smallest resident-CTA count over the variants (a safe cooperative grid).
-int fused_configure(int F, size_t smem, int *blocks_per_sm) {
+static const void *fused_fn(int F, int T, bool rb) { return rb ? fused_fn_t<true>(F, T) : fused_fn_t<false>(F, T); }
+
+// Shared-memory opt-in for every token-count variant of one mode (only ever
+// raised, so contexts of different shapes coexist); *blocks_per_sm gets the
+// smallest resident-CTA count over the variants (a safe cooperative grid).
+static int configure_mode(int F, size_t smem, bool rb, int *blocks_per_sm) {
+    static std::mutex mu;
+    static std::map<const void *, size_t> opted;
+    std::lock_guard<std::mutex> lk(mu);
     int best = 1 << 30;
     for (int T : {1, 2, 4, 8}) {
-        const void *fn = fused_fn(F, T);
-        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return (int)e;
+        const void *fn = fused_fn(F, T, rb);
+        size_t &cur = opted[fn];
+        if (smem > cur) {
+            cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return (int)e;
+            cur = smem;
+        }
         int b = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, fn, 256, smem);
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, fn, 256, smem);
         if (e != cudaSuccess) return (int)e;
         best = b < best ? b : best;
     }
     *blocks_per_sm = best;
     return 0;
 }
+
+int fused_configure(int F, size_t smem, int *blocks_per_sm) { return configure_mode(F, smem, false, blocks_per_sm); }
+int fused_configure_rb(int F, size_t smem, int *blocks_per_sm) { return configure_mode(F, smem, true, blocks_per_sm); }
+
+// Row-block down mode: rows of H per down item for a launch of T tokens, or
+// 0 when the mode does not apply (more than kMaxRbA assignments or 8 tokens,
+// h of all assignments above kRbStageBudget, or no row count whose staged
+// rows fit kRbPrefetchBudget in one pass of (expert, row) pairs).
+constexpr size_t kRbStageBudget = 40u << 10;
+constexpr size_t kRbPrefetchBudget = 52u << 10;
+
+int fused_rb_rows(int H, int F, int T, int k, int E) {
+    const int A = T * k, U = A < E ? A : E, nbf = F / kBlock, LD = fused_down_lanes(F);
+    if (T < 1 || T > kMaxChunk || A > kMaxRbA) return 0;
+    if ((size_t)A * F + (size_t)A * nbf * sizeof(BlockScale) + 16 > kRbStageBudget) return 0;
+    for (int R = kMaxRbRows; R >= 2; R >>= 1) {
+        if (H % R || (R * nbf * 2) % 16) continue;
+        if (U * R > 256 / LD) continue;
+        if ((size_t)U * R * nbf * kBlockBytes > kRbPrefetchBudget) continue;
+        return R;
+    }
+    return 0;
+}
+
+// Dynamic shared memory of a row-block launch: x staging or h staging
+// (aliased; x is dead once the CTA's gate/up items are done), then the
+// staged down rows.
+size_t fused_rb_smem(int H, int F, int T, int k, int E, int rows, int *pre_off) {
+    const int A = T * k, U = A < E ? A : E, nbf = F / kBlock, nbx = H / kBlock;
+    const size_t xs = (size_t)kMaxChunk * H + (size_t)kMaxChunk * nbx * sizeof(BlockScale);
+    const size_t hs = (((size_t)A * F + 15) & ~(size_t)15) + (size_t)A * nbf * sizeof(BlockScale);
+    const size_t r0 = ((xs > hs ? xs : hs) + 15) / 16 * 16;
+    if (pre_off) *pre_off = (int)r0;
+    return r0 + (size_t)U * rows * nbf * kBlockBytes;
+}
+
+// The early-start path for one routed token keeps the logits in registers
+// (16 per lane) and copies the gate and up table rows with 16-byte copies.
+bool fused_t1_ok(int E, int k) { return E <= 32 * 16 && E % 2 == 0 && k <= 32; }
+
 
 int launch_fused(const FusedParams &p, int grid, size_t smem, cudaStream_t st, cudaEvent_t const *ev) {
     cudaLaunchConfig_t cfg{};
@@ -1187,7 +1621,7 @@ int launch_fused(const FusedParams &p, int grid, size_t smem, cudaStream_t st, c
     cfg.numAttrs = p.pdl ? 2 : 1;
     if (ev) record(ev[0], st);
     void *args[] = {(void *)&p};
-    cudaError_t e = cudaLaunchKernelExC(&cfg, fused_fn(p.g.F, p.g.n_tokens), args);
+    cudaError_t e = cudaLaunchKernelExC(&cfg, fused_fn(p.g.F, p.g.n_tokens, p.rb_rows > 0), args);
     if (ev) {
         record(ev[1], st);
         record(ev[2], st);

@@ -78,8 +78,8 @@ struct moe_ctx {
     int stage_cap = 0;
     // fused small-batch layer kernel
     unsigned *done_gu = nullptr, *exit_count = nullptr;
-    size_t fused_smem = 0;
-    int fused_blocks = 0;
+    size_t fused_smem = 0, fused_smem_rb = 0;
+    int fused_blocks = 0, fused_blocks_rb = 0;
     int pdl = 1;  // fused layer kernels use programmatic dependent launch
 
     uint32_t *h_readback = nullptr;  // pinned: count + miss list
@@ -350,6 +350,19 @@ int moe_layer_init(const moe_cfg *cfg, void *cuda_stream, moe_ctx **out) {
         int bps = 0;
         CKI((cudaError_t)moe::fused_configure(ctx->F, ctx->fused_smem, &bps));
         ctx->fused_blocks = bps * ctx->n_sm;
+        // row-block down mode: the largest launch of up to 8 tokens that uses it
+        for (int T = 1; T <= std::min(ctx->M, 8); ++T) {
+            const int rows = moe::fused_rb_rows(ctx->H, ctx->F, T, ctx->k, E);
+            if (rows > 0) {
+                size_t sm = moe::fused_rb_smem(ctx->H, ctx->F, T, ctx->k, E, rows, nullptr);
+                if (T == 1 && moe::fused_t1_ok(E, ctx->k)) sm = (sm + 15) / 16 * 16 + (size_t)24 * E;
+                ctx->fused_smem_rb = std::max(ctx->fused_smem_rb, sm);
+            }
+        }
+        if (ctx->fused_smem_rb > 0) {
+            CKI((cudaError_t)moe::fused_configure_rb(ctx->F, ctx->fused_smem_rb, &bps));
+            ctx->fused_blocks_rb = bps * ctx->n_sm;
+        }
     }
 
     CKI(cudaHostAlloc(&ctx->h_readback, sizeof(uint32_t) * (1 + (size_t)ctx->miss_cap), cudaHostAllocDefault));
@@ -525,14 +538,28 @@ static int ffn_forward_impl(moe_ctx *ctx, int layer, const float *d_x, int n_tok
         fp.w_out = w_out;
         fp.renorm = ctx->cfg.renorm_topk;
         fp.pdl = ctx->pdl;
-        const int items = U * std::max(ctx->F / 32, ctx->n_counters);
-        const int grid = std::min(items, ctx->fused_blocks);
+        int items = U * std::max(ctx->F / 32, ctx->n_counters);
+        int grid = std::min(items, ctx->fused_blocks);
+        size_t smem = ctx->fused_smem;
+        const int rows = ctx->fused_blocks_rb > 0 ? moe::fused_rb_rows(H, ctx->F, T, ctx->k, ctx->E) : 0;
+        if (rows > 0) {
+            // row-block down mode: each down item sums y for its rows
+            fp.rb_rows = rows;
+            smem = moe::fused_rb_smem(H, ctx->F, T, ctx->k, ctx->E, rows, &fp.pre_off);
+            if (T == 1 && d_logits && moe::fused_t1_ok(ctx->E, ctx->k)) {
+                // one routed token: the gate, up and down table rows follow
+                fp.tbl_off = (int)((smem + 15) / 16 * 16);
+                smem = (size_t)fp.tbl_off + (size_t)24 * ctx->E;
+            }
+            items = std::max(U * (ctx->F / 32), H / rows);
+            grid = std::min(items, ctx->fused_blocks_rb);
+        }
         const cudaEvent_t *ev = nullptr;
         if (ctx->timing) {
             ev = ctx->tev.data() + 4 * (size_t)layer;
             ctx->tev_used[layer] = 1;
         }
-        rc = moe::launch_fused(fp, grid, ctx->fused_smem, st, ev);
+        rc = moe::launch_fused(fp, grid, smem, st, ev);
         if (rc) return fail(ctx, MOE_ERR_CUDA, std::string("fused launch: ") + cudaGetErrorString((cudaError_t)rc));
         ctx->last_T = T;
         return MOE_OK;
