@@ -112,12 +112,15 @@ struct CacheView {
     uint32_t *miss_count;      // [1]
     const uint32_t *clock;     // [1]: token clock after the last promotion pass
     unsigned long long *cold_reads;  // [1]: (tensor, expert) zero-copy passes
-    int E, slots_per_tensor, bitmap_words, miss_cap;
+    uint32_t *hit_bitmap;      // [n_tensors][hit_words]: slots hit since the last promotion pass (or null)
+    int E, slots_per_tensor, bitmap_words, miss_cap, hit_words;
 };
 
 // Record one (tensor, expert) read: a cold read sets its bit in the miss
 // bitmap and, when newly set, appends (tensor << 12 | expert) to the miss
-// list; a pool hit writes the step's clock into the slot's stamp.
+// list; a pool hit writes the step's clock into the slot's stamp and sets
+// the slot's bit in the hit bitmap (the hit count of the step, read by the
+// promotion pass without reading every stamp).
 __device__ __forceinline__ void record_read(const CacheView &cv, int tid, int e, uint64_t entry, uint32_t step_clock) {
     if (entry & 1ull) {
         uint32_t bit = 1u << (e & 31);
@@ -128,7 +131,10 @@ __device__ __forceinline__ void record_read(const CacheView &cv, int tid, int e,
         }
     } else {
         int s = cv.slot[(size_t)tid * cv.E + e];
-        if (s >= 0) cv.stamps[(size_t)tid * cv.slots_per_tensor + s] = step_clock;
+        if (s >= 0) {
+            cv.stamps[(size_t)tid * cv.slots_per_tensor + s] = step_clock;
+            if (cv.hit_bitmap) atomicOr(&cv.hit_bitmap[(size_t)tid * cv.hit_words + (s >> 5)], 1u << (s & 31));
+        }
     }
 }
 

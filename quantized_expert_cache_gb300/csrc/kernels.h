@@ -138,7 +138,7 @@ int launch_prefill(const PrefillLaunch &L, cudaStream_t st);
 int launch_stage(const StageParams &p, size_t blob_bytes, int n_sm, cudaStream_t st);
 int gemm_configure();
 int gemm_bn(bool dual);
-int launch_apply_updates(const Update *u, int n, uint64_t *tbl, int32_t *slot, uint32_t *stamps, uint32_t *clock,
-                         uint32_t new_clock, cudaStream_t st);
+int launch_step_finish(const Update *u, int n, uint64_t *tbl, int32_t *slot, uint32_t *stamps, uint32_t *clock,
+                       uint32_t new_clock, uint32_t *clear_a, int n_a, uint32_t *clear_b, int n_b, cudaStream_t st);
 
 }  // namespace moe

@@ -1679,25 +1679,34 @@ int launch_stream_read(const void *src, size_t bytes, uint32_t *sink, int n_sm, 
 }
 
 // Table / stamp updates published by the promotion pass.
-__global__ void apply_updates_kernel(const Update *__restrict__ u, int n, uint64_t *tbl, int32_t *slot,
-                                     uint32_t *stamps, uint32_t *clock, uint32_t new_clock) {
-    const int i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i == 0) *clock = new_clock;
-    if (i >= n) return;
-    const Update x = u[i];
-    if (x.what == 0)
-        tbl[x.index] = x.value;
-    else if (x.what == 1)
-        slot[x.index] = (int32_t)(int64_t)x.value;
-    else
-        stamps[x.index] = (uint32_t)x.value;
+// Between-step state update: the promotion pass's table / slot / stamp
+// writes (read straight from the host's pinned list), the new clock, and the
+// per-step records cleared (hit bitmap + miss count, miss bitmap).
+__global__ void step_finish_kernel(const Update *__restrict__ u, int n, uint64_t *tbl, int32_t *slot,
+                                   uint32_t *stamps, uint32_t *clock, uint32_t new_clock, uint32_t *clear_a, int n_a,
+                                   uint32_t *clear_b, int n_b) {
+    const int stride = gridDim.x * blockDim.x;
+    const int i0 = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i0 == 0) *clock = new_clock;
+    for (int i = i0; i < n; i += stride) {
+        const Update x = u[i];
+        if (x.what == 0)
+            tbl[x.index] = x.value;
+        else if (x.what == 1)
+            slot[x.index] = (int32_t)(int64_t)x.value;
+        else
+            stamps[x.index] = (uint32_t)x.value;
+    }
+    for (int i = i0; i < n_a; i += stride) clear_a[i] = 0u;
+    for (int i = i0; i < n_b; i += stride) clear_b[i] = 0u;
 }
 
-int launch_apply_updates(const Update *u, int n, uint64_t *tbl, int32_t *slot, uint32_t *stamps, uint32_t *clock,
-                         uint32_t new_clock, cudaStream_t st) {
-    int grid = (n + 255) / 256;
-    if (grid < 1) grid = 1;
-    apply_updates_kernel<<<grid, 256, 0, st>>>(u, n, tbl, slot, stamps, clock, new_clock);
+int launch_step_finish(const Update *u, int n, uint64_t *tbl, int32_t *slot, uint32_t *stamps, uint32_t *clock,
+                       uint32_t new_clock, uint32_t *clear_a, int n_a, uint32_t *clear_b, int n_b, cudaStream_t st) {
+    const int work = n > n_a ? (n > n_b ? n : n_b) : (n_a > n_b ? n_a : n_b);
+    int grid = (work + 255) / 256;
+    grid = grid < 1 ? 1 : grid > 64 ? 64 : grid;
+    step_finish_kernel<<<grid, 256, 0, st>>>(u, n, tbl, slot, stamps, clock, new_clock, clear_a, n_a, clear_b, n_b);
     return (int)cudaGetLastError();
 }
 

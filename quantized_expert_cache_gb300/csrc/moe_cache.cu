@@ -82,9 +82,11 @@ struct moe_ctx {
     int fused_blocks = 0, fused_blocks_rb = 0;
     int pdl = 1;  // fused layer kernels use programmatic dependent launch
 
-    uint32_t *h_readback = nullptr;  // pinned: count + miss list
-    uint32_t *h_stamps = nullptr;    // pinned
-    Update *h_upd = nullptr, *d_upd = nullptr;
+    uint32_t *h_stamps = nullptr;    // pinned mirror, refreshed per tensor when a victim is chosen
+    uint32_t *d_stepbuf = nullptr;   // [hit bitmap: n_tensors x hit_words][miss count][miss keys]
+    uint32_t *h_step = nullptr;      // pinned: hit bitmap, miss count and the first kStepKeys keys
+    int hit_words = 0;
+    Update *h_upd = nullptr, *d_upd = nullptr;  // pinned, mapped (d_upd: its device address)
     int upd_cap = 0, n_upd = 0;
 
     std::vector<TensorState> t;
@@ -144,13 +146,17 @@ void set_entry(moe_ctx *c, int tid, int e, uint64_t entry, int32_t slot) {
     push_upd(c, 1, (size_t)tid * c->E + e, (uint64_t)(int64_t)slot);
 }
 
-// Publish the queued updates on `st` (table, slots, stamps, clock).
-int publish(moe_ctx *ctx, cudaStream_t st) {
-    if (ctx->n_upd > 0)
-        CK(cudaMemcpyAsync(ctx->d_upd, ctx->h_upd, sizeof(Update) * ctx->n_upd, cudaMemcpyHostToDevice, st));
-    int rc = moe::launch_apply_updates(ctx->d_upd, ctx->n_upd, ctx->d_tbl, ctx->d_slot, ctx->d_stamps, ctx->d_clock,
-                                       (uint32_t)ctx->clock, st);
-    if (rc) return fail(ctx, MOE_ERR_CUDA, std::string("apply_updates: ") + cudaGetErrorString((cudaError_t)rc));
+constexpr size_t kStepKeys = 256;  // miss keys read back with the hit bitmap
+
+// Publish the queued updates on `st` (table, slots, stamps, clock) in one
+// kernel that reads them from the pinned list; with clear_step, the step's
+// hit bitmap, miss count and miss bitmap are zeroed too.
+int publish(moe_ctx *ctx, cudaStream_t st, bool clear_step = false) {
+    const int na = clear_step ? ctx->n_tensors * ctx->hit_words + 1 : 0;
+    const int nb = clear_step ? ctx->n_tensors * ctx->bitmap_words : 0;
+    int rc = moe::launch_step_finish(ctx->d_upd, ctx->n_upd, ctx->d_tbl, ctx->d_slot, ctx->d_stamps, ctx->d_clock,
+                                     (uint32_t)ctx->clock, ctx->d_stepbuf, na, ctx->d_bitmap, nb, st);
+    if (rc) return fail(ctx, MOE_ERR_CUDA, std::string("step finish: ") + cudaGetErrorString((cudaError_t)rc));
     ctx->n_upd = 0;
     return MOE_OK;
 }
@@ -298,8 +304,13 @@ int moe_layer_init(const moe_cfg *cfg, void *cuda_stream, moe_ctx **out) {
     CKI(cudaMemset(ctx->d_stamps, 0, sizeof(uint32_t) * (size_t)nt * std::max(1, ctx->spt)));
     CKI(cudaMalloc(&ctx->d_bitmap, sizeof(uint32_t) * (size_t)nt * ctx->bitmap_words));
     CKI(cudaMemset(ctx->d_bitmap, 0, sizeof(uint32_t) * (size_t)nt * ctx->bitmap_words));
-    CKI(cudaMalloc(&ctx->d_misslog, sizeof(uint32_t) * (1 + (size_t)ctx->miss_cap)));
-    CKI(cudaMemset(ctx->d_misslog, 0, sizeof(uint32_t)));
+    ctx->hit_words = (std::max(1, ctx->spt) + 31) / 32;
+    {
+        const size_t hb = (size_t)nt * ctx->hit_words;
+        CKI(cudaMalloc(&ctx->d_stepbuf, sizeof(uint32_t) * (hb + 1 + (size_t)ctx->miss_cap)));
+        CKI(cudaMemset(ctx->d_stepbuf, 0, sizeof(uint32_t) * (hb + 1)));
+        ctx->d_misslog = ctx->d_stepbuf + hb;
+    }
     CKI(cudaMalloc(&ctx->d_clock, sizeof(uint32_t)));
     CKI(cudaMemset(ctx->d_clock, 0, sizeof(uint32_t)));
     CKI(cudaMalloc(&ctx->d_cold, sizeof(unsigned long long)));
@@ -365,11 +376,12 @@ int moe_layer_init(const moe_cfg *cfg, void *cuda_stream, moe_ctx **out) {
         }
     }
 
-    CKI(cudaHostAlloc(&ctx->h_readback, sizeof(uint32_t) * (1 + (size_t)ctx->miss_cap), cudaHostAllocDefault));
     CKI(cudaHostAlloc(&ctx->h_stamps, sizeof(uint32_t) * (size_t)nt * std::max(1, ctx->spt), cudaHostAllocDefault));
     ctx->upd_cap = 6 * nt * E + 64;
-    CKI(cudaHostAlloc(&ctx->h_upd, sizeof(Update) * (size_t)ctx->upd_cap, cudaHostAllocDefault));
-    CKI(cudaMalloc(&ctx->d_upd, sizeof(Update) * (size_t)ctx->upd_cap));
+    CKI(cudaHostAlloc(&ctx->h_upd, sizeof(Update) * (size_t)ctx->upd_cap, cudaHostAllocMapped));
+    CKI(cudaHostGetDevicePointer((void **)&ctx->d_upd, ctx->h_upd, 0));
+    CKI(cudaHostAlloc(&ctx->h_step, sizeof(uint32_t) * ((size_t)nt * ctx->hit_words + 1 + kStepKeys),
+                      cudaHostAllocDefault));
     CKI(cudaDeviceSynchronize());
 #undef CKI
     ctx->t.resize(nt);
@@ -503,6 +515,8 @@ static int ffn_forward_impl(moe_ctx *ctx, int layer, const float *d_x, int n_tok
     gp.cv.slots_per_tensor = std::max(1, ctx->spt);
     gp.cv.bitmap_words = ctx->bitmap_words;
     gp.cv.miss_cap = ctx->miss_cap;
+    gp.cv.hit_bitmap = ctx->d_stepbuf;
+    gp.cv.hit_words = ctx->hit_words;
     gp.tid_gate = layer * 3 + 0;
     gp.tid_up = layer * 3 + 1;
     gp.tid_down = layer * 3 + 2;
@@ -684,32 +698,40 @@ int cache_step(moe_ctx *ctx, int n_tokens) {
     if (n_tokens < 0) return fail(ctx, MOE_ERR_ARG, "cache_step: n_tokens < 0");
     CK(cudaSetDevice(ctx->dev));
     const int nt = ctx->n_tensors, spt = std::max(1, ctx->spt);
-    const size_t fast = std::min<size_t>(ctx->miss_cap, 4096);
-    // read back the miss log and the stamps after the forwards issued so far
-    CK(cudaMemcpyAsync(ctx->h_readback, ctx->d_misslog, sizeof(uint32_t) * (1 + fast), cudaMemcpyDeviceToHost,
-                       ctx->stream));
-    CK(cudaMemcpyAsync(ctx->h_stamps, ctx->d_stamps, sizeof(uint32_t) * (size_t)nt * spt, cudaMemcpyDeviceToHost,
+    const size_t hb = (size_t)nt * ctx->hit_words;
+    const size_t fast = std::min<size_t>(ctx->miss_cap, kStepKeys);
+    // one read-back after the forwards issued so far: hit bitmap, miss count
+    // and the first keys (the stamps are read only for tensors that admit)
+    CK(cudaMemcpyAsync(ctx->h_step, ctx->d_stepbuf, sizeof(uint32_t) * (hb + 1 + fast), cudaMemcpyDeviceToHost,
                        ctx->stream));
     CK(cudaEventRecord(ctx->ev_fwd, ctx->stream));
     int rc = wait_event(ctx, ctx->ev_fwd);
     if (rc) return rc;
-    size_t n_miss = std::min<size_t>(ctx->h_readback[0], ctx->miss_cap);
-    if (n_miss > fast) {
-        CK(cudaMemcpy(ctx->h_readback + 1 + fast, ctx->d_misslog + 1 + fast, sizeof(uint32_t) * (n_miss - fast),
+    const uint32_t *hits = ctx->h_step;
+    const size_t n_miss = std::min<size_t>(ctx->h_step[hb], ctx->miss_cap);
+    std::vector<uint32_t> keys(n_miss);
+    std::copy(ctx->h_step + hb + 1, ctx->h_step + hb + 1 + std::min(n_miss, fast), keys.begin());
+    if (n_miss > fast)
+        CK(cudaMemcpy(keys.data() + fast, ctx->d_misslog + 1 + fast, sizeof(uint32_t) * (n_miss - fast),
                       cudaMemcpyDeviceToHost));
-    }
-    std::vector<uint32_t> keys(ctx->h_readback + 1, ctx->h_readback + 1 + n_miss);
     std::sort(keys.begin(), keys.end());
     keys.erase(std::unique(keys.begin(), keys.end()), keys.end());
 
     ctx->clock += (uint64_t)n_tokens;
     const uint64_t clk = ctx->clock;
     const uint32_t clk32 = (uint32_t)clk;
+    // hits of the step: pool slots (with an owner) whose bit is set
     for (int tid = 0; tid < nt; ++tid) {
         const TensorState &ts = ctx->t[tid];
         if (!ts.registered) continue;
-        for (int s = 0; s < ts.capacity; ++s)
-            if (ts.owner[s] >= 0 && ctx->h_stamps[(size_t)tid * spt + s] == clk32) ctx->stats.hits++;
+        for (int w = 0; w < ctx->hit_words; ++w) {
+            uint32_t m = hits[(size_t)tid * ctx->hit_words + w];
+            while (m) {
+                const int sl = w * 32 + __builtin_ctz(m);
+                m &= m - 1;
+                if (sl < ts.capacity && ts.owner[sl] >= 0) ctx->stats.hits++;
+            }
+        }
     }
     ctx->stats.misses += keys.size();
     ctx->stats.steps++;
@@ -719,7 +741,8 @@ int cache_step(moe_ctx *ctx, int n_tokens) {
     }
 
     ctx->n_upd = 0;
-    int fault = 0, swaps = 0;
+    int fault = 0, swaps = 0, uploads = 0;
+    std::vector<char> fresh;  // tensors whose stamp mirror was read back this step
     if (ctx->n_lent == 0) {
         for (uint32_t key : keys) {
             const int tid = (int)(key >> 12), e = (int)(key & 0xfff);
@@ -731,6 +754,14 @@ int cache_step(moe_ctx *ctx, int n_tokens) {
                 continue;
             }
             if (ctx->cfg.max_swaps_per_step && swaps >= ctx->cfg.max_swaps_per_step) continue;
+            if (fresh.empty()) fresh.assign(nt, 0);
+            if (!fresh[tid]) {
+                // the device stamps of this tensor (the stream is idle here),
+                // before this step's first admission into it edits the mirror
+                CK(cudaMemcpy(ctx->h_stamps + (size_t)tid * spt, ctx->d_stamps + (size_t)tid * spt,
+                              sizeof(uint32_t) * spt, cudaMemcpyDeviceToHost));
+                fresh[tid] = 1;
+            }
             int slot = -1;
             for (int s = 0; s < ts.capacity; ++s)
                 if (!ts.lent[s] && ts.owner[s] < 0) {
@@ -766,6 +797,7 @@ int cache_step(moe_ctx *ctx, int n_tokens) {
             const uint64_t dst = pool_addr(ctx, tid, slot);
             CK(cudaMemcpyAsync((void *)(uintptr_t)dst, ts.home + (size_t)e * ctx->stride, ctx->blob,
                                cudaMemcpyHostToDevice, ctx->up));
+            uploads++;
             set_entry(ctx, tid, e, dst, slot);
             ts.owner[slot] = e;
             ts.last_seen[e] = -1;
@@ -775,12 +807,14 @@ int cache_step(moe_ctx *ctx, int n_tokens) {
             ctx->stats.upload_bytes += ctx->blob;
         }
     }
-    rc = publish(ctx, ctx->up);
+    if (uploads) {
+        // the table entries of this step's admissions flip once their uploads
+        // (side stream) are in
+        CK(cudaEventRecord(ctx->ev_up, ctx->up));
+        CK(cudaStreamWaitEvent(ctx->stream, ctx->ev_up, 0));
+    }
+    rc = publish(ctx, ctx->stream, true);
     if (rc) return rc;
-    CK(cudaMemsetAsync(ctx->d_bitmap, 0, sizeof(uint32_t) * (size_t)nt * ctx->bitmap_words, ctx->up));
-    CK(cudaMemsetAsync(ctx->d_misslog, 0, sizeof(uint32_t), ctx->up));
-    CK(cudaEventRecord(ctx->ev_up, ctx->up));
-    CK(cudaStreamWaitEvent(ctx->stream, ctx->ev_up, 0));
     ctx->stats.clock = clk;
     if (fault) return fail(ctx, MOE_ERR_FAULT, "injected upload failure (admission rolled back)");
     return MOE_OK;
@@ -804,7 +838,8 @@ int miss_drain(moe_ctx *ctx, uint32_t *host_out, size_t cap, size_t *n_out) {
         memcpy(host_out, keys.data(), sizeof(uint32_t) * keys.size());
     }
     CK(cudaMemsetAsync(ctx->d_bitmap, 0, sizeof(uint32_t) * (size_t)ctx->n_tensors * ctx->bitmap_words, ctx->stream));
-    CK(cudaMemsetAsync(ctx->d_misslog, 0, sizeof(uint32_t), ctx->stream));
+    CK(cudaMemsetAsync(ctx->d_stepbuf, 0, sizeof(uint32_t) * ((size_t)ctx->n_tensors * ctx->hit_words + 1),
+                       ctx->stream));
     CK(cudaStreamSynchronize(ctx->stream));
     return MOE_OK;
 }
@@ -927,7 +962,7 @@ void moe_destroy(moe_ctx *ctx) {
     cudaFree(ctx->d_slot);
     cudaFree(ctx->d_stamps);
     cudaFree(ctx->d_bitmap);
-    cudaFree(ctx->d_misslog);
+    cudaFree(ctx->d_stepbuf);
     cudaFree(ctx->d_clock);
     cudaFree(ctx->d_cold);
     cudaFree(ctx->xq);
@@ -938,7 +973,6 @@ void moe_destroy(moe_ctx *ctx) {
     cudaFree(ctx->hds);
     cudaFree(ctx->o);
     cudaFree(ctx->counters);
-    cudaFree(ctx->d_upd);
     cudaFree(ctx->xs16);
     cudaFree(ctx->xdT);
     cudaFree(ctx->hq16);
@@ -948,9 +982,9 @@ void moe_destroy(moe_ctx *ctx) {
     cudaFree(ctx->etbl);
     cudaFree(ctx->stage_jobs);
     cudaFree(ctx->stage_n);
-    if (ctx->h_readback) cudaFreeHost(ctx->h_readback);
     if (ctx->h_stamps) cudaFreeHost(ctx->h_stamps);
     if (ctx->h_upd) cudaFreeHost(ctx->h_upd);
+    if (ctx->h_step) cudaFreeHost(ctx->h_step);
     for (cudaEvent_t e : ctx->tev) cudaEventDestroy(e);
     if (ctx->ev_fwd) cudaEventDestroy(ctx->ev_fwd);
     if (ctx->ev_up) cudaEventDestroy(ctx->ev_up);

@@ -99,6 +99,7 @@ def test_decode_b1_pool25_state_every_step():
         st = qec.moe_stats(m.ctx)
         assert st["admissions"] == m.policy.stats["admissions"] > 0
         assert st["evictions"] == m.policy.stats["evictions"] > 0
+        assert st["hits"] == m.policy.stats["hits"] and st["misses"] == m.policy.stats["misses"]
     finally:
         m.close()
 
