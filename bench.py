@@ -49,6 +49,10 @@ def parse():
     ap.add_argument("--cpu-sample-steps", type=int, default=6)
     ap.add_argument("--prefill-steps", type=int, default=2)
     ap.add_argument("--prefill-workload", default="prefill_t4096")
+    ap.add_argument("--case", default=None, choices=["decode_layer", "prefill_layer"],
+                    help="small profiling case: one layer (hidden 2048, 512 experts, top-8, FFN 1152, every "
+                         "expert resident), --launches forwards at batch 1 (routed) or 4096 tokens")
+    ap.add_argument("--launches", type=int, default=20)
     return ap.parse_args()
 
 
@@ -222,11 +226,26 @@ def run_ours(args):
     y = torch.empty((L, T, H), device="cuda")
     sptr = stream.cuda_stream
 
-    def layers():
+    # the fully resident layers, timed as one segment inside the step graph
+    # (two event nodes; the launches between them stay chained)
+    resident = [l for l in range(L) if wl.layer_capacity(l) == E]
+    seg = None
+    if resident and resident == list(range(resident[0], resident[-1] + 1)) and not args.no_graph:
+        try:
+            seg = (torch.cuda.Event(enable_timing=True, external=True),
+                   torch.cuda.Event(enable_timing=True, external=True))
+        except TypeError:
+            seg = None
+
+    def layers(mark=False):
         # router top-k + expert FFN per layer (one launch per layer for
         # small batches: every CTA routes the tokens itself)
         for l in range(L):
+            if mark and seg is not None and l == resident[0]:
+                seg[0].record(stream)
             qec.moe_ffn_forward_routed(ctx, l, xin[l], lin[l], T, idx[l], w[l], y[l], sptr)
+            if mark and seg is not None and l == resident[-1]:
+                seg[1].record(stream)
 
     graph = None
     if not args.no_graph:
@@ -239,7 +258,7 @@ def run_ours(args):
         qec.miss_drain(ctx)
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=stream):
-            layers()
+            layers(mark=True)
     launches_per_step = L * (1 if T * k <= 256 else 4) + 1  # per layer + the table update kernel
     used_graph = graph is not None
 
@@ -271,9 +290,14 @@ def run_ours(args):
     barrier()
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    seg_ms, seg_n = 0.0, 0
     ev0.record(stream)
     for s in range(args.warmup, S):
         step(s)
+        if seg is not None:
+            # cache_step has waited for this step's forwards
+            seg_ms += seg[0].elapsed_time(seg[1])
+            seg_n += 1
     ev1.record(stream)
     stream.synchronize()
     clk = clocks.stop()
@@ -305,30 +329,38 @@ def run_ours(args):
     e2e_tok = world * args.steps * T / e2e_s
     log(f"e2e: {e2e_tok:.1f} tokens/s")
 
-    # roofline of the fused expert-FFN layer kernel (gate/up + SwiGLU + down +
-    # combine, one launch per layer) over the fully resident layers: CUDA
-    # events on the context stream around each launch, in a pass of eager
-    # steps after the timed one (event nodes inside a graph do not bracket
-    # kernel execution)
-    qec.moe_debug_timing(ctx, True)
-    graph = None
-    resident = [l for l in range(L) if wl.layer_capacity(l) == E]
+    # roofline of the fused expert-FFN layer kernel (routing, gate/up, SwiGLU,
+    # down and combine in one launch per layer) over the fully resident
+    # layers: their segment of every timed step graph (CUDA events on the
+    # context stream), algorithmic bytes = the weights of the experts each
+    # launch uses (3 tensors) + x and y
     blob = wl.tensor_bytes(0)
-    gu_ms, dn_ms, gu_bytes, dn_bytes, n_launch = 0.0, 0.0, 0, 0, 0
-    n_roof = min(args.steps, 32)
-    for s in range(args.warmup, args.warmup + n_roof):
-        step(s)
-        g_ms, d_ms = qec.moe_debug_timing_read(ctx, L)
-        uniq = [len(np.unique(LGh[s, l].argsort(axis=1)[:, -k:])) for l in resident]
-        for j, l in enumerate(resident):
-            gu_ms += g_ms[l]
-            dn_ms += d_ms[l]
-            # weights of the used experts (3 tensors) + x (fp32) + y (fp32)
-            gu_bytes += uniq[j] * 3 * blob + T * H * 4 + T * H * 4
-            n_launch += 1
-    qec.moe_debug_timing(ctx, False)
     peaks, peak_src = load_peaks()
-    achieved = gu_bytes / (gu_ms / 1e3) / 1e9
+    if seg is not None and seg_n > 0:
+        alg = 0
+        for s in range(args.warmup, S):
+            for l in resident:
+                alg += len(np.unique(LGh[s, l].argsort(axis=1)[:, -k:])) * 3 * blob + 2 * T * H * 4
+        n_launch = seg_n * len(resident)
+        launch_us = 1e3 * seg_ms / n_launch
+        achieved = alg / (seg_ms / 1e3) / 1e9
+        roof_how = "segment of the timed step graph: fully resident layers, events around the segment"
+    else:
+        # eager pass with events around each launch (no graph)
+        graph = None
+        qec.moe_debug_timing(ctx, True)
+        gu_ms, alg, n_launch = 0.0, 0, 0
+        for s in range(args.warmup, args.warmup + min(args.steps, 32)):
+            step(s)
+            g_ms, _ = qec.moe_debug_timing_read(ctx, L)
+            for l in resident:
+                gu_ms += g_ms[l]
+                alg += len(np.unique(LGh[s, l].argsort(axis=1)[:, -k:])) * 3 * blob + 2 * T * H * 4
+                n_launch += 1
+        qec.moe_debug_timing(ctx, False)
+        launch_us = 1e3 * gu_ms / max(1, n_launch)
+        achieved = alg / (gu_ms / 1e3) / 1e9
+        roof_how = "eager launches, events around each launch"
     traffic = read_traffic("decode_layer_kernel_decode_b1.txt", "bench.traffic_bytes_per_launch")
 
     # bytes of the whole step (weights of the unique experts of every layer)
@@ -355,8 +387,8 @@ def run_ours(args):
                      "achieved": round(achieved, 1),
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                      "peak_source": f"{peak_src} hbm_gbs (copy)", "traffic": traffic,
-                     "algorithmic_bytes_per_launch": round(gu_bytes / max(1, n_launch)),
-                     "avg_launch_us": round(1e3 * gu_ms / max(1, n_launch), 3)},
+                     "algorithmic_bytes_per_launch": round(alg / max(1, n_launch)),
+                     "avg_launch_us": round(launch_us, 3), "launches": n_launch, "timing": roof_how},
         "step_weight_gbs": round(step_bytes / (ms_max / args.steps / 1e3) / 1e9, 1),
         "host_link": {"zero_copy_read_gbs": round(zc_gbs, 1), "copy_engine_h2d_gbs": round(ce_gbs, 1)},
         "cache": {"hits": st_main["hits"], "misses": st_main["misses"], "admissions": st_main["admissions"],
@@ -376,6 +408,41 @@ def run_ours(args):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def run_case(args):
+    """One layer of the decode / prefill workload shape with every expert
+    resident, args.launches forwards on fresh seeded inputs, each timed with
+    CUDA events; the small case that profiler captures run."""
+    import torch
+    import quantized_expert_cache_gb300 as qec
+    import synth
+    qec.load()
+    H, F, E, k = 2048, 1152, 512, 8
+    T = 1 if args.case == "decode_layer" else 4096
+    n = max(3, args.launches)
+    wl = synth.Workload("case", H, E, k, F, 1, routing="zipf", zipf_s=1.1, capacity=[E])
+    st = torch.cuda.current_stream()
+    ctx = qec.moe_layer_init(H, F, E, k, 1, E, T, stream=st.cuda_stream)
+    for kind in range(3):
+        rows, cols = wl.tensor_shapes[kind]
+        qec.register_expert_tensor(ctx, 0, kind, wl.expert_tensor(0, kind), rows, cols, E, wl.seed_order(0), E)
+    xs = [torch.from_numpy(wl.x(0, s, T)).cuda() for s in range(n)]
+    lgs = [torch.from_numpy(wl.logits(0, s, T)).cuda() for s in range(n)]
+    idx = torch.empty((n, T, k), dtype=torch.int32, device="cuda")
+    w = torch.empty((n, T, k), device="cuda")
+    y = torch.empty((T, H), device="cuda")
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for s in range(n):
+        evs[s][0].record(st)
+        qec.moe_ffn_forward_routed(ctx, 0, xs[s], lgs[s], T, idx[s], w[s], y, st.cuda_stream)
+        evs[s][1].record(st)
+    torch.cuda.synchronize()
+    ms = [a.elapsed_time(b) for a, b in evs]
+    qec.moe_destroy(ctx)
+    print(json.dumps({"case": args.case, "tokens": T, "launches": n,
+                      "median_ms_per_forward": round(float(np.median(ms[2:])), 5)}), flush=True)
 
 
 def run_prefill_leg(args, qec, synth, torch, log):
@@ -517,7 +584,9 @@ def run_reference(args):
 
 if __name__ == "__main__":
     a = parse()
-    if a.impl == "reference":
+    if a.case:
+        run_case(a)
+    elif a.impl == "reference":
         run_reference(a)
     else:
         run_ours(a)
