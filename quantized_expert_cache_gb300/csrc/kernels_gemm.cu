@@ -71,8 +71,8 @@ struct Cfg {
     static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
     static constexpr int SMEM = MISC_OFF + 16 + 1024;  // + alignment slack
     // epilogue warps: EPI_SPLIT per TMEM lane quarter, each owning BN / EPI_SPLIT
-    // token columns (gate/up: 16 warps; down, one tensor: 8)
-    static constexpr int N_EPI = DUAL ? 16 : 8;
+    // token columns (32 for gate/up with its two tensors, 64 for down)
+    static constexpr int N_EPI = 8;
     static constexpr int EPI_SPLIT = N_EPI / 4;
     static constexpr int NTHREADS = (W_EPI + N_EPI) * 32;
 };
@@ -89,12 +89,16 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 __device__ __forceinline__ void mbar_arrive_tx(uint32_t bar, uint32_t tx) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(tx) : "memory");
 }
+// One try: the thread is suspended (not spinning) until the phase completes
+// or about kSuspendNs pass, so waiting warps leave their issue slots to the
+// converter and epilogue warps.
+constexpr uint32_t kSuspendNs = 20000;
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
-        "{\n.reg .pred P;\nmbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2;\nselp.u32 %0, 1, 0, P;\n}"
+        "{\n.reg .pred P;\nmbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2, %3;\nselp.u32 %0, 1, 0, P;\n}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(kSuspendNs)
         : "memory");
     return ok != 0;
 }
@@ -175,6 +179,45 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// 16 consecutive TMEM columns of this warp's 32 lanes (raw fp32 bits)
+__device__ __forceinline__ void tmem_ld16u(uint32_t taddr, uint32_t *r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+// 32 consecutive TMEM columns of this warp's 32 lanes (one fp32 per column)
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t *r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+
+// Packed fp32 pairs (two IEEE round-to-nearest operations per instruction).
+__device__ __forceinline__ unsigned long long pk2(uint32_t lo, uint32_t hi) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+    return r;
+}
+// acc{0,1} += sum{0,1} * (dw * da{0,1}): the scale products and the
+// accumulation as packed fp32 pairs (mul.rn.f32x2, fma.rn.f32x2).
+__device__ __forceinline__ void fma_scaled2(float &acc0, float &acc1, uint32_t sum0, uint32_t sum1, float da0, float da1,
+                                            float dw) {
+    asm("{\n.reg .b64 a, p, d, w, s;\n"
+        "mov.b64 a, {%0, %1};\nmov.b64 p, {%2, %3};\nmov.b64 d, {%4, %5};\nmov.b64 w, {%6, %6};\n"
+        "mul.rn.f32x2 s, w, d;\nfma.rn.f32x2 a, p, s, a;\nmov.b64 {%0, %1}, a;\n}"
+        : "+f"(acc0), "+f"(acc1)
+        : "r"(sum0), "r"(sum1), "f"(da0), "f"(da1), "f"(dw));
+}
+
+
 // acc{0,1} += p{0,1} * s{0,1}, two IEEE fp32 fused multiply-adds.
 __device__ __forceinline__ void fma2(float &a0, float &a1, float p0, float p1, float s0, float s1) {
     unsigned long long acc, pp, ss;
@@ -199,6 +242,19 @@ __device__ __forceinline__ uint32_t nib_pair(uint32_t w, int sel, int hi) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
+// Four codes (one nibble per byte of n, values 0..15) -> two fp16 pairs
+// (q0 - 8, q1 - 8), (q2 - 8, q3 - 8): the bytes are placed under the fp16
+// exponent byte 0x64 (1024 + q, exact) and 1032 is subtracted (exact).
+__device__ __forceinline__ void nib4(uint32_t n, uint32_t &p01, uint32_t &p23) {
+    const __half2 off = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));
+    uint32_t a = __byte_perm(n, 0x64646464u, 0x5150);  // (1024 + q0, 1024 + q1)
+    uint32_t b = __byte_perm(n, 0x64646464u, 0x5352);  // (1024 + q2, 1024 + q3)
+    __half2 ha = __hsub2(*reinterpret_cast<__half2 *>(&a), off);
+    __half2 hb = __hsub2(*reinterpret_cast<__half2 *>(&b), off);
+    p01 = *reinterpret_cast<uint32_t *>(&ha);
+    p23 = *reinterpret_cast<uint32_t *>(&hb);
+}
+
 __device__ __forceinline__ void convert_store_row(uint8_t *tile, int r, uint4 c0, uint4 c1) {
     const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
     uint8_t *rowbase = tile + (r >> 3) * 1024 + (r & 7) * 128;
@@ -209,13 +265,12 @@ __device__ __forceinline__ void convert_store_row(uint8_t *tile, int r, uint4 c0
         for (int part = 0; part < 4; ++part) {
             // part 0: elements 0..7 (low nibbles of bytes 0..7), 1: 8..15
             // (low, bytes 8..15), 2: 16..23 (high, bytes 0..7), 3: 24..31
-            const int hi = part >> 1;
             const uint32_t wa = q[(part & 1) * 2], wb = q[(part & 1) * 2 + 1];
+            const uint32_t na = (part >> 1) ? (wa >> 4) & 0x0F0F0F0Fu : wa & 0x0F0F0F0Fu;
+            const uint32_t nb = (part >> 1) ? (wb >> 4) & 0x0F0F0F0Fu : wb & 0x0F0F0F0Fu;
             uint4 out;
-            out.x = nib_pair(wa, 0x4140, hi);
-            out.y = nib_pair(wa, 0x4342, hi);
-            out.z = nib_pair(wb, 0x4140, hi);
-            out.w = nib_pair(wb, 0x4342, hi);
+            nib4(na, out.x, out.y);
+            nib4(nb, out.z, out.w);
             const int chunk = blk * 4 + part;
             *reinterpret_cast<uint4 *>(rowbase + ((chunk ^ (r & 7)) << 4)) = out;
         }
@@ -242,17 +297,29 @@ __device__ __forceinline__ void decode_tile(int t, const int32_t *tile_off, int 
 }
 
 // Stage cursor over the flattened (tile, K stage) sequence of one CTA.
+// The tile's expert-table entries (weight blobs) and first token position
+// are looked up once per tile, not per stage.
 struct StageCur {
-    int t, kt, u, rt, tt;
+    int t, kt, u, rt, tt, pos0;
+    const uint8_t *blob[2];
     bool valid;
 };
+
+template <int BN>
+__device__ __forceinline__ void cur_tile(StageCur &c, const GemmParams &p, int n_uniq) {
+    decode_tile(c.t, p.tile_off, n_uniq, p.uniq_off, BN, c.u, c.rt, c.tt);
+    const int e = p.uniq_e[c.u];
+    c.blob[0] = (const uint8_t *)(uintptr_t)(p.tbl[0][e] & ~1ull);
+    c.blob[1] = p.tbl[1] ? (const uint8_t *)(uintptr_t)(p.tbl[1][e] & ~1ull) : c.blob[0];
+    c.pos0 = p.uniq_off[c.u] + c.tt * BN;
+}
 
 template <int BN>
 __device__ __forceinline__ void cur_init(StageCur &c, const GemmParams &p, int n_uniq, int total) {
     c.t = blockIdx.x;
     c.kt = 0;
     c.valid = c.t < total;
-    if (c.valid) decode_tile(c.t, p.tile_off, n_uniq, p.uniq_off, BN, c.u, c.rt, c.tt);
+    if (c.valid) cur_tile<BN>(c, p, n_uniq);
 }
 
 template <int BN>
@@ -262,7 +329,7 @@ __device__ __forceinline__ void cur_next(StageCur &c, const GemmParams &p, int n
         c.kt = 0;
         c.t += gridDim.x;
         c.valid = c.t < total;
-        if (c.valid) decode_tile(c.t, p.tile_off, n_uniq, p.uniq_off, BN, c.u, c.rt, c.tt);
+        if (c.valid) cur_tile<BN>(c, p, n_uniq);
     }
 }
 
@@ -368,19 +435,18 @@ __global__ void __launch_bounds__(Cfg<DUAL>::NTHREADS, 1)
         // into raw ring entry s % RR; stage s is then converted into its slot.
         const int r = threadIdx.x - W_CONV * 32;
         uint8_t *raw = smem + C::RAW_OFF;
-        StageCur fc, cc;  // fetch and convert cursors
+        StageCur fc;  // fetch cursor; conversion only counts stages
         cur_init<BN>(fc, p, n_uniq, total);
-        cur_init<BN>(cc, p, n_uniq, total);
+        const int n_stages = blockIdx.x < total ? ((total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1) * nkt : 0;
         auto fetch = [&](const StageCur &c, int rs) {
             uint8_t *ent = raw + rs * C::RAW_BYTES;
             if (c.valid) {
-                const int e = p.uniq_e[c.u];
                 const int row = c.rt * BM + r;
                 const bool vrow = row < p.rows;
                 const int srow = vrow ? row : 0;
 #pragma unroll
                 for (int a = 0; a < NA; ++a) {
-                    const uint8_t *blob = (const uint8_t *)(uintptr_t)(p.tbl[a][e] & ~1ull);
+                    const uint8_t *blob = c.blob[a];
                     const uint8_t *src = blob + ((size_t)srow * nbk + 2 * c.kt) * 16;
                     const uint32_t dst = smem_u32(ent + (a * BM + r) * 32);
                     cp_async(dst, src, 16, vrow);
@@ -388,7 +454,7 @@ __global__ void __launch_bounds__(Cfg<DUAL>::NTHREADS, 1)
                     const uint8_t *ssrc = blob + scale_off + ((size_t)srow * nbk + 2 * c.kt) * 2;
                     cp_async(smem_u32(ent + C::RAW_CODES + (a * BM + r) * 4), ssrc, 4, vrow);
                 }
-                const int pos0 = p.uniq_off[c.u] + c.tt * BN;
+                const int pos0 = c.pos0;
                 for (int i = r; i < 2 * BN; i += 128) {
                     const int q = i / BN, col = i - q * BN;
                     const int pos = pos0 + col;
@@ -404,7 +470,7 @@ __global__ void __launch_bounds__(Cfg<DUAL>::NTHREADS, 1)
             cur_next<BN>(fc, p, n_uniq, total, nkt);
         }
         int it = 0;
-        while (cc.valid) {
+        while (it < n_stages) {
             fetch(fc, (it + C::PD) % C::RR);
             cur_next<BN>(fc, p, n_uniq, total, nkt);
             cp_wait<C::PD>();
@@ -430,16 +496,20 @@ __global__ void __launch_bounds__(Cfg<DUAL>::NTHREADS, 1)
             fence_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(full0 + 8 * slot);
-            cur_next<BN>(cc, p, n_uniq, total, nkt);
             ++it;
         }
         cp_wait<0>();
     } else {
         // epilogue: TMEM lane quarter = warp % 4 (thread = weight row), half =
-        // which BN/2 token columns this warp owns
+        // which HC token columns this warp owns.  Per K stage: one wait (the
+        // MMA's commit after the stage's second block covers the first), the
+        // activation scales of the warp's columns read once per block, the
+        // block sums read 32 columns per TMEM load, and the scaling as packed
+        // fp32 pairs: s = d_w * d_a (mul.f32x2), acc += sum * s (fma.f32x2).
         const int quarter = warp & 3;
         const int half = (warp - W_EPI) >> 2;  // which column part this warp owns
         constexpr int HC = BN / EPI_SPLIT;      // token columns per epilogue warp
+        static_assert(HC % 32 == 0, "32-column groups per epilogue warp");
         const int r = quarter * 32 + lane;
         int qc = 0, it = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
@@ -454,53 +524,69 @@ __global__ void __launch_bounds__(Cfg<DUAL>::NTHREADS, 1)
             for (int a = 0; a < NA; ++a)
 #pragma unroll
                 for (int c = 0; c < HC; ++c) acc[a][c] = 0.0f;
-            for (int kt = 0; kt < nkt; ++kt, ++it) {
+            for (int kt = 0; kt < nkt; ++kt, ++it, qc += 2) {
                 const int slot = it % STAGES;
                 const uint8_t *st = slot_ptr(slot);
+                const int j0 = qc % NTBUF, j1 = (qc + 1) % NTBUF;
                 bool ok = true;
-                // the slot's scales were written before its full barrier completed
-                if (lane == 0) ok = mbar_wait(full0 + 8 * slot, (uint32_t)(it / STAGES) & 1u, abort_flag, p.error, 64);
+                // the slot's scales were written before its full barrier
+                // completed; the second block's commit covers both blocks
+                if (lane == 0) {
+                    ok = mbar_wait(full0 + 8 * slot, (uint32_t)(it / STAGES) & 1u, abort_flag, p.error, 64) &&
+                         mbar_wait(tfull0 + 8 * j1, (uint32_t)((qc + 1) / NTBUF) & 1u, abort_flag, p.error, 32);
+                }
                 ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                 if (!ok) goto epi_done;
-                __half2 wsc[NA];
+                tc_fence_after();
+                uint32_t wsc[NA];
 #pragma unroll
                 for (int a = 0; a < NA; ++a)
-                    wsc[a] = *(const __half2 *)(st + NA * C::A_BYTES + C::B_BYTES + (a * BM + r) * 4);
+                    wsc[a] = *(const uint32_t *)(st + NA * C::A_BYTES + C::B_BYTES + (a * BM + r) * 4);
                 const float *asc = (const float *)(st + NA * C::A_BYTES + C::B_BYTES + C::WS_BYTES) + half * HC;
-                for (int blk = 0; blk < 2; ++blk, ++qc) {
-                    const int j = qc % NTBUF;
-                    if (lane == 0) ok = mbar_wait(tfull0 + 8 * j, (uint32_t)(qc / NTBUF) & 1u, abort_flag, p.error, 32);
-                    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-                    if (!ok) goto epi_done;
-                    tc_fence_after();
+#pragma unroll
+                for (int blk = 0; blk < 2; ++blk) {
+                    const int j = blk ? j1 : j0;
                     const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(j * C::TBUF + half * HC);
-                    const float *dq = asc + blk * BN;
+                    float dw[NA];
 #pragma unroll
                     for (int a = 0; a < NA; ++a) {
-                        // up to 32 columns loaded per wait
-                        constexpr int LC = HC < 32 ? HC : 32;
-                        const float dw = blk ? __high2float(wsc[a]) : __low2float(wsc[a]);
+                        const uint32_t dwb = blk ? (wsc[a] >> 16) : (wsc[a] & 0xffffu);
+                        dw[a] = __half2float(__ushort_as_half((unsigned short)dwb));
+                    }
+                    const float2 *dq2 = reinterpret_cast<const float2 *>(asc + blk * BN);
 #pragma unroll
-                        for (int cb = 0; cb < HC; cb += LC) {
-                            float pv[LC];
+                    for (int cb = 0; cb < HC; cb += 16) {
 #pragma unroll
-                            for (int c0 = 0; c0 < LC; c0 += 16) tmem_ld16(tb + (uint32_t)(a * BN + cb + c0), pv + c0);
+                        for (int a = 0; a < NA; ++a) {
+                            // block sums of 16 columns of tensor a
+                            uint32_t pv[16];
+                            tmem_ld16u(tb + (uint32_t)(a * BN + cb), pv);
                             tmem_ld_wait();
 #pragma unroll
-                            for (int c = 0; c < LC; c += 2) {
-                                const float2 d2 = *reinterpret_cast<const float2 *>(dq + cb + c);
-                                fma2(acc[a][cb + c], acc[a][cb + c + 1], pv[c], pv[c + 1], dw * d2.x, dw * d2.y);
+                            for (int c = 0; c < 8; ++c) {
+                                const float2 d2 = dq2[(cb >> 1) + c];  // activation scales: broadcast reads
+                                fma_scaled2(acc[a][cb + 2 * c], acc[a][cb + 2 * c + 1], pv[2 * c], pv[2 * c + 1], d2.x,
+                                            d2.y, dw[a]);
                             }
                         }
                     }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(tempty0 + 8 * j);
                 }
+                tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(empty0 + 8 * slot);
+                if (lane == 0) {
+                    mbar_arrive(tempty0 + 8 * j0);
+                    mbar_arrive(tempty0 + 8 * j1);
+                    mbar_arrive(empty0 + 8 * slot);
+                }
             }
-            // tile outputs (this warp's token columns)
+            // tile outputs (this warp's token columns); the assignment ids of
+            // the columns are fetched once (lane i: columns i, i + 32, ...)
+            int asg_l[HC / 32];
+#pragma unroll
+            for (int i = 0; i < HC / 32; ++i) {
+                const int pos = pos0 + i * 32 + lane;
+                asg_l[i] = pos < pos_end ? __ldg(p.assign + pos) : 0;
+            }
             if (DUAL) {
                 const int fb = (rt * BM + quarter * 32) / kBlock;  // h block index along F
                 const bool vblk = rt * BM + quarter * 32 < p.rows;
@@ -514,8 +600,8 @@ __global__ void __launch_bounds__(Cfg<DUAL>::NTHREADS, 1)
                     int qv = 0;
                     if (dd != 0.0f) qv = (int)fminf(fmaxf(rintf(h / dd), -127.0f), 127.0f);
                     const int s = warp_sum_i(qv);
+                    const int a = __shfl_sync(0xffffffffu, asg_l[c / 32], c % 32);
                     if (vblk && pos < pos_end) {
-                        const int a = p.assign[pos];
                         p.hq16[(size_t)pos * p.F_out + row] = __int2half_rn(qv);
                         p.hq[(size_t)a * p.F_out + row] = (int8_t)qv;
                         if (lane == 0) {
@@ -528,7 +614,8 @@ __global__ void __launch_bounds__(Cfg<DUAL>::NTHREADS, 1)
 #pragma unroll
                 for (int c = 0; c < HC; ++c) {
                     const int pos = pos0 + c;
-                    if (vrow && pos < pos_end) p.o[(size_t)p.assign[pos] * p.rows + row] = acc[0][c];
+                    const int a = __shfl_sync(0xffffffffu, asg_l[c / 32], c % 32);
+                    if (vrow && pos < pos_end) p.o[(size_t)a * p.rows + row] = acc[0][c];
                 }
             }
         }
