@@ -69,6 +69,7 @@ struct FusedParams {
 // One grouped GEMM launch (gate/up with SwiGLU + h quantization, or down).
 struct GemmParams {
     const int32_t *n_uniq, *uniq_e, *uniq_off, *tile_off, *assign;
+    const uint2 *tile_rec;      // per tile: (u | row tile << 16, token tile | valid columns << 16)
     const uint64_t *tbl[2];     // expert tables of the A operands (gate, up) or (down, -)
     const float *a_scaleT;      // [K/32][A_pad]: block scales of the sorted activation rows
     int rows, K;                // weight rows (output features) and reduction length
@@ -85,6 +86,8 @@ struct TilingParams {
     CacheView cv;
     const int32_t *n_uniq, *uniq_e, *uniq_off;
     int32_t *tile_off_gu, *tile_off_dn;
+    uint2 *rec_gu, *rec_dn;
+    int cap_gu, cap_dn;
     int tid0, n_tokens, rt_gu, bn_gu, rt_dn, bn_dn;
 };
 

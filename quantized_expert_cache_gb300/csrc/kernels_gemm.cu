@@ -277,37 +277,29 @@ __device__ __forceinline__ void convert_store_row(uint8_t *tile, int r, uint4 c0
     }
 }
 
-// tile index -> (used expert u, row tile, token tile); token tile innermost.
-__device__ __forceinline__ void decode_tile(int t, const int32_t *tile_off, int n_uniq, const int32_t *uniq_off,
-                                            int bn, int &u, int &row_tile, int &tok_tile) {
-    int lo = 0, hi = n_uniq - 1;
-    while (lo < hi) {
-        int mid = (lo + hi + 1) >> 1;
-        if (tile_off[mid] <= t)
-            lo = mid;
-        else
-            hi = mid - 1;
-    }
-    u = lo;
-    const int n = uniq_off[u + 1] - uniq_off[u];
-    const int ntok = (n + bn - 1) / bn;
-    const int local = t - tile_off[u];
-    row_tile = local / ntok;
-    tok_tile = local - row_tile * ntok;
+// tile index -> (used expert u, row tile, token tile, valid token columns),
+// from the per-tile records the tiling kernel writes (token tile innermost).
+__device__ __forceinline__ void decode_tile(const uint2 *rec, int t, int &u, int &row_tile, int &tok_tile,
+                                            int &ncols) {
+    const uint2 r = __ldg(rec + t);
+    u = (int)(r.x & 0xffffu);
+    row_tile = (int)(r.x >> 16);
+    tok_tile = (int)(r.y & 0xffffu);
+    ncols = (int)(r.y >> 16);
 }
 
 // Stage cursor over the flattened (tile, K stage) sequence of one CTA.
 // The tile's expert-table entries (weight blobs) and first token position
 // are looked up once per tile, not per stage.
 struct StageCur {
-    int t, kt, u, rt, tt, pos0;
+    int t, kt, u, rt, tt, nc, pos0;
     const uint8_t *blob[2];
     bool valid;
 };
 
 template <int BN>
 __device__ __forceinline__ void cur_tile(StageCur &c, const GemmParams &p, int n_uniq) {
-    decode_tile(c.t, p.tile_off, n_uniq, p.uniq_off, BN, c.u, c.rt, c.tt);
+    decode_tile(p.tile_rec, c.t, c.u, c.rt, c.tt, c.nc);
     const int e = p.uniq_e[c.u];
     c.blob[0] = (const uint8_t *)(uintptr_t)(p.tbl[0][e] & ~1ull);
     c.blob[1] = p.tbl[1] ? (const uint8_t *)(uintptr_t)(p.tbl[1][e] & ~1ull) : c.blob[0];
@@ -382,8 +374,8 @@ __global__ void __launch_bounds__(Cfg<DUAL>::NTHREADS, 1)
         if (lane == 0) {
             int it = 0;
             for (int t = blockIdx.x; t < total; t += gridDim.x) {
-                int u, rt, tt;
-                decode_tile(t, p.tile_off, n_uniq, p.uniq_off, BN, u, rt, tt);
+                int u, rt, tt, nc;
+                decode_tile(p.tile_rec, t, u, rt, tt, nc);
                 const int pos0 = p.uniq_off[u] + tt * BN;
                 for (int kt = 0; kt < nkt; ++kt, ++it) {
                     const int slot = it % STAGES;
@@ -397,9 +389,15 @@ __global__ void __launch_bounds__(Cfg<DUAL>::NTHREADS, 1)
         }
     } else if (warp == W_MMA) {
         if (lane == 0) {
-            const uint32_t idesc = idesc_f16(BM, BN);
             int it = 0, qc = 0;
+            // the tile's MMA width: its valid token columns rounded up to 16
+            // (the record of the next tile is requested a tile ahead)
+            uint2 rec_next = blockIdx.x < total ? __ldg(p.tile_rec + blockIdx.x) : make_uint2(0, 0);
             for (int t = blockIdx.x; t < total; t += gridDim.x) {
+                const int ncols = (int)(rec_next.y >> 16);
+                if (t + (int)gridDim.x < total) rec_next = __ldg(p.tile_rec + t + gridDim.x);
+                const int nmma = min(BN, (ncols + 15) & ~15);
+                const uint32_t idesc = idesc_f16(BM, nmma < 16 ? 16 : nmma);
                 for (int kt = 0; kt < nkt; ++kt, ++it) {
                     const int slot = it % STAGES;
                     if (!mbar_wait(full0 + 8 * slot, (uint32_t)(it / STAGES) & 1u, abort_flag, p.error, 4))
@@ -513,8 +511,9 @@ __global__ void __launch_bounds__(Cfg<DUAL>::NTHREADS, 1)
         const int r = quarter * 32 + lane;
         int qc = 0, it = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
-            int u, rt, tt;
-            decode_tile(t, p.tile_off, n_uniq, p.uniq_off, BN, u, rt, tt);
+            int u, rt, tt, ncols;
+            decode_tile(p.tile_rec, t, u, rt, tt, ncols);
+            const int ncw = ncols - half * HC;  // this warp's valid columns (may be <= 0)
             const int row = rt * BM + r;
             const bool vrow = row < p.rows;
             const int pos0 = p.uniq_off[u] + tt * BN + half * HC;
@@ -556,6 +555,7 @@ __global__ void __launch_bounds__(Cfg<DUAL>::NTHREADS, 1)
                     const float2 *dq2 = reinterpret_cast<const float2 *>(asc + blk * BN);
 #pragma unroll
                     for (int cb = 0; cb < HC; cb += 16) {
+                        if (cb >= ncw) break;  // columns past the tile's tokens (warp-uniform)
 #pragma unroll
                         for (int a = 0; a < NA; ++a) {
                             // block sums of 16 columns of tensor a
@@ -592,6 +592,7 @@ __global__ void __launch_bounds__(Cfg<DUAL>::NTHREADS, 1)
                 const bool vblk = rt * BM + quarter * 32 < p.rows;
 #pragma unroll
                 for (int c = 0; c < HC; ++c) {
+                    if (c >= ncw) break;  // warp-uniform
                     const int pos = pos0 + c;
                     const float g = acc[0][c], uu = acc[NA - 1][c];
                     const float h = g * uu / (1.0f + expf(-g));
@@ -613,6 +614,7 @@ __global__ void __launch_bounds__(Cfg<DUAL>::NTHREADS, 1)
             } else {
 #pragma unroll
                 for (int c = 0; c < HC; ++c) {
+                    if (c >= ncw) break;  // warp-uniform
                     const int pos = pos0 + c;
                     const int a = __shfl_sync(0xffffffffu, asg_l[c / 32], c % 32);
                     if (vrow && pos < pos_end) p.o[(size_t)a * p.rows + row] = acc[0][c];
@@ -699,6 +701,25 @@ __global__ void tiling_kernel(TilingParams p) {
         run_gu += warp_tot[0];
         run_dn += warp_tot[1];
         __syncthreads();
+    }
+    __syncthreads();
+    // per-tile records: (u | row tile << 16, token tile | valid columns << 16)
+    for (int u = threadIdx.x; u < n_uniq; u += blockDim.x) {
+        const int n = p.uniq_off[u + 1] - p.uniq_off[u];
+        const int ng = (n + p.bn_gu - 1) / p.bn_gu, nd = (n + p.bn_dn - 1) / p.bn_dn;
+        const int bg = p.tile_off_gu[u], bd = p.tile_off_dn[u];
+        for (int i = 0; i < p.rt_gu * ng; ++i) {
+            const int rt = i / ng, tt = i - rt * ng;
+            if (bg + i < p.cap_gu)
+                p.rec_gu[bg + i] = make_uint2((unsigned)u | ((unsigned)rt << 16),
+                                              (unsigned)tt | ((unsigned)min(p.bn_gu, n - tt * p.bn_gu) << 16));
+        }
+        for (int i = 0; i < p.rt_dn * nd; ++i) {
+            const int rt = i / nd, tt = i - rt * nd;
+            if (bd + i < p.cap_dn)
+                p.rec_dn[bd + i] = make_uint2((unsigned)u | ((unsigned)rt << 16),
+                                              (unsigned)tt | ((unsigned)min(p.bn_dn, n - tt * p.bn_dn) << 16));
+        }
     }
     if (threadIdx.x == 0) {
         p.tile_off_gu[n_uniq] = run_gu;

@@ -70,6 +70,8 @@ struct moe_ctx {
     __half *xs16 = nullptr, *hq16 = nullptr;
     float *xdT = nullptr, *hdT = nullptr;
     int32_t *tile_off = nullptr;  // [2][U + 1]
+    uint2 *tile_rec = nullptr;    // per-tile records: [cap_gu] gate/up, then [cap_dn] down
+    int cap_gu = 0, cap_dn = 0;
     CUtensorMap tm_x{}, tm_h{};
     // prefill staging of cold experts into lent slots
     uint64_t *etbl = nullptr;     // [3][E]
@@ -342,6 +344,10 @@ int moe_layer_init(const moe_cfg *cfg, void *cuda_stream, moe_ctx **out) {
         CKI(cudaMalloc(&ctx->hdT, sizeof(float) * AP * (ctx->F / 32)));
         CKI(cudaMemset(ctx->hdT, 0, sizeof(float) * AP * (ctx->F / 32)));
         CKI(cudaMalloc(&ctx->tile_off, sizeof(int32_t) * 2 * (U + 1)));
+        // tiles per GEMM <= row tiles x (assignments / tile width + used experts)
+        ctx->cap_gu = ((ctx->F + 127) / 128) * (int)((A + moe::gemm_bn(true) - 1) / moe::gemm_bn(true) + U);
+        ctx->cap_dn = ((ctx->H + 127) / 128) * (int)((A + moe::gemm_bn(false) - 1) / moe::gemm_bn(false) + U);
+        CKI(cudaMalloc(&ctx->tile_rec, sizeof(uint2) * ((size_t)ctx->cap_gu + ctx->cap_dn)));
         CKI(cudaMalloc(&ctx->etbl, sizeof(uint64_t) * 3 * E));
         ctx->stage_cap = 3 * E;
         CKI(cudaMalloc(&ctx->stage_jobs, sizeof(uint64_t) * 2 * ctx->stage_cap));
@@ -608,6 +614,10 @@ static int ffn_forward_impl(moe_ctx *ctx, int layer, const float *d_x, int n_tok
         L.tiling.uniq_off = gp.uniq_off;
         L.tiling.tile_off_gu = ctx->tile_off;
         L.tiling.tile_off_dn = ctx->tile_off + Umax + 1;
+        L.tiling.rec_gu = ctx->tile_rec;
+        L.tiling.rec_dn = ctx->tile_rec + ctx->cap_gu;
+        L.tiling.cap_gu = ctx->cap_gu;
+        L.tiling.cap_dn = ctx->cap_dn;
         L.tiling.tid0 = layer * 3;
         L.tiling.n_tokens = T;
         L.tiling.rt_gu = (ctx->F + 127) / 128;
@@ -626,6 +636,7 @@ static int ffn_forward_impl(moe_ctx *ctx, int layer, const float *d_x, int n_tok
         g.error = ctx->d_error;
         L.gu = g;
         L.gu.tile_off = L.tiling.tile_off_gu;
+        L.gu.tile_rec = L.tiling.rec_gu;
         // with pool slots lent to this prompt pass, the layer's cold expert
         // tensors are staged there once and read from HBM by the GEMMs
         const uint64_t *rows = ctx->d_tbl + (size_t)(layer * 3) * ctx->E;
@@ -658,6 +669,7 @@ static int ffn_forward_impl(moe_ctx *ctx, int layer, const float *d_x, int n_tok
         L.gu.hds = ctx->hds;
         L.dn = g;
         L.dn.tile_off = L.tiling.tile_off_dn;
+        L.dn.tile_rec = L.tiling.rec_dn;
         L.dn.tbl[0] = rows + 2 * (size_t)ctx->E;
         L.dn.tbl[1] = nullptr;
         L.dn.a_scaleT = ctx->hdT;
@@ -978,6 +990,7 @@ void moe_destroy(moe_ctx *ctx) {
     cudaFree(ctx->hq16);
     cudaFree(ctx->hdT);
     cudaFree(ctx->tile_off);
+    cudaFree(ctx->tile_rec);
     cudaFree(ctx->done_gu);
     cudaFree(ctx->etbl);
     cudaFree(ctx->stage_jobs);
