@@ -468,39 +468,49 @@ def run_prefill_leg(args, qec, synth, torch, log):
             qec.route_topk(ctx, lg[l], T, E, k, idx, w, sp)
             qec.moe_ffn_forward(ctx, l, x[l], T, idx, w, y, sp)
 
-    pass_()
-    stream.synchronize()
-    qec.miss_drain(ctx)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(L)]
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    per_layer = np.zeros(L)
-    total = 0.0
-    for s in range(args.prefill_steps):
-        with torch.cuda.stream(stream):
-            e0.record()
-            for l in range(L):
-                qec.route_topk(ctx, lg[l], T, E, k, idx, w, sp)
-                ev[l][0].record()
-                qec.moe_ffn_forward(ctx, l, x[l], T, idx, w, y, sp)
-                ev[l][1].record()
-            e1.record()
+    def timed():
+        pass_()
         stream.synchronize()
         qec.miss_drain(ctx)
-        total += e0.elapsed_time(e1)
-        per_layer += np.array([a.elapsed_time(b) for a, b in ev])
-    ms = total / args.prefill_steps
-    per_layer /= args.prefill_steps
-    resident = [l for l in range(L) if wl.layer_capacity(l) == E]
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(L)]
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        per_layer = np.zeros(L)
+        total = 0.0
+        for s in range(args.prefill_steps):
+            with torch.cuda.stream(stream):
+                e0.record()
+                for l in range(L):
+                    qec.route_topk(ctx, lg[l], T, E, k, idx, w, sp)
+                    ev[l][0].record()
+                    qec.moe_ffn_forward(ctx, l, x[l], T, idx, w, y, sp)
+                    ev[l][1].record()
+                e1.record()
+            stream.synchronize()
+            qec.miss_drain(ctx)
+            total += e0.elapsed_time(e1)
+            per_layer += np.array([a.elapsed_time(b) for a, b in ev])
+        return total / args.prefill_steps, per_layer / args.prefill_steps
+
+    # cold experts read zero-copy by the GEMM's converters, then with the
+    # lookahead prefetch (layer l + 1's cold experts uploaded by the copy
+    # engine while layer l computes)
+    ms_zc, per_layer_zc = timed()
+    qec.moe_set_lookahead(ctx, True)
+    ms, per_layer = timed()
     flop = 2.0 * T * k * 3 * H * F
     peaks, src = load_peaks()
     best = float(per_layer.min())
     tfl = flop / (best * 1e-3) / 1e12
     qec.moe_destroy(ctx)
-    log(f"prefill: {T / (ms * 1e-3):.0f} tokens/s through {L} layers, best layer {best:.3f} ms = {tfl:.1f} TFLOP/s")
+    log(f"prefill: {T / (ms * 1e-3):.0f} tokens/s through {L} layers with lookahead prefetch "
+        f"({T / (ms_zc * 1e-3):.0f} with zero-copy cold reads), best layer {best:.3f} ms = {tfl:.1f} TFLOP/s")
     return {"workload": f"{wl.name}: {T} tokens, {L} layers, hidden {H}, {E} experts, top-{k}, FFN {F}, "
-                        f"pool {wl.layer_capacity(0)}/{E} per layer (cold experts read zero-copy)",
+                        f"pool {wl.layer_capacity(0)}/{E} per layer",
+            "cold_experts": "uploaded a layer ahead by the copy engine (lookahead prefetch)",
             "tokens_per_s": round(T / (ms * 1e-3), 1), "ms_per_pass": round(ms, 3),
             "layer_ms_median": round(float(np.median(per_layer)), 3),
+            "zero_copy": {"tokens_per_s": round(T / (ms_zc * 1e-3), 1),
+                          "layer_ms_median": round(float(np.median(per_layer_zc)), 3)},
             "gemm": {"bound": "tensor", "achieved_tflops_best_layer": round(tfl, 1),
                      "peak_tflops": peaks.get("bf16_tflops"), "unit": "TFLOP/s",
                      "frac": round(tfl / peaks.get("bf16_tflops", 1900.0), 4),

@@ -201,6 +201,26 @@ int moe_pool_borrow(moe_ctx *ctx, int n_slots, void **d_ws, size_t *bytes);
 int moe_pool_return(moe_ctx *ctx);
 
 /*
+ * Lookahead prefetch for prompt passes (mihailescu2m/llama.cpp, Metal
+ * streaming notes: expert reads for the next layer start a layer early).
+ * With enable = 1, every forward of more than 32 tokens for layer l also
+ * enqueues, on the context's upload stream, copy-engine uploads of the
+ * expert tensors of layer (l + 1) mod L that are cold at that moment into
+ * one of two device prefetch buffers; the prompt forward of that layer then
+ * reads those experts from the buffer instead of zero-copy host memory.  A
+ * prompt micro-batch of thousands of tokens uses every expert of a layer, so
+ * the predicted set is the layer's whole cold set.  The effective table is
+ * rebuilt from the live table when the layer runs: an expert admitted in the
+ * meantime is read from its pool slot, one evicted in the meantime from host
+ * memory.  Cache state, miss log, stamps and results are the same as without
+ * prefetch.  Enable after every tensor is registered: the buffers (2 x 3 x
+ * (the largest cold count of a tensor) x tensor slot bytes of device memory)
+ * are sized then.  enable = 0 stops issuing prefetches (buffers are kept).
+ * Errors: MOE_ERR_STATE (a layer not registered), MOE_ERR_CUDA (allocation).
+ */
+int moe_set_lookahead(moe_ctx *ctx, int enable);
+
+/*
  * Snapshot of one tensor's cache state (synchronizes with all streams).
  * Any output may be NULL.  tbl: uint64 [E], the device pointer table as the
  * kernels read it; slot_of: int32 [E] (-1 = cold); last_seen: int32 [E]

@@ -54,6 +54,7 @@ SIGNATURES = {
     "miss_drain": (_i32, [_vp, _vp, _sz, ctypes.POINTER(_sz)]),
     "moe_pool_borrow": (_i32, [_vp, _i32, ctypes.POINTER(_vp), ctypes.POINTER(_sz)]),
     "moe_pool_return": (_i32, [_vp]),
+    "moe_set_lookahead": (_i32, [_vp, _i32]),
     "moe_cache_snapshot": (_i32, [_vp, _i32, _vp, _vp, _vp, _vp, _vp]),
     "moe_cache_layout": (_i32, [_vp, _i32, _vp, _vp, _vp, _vp]),
     "moe_stats": (_i32, [_vp, ctypes.POINTER(moe_stats_t)]),
@@ -183,6 +184,10 @@ def moe_pool_borrow(ctx, n_slots):
 
 def moe_pool_return(ctx):
     return _check(ctx, load().moe_pool_return(ctx))
+
+
+def moe_set_lookahead(ctx, enable=True):
+    return _check(ctx, load().moe_set_lookahead(ctx, 1 if enable else 0))
 
 
 def moe_cache_snapshot(ctx, tensor_id, n_experts, slots_per_tensor):

@@ -139,6 +139,8 @@ int fused_configure_rb(int F, size_t smem, int *blocks_per_sm);
 int launch_fused(const FusedParams &p, int grid, size_t smem, cudaStream_t st, cudaEvent_t const *ev);
 int launch_prefill(const PrefillLaunch &L, cudaStream_t st);
 int launch_stage(const StageParams &p, size_t blob_bytes, int n_sm, cudaStream_t st);
+int launch_prefetch_table(const uint64_t *tbl_rows, const int32_t *map, const void *buf, int cap, size_t stride,
+                          int E, uint64_t *etbl, cudaStream_t st);
 int gemm_configure();
 int gemm_bn(bool dual);
 int launch_step_finish(const Update *u, int n, uint64_t *tbl, int32_t *slot, uint32_t *stamps, uint32_t *clock,

@@ -800,6 +800,26 @@ __global__ void __launch_bounds__(256) stage_copy_kernel(const uint64_t *__restr
     }
 }
 
+// Effective table rows of a layer whose cold experts were prefetched: an
+// entry that is cold now (host tag) and has a copy in the prefetch buffer
+// points at that copy; every other entry is the live table entry.
+__global__ void prefetch_table_kernel(const uint64_t *__restrict__ tbl, const int32_t *__restrict__ map,
+                                      uint64_t buf, int cap, size_t stride, int E, uint64_t *etbl) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < 3 * E; i += gridDim.x * blockDim.x) {
+        const uint64_t entry = tbl[i];
+        const int m = map[i];
+        const int kd = i / E;
+        etbl[i] = ((entry & 1ull) && m >= 0) ? buf + ((size_t)kd * cap + (size_t)m) * stride : entry;
+    }
+}
+
+int launch_prefetch_table(const uint64_t *tbl_rows, const int32_t *map, const void *buf, int cap, size_t stride,
+                          int E, uint64_t *etbl, cudaStream_t st) {
+    const int grid = (3 * E + 255) / 256;
+    prefetch_table_kernel<<<grid, 256, 0, st>>>(tbl_rows, map, (uint64_t)(uintptr_t)buf, cap, stride, E, etbl);
+    return (int)cudaGetLastError();
+}
+
 int launch_stage(const StageParams &p, size_t blob_bytes, int n_sm, cudaStream_t st) {
     stage_plan_kernel<<<1, 256, 0, st>>>(p);
     stage_copy_kernel<<<n_sm * 8, 256, 0, st>>>(p.jobs, p.n_jobs, blob_bytes / 16);

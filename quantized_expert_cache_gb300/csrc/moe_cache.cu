@@ -78,6 +78,14 @@ struct moe_ctx {
     uint64_t *stage_jobs = nullptr;
     int *stage_n = nullptr;
     int stage_cap = 0;
+    // lookahead prefetch of the next layer's cold experts (prompt passes)
+    bool lookahead = false;
+    int pf_cap = 0;                         // expert blobs per tensor per buffer
+    uint8_t *pf_buf[2] = {nullptr, nullptr};  // [3][pf_cap] blobs of `stride` bytes
+    int32_t *d_pfmap[2] = {nullptr, nullptr}, *h_pfmap[2] = {nullptr, nullptr};  // [3][E]: buffer index or -1
+    cudaEvent_t ev_pf[2] = {nullptr, nullptr}, ev_pf_free[2] = {nullptr, nullptr};
+    int pf_layer[2] = {-1, -1};
+    bool pf_map_pending[2] = {false, false};
     // fused small-batch layer kernel
     unsigned *done_gu = nullptr, *exit_count = nullptr;
     size_t fused_smem = 0, fused_smem_rb = 0;
@@ -229,6 +237,50 @@ int make_tmap(moe_ctx *ctx, CUtensorMap *tm, void *base, uint64_t rows, uint64_t
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(ctx, MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+    return MOE_OK;
+}
+
+// Lookahead prefetch: copy-engine uploads of layer l's currently cold expert
+// tensors into prefetch buffer l % 2 on the upload stream, after the last
+// prompt forward that read that buffer.  A run of consecutive cold experts is
+// one copy.  The buffer's map (expert -> copy index or -1) goes along.
+int prefetch_layer(moe_ctx *ctx, int l) {
+    const int b = l & 1, E = ctx->E;
+    for (int kd = 0; kd < 3; ++kd)
+        if (!ctx->t[l * 3 + kd].registered) return MOE_OK;
+    // the previous prefetch into this buffer copied the host map: it has to
+    // be done before the map is rewritten
+    if (ctx->pf_map_pending[b]) CK(cudaEventSynchronize(ctx->ev_pf[b]));
+    ctx->pf_map_pending[b] = false;
+    CK(cudaStreamWaitEvent(ctx->up, ctx->ev_pf_free[b], 0));
+    int32_t *map = ctx->h_pfmap[b];
+    for (int kd = 0; kd < 3; ++kd) {
+        const TensorState &ts = ctx->t[l * 3 + kd];
+        uint8_t *dst0 = ctx->pf_buf[b] + (size_t)kd * ctx->pf_cap * ctx->stride;
+        int n = 0, run_e = 0, run_m = 0, run_len = 0;
+        for (int e = 0; e <= E; ++e) {
+            const bool cold = e < E && ts.slot_of[e] < 0 && n < ctx->pf_cap;
+            if (run_len && (!cold || run_e + run_len != e)) {
+                CK(cudaMemcpyAsync(dst0 + (size_t)run_m * ctx->stride, ts.home + (size_t)run_e * ctx->stride,
+                                   (size_t)run_len * ctx->stride, cudaMemcpyHostToDevice, ctx->up));
+                run_len = 0;
+            }
+            if (e == E) break;
+            map[kd * E + e] = cold ? n : -1;
+            if (cold) {
+                if (!run_len) {
+                    run_e = e;
+                    run_m = n;
+                }
+                ++run_len;
+                ++n;
+            }
+        }
+    }
+    CK(cudaMemcpyAsync(ctx->d_pfmap[b], map, sizeof(int32_t) * 3 * E, cudaMemcpyHostToDevice, ctx->up));
+    CK(cudaEventRecord(ctx->ev_pf[b], ctx->up));
+    ctx->pf_map_pending[b] = true;
+    ctx->pf_layer[b] = l;
     return MOE_OK;
 }
 
@@ -640,7 +692,17 @@ static int ffn_forward_impl(moe_ctx *ctx, int layer, const float *d_x, int n_tok
         // with pool slots lent to this prompt pass, the layer's cold expert
         // tensors are staged there once and read from HBM by the GEMMs
         const uint64_t *rows = ctx->d_tbl + (size_t)(layer * 3) * ctx->E;
-        if (ctx->n_lent > 0) {
+        const int pb = layer & 1;
+        const bool prefetched = ctx->lookahead && ctx->pf_layer[pb] == layer;
+        if (prefetched) {
+            // this layer's cold experts were uploaded a layer ahead: read them
+            // from the prefetch buffer (entries rebuilt from the live table)
+            CK(cudaStreamWaitEvent(st, ctx->ev_pf[pb], 0));
+            rc = moe::launch_prefetch_table(rows, ctx->d_pfmap[pb], ctx->pf_buf[pb], ctx->pf_cap, ctx->stride, ctx->E,
+                                            ctx->etbl, st);
+            if (rc) return fail(ctx, MOE_ERR_CUDA, "prefetch table launch failed");
+            rows = ctx->etbl;
+        } else if (ctx->n_lent > 0) {
             const int nt = ctx->n_tensors, G = nt * ctx->spt;
             moe::StageParams sp{};
             sp.tbl = ctx->d_tbl;
@@ -691,6 +753,15 @@ static int ffn_forward_impl(moe_ctx *ctx, int layer, const float *d_x, int n_tok
         rc = moe::launch_prefill(L, st);
         if (rc) return fail(ctx, MOE_ERR_CUDA, std::string("prefill launch: ") + cudaGetErrorString((cudaError_t)rc));
         ctx->last_T = T;
+        if (prefetched) {
+            CK(cudaEventRecord(ctx->ev_pf_free[pb], st));  // the buffer may be refilled after this layer
+            ctx->pf_layer[pb] = -1;
+        }
+        if (ctx->lookahead) {
+            // the next layer's cold experts, uploaded while this layer computes
+            rc = prefetch_layer(ctx, (layer + 1) % ctx->cfg.n_layers);
+            if (rc) return rc;
+        }
         return MOE_OK;
     }
     int max_gu = U * (ctx->F / 32), max_dn = U * ctx->n_counters;
@@ -921,6 +992,41 @@ int moe_pool_return(moe_ctx *ctx) {
     return MOE_OK;
 }
 
+int moe_set_lookahead(moe_ctx *ctx, int enable) {
+    if (!ctx) return fail(nullptr, MOE_ERR_ARG, "null ctx");
+    CK(cudaSetDevice(ctx->dev));
+    if (!enable) {
+        ctx->lookahead = false;
+        return MOE_OK;
+    }
+    if (!ctx->gemm_ok) return fail(ctx, MOE_ERR_STATE, "lookahead: no prompt-pass path in this context");
+    int cap = 0;
+    for (int tid = 0; tid < ctx->n_tensors; ++tid) {
+        const TensorState &ts = ctx->t[tid];
+        if (!ts.registered) return fail(ctx, MOE_ERR_STATE, "lookahead: register every tensor first");
+        cap = std::max(cap, ctx->E - ts.capacity);
+    }
+    if (cap > ctx->pf_cap) {
+        int rc = sync_all(ctx);
+        if (rc) return rc;
+        for (int b = 0; b < 2; ++b) {
+            cudaFree(ctx->pf_buf[b]);
+            ctx->pf_buf[b] = nullptr;
+            CK(cudaMalloc(&ctx->pf_buf[b], (size_t)3 * cap * ctx->stride));
+            ctx->pf_layer[b] = -1;
+        }
+        ctx->pf_cap = cap;
+    }
+    for (int b = 0; b < 2; ++b) {
+        if (!ctx->d_pfmap[b]) CK(cudaMalloc(&ctx->d_pfmap[b], sizeof(int32_t) * 3 * ctx->E));
+        if (!ctx->h_pfmap[b]) CK(cudaHostAlloc(&ctx->h_pfmap[b], sizeof(int32_t) * 3 * ctx->E, cudaHostAllocDefault));
+        if (!ctx->ev_pf[b]) CK(cudaEventCreateWithFlags(&ctx->ev_pf[b], cudaEventDisableTiming));
+        if (!ctx->ev_pf_free[b]) CK(cudaEventCreateWithFlags(&ctx->ev_pf_free[b], cudaEventDisableTiming));
+    }
+    ctx->lookahead = cap > 0;
+    return MOE_OK;
+}
+
 int moe_cache_snapshot(moe_ctx *ctx, int tensor_id, uint64_t *tbl, int32_t *slot_of, int32_t *last_seen,
                        int32_t *owner, uint32_t *stamps) {
     if (!ctx) return fail(nullptr, MOE_ERR_ARG, "null ctx");
@@ -995,6 +1101,13 @@ void moe_destroy(moe_ctx *ctx) {
     cudaFree(ctx->etbl);
     cudaFree(ctx->stage_jobs);
     cudaFree(ctx->stage_n);
+    for (int b = 0; b < 2; ++b) {
+        cudaFree(ctx->pf_buf[b]);
+        cudaFree(ctx->d_pfmap[b]);
+        if (ctx->h_pfmap[b]) cudaFreeHost(ctx->h_pfmap[b]);
+        if (ctx->ev_pf[b]) cudaEventDestroy(ctx->ev_pf[b]);
+        if (ctx->ev_pf_free[b]) cudaEventDestroy(ctx->ev_pf_free[b]);
+    }
     if (ctx->h_stamps) cudaFreeHost(ctx->h_stamps);
     if (ctx->h_upd) cudaFreeHost(ctx->h_upd);
     if (ctx->h_step) cudaFreeHost(ctx->h_step);

@@ -92,3 +92,43 @@ def test_prefill_with_lent_slots_stages_cold_experts(n_borrow):
             assert np.array_equal(snap["tbl"], m.expected_tbl(tid))
     finally:
         m.close()
+
+
+def test_prefill_lookahead_prefetch_matches_plain_run():
+    """Lookahead prefetch: a prompt forward of layer l uploads layer l + 1's
+    cold expert tensors, and that layer reads them from the prefetch buffer.
+    Outputs, stats and cache state equal those of the same run without
+    prefetch, also across promotion passes that change the cold sets while a
+    prefetch is pending (admissions on the second sighting)."""
+    # a wide window: prompt-length steps then admit on the second sighting;
+    # the layers' token counts differ, so some stamps are older than the clock
+    kw = dict(H=512, F=384, E=16, k=2, L=3, capacity=8, max_tokens=400, zipf_s=0.5, window=10000)
+    a, b = Model(**kw), Model(**kw)
+    try:
+        qec.moe_set_lookahead(b.ctx, True)
+        for p in range(3):
+            for layer in range(3):
+                T = 400 - 37 * layer
+                x, lg = a.wl.x(layer, p, T), a.wl.logits(layer, p, T)
+                ia, wa = a.route(lg)
+                ib, wb = b.route(lg)
+                ya = a.forward(layer, x, ia, wa)
+                yb = b.forward(layer, x, ib, wb)
+                torch.cuda.synchronize()
+                assert torch.equal(ya, yb), (p, layer)
+                if p == 0:
+                    check_layer_parity(a, layer, x, lg, ya.cpu().numpy(), ia.cpu().numpy(), wa.cpu().numpy())
+            qec.cache_step(a.ctx, 400)
+            qec.cache_step(b.ctx, 400)
+        sa, sb = qec.moe_stats(a.ctx), qec.moe_stats(b.ctx)
+        for key in ("hits", "misses", "admissions", "evictions", "cold_bytes"):
+            assert sa[key] == sb[key], key
+        assert sa["admissions"] > 0
+        for tid in range(9):
+            xa = qec.moe_cache_snapshot(a.ctx, tid, a.E, a.spt)
+            xb = qec.moe_cache_snapshot(b.ctx, tid, b.E, b.spt)
+            for key in ("slot_of", "last_seen", "owner", "stamps"):
+                assert np.array_equal(xa[key], xb[key]), (tid, key)
+    finally:
+        a.close()
+        b.close()
