@@ -23,8 +23,8 @@
  * pointer-table GEMV diagram and the paragraphs after it: per-tensor d_tbl
  * with an LSB tag, the HBM pool, zero-copy reads of pinned host memory, the
  * miss recorder, stamps and the promotion pass between graphs);
- * neurall/llama.cpp, "How it works" (admission on repeated use within the
- * last 64 tokens; expert blocks borrowed by the prompt pass and returned);
+ * neurall/llama.cpp, "How it works" (an expert is admitted after a second
+ * miss inside a 64-token window; expert blocks borrowed by the prompt pass and returned);
  * mx-llama.cpp FEATURES.md (q8_1 activation quantization reused across the
  * matmuls of one input; planes of quants and scales); mihailescu2m/llama.cpp
  * (MUL_MAT_ID over used tiles only; top-k of 512 scores).
@@ -161,7 +161,7 @@ int moe_ffn_forward_routed(moe_ctx *ctx, int layer, const float *d_x, const floa
 /*
  * Promotion pass between steps (Zapdev-labs/a6000-custom-kernels:
  * ggml_cuda_moe_cache_step between graphs, never captured; neurall/llama.cpp:
- * admission after repeated use within the last 64 tokens).  Waits (host
+ * admission on a second miss inside a 64-token window).  Waits (host
  * poll, bounded by cfg.poll_timeout_ms) for the forwards issued so far,
  * advances the clock by n_tokens, reads the miss log and the stamps, and
  * for each miss in ascending key order: admits the expert when its previous
@@ -184,7 +184,7 @@ int miss_drain(moe_ctx *ctx, uint32_t *host_out, size_t cap, size_t *n_out);
 
 /*
  * Lend n_slots pool slots to a prefill pass (neurall/llama.cpp, "How it
- * works": the big micro-batch buffer is lent only to the prompt pass).
+ * works": the large micro-batch workspace exists only during a prompt pass).
  * Global slot g is local slot g / (3L) of tensor g % (3L); the n highest
  * global slots are taken, their experts evicted (table entries back to
  * host).  *d_ws gets the device address of the contiguous lent region and

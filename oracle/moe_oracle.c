@@ -10,8 +10,8 @@
  * Sources (page titles and sections):
  *  [A2] Zapdev-labs/a6000-custom-kernels -- the pointer-table GEMV diagram
  *       ("router (top-8 of 512 experts, per layer)", moe_cache_gemv) and the
- *       paragraph on the MMVQ dot kernels and "the full MMVQ fusion argument
- *       set (... GLU ...)".
+ *       paragraph on the MMVQ dot kernels, which keep every fusion argument
+ *       of the stock path, the GLU among them.
  *  [M4] mx-llama.cpp FEATURES.md -- activation quantization to q8_1 reused
  *       by the matmuls that share one input (router and gate/up).
  *  [S5] mihailescu2m/llama.cpp -- "the graph-shape problem" (top-k of 512

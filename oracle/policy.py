@@ -4,15 +4,15 @@ HBM expert pool, per tensor or global across layers.
 Sources (page titles and sections):
 - Zapdev-labs/a6000-custom-kernels, the pointer-table paragraph: each expert
   tensor has its own table, pool and stamp array; cold reads are logged as
-  (tensor_id << 12 | expert); a promotion pass between decode steps admits
-  repeatedly-missed experts (2nd sighting) into free pool slots and evicts by
-  stamp scan; pools are seeded from a routing-frequency table.
-- neurall/llama.cpp, "How it works", Expert cache: a missed expert takes a
-  slot only after repeated use within the last 64 tokens; the fixed reserve
-  per layer became one global pool of expert blocks shared by all layers;
+  (tensor_id << 12 | expert); between decode steps a promotion pass moves an
+  expert into a free pool slot on its second miss, choosing victims by a scan
+  of the stamps; pools start from a routing-frequency table.
+- neurall/llama.cpp, "How it works", Expert cache: an expert that missed is
+  admitted only when it missed again inside a 64-token window; instead of a
+  fixed number of blocks per layer, every layer draws on one shared pool;
   the prompt pass borrows expert blocks and gives them back afterwards,
-  refilled with the model's globally hot experts and with the experts the
-  prompt pass has just used (prefill preheat); the features table measures
+  refilled with the model's globally hot experts and with experts that the
+  prompt pass itself needed (prefill preheat); the features table measures
   both (global expert pool; prefill preheat).
 
 State per tensor t: slot_of[e] (-1 = cold) and last_seen[e] (-1 = no

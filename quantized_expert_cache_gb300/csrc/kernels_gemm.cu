@@ -2,8 +2,8 @@
 // 5th-generation tensor cores (tcgen05, accumulators in TMEM), over tokens
 // sorted by expert, only over (expert, tile) pairs that hold tokens.
 //
-// Sources: mihailescu2m/llama.cpp, Metal kernels ("MUL_MAT_ID over used tiles
-// only": the expert GEMM runs only over the (expert, tile) pairs that hold
+// Sources: mihailescu2m/llama.cpp, Metal kernels (MUL_MAT_ID restricted to the
+// used tiles: no work is launched for an (expert, tile) pair without
 // tokens); neurall/llama.cpp, "How it works" (prompts in few big passes, each
 // expert upload serving many prompt tokens); the Q4 / q8_1 block formats of
 // the mat-vec kernels (Zapdev-labs/a6000-custom-kernels; mx-llama.cpp

@@ -7,7 +7,7 @@
 // Sources: Zapdev-labs/a6000-custom-kernels (per-tensor d_tbl / pool / stamp
 // array, LSB-tagged host entries, miss buffer, promotion pass between
 // graphs, seeding from a routing-frequency file); neurall/llama.cpp, "How it
-// works" (admission after repeated use within the last 64 tokens; the prompt
+// works" (an expert is admitted once it has been missed twice inside a 64-token window; the prompt
 // pass borrows expert blocks and gives them back refilled with hot experts).
 #include "../../include/moe_cache.h"
 #include "kernels.h"
