@@ -167,7 +167,10 @@ int moe_ffn_forward_routed(moe_ctx *ctx, int layer, const float *d_x, const floa
  * for each miss in ascending key order: admits the expert when its previous
  * sighting is less than window_tokens old, into the lowest free slot or
  * else the slot with the smallest stamp older than this step (ties: lowest
- * slot), otherwise records the sighting.  Uploads run on the context's
+ * slot), otherwise records the sighting.  Per-tensor pools (the default)
+ * search the missing tensor's own slots; a shared pool (moe_set_global_pool)
+ * searches every pool slot of the arena, whichever layer's expert it holds.
+ * Uploads run on the context's
  * upload stream; the context stream waits for them before its next forward.
  * While pool slots are borrowed, nothing is admitted.  The miss log is
  * cleared.  Errors: MOE_ERR_TIMEOUT, MOE_ERR_CUDA, MOE_ERR_FAULT (injected).
@@ -194,11 +197,52 @@ int miss_drain(moe_ctx *ctx, uint32_t *host_out, size_t cap, size_t *n_out);
 int moe_pool_borrow(moe_ctx *ctx, int n_slots, void **d_ws, size_t *bytes);
 
 /*
- * Give the lent slots back: each returned slot, in ascending global order,
- * is refilled with its tensor's most frequent non-resident expert by seed
- * order (stamp = clock).  Synchronous.  Errors: MOE_ERR_STATE.
+ * Give the lent slots back: each returned pool slot, in ascending global
+ * order, is refilled (stamp = clock) with the best non-resident expert, by
+ * (use count of the prompt pass, descending; rank in its tensor's seed
+ * order, ascending; tensor id, ascending).  Per-tensor pools take the slot's
+ * own tensor's experts, a shared pool every tensor's.  Without preheat every
+ * use count is 0: the refill follows seed order (the learned hot experts).
+ * Synchronous.  Errors: MOE_ERR_STATE.
  */
 int moe_pool_return(moe_ctx *ctx);
+
+/*
+ * One pool of expert blocks for all layers (neurall/llama.cpp, "How it
+ * works", Expert cache: the per-layer reserve gave way to one pool that every
+ * layer draws on; features table, global expert pool row).  With enable = 1
+ * the arena's slots of every registered tensor (its capacity's worth, at
+ * global slots s * 3L + tensor_id, s < capacity) form one pool: seeding is
+ * unchanged, but an admission takes the lowest free pool slot of the whole
+ * arena, else the pool slot with the oldest stamp below the clock (ties:
+ * lowest global slot), evicting whichever layer's expert holds it.  Tensors
+ * registered with capacity 0 still receive slots.  The promotion pass then
+ * reads all 3L x slots_per_tensor stamps when it admits.  Call before the
+ * first register_expert_tensor.  Errors: MOE_ERR_STATE (a tensor is already
+ * registered).
+ */
+int moe_set_global_pool(moe_ctx *ctx, int enable);
+
+/*
+ * Prefill preheat (neurall/llama.cpp, "How it works": blocks lent to a
+ * prompt pass come back holding the model's hot experts and the experts the
+ * pass itself needed; features table, prefill preheat row).  With
+ * enable = 1, every forward issued while slots are lent also adds its
+ * (token, expert) assignments to per-(layer, expert) use counts (one small
+ * kernel after the layer, on the context stream); moe_pool_return ranks the
+ * refill by them and clears them.  Allocates 4 x L x E bytes of device
+ * memory on first use.  Errors: MOE_ERR_STATE (slots are lent), MOE_ERR_CUDA.
+ */
+int moe_set_preheat(moe_ctx *ctx, int enable);
+
+/*
+ * Owner and stamp of every arena slot (3L x slots_per_tensor entries, global
+ * slot g = local slot g / 3L of tensor g % 3L), either pool mode; synchronizes
+ * with all streams.  owner_key: (tensor_id << 12 | expert), or -1 for a free,
+ * lent or unused slot; stamps: the device stamp of the slot.  Either output
+ * may be NULL.
+ */
+int moe_pool_snapshot(moe_ctx *ctx, int32_t *owner_key, uint32_t *stamps);
 
 /*
  * Lookahead prefetch for prompt passes (mihailescu2m/llama.cpp, Metal
@@ -223,9 +267,12 @@ int moe_set_lookahead(moe_ctx *ctx, int enable);
 /*
  * Snapshot of one tensor's cache state (synchronizes with all streams).
  * Any output may be NULL.  tbl: uint64 [E], the device pointer table as the
- * kernels read it; slot_of: int32 [E] (-1 = cold); last_seen: int32 [E]
- * (-1 = no sighting); owner: int32 [slots_per_tensor] (-1 = free or lent);
- * stamps: uint32 [slots_per_tensor] (device stamp array).
+ * kernels read it; slot_of: int32 [E] (-1 = cold; the local slot, or the
+ * global slot with a shared pool); last_seen: int32 [E] (-1 = no sighting);
+ * owner: int32 [slots_per_tensor] (-1 = free or lent; with a shared pool,
+ * the expert of this tensor held in its home slot s * 3L + tensor_id, -1 if
+ * another tensor's or free); stamps: uint32 [slots_per_tensor] (device stamp
+ * of each of those slots).
  */
 int moe_cache_snapshot(moe_ctx *ctx, int tensor_id, uint64_t *tbl, int32_t *slot_of, int32_t *last_seen,
                        int32_t *owner, uint32_t *stamps);

@@ -55,6 +55,9 @@ SIGNATURES = {
     "moe_pool_borrow": (_i32, [_vp, _i32, ctypes.POINTER(_vp), ctypes.POINTER(_sz)]),
     "moe_pool_return": (_i32, [_vp]),
     "moe_set_lookahead": (_i32, [_vp, _i32]),
+    "moe_set_global_pool": (_i32, [_vp, _i32]),
+    "moe_set_preheat": (_i32, [_vp, _i32]),
+    "moe_pool_snapshot": (_i32, [_vp, _vp, _vp]),
     "moe_cache_snapshot": (_i32, [_vp, _i32, _vp, _vp, _vp, _vp, _vp]),
     "moe_cache_layout": (_i32, [_vp, _i32, _vp, _vp, _vp, _vp]),
     "moe_stats": (_i32, [_vp, ctypes.POINTER(moe_stats_t)]),
@@ -188,6 +191,23 @@ def moe_pool_return(ctx):
 
 def moe_set_lookahead(ctx, enable=True):
     return _check(ctx, load().moe_set_lookahead(ctx, 1 if enable else 0))
+
+
+def moe_set_global_pool(ctx, enable=True):
+    return _check(ctx, load().moe_set_global_pool(ctx, 1 if enable else 0))
+
+
+def moe_set_preheat(ctx, enable=True):
+    return _check(ctx, load().moe_set_preheat(ctx, 1 if enable else 0))
+
+
+def moe_pool_snapshot(ctx, n_slots):
+    """Owner key (tensor << 12 | expert, or -1) and stamp of each of the
+    n_slots = 3L x slots_per_tensor arena slots."""
+    owner = np.empty(max(1, n_slots), np.int32)
+    stamps = np.empty(max(1, n_slots), np.uint32)
+    _check(ctx, load().moe_pool_snapshot(ctx, _host(owner), _host(stamps)))
+    return dict(owner=owner[:n_slots], stamps=stamps[:n_slots])
 
 
 def moe_cache_snapshot(ctx, tensor_id, n_experts, slots_per_tensor):

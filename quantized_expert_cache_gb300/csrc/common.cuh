@@ -105,14 +105,14 @@ __device__ __forceinline__ float ld_scale(const __half *p) { return __half2float
 // the miss log (Zapdev-labs/a6000-custom-kernels, pointer-table GEMV).
 struct CacheView {
     const uint64_t *tbl;       // [n_tensors][E]: pool address (bit0 = 0) or host address | 1
-    const int32_t *slot;       // [n_tensors][E]: local pool slot or -1
-    uint32_t *stamps;          // [n_tensors][slots_per_tensor]
+    const int32_t *slot;       // [n_tensors][E]: stamp index of the expert's pool slot, or -1
+    uint32_t *stamps;          // [n_tensors * slots_per_tensor], indexed by stamp index
     uint32_t *miss_bitmap;     // [n_tensors][ceil(E/32)]
     uint32_t *miss_list;       // [miss_cap]
     uint32_t *miss_count;      // [1]
     const uint32_t *clock;     // [1]: token clock after the last promotion pass
     unsigned long long *cold_reads;  // [1]: (tensor, expert) zero-copy passes
-    uint32_t *hit_bitmap;      // [n_tensors][hit_words]: slots hit since the last promotion pass (or null)
+    uint32_t *hit_bitmap;      // [hit_words]: stamp indices hit since the last promotion pass (or null)
     int E, slots_per_tensor, bitmap_words, miss_cap, hit_words;
 };
 
@@ -120,7 +120,9 @@ struct CacheView {
 // bitmap and, when newly set, appends (tensor << 12 | expert) to the miss
 // list; a pool hit writes the step's clock into the slot's stamp and sets
 // the slot's bit in the hit bitmap (the hit count of the step, read by the
-// promotion pass without reading every stamp).
+// promotion pass without reading every stamp).  The host chooses the stamp
+// index of a slot: tensor * slots_per_tensor + local slot for per-tensor
+// pools, the arena slot for one pool shared by all layers.
 __device__ __forceinline__ void record_read(const CacheView &cv, int tid, int e, uint64_t entry, uint32_t step_clock) {
     if (entry & 1ull) {
         uint32_t bit = 1u << (e & 31);
@@ -132,8 +134,8 @@ __device__ __forceinline__ void record_read(const CacheView &cv, int tid, int e,
     } else {
         int s = cv.slot[(size_t)tid * cv.E + e];
         if (s >= 0) {
-            cv.stamps[(size_t)tid * cv.slots_per_tensor + s] = step_clock;
-            if (cv.hit_bitmap) atomicOr(&cv.hit_bitmap[(size_t)tid * cv.hit_words + (s >> 5)], 1u << (s & 31));
+            cv.stamps[s] = step_clock;
+            if (cv.hit_bitmap) atomicOr(&cv.hit_bitmap[s >> 5], 1u << (s & 31));
         }
     }
 }

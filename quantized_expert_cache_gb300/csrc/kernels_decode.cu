@@ -1710,4 +1710,27 @@ int launch_step_finish(const Update *u, int n, uint64_t *tbl, int32_t *slot, uin
     return (int)cudaGetLastError();
 }
 
+// Prefill preheat: the (token, expert) assignments of one layer added to the
+// layer's use counts, through a per-block histogram in shared memory.
+__global__ void count_assign_kernel(const int32_t *__restrict__ idx, int n, int E, uint32_t *cnt) {
+    extern __shared__ uint32_t hist[];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0u;
+    __syncthreads();
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+        const int e = idx[i];
+        if ((unsigned)e < (unsigned)E) atomicAdd(&hist[e], 1u);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+        if (hist[e]) atomicAdd(&cnt[e], hist[e]);
+}
+
+int launch_count_assign(const int32_t *idx, int n, int E, uint32_t *cnt, cudaStream_t st) {
+    if (n <= 0) return 0;
+    int grid = (n + 1023) / 1024;
+    grid = grid > 152 ? 152 : grid;
+    count_assign_kernel<<<grid, 256, sizeof(uint32_t) * (size_t)E, st>>>(idx, n, E, cnt);
+    return (int)cudaGetLastError();
+}
+
 }  // namespace moe

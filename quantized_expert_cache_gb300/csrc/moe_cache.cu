@@ -34,7 +34,7 @@ struct TensorState {
     int capacity = 0;
     uint8_t *home = nullptr;  // pinned, device-mapped: n_experts blobs of slot_stride bytes
     uint64_t home_dev = 0;
-    std::vector<int32_t> seed_order, slot_of, owner, last_seen;
+    std::vector<int32_t> seed_order, rank, slot_of, owner, last_seen;  // slot_of: global slot in a shared pool
     std::vector<uint64_t> tbl;  // host mirror of the device table row
     std::vector<uint8_t> lent;
 };
@@ -93,15 +93,23 @@ struct moe_ctx {
     int pdl = 1;  // fused layer kernels use programmatic dependent launch
 
     uint32_t *h_stamps = nullptr;    // pinned mirror, refreshed per tensor when a victim is chosen
-    uint32_t *d_stepbuf = nullptr;   // [hit bitmap: n_tensors x hit_words][miss count][miss keys]
+    uint32_t *d_stepbuf = nullptr;   // [hit bitmap: hit_words][miss count][miss keys]
     uint32_t *h_step = nullptr;      // pinned: hit bitmap, miss count and the first kStepKeys keys
-    int hit_words = 0;
+    int hit_words = 0;               // words of the hit bitmap: one bit per stamp index
     Update *h_upd = nullptr, *d_upd = nullptr;  // pinned, mapped (d_upd: its device address)
     int upd_cap = 0, n_upd = 0;
 
     std::vector<TensorState> t;
     uint64_t clock = 0;
     int n_lent = 0;
+    // one pool of expert blocks shared by all layers (instead of a reserve
+    // per tensor): owner and membership of every arena slot
+    bool global_pool = false;
+    std::vector<int32_t> g_owner;  // (tid << 12 | e) or -1
+    std::vector<uint8_t> g_pool, g_lent;
+    // prefill preheat: assignments per (layer, expert) routed while slots are lent
+    bool preheat = false;
+    uint32_t *d_use = nullptr;
     moe_stats_t stats{};
     int last_T = -1;
     int fail_nth = 0;
@@ -140,6 +148,13 @@ inline uint64_t pool_addr(moe_ctx *c, int tid, int local) {
     size_t g = (size_t)local * c->n_tensors + tid;
     return (uint64_t)(uintptr_t)(c->arena + g * c->stride);
 }
+inline uint64_t slot_addr(moe_ctx *c, size_t g) { return (uint64_t)(uintptr_t)(c->arena + g * c->stride); }
+// Stamp index of a pool slot (the device's stamp and hit-bit position):
+// tensor-major for per-tensor pools, the arena slot for a shared pool.
+inline int32_t stamp_index(moe_ctx *c, int tid, int slot) {
+    if (slot < 0) return -1;
+    return c->global_pool ? slot : tid * std::max(1, c->spt) + slot;
+}
 inline uint64_t home_entry(moe_ctx *c, int tid, int e) {
     return (c->t[tid].home_dev + (uint64_t)e * c->stride) | 1ull;
 }
@@ -153,7 +168,7 @@ void set_entry(moe_ctx *c, int tid, int e, uint64_t entry, int32_t slot) {
     ts.tbl[e] = entry;
     ts.slot_of[e] = slot;
     push_upd(c, 0, (size_t)tid * c->E + e, entry);
-    push_upd(c, 1, (size_t)tid * c->E + e, (uint64_t)(int64_t)slot);
+    push_upd(c, 1, (size_t)tid * c->E + e, (uint64_t)(int64_t)stamp_index(c, tid, slot));
 }
 
 constexpr size_t kStepKeys = 256;  // miss keys read back with the hit bitmap
@@ -162,7 +177,7 @@ constexpr size_t kStepKeys = 256;  // miss keys read back with the hit bitmap
 // kernel that reads them from the pinned list; with clear_step, the step's
 // hit bitmap, miss count and miss bitmap are zeroed too.
 int publish(moe_ctx *ctx, cudaStream_t st, bool clear_step = false) {
-    const int na = clear_step ? ctx->n_tensors * ctx->hit_words + 1 : 0;
+    const int na = clear_step ? ctx->hit_words + 1 : 0;
     const int nb = clear_step ? ctx->n_tensors * ctx->bitmap_words : 0;
     int rc = moe::launch_step_finish(ctx->d_upd, ctx->n_upd, ctx->d_tbl, ctx->d_slot, ctx->d_stamps, ctx->d_clock,
                                      (uint32_t)ctx->clock, ctx->d_stepbuf, na, ctx->d_bitmap, nb, st);
@@ -284,6 +299,82 @@ int prefetch_layer(moe_ctx *ctx, int l) {
     return MOE_OK;
 }
 
+// Victim search of the shared pool for one promotion pass: the free pool
+// slots in arena order first, then (built at the first eviction) the
+// occupied slots stamped before this step, by (stamp, slot).  Slots filled
+// in this pass carry the new clock, so they never become victims, and a
+// candidate changes hands only by being taken: one sorted list serves every
+// admission of the step.
+struct GlobalPick {
+    bool stamps_read = false, free_built = false, victims_built = false;
+    std::vector<int> free_slots;
+    size_t fpos = 0;
+    std::vector<std::pair<uint32_t, int>> victims;
+    size_t vpos = 0;
+    int took = 0;
+};
+
+// One admission of (tid, e) into the shared pool: lowest free slot, else the
+// oldest stamp below the clock (ties: lowest slot), whichever layer holds it.
+int admit_global(moe_ctx *ctx, GlobalPick &gs, int tid, int e, uint64_t clk, int &fault, int &uploads) {
+    const int G = ctx->n_tensors * std::max(1, ctx->spt);
+    gs.took = 0;
+    if (!gs.stamps_read) {
+        // the device stamps (the stream is idle here), before this step's
+        // first admission edits the mirror
+        CK(cudaMemcpy(ctx->h_stamps, ctx->d_stamps, sizeof(uint32_t) * G, cudaMemcpyDeviceToHost));
+        gs.stamps_read = true;
+    }
+    if (!gs.free_built) {
+        for (int g = 0; g < G; ++g)
+            if (ctx->g_pool[g] && !ctx->g_lent[g] && ctx->g_owner[g] < 0) gs.free_slots.push_back(g);
+        gs.free_built = true;
+    }
+    int g = -1;
+    if (gs.fpos < gs.free_slots.size()) {
+        g = gs.free_slots[gs.fpos++];
+    } else {
+        if (!gs.victims_built) {
+            for (int v = 0; v < G; ++v)
+                if (ctx->g_pool[v] && !ctx->g_lent[v] && ctx->g_owner[v] >= 0 && (uint64_t)ctx->h_stamps[v] < clk)
+                    gs.victims.emplace_back(ctx->h_stamps[v], v);
+            std::sort(gs.victims.begin(), gs.victims.end());
+            gs.victims_built = true;
+        }
+        if (gs.vpos < gs.victims.size()) g = gs.victims[gs.vpos++].second;
+    }
+    if (g < 0) return MOE_OK;  // every pool slot was used this step: skipped, the sighting stays
+    const int vkey = ctx->g_owner[g];
+    if (vkey >= 0) {
+        const int vt = vkey >> 12, ve = vkey & 0xfff;
+        set_entry(ctx, vt, ve, home_entry(ctx, vt, ve), -1);
+        ctx->t[vt].last_seen[ve] = -1;
+        ctx->g_owner[g] = -1;
+        ctx->stats.evictions++;
+    }
+    gs.took = 1;
+    if (ctx->fail_nth > 0 && --ctx->fail_nth == 0) {
+        // injected upload failure: rolled back; the slot is the next
+        // admission's lowest free slot
+        fault = 1;
+        gs.free_slots.insert(std::lower_bound(gs.free_slots.begin() + (long)gs.fpos, gs.free_slots.end(), g), g);
+        return MOE_OK;
+    }
+    TensorState &ts = ctx->t[tid];
+    const uint64_t dst = slot_addr(ctx, (size_t)g);
+    CK(cudaMemcpyAsync((void *)(uintptr_t)dst, ts.home + (size_t)e * ctx->stride, ctx->blob, cudaMemcpyHostToDevice,
+                       ctx->up));
+    uploads++;
+    set_entry(ctx, tid, e, dst, g);
+    ctx->g_owner[g] = (tid << 12) | e;
+    ts.last_seen[e] = -1;
+    ctx->h_stamps[g] = (uint32_t)clk;
+    push_upd(ctx, 2, (size_t)g, (uint32_t)clk);
+    ctx->stats.admissions++;
+    ctx->stats.upload_bytes += ctx->blob;
+    return MOE_OK;
+}
+
 uint16_t f32_to_half_bits(float v) {
     __half h = __float2half_rn(v);
     uint16_t b;
@@ -358,9 +449,9 @@ int moe_layer_init(const moe_cfg *cfg, void *cuda_stream, moe_ctx **out) {
     CKI(cudaMemset(ctx->d_stamps, 0, sizeof(uint32_t) * (size_t)nt * std::max(1, ctx->spt)));
     CKI(cudaMalloc(&ctx->d_bitmap, sizeof(uint32_t) * (size_t)nt * ctx->bitmap_words));
     CKI(cudaMemset(ctx->d_bitmap, 0, sizeof(uint32_t) * (size_t)nt * ctx->bitmap_words));
-    ctx->hit_words = (std::max(1, ctx->spt) + 31) / 32;
+    ctx->hit_words = (int)(((size_t)nt * std::max(1, ctx->spt) + 31) / 32);
     {
-        const size_t hb = (size_t)nt * ctx->hit_words;
+        const size_t hb = (size_t)ctx->hit_words;
         CKI(cudaMalloc(&ctx->d_stepbuf, sizeof(uint32_t) * (hb + 1 + (size_t)ctx->miss_cap)));
         CKI(cudaMemset(ctx->d_stepbuf, 0, sizeof(uint32_t) * (hb + 1)));
         ctx->d_misslog = ctx->d_stepbuf + hb;
@@ -438,7 +529,7 @@ int moe_layer_init(const moe_cfg *cfg, void *cuda_stream, moe_ctx **out) {
     ctx->upd_cap = 6 * nt * E + 64;
     CKI(cudaHostAlloc(&ctx->h_upd, sizeof(Update) * (size_t)ctx->upd_cap, cudaHostAllocMapped));
     CKI(cudaHostGetDevicePointer((void **)&ctx->d_upd, ctx->h_upd, 0));
-    CKI(cudaHostAlloc(&ctx->h_step, sizeof(uint32_t) * ((size_t)nt * ctx->hit_words + 1 + kStepKeys),
+    CKI(cudaHostAlloc(&ctx->h_step, sizeof(uint32_t) * ((size_t)ctx->hit_words + 1 + kStepKeys),
                       cudaHostAllocDefault));
     CKI(cudaDeviceSynchronize());
 #undef CKI
@@ -487,24 +578,36 @@ int register_expert_tensor(moe_ctx *ctx, int layer, int kind, const void *host_q
     repack((const uint8_t *)host_q4, ts.home, E, rows, cols / 32, ctx->stride);
     ts.capacity = capacity;
     ts.seed_order = order;
+    ts.rank.assign(E, 0);
+    for (int i = 0; i < E; ++i) ts.rank[order[i]] = i;
     ts.slot_of.assign(E, -1);
     ts.owner.assign(ctx->spt, -1);
     ts.last_seen.assign(E, -1);
     ts.lent.assign(ctx->spt, 0);
     ts.tbl.resize(E);
     for (int e = 0; e < E; ++e) ts.tbl[e] = home_entry(ctx, tid, e);
+    if (ctx->global_pool)
+        for (int s = 0; s < capacity; ++s) ctx->g_pool[(size_t)s * ctx->n_tensors + tid] = 1;
     for (int s = 0; s < n_seed; ++s) {
         int e = order[s];
         uint64_t dst = pool_addr(ctx, tid, s);
         CK(cudaMemcpyAsync((void *)(uintptr_t)dst, ts.home + (size_t)e * ctx->stride, ctx->blob,
                            cudaMemcpyHostToDevice, ctx->up));
         ts.tbl[e] = dst;
-        ts.slot_of[e] = s;
-        ts.owner[s] = e;
+        if (ctx->global_pool) {
+            const int g = s * ctx->n_tensors + tid;
+            ts.slot_of[e] = g;
+            ctx->g_owner[g] = (tid << 12) | e;
+        } else {
+            ts.slot_of[e] = s;
+            ts.owner[s] = e;
+        }
     }
+    std::vector<int32_t> dslot(E);
+    for (int e = 0; e < E; ++e) dslot[e] = stamp_index(ctx, tid, ts.slot_of[e]);
     CK(cudaMemcpyAsync(ctx->d_tbl + (size_t)tid * E, ts.tbl.data(), sizeof(uint64_t) * E, cudaMemcpyHostToDevice,
                        ctx->up));
-    CK(cudaMemcpyAsync(ctx->d_slot + (size_t)tid * E, ts.slot_of.data(), sizeof(int32_t) * E, cudaMemcpyHostToDevice,
+    CK(cudaMemcpyAsync(ctx->d_slot + (size_t)tid * E, dslot.data(), sizeof(int32_t) * E, cudaMemcpyHostToDevice,
                        ctx->up));
     CK(cudaStreamSynchronize(ctx->up));
     ts.registered = true;
@@ -544,7 +647,23 @@ int moe_ffn_forward_routed(moe_ctx *ctx, int layer, const float *d_x, const floa
     return ffn_forward_impl(ctx, layer, d_x, n_tokens, d_idx, d_w, d_y, stream, nullptr, nullptr, nullptr);
 }
 
+static int ffn_forward_body(moe_ctx *ctx, int layer, const float *d_x, int n_tokens, const int32_t *d_idx,
+                            const float *d_w, float *d_y, void *stream, const float *d_logits, int32_t *idx_out,
+                            float *w_out);
+
+// One layer, then (prefill preheat, while pool slots are lent to a prompt
+// pass) the layer's (token, expert) assignments added to its use counts.
 static int ffn_forward_impl(moe_ctx *ctx, int layer, const float *d_x, int n_tokens, const int32_t *d_idx,
+                            const float *d_w, float *d_y, void *stream, const float *d_logits, int32_t *idx_out,
+                            float *w_out) {
+    int rc = ffn_forward_body(ctx, layer, d_x, n_tokens, d_idx, d_w, d_y, stream, d_logits, idx_out, w_out);
+    if (rc || !ctx->preheat || !ctx->n_lent || n_tokens <= 0 || !ctx->d_use) return rc;
+    rc = moe::launch_count_assign(d_idx, n_tokens * ctx->k, ctx->E, ctx->d_use + (size_t)layer * ctx->E, ctx->stream);
+    if (rc) return fail(ctx, MOE_ERR_CUDA, std::string("use counts: ") + cudaGetErrorString((cudaError_t)rc));
+    return MOE_OK;
+}
+
+static int ffn_forward_body(moe_ctx *ctx, int layer, const float *d_x, int n_tokens, const int32_t *d_idx,
                             const float *d_w, float *d_y, void *stream, const float *d_logits, int32_t *idx_out,
                             float *w_out) {
     if (!ctx) return fail(nullptr, MOE_ERR_ARG, "null ctx");
@@ -781,7 +900,7 @@ int cache_step(moe_ctx *ctx, int n_tokens) {
     if (n_tokens < 0) return fail(ctx, MOE_ERR_ARG, "cache_step: n_tokens < 0");
     CK(cudaSetDevice(ctx->dev));
     const int nt = ctx->n_tensors, spt = std::max(1, ctx->spt);
-    const size_t hb = (size_t)nt * ctx->hit_words;
+    const size_t hb = (size_t)ctx->hit_words;
     const size_t fast = std::min<size_t>(ctx->miss_cap, kStepKeys);
     // one read-back after the forwards issued so far: hit bitmap, miss count
     // and the first keys (the stamps are read only for tensors that admit)
@@ -804,16 +923,19 @@ int cache_step(moe_ctx *ctx, int n_tokens) {
     const uint64_t clk = ctx->clock;
     const uint32_t clk32 = (uint32_t)clk;
     // hits of the step: pool slots (with an owner) whose bit is set
-    for (int tid = 0; tid < nt; ++tid) {
-        const TensorState &ts = ctx->t[tid];
-        if (!ts.registered) continue;
-        for (int w = 0; w < ctx->hit_words; ++w) {
-            uint32_t m = hits[(size_t)tid * ctx->hit_words + w];
-            while (m) {
-                const int sl = w * 32 + __builtin_ctz(m);
-                m &= m - 1;
-                if (sl < ts.capacity && ts.owner[sl] >= 0) ctx->stats.hits++;
+    for (int w = 0; w < ctx->hit_words; ++w) {
+        uint32_t m = hits[w];
+        while (m) {
+            const int b = w * 32 + __builtin_ctz(m);
+            m &= m - 1;
+            if (ctx->global_pool) {
+                if (b < nt * spt && ctx->g_owner[b] >= 0) ctx->stats.hits++;
+                continue;
             }
+            const int tid = b / spt, sl = b % spt;
+            if (tid >= nt || !ctx->t[tid].registered) continue;
+            const TensorState &ts = ctx->t[tid];
+            if (sl < ts.capacity && ts.owner[sl] >= 0) ctx->stats.hits++;
         }
     }
     ctx->stats.misses += keys.size();
@@ -826,6 +948,7 @@ int cache_step(moe_ctx *ctx, int n_tokens) {
     ctx->n_upd = 0;
     int fault = 0, swaps = 0, uploads = 0;
     std::vector<char> fresh;  // tensors whose stamp mirror was read back this step
+    GlobalPick gs;            // shared pool: free slots and victims of this step
     if (ctx->n_lent == 0) {
         for (uint32_t key : keys) {
             const int tid = (int)(key >> 12), e = (int)(key & 0xfff);
@@ -837,6 +960,12 @@ int cache_step(moe_ctx *ctx, int n_tokens) {
                 continue;
             }
             if (ctx->cfg.max_swaps_per_step && swaps >= ctx->cfg.max_swaps_per_step) continue;
+            if (ctx->global_pool) {
+                int rc2 = admit_global(ctx, gs, tid, e, clk, fault, uploads);
+                if (rc2) return rc2;
+                swaps += gs.took;
+                continue;
+            }
             if (fresh.empty()) fresh.assign(nt, 0);
             if (!fresh[tid]) {
                 // the device stamps of this tensor (the stream is idle here),
@@ -921,7 +1050,7 @@ int miss_drain(moe_ctx *ctx, uint32_t *host_out, size_t cap, size_t *n_out) {
         memcpy(host_out, keys.data(), sizeof(uint32_t) * keys.size());
     }
     CK(cudaMemsetAsync(ctx->d_bitmap, 0, sizeof(uint32_t) * (size_t)ctx->n_tensors * ctx->bitmap_words, ctx->stream));
-    CK(cudaMemsetAsync(ctx->d_stepbuf, 0, sizeof(uint32_t) * ((size_t)ctx->n_tensors * ctx->hit_words + 1),
+    CK(cudaMemsetAsync(ctx->d_stepbuf, 0, sizeof(uint32_t) * ((size_t)ctx->hit_words + 1),
                        ctx->stream));
     CK(cudaStreamSynchronize(ctx->stream));
     return MOE_OK;
@@ -937,6 +1066,18 @@ int moe_pool_borrow(moe_ctx *ctx, int n_slots, void **d_ws, size_t *bytes) {
     if (rc) return rc;
     ctx->n_upd = 0;
     for (int g = G - n_slots; g < G; ++g) {
+        if (ctx->global_pool) {
+            const int key = ctx->g_owner[g];
+            if (key >= 0) {
+                const int vt = key >> 12, ve = key & 0xfff;
+                set_entry(ctx, vt, ve, home_entry(ctx, vt, ve), -1);
+                ctx->t[vt].last_seen[ve] = -1;
+                ctx->g_owner[g] = -1;
+                ctx->stats.evictions++;
+            }
+            ctx->g_lent[g] = 1;
+            continue;
+        }
         const int tid = g % nt, local = g / nt;
         TensorState &ts = ctx->t[tid];
         if (!ts.registered || local >= ts.capacity) continue;
@@ -964,31 +1105,125 @@ int moe_pool_return(moe_ctx *ctx) {
     CK(cudaSetDevice(ctx->dev));
     int rc = sync_all(ctx);
     if (rc) return rc;
-    const int nt = ctx->n_tensors, G = nt * ctx->spt, spt = std::max(1, ctx->spt);
+    const int nt = ctx->n_tensors, G = nt * ctx->spt, E = ctx->E;
     const uint32_t clk32 = (uint32_t)ctx->clock;
-    ctx->n_upd = 0;
-    for (int g = G - ctx->n_lent; g < G; ++g) {
-        const int tid = g % nt, local = g / nt;
+    // prefill preheat: the prompt pass's assignments per (layer, expert)
+    std::vector<uint32_t> use;
+    if (ctx->preheat && ctx->d_use) {
+        use.resize((size_t)ctx->cfg.n_layers * E);
+        CK(cudaMemcpy(use.data(), ctx->d_use, sizeof(uint32_t) * use.size(), cudaMemcpyDeviceToHost));
+        CK(cudaMemset(ctx->d_use, 0, sizeof(uint32_t) * use.size()));
+    }
+    // candidate order: prompt use count (desc), seed rank (asc), tensor (asc)
+    auto better = [&](int ta, int ea, int tb, int eb) {
+        const uint32_t ca = use.empty() ? 0 : use[(size_t)(ta / 3) * E + ea];
+        const uint32_t cb = use.empty() ? 0 : use[(size_t)(tb / 3) * E + eb];
+        if (ca != cb) return ca > cb;
+        const int ra = ctx->t[ta].rank[ea], rb = ctx->t[tb].rank[eb];
+        if (ra != rb) return ra < rb;
+        return ta < tb;
+    };
+    auto fill = [&](int tid, int e, int slot, uint64_t dst) -> int {
         TensorState &ts = ctx->t[tid];
-        if (!ts.registered || local >= ts.capacity) continue;
-        ts.lent[local] = 0;
-        for (int e : ts.seed_order) {
-            if (ts.slot_of[e] >= 0) continue;
-            const uint64_t dst = pool_addr(ctx, tid, local);
-            CK(cudaMemcpyAsync((void *)(uintptr_t)dst, ts.home + (size_t)e * ctx->stride, ctx->blob,
-                               cudaMemcpyHostToDevice, ctx->stream));
-            set_entry(ctx, tid, e, dst, local);
-            ts.owner[local] = e;
-            ts.last_seen[e] = -1;
-            push_upd(ctx, 2, (size_t)tid * spt + local, clk32);
-            ctx->stats.upload_bytes += ctx->blob;
-            break;
+        CK(cudaMemcpyAsync((void *)(uintptr_t)dst, ts.home + (size_t)e * ctx->stride, ctx->blob,
+                           cudaMemcpyHostToDevice, ctx->stream));
+        set_entry(ctx, tid, e, dst, slot);
+        ts.last_seen[e] = -1;
+        push_upd(ctx, 2, (size_t)stamp_index(ctx, tid, slot), clk32);
+        ctx->stats.upload_bytes += ctx->blob;
+        return MOE_OK;
+    };
+    ctx->n_upd = 0;
+    if (ctx->global_pool) {
+        std::vector<std::pair<int, int>> cands;
+        for (int tid = 0; tid < nt; ++tid) {
+            if (!ctx->t[tid].registered) continue;
+            for (int e = 0; e < E; ++e)
+                if (ctx->t[tid].slot_of[e] < 0) cands.emplace_back(tid, e);
+        }
+        std::sort(cands.begin(), cands.end(), [&](const std::pair<int, int> &a, const std::pair<int, int> &b) {
+            return better(a.first, a.second, b.first, b.second);
+        });
+        size_t pos = 0;
+        for (int g = G - ctx->n_lent; g < G; ++g) {
+            ctx->g_lent[g] = 0;
+            if (!ctx->g_pool[g] || pos == cands.size()) continue;
+            const int tid = cands[pos].first, e = cands[pos].second;
+            ++pos;
+            rc = fill(tid, e, g, slot_addr(ctx, (size_t)g));
+            if (rc) return rc;
+            ctx->g_owner[g] = (tid << 12) | e;
+        }
+    } else {
+        for (int g = G - ctx->n_lent; g < G; ++g) {
+            const int tid = g % nt, local = g / nt;
+            TensorState &ts = ctx->t[tid];
+            if (!ts.registered || local >= ts.capacity) continue;
+            ts.lent[local] = 0;
+            int best = -1;
+            for (int e = 0; e < E; ++e)
+                if (ts.slot_of[e] < 0 && (best < 0 || better(tid, e, tid, best))) best = e;
+            if (best < 0) continue;
+            rc = fill(tid, best, local, pool_addr(ctx, tid, local));
+            if (rc) return rc;
+            ts.owner[local] = best;
         }
     }
     rc = publish(ctx, ctx->stream);
     if (rc) return rc;
     CK(cudaStreamSynchronize(ctx->stream));
     ctx->n_lent = 0;
+    return MOE_OK;
+}
+
+int moe_set_global_pool(moe_ctx *ctx, int enable) {
+    if (!ctx) return fail(nullptr, MOE_ERR_ARG, "null ctx");
+    for (const TensorState &ts : ctx->t)
+        if (ts.registered) return fail(ctx, MOE_ERR_STATE, "global pool: choose the pool mode before registering");
+    ctx->global_pool = enable != 0;
+    const size_t G = (size_t)ctx->n_tensors * ctx->spt;
+    ctx->g_owner.assign(ctx->global_pool ? G : 0, -1);
+    ctx->g_pool.assign(ctx->global_pool ? G : 0, 0);
+    ctx->g_lent.assign(ctx->global_pool ? G : 0, 0);
+    return MOE_OK;
+}
+
+int moe_set_preheat(moe_ctx *ctx, int enable) {
+    if (!ctx) return fail(nullptr, MOE_ERR_ARG, "null ctx");
+    if (ctx->n_lent) return fail(ctx, MOE_ERR_STATE, "preheat: switch it while no slot is lent");
+    CK(cudaSetDevice(ctx->dev));
+    if (enable && !ctx->d_use) {
+        const size_t n = (size_t)ctx->cfg.n_layers * ctx->E;
+        CK(cudaMalloc(&ctx->d_use, sizeof(uint32_t) * n));
+        CK(cudaMemset(ctx->d_use, 0, sizeof(uint32_t) * n));
+        CK(cudaDeviceSynchronize());
+    }
+    ctx->preheat = enable != 0;
+    return MOE_OK;
+}
+
+int moe_pool_snapshot(moe_ctx *ctx, int32_t *owner_key, uint32_t *stamps) {
+    if (!ctx) return fail(nullptr, MOE_ERR_ARG, "null ctx");
+    CK(cudaSetDevice(ctx->dev));
+    int rc = sync_all(ctx);
+    if (rc) return rc;
+    const int nt = ctx->n_tensors, spt = ctx->spt, G = nt * spt;
+    if (!G) return MOE_OK;
+    std::vector<uint32_t> st((size_t)nt * std::max(1, spt));
+    if (stamps) CK(cudaMemcpy(st.data(), ctx->d_stamps, sizeof(uint32_t) * st.size(), cudaMemcpyDeviceToHost));
+    for (int g = 0; g < G; ++g) {
+        const int tid = g % nt, local = g / nt;
+        int key = -1;
+        if (ctx->global_pool) {
+            key = ctx->g_owner[g];
+        } else {
+            const TensorState &ts = ctx->t[tid];
+            if (ts.registered && local < ts.capacity && !ts.lent[local] && ts.owner[local] >= 0)
+                key = (tid << 12) | ts.owner[local];
+        }
+        if (owner_key) owner_key[g] = key;
+        if (stamps) stamps[g] = st[ctx->global_pool ? (size_t)g : (size_t)tid * spt + local];
+    }
     return MOE_OK;
 }
 
@@ -1040,6 +1275,22 @@ int moe_cache_snapshot(moe_ctx *ctx, int tensor_id, uint64_t *tbl, int32_t *slot
     if (tbl) CK(cudaMemcpy(tbl, ctx->d_tbl + (size_t)tensor_id * E, sizeof(uint64_t) * E, cudaMemcpyDeviceToHost));
     if (slot_of) memcpy(slot_of, ts.slot_of.data(), sizeof(int32_t) * E);
     if (last_seen) memcpy(last_seen, ts.last_seen.data(), sizeof(int32_t) * E);
+    if (ctx->global_pool) {
+        // the tensor's home slots g = s * n_tensors + tensor_id of the shared pool
+        const int nt = ctx->n_tensors;
+        std::vector<uint32_t> st;
+        if (stamps && ctx->spt) {
+            st.resize((size_t)nt * ctx->spt);
+            CK(cudaMemcpy(st.data(), ctx->d_stamps, sizeof(uint32_t) * st.size(), cudaMemcpyDeviceToHost));
+        }
+        for (int s = 0; s < ctx->spt; ++s) {
+            const size_t g = (size_t)s * nt + tensor_id;
+            const int key = ctx->g_owner[g];
+            if (owner) owner[s] = (key >= 0 && (key >> 12) == tensor_id) ? (key & 0xfff) : -1;
+            if (stamps) stamps[s] = st[g];
+        }
+        return MOE_OK;
+    }
     if (owner)
         for (int s = 0; s < ctx->spt; ++s) owner[s] = ts.lent[s] ? -1 : ts.owner[s];
     if (stamps && ctx->spt)
@@ -1079,6 +1330,7 @@ void moe_destroy(moe_ctx *ctx) {
     cudaFree(ctx->d_tbl);
     cudaFree(ctx->d_slot);
     cudaFree(ctx->d_stamps);
+    cudaFree(ctx->d_use);
     cudaFree(ctx->d_bitmap);
     cudaFree(ctx->d_stepbuf);
     cudaFree(ctx->d_clock);

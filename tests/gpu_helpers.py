@@ -82,7 +82,7 @@ class Model:
     """A small stack of expert tensors registered in one context."""
 
     def __init__(self, H, F, E, k, L, capacity, max_tokens, seed=0, routing="zipf", zipf_s=1.1, window=64,
-                 slots_per_tensor=None, max_swaps=0, stream=None):
+                 slots_per_tensor=None, max_swaps=0, stream=None, global_pool=False, preheat=False):
         import torch
         self.torch = torch
         self.wl = synth.Workload("test", H, E, k, F, L, routing=routing, zipf_s=zipf_s, seed=seed,
@@ -95,8 +95,13 @@ class Model:
         self.ctx = qec.moe_layer_init(H, F, E, k, L, self.spt, max_tokens, window_tokens=window,
                                       max_swaps_per_step=max_swaps, stream=stream)
         self.tensors = {}
+        self.global_pool = global_pool
+        if global_pool:
+            qec.moe_set_global_pool(self.ctx, True)
+        if preheat:
+            qec.moe_set_preheat(self.ctx, True)
         self.policy = oracle.PolicyOracle(E, window=window, max_swaps_per_step=max_swaps,
-                                          slots_per_tensor=self.spt, n_tensors=3 * L)
+                                          slots_per_tensor=self.spt, n_tensors=3 * L, global_pool=global_pool)
         for layer in range(L):
             order = self.wl.seed_order(layer)
             cap = self.wl.layer_capacity(layer)
@@ -154,7 +159,8 @@ class Model:
         for e in range(self.E):
             s = snap["slot_of"][e]
             if s >= 0:
-                out[e] = lay["pool_base"] + (s * lay["n_tensors"] + tid) * lay["slot_bytes"]
+                g = s if self.global_pool else s * lay["n_tensors"] + tid
+                out[e] = lay["pool_base"] + g * lay["slot_bytes"]
             else:
                 out[e] = (lay["host_base"] + e * lay["slot_bytes"]) | 1
         return out
