@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--cpu-sample-steps", type=int, default=6)
     ap.add_argument("--prefill-steps", type=int, default=2)
     ap.add_argument("--prefill-workload", default="prefill_t4096")
+    ap.add_argument("--pool-steps", type=int, default=256,
+                    help="decode tokens per run of the pool-mode / preheat leg (0 skips it)")
     ap.add_argument("--case", default=None, choices=["decode_layer", "prefill_layer"],
                     help="small profiling case: one layer (hidden 2048, 512 experts, top-8, FFN 1152, every "
                          "expert resident), --launches forwards at batch 1 (routed) or 4096 tokens")
@@ -402,6 +404,8 @@ def run_ours(args):
     del X, LG, Xp, LGp
     if args.prefill_steps > 0:
         out["prefill"] = run_prefill_leg(args, qec, synth, torch, log)
+    if args.pool_steps > 0:
+        out["pool"] = run_pool_leg(args, qec, synth, torch, log)
     if rank == 0:
         out["cpu_baseline"] = cpu_baseline(wl, args.cpu_sample_steps, T) if args.cpu_sample_steps > 0 else None
         print(json.dumps(out), flush=True)
@@ -443,6 +447,99 @@ def run_case(args):
     qec.moe_destroy(ctx)
     print(json.dumps({"case": args.case, "tokens": T, "launches": n,
                       "median_ms_per_forward": round(float(np.median(ms[2:])), 5)}), flush=True)
+
+
+def run_pool_leg(args, qec, synth, torch, log):
+    """Shared expert pool and prefill preheat against per-tensor pools, on
+    the 25%-pool model (one registration; moe_cache_reset puts the seeded
+    state back before every run).  (1) decode_b1_pool25: args.pool_steps
+    batch-1 decode tokens from the seeded state with a pool per tensor and
+    with one pool for all layers, alternated twice.  (2)
+    prompt_then_decode_pool25 (same weights and seeding, the request's
+    popularity drifted from the seeding table), one pool: half of the pool is
+    lent to a 4096-token prompt pass, given back refilled by seed order or,
+    with prefill preheat, by the prompt's use counts, then args.pool_steps
+    decode tokens.  Tokens/s from CUDA events around the decode loop (forwards
+    and promotion passes), hit rate from the library's counters."""
+    stream = torch.cuda.Stream()
+    sp = stream.cuda_stream
+    wl = synth.WORKLOADS["decode_b1_pool25"]
+    wp = synth.WORKLOADS["prompt_then_decode_pool25"]
+    L, H, E, k, F = wl.n_layers, wl.hidden, wl.n_experts, wl.top_k, wl.ffn
+    T = wp.phases[0][1]
+    spt = max(wl.layer_capacity(l) for l in range(L))
+    ctx = qec.moe_layer_init(H, F, E, k, L, spt, T, stream=sp)
+    register_workload(qec, synth, ctx, wl, log)
+    idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, k), device="cuda")
+    y = torch.empty((T, H), device="cuda")
+
+    def inputs(w_, n, phase):
+        X = np.stack([np.stack([w_.x(l, s, 1, phase) for l in range(L)]) for s in range(n)])
+        LG = np.stack([np.stack([w_.logits(l, s, 1, phase) for l in range(L)]) for s in range(n)])
+        return torch.from_numpy(X).cuda(), torch.from_numpy(LG).cuda()
+
+    def decode(X, LG):
+        n = X.shape[0]
+        torch.cuda.synchronize()
+        s0 = qec.moe_stats(ctx)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for s in range(n):
+            for l in range(L):
+                qec.moe_ffn_forward_routed(ctx, l, X[s, l], LG[s, l], 1, idx[:1], w[:1], y[:1], sp)
+            qec.cache_step(ctx, 1)
+        e1.record(stream)
+        stream.synchronize()
+        ms = e0.elapsed_time(e1)
+        s1 = qec.moe_stats(ctx)
+        d = {key: s1[key] - s0[key] for key in ("hits", "misses", "admissions", "evictions", "cold_bytes")}
+        return {"tokens_per_s": round(n / (ms * 1e-3), 1), "ms_per_token": round(ms / n, 4),
+                "hit_rate": round(d["hits"] / max(1, d["hits"] + d["misses"]), 4), **d}
+
+    out = {"workload": (f"{wl.name}: {L} layers, hidden {H}, {E} experts, top-{k}, FFN {F}, Zipf({wl.zipf_s}) "
+                        f"routing, 128/512 experts per tensor seeded, {args.pool_steps} batch-1 decode tokens "
+                        f"from the seeded state per run")}
+    X, LG = inputs(wl, args.pool_steps, 0)
+    runs = {"per_tensor": [], "global": []}
+    for name in ("per_tensor", "global", "per_tensor", "global"):
+        qec.moe_cache_reset(ctx, name == "global")
+        runs[name].append(decode(X, LG))
+        log(f"pool leg, {wl.name}, {name} pool: {runs[name][-1]}")
+    for name, r in runs.items():
+        out[name] = dict(r[-1], tokens_per_s_runs=[v["tokens_per_s"] for v in r])
+    del X, LG
+    # prompt pass, then decode
+    n_borrow = 3 * L * spt // 2
+    PX = [torch.from_numpy(wp.x(l, 0, T, 0)).cuda() for l in range(L)]
+    PLG = [torch.from_numpy(wp.logits(l, 0, T, 0)).cuda() for l in range(L)]
+    X, LG = inputs(wp, args.pool_steps, 1)
+    prompt = {}
+    for name in ("seed_refill", "preheat"):
+        qec.moe_cache_reset(ctx, True)
+        qec.moe_set_preheat(ctx, name == "preheat")
+        qec.moe_pool_borrow(ctx, n_borrow)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for l in range(L):
+            qec.route_topk(ctx, PLG[l], T, E, k, idx, w, sp)
+            qec.moe_ffn_forward(ctx, l, PX[l], T, idx, w, y, sp)
+        e1.record(stream)
+        stream.synchronize()
+        qec.miss_drain(ctx)
+        qec.moe_pool_return(ctx)
+        r = decode(X, LG)
+        r["prompt_pass_ms"] = round(e0.elapsed_time(e1), 2)
+        prompt[name] = r
+        log(f"pool leg, {wp.name}, {name}: {r}")
+    qec.moe_destroy(ctx)
+    prompt["workload"] = (f"{wp.name}: one pool for all layers (128/512 per tensor seeded), {n_borrow} of "
+                          f"{3 * L * spt} blocks lent to a {T}-token prompt pass (cold experts staged through the "
+                          f"lent blocks), then {args.pool_steps} decode tokens; the request's popularity ranks "
+                          f"drift from the seeding table (rank noise {wp.drift} x E)")
+    out["prompt_then_decode"] = prompt
+    return out
 
 
 def run_prefill_leg(args, qec, synth, torch, log):

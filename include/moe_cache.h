@@ -236,6 +236,20 @@ int moe_set_global_pool(moe_ctx *ctx, int enable);
 int moe_set_preheat(moe_ctx *ctx, int enable);
 
 /*
+ * Put the cache back in its registered state, with a pool mode chosen anew
+ * (global_pool = 1: one pool for all layers, as moe_set_global_pool; 0: a
+ * pool per tensor).  Every tensor holds its seeded experts again (seed order
+ * in local slots 0..n_seed-1; slots already holding their seed expert are
+ * not uploaded again), stamps, sightings, clock, miss log and preheat counts
+ * are cleared, statistics restart from zero (upload_bytes keeps counting),
+ * and lookahead buffers are marked empty.  Lets runs that must start from
+ * the same state (a per-tensor and a shared pool, say) share one
+ * registration and its pinned host copies.  Synchronous.  Errors:
+ * MOE_ERR_STATE (slots are lent), MOE_ERR_CUDA.
+ */
+int moe_cache_reset(moe_ctx *ctx, int global_pool);
+
+/*
  * Owner and stamp of every arena slot (3L x slots_per_tensor entries, global
  * slot g = local slot g / 3L of tensor g % 3L), either pool mode; synchronizes
  * with all streams.  owner_key: (tensor_id << 12 | expert), or -1 for a free,

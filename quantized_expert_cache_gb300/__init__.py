@@ -58,6 +58,7 @@ SIGNATURES = {
     "moe_set_global_pool": (_i32, [_vp, _i32]),
     "moe_set_preheat": (_i32, [_vp, _i32]),
     "moe_pool_snapshot": (_i32, [_vp, _vp, _vp]),
+    "moe_cache_reset": (_i32, [_vp, _i32]),
     "moe_cache_snapshot": (_i32, [_vp, _i32, _vp, _vp, _vp, _vp, _vp]),
     "moe_cache_layout": (_i32, [_vp, _i32, _vp, _vp, _vp, _vp]),
     "moe_stats": (_i32, [_vp, ctypes.POINTER(moe_stats_t)]),
@@ -199,6 +200,10 @@ def moe_set_global_pool(ctx, enable=True):
 
 def moe_set_preheat(ctx, enable=True):
     return _check(ctx, load().moe_set_preheat(ctx, 1 if enable else 0))
+
+
+def moe_cache_reset(ctx, global_pool=False):
+    return _check(ctx, load().moe_cache_reset(ctx, 1 if global_pool else 0))
 
 
 def moe_pool_snapshot(ctx, n_slots):

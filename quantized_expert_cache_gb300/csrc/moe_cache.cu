@@ -31,7 +31,7 @@ thread_local std::string g_init_error;
 
 struct TensorState {
     bool registered = false;
-    int capacity = 0;
+    int capacity = 0, n_seed = 0;
     uint8_t *home = nullptr;  // pinned, device-mapped: n_experts blobs of slot_stride bytes
     uint64_t home_dev = 0;
     std::vector<int32_t> seed_order, rank, slot_of, owner, last_seen;  // slot_of: global slot in a shared pool
@@ -312,6 +312,7 @@ struct GlobalPick {
     std::vector<std::pair<uint32_t, int>> victims;
     size_t vpos = 0;
     int took = 0;
+    int n_qualified = 0;  // misses of the step that qualify for admission
 };
 
 // One admission of (tid, e) into the shared pool: lowest free slot, else the
@@ -338,6 +339,10 @@ int admit_global(moe_ctx *ctx, GlobalPick &gs, int tid, int e, uint64_t clk, int
             for (int v = 0; v < G; ++v)
                 if (ctx->g_pool[v] && !ctx->g_lent[v] && ctx->g_owner[v] >= 0 && (uint64_t)ctx->h_stamps[v] < clk)
                     gs.victims.emplace_back(ctx->h_stamps[v], v);
+            // no more victims than admissions can be asked for this step
+            const size_t need = std::min(gs.victims.size(), (size_t)std::max(0, gs.n_qualified));
+            std::nth_element(gs.victims.begin(), gs.victims.begin() + (long)need, gs.victims.end());
+            gs.victims.resize(need);
             std::sort(gs.victims.begin(), gs.victims.end());
             gs.victims_built = true;
         }
@@ -577,6 +582,7 @@ int register_expert_tensor(moe_ctx *ctx, int layer, int kind, const void *host_q
     ts.home_dev = (uint64_t)(uintptr_t)home_dev;
     repack((const uint8_t *)host_q4, ts.home, E, rows, cols / 32, ctx->stride);
     ts.capacity = capacity;
+    ts.n_seed = n_seed;
     ts.seed_order = order;
     ts.rank.assign(E, 0);
     for (int i = 0; i < E; ++i) ts.rank[order[i]] = i;
@@ -950,6 +956,26 @@ int cache_step(moe_ctx *ctx, int n_tokens) {
     std::vector<char> fresh;  // tensors whose stamp mirror was read back this step
     GlobalPick gs;            // shared pool: free slots and victims of this step
     if (ctx->n_lent == 0) {
+        // the misses that qualify for admission (second sighting inside the
+        // window; each key is unique and cold, so nothing below changes this)
+        std::vector<int> q_tid;
+        for (uint32_t key : keys) {
+            const int tid = (int)(key >> 12), e = (int)(key & 0xfff);
+            if (tid >= nt || e >= ctx->E || !ctx->t[tid].registered) continue;
+            const int64_t ls = ctx->t[tid].last_seen[e];
+            if (ls >= 0 && (int64_t)clk - ls < (int64_t)ctx->cfg.window_tokens) q_tid.push_back(tid);
+        }
+        gs.n_qualified = (int)q_tid.size();
+        if (!ctx->global_pool && !q_tid.empty()) {
+            // many admitting tensors: one read of every stamp beats one
+            // round trip per tensor
+            const size_t n_q = (size_t)(std::unique(q_tid.begin(), q_tid.end()) - q_tid.begin());
+            if ((size_t)nt * spt * sizeof(uint32_t) <= n_q * 16384) {
+                CK(cudaMemcpy(ctx->h_stamps, ctx->d_stamps, sizeof(uint32_t) * (size_t)nt * spt,
+                              cudaMemcpyDeviceToHost));
+                fresh.assign(nt, 1);
+            }
+        }
         for (uint32_t key : keys) {
             const int tid = (int)(key >> 12), e = (int)(key & 0xfff);
             if (tid >= nt || e >= ctx->E || !ctx->t[tid].registered) continue;
@@ -1199,6 +1225,87 @@ int moe_set_preheat(moe_ctx *ctx, int enable) {
         CK(cudaDeviceSynchronize());
     }
     ctx->preheat = enable != 0;
+    return MOE_OK;
+}
+
+int moe_cache_reset(moe_ctx *ctx, int global_pool) {
+    if (!ctx) return fail(nullptr, MOE_ERR_ARG, "null ctx");
+    if (ctx->n_lent) return fail(ctx, MOE_ERR_STATE, "reset: slots are lent");
+    CK(cudaSetDevice(ctx->dev));
+    int rc = sync_all(ctx);
+    if (rc) return rc;
+    const int nt = ctx->n_tensors, E = ctx->E, spt = ctx->spt;
+    const size_t G = (size_t)nt * spt;
+    // what every arena slot holds now: slots that already hold their seed
+    // expert are not uploaded again
+    std::vector<int32_t> held(G, -1);
+    for (int tid = 0; tid < nt; ++tid) {
+        const TensorState &ts = ctx->t[tid];
+        if (!ts.registered) continue;
+        for (int e = 0; e < E; ++e) {
+            const int s = ts.slot_of[e];
+            if (s >= 0) held[ctx->global_pool ? (size_t)s : (size_t)s * nt + tid] = (tid << 12) | e;
+        }
+    }
+    ctx->global_pool = global_pool != 0;
+    ctx->g_owner.assign(ctx->global_pool ? G : 0, -1);
+    ctx->g_pool.assign(ctx->global_pool ? G : 0, 0);
+    ctx->g_lent.assign(ctx->global_pool ? G : 0, 0);
+    std::vector<uint64_t> tbl((size_t)nt * E, 0);
+    std::vector<int32_t> dslot((size_t)nt * E, -1);
+    for (int tid = 0; tid < nt; ++tid) {
+        TensorState &ts = ctx->t[tid];
+        if (!ts.registered) continue;
+        ts.slot_of.assign(E, -1);
+        ts.owner.assign(spt, -1);
+        ts.last_seen.assign(E, -1);
+        ts.lent.assign(spt, 0);
+        for (int e = 0; e < E; ++e) ts.tbl[e] = home_entry(ctx, tid, e);
+        if (ctx->global_pool)
+            for (int s = 0; s < ts.capacity; ++s) ctx->g_pool[(size_t)s * nt + tid] = 1;
+        for (int s = 0; s < ts.n_seed; ++s) {
+            const int e = ts.seed_order[s];
+            const size_t g = (size_t)s * nt + tid;
+            const uint64_t dst = slot_addr(ctx, g);
+            if (held[g] != ((tid << 12) | e)) {
+                CK(cudaMemcpyAsync((void *)(uintptr_t)dst, ts.home + (size_t)e * ctx->stride, ctx->blob,
+                                   cudaMemcpyHostToDevice, ctx->stream));
+                ctx->stats.upload_bytes += ctx->blob;
+            }
+            ts.tbl[e] = dst;
+            if (ctx->global_pool) {
+                ts.slot_of[e] = (int32_t)g;
+                ctx->g_owner[g] = (tid << 12) | e;
+            } else {
+                ts.slot_of[e] = s;
+                ts.owner[s] = e;
+            }
+        }
+        for (int e = 0; e < E; ++e) {
+            tbl[(size_t)tid * E + e] = ts.tbl[e];
+            dslot[(size_t)tid * E + e] = stamp_index(ctx, tid, ts.slot_of[e]);
+        }
+    }
+    CK(cudaMemcpyAsync(ctx->d_tbl, tbl.data(), sizeof(uint64_t) * tbl.size(), cudaMemcpyHostToDevice, ctx->stream));
+    CK(cudaMemcpyAsync(ctx->d_slot, dslot.data(), sizeof(int32_t) * dslot.size(), cudaMemcpyHostToDevice,
+                       ctx->stream));
+    CK(cudaMemsetAsync(ctx->d_stamps, 0, sizeof(uint32_t) * (size_t)nt * std::max(1, spt), ctx->stream));
+    CK(cudaMemsetAsync(ctx->d_bitmap, 0, sizeof(uint32_t) * (size_t)nt * ctx->bitmap_words, ctx->stream));
+    CK(cudaMemsetAsync(ctx->d_stepbuf, 0, sizeof(uint32_t) * ((size_t)ctx->hit_words + 1), ctx->stream));
+    CK(cudaMemsetAsync(ctx->d_clock, 0, sizeof(uint32_t), ctx->stream));
+    CK(cudaMemsetAsync(ctx->d_cold, 0, sizeof(unsigned long long), ctx->stream));
+    if (ctx->d_use)
+        CK(cudaMemsetAsync(ctx->d_use, 0, sizeof(uint32_t) * (size_t)ctx->cfg.n_layers * E, ctx->stream));
+    CK(cudaStreamSynchronize(ctx->stream));
+    for (int b = 0; b < 2; ++b) {
+        ctx->pf_layer[b] = -1;
+        ctx->pf_map_pending[b] = false;
+    }
+    ctx->n_upd = 0;
+    ctx->clock = 0;
+    const uint64_t up = ctx->stats.upload_bytes;
+    ctx->stats = moe_stats_t{};
+    ctx->stats.upload_bytes = up;
     return MOE_OK;
 }
 

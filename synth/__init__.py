@@ -27,6 +27,7 @@ STREAM_WEIGHTS = 1
 STREAM_X = 2
 STREAM_LOGITS = 3
 STREAM_PERM = 4
+STREAM_DRIFT = 5
 
 KIND_GATE, KIND_UP, KIND_DOWN = 0, 1, 2
 Q4_BLOCK_BYTES = 18
@@ -152,6 +153,9 @@ class Workload:
     # pool slots per layer (same for gate/up/down of a layer); None = all.
     capacity: list | None = None
     phases: list = field(default_factory=list)  # (label, n_tokens, n_steps)
+    # request drift: the routed popularity ranks are the seeding table's
+    # ranks plus N(0, (drift * E)^2) noise, re-ranked (0 = the table exactly)
+    drift: float = 0.0
 
     @property
     def tensor_shapes(self):
@@ -181,6 +185,16 @@ class Workload:
         """perm[r] = the expert holding popularity rank r+1 in this layer."""
         return permutation(key(self.seed, STREAM_PERM, layer), self.n_experts)
 
+    def request_perm(self, layer: int) -> np.ndarray:
+        """The permutation the logits are drawn with: perm(layer), or with
+        drift its ranks jittered by seeded Gaussian noise and re-ranked."""
+        base = self.perm(layer)
+        if self.drift <= 0.0:
+            return base
+        z = normal(key(self.seed, STREAM_DRIFT, layer), (self.n_experts,)).astype(np.float64)
+        order = np.argsort(np.arange(self.n_experts) + self.drift * self.n_experts * z, kind="stable")
+        return base[order]
+
     def seed_order(self, layer: int) -> np.ndarray:
         """Synthetic routing-frequency table: experts by expected pick
         frequency, most frequent first (rank order of the popularity)."""
@@ -201,7 +215,7 @@ class Workload:
         p = self.popularity()
         if p is None:
             return normal(k, (T, self.n_experts))
-        perm = self.perm(layer)
+        perm = self.request_perm(layer)
         base = np.empty(self.n_experts, np.float64)
         base[perm] = np.log(p)
         return gumbel_logits(k, base, T)
@@ -224,6 +238,11 @@ WORKLOADS = {
                                    zipf_s=1.1, capacity=_c1_capacity(), phases=[("decode", 1, 128)]),
     "decode_b1_pool25": Workload("decode_b1_pool25", 2048, 512, 8, 1152, 48, routing="zipf",
                                  zipf_s=1.1, capacity=[128] * 48, phases=[("decode", 1, 256)]),
+    # a 4096-token prompt, then decode, on the 25% pool; the request's expert
+    # popularity drifts from the seeding table (rank noise 0.15 E)
+    "prompt_then_decode_pool25": Workload("prompt_then_decode_pool25", 2048, 512, 8, 1152, 48, routing="zipf",
+                                          zipf_s=1.1, capacity=[128] * 48, drift=0.15,
+                                          phases=[("prefill", 4096, 1), ("decode", 1, 256)]),
     "prefill_t4096": Workload("prefill_t4096", 2048, 512, 8, 1152, 48, routing="zipf", zipf_s=1.1,
                               capacity=[384] * 48, phases=[("prefill", 4096, 1)]),
     "large_expert": Workload("large_expert", 2880, 128, 4, 2880, 36, routing="mix", zipf_s=0.8,

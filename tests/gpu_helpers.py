@@ -100,8 +100,8 @@ class Model:
             qec.moe_set_global_pool(self.ctx, True)
         if preheat:
             qec.moe_set_preheat(self.ctx, True)
-        self.policy = oracle.PolicyOracle(E, window=window, max_swaps_per_step=max_swaps,
-                                          slots_per_tensor=self.spt, n_tensors=3 * L, global_pool=global_pool)
+        self.window, self.max_swaps = window, max_swaps
+        self._new_policy()
         for layer in range(L):
             order = self.wl.seed_order(layer)
             cap = self.wl.layer_capacity(layer)
@@ -112,6 +112,21 @@ class Model:
                 assert tid == layer * 3 + kind
                 self.tensors[tid] = t
                 self.policy.add_tensor(tid, cap, order, cap)
+
+    def _new_policy(self):
+        self.policy = oracle.PolicyOracle(self.E, window=self.window, max_swaps_per_step=self.max_swaps,
+                                          slots_per_tensor=self.spt, n_tensors=3 * self.L,
+                                          global_pool=self.global_pool)
+
+    def reset(self, global_pool):
+        """Registered state again (library and oracle), in a pool mode."""
+        qec.moe_cache_reset(self.ctx, global_pool)
+        self.global_pool = global_pool
+        self._new_policy()
+        for layer in range(self.L):
+            cap = self.wl.layer_capacity(layer)
+            for kind in range(3):
+                self.policy.add_tensor(layer * 3 + kind, cap, self.wl.seed_order(layer), cap)
 
     def close(self):
         qec.moe_destroy(self.ctx)

@@ -184,3 +184,20 @@ def test_pool_mode_errors():
         qec.moe_pool_return(ctx)
     finally:
         qec.moe_destroy(ctx)
+
+
+def test_cache_reset_switches_pool_mode_and_restarts_from_seeding():
+    m = Model(H=256, F=256, E=32, k=4, L=2, capacity=[8, 3], max_tokens=4, window=8, zipf_s=1.0,
+              slots_per_tensor=8)
+    try:
+        for gp in (False, True, True, False):
+            if gp or m.policy.clock:
+                m.reset(gp)
+            _assert_state(m)
+            st = qec.moe_stats(m.ctx)
+            assert st["hits"] == st["misses"] == st["admissions"] == st["steps"] == 0
+            for _ in _steps(m, 25, lambda s: 1 if s % 4 else 2, check_every=12):
+                _assert_state(m)
+            _stats_match(m)
+    finally:
+        m.close()

@@ -284,3 +284,18 @@ def test_quantizer_exact_ties_round_half_even():
     assert dd[0, 0] == np.float16(d).view(np.uint16)
     assert q[0, 0] == 127
     assert q[0, 1:1 + len(halves)].tolist() == expect
+
+
+def test_request_drift_is_a_seeded_jitter_of_the_table():
+    wl = synth.WORKLOADS["prompt_then_decode_pool25"]
+    base = synth.Workload("b", wl.hidden, wl.n_experts, wl.top_k, wl.ffn, wl.n_layers, routing="zipf",
+                          zipf_s=wl.zipf_s, capacity=wl.capacity)
+    for layer in (0, 17):
+        p, q = wl.perm(layer), wl.request_perm(layer)
+        assert np.array_equal(p, base.perm(layer)) and np.array_equal(base.request_perm(layer), p)
+        assert sorted(q.tolist()) == list(range(wl.n_experts)) and not np.array_equal(p, q)
+        assert np.array_equal(q, wl.request_perm(layer))
+        # rank noise 0.15 E: the hot sets overlap but are not the same
+        top = len(set(p[:128].tolist()) & set(q[:128].tolist()))
+        assert 64 < top < 128
+        assert np.array_equal(wl.seed_order(layer), p)
