@@ -5,7 +5,7 @@ with a quantized expert cache, used to check the CUDA path.  Only the tests,
 ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline leg may import
 it.  It shares no code with the CUDA library, and the library never calls it.
 
-- ``moe_oracle.c``: numerics (top-k, activation quantization, Q4 block dots,
+- ``moe_oracle.c``: numerics (top-k, activation quantization, Q4 and Q8_0 block dots,
   SwiGLU, down projection and combine), binary64 with the integer-deciding
   steps in binary32 (see the header of that file);
 - ``policy.py``: the admission / eviction policy of the expert pools.
@@ -55,14 +55,14 @@ def lib():
         L.orc_f2h.argtypes = [f32]
         L.orc_topk.argtypes = [vp, i32, i32, i32, i32, vp, vp]
         L.orc_quantize_blocks.argtypes = [vp, i32, vp, vp]
-        L.orc_dequant.argtypes = [vp, i32, vp]
-        L.orc_block_dot.restype = ctypes.c_int32
-        L.orc_block_dot.argtypes = [vp, vp]
-        L.orc_row_dot.restype = ctypes.c_double
-        L.orc_row_dot.argtypes = [vp, vp, vp, i32, vp]
-        L.orc_expert.argtypes = [vp, vp, vp, i32, i32, vp, vp] + [vp] * 8
-        L.orc_down_combine.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]
-        L.orc_layer.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp] + [vp] * 9
+        L.orc_dequant_fmt.argtypes = [vp, i32, i32, vp]
+        L.orc_block_dot_fmt.restype = ctypes.c_int32
+        L.orc_block_dot_fmt.argtypes = [vp, vp, i32]
+        L.orc_row_dot_fmt.restype = ctypes.c_double
+        L.orc_row_dot_fmt.argtypes = [vp, vp, vp, i32, i32, vp]
+        L.orc_expert.argtypes = [vp, vp, vp, i32, i32, vp, vp] + [vp] * 8 + [i32]
+        L.orc_down_combine.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, i32]
+        L.orc_layer.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp] + [vp] * 9 + [i32]
         _lib = L
     return _lib
 
@@ -101,19 +101,29 @@ def quantize(x: np.ndarray):
     return q, d
 
 
+BLOCK_BYTES = {18: 0, 34: 1}  # canonical block size -> format (0: Q4, 1: Q8_0)
+
+
+def _fmt(blocks) -> int:
+    """Format of canonical blocks from their last dimension (18: Q4, 34: Q8_0)."""
+    if blocks.shape[-1] not in BLOCK_BYTES:
+        raise ValueError(f"unknown block size {blocks.shape[-1]}")
+    return BLOCK_BYTES[blocks.shape[-1]]
+
+
 def dequant(blocks: np.ndarray) -> np.ndarray:
-    """Canonical Q4 blocks [..., nb, 18] -> float64 [..., nb*32]."""
+    """Canonical blocks [..., nb, 18 (Q4) or 34 (Q8_0)] -> float64 [..., nb*32]."""
     blocks = np.ascontiguousarray(blocks, np.uint8)
-    nb = blocks.size // 18
+    nb = blocks.size // blocks.shape[-1]
     out = np.empty(blocks.shape[:-2] + (blocks.shape[-2] * 32,), np.float64)
-    lib().orc_dequant(_p(blocks), nb, _p(out))
+    lib().orc_dequant_fmt(_p(blocks), nb, _fmt(blocks), _p(out))
     return out
 
 
 def block_dot(block: np.ndarray, qa: np.ndarray) -> int:
     block = np.ascontiguousarray(block, np.uint8)
     qa = np.ascontiguousarray(qa, np.int8)
-    return int(lib().orc_block_dot(_p(block), _p(qa)))
+    return int(lib().orc_block_dot_fmt(_p(block), _p(qa), _fmt(block)))
 
 
 def row_dot(row: np.ndarray, qa: np.ndarray, da: np.ndarray):
@@ -121,20 +131,23 @@ def row_dot(row: np.ndarray, qa: np.ndarray, da: np.ndarray):
     qa = np.ascontiguousarray(qa, np.int8)
     da = np.ascontiguousarray(da, np.uint16)
     a = np.zeros(1, np.float64)
-    r = lib().orc_row_dot(_p(row), _p(qa), _p(da), row.size // 18, _p(a))
+    r = lib().orc_row_dot_fmt(_p(row), _p(qa), _p(da), row.size // row.shape[-1], _fmt(row), _p(a))
     return float(r), float(a[0])
 
 
 def _expert_ptrs(tensor):
-    """Expert tensor given as an array [E, rows, nb, 18] or a dict {e: [rows, nb, 18]}."""
+    """Expert tensor given as an array [E, rows, nb, B] or a dict {e: [rows, nb, B]}
+    (B = 18: Q4, 34: Q8_0).  Returns (pointers, kept arrays, format)."""
     if isinstance(tensor, dict):
         E = max(tensor) + 1
         arrs = {e: np.ascontiguousarray(v, np.uint8) for e, v in tensor.items()}
         ptrs = (ctypes.c_void_p * E)(*[arrs[e].ctypes.data if e in arrs else None for e in range(E)])
-        return ptrs, arrs
+        fmts = {_fmt(v) for v in arrs.values()}
+        assert len(fmts) == 1, "one weight format per tensor"
+        return ptrs, arrs, fmts.pop()
     t = np.ascontiguousarray(tensor, np.uint8)
     ptrs = (ctypes.c_void_p * t.shape[0])(*[t[e].ctypes.data for e in range(t.shape[0])])
-    return ptrs, t
+    return ptrs, t, _fmt(t)
 
 
 def layer(x, idx, w, gate, up, down, H, F, want_intermediates=False):
@@ -143,9 +156,10 @@ def layer(x, idx, w, gate, up, down, H, F, want_intermediates=False):
     idx = np.ascontiguousarray(idx, np.int32)
     w = np.ascontiguousarray(w, np.float64)
     T, k = idx.shape
-    gp, g_keep = _expert_ptrs(gate)
-    upp, u_keep = _expert_ptrs(up)
-    dp, d_keep = _expert_ptrs(down)
+    gp, g_keep, fg = _expert_ptrs(gate)
+    upp, u_keep, fu = _expert_ptrs(up)
+    dp, d_keep, fd = _expert_ptrs(down)
+    assert fg == fu == fd, "gate, up and down share one weight format"
     y = np.empty((T, H), np.float64)
     out = {}
     if want_intermediates:
@@ -157,7 +171,7 @@ def layer(x, idx, w, gate, up, down, H, F, want_intermediates=False):
     lib().orc_layer(T, H, F, k, _p(x), _p(idx), _p(w), ctypes.cast(gp, ctypes.c_void_p),
                     ctypes.cast(upp, ctypes.c_void_p), ctypes.cast(dp, ctypes.c_void_p), _p(y),
                     _p(o.get("xq")), _p(o.get("xd")), _p(o.get("g")), _p(o.get("u")), _p(o.get("gabs")),
-                    _p(o.get("uabs")), _p(o.get("h")), _p(o.get("hq")), _p(o.get("hd")))
+                    _p(o.get("uabs")), _p(o.get("h")), _p(o.get("hq")), _p(o.get("hd")), fg)
     del g_keep, u_keep, d_keep
     return (y, out) if want_intermediates else y
 
@@ -168,8 +182,8 @@ def down_combine(idx, w, down, hq, hd, H, F):
     hq = np.ascontiguousarray(hq, np.int8)
     hd = np.ascontiguousarray(hd, np.uint16)
     T, k = idx.shape
-    dp, keep = _expert_ptrs(down)
+    dp, keep, fd = _expert_ptrs(down)
     y = np.empty((T, H), np.float64)
-    lib().orc_down_combine(T, H, F, k, _p(idx), _p(w), ctypes.cast(dp, ctypes.c_void_p), _p(hq), _p(hd), _p(y))
+    lib().orc_down_combine(T, H, F, k, _p(idx), _p(w), ctypes.cast(dp, ctypes.c_void_p), _p(hq), _p(hd), _p(y), fd)
     del keep
     return y

@@ -16,10 +16,15 @@
  *       by the matmuls that share one input (router and gate/up).
  *  [S5] mihailescu2m/llama.cpp -- "the graph-shape problem" (top-k of 512
  *       expert scores).
- *  Format of the weights: Q4 blocks of 32 weights with one binary16 scale d
- *  and 4-bit codes q, w = d * (q - 8) (the block-quantized weight format of
- *  the workloads); byte j of the 16 code bytes holds element j in its low
- *  nibble and element j+16 in its high nibble (the canonical Q4 block order).
+ *  Format of the weights (fmt): 0 = Q4 blocks of 32 weights with one
+ *  binary16 scale d and 4-bit codes q, w = d * (q - 8) (the block-quantized
+ *  weight format of the workloads); byte j of the 16 code bytes holds element
+ *  j in its low nibble and element j+16 in its high nibble (the canonical Q4
+ *  block order).  1 = Q8_0, one of the other block formats the
+ *  Zapdev-labs/a6000-custom-kernels dot kernels accept: blocks of 32 with one
+ *  binary16 scale d and 32 signed 8-bit codes q, w = d * q; the pages give no
+ *  byte layout, the reading is d (little endian) followed by code bytes 0..31
+ *  in element order (34 bytes).
  *
  * Readings where the pages are silent (each listed in the design notes):
  *  - top-k order is (logit descending, expert index ascending): ties go to
@@ -45,6 +50,9 @@
 
 #define ORC_BLOCK 32
 #define ORC_BLOCK_BYTES 18
+#define ORC_Q8_BLOCK_BYTES 34
+
+static size_t orc_bbytes(int fmt) { return fmt == 1 ? ORC_Q8_BLOCK_BYTES : ORC_BLOCK_BYTES; }
 
 /* ---- binary16 <-> binary64/32 from the IEEE 754 definition ------------- */
 
@@ -145,7 +153,7 @@ void orc_quantize_blocks(const float *x, int n, int8_t *q, uint16_t *d) {
     }
 }
 
-/* ---- Q4 weights ------------------------------------------------------------ */
+/* ---- quantized weights ------------------------------------------------------ */
 
 /* 4-bit code of element i (0..31) of a canonical 18-byte block. */
 static int orc_code(const uint8_t *blk, int i) {
@@ -153,32 +161,42 @@ static int orc_code(const uint8_t *blk, int i) {
     return i < 16 ? (qs[i] & 15) : (qs[i - 16] >> 4);
 }
 
+/* Signed weight code of element i: q - 8 (Q4) or q (Q8_0), so w = d * code. */
+static int orc_wcode(const uint8_t *blk, int i, int fmt) {
+    return fmt == 1 ? (int)(int8_t)blk[2 + i] : orc_code(blk, i) - 8;
+}
+
 static uint16_t orc_block_scale(const uint8_t *blk) { return (uint16_t)(blk[0] | (blk[1] << 8)); }
 
-/* Dequantized weights of nb blocks: w = d * (q - 8). */
-void orc_dequant(const uint8_t *blocks, int nb, double *out) {
+/* Dequantized weights of nb blocks: w = d * (q - 8) (Q4) or d * q (Q8_0). */
+void orc_dequant_fmt(const uint8_t *blocks, int nb, int fmt, double *out) {
     for (int b = 0; b < nb; ++b) {
-        const uint8_t *blk = blocks + (size_t)b * ORC_BLOCK_BYTES;
+        const uint8_t *blk = blocks + (size_t)b * orc_bbytes(fmt);
         double d = orc_h2d(orc_block_scale(blk));
-        for (int i = 0; i < ORC_BLOCK; ++i) out[(size_t)b * ORC_BLOCK + i] = d * (double)(orc_code(blk, i) - 8);
+        for (int i = 0; i < ORC_BLOCK; ++i) out[(size_t)b * ORC_BLOCK + i] = d * (double)orc_wcode(blk, i, fmt);
     }
 }
 
-/* [A2] integer block dot: sum_i (q_w,i - 8) * q_a,i, exact in int32. */
-int32_t orc_block_dot(const uint8_t *blk, const int8_t *qa) {
+void orc_dequant(const uint8_t *blocks, int nb, double *out) { orc_dequant_fmt(blocks, nb, 0, out); }
+
+/* [A2] integer block dot: sum_i code_w,i * q_a,i, exact in int32
+ * (|sum| <= 32 * 8 * 127 for Q4, 32 * 128 * 127 for Q8_0). */
+int32_t orc_block_dot_fmt(const uint8_t *blk, const int8_t *qa, int fmt) {
     int32_t s = 0;
-    for (int i = 0; i < ORC_BLOCK; ++i) s += (int32_t)(orc_code(blk, i) - 8) * (int32_t)qa[i];
+    for (int i = 0; i < ORC_BLOCK; ++i) s += (int32_t)orc_wcode(blk, i, fmt) * (int32_t)qa[i];
     return s;
 }
+
+int32_t orc_block_dot(const uint8_t *blk, const int8_t *qa) { return orc_block_dot_fmt(blk, qa, 0); }
 
 /* One weight row (nb blocks) against one quantized activation vector:
  * r = sum_b d_w,b * d_a,b * sumi_b, in binary64, block order.  abs_sum gets
  * sum_b |d_w,b * d_a,b * sumi_b| (for error bounds), if not NULL. */
-double orc_row_dot(const uint8_t *row, const int8_t *qa, const uint16_t *da, int nb, double *abs_sum) {
+double orc_row_dot_fmt(const uint8_t *row, const int8_t *qa, const uint16_t *da, int nb, int fmt, double *abs_sum) {
     double acc = 0.0, aacc = 0.0;
     for (int b = 0; b < nb; ++b) {
-        const uint8_t *blk = row + (size_t)b * ORC_BLOCK_BYTES;
-        int32_t s = orc_block_dot(blk, qa + (size_t)b * ORC_BLOCK);
+        const uint8_t *blk = row + (size_t)b * orc_bbytes(fmt);
+        int32_t s = orc_block_dot_fmt(blk, qa + (size_t)b * ORC_BLOCK, fmt);
         double term = orc_h2d(orc_block_scale(blk)) * orc_h2d(da[b]) * (double)s;
         acc += term;
         aacc += fabs(term);
@@ -187,23 +205,28 @@ double orc_row_dot(const uint8_t *row, const int8_t *qa, const uint16_t *da, int
     return acc;
 }
 
+double orc_row_dot(const uint8_t *row, const int8_t *qa, const uint16_t *da, int nb, double *abs_sum) {
+    return orc_row_dot_fmt(row, qa, da, nb, 0, abs_sum);
+}
+
 /* ---- [A2] one routed expert on one token: gate/up, SwiGLU, quantize, down --- */
 
-/* gate, up: F rows x (H/32) blocks; down: H rows x (F/32) blocks (canonical).
+/* gate, up: F rows x (H/32) blocks; down: H rows x (F/32) blocks (canonical,
+ * format fmt).
  * Outputs (any may be NULL except o): g, u, |terms| sums of g and u, h (binary64),
  * hq/hd (the quantized h), o (binary64, H values). */
 void orc_expert(const uint8_t *gate, const uint8_t *up, const uint8_t *down, int H, int F, const int8_t *xq,
                 const uint16_t *xd, double *g_out, double *u_out, double *gabs, double *uabs, double *h_out,
-                int8_t *hq_out, uint16_t *hd_out, double *o) {
+                int8_t *hq_out, uint16_t *hd_out, double *o, int fmt) {
     int nbh = H / ORC_BLOCK, nbf = F / ORC_BLOCK;
-    size_t rowh = (size_t)nbh * ORC_BLOCK_BYTES, rowf = (size_t)nbf * ORC_BLOCK_BYTES;
+    size_t rowh = (size_t)nbh * orc_bbytes(fmt), rowf = (size_t)nbf * orc_bbytes(fmt);
     float h32[F > 0 ? F : 1];
     int8_t hq[F > 0 ? F : 1];
     uint16_t hd[F / ORC_BLOCK > 0 ? F / ORC_BLOCK : 1];
     for (int r = 0; r < F; ++r) {
         double ga, ua;
-        double g = orc_row_dot(gate + r * rowh, xq, xd, nbh, &ga);
-        double u = orc_row_dot(up + r * rowh, xq, xd, nbh, &ua);
+        double g = orc_row_dot_fmt(gate + r * rowh, xq, xd, nbh, fmt, &ga);
+        double u = orc_row_dot_fmt(up + r * rowh, xq, xd, nbh, fmt, &ua);
         double h = g * u / (1.0 + exp(-g));
         if (g_out) g_out[r] = g;
         if (u_out) u_out[r] = u;
@@ -215,15 +238,15 @@ void orc_expert(const uint8_t *gate, const uint8_t *up, const uint8_t *down, int
     orc_quantize_blocks(h32, F, hq, hd);
     if (hq_out) memcpy(hq_out, hq, (size_t)F);
     if (hd_out) memcpy(hd_out, hd, sizeof(uint16_t) * (size_t)nbf);
-    for (int i = 0; i < H; ++i) o[i] = orc_row_dot(down + i * rowf, hq, hd, nbf, NULL);
+    for (int i = 0; i < H; ++i) o[i] = orc_row_dot_fmt(down + i * rowf, hq, hd, nbf, fmt, NULL);
 }
 
 /* Down projection + combine from given quantized h (one entry per
  * assignment a = t*k + j): y[t] = sum_j w[t,j] * (W_down[idx[t,j]] . h_a). */
 void orc_down_combine(int T, int H, int F, int k, const int32_t *idx, const double *w,
-                      const uint8_t *const *down, const int8_t *hq, const uint16_t *hd, double *y) {
+                      const uint8_t *const *down, const int8_t *hq, const uint16_t *hd, double *y, int fmt) {
     int nbf = F / ORC_BLOCK;
-    size_t rowf = (size_t)nbf * ORC_BLOCK_BYTES;
+    size_t rowf = (size_t)nbf * orc_bbytes(fmt);
     for (int t = 0; t < T; ++t) {
         double *yt = y + (size_t)t * H;
         for (int i = 0; i < H; ++i) yt[i] = 0.0;
@@ -231,7 +254,7 @@ void orc_down_combine(int T, int H, int F, int k, const int32_t *idx, const doub
             size_t a = (size_t)t * k + j;
             const uint8_t *dn = down[idx[a]];
             for (int i = 0; i < H; ++i)
-                yt[i] += w[a] * orc_row_dot(dn + i * rowf, hq + a * F, hd + a * nbf, nbf, NULL);
+                yt[i] += w[a] * orc_row_dot_fmt(dn + i * rowf, hq + a * F, hd + a * nbf, nbf, fmt, NULL);
         }
     }
 }
@@ -245,7 +268,7 @@ void orc_down_combine(int T, int H, int F, int k, const int32_t *idx, const doub
 void orc_layer(int T, int H, int F, int k, const float *x, const int32_t *idx, const double *w,
                const uint8_t *const *gate, const uint8_t *const *up, const uint8_t *const *down, double *y,
                int8_t *xq_out, uint16_t *xd_out, double *g_out, double *u_out, double *gabs, double *uabs,
-               double *h_out, int8_t *hq_out, uint16_t *hd_out) {
+               double *h_out, int8_t *hq_out, uint16_t *hd_out, int fmt) {
     int nbh = H / ORC_BLOCK, nbf = F / ORC_BLOCK;
     int8_t xq[H];
     uint16_t xd[H / ORC_BLOCK];
@@ -262,7 +285,7 @@ void orc_layer(int T, int H, int F, int k, const float *x, const int32_t *idx, c
             orc_expert(gate[e], up[e], down[e], H, F, xq, xd, g_out ? g_out + a * F : NULL,
                        u_out ? u_out + a * F : NULL, gabs ? gabs + a * F : NULL, uabs ? uabs + a * F : NULL,
                        h_out ? h_out + a * F : NULL, hq_out ? hq_out + a * F : NULL,
-                       hd_out ? hd_out + a * nbf : NULL, o);
+                       hd_out ? hd_out + a * nbf : NULL, o, fmt);
             for (int i = 0; i < H; ++i) yt[i] += w[a] * o[i];
         }
     }

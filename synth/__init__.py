@@ -31,6 +31,11 @@ STREAM_DRIFT = 5
 
 KIND_GATE, KIND_UP, KIND_DOWN = 0, 1, 2
 Q4_BLOCK_BYTES = 18
+Q8_BLOCK_BYTES = 34
+FMT_Q4, FMT_Q8_0 = 0, 1
+BLOCK_BYTES = {FMT_Q4: Q4_BLOCK_BYTES, FMT_Q8_0: Q8_BLOCK_BYTES}
+# scale ranges: |w| <= 0.16 in both formats (|q - 8| <= 8 for Q4, |q| <= 127 for Q8_0)
+D_RANGE = {FMT_Q4: (0.005, 0.02), FMT_Q8_0: (0.005 / 16, 0.02 / 16)}
 
 
 def build(force: bool = False) -> str:
@@ -59,6 +64,8 @@ def lib():
         L.synth_normal_f32.argtypes = [u64, vp, sz]
         L.synth_q4_blocks.argtypes = [u64, vp, sz, dbl, dbl]
         L.synth_q4_experts.argtypes = [u64, u64, i32, i32, sz, vp, dbl, dbl, i32]
+        L.synth_q8_blocks.argtypes = [u64, vp, sz, dbl, dbl]
+        L.synth_experts.argtypes = [u64, u64, i32, i32, sz, vp, dbl, dbl, i32, i32]
         L.synth_permutation.argtypes = [u64, vp, i32]
         L.synth_gumbel_logits.argtypes = [u64, vp, i32, i32, vp]
         _lib = L
@@ -92,23 +99,34 @@ def q4_blocks(k: int, n_blocks: int, dlo: float = 0.005, dhi: float = 0.02) -> n
     return out
 
 
-def q4_experts(seed: int, tensor_tag: int, e_begin: int, e_end: int, rows: int, cols: int,
-               out: np.ndarray | None = None, dlo: float = 0.005, dhi: float = 0.02,
-               threads: int | None = None) -> np.ndarray:
-    """Canonical Q4 weights of experts [e_begin, e_end) of one expert tensor.
+def q8_blocks(k: int, n_blocks: int, dlo: float = D_RANGE[FMT_Q8_0][0],
+              dhi: float = D_RANGE[FMT_Q8_0][1]) -> np.ndarray:
+    out = np.empty((n_blocks, Q8_BLOCK_BYTES), np.uint8)
+    lib().synth_q8_blocks(k, _ptr(out), n_blocks, dlo, dhi)
+    return out
 
-    Shape [n, rows, cols/32, 18] uint8; expert e's bytes do not depend on the
-    range it was generated in, nor on the thread count.
+
+def q4_experts(seed: int, tensor_tag: int, e_begin: int, e_end: int, rows: int, cols: int,
+               out: np.ndarray | None = None, dlo: float | None = None, dhi: float | None = None,
+               threads: int | None = None, fmt: int = FMT_Q4) -> np.ndarray:
+    """Canonical weights (Q4, or Q8_0 with fmt = 1) of experts
+    [e_begin, e_end) of one expert tensor.
+
+    Shape [n, rows, cols/32, 18 or 34] uint8; expert e's bytes do not depend
+    on the range it was generated in, nor on the thread count.
     """
     assert cols % 32 == 0
+    bb = BLOCK_BYTES[fmt]
+    dlo = D_RANGE[fmt][0] if dlo is None else dlo
+    dhi = D_RANGE[fmt][1] if dhi is None else dhi
     n = e_end - e_begin
     nbe = rows * (cols // 32)
     if out is None:
-        out = np.empty((n, rows, cols // 32, Q4_BLOCK_BYTES), np.uint8)
-    assert out.nbytes == n * nbe * Q4_BLOCK_BYTES and out.flags["C_CONTIGUOUS"]
+        out = np.empty((n, rows, cols // 32, bb), np.uint8)
+    assert out.nbytes == n * nbe * bb and out.flags["C_CONTIGUOUS"]
     if threads is None:
         threads = max(1, min(16, os.cpu_count() or 1))
-    lib().synth_q4_experts(seed, tensor_tag, e_begin, e_end, nbe, _ptr(out), dlo, dhi, threads)
+    lib().synth_experts(seed, tensor_tag, e_begin, e_end, nbe, _ptr(out), dlo, dhi, threads, fmt)
     return out
 
 
@@ -156,6 +174,8 @@ class Workload:
     # request drift: the routed popularity ranks are the seeding table's
     # ranks plus N(0, (drift * E)^2) noise, re-ranked (0 = the table exactly)
     drift: float = 0.0
+    # expert weight format: FMT_Q4 (canonical Q4 blocks) or FMT_Q8_0
+    weight_format: int = FMT_Q4
 
     @property
     def tensor_shapes(self):
@@ -171,7 +191,7 @@ class Workload:
         if e_end is None:
             e_end = self.n_experts
         return q4_experts(self.seed, self.tensor_tag(layer, kind), e_begin, e_end, rows, cols,
-                          out=out, threads=threads)
+                          out=out, threads=threads, fmt=self.weight_format)
 
     def popularity(self) -> np.ndarray | None:
         E = self.n_experts
@@ -222,7 +242,7 @@ class Workload:
 
     def tensor_bytes(self, kind: int) -> int:
         rows, cols = self.tensor_shapes[kind]
-        return rows * (cols // 32) * Q4_BLOCK_BYTES
+        return rows * (cols // 32) * BLOCK_BYTES[self.weight_format]
 
 
 def _c1_capacity(L=48, E=512):

@@ -137,9 +137,35 @@ void synth_q4_blocks(uint64_t key, uint8_t *out, size_t n_blocks, double dlo, do
     }
 }
 
+/*
+ * Canonical Q8_0 blocks of 32 weights, 34 bytes each: a little-endian
+ * binary16 scale d ~ U(dlo, dhi) (rounded to binary16), then 32 signed code
+ * bytes q ~ U{-127..127} in element order.  Each 64-bit draw gives four codes
+ * from its 16-bit quarters c as (c * 255) >> 16, minus 127.
+ */
+void synth_q8_blocks(uint64_t key, uint8_t *out, size_t n_blocks, double dlo, double dhi) {
+    xo_t g;
+    xo_init(&g, key);
+    for (size_t b = 0; b < n_blocks; ++b) {
+        uint8_t *blk = out + b * 34;
+        double d = dlo + (dhi - dlo) * xo_unit(&g);
+        uint16_t h = gen_f16_bits((float)d);
+        blk[0] = (uint8_t)(h & 0xff);
+        blk[1] = (uint8_t)(h >> 8);
+        for (int w = 0; w < 8; ++w) {
+            uint64_t v = xo_next(&g);
+            for (int j = 0; j < 4; ++j) {
+                uint32_t c = (uint32_t)((v >> (16 * j)) & 0xffffu);
+                int q = (int)((c * 255u) >> 16) - 127;
+                blk[2 + 4 * w + j] = (uint8_t)(int8_t)q;
+            }
+        }
+    }
+}
+
 typedef struct {
     uint64_t seed, tag;
-    int e0, e1;
+    int e0, e1, fmt;
     size_t blocks_per_expert;
     uint8_t *out;
     double dlo, dhi;
@@ -147,21 +173,28 @@ typedef struct {
 
 static void *q4_worker(void *arg) {
     q4_job_t *j = (q4_job_t *)arg;
+    const size_t bb = j->fmt == 1 ? 34 : 18;
     for (int e = j->e0; e < j->e1; ++e) {
         uint64_t key = synth_key(j->seed, 1, j->tag, (uint64_t)e, 0);
-        synth_q4_blocks(key, j->out + (size_t)e * j->blocks_per_expert * 18, j->blocks_per_expert, j->dlo, j->dhi);
+        uint8_t *dst = j->out + (size_t)e * j->blocks_per_expert * bb;
+        if (j->fmt == 1)
+            synth_q8_blocks(key, dst, j->blocks_per_expert, j->dlo, j->dhi);
+        else
+            synth_q4_blocks(key, dst, j->blocks_per_expert, j->dlo, j->dhi);
     }
     return NULL;
 }
 
 /*
- * All experts of one expert tensor, expert-major: out[e][block] (18 B each).
+ * All experts of one expert tensor, expert-major: out[e][block] (18 B each
+ * for Q4, fmt 0; 34 B for Q8_0, fmt 1).
  * Expert e is drawn from its own stream keyed by (seed, 1, tensor_tag, e), so
  * the result does not depend on n_threads and any expert can be regenerated
- * alone with synth_q4_experts(seed, tag, e, e+1, ...).
+ * alone with synth_experts(seed, tag, e, e+1, ...).
  */
-void synth_q4_experts(uint64_t seed, uint64_t tensor_tag, int e_begin, int e_end, size_t blocks_per_expert,
-                      uint8_t *out, double dlo, double dhi, int n_threads) {
+void synth_experts(uint64_t seed, uint64_t tensor_tag, int e_begin, int e_end, size_t blocks_per_expert,
+                   uint8_t *out, double dlo, double dhi, int n_threads, int fmt) {
+    const size_t bb = fmt == 1 ? 34 : 18;
     int n = e_end - e_begin;
     if (n <= 0) return;
     if (n_threads < 1) n_threads = 1;
@@ -174,14 +207,20 @@ void synth_q4_experts(uint64_t seed, uint64_t tensor_tag, int e_begin, int e_end
         jobs[t].tag = tensor_tag;
         jobs[t].e0 = e_begin + (int)((long)n * t / n_threads);
         jobs[t].e1 = e_begin + (int)((long)n * (t + 1) / n_threads);
+        jobs[t].fmt = fmt;
         jobs[t].blocks_per_expert = blocks_per_expert;
-        jobs[t].out = out - (size_t)e_begin * blocks_per_expert * 18;
+        jobs[t].out = out - (size_t)e_begin * blocks_per_expert * bb;
         jobs[t].dlo = dlo;
         jobs[t].dhi = dhi;
     }
     for (int t = 1; t < n_threads; ++t) pthread_create(&th[t], NULL, q4_worker, &jobs[t]);
     q4_worker(&jobs[0]);
     for (int t = 1; t < n_threads; ++t) pthread_join(th[t], NULL);
+}
+
+void synth_q4_experts(uint64_t seed, uint64_t tensor_tag, int e_begin, int e_end, size_t blocks_per_expert,
+                      uint8_t *out, double dlo, double dhi, int n_threads) {
+    synth_experts(seed, tensor_tag, e_begin, e_end, blocks_per_expert, out, dlo, dhi, n_threads, 0);
 }
 
 /* Uniform random permutation of 0..n-1 (Fisher-Yates, Lemire-free modulo with

@@ -299,3 +299,90 @@ def test_request_drift_is_a_seeded_jitter_of_the_table():
         top = len(set(p[:128].tolist()) & set(q[:128].tolist()))
         assert 64 < top < 128
         assert np.array_equal(wl.seed_order(layer), p)
+
+
+# ---------------------------------------------------------------- Q8_0 weights
+def _np_dequant_q8(blocks):
+    """Independent Q8_0 decode: numpy's float16 scale and int8 view of the codes."""
+    d = np.ascontiguousarray(blocks[..., :2]).view(np.float16)[..., 0].astype(np.float64)
+    codes = np.ascontiguousarray(blocks[..., 2:]).view(np.int8).astype(np.int64)
+    return codes, d
+
+
+def test_q8_block_dot_golden(golden):
+    for qs_hex, acts, expect in golden("q8_block_dot.txt"):
+        blk = np.zeros(34, np.uint8)
+        blk[2:] = np.frombuffer(bytes.fromhex(qs_hex), np.uint8)
+        a = np.array([int(v) for v in acts.split(",")], np.int8)
+        assert oracle.block_dot(blk, a) == int(expect)
+
+
+def test_q8_block_dot_brute_force_and_extremes():
+    blocks = synth.q8_blocks(synth.key(7, 199), 500)
+    acts = RNG.integers(-127, 128, (500, 32)).astype(np.int8)
+    codes, _ = _np_dequant_q8(blocks)
+    ref = (codes * acts.astype(np.int64)).sum(axis=1)
+    got = np.array([oracle.block_dot(blocks[i], acts[i]) for i in range(500)])
+    assert np.array_equal(got, ref)
+    # every code value, against every activation value, one element at a time
+    for qv in (-128, -127, -1, 0, 1, 126, 127):
+        for av in (-127, -3, 0, 5, 127):
+            blk = np.zeros(34, np.uint8)
+            blk[2 + 13] = np.uint8(qv & 0xFF)
+            a = np.zeros(32, np.int8)
+            a[13] = av
+            assert oracle.block_dot(blk, a) == qv * av
+
+
+def test_q8_dequant_vs_independent():
+    blocks = synth.q8_blocks(synth.key(7, 200), 300).reshape(10, 30, 34)
+    codes, d = _np_dequant_q8(blocks)
+    ref = (d[..., None] * codes).reshape(10, 30 * 32)
+    assert np.array_equal(oracle.dequant(blocks), ref)
+    assert codes.min() >= -127 and codes.max() <= 127 and np.abs(ref).max() <= 127 * 0.02 / 16 * 1.001
+
+
+def test_q8_row_dot_vs_dense_fp64():
+    nb = 64
+    row = synth.q8_blocks(synth.key(7, 201), nb)
+    x = RNG.standard_normal(nb * 32).astype(np.float32)
+    qa, da = oracle.quantize(x)
+    r, abs_sum = oracle.row_dot(row, qa, da)
+    codes, dw = _np_dequant_q8(row)
+    w_ind = (dw[:, None] * codes).reshape(-1)
+    a = qa.astype(np.float64) * np.repeat(da.view(np.float16).astype(np.float64), 32)
+    assert abs(r - float(np.dot(w_ind, a))) <= 4 * nb * 2.0 ** -52 * abs_sum
+
+
+def test_q8_layer_vs_dense_fp64_brute_force():
+    wl = synth.Workload("tiny_q8", 256, 8, 2, 512, 1, routing="normal", weight_format=synth.FMT_Q8_0)
+    H, F, k, T = wl.hidden, wl.ffn, wl.top_k, 4
+    gate, up, down = (wl.expert_tensor(0, kd) for kd in range(3))
+    x, logits = wl.x(0, 0, T), wl.logits(0, 0, T)
+    idx, w = oracle.topk(logits, k)
+    y, it = oracle.layer(x, idx, w, gate, up, down, H, F, want_intermediates=True)
+
+    def deq(t):
+        codes, d = _np_dequant_q8(t)
+        return (d[..., None] * codes).reshape(t.shape[0], t.shape[1], -1)
+
+    Wg, Wu, Wd = deq(gate), deq(up), deq(down)
+    xa = it["xq"].astype(np.float64) * np.repeat(it["xd"].view(np.float16).astype(np.float64), 32, axis=1)
+    y_bf = np.zeros((T, H))
+    for t in range(T):
+        for j in range(k):
+            a, e = t * k + j, idx[t, j]
+            g, u = Wg[e] @ xa[t], Wu[e] @ xa[t]
+            np.testing.assert_allclose(it["g"][a], g, rtol=0, atol=1e-12 * np.abs(g).max())
+            np.testing.assert_allclose(it["u"][a], u, rtol=0, atol=1e-12 * np.abs(u).max())
+            h = g * u * expit(g)
+            hq, hd = oracle.quantize(h.astype(np.float32))
+            assert np.array_equal(hq, it["hq"][a]) and np.array_equal(hd, it["hd"][a])
+            ha = hq.astype(np.float64) * np.repeat(hd.view(np.float16).astype(np.float64), 32)
+            y_bf[t] += w[t, j] * (Wd[e] @ ha)
+    np.testing.assert_allclose(y, y_bf, rtol=1e-12, atol=1e-12 * np.abs(y_bf).max())
+    assert np.array_equal(oracle.down_combine(idx, w, down, it["hq"], it["hd"], H, F), y)
+    # the same weights in Q4 would give another layer: the format is really used
+    q4 = synth.Workload("tiny", 256, 8, 2, 512, 1, routing="normal")
+    y4 = oracle.layer(x, idx, w, *(q4.expert_tensor(0, kd) for kd in range(3)), H, F)
+    assert not np.allclose(y4, y)
