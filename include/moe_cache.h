@@ -69,7 +69,20 @@ typedef struct moe_cfg {
     int32_t renorm_topk;        /* 1: weights = softmax over the k selected */
     int32_t poll_timeout_ms;    /* host poll limit in cache_step (0 = 10 s) */
     int32_t device;             /* CUDA device ordinal */
+    int32_t weight_format;      /* MOE_FMT_Q4_0 (0) or MOE_FMT_Q8_0 (1), for every expert tensor */
 } moe_cfg;
+
+/* Expert weight formats (blocks of 32 weights, one binary16 scale d each).
+ * Q4_0: 18-byte blocks, d then 16 code bytes (byte j = element j in the low
+ *   nibble, element j+16 in the high nibble), w = d * (q - 8).
+ * Q8_0: 34-byte blocks, d then 32 signed code bytes in element order,
+ *   w = d * q (one of the other block formats the dot kernels of
+ *   Zapdev-labs/a6000-custom-kernels accept; the byte layout is the plain
+ *   reading: scale, then codes in element order).
+ * Q8_0 contexts run every forward through the mat-vec kernels (no fused
+ * single-launch layer, no tensor-core prompt path, no lookahead). */
+#define MOE_FMT_Q4_0 0
+#define MOE_FMT_Q8_0 1
 
 typedef struct moe_stats_t {
     uint64_t steps;        /* cache_step calls */
@@ -86,7 +99,7 @@ typedef struct moe_stats_t {
  * Create a context on cfg->device.  cuda_stream (cudaStream_t; NULL is the
  * legacy default stream, as everywhere in CUDA) is the stream every forward
  * of this context runs on; the caller keeps owning it.  The library allocates and owns: the HBM
- * expert pool (3*L*slots_per_tensor slots of rows*cols/32*18 bytes), the
+ * expert pool (3*L*slots_per_tensor slots of rows*cols/32*(18 or 34) bytes), the
  * pointer tables, stamps, miss log, workspaces, an upload stream and the
  * pinned host copies of registered tensors.  *out receives the context.
  * Errors: MOE_ERR_ARG (sizes), MOE_ERR_OOM, MOE_ERR_CUDA.
@@ -95,7 +108,8 @@ int moe_layer_init(const moe_cfg *cfg, void *cuda_stream, moe_ctx **out);
 
 /*
  * Register one expert tensor (layer, kind) and seed its pool.
- * host_q4: canonical Q4 tensor [n_experts][rows][cols/32][18 B], any host
+ * host_q4: canonical tensor [n_experts][rows][cols/32][18 B] (Q4_0) or
+ *   [...][34 B] (Q8_0, per cfg.weight_format), any host
  *   memory; the library copies it into its own pinned, device-mapped host
  *   memory in plane layout (all codes, then all scales) and never reads
  *   host_q4 again, so the caller may free it on return.

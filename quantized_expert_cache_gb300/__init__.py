@@ -23,6 +23,7 @@ MOE_OK = 0
 ERRORS = {-1: "MOE_ERR_ARG", -2: "MOE_ERR_OOM", -3: "MOE_ERR_CUDA", -4: "MOE_ERR_NOT_PINNED",
           -5: "MOE_ERR_TIMEOUT", -6: "MOE_ERR_CAPACITY", -7: "MOE_ERR_STATE", -8: "MOE_ERR_FAULT"}
 KIND_GATE, KIND_UP, KIND_DOWN = 0, 1, 2
+FMT_Q4_0, FMT_Q8_0 = 0, 1
 
 
 class MoeError(RuntimeError):
@@ -34,7 +35,7 @@ class MoeError(RuntimeError):
 class moe_cfg(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "hidden", "ffn", "n_experts", "top_k", "n_layers", "slots_per_tensor", "max_tokens", "window_tokens",
-        "max_swaps_per_step", "renorm_topk", "poll_timeout_ms", "device")]
+        "max_swaps_per_step", "renorm_topk", "poll_timeout_ms", "device", "weight_format")]
 
 
 class moe_stats_t(ctypes.Structure):
@@ -136,9 +137,10 @@ def _check(ctx, rc):
 
 
 def moe_layer_init(hidden, ffn, n_experts, top_k, n_layers, slots_per_tensor, max_tokens, window_tokens=64,
-                   max_swaps_per_step=0, renorm_topk=1, poll_timeout_ms=10000, device=0, stream=None) -> int:
+                   max_swaps_per_step=0, renorm_topk=1, poll_timeout_ms=10000, device=0, stream=None,
+                   weight_format=FMT_Q4_0) -> int:
     cfg = moe_cfg(hidden, ffn, n_experts, top_k, n_layers, slots_per_tensor, max_tokens, window_tokens,
-                  max_swaps_per_step, renorm_topk, poll_timeout_ms, device)
+                  max_swaps_per_step, renorm_topk, poll_timeout_ms, device, weight_format)
     out = ctypes.c_void_p()
     _check(None, load().moe_layer_init(ctypes.byref(cfg), _stream(stream), ctypes.byref(out)))
     return out.value

@@ -22,6 +22,19 @@ constexpr int kMaxChunk = 8;       // tokens per expert handled per weight pass
 __host__ __device__ inline size_t blob_scales_offset(int rows, int nb) { return (size_t)rows * nb * 16; }
 __host__ __device__ inline size_t blob_bytes(int rows, int nb) { return (size_t)rows * nb * kBlockBytes; }
 
+// Weight formats: Q4 (16 code bytes per block, w = d (q - 8)) and Q8_0 (32
+// signed code bytes per block in element order, w = d q).  The blob layout
+// is the same for both: [codes: rows x nb x code bytes][scales: rows x nb x
+// binary16].
+constexpr int kFmtQ4 = 0, kFmtQ8 = 1;
+__host__ __device__ constexpr int code_bytes(int fmt) { return fmt == kFmtQ8 ? 32 : 16; }
+__host__ __device__ inline size_t blob_scales_offset_fmt(int fmt, int rows, int nb) {
+    return (size_t)rows * nb * code_bytes(fmt);
+}
+__host__ __device__ inline size_t blob_bytes_fmt(int fmt, int rows, int nb) {
+    return (size_t)rows * nb * (code_bytes(fmt) + 2);
+}
+
 // Per-activation-block data kept next to the int8 codes: the binary16 scale
 // (held as the exactly equal fp32 value) and the sum of the 32 codes, so that
 // sum_i (q_w,i - 8) q_a,i = sum_i q_w,i q_a,i - 8 * sum_i q_a,i.
@@ -100,6 +113,39 @@ __device__ __forceinline__ int q4_block_dot(const uint4 &w, const int4 &a0, cons
 __device__ __forceinline__ uint4 ld_weights(const uint4 *p) { return __ldcs(p); }
 
 __device__ __forceinline__ float ld_scale(const __half *p) { return __half2float(__ldcs(p)); }
+
+// Codes of one weight block held in registers, per format: load block b of a
+// row's code plane, and its exact int32 dot with 32 int8 activations (two
+// 16-byte halves a0 = elements 0..15, a1 = 16..31; a_sum = their sum).
+template <int FMT>
+struct WCodes;
+template <>
+struct WCodes<kFmtQ4> {
+    uint4 c;
+    __device__ __forceinline__ void load(const uint8_t *row, int b) { c = ld_weights((const uint4 *)row + b); }
+    __device__ __forceinline__ int dot(const int4 &a0, const int4 &a1, int a_sum) const {
+        return q4_block_dot(c, a0, a1, a_sum);
+    }
+};
+template <>
+struct WCodes<kFmtQ8> {
+    uint4 lo, hi;  // elements 0..15, 16..31
+    __device__ __forceinline__ void load(const uint8_t *row, int b) {
+        const uint4 *p = (const uint4 *)row + 2 * (size_t)b;
+        lo = ld_weights(p);
+        hi = ld_weights(p + 1);
+    }
+    __device__ __forceinline__ int dot(const int4 &a0, const int4 &a1, int) const {
+        int s = __dp4a((int)lo.x, a0.x, 0);
+        s = __dp4a((int)lo.y, a0.y, s);
+        s = __dp4a((int)lo.z, a0.z, s);
+        s = __dp4a((int)lo.w, a0.w, s);
+        s = __dp4a((int)hi.x, a1.x, s);
+        s = __dp4a((int)hi.y, a1.y, s);
+        s = __dp4a((int)hi.z, a1.z, s);
+        return __dp4a((int)hi.w, a1.w, s);
+    }
+};
 
 // Cache-state arrays of one forward: pointer tables, local slots, stamps and
 // the miss log (Zapdev-labs/a6000-custom-kernels, pointer-table GEMV).

@@ -39,6 +39,7 @@ struct GemvParams {
     float *y;             // [T][H]
     int8_t *xq_out;       // fused path: [T][H] copy of the quantized x
     BlockScale *xds_out;  // fused path: [T][H/32]
+    int fmt;              // weight format of the mat-vec kernels (kFmtQ4 / kFmtQ8)
 };
 
 // Fused small-batch layer (cooperative launch).
@@ -127,8 +128,8 @@ int launch_quantize(const float *x, int n_blocks, int8_t *q, BlockScale *ds, int
 int launch_plan(const PlanParams &p, cudaStream_t st);
 int launch_gemv(const GemvParams &p, int grid_gu, int grid_dn, cudaStream_t st, cudaEvent_t const *ev = nullptr);
 int down_rows_per_item(int F);
-int launch_block_dots(const uint8_t *blob, int rows, int nb, int row0, int n_rows, const int8_t *qa, int32_t *out,
-                      cudaStream_t st);
+int launch_block_dots(const uint8_t *blob, int fmt, int rows, int nb, int row0, int n_rows, const int8_t *qa,
+                      int32_t *out, cudaStream_t st);
 int launch_stream_read(const void *src, size_t bytes, uint32_t *sink, int n_sm, cudaStream_t st);
 size_t fused_smem_bytes(int H, int F);
 int fused_configure(int F, size_t smem, int *blocks_per_sm);

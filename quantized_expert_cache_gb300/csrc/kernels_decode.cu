@@ -242,6 +242,7 @@ int launch_plan(const PlanParams &p, cudaStream_t st) {
 // quantized by one warp per token.
 constexpr int kGULanes = 8;
 
+template <int FMT>
 __global__ void __launch_bounds__(256) gate_up_kernel(GemvParams p) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int sub = lane % kGULanes, grp = lane / kGULanes;
@@ -251,7 +252,7 @@ __global__ void __launch_bounds__(256) gate_up_kernel(GemvParams p) {
     const int n_uniq = *p.n_uniq;
     const int n_items = n_uniq * rgs;
     const uint32_t step_clock = *p.cv.clock + (uint32_t)p.n_tokens;
-    const size_t scale_off = blob_scales_offset(p.F, nbx);
+    const size_t scale_off = blob_scales_offset_fmt(FMT, p.F, nbx);
     __shared__ float sh_h[kMaxChunk][32];
 
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
@@ -267,8 +268,8 @@ __global__ void __launch_bounds__(256) gate_up_kernel(GemvParams p) {
         const uint8_t *bg = (const uint8_t *)(uintptr_t)(eg & ~1ull);
         const uint8_t *bu = (const uint8_t *)(uintptr_t)(eu & ~1ull);
         const int r = rg * 32 + rloc;
-        const uint4 *qg = (const uint4 *)bg + (size_t)r * nbx;
-        const uint4 *qu = (const uint4 *)bu + (size_t)r * nbx;
+        const uint8_t *qg = bg + (size_t)r * nbx * code_bytes(FMT);
+        const uint8_t *qu = bu + (size_t)r * nbx * code_bytes(FMT);
         const __half *dg = (const __half *)(bg + scale_off) + (size_t)r * nbx;
         const __half *du = (const __half *)(bu + scale_off) + (size_t)r * nbx;
 
@@ -281,14 +282,14 @@ __global__ void __launch_bounds__(256) gate_up_kernel(GemvParams p) {
 #pragma unroll
             for (int t = 0; t < kMaxChunk; ++t) ag[t] = au[t] = 0.0f;
             for (int b0 = sub; b0 < nbx; b0 += 4 * kGULanes) {
-                uint4 wg4[4], wu4[4];
+                WCodes<FMT> wg4[4], wu4[4];
                 float sg[4], su[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     int b = b0 + i * kGULanes;
                     if (b < nbx) {
-                        wg4[i] = ld_weights(qg + b);
-                        wu4[i] = ld_weights(qu + b);
+                        wg4[i].load(qg, b);
+                        wu4[i].load(qu, b);
                         sg[i] = ld_scale(dg + b);
                         su[i] = ld_scale(du + b);
                     }
@@ -303,8 +304,8 @@ __global__ void __launch_bounds__(256) gate_up_kernel(GemvParams p) {
                                 const int4 *xa = (const int4 *)(p.xq + (size_t)tok[t] * p.H + (size_t)b * kBlock);
                                 int4 x0 = __ldg(xa), x1 = __ldg(xa + 1);
                                 BlockScale xs = p.xds[(size_t)tok[t] * nbx + b];
-                                int ig = q4_block_dot(wg4[i], x0, x1, xs.s);
-                                int iu = q4_block_dot(wu4[i], x0, x1, xs.s);
+                                int ig = wg4[i].dot(x0, x1, xs.s);
+                                int iu = wu4[i].dot(x0, x1, xs.s);
                                 ag[t] += (float)ig * (sg[i] * xs.d);
                                 au[t] += (float)iu * (su[i] * xs.d);
                             }
@@ -344,7 +345,7 @@ __global__ void __launch_bounds__(256) gate_up_kernel(GemvParams p) {
 // (blocks of a row: F/32).  Each item writes o[a][rows] for the assignments
 // of u; the last item of a row block to finish (counted with an atomic per
 // row block) sums y[t][rows] = sum_j w[t][j] * o[t*k+j][rows] in j order.
-template <int L>
+template <int L, int FMT>
 __global__ void __launch_bounds__(256) down_kernel(GemvParams p) {
     constexpr int G = 32 / L;          // rows per warp
     constexpr int ROWS = kWarps * G;   // rows per item
@@ -356,7 +357,7 @@ __global__ void __launch_bounds__(256) down_kernel(GemvParams p) {
     const int n_uniq = *p.n_uniq;
     const int n_items = n_uniq * n_rb;
     const uint32_t step_clock = *p.cv.clock + (uint32_t)p.n_tokens;
-    const size_t scale_off = blob_scales_offset(p.H, nbf);
+    const size_t scale_off = blob_scales_offset_fmt(FMT, p.H, nbf);
     __shared__ int sh_last;
 
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
@@ -367,7 +368,7 @@ __global__ void __launch_bounds__(256) down_kernel(GemvParams p) {
         if (rb == 0 && threadIdx.x == 0) record_read(p.cv, p.tid_down, e, ed, step_clock);
         const uint8_t *bd = (const uint8_t *)(uintptr_t)(ed & ~1ull);
         const int r = rb * ROWS + rloc;
-        const uint4 *qd = (const uint4 *)bd + (size_t)r * nbf;
+        const uint8_t *qd = bd + (size_t)r * nbf * code_bytes(FMT);
         const __half *dd = (const __half *)(bd + scale_off) + (size_t)r * nbf;
 
         for (int c0 = a0; c0 < a1; c0 += kMaxChunk) {
@@ -379,13 +380,13 @@ __global__ void __launch_bounds__(256) down_kernel(GemvParams p) {
 #pragma unroll
             for (int t = 0; t < kMaxChunk; ++t) acc[t] = 0.0f;
             for (int b0 = sub; b0 < nbf; b0 += 4 * L) {
-                uint4 w4[4];
+                WCodes<FMT> w4[4];
                 float sw[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     int b = b0 + i * L;
                     if (b < nbf) {
-                        w4[i] = ld_weights(qd + b);
+                        w4[i].load(qd, b);
                         sw[i] = ld_scale(dd + b);
                     }
                 }
@@ -399,7 +400,7 @@ __global__ void __launch_bounds__(256) down_kernel(GemvParams p) {
                                 const int4 *ha = (const int4 *)(p.hq + (size_t)asg[t] * p.F + (size_t)b * kBlock);
                                 int4 h0 = __ldcg(ha), h1 = __ldcg(ha + 1);
                                 BlockScale hs = p.hds[(size_t)asg[t] * nbf + b];
-                                int id = q4_block_dot(w4[i], h0, h1, hs.s);
+                                int id = w4[i].dot(h0, h1, hs.s);
                                 acc[t] += (float)id * (sw[i] * hs.d);
                             }
                         }
@@ -451,15 +452,26 @@ int down_rows_per_item(int F) {
 
 // ev (optional): 4 events recorded around the gate/up and the down launch.
 int launch_gemv(const GemvParams &p, int grid_gu, int grid_dn, cudaStream_t st, cudaEvent_t const *ev) {
+    const bool q8 = p.fmt == kFmtQ8;
     if (ev) record(ev[0], st);
-    gate_up_kernel<<<grid_gu, 256, 0, st>>>(p);
+    if (q8)
+        gate_up_kernel<kFmtQ8><<<grid_gu, 256, 0, st>>>(p);
+    else
+        gate_up_kernel<kFmtQ4><<<grid_gu, 256, 0, st>>>(p);
     if (ev) record(ev[1], st);
     int nbf = p.F / kBlock;
     if (ev) record(ev[2], st);
-    if (nbf <= 40)
-        down_kernel<4><<<grid_dn, 256, 0, st>>>(p);
-    else
-        down_kernel<8><<<grid_dn, 256, 0, st>>>(p);
+    if (nbf <= 40) {
+        if (q8)
+            down_kernel<4, kFmtQ8><<<grid_dn, 256, 0, st>>>(p);
+        else
+            down_kernel<4, kFmtQ4><<<grid_dn, 256, 0, st>>>(p);
+    } else {
+        if (q8)
+            down_kernel<8, kFmtQ8><<<grid_dn, 256, 0, st>>>(p);
+        else
+            down_kernel<8, kFmtQ4><<<grid_dn, 256, 0, st>>>(p);
+    }
     if (ev) record(ev[3], st);
     return (int)cudaGetLastError();
 }
@@ -1633,25 +1645,30 @@ int launch_fused(const FusedParams &p, int grid, size_t smem, cudaStream_t st, c
 // --------------------------------------------------------------- hooks
 // Block dots of rows row0.. of one expert through the pointer table, with
 // the same routine the mat-vec kernels use.  One warp per (row, 32 blocks).
+template <int FMT>
 __global__ void block_dots_kernel(const uint8_t *blob, int rows, int nb, int row0, int n_rows,
                                   const int8_t *__restrict__ qa, int32_t *__restrict__ out) {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n_rows * nb) return;
     const int r = row0 + i / nb, b = i % nb;
-    const uint4 w = ld_weights((const uint4 *)blob + (size_t)r * nb + b);
+    WCodes<FMT> w;
+    w.load(blob + (size_t)r * nb * code_bytes(FMT), b);
     const int4 *xa = (const int4 *)(qa + (size_t)b * kBlock);
     int4 x0 = xa[0], x1 = xa[1];
     int s = 0;
     const int8_t *q8 = qa + (size_t)b * kBlock;
     for (int j = 0; j < kBlock; ++j) s += q8[j];
-    out[i] = q4_block_dot(w, x0, x1, s);
+    out[i] = w.dot(x0, x1, s);
 }
 
-int launch_block_dots(const uint8_t *blob, int rows, int nb, int row0, int n_rows, const int8_t *qa, int32_t *out,
-                      cudaStream_t st) {
+int launch_block_dots(const uint8_t *blob, int fmt, int rows, int nb, int row0, int n_rows, const int8_t *qa,
+                      int32_t *out, cudaStream_t st) {
     int n = n_rows * nb;
     if (n <= 0) return 0;
-    block_dots_kernel<<<(n + 255) / 256, 256, 0, st>>>(blob, rows, nb, row0, n_rows, qa, out);
+    if (fmt == kFmtQ8)
+        block_dots_kernel<kFmtQ8><<<(n + 255) / 256, 256, 0, st>>>(blob, rows, nb, row0, n_rows, qa, out);
+    else
+        block_dots_kernel<kFmtQ4><<<(n + 255) / 256, 256, 0, st>>>(blob, rows, nb, row0, n_rows, qa, out);
     return (int)cudaGetLastError();
 }
 

@@ -46,6 +46,7 @@ struct moe_ctx {
     int dev = 0, n_sm = 0;
     int n_tensors = 0, E = 0, spt = 0, H = 0, F = 0, k = 0, M = 0;
     size_t blob = 0, stride = 0;
+    int fmt = 0;  // moe::kFmtQ4 or moe::kFmtQ8
     cudaStream_t stream = nullptr, up = nullptr;
     cudaEvent_t ev_fwd = nullptr, ev_up = nullptr;
 
@@ -205,18 +206,19 @@ int sync_all(moe_ctx *ctx) {
     return MOE_OK;
 }
 
-// Repack canonical 18-byte blocks of n_experts experts into plane blobs.
-void repack(const uint8_t *src, uint8_t *dst, int n_experts, int rows, int nb, size_t stride) {
-    const size_t nblk = (size_t)rows * nb;
+// Repack canonical blocks (binary16 d, then the code bytes: 18 bytes for
+// Q4, 34 for Q8_0) of n_experts experts into plane blobs.
+void repack(const uint8_t *src, uint8_t *dst, int fmt, int n_experts, int rows, int nb, size_t stride) {
+    const size_t nblk = (size_t)rows * nb, cb = (size_t)moe::code_bytes(fmt), bb = cb + 2;
     auto work = [&](int e0, int e1) {
         for (int e = e0; e < e1; ++e) {
-            const uint8_t *s = src + (size_t)e * nblk * 18;
+            const uint8_t *s = src + (size_t)e * nblk * bb;
             uint8_t *q = dst + (size_t)e * stride;
-            uint8_t *d = q + nblk * 16;
+            uint8_t *d = q + nblk * cb;
             for (size_t b = 0; b < nblk; ++b) {
-                d[2 * b] = s[18 * b];
-                d[2 * b + 1] = s[18 * b + 1];
-                memcpy(q + 16 * b, s + 18 * b + 2, 16);
+                d[2 * b] = s[bb * b];
+                d[2 * b + 1] = s[bb * b + 1];
+                memcpy(q + cb * b, s + bb * b + 2, cb);
             }
         }
     };
@@ -403,9 +405,10 @@ int moe_layer_init(const moe_cfg *cfg, void *cuda_stream, moe_ctx **out) {
     if (c.hidden <= 0 || c.hidden % 32 || c.ffn <= 0 || c.ffn % 32 || c.n_experts < 1 || c.n_experts > 4096 ||
         c.top_k < 1 || c.top_k > 32 || c.top_k > c.n_experts || c.n_layers < 1 || c.n_layers * 3 > (1 << 20) ||
         c.slots_per_tensor < 0 || c.slots_per_tensor > c.n_experts || c.max_tokens < 1 || c.window_tokens < 1 ||
-        c.max_swaps_per_step < 0)
+        c.max_swaps_per_step < 0 || (c.weight_format != MOE_FMT_Q4_0 && c.weight_format != MOE_FMT_Q8_0))
         return fail(nullptr, MOE_ERR_ARG,
-                    "bad cfg: hidden%32, ffn%32, 1<=E<=4096, 1<=k<=min(32,E), layers>=1, 0<=slots<=E, max_tokens>=1");
+                    "bad cfg: hidden%32, ffn%32, 1<=E<=4096, 1<=k<=min(32,E), layers>=1, 0<=slots<=E, max_tokens>=1, "
+                    "weight_format Q4_0 or Q8_0");
     int down_rows = moe::down_rows_per_item(c.ffn);
     if (c.hidden % down_rows) return fail(nullptr, MOE_ERR_ARG, "hidden must be a multiple of the down row block");
     ctx = new moe_ctx();
@@ -418,7 +421,8 @@ int moe_layer_init(const moe_cfg *cfg, void *cuda_stream, moe_ctx **out) {
     ctx->M = c.max_tokens;
     ctx->n_tensors = 3 * c.n_layers;
     ctx->spt = c.slots_per_tensor;
-    ctx->blob = moe::blob_bytes(c.ffn, c.hidden / 32);
+    ctx->fmt = c.weight_format == MOE_FMT_Q8_0 ? moe::kFmtQ8 : moe::kFmtQ4;
+    ctx->blob = moe::blob_bytes_fmt(ctx->fmt, c.ffn, c.hidden / 32);
     ctx->stride = (ctx->blob + 255) / 256 * 256;
     auto cleanup_fail = [&](int rc) {
         std::string m = ctx->err;
@@ -480,7 +484,8 @@ int moe_layer_init(const moe_cfg *cfg, void *cuda_stream, moe_ctx **out) {
     CKI(cudaMemset(ctx->counters, 0, sizeof(unsigned) * ctx->n_counters));
 
     // prefill workspaces: sorted fp16 operands of the grouped GEMM
-    if (ctx->M > 32 && ctx->H % 64 == 0 && ctx->F % 64 == 0) {
+    // (Q4 only: the GEMM's converters expand 4-bit codes)
+    if (ctx->M > 32 && ctx->H % 64 == 0 && ctx->F % 64 == 0 && ctx->fmt == moe::kFmtQ4) {
         ctx->A_pad = (int)((A + 127) / 128 * 128 + 128);
         const size_t AP = ctx->A_pad;
         CKI(cudaMalloc(&ctx->xs16, sizeof(__half) * AP * ctx->H));
@@ -527,6 +532,12 @@ int moe_layer_init(const moe_cfg *cfg, void *cuda_stream, moe_ctx **out) {
         if (ctx->fused_smem_rb > 0) {
             CKI((cudaError_t)moe::fused_configure_rb(ctx->F, ctx->fused_smem_rb, &bps));
             ctx->fused_blocks_rb = bps * ctx->n_sm;
+        }
+        if (ctx->fmt != moe::kFmtQ4) {
+            // the single-launch layer reads 4-bit codes: other formats take
+            // the mat-vec kernels
+            ctx->fused_blocks = 0;
+            ctx->fused_blocks_rb = 0;
         }
     }
 
@@ -580,7 +591,7 @@ int register_expert_tensor(moe_ctx *ctx, int layer, int kind, const void *host_q
     }
     ts.home = (uint8_t *)home;
     ts.home_dev = (uint64_t)(uintptr_t)home_dev;
-    repack((const uint8_t *)host_q4, ts.home, E, rows, cols / 32, ctx->stride);
+    repack((const uint8_t *)host_q4, ts.home, ctx->fmt, E, rows, cols / 32, ctx->stride);
     ts.capacity = capacity;
     ts.n_seed = n_seed;
     ts.seed_order = order;
@@ -722,6 +733,7 @@ static int ffn_forward_body(moe_ctx *ctx, int layer, const float *d_x, int n_tok
     const int A = T * ctx->k, U = std::min(A, ctx->E);
     gp.xq_out = ctx->xq;
     gp.xds_out = ctx->xds;
+    gp.fmt = ctx->fmt;
     if (small && A <= 256 && ctx->fused_blocks > 0) {
         moe::FusedParams fp{};
         fp.g = gp;
@@ -1490,7 +1502,7 @@ int moe_debug_block_dots(moe_ctx *ctx, int tensor_id, int expert, int row0, int 
     int rc = sync_all(ctx);
     if (rc) return rc;
     const uint8_t *blob = (const uint8_t *)(uintptr_t)(ctx->t[tensor_id].tbl[expert] & ~1ull);
-    rc = moe::launch_block_dots(blob, rows, cols / 32, row0, n_rows, d_qa, d_out, ctx->stream);
+    rc = moe::launch_block_dots(blob, ctx->fmt, rows, cols / 32, row0, n_rows, d_qa, d_out, ctx->stream);
     if (rc) return fail(ctx, MOE_ERR_CUDA, "block_dots launch failed");
     CK(cudaStreamSynchronize(ctx->stream));
     return MOE_OK;

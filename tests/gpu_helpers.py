@@ -82,18 +82,20 @@ class Model:
     """A small stack of expert tensors registered in one context."""
 
     def __init__(self, H, F, E, k, L, capacity, max_tokens, seed=0, routing="zipf", zipf_s=1.1, window=64,
-                 slots_per_tensor=None, max_swaps=0, stream=None, global_pool=False, preheat=False):
+                 slots_per_tensor=None, max_swaps=0, stream=None, global_pool=False, preheat=False,
+                 weight_format=0):
         import torch
         self.torch = torch
         self.wl = synth.Workload("test", H, E, k, F, L, routing=routing, zipf_s=zipf_s, seed=seed,
-                                 capacity=[capacity] * L if isinstance(capacity, int) else list(capacity))
+                                 capacity=[capacity] * L if isinstance(capacity, int) else list(capacity),
+                                 weight_format=weight_format)
         self.H, self.F, self.E, self.k, self.L = H, F, E, k, L
         self.spt = slots_per_tensor if slots_per_tensor is not None else max(self.wl.capacity)
         # one stream for torch's copies / allocations and the library's kernels
         if stream is None:
             stream = torch.cuda.current_stream().cuda_stream
         self.ctx = qec.moe_layer_init(H, F, E, k, L, self.spt, max_tokens, window_tokens=window,
-                                      max_swaps_per_step=max_swaps, stream=stream)
+                                      max_swaps_per_step=max_swaps, stream=stream, weight_format=weight_format)
         self.tensors = {}
         self.global_pool = global_pool
         if global_pool:
@@ -226,6 +228,7 @@ class FullModel(Model):
         self.wl = wl
         self.H, self.F, self.E, self.k, self.L = wl.hidden, wl.ffn, wl.n_experts, wl.top_k, wl.n_layers
         self.spt = slots_per_tensor or max(wl.layer_capacity(l) for l in range(wl.n_layers))
+        self.global_pool = False
         if stream is None:
             stream = torch.cuda.current_stream().cuda_stream
         self.ctx = qec.moe_layer_init(self.H, self.F, self.E, self.k, self.L, self.spt, max_tokens,
