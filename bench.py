@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--cpu-sample-steps", type=int, default=6)
     ap.add_argument("--prefill-steps", type=int, default=2)
     ap.add_argument("--prefill-workload", default="prefill_t4096")
+    ap.add_argument("--q8-steps", type=int, default=64,
+                    help="timed decode steps of the Q8_0 weight-format leg (0 skips it)")
     ap.add_argument("--pool-steps", type=int, default=256,
                     help="decode tokens per run of the pool-mode / preheat leg (0 skips it)")
     ap.add_argument("--case", default=None, choices=["decode_layer", "prefill_layer"],
@@ -168,7 +170,8 @@ def register_workload(qec, synth, ctx, wl, log):
             rows, cols = wl.tensor_shapes[kind]
             key = (rows, cols)
             if key not in bufs:
-                bufs[key] = np.empty((wl.n_experts, rows, cols // 32, 18), np.uint8)
+                bufs[key] = np.empty((wl.n_experts, rows, cols // 32, synth.BLOCK_BYTES[wl.weight_format]),
+                                     np.uint8)
             wl.expert_tensor(layer, kind, out=bufs[key])
             qec.register_expert_tensor(ctx, layer, kind, bufs[key], rows, cols, cap, order, cap)
     log(f"registered {3 * wl.n_layers} expert tensors in {time.time() - t0:.1f}s")
@@ -406,6 +409,8 @@ def run_ours(args):
         out["prefill"] = run_prefill_leg(args, qec, synth, torch, log)
     if args.pool_steps > 0:
         out["pool"] = run_pool_leg(args, qec, synth, torch, log)
+    if args.q8_steps > 0:
+        out["q8_0"] = run_q8_leg(args, qec, synth, torch, log)
     if rank == 0:
         out["cpu_baseline"] = cpu_baseline(wl, args.cpu_sample_steps, T) if args.cpu_sample_steps > 0 else None
         print(json.dumps(out), flush=True)
@@ -540,6 +545,74 @@ def run_pool_leg(args, qec, synth, torch, log):
                           f"drift from the seeding table (rank noise {wp.drift} x E)")
     out["prompt_then_decode"] = prompt
     return out
+
+
+def run_q8_leg(args, qec, synth, torch, log):
+    """Q8_0 expert weights (32 signed 8-bit codes per block) on 16 fully
+    resident layers of the decode shape: batch-1 decode steps captured in a
+    CUDA graph (router top-k, plan, gate/up and down mat-vec launches per
+    layer), timed with CUDA events on the context stream; roofline = the
+    weights of the experts each step uses (3 tensors of 34-byte blocks) + x
+    and y, over the step time."""
+    wl = synth.WORKLOADS["decode_b1_q8_resident16"]
+    L, H, E, k, F = wl.n_layers, wl.hidden, wl.n_experts, wl.top_k, wl.ffn
+    T = 1
+    stream = torch.cuda.Stream()
+    sp = stream.cuda_stream
+    ctx = qec.moe_layer_init(H, F, E, k, L, E, T, stream=sp, weight_format=qec.FMT_Q8_0)
+    register_workload(qec, synth, ctx, wl, log)
+    n = args.q8_steps
+    W = args.warmup
+    Xh, LGh = make_inputs(wl, W + n, T)
+    X, LG = torch.from_numpy(Xh).cuda(), torch.from_numpy(LGh).cuda()
+    xin = torch.empty((L, T, H), device="cuda")
+    lin = torch.empty((L, T, E), device="cuda")
+    idx = torch.empty((L, T, k), dtype=torch.int32, device="cuda")
+    w = torch.empty((L, T, k), device="cuda")
+    y = torch.empty((L, T, H), device="cuda")
+
+    def layers():
+        for l in range(L):
+            qec.moe_ffn_forward_routed(ctx, l, xin[l], lin[l], T, idx[l], w[l], y[l], sp)
+
+    with torch.cuda.stream(stream):
+        xin.copy_(X[0])
+        lin.copy_(LG[0])
+    layers()
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        layers()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for s in range(W + n):
+        if s == W:
+            stream.synchronize()
+            e0.record(stream)
+        with torch.cuda.stream(stream):
+            xin.copy_(X[s])
+            lin.copy_(LG[s])
+            graph.replay()
+    e1.record(stream)
+    stream.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    blob = wl.tensor_bytes(0)
+    alg = 0
+    for s in range(W, W + n):
+        for l in range(L):
+            alg += len(np.unique(LGh[s, l].argsort(axis=1)[:, -k:])) * 3 * blob + 2 * T * H * 4
+    alg /= n
+    peaks, src = load_peaks()
+    gbs = alg / (ms * 1e-3) / 1e9
+    qec.moe_destroy(ctx)
+    log(f"Q8_0 leg: {T / (ms * 1e-3):.1f} tokens/s through {L} resident layers, {ms * 1e3 / L:.2f} us per layer, "
+        f"{gbs:.0f} GB/s")
+    return {"workload": f"{wl.name}: {L} layers, hidden {H}, {E} experts, top-{k}, FFN {F}, Q8_0 blocks of 32 "
+                        f"(34 B), every expert resident, batch-1 decode, {n} timed steps in a CUDA graph",
+            "tokens_per_s": round(T / (ms * 1e-3), 1), "us_per_layer": round(ms * 1e3 / L, 3),
+            "roofline": {"bound": "hbm", "kernels": "topk + plan + gate_up_kernel<Q8_0> + down_kernel<Q8_0> per layer",
+                         "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(gbs / peaks["hbm_gbs"], 4), "peak_source": f"{src} hbm_gbs (copy)",
+                         "algorithmic_bytes_per_step": int(alg), "traffic": None}}
 
 
 def run_prefill_leg(args, qec, synth, torch, log):

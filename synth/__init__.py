@@ -263,6 +263,10 @@ WORKLOADS = {
     "prompt_then_decode_pool25": Workload("prompt_then_decode_pool25", 2048, 512, 8, 1152, 48, routing="zipf",
                                           zipf_s=1.1, capacity=[128] * 48, drift=0.15,
                                           phases=[("prefill", 4096, 1), ("decode", 1, 256)]),
+    # Q8_0 expert weights: 16 layers of the decode shape, every expert resident
+    "decode_b1_q8_resident16": Workload("decode_b1_q8_resident16", 2048, 512, 8, 1152, 16, routing="zipf",
+                                        zipf_s=1.1, capacity=[512] * 16, phases=[("decode", 1, 64)],
+                                        weight_format=FMT_Q8_0),
     "prefill_t4096": Workload("prefill_t4096", 2048, 512, 8, 1152, 48, routing="zipf", zipf_s=1.1,
                               capacity=[384] * 48, phases=[("prefill", 4096, 1)]),
     "large_expert": Workload("large_expert", 2880, 128, 4, 2880, 36, routing="mix", zipf_s=0.8,
