@@ -103,7 +103,7 @@ struct moe_ctx {
     std::vector<TensorState> t;
     uint64_t clock = 0;
     int n_lent = 0;
-    // one pool of expert blocks shared by all layers (instead of a reserve
+    // a single pool that every layer draws on (instead of a reserve
     // per tensor): owner and membership of every arena slot
     bool global_pool = false;
     std::vector<int32_t> g_owner;  // (tid << 12 | e) or -1
