@@ -5,7 +5,7 @@ with a quantized expert cache, used to check the CUDA path.  Only the tests,
 ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline leg may import
 it.  It shares no code with the CUDA library, and the library never calls it.
 
-- ``moe_oracle.c``: numerics (top-k, activation quantization, Q4 and Q8_0 block dots,
+- ``moe_oracle.c``: numerics (top-k, activation quantization, Q4, Q8_0 and Q5_0 block dots,
   SwiGLU, down projection and combine), binary64 with the integer-deciding
   steps in binary32 (see the header of that file);
 - ``policy.py``: the admission / eviction policy of the expert pools.
@@ -101,18 +101,18 @@ def quantize(x: np.ndarray):
     return q, d
 
 
-BLOCK_BYTES = {18: 0, 34: 1}  # canonical block size -> format (0: Q4, 1: Q8_0)
+BLOCK_BYTES = {18: 0, 34: 1, 22: 2}  # canonical block size -> format (0: Q4, 1: Q8_0, 2: Q5_0)
 
 
 def _fmt(blocks) -> int:
-    """Format of canonical blocks from their last dimension (18: Q4, 34: Q8_0)."""
+    """Format of canonical blocks from their last dimension (18: Q4, 34: Q8_0, 22: Q5_0)."""
     if blocks.shape[-1] not in BLOCK_BYTES:
         raise ValueError(f"unknown block size {blocks.shape[-1]}")
     return BLOCK_BYTES[blocks.shape[-1]]
 
 
 def dequant(blocks: np.ndarray) -> np.ndarray:
-    """Canonical blocks [..., nb, 18 (Q4) or 34 (Q8_0)] -> float64 [..., nb*32]."""
+    """Canonical blocks [..., nb, 18 (Q4), 34 (Q8_0) or 22 (Q5_0)] -> float64 [..., nb*32]."""
     blocks = np.ascontiguousarray(blocks, np.uint8)
     nb = blocks.size // blocks.shape[-1]
     out = np.empty(blocks.shape[:-2] + (blocks.shape[-2] * 32,), np.float64)
@@ -137,7 +137,7 @@ def row_dot(row: np.ndarray, qa: np.ndarray, da: np.ndarray):
 
 def _expert_ptrs(tensor):
     """Expert tensor given as an array [E, rows, nb, B] or a dict {e: [rows, nb, B]}
-    (B = 18: Q4, 34: Q8_0).  Returns (pointers, kept arrays, format)."""
+    (B = 18: Q4, 34: Q8_0, 22: Q5_0).  Returns (pointers, kept arrays, format)."""
     if isinstance(tensor, dict):
         E = max(tensor) + 1
         arrs = {e: np.ascontiguousarray(v, np.uint8) for e, v in tensor.items()}

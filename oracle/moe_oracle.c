@@ -24,7 +24,11 @@
  *  Zapdev-labs/a6000-custom-kernels dot kernels accept: blocks of 32 with one
  *  binary16 scale d and 32 signed 8-bit codes q, w = d * q; the pages give no
  *  byte layout, the reading is d (little endian) followed by code bytes 0..31
- *  in element order (34 bytes).
+ *  in element order (34 bytes).  2 = Q5_0, another of those formats: blocks
+ *  of 32 with one binary16 scale d and 5-bit codes q, w = d * (q - 16); the
+ *  reading of the layout is d, then 4 bytes of high bits (bit j of the
+ *  little-endian word = bit 4 of element j), then 16 bytes of low nibbles in
+ *  the Q4 order (22 bytes).
  *
  * Readings where the pages are silent (each listed in the design notes):
  *  - top-k order is (logit descending, expert index ascending): ties go to
@@ -51,8 +55,11 @@
 #define ORC_BLOCK 32
 #define ORC_BLOCK_BYTES 18
 #define ORC_Q8_BLOCK_BYTES 34
+#define ORC_Q5_BLOCK_BYTES 22
 
-static size_t orc_bbytes(int fmt) { return fmt == 1 ? ORC_Q8_BLOCK_BYTES : ORC_BLOCK_BYTES; }
+static size_t orc_bbytes(int fmt) {
+    return fmt == 1 ? ORC_Q8_BLOCK_BYTES : fmt == 2 ? ORC_Q5_BLOCK_BYTES : ORC_BLOCK_BYTES;
+}
 
 /* ---- binary16 <-> binary64/32 from the IEEE 754 definition ------------- */
 
@@ -161,14 +168,28 @@ static int orc_code(const uint8_t *blk, int i) {
     return i < 16 ? (qs[i] & 15) : (qs[i - 16] >> 4);
 }
 
-/* Signed weight code of element i: q - 8 (Q4) or q (Q8_0), so w = d * code. */
+/* 5-bit code of element i of a canonical 22-byte Q5_0 block: low nibble
+ * from the 16 code bytes (Q4 order, after the 4 high-bit bytes), bit 4 from
+ * bit i of the high-bit word. */
+static int orc_code5(const uint8_t *blk, int i) {
+    const uint8_t *qh = blk + 2, *qs = blk + 6;
+    const int lo = i < 16 ? (qs[i] & 15) : (qs[i - 16] >> 4);
+    const int hi = (qh[i / 8] >> (i % 8)) & 1;
+    return lo | (hi << 4);
+}
+
+/* Signed weight code of element i: q - 8 (Q4), q (Q8_0) or q - 16 (Q5_0),
+ * so w = d * code. */
 static int orc_wcode(const uint8_t *blk, int i, int fmt) {
-    return fmt == 1 ? (int)(int8_t)blk[2 + i] : orc_code(blk, i) - 8;
+    if (fmt == 1) return (int)(int8_t)blk[2 + i];
+    if (fmt == 2) return orc_code5(blk, i) - 16;
+    return orc_code(blk, i) - 8;
 }
 
 static uint16_t orc_block_scale(const uint8_t *blk) { return (uint16_t)(blk[0] | (blk[1] << 8)); }
 
-/* Dequantized weights of nb blocks: w = d * (q - 8) (Q4) or d * q (Q8_0). */
+/* Dequantized weights of nb blocks: w = d * (q - 8) (Q4), d * q (Q8_0) or
+ * d * (q - 16) (Q5_0). */
 void orc_dequant_fmt(const uint8_t *blocks, int nb, int fmt, double *out) {
     for (int b = 0; b < nb; ++b) {
         const uint8_t *blk = blocks + (size_t)b * orc_bbytes(fmt);
@@ -180,7 +201,8 @@ void orc_dequant_fmt(const uint8_t *blocks, int nb, int fmt, double *out) {
 void orc_dequant(const uint8_t *blocks, int nb, double *out) { orc_dequant_fmt(blocks, nb, 0, out); }
 
 /* [A2] integer block dot: sum_i code_w,i * q_a,i, exact in int32
- * (|sum| <= 32 * 8 * 127 for Q4, 32 * 128 * 127 for Q8_0). */
+ * (|sum| <= 32 * 8 * 127 for Q4, 32 * 16 * 127 for Q5_0, 32 * 128 * 127 for
+ * Q8_0). */
 int32_t orc_block_dot_fmt(const uint8_t *blk, const int8_t *qa, int fmt) {
     int32_t s = 0;
     for (int i = 0; i < ORC_BLOCK; ++i) s += (int32_t)orc_wcode(blk, i, fmt) * (int32_t)qa[i];

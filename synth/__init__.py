@@ -32,10 +32,12 @@ STREAM_DRIFT = 5
 KIND_GATE, KIND_UP, KIND_DOWN = 0, 1, 2
 Q4_BLOCK_BYTES = 18
 Q8_BLOCK_BYTES = 34
-FMT_Q4, FMT_Q8_0 = 0, 1
-BLOCK_BYTES = {FMT_Q4: Q4_BLOCK_BYTES, FMT_Q8_0: Q8_BLOCK_BYTES}
-# scale ranges: |w| <= 0.16 in both formats (|q - 8| <= 8 for Q4, |q| <= 127 for Q8_0)
-D_RANGE = {FMT_Q4: (0.005, 0.02), FMT_Q8_0: (0.005 / 16, 0.02 / 16)}
+Q5_BLOCK_BYTES = 22
+FMT_Q4, FMT_Q8_0, FMT_Q5_0 = 0, 1, 2
+BLOCK_BYTES = {FMT_Q4: Q4_BLOCK_BYTES, FMT_Q8_0: Q8_BLOCK_BYTES, FMT_Q5_0: Q5_BLOCK_BYTES}
+# scale ranges: |w| <= 0.16 in every format (|q - 8| <= 8 for Q4, |q| <= 127
+# for Q8_0, |q - 16| <= 16 for Q5_0)
+D_RANGE = {FMT_Q4: (0.005, 0.02), FMT_Q8_0: (0.005 / 16, 0.02 / 16), FMT_Q5_0: (0.0025, 0.01)}
 
 
 def build(force: bool = False) -> str:
@@ -65,6 +67,7 @@ def lib():
         L.synth_q4_blocks.argtypes = [u64, vp, sz, dbl, dbl]
         L.synth_q4_experts.argtypes = [u64, u64, i32, i32, sz, vp, dbl, dbl, i32]
         L.synth_q8_blocks.argtypes = [u64, vp, sz, dbl, dbl]
+        L.synth_q5_blocks.argtypes = [u64, vp, sz, dbl, dbl]
         L.synth_experts.argtypes = [u64, u64, i32, i32, sz, vp, dbl, dbl, i32, i32]
         L.synth_permutation.argtypes = [u64, vp, i32]
         L.synth_gumbel_logits.argtypes = [u64, vp, i32, i32, vp]
@@ -106,13 +109,20 @@ def q8_blocks(k: int, n_blocks: int, dlo: float = D_RANGE[FMT_Q8_0][0],
     return out
 
 
+def q5_blocks(k: int, n_blocks: int, dlo: float = D_RANGE[FMT_Q5_0][0],
+              dhi: float = D_RANGE[FMT_Q5_0][1]) -> np.ndarray:
+    out = np.empty((n_blocks, Q5_BLOCK_BYTES), np.uint8)
+    lib().synth_q5_blocks(k, _ptr(out), n_blocks, dlo, dhi)
+    return out
+
+
 def q4_experts(seed: int, tensor_tag: int, e_begin: int, e_end: int, rows: int, cols: int,
                out: np.ndarray | None = None, dlo: float | None = None, dhi: float | None = None,
                threads: int | None = None, fmt: int = FMT_Q4) -> np.ndarray:
-    """Canonical weights (Q4, or Q8_0 with fmt = 1) of experts
+    """Canonical weights (Q4, Q8_0 with fmt = 1, Q5_0 with fmt = 2) of experts
     [e_begin, e_end) of one expert tensor.
 
-    Shape [n, rows, cols/32, 18 or 34] uint8; expert e's bytes do not depend
+    Shape [n, rows, cols/32, 18, 34 or 22] uint8; expert e's bytes do not depend
     on the range it was generated in, nor on the thread count.
     """
     assert cols % 32 == 0
@@ -174,7 +184,7 @@ class Workload:
     # request drift: the routed popularity ranks are the seeding table's
     # ranks plus N(0, (drift * E)^2) noise, re-ranked (0 = the table exactly)
     drift: float = 0.0
-    # expert weight format: FMT_Q4 (canonical Q4 blocks) or FMT_Q8_0
+    # expert weight format: FMT_Q4 (canonical Q4 blocks), FMT_Q8_0 or FMT_Q5_0
     weight_format: int = FMT_Q4
 
     @property

@@ -163,6 +163,29 @@ void synth_q8_blocks(uint64_t key, uint8_t *out, size_t n_blocks, double dlo, do
     }
 }
 
+/*
+ * Canonical Q5_0 blocks of 32 weights, 22 bytes each: a little-endian
+ * binary16 scale d ~ U(dlo, dhi) (rounded to binary16), then 4 bytes of high
+ * bits and 16 bytes of low nibbles (codes q ~ U{0..31}: every bit uniform).
+ */
+void synth_q5_blocks(uint64_t key, uint8_t *out, size_t n_blocks, double dlo, double dhi) {
+    xo_t g;
+    xo_init(&g, key);
+    for (size_t b = 0; b < n_blocks; ++b) {
+        uint8_t *blk = out + b * 22;
+        double d = dlo + (dhi - dlo) * xo_unit(&g);
+        uint16_t h = gen_f16_bits((float)d);
+        blk[0] = (uint8_t)(h & 0xff);
+        blk[1] = (uint8_t)(h >> 8);
+        uint64_t w0 = xo_next(&g), w1 = xo_next(&g), w2 = xo_next(&g);
+        for (int j = 0; j < 4; ++j) blk[2 + j] = (uint8_t)(w2 >> (8 * j));
+        for (int j = 0; j < 8; ++j) {
+            blk[6 + j] = (uint8_t)(w0 >> (8 * j));
+            blk[14 + j] = (uint8_t)(w1 >> (8 * j));
+        }
+    }
+}
+
 typedef struct {
     uint64_t seed, tag;
     int e0, e1, fmt;
@@ -173,12 +196,14 @@ typedef struct {
 
 static void *q4_worker(void *arg) {
     q4_job_t *j = (q4_job_t *)arg;
-    const size_t bb = j->fmt == 1 ? 34 : 18;
+    const size_t bb = j->fmt == 1 ? 34 : j->fmt == 2 ? 22 : 18;
     for (int e = j->e0; e < j->e1; ++e) {
         uint64_t key = synth_key(j->seed, 1, j->tag, (uint64_t)e, 0);
         uint8_t *dst = j->out + (size_t)e * j->blocks_per_expert * bb;
         if (j->fmt == 1)
             synth_q8_blocks(key, dst, j->blocks_per_expert, j->dlo, j->dhi);
+        else if (j->fmt == 2)
+            synth_q5_blocks(key, dst, j->blocks_per_expert, j->dlo, j->dhi);
         else
             synth_q4_blocks(key, dst, j->blocks_per_expert, j->dlo, j->dhi);
     }
@@ -187,14 +212,14 @@ static void *q4_worker(void *arg) {
 
 /*
  * All experts of one expert tensor, expert-major: out[e][block] (18 B each
- * for Q4, fmt 0; 34 B for Q8_0, fmt 1).
+ * for Q4, fmt 0; 34 B for Q8_0, fmt 1; 22 B for Q5_0, fmt 2).
  * Expert e is drawn from its own stream keyed by (seed, 1, tensor_tag, e), so
  * the result does not depend on n_threads and any expert can be regenerated
  * alone with synth_experts(seed, tag, e, e+1, ...).
  */
 void synth_experts(uint64_t seed, uint64_t tensor_tag, int e_begin, int e_end, size_t blocks_per_expert,
                    uint8_t *out, double dlo, double dhi, int n_threads, int fmt) {
-    const size_t bb = fmt == 1 ? 34 : 18;
+    const size_t bb = fmt == 1 ? 34 : fmt == 2 ? 22 : 18;
     int n = e_end - e_begin;
     if (n <= 0) return;
     if (n_threads < 1) n_threads = 1;

@@ -386,3 +386,75 @@ def test_q8_layer_vs_dense_fp64_brute_force():
     q4 = synth.Workload("tiny", 256, 8, 2, 512, 1, routing="normal")
     y4 = oracle.layer(x, idx, w, *(q4.expert_tensor(0, kd) for kd in range(3)), H, F)
     assert not np.allclose(y4, y)
+
+
+# ---------------------------------------------------------------- Q5_0 weights
+def _np_dequant_q5(blocks):
+    """Independent Q5_0 decode with numpy: float16 scale, 32-bit high-bit word,
+    nibble planes unpacked with shifts."""
+    d = np.ascontiguousarray(blocks[..., :2]).view(np.float16)[..., 0].astype(np.float64)
+    qh = np.ascontiguousarray(blocks[..., 2:6]).view(np.uint32)[..., 0].astype(np.int64)
+    qs = blocks[..., 6:22].astype(np.int64)
+    lo = np.concatenate([qs & 15, qs >> 4], axis=-1)
+    hi = (qh[..., None] >> np.arange(32)) & 1
+    return lo + 16 * hi - 16, d
+
+
+def test_q5_block_dot_golden(golden):
+    for qh_hex, qs_hex, acts, expect in golden("q5_block_dot.txt"):
+        blk = np.zeros(22, np.uint8)
+        blk[2:6] = np.frombuffer(bytes.fromhex(qh_hex), np.uint8)
+        blk[6:] = np.frombuffer(bytes.fromhex(qs_hex), np.uint8)
+        a = np.array([int(v) for v in acts.split(",")], np.int8)
+        assert oracle.block_dot(blk, a) == int(expect)
+
+
+def test_q5_block_dot_brute_force_every_code():
+    blocks = synth.q5_blocks(synth.key(7, 299), 500)
+    acts = RNG.integers(-127, 128, (500, 32)).astype(np.int8)
+    codes, _ = _np_dequant_q5(blocks)
+    assert codes.min() == -16 and codes.max() == 15
+    ref = (codes * acts.astype(np.int64)).sum(axis=1)
+    got = np.array([oracle.block_dot(blocks[i], acts[i]) for i in range(500)])
+    assert np.array_equal(got, ref)
+    # each of the 32 codes at each element position picks out that element
+    for q in range(32):
+        for i in (0, 7, 15, 16, 30, 31):
+            blk = np.zeros(22, np.uint8)
+            blk[2 + i // 8] = ((q >> 4) & 1) << (i % 8)
+            blk[6 + i % 16] = (q & 15) << (4 if i >= 16 else 0)
+            a = np.zeros(32, np.int8)
+            a[i] = 3
+            # every other element has q = 0 (w = -16) against a = 0
+            assert oracle.block_dot(blk, a) == 3 * (q - 16)
+
+
+def test_q5_dequant_and_layer_vs_dense_fp64():
+    blocks = synth.q5_blocks(synth.key(7, 300), 300).reshape(10, 30, 22)
+    codes, d = _np_dequant_q5(blocks)
+    assert np.array_equal(oracle.dequant(blocks), (d[..., None] * codes).reshape(10, 30 * 32))
+    wl = synth.Workload("tiny_q5", 256, 8, 2, 512, 1, routing="normal", weight_format=synth.FMT_Q5_0)
+    H, F, k, T = wl.hidden, wl.ffn, wl.top_k, 3
+    gate, up, down = (wl.expert_tensor(0, kd) for kd in range(3))
+    x, logits = wl.x(0, 0, T), wl.logits(0, 0, T)
+    idx, w = oracle.topk(logits, k)
+    y, it = oracle.layer(x, idx, w, gate, up, down, H, F, want_intermediates=True)
+
+    def deq(t):
+        c, dd = _np_dequant_q5(t)
+        return (dd[..., None] * c).reshape(t.shape[0], t.shape[1], -1)
+
+    Wg, Wu, Wd = deq(gate), deq(up), deq(down)
+    xa = it["xq"].astype(np.float64) * np.repeat(it["xd"].view(np.float16).astype(np.float64), 32, axis=1)
+    y_bf = np.zeros((T, H))
+    for t in range(T):
+        for j in range(k):
+            a, e = t * k + j, idx[t, j]
+            g, u = Wg[e] @ xa[t], Wu[e] @ xa[t]
+            np.testing.assert_allclose(it["g"][a], g, rtol=0, atol=1e-12 * np.abs(g).max())
+            h = g * u * expit(g)
+            hq, hd = oracle.quantize(h.astype(np.float32))
+            assert np.array_equal(hq, it["hq"][a]) and np.array_equal(hd, it["hd"][a])
+            ha = hq.astype(np.float64) * np.repeat(hd.view(np.float16).astype(np.float64), 32)
+            y_bf[t] += w[t, j] * (Wd[e] @ ha)
+    np.testing.assert_allclose(y, y_bf, rtol=1e-12, atol=1e-12 * np.abs(y_bf).max())
