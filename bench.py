@@ -50,7 +50,7 @@ def parse():
     ap.add_argument("--prefill-steps", type=int, default=2)
     ap.add_argument("--prefill-workload", default="prefill_t4096")
     ap.add_argument("--q8-steps", type=int, default=64,
-                    help="timed decode steps of the Q8_0 weight-format leg (0 skips it)")
+                    help="timed decode steps of each of the Q8_0 / Q5_0 weight-format legs (0 skips them)")
     ap.add_argument("--pool-steps", type=int, default=256,
                     help="decode tokens per run of the pool-mode / preheat leg (0 skips it)")
     ap.add_argument("--case", default=None, choices=["decode_layer", "prefill_layer"],
@@ -410,7 +410,8 @@ def run_ours(args):
     if args.pool_steps > 0:
         out["pool"] = run_pool_leg(args, qec, synth, torch, log)
     if args.q8_steps > 0:
-        out["q8_0"] = run_q8_leg(args, qec, synth, torch, log)
+        out["formats"] = {"q8_0": run_format_leg(args, qec, synth, torch, log, "decode_b1_q8_resident16"),
+                          "q5_0": run_format_leg(args, qec, synth, torch, log, "decode_b1_q5_resident16")}
     if rank == 0:
         out["cpu_baseline"] = cpu_baseline(wl, args.cpu_sample_steps, T) if args.cpu_sample_steps > 0 else None
         print(json.dumps(out), flush=True)
@@ -547,19 +548,19 @@ def run_pool_leg(args, qec, synth, torch, log):
     return out
 
 
-def run_q8_leg(args, qec, synth, torch, log):
-    """Q8_0 expert weights (32 signed 8-bit codes per block) on 16 fully
-    resident layers of the decode shape: batch-1 decode steps captured in a
-    CUDA graph (router top-k, plan, gate/up and down mat-vec launches per
-    layer), timed with CUDA events on the context stream; roofline = the
-    weights of the experts each step uses (3 tensors of 34-byte blocks) + x
-    and y, over the step time."""
-    wl = synth.WORKLOADS["decode_b1_q8_resident16"]
+def run_format_leg(args, qec, synth, torch, log, name):
+    """Q8_0 or Q5_0 expert weights on 16 fully resident layers of the decode
+    shape: batch-1 decode steps captured in a CUDA graph (router top-k, plan,
+    gate/up and down mat-vec launches per layer), timed with CUDA events on
+    the context stream; roofline = the weights of the experts each step uses
+    (3 tensors of 34- or 22-byte blocks) + x and y, over the step time."""
+    wl = synth.WORKLOADS[name]
     L, H, E, k, F = wl.n_layers, wl.hidden, wl.n_experts, wl.top_k, wl.ffn
+    fmt_name = {synth.FMT_Q8_0: "Q8_0", synth.FMT_Q5_0: "Q5_0"}[wl.weight_format]
     T = 1
     stream = torch.cuda.Stream()
     sp = stream.cuda_stream
-    ctx = qec.moe_layer_init(H, F, E, k, L, E, T, stream=sp, weight_format=qec.FMT_Q8_0)
+    ctx = qec.moe_layer_init(H, F, E, k, L, E, T, stream=sp, weight_format=wl.weight_format)
     register_workload(qec, synth, ctx, wl, log)
     n = args.q8_steps
     W = args.warmup
@@ -604,12 +605,14 @@ def run_q8_leg(args, qec, synth, torch, log):
     peaks, src = load_peaks()
     gbs = alg / (ms * 1e-3) / 1e9
     qec.moe_destroy(ctx)
-    log(f"Q8_0 leg: {T / (ms * 1e-3):.1f} tokens/s through {L} resident layers, {ms * 1e3 / L:.2f} us per layer, "
-        f"{gbs:.0f} GB/s")
-    return {"workload": f"{wl.name}: {L} layers, hidden {H}, {E} experts, top-{k}, FFN {F}, Q8_0 blocks of 32 "
-                        f"(34 B), every expert resident, batch-1 decode, {n} timed steps in a CUDA graph",
+    log(f"{fmt_name} leg: {T / (ms * 1e-3):.1f} tokens/s through {L} resident layers, {ms * 1e3 / L:.2f} us per "
+        f"layer, {gbs:.0f} GB/s")
+    return {"workload": f"{wl.name}: {L} layers, hidden {H}, {E} experts, top-{k}, FFN {F}, {fmt_name} blocks of 32 "
+                        f"({synth.BLOCK_BYTES[wl.weight_format]} B), every expert resident, batch-1 decode, {n} timed "
+                        f"steps in a CUDA graph",
             "tokens_per_s": round(T / (ms * 1e-3), 1), "us_per_layer": round(ms * 1e3 / L, 3),
-            "roofline": {"bound": "hbm", "kernels": "topk + plan + gate_up_kernel<Q8_0> + down_kernel<Q8_0> per layer",
+            "roofline": {"bound": "hbm",
+                         "kernels": f"topk + plan + gate_up_kernel<{fmt_name}> + down_kernel<{fmt_name}> per layer",
                          "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": round(gbs / peaks["hbm_gbs"], 4), "peak_source": f"{src} hbm_gbs (copy)",
                          "algorithmic_bytes_per_step": int(alg), "traffic": None}}

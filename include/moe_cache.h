@@ -69,7 +69,7 @@ typedef struct moe_cfg {
     int32_t renorm_topk;        /* 1: weights = softmax over the k selected */
     int32_t poll_timeout_ms;    /* host poll limit in cache_step (0 = 10 s) */
     int32_t device;             /* CUDA device ordinal */
-    int32_t weight_format;      /* MOE_FMT_Q4_0 (0) or MOE_FMT_Q8_0 (1), for every expert tensor */
+    int32_t weight_format;      /* MOE_FMT_Q4_0 (0), MOE_FMT_Q8_0 (1) or MOE_FMT_Q5_0 (2), every tensor */
 } moe_cfg;
 
 /* Expert weight formats (blocks of 32 weights, one binary16 scale d each).
@@ -79,10 +79,15 @@ typedef struct moe_cfg {
  *   w = d * q (one of the other block formats the dot kernels of
  *   Zapdev-labs/a6000-custom-kernels accept; the byte layout is the plain
  *   reading: scale, then codes in element order).
- * Q8_0 contexts run every forward through the mat-vec kernels (no fused
- * single-launch layer, no tensor-core prompt path, no lookahead). */
+ * Q5_0: 22-byte blocks, d, then 4 bytes whose little-endian word holds bit 4
+ *   of element j in bit j, then 16 nibble bytes in the Q4 order;
+ *   w = d * (q - 16) with q in 0..31 (another of those formats; same reading
+ *   of the layout).
+ * Q8_0 and Q5_0 contexts run every forward through the mat-vec kernels (no
+ * fused single-launch layer, no tensor-core prompt path, no lookahead). */
 #define MOE_FMT_Q4_0 0
 #define MOE_FMT_Q8_0 1
+#define MOE_FMT_Q5_0 2
 
 typedef struct moe_stats_t {
     uint64_t steps;        /* cache_step calls */
@@ -99,7 +104,7 @@ typedef struct moe_stats_t {
  * Create a context on cfg->device.  cuda_stream (cudaStream_t; NULL is the
  * legacy default stream, as everywhere in CUDA) is the stream every forward
  * of this context runs on; the caller keeps owning it.  The library allocates and owns: the HBM
- * expert pool (3*L*slots_per_tensor slots of rows*cols/32*(18 or 34) bytes), the
+ * expert pool (3*L*slots_per_tensor slots of rows*cols/32*(18, 34 or 22) bytes), the
  * pointer tables, stamps, miss log, workspaces, an upload stream and the
  * pinned host copies of registered tensors.  *out receives the context.
  * Errors: MOE_ERR_ARG (sizes), MOE_ERR_OOM, MOE_ERR_CUDA.
@@ -108,8 +113,8 @@ int moe_layer_init(const moe_cfg *cfg, void *cuda_stream, moe_ctx **out);
 
 /*
  * Register one expert tensor (layer, kind) and seed its pool.
- * host_q4: canonical tensor [n_experts][rows][cols/32][18 B] (Q4_0) or
- *   [...][34 B] (Q8_0, per cfg.weight_format), any host
+ * host_q4: canonical tensor [n_experts][rows][cols/32][18 B] (Q4_0),
+ *   [...][34 B] (Q8_0) or [...][22 B] (Q5_0), per cfg.weight_format, any host
  *   memory; the library copies it into its own pinned, device-mapped host
  *   memory in plane layout (all codes, then all scales) and never reads
  *   host_q4 again, so the caller may free it on return.

@@ -22,12 +22,13 @@ constexpr int kMaxChunk = 8;       // tokens per expert handled per weight pass
 __host__ __device__ inline size_t blob_scales_offset(int rows, int nb) { return (size_t)rows * nb * 16; }
 __host__ __device__ inline size_t blob_bytes(int rows, int nb) { return (size_t)rows * nb * kBlockBytes; }
 
-// Weight formats: Q4 (16 code bytes per block, w = d (q - 8)) and Q8_0 (32
-// signed code bytes per block in element order, w = d q).  The blob layout
-// is the same for both: [codes: rows x nb x code bytes][scales: rows x nb x
-// binary16].
-constexpr int kFmtQ4 = 0, kFmtQ8 = 1;
-__host__ __device__ constexpr int code_bytes(int fmt) { return fmt == kFmtQ8 ? 32 : 16; }
+// Weight formats: Q4 (16 code bytes per block, w = d (q - 8)), Q8_0 (32
+// signed code bytes per block in element order, w = d q) and Q5_0 (16 nibble
+// bytes as Q4 plus a 32-bit word of fifth bits, w = d (q - 16)).  Blob
+// layout, N = rows x nb blocks: [codes: N x 16 or 32 B][Q5_0 only: fifth
+// bits, N x 4 B][scales: N x binary16]; code_bytes counts both code planes.
+constexpr int kFmtQ4 = 0, kFmtQ8 = 1, kFmtQ5 = 2;
+__host__ __device__ constexpr int code_bytes(int fmt) { return fmt == kFmtQ8 ? 32 : fmt == kFmtQ5 ? 20 : 16; }
 __host__ __device__ inline size_t blob_scales_offset_fmt(int fmt, int rows, int nb) {
     return (size_t)rows * nb * code_bytes(fmt);
 }
@@ -114,15 +115,18 @@ __device__ __forceinline__ uint4 ld_weights(const uint4 *p) { return __ldcs(p); 
 
 __device__ __forceinline__ float ld_scale(const __half *p) { return __half2float(__ldcs(p)); }
 
-// Codes of one weight block held in registers, per format: load block b of a
-// row's code plane, and its exact int32 dot with 32 int8 activations (two
-// 16-byte halves a0 = elements 0..15, a1 = 16..31; a_sum = their sum).
+// Codes of one weight block held in registers, per format: load block i of a
+// blob of n blocks (i = row * nb + block), and its exact int32 dot with 32
+// int8 activations (two 16-byte halves a0 = elements 0..15, a1 = 16..31;
+// a_sum = their sum).
 template <int FMT>
 struct WCodes;
 template <>
 struct WCodes<kFmtQ4> {
     uint4 c;
-    __device__ __forceinline__ void load(const uint8_t *row, int b) { c = ld_weights((const uint4 *)row + b); }
+    __device__ __forceinline__ void load(const uint8_t *blob, size_t, size_t i) {
+        c = ld_weights((const uint4 *)blob + i);
+    }
     __device__ __forceinline__ int dot(const int4 &a0, const int4 &a1, int a_sum) const {
         return q4_block_dot(c, a0, a1, a_sum);
     }
@@ -130,8 +134,8 @@ struct WCodes<kFmtQ4> {
 template <>
 struct WCodes<kFmtQ8> {
     uint4 lo, hi;  // elements 0..15, 16..31
-    __device__ __forceinline__ void load(const uint8_t *row, int b) {
-        const uint4 *p = (const uint4 *)row + 2 * (size_t)b;
+    __device__ __forceinline__ void load(const uint8_t *blob, size_t, size_t i) {
+        const uint4 *p = (const uint4 *)blob + 2 * i;
         lo = ld_weights(p);
         hi = ld_weights(p + 1);
     }
@@ -144,6 +148,32 @@ struct WCodes<kFmtQ8> {
         s = __dp4a((int)hi.y, a1.y, s);
         s = __dp4a((int)hi.z, a1.z, s);
         return __dp4a((int)hi.w, a1.w, s);
+    }
+};
+// Bits 0..3 of x moved to bit 0 of bytes 0..3 (the four shifted copies do
+// not overlap, so the product carries nothing).
+__device__ __forceinline__ uint32_t spread4(uint32_t x) { return (x * 0x00204081u) & 0x01010101u; }
+template <>
+struct WCodes<kFmtQ5> {
+    uint4 c;     // low nibbles, Q4 order
+    uint32_t h;  // bit j = bit 4 of element j
+    __device__ __forceinline__ void load(const uint8_t *blob, size_t n, size_t i) {
+        c = ld_weights((const uint4 *)blob + i);
+        h = __ldcs((const unsigned int *)(blob + 16 * n) + i);
+    }
+    __device__ __forceinline__ int dot(const int4 &a0, const int4 &a1, int a_sum) const {
+        const uint32_t m = 0x0F0F0F0Fu;
+        const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+        const int aw0[4] = {a0.x, a0.y, a0.z, a0.w}, aw1[4] = {a1.x, a1.y, a1.z, a1.w};
+        int s = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t lo = (cw[k] & m) | (spread4((h >> (4 * k)) & 15u) << 4);
+            const uint32_t hi = ((cw[k] >> 4) & m) | (spread4((h >> (16 + 4 * k)) & 15u) << 4);
+            s = __dp4a((int)lo, aw0[k], s);
+            s = __dp4a((int)hi, aw1[k], s);
+        }
+        return s - 16 * a_sum;
     }
 };
 

@@ -268,8 +268,7 @@ __global__ void __launch_bounds__(256) gate_up_kernel(GemvParams p) {
         const uint8_t *bg = (const uint8_t *)(uintptr_t)(eg & ~1ull);
         const uint8_t *bu = (const uint8_t *)(uintptr_t)(eu & ~1ull);
         const int r = rg * 32 + rloc;
-        const uint8_t *qg = bg + (size_t)r * nbx * code_bytes(FMT);
-        const uint8_t *qu = bu + (size_t)r * nbx * code_bytes(FMT);
+        const size_t nblk = (size_t)p.F * nbx, rb0 = (size_t)r * nbx;
         const __half *dg = (const __half *)(bg + scale_off) + (size_t)r * nbx;
         const __half *du = (const __half *)(bu + scale_off) + (size_t)r * nbx;
 
@@ -288,8 +287,8 @@ __global__ void __launch_bounds__(256) gate_up_kernel(GemvParams p) {
                 for (int i = 0; i < 4; ++i) {
                     int b = b0 + i * kGULanes;
                     if (b < nbx) {
-                        wg4[i].load(qg, b);
-                        wu4[i].load(qu, b);
+                        wg4[i].load(bg, nblk, rb0 + b);
+                        wu4[i].load(bu, nblk, rb0 + b);
                         sg[i] = ld_scale(dg + b);
                         su[i] = ld_scale(du + b);
                     }
@@ -368,7 +367,7 @@ __global__ void __launch_bounds__(256) down_kernel(GemvParams p) {
         if (rb == 0 && threadIdx.x == 0) record_read(p.cv, p.tid_down, e, ed, step_clock);
         const uint8_t *bd = (const uint8_t *)(uintptr_t)(ed & ~1ull);
         const int r = rb * ROWS + rloc;
-        const uint8_t *qd = bd + (size_t)r * nbf * code_bytes(FMT);
+        const size_t nblk = (size_t)p.H * nbf, rb0 = (size_t)r * nbf;
         const __half *dd = (const __half *)(bd + scale_off) + (size_t)r * nbf;
 
         for (int c0 = a0; c0 < a1; c0 += kMaxChunk) {
@@ -386,7 +385,7 @@ __global__ void __launch_bounds__(256) down_kernel(GemvParams p) {
                 for (int i = 0; i < 4; ++i) {
                     int b = b0 + i * L;
                     if (b < nbf) {
-                        w4[i].load(qd, b);
+                        w4[i].load(bd, nblk, rb0 + b);
                         sw[i] = ld_scale(dd + b);
                     }
                 }
@@ -450,28 +449,26 @@ int down_rows_per_item(int F) {
     return kWarps * (32 / L);
 }
 
+template <int FMT>
+void launch_gemv_fmt(const GemvParams &p, int grid_gu, int grid_dn, cudaStream_t st, cudaEvent_t const *ev) {
+    gate_up_kernel<FMT><<<grid_gu, 256, 0, st>>>(p);
+    if (ev) record(ev[1], st);
+    if (ev) record(ev[2], st);
+    if (p.F / kBlock <= 40)
+        down_kernel<4, FMT><<<grid_dn, 256, 0, st>>>(p);
+    else
+        down_kernel<8, FMT><<<grid_dn, 256, 0, st>>>(p);
+}
+
 // ev (optional): 4 events recorded around the gate/up and the down launch.
 int launch_gemv(const GemvParams &p, int grid_gu, int grid_dn, cudaStream_t st, cudaEvent_t const *ev) {
-    const bool q8 = p.fmt == kFmtQ8;
     if (ev) record(ev[0], st);
-    if (q8)
-        gate_up_kernel<kFmtQ8><<<grid_gu, 256, 0, st>>>(p);
+    if (p.fmt == kFmtQ8)
+        launch_gemv_fmt<kFmtQ8>(p, grid_gu, grid_dn, st, ev);
+    else if (p.fmt == kFmtQ5)
+        launch_gemv_fmt<kFmtQ5>(p, grid_gu, grid_dn, st, ev);
     else
-        gate_up_kernel<kFmtQ4><<<grid_gu, 256, 0, st>>>(p);
-    if (ev) record(ev[1], st);
-    int nbf = p.F / kBlock;
-    if (ev) record(ev[2], st);
-    if (nbf <= 40) {
-        if (q8)
-            down_kernel<4, kFmtQ8><<<grid_dn, 256, 0, st>>>(p);
-        else
-            down_kernel<4, kFmtQ4><<<grid_dn, 256, 0, st>>>(p);
-    } else {
-        if (q8)
-            down_kernel<8, kFmtQ8><<<grid_dn, 256, 0, st>>>(p);
-        else
-            down_kernel<8, kFmtQ4><<<grid_dn, 256, 0, st>>>(p);
-    }
+        launch_gemv_fmt<kFmtQ4>(p, grid_gu, grid_dn, st, ev);
     if (ev) record(ev[3], st);
     return (int)cudaGetLastError();
 }
@@ -1652,7 +1649,7 @@ __global__ void block_dots_kernel(const uint8_t *blob, int rows, int nb, int row
     if (i >= n_rows * nb) return;
     const int r = row0 + i / nb, b = i % nb;
     WCodes<FMT> w;
-    w.load(blob + (size_t)r * nb * code_bytes(FMT), b);
+    w.load(blob, (size_t)rows * nb, (size_t)r * nb + b);
     const int4 *xa = (const int4 *)(qa + (size_t)b * kBlock);
     int4 x0 = xa[0], x1 = xa[1];
     int s = 0;
@@ -1667,6 +1664,8 @@ int launch_block_dots(const uint8_t *blob, int fmt, int rows, int nb, int row0, 
     if (n <= 0) return 0;
     if (fmt == kFmtQ8)
         block_dots_kernel<kFmtQ8><<<(n + 255) / 256, 256, 0, st>>>(blob, rows, nb, row0, n_rows, qa, out);
+    else if (fmt == kFmtQ5)
+        block_dots_kernel<kFmtQ5><<<(n + 255) / 256, 256, 0, st>>>(blob, rows, nb, row0, n_rows, qa, out);
     else
         block_dots_kernel<kFmtQ4><<<(n + 255) / 256, 256, 0, st>>>(blob, rows, nb, row0, n_rows, qa, out);
     return (int)cudaGetLastError();

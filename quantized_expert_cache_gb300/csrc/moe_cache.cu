@@ -46,7 +46,7 @@ struct moe_ctx {
     int dev = 0, n_sm = 0;
     int n_tensors = 0, E = 0, spt = 0, H = 0, F = 0, k = 0, M = 0;
     size_t blob = 0, stride = 0;
-    int fmt = 0;  // moe::kFmtQ4 or moe::kFmtQ8
+    int fmt = 0;  // moe::kFmtQ4, kFmtQ8 or kFmtQ5
     cudaStream_t stream = nullptr, up = nullptr;
     cudaEvent_t ev_fwd = nullptr, ev_up = nullptr;
 
@@ -207,7 +207,8 @@ int sync_all(moe_ctx *ctx) {
 }
 
 // Repack canonical blocks (binary16 d, then the code bytes: 18 bytes for
-// Q4, 34 for Q8_0) of n_experts experts into plane blobs.
+// Q4, 34 for Q8_0; d, 4 fifth-bit bytes, 16 nibble bytes = 22 for Q5_0) of
+// n_experts experts into plane blobs.
 void repack(const uint8_t *src, uint8_t *dst, int fmt, int n_experts, int rows, int nb, size_t stride) {
     const size_t nblk = (size_t)rows * nb, cb = (size_t)moe::code_bytes(fmt), bb = cb + 2;
     auto work = [&](int e0, int e1) {
@@ -218,7 +219,12 @@ void repack(const uint8_t *src, uint8_t *dst, int fmt, int n_experts, int rows, 
             for (size_t b = 0; b < nblk; ++b) {
                 d[2 * b] = s[bb * b];
                 d[2 * b + 1] = s[bb * b + 1];
-                memcpy(q + cb * b, s + bb * b + 2, cb);
+                if (fmt == moe::kFmtQ5) {
+                    memcpy(q + 16 * b, s + bb * b + 6, 16);              // nibbles
+                    memcpy(q + 16 * nblk + 4 * b, s + bb * b + 2, 4);  // fifth bits
+                } else {
+                    memcpy(q + cb * b, s + bb * b + 2, cb);
+                }
             }
         }
     };
@@ -405,10 +411,11 @@ int moe_layer_init(const moe_cfg *cfg, void *cuda_stream, moe_ctx **out) {
     if (c.hidden <= 0 || c.hidden % 32 || c.ffn <= 0 || c.ffn % 32 || c.n_experts < 1 || c.n_experts > 4096 ||
         c.top_k < 1 || c.top_k > 32 || c.top_k > c.n_experts || c.n_layers < 1 || c.n_layers * 3 > (1 << 20) ||
         c.slots_per_tensor < 0 || c.slots_per_tensor > c.n_experts || c.max_tokens < 1 || c.window_tokens < 1 ||
-        c.max_swaps_per_step < 0 || (c.weight_format != MOE_FMT_Q4_0 && c.weight_format != MOE_FMT_Q8_0))
+        c.max_swaps_per_step < 0 ||
+        (c.weight_format != MOE_FMT_Q4_0 && c.weight_format != MOE_FMT_Q8_0 && c.weight_format != MOE_FMT_Q5_0))
         return fail(nullptr, MOE_ERR_ARG,
                     "bad cfg: hidden%32, ffn%32, 1<=E<=4096, 1<=k<=min(32,E), layers>=1, 0<=slots<=E, max_tokens>=1, "
-                    "weight_format Q4_0 or Q8_0");
+                    "weight_format Q4_0, Q8_0 or Q5_0");
     int down_rows = moe::down_rows_per_item(c.ffn);
     if (c.hidden % down_rows) return fail(nullptr, MOE_ERR_ARG, "hidden must be a multiple of the down row block");
     ctx = new moe_ctx();
@@ -421,7 +428,7 @@ int moe_layer_init(const moe_cfg *cfg, void *cuda_stream, moe_ctx **out) {
     ctx->M = c.max_tokens;
     ctx->n_tensors = 3 * c.n_layers;
     ctx->spt = c.slots_per_tensor;
-    ctx->fmt = c.weight_format == MOE_FMT_Q8_0 ? moe::kFmtQ8 : moe::kFmtQ4;
+    ctx->fmt = c.weight_format == MOE_FMT_Q8_0 ? moe::kFmtQ8 : c.weight_format == MOE_FMT_Q5_0 ? moe::kFmtQ5 : moe::kFmtQ4;
     ctx->blob = moe::blob_bytes_fmt(ctx->fmt, c.ffn, c.hidden / 32);
     ctx->stride = (ctx->blob + 255) / 256 * 256;
     auto cleanup_fail = [&](int rc) {

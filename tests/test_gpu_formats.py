@@ -1,8 +1,9 @@
-"""GPU parity of Q8_0 expert weights (blocks of 32 signed 8-bit codes and one
-binary16 scale, w = d * q) through the C ABI, against the oracle: integer
-block dots bit-exact from pool slots and from pinned host memory, whole
-layers (decode and prompt-sized batches, hot and cold experts, ragged
-shapes), the miss log, and the cache state after every promotion pass."""
+"""GPU parity of the other expert weight formats through the C ABI, against
+the oracle: Q8_0 (blocks of 32 signed 8-bit codes and one binary16 scale,
+w = d * q) and Q5_0 (5-bit codes, w = d * (q - 16)).  Integer block dots
+bit-exact from pool slots and from pinned host memory, whole layers (decode
+and prompt-sized batches, hot and cold experts, ragged shapes), the miss
+log, and the cache state after every promotion pass."""
 import numpy as np
 import pytest
 
@@ -13,7 +14,7 @@ from gpu_helpers import Model, check_layer_parity
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
-Q8 = qec.FMT_Q8_0
+FMTS = [pytest.param(qec.FMT_Q8_0, id="q8_0"), pytest.param(qec.FMT_Q5_0, id="q5_0")]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -23,8 +24,9 @@ def _gpu():
     qec.load()
 
 
-def test_q8_block_dots_bit_exact_hot_and_cold():
-    m = Model(H=256, F=512, E=8, k=2, L=1, capacity=4, max_tokens=4, routing="normal", weight_format=Q8)
+@pytest.mark.parametrize("fmt", FMTS)
+def test_block_dots_bit_exact_hot_and_cold(fmt):
+    m = Model(H=256, F=512, E=8, k=2, L=1, capacity=4, max_tokens=4, routing="normal", weight_format=fmt)
     try:
         rng = np.random.default_rng(5)
         for tid in (0, 1, 2):
@@ -40,7 +42,7 @@ def test_q8_block_dots_bit_exact_hot_and_cold():
                 out = torch.empty((n_rows, cols // 32), dtype=torch.int32, device="cuda")
                 qec.moe_debug_block_dots(m.ctx, tid, e, 5, n_rows, torch.from_numpy(qa).cuda(), out)
                 W = m.tensors[tid][e]
-                assert W.shape[-1] == 34
+                assert W.shape[-1] == synth.BLOCK_BYTES[fmt]
                 ref = np.array([[oracle.block_dot(W[5 + r, b], qa[32 * b:32 * b + 32]) for b in range(cols // 32)]
                                 for r in range(n_rows)])
                 assert np.array_equal(out.cpu().numpy(), ref)
@@ -48,11 +50,12 @@ def test_q8_block_dots_bit_exact_hot_and_cold():
         m.close()
 
 
+@pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("H,F,E,k,T", [(256, 512, 8, 2, 4), (512, 384, 64, 4, 1), (512, 384, 64, 4, 7),
                                        (512, 384, 64, 4, 33), (640, 1440, 16, 3, 5), (640, 1440, 16, 3, 40),
                                        (2048, 1152, 64, 8, 1)])
-def test_q8_layer_parity_hot_and_cold(H, F, E, k, T):
-    m = Model(H=H, F=F, E=E, k=k, L=2, capacity=E // 2, max_tokens=T, zipf_s=0.6, weight_format=Q8)
+def test_layer_parity_hot_and_cold(H, F, E, k, T, fmt):
+    m = Model(H=H, F=F, E=E, k=k, L=2, capacity=E // 2, max_tokens=T, zipf_s=0.6, weight_format=fmt)
     try:
         for layer in range(2):
             x, lg = m.wl.x(layer, 1, T), m.wl.logits(layer, 1, T)
@@ -69,8 +72,9 @@ def test_q8_layer_parity_hot_and_cold(H, F, E, k, T):
         m.close()
 
 
-def test_q8_routed_forward_and_cache_steps():
-    m = Model(H=512, F=384, E=32, k=4, L=2, capacity=8, max_tokens=4, window=8, zipf_s=1.1, weight_format=Q8)
+@pytest.mark.parametrize("fmt", FMTS)
+def test_routed_forward_and_cache_steps(fmt):
+    m = Model(H=512, F=384, E=32, k=4, L=2, capacity=8, max_tokens=4, window=8, zipf_s=1.1, weight_format=fmt)
     try:
         for step in range(30):
             T = 1 if step % 6 else 3
@@ -109,13 +113,13 @@ def test_q8_routed_forward_and_cache_steps():
         m.close()
 
 
-def test_q8_format_is_checked():
+def test_format_is_checked():
     with pytest.raises(qec.MoeError) as ex:
         qec.moe_layer_init(256, 256, 8, 2, 1, 4, 4, weight_format=7,
                            stream=torch.cuda.current_stream().cuda_stream)
     assert ex.value.code == -1
     # a Q8_0 context has no prompt tensor-core path, so no lookahead either
-    m = Model(H=256, F=256, E=8, k=2, L=1, capacity=4, max_tokens=64, weight_format=Q8)
+    m = Model(H=256, F=256, E=8, k=2, L=1, capacity=4, max_tokens=64, weight_format=qec.FMT_Q8_0)
     try:
         with pytest.raises(qec.MoeError) as ex:
             qec.moe_set_lookahead(m.ctx, True)
