@@ -176,6 +176,29 @@ def layer(x, idx, w, gate, up, down, H, F, want_intermediates=False):
     return (y, out) if want_intermediates else y
 
 
+def with_shared(idx, w, gate, up, down, shared):
+    """Routing and expert tensors of a layer with a shared expert (the
+    shared-expert block among the fusion arguments of the dot kernels,
+    Zapdev-labs/a6000-custom-kernels): every token also runs the shared
+    expert on the same quantized x, and y = sum_j w_j o_j + o_shared.  The
+    shared expert is appended as one more assignment per token, after the
+    routed ones, with weight 1 and expert id E (one past the routed ids).
+    shared: (gate, up, down) canonical tensors [rows, nb, B] of one expert."""
+    idx = np.ascontiguousarray(idx, np.int32)
+    T, k = idx.shape
+    E = gate.shape[0] if not isinstance(gate, dict) else max(gate) + 1
+    E = max(E, int(idx.max()) + 1 if idx.size else 0)
+    idx2 = np.concatenate([idx, np.full((T, 1), E, np.int32)], axis=1)
+    w2 = np.concatenate([np.asarray(w, np.float64), np.ones((T, 1))], axis=1)
+
+    def ext(t, s):
+        d = dict(t) if isinstance(t, dict) else {e: t[e] for e in sorted(set(idx.ravel().tolist()))}
+        d[E] = s
+        return d
+
+    return idx2, w2, ext(gate, shared[0]), ext(up, shared[1]), ext(down, shared[2])
+
+
 def down_combine(idx, w, down, hq, hd, H, F):
     idx = np.ascontiguousarray(idx, np.int32)
     w = np.ascontiguousarray(w, np.float64)

@@ -458,3 +458,31 @@ def test_q5_dequant_and_layer_vs_dense_fp64():
             ha = hq.astype(np.float64) * np.repeat(hd.view(np.float16).astype(np.float64), 32)
             y_bf[t] += w[t, j] * (Wd[e] @ ha)
     np.testing.assert_allclose(y, y_bf, rtol=1e-12, atol=1e-12 * np.abs(y_bf).max())
+
+
+# ---------------------------------------------------------------- shared expert
+def test_shared_expert_layer_vs_dense_fp64():
+    wl, H, F, E, k, T, gate, up, down, x, logits = _tiny_layer()
+    sh = synth.Workload("shared", H, 1, 1, F, 1, routing="normal", seed=9)
+    shared = tuple(sh.expert_tensor(0, kd)[0] for kd in range(3))
+    idx, w = oracle.topk(logits, k)
+    idx2, w2, g2, u2, d2 = oracle.with_shared(idx, w, gate, up, down, shared)
+    assert idx2.shape == (T, k + 1) and (idx2[:, k] == E).all() and (w2[:, k] == 1.0).all()
+    y, it = oracle.layer(x, idx2, w2, g2, u2, d2, H, F, want_intermediates=True)
+    y0 = oracle.layer(x, idx, w, gate, up, down, H, F)
+
+    def deq(b):
+        codes, d = _np_dequant(b)
+        return (d[..., None] * (codes - 8)).reshape(b.shape[0], -1)
+
+    Sg, Su, Sd = (deq(t) for t in shared)
+    xa = it["xq"].astype(np.float64) * np.repeat(it["xd"].view(np.float16).astype(np.float64), 32, axis=1)
+    for t in range(T):
+        g, u = Sg @ xa[t], Su @ xa[t]
+        h = g * u * expit(g)
+        hq, hd = oracle.quantize(h.astype(np.float32))
+        a = t * (k + 1) + k
+        assert np.array_equal(hq, it["hq"][a]) and np.array_equal(hd, it["hd"][a])
+        o = Sd @ (hq.astype(np.float64) * np.repeat(hd.view(np.float16).astype(np.float64), 32))
+        # y = (routed sum) + o_shared: the routed part is the plain layer
+        np.testing.assert_allclose(y[t], y0[t] + o, rtol=1e-12, atol=1e-12 * np.abs(o).max())
