@@ -70,6 +70,7 @@ typedef struct moe_cfg {
     int32_t poll_timeout_ms;    /* host poll limit in cache_step (0 = 10 s) */
     int32_t device;             /* CUDA device ordinal */
     int32_t weight_format;      /* MOE_FMT_Q4_0 (0), MOE_FMT_Q8_0 (1) or MOE_FMT_Q5_0 (2), every tensor */
+    int32_t shared_experts;     /* 1: every layer has one shared expert (register_shared_expert), E <= 4095 */
 } moe_cfg;
 
 /* Expert weight formats (blocks of 32 weights, one binary16 scale d each).
@@ -130,6 +131,24 @@ int moe_layer_init(const moe_cfg *cfg, void *cuda_stream, moe_ctx **out);
  */
 int register_expert_tensor(moe_ctx *ctx, int layer, int kind, const void *host_q4, int rows, int cols,
                            int capacity, const int32_t *seed_order, int n_seed, int *tensor_id);
+
+/*
+ * Register the shared expert of (layer, kind) (the shared-expert block among
+ * the fusion arguments of the dot kernels, Zapdev-labs/a6000-custom-kernels):
+ * one expert that every token runs next to its routed ones, with weight 1:
+ * y[t] = sum_j w[t,j] o[t,j] + o_shared[t].  Needs cfg.shared_experts = 1;
+ * then every layer needs its three shared tensors before its first forward.
+ * host_w: one canonical expert [rows][cols/32][block bytes] in the context's
+ * weight format, copied (the caller may free it).  The shared expert lives
+ * in its own HBM allocation, never cold and never in the pool: its table
+ * entry is column E of the tensor's row, so it runs inside the same gate/up,
+ * down (and, for prompts, grouped GEMM) launches as the routed experts, as
+ * assignment k of every token.  Shared-expert contexts run the mat-vec
+ * kernels for small batches (no single-launch layer).  Synchronous.
+ * Errors: MOE_ERR_STATE (no shared experts in cfg), MOE_ERR_ARG (shape,
+ * already registered), MOE_ERR_OOM, MOE_ERR_CUDA.
+ */
+int register_shared_expert(moe_ctx *ctx, int layer, int kind, const void *host_w, int rows, int cols);
 
 /*
  * Router top-k (mihailescu2m/llama.cpp, "the graph-shape problem": only the

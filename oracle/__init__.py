@@ -176,18 +176,22 @@ def layer(x, idx, w, gate, up, down, H, F, want_intermediates=False):
     return (y, out) if want_intermediates else y
 
 
-def with_shared(idx, w, gate, up, down, shared):
+def with_shared(idx, w, gate, up, down, shared, e_shared=None):
     """Routing and expert tensors of a layer with a shared expert (the
     shared-expert block among the fusion arguments of the dot kernels,
     Zapdev-labs/a6000-custom-kernels): every token also runs the shared
     expert on the same quantized x, and y = sum_j w_j o_j + o_shared.  The
     shared expert is appended as one more assignment per token, after the
     routed ones, with weight 1 and expert id E (one past the routed ids).
-    shared: (gate, up, down) canonical tensors [rows, nb, B] of one expert."""
+    shared: (gate, up, down) canonical tensors [rows, nb, B] of one expert;
+    e_shared: the id to give it (default: one past every routed id given)."""
     idx = np.ascontiguousarray(idx, np.int32)
     T, k = idx.shape
     E = gate.shape[0] if not isinstance(gate, dict) else max(gate) + 1
     E = max(E, int(idx.max()) + 1 if idx.size else 0)
+    if e_shared is not None:
+        assert e_shared >= E, "the shared id must not collide with a routed one"
+        E = int(e_shared)
     idx2 = np.concatenate([idx, np.full((T, 1), E, np.int32)], axis=1)
     w2 = np.concatenate([np.asarray(w, np.float64), np.ones((T, 1))], axis=1)
 

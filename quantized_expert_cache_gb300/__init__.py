@@ -35,7 +35,7 @@ class MoeError(RuntimeError):
 class moe_cfg(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "hidden", "ffn", "n_experts", "top_k", "n_layers", "slots_per_tensor", "max_tokens", "window_tokens",
-        "max_swaps_per_step", "renorm_topk", "poll_timeout_ms", "device", "weight_format")]
+        "max_swaps_per_step", "renorm_topk", "poll_timeout_ms", "device", "weight_format", "shared_experts")]
 
 
 class moe_stats_t(ctypes.Structure):
@@ -48,6 +48,7 @@ _vp, _i32, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
 SIGNATURES = {
     "moe_layer_init": (_i32, [ctypes.POINTER(moe_cfg), _vp, ctypes.POINTER(_vp)]),
     "register_expert_tensor": (_i32, [_vp, _i32, _i32, _vp, _i32, _i32, _i32, _vp, _i32, ctypes.POINTER(_i32)]),
+    "register_shared_expert": (_i32, [_vp, _i32, _i32, _vp, _i32, _i32]),
     "route_topk": (_i32, [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp]),
     "moe_ffn_forward": (_i32, [_vp, _i32, _vp, _i32, _vp, _vp, _vp, _vp]),
     "moe_ffn_forward_routed": (_i32, [_vp, _i32, _vp, _vp, _i32, _vp, _vp, _vp, _vp]),
@@ -138,9 +139,9 @@ def _check(ctx, rc):
 
 def moe_layer_init(hidden, ffn, n_experts, top_k, n_layers, slots_per_tensor, max_tokens, window_tokens=64,
                    max_swaps_per_step=0, renorm_topk=1, poll_timeout_ms=10000, device=0, stream=None,
-                   weight_format=FMT_Q4_0) -> int:
+                   weight_format=FMT_Q4_0, shared_experts=0) -> int:
     cfg = moe_cfg(hidden, ffn, n_experts, top_k, n_layers, slots_per_tensor, max_tokens, window_tokens,
-                  max_swaps_per_step, renorm_topk, poll_timeout_ms, device, weight_format)
+                  max_swaps_per_step, renorm_topk, poll_timeout_ms, device, weight_format, shared_experts)
     out = ctypes.c_void_p()
     _check(None, load().moe_layer_init(ctypes.byref(cfg), _stream(stream), ctypes.byref(out)))
     return out.value
@@ -153,6 +154,10 @@ def register_expert_tensor(ctx, layer, kind, host_q4: np.ndarray, rows, cols, ca
     _check(ctx, load().register_expert_tensor(ctx, layer, kind, _host(host_q4), rows, cols, capacity, _host(so),
                                               n_seed, ctypes.byref(tid)))
     return tid.value
+
+
+def register_shared_expert(ctx, layer, kind, host_w: np.ndarray, rows, cols):
+    return _check(ctx, load().register_shared_expert(ctx, layer, kind, _host(host_w), rows, cols))
 
 
 def route_topk(ctx, logits, n_tokens, n_experts, k, idx, w, stream=None):

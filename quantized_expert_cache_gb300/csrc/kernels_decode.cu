@@ -1749,4 +1749,36 @@ int launch_count_assign(const int32_t *idx, int n, int E, uint32_t *cnt, cudaStr
     return (int)cudaGetLastError();
 }
 
+// Shared expert: the routed assignments of every token followed by one more,
+// expert e_shared with weight 1 (routed ids outside [0, e_shared) set error
+// bit 0 and are replaced by e_shared, which the plan then reads as valid).
+__global__ void shared_assign_kernel(const int32_t *__restrict__ idx, const float *__restrict__ w, int T, int k,
+                                     int e_shared, int32_t *idx_a, float *w_a, int *error) {
+    const int ka = k + 1;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < T * ka; i += gridDim.x * blockDim.x) {
+        const int t = i / ka, j = i - t * ka;
+        if (j == k) {
+            idx_a[i] = e_shared;
+            w_a[i] = 1.0f;
+        } else {
+            int e = idx[(size_t)t * k + j];
+            if (e < 0 || e >= e_shared) {
+                atomicOr(error, 1);
+                e = e_shared;
+            }
+            idx_a[i] = e;
+            w_a[i] = w[(size_t)t * k + j];
+        }
+    }
+}
+
+int launch_shared_assign(const int32_t *idx, const float *w, int T, int k, int e_shared, int32_t *idx_a, float *w_a,
+                         int *error, cudaStream_t st) {
+    const int n = T * (k + 1);
+    if (n <= 0) return 0;
+    const int grid = (n + 255) / 256 < 152 ? (n + 255) / 256 : 152;
+    shared_assign_kernel<<<grid, 256, 0, st>>>(idx, w, T, k, e_shared, idx_a, w_a, error);
+    return (int)cudaGetLastError();
+}
+
 }  // namespace moe

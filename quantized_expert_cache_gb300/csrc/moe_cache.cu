@@ -45,6 +45,14 @@ struct moe_ctx {
     moe_cfg cfg{};
     int dev = 0, n_sm = 0;
     int n_tensors = 0, E = 0, spt = 0, H = 0, F = 0, k = 0, M = 0;
+    // shared expert (cfg.shared_experts): table rows hold E + 1 entries (the
+    // last = the layer's shared expert, always in HBM) and every token gets
+    // k + 1 assignments (the last = the shared expert, weight 1)
+    bool shared = false;
+    int Et = 0, ka = 0;                    // table row length, assignments per token
+    std::vector<uint8_t *> sh_blob;        // [n_tensors]: device blob of the shared expert
+    int32_t *idx_a = nullptr;              // [M][ka]: routed ids + E
+    float *w_a = nullptr;                  // [M][ka]: routed weights + 1
     size_t blob = 0, stride = 0;
     int fmt = 0;  // moe::kFmtQ4, kFmtQ8 or kFmtQ5
     cudaStream_t stream = nullptr, up = nullptr;
@@ -75,7 +83,7 @@ struct moe_ctx {
     int cap_gu = 0, cap_dn = 0;
     CUtensorMap tm_x{}, tm_h{};
     // prefill staging of cold experts into lent slots
-    uint64_t *etbl = nullptr;     // [3][E]
+    uint64_t *etbl = nullptr;     // [3][Et]
     uint64_t *stage_jobs = nullptr;
     int *stage_n = nullptr;
     int stage_cap = 0;
@@ -83,7 +91,7 @@ struct moe_ctx {
     bool lookahead = false;
     int pf_cap = 0;                         // expert blobs per tensor per buffer
     uint8_t *pf_buf[2] = {nullptr, nullptr};  // [3][pf_cap] blobs of `stride` bytes
-    int32_t *d_pfmap[2] = {nullptr, nullptr}, *h_pfmap[2] = {nullptr, nullptr};  // [3][E]: buffer index or -1
+    int32_t *d_pfmap[2] = {nullptr, nullptr}, *h_pfmap[2] = {nullptr, nullptr};  // [3][Et]: buffer index or -1
     cudaEvent_t ev_pf[2] = {nullptr, nullptr}, ev_pf_free[2] = {nullptr, nullptr};
     int pf_layer[2] = {-1, -1};
     bool pf_map_pending[2] = {false, false};
@@ -142,8 +150,8 @@ int fail(moe_ctx *c, int code, const std::string &msg) {
 
 inline int32_t *p_n_uniq(moe_ctx *c) { return c->plan_i; }
 inline int32_t *p_uniq_e(moe_ctx *c) { return c->plan_i + 1; }
-inline int32_t *p_uniq_off(moe_ctx *c) { return c->plan_i + 1 + std::min(c->M * c->k, c->E); }
-inline int32_t *p_assign(moe_ctx *c) { return c->plan_i + 2 + 2 * std::min(c->M * c->k, c->E); }
+inline int32_t *p_uniq_off(moe_ctx *c) { return c->plan_i + 1 + std::min(c->M * c->ka, c->Et); }
+inline int32_t *p_assign(moe_ctx *c) { return c->plan_i + 2 + 2 * std::min(c->M * c->ka, c->Et); }
 
 inline uint64_t pool_addr(moe_ctx *c, int tid, int local) {
     size_t g = (size_t)local * c->n_tensors + tid;
@@ -168,8 +176,8 @@ void set_entry(moe_ctx *c, int tid, int e, uint64_t entry, int32_t slot) {
     TensorState &ts = c->t[tid];
     ts.tbl[e] = entry;
     ts.slot_of[e] = slot;
-    push_upd(c, 0, (size_t)tid * c->E + e, entry);
-    push_upd(c, 1, (size_t)tid * c->E + e, (uint64_t)(int64_t)stamp_index(c, tid, slot));
+    push_upd(c, 0, (size_t)tid * c->Et + e, entry);
+    push_upd(c, 1, (size_t)tid * c->Et + e, (uint64_t)(int64_t)stamp_index(c, tid, slot));
 }
 
 constexpr size_t kStepKeys = 256;  // miss keys read back with the hit bitmap
@@ -268,7 +276,7 @@ int make_tmap(moe_ctx *ctx, CUtensorMap *tm, void *base, uint64_t rows, uint64_t
 // prompt forward that read that buffer.  A run of consecutive cold experts is
 // one copy.  The buffer's map (expert -> copy index or -1) goes along.
 int prefetch_layer(moe_ctx *ctx, int l) {
-    const int b = l & 1, E = ctx->E;
+    const int b = l & 1, E = ctx->E, Et = ctx->Et;
     for (int kd = 0; kd < 3; ++kd)
         if (!ctx->t[l * 3 + kd].registered) return MOE_OK;
     // the previous prefetch into this buffer copied the host map: it has to
@@ -289,7 +297,7 @@ int prefetch_layer(moe_ctx *ctx, int l) {
                 run_len = 0;
             }
             if (e == E) break;
-            map[kd * E + e] = cold ? n : -1;
+            map[kd * Et + e] = cold ? n : -1;
             if (cold) {
                 if (!run_len) {
                     run_e = e;
@@ -300,7 +308,9 @@ int prefetch_layer(moe_ctx *ctx, int l) {
             }
         }
     }
-    CK(cudaMemcpyAsync(ctx->d_pfmap[b], map, sizeof(int32_t) * 3 * E, cudaMemcpyHostToDevice, ctx->up));
+    if (Et > E)
+        for (int kd = 0; kd < 3; ++kd) map[kd * Et + E] = -1;  // the shared expert stays where it is
+    CK(cudaMemcpyAsync(ctx->d_pfmap[b], map, sizeof(int32_t) * 3 * Et, cudaMemcpyHostToDevice, ctx->up));
     CK(cudaEventRecord(ctx->ev_pf[b], ctx->up));
     ctx->pf_map_pending[b] = true;
     ctx->pf_layer[b] = l;
@@ -411,11 +421,11 @@ int moe_layer_init(const moe_cfg *cfg, void *cuda_stream, moe_ctx **out) {
     if (c.hidden <= 0 || c.hidden % 32 || c.ffn <= 0 || c.ffn % 32 || c.n_experts < 1 || c.n_experts > 4096 ||
         c.top_k < 1 || c.top_k > 32 || c.top_k > c.n_experts || c.n_layers < 1 || c.n_layers * 3 > (1 << 20) ||
         c.slots_per_tensor < 0 || c.slots_per_tensor > c.n_experts || c.max_tokens < 1 || c.window_tokens < 1 ||
-        c.max_swaps_per_step < 0 ||
+        c.max_swaps_per_step < 0 || (c.shared_experts != 0 && (c.shared_experts != 1 || c.n_experts > 4095)) ||
         (c.weight_format != MOE_FMT_Q4_0 && c.weight_format != MOE_FMT_Q8_0 && c.weight_format != MOE_FMT_Q5_0))
         return fail(nullptr, MOE_ERR_ARG,
                     "bad cfg: hidden%32, ffn%32, 1<=E<=4096, 1<=k<=min(32,E), layers>=1, 0<=slots<=E, max_tokens>=1, "
-                    "weight_format Q4_0, Q8_0 or Q5_0");
+                    "weight_format Q4_0, Q8_0 or Q5_0, shared_experts 0 or 1 (then E <= 4095)");
     int down_rows = moe::down_rows_per_item(c.ffn);
     if (c.hidden % down_rows) return fail(nullptr, MOE_ERR_ARG, "hidden must be a multiple of the down row block");
     ctx = new moe_ctx();
@@ -425,6 +435,9 @@ int moe_layer_init(const moe_cfg *cfg, void *cuda_stream, moe_ctx **out) {
     ctx->H = c.hidden;
     ctx->F = c.ffn;
     ctx->k = c.top_k;
+    ctx->shared = c.shared_experts != 0;
+    ctx->Et = c.n_experts + (ctx->shared ? 1 : 0);
+    ctx->ka = c.top_k + (ctx->shared ? 1 : 0);
     ctx->M = c.max_tokens;
     ctx->n_tensors = 3 * c.n_layers;
     ctx->spt = c.slots_per_tensor;
@@ -452,15 +465,16 @@ int moe_layer_init(const moe_cfg *cfg, void *cuda_stream, moe_ctx **out) {
     CKI(cudaEventCreateWithFlags(&ctx->ev_fwd, cudaEventDisableTiming));
     CKI(cudaEventCreateWithFlags(&ctx->ev_up, cudaEventDisableTiming));
 
-    const int nt = ctx->n_tensors, E = ctx->E;
+    const int nt = ctx->n_tensors, E = ctx->E, Et = ctx->Et;
     ctx->arena_bytes = (size_t)nt * ctx->spt * ctx->stride;
     if (ctx->arena_bytes) CKI(cudaMalloc(&ctx->arena, ctx->arena_bytes));
-    ctx->bitmap_words = (E + 31) / 32;
+    ctx->bitmap_words = (Et + 31) / 32;
     ctx->miss_cap = nt * E;
-    CKI(cudaMalloc(&ctx->d_tbl, sizeof(uint64_t) * nt * E));
-    CKI(cudaMalloc(&ctx->d_slot, sizeof(int32_t) * nt * E));
-    CKI(cudaMemset(ctx->d_slot, 0xff, sizeof(int32_t) * nt * E));
-    CKI(cudaMemset(ctx->d_tbl, 0, sizeof(uint64_t) * nt * E));
+    CKI(cudaMalloc(&ctx->d_tbl, sizeof(uint64_t) * nt * Et));
+    CKI(cudaMalloc(&ctx->d_slot, sizeof(int32_t) * nt * Et));
+    CKI(cudaMemset(ctx->d_slot, 0xff, sizeof(int32_t) * nt * Et));
+    CKI(cudaMemset(ctx->d_tbl, 0, sizeof(uint64_t) * nt * Et));
+    ctx->sh_blob.assign(nt, nullptr);
     CKI(cudaMalloc(&ctx->d_stamps, sizeof(uint32_t) * (size_t)nt * std::max(1, ctx->spt)));
     CKI(cudaMemset(ctx->d_stamps, 0, sizeof(uint32_t) * (size_t)nt * std::max(1, ctx->spt)));
     CKI(cudaMalloc(&ctx->d_bitmap, sizeof(uint32_t) * (size_t)nt * ctx->bitmap_words));
@@ -477,7 +491,11 @@ int moe_layer_init(const moe_cfg *cfg, void *cuda_stream, moe_ctx **out) {
     CKI(cudaMalloc(&ctx->d_cold, sizeof(unsigned long long)));
     CKI(cudaMemset(ctx->d_cold, 0, sizeof(unsigned long long)));
 
-    const size_t M = ctx->M, A = M * ctx->k, U = std::min<size_t>(A, E);
+    const size_t M = ctx->M, A = M * ctx->ka, U = std::min<size_t>(A, Et);
+    if (ctx->shared) {
+        CKI(cudaMalloc(&ctx->idx_a, sizeof(int32_t) * A));
+        CKI(cudaMalloc(&ctx->w_a, sizeof(float) * A));
+    }
     CKI(cudaMalloc(&ctx->xq, M * ctx->H));
     CKI(cudaMalloc(&ctx->xds, sizeof(BlockScale) * M * (ctx->H / 32)));
     CKI(cudaMalloc(&ctx->plan_i, sizeof(int32_t) * (2 + 2 * U + A)));
@@ -508,7 +526,7 @@ int moe_layer_init(const moe_cfg *cfg, void *cuda_stream, moe_ctx **out) {
         ctx->cap_gu = ((ctx->F + 127) / 128) * (int)((A + moe::gemm_bn(true) - 1) / moe::gemm_bn(true) + U);
         ctx->cap_dn = ((ctx->H + 127) / 128) * (int)((A + moe::gemm_bn(false) - 1) / moe::gemm_bn(false) + U);
         CKI(cudaMalloc(&ctx->tile_rec, sizeof(uint2) * ((size_t)ctx->cap_gu + ctx->cap_dn)));
-        CKI(cudaMalloc(&ctx->etbl, sizeof(uint64_t) * 3 * E));
+        CKI(cudaMalloc(&ctx->etbl, sizeof(uint64_t) * 3 * Et));
         ctx->stage_cap = 3 * E;
         CKI(cudaMalloc(&ctx->stage_jobs, sizeof(uint64_t) * 2 * ctx->stage_cap));
         CKI(cudaMalloc(&ctx->stage_n, sizeof(int)));
@@ -540,9 +558,9 @@ int moe_layer_init(const moe_cfg *cfg, void *cuda_stream, moe_ctx **out) {
             CKI((cudaError_t)moe::fused_configure_rb(ctx->F, ctx->fused_smem_rb, &bps));
             ctx->fused_blocks_rb = bps * ctx->n_sm;
         }
-        if (ctx->fmt != moe::kFmtQ4) {
-            // the single-launch layer reads 4-bit codes: other formats take
-            // the mat-vec kernels
+        if (ctx->fmt != moe::kFmtQ4 || ctx->shared) {
+            // the single-launch layer reads 4-bit codes and routed experts
+            // only: other formats and shared experts take the mat-vec kernels
             ctx->fused_blocks = 0;
             ctx->fused_blocks_rb = 0;
         }
@@ -629,14 +647,41 @@ int register_expert_tensor(moe_ctx *ctx, int layer, int kind, const void *host_q
     }
     std::vector<int32_t> dslot(E);
     for (int e = 0; e < E; ++e) dslot[e] = stamp_index(ctx, tid, ts.slot_of[e]);
-    CK(cudaMemcpyAsync(ctx->d_tbl + (size_t)tid * E, ts.tbl.data(), sizeof(uint64_t) * E, cudaMemcpyHostToDevice,
-                       ctx->up));
-    CK(cudaMemcpyAsync(ctx->d_slot + (size_t)tid * E, dslot.data(), sizeof(int32_t) * E, cudaMemcpyHostToDevice,
+    CK(cudaMemcpyAsync(ctx->d_tbl + (size_t)tid * ctx->Et, ts.tbl.data(), sizeof(uint64_t) * E,
+                       cudaMemcpyHostToDevice, ctx->up));
+    CK(cudaMemcpyAsync(ctx->d_slot + (size_t)tid * ctx->Et, dslot.data(), sizeof(int32_t) * E, cudaMemcpyHostToDevice,
                        ctx->up));
     CK(cudaStreamSynchronize(ctx->up));
     ts.registered = true;
     ctx->stats.upload_bytes += (uint64_t)n_seed * ctx->blob;
     if (tensor_id) *tensor_id = tid;
+    return MOE_OK;
+}
+
+int register_shared_expert(moe_ctx *ctx, int layer, int kind, const void *host_w, int rows, int cols) {
+    if (!ctx) return fail(nullptr, MOE_ERR_ARG, "null ctx");
+    if (!ctx->shared) return fail(ctx, MOE_ERR_STATE, "shared expert: the context was made without shared_experts");
+    if (layer < 0 || layer >= ctx->cfg.n_layers || kind < 0 || kind > 2 || !host_w)
+        return fail(ctx, MOE_ERR_ARG, "bad layer/kind/pointer");
+    const int er = kind == MOE_KIND_DOWN ? ctx->H : ctx->F, ec = kind == MOE_KIND_DOWN ? ctx->F : ctx->H;
+    if (rows != er || cols != ec) return fail(ctx, MOE_ERR_ARG, "shared expert shape does not match cfg");
+    const int tid = layer * 3 + kind;
+    if (ctx->sh_blob[tid]) return fail(ctx, MOE_ERR_ARG, "shared expert already registered");
+    CK(cudaSetDevice(ctx->dev));
+    std::vector<uint8_t> blob(ctx->blob);
+    repack((const uint8_t *)host_w, blob.data(), ctx->fmt, 1, rows, cols / 32, ctx->blob);
+    uint8_t *d = nullptr;
+    CK(cudaMalloc(&d, ctx->stride));
+    cudaError_t e = cudaMemcpy(d, blob.data(), ctx->blob, cudaMemcpyHostToDevice);
+    const uint64_t entry = (uint64_t)(uintptr_t)d;
+    if (e == cudaSuccess)
+        e = cudaMemcpy(ctx->d_tbl + (size_t)tid * ctx->Et + ctx->E, &entry, sizeof(entry), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) {
+        cudaFree(d);
+        return fail(ctx, MOE_ERR_CUDA, std::string("shared expert upload: ") + cudaGetErrorString(e));
+    }
+    ctx->sh_blob[tid] = d;
+    ctx->stats.upload_bytes += ctx->blob;
     return MOE_OK;
 }
 
@@ -700,6 +745,18 @@ static int ffn_forward_body(moe_ctx *ctx, int layer, const float *d_x, int n_tok
     if (n_tokens == 0) return MOE_OK;
     if (!d_x || !d_idx || !d_w || !d_y) return fail(ctx, MOE_ERR_ARG, "forward: null pointer");
     cudaStream_t st = ctx->stream;
+    if (ctx->shared) {
+        // the layer's shared expert joins every token as assignment k (id E,
+        // weight 1); the routed ids are checked against E here
+        for (int kd = 0; kd < 3; ++kd)
+            if (!ctx->sh_blob[layer * 3 + kd])
+                return fail(ctx, MOE_ERR_STATE, "forward: shared expert of this layer not registered");
+        int rc0 = moe::launch_shared_assign(d_idx, d_w, n_tokens, ctx->k, ctx->E, ctx->idx_a, ctx->w_a, ctx->d_error,
+                                            st);
+        if (rc0) return fail(ctx, MOE_ERR_CUDA, "shared-expert assignment launch failed");
+        d_idx = ctx->idx_a;
+        d_w = ctx->w_a;
+    }
     const int T = n_tokens, H = ctx->H;
     const bool small = T <= 32;
     int rc = 0;
@@ -712,7 +769,7 @@ static int ffn_forward_body(moe_ctx *ctx, int layer, const float *d_x, int n_tok
     gp.cv.miss_count = ctx->d_misslog;
     gp.cv.clock = ctx->d_clock;
     gp.cv.cold_reads = ctx->d_cold;
-    gp.cv.E = ctx->E;
+    gp.cv.E = ctx->Et;
     gp.cv.slots_per_tensor = std::max(1, ctx->spt);
     gp.cv.bitmap_words = ctx->bitmap_words;
     gp.cv.miss_cap = ctx->miss_cap;
@@ -722,7 +779,7 @@ static int ffn_forward_body(moe_ctx *ctx, int layer, const float *d_x, int n_tok
     gp.tid_up = layer * 3 + 1;
     gp.tid_down = layer * 3 + 2;
     gp.n_tokens = T;
-    gp.k = ctx->k;
+    gp.k = ctx->ka;
     gp.H = H;
     gp.F = ctx->F;
     gp.xq = ctx->xq;
@@ -737,7 +794,7 @@ static int ffn_forward_body(moe_ctx *ctx, int layer, const float *d_x, int n_tok
     gp.counters = ctx->counters;
     gp.w = d_w;
     gp.y = d_y;
-    const int A = T * ctx->k, U = std::min(A, ctx->E);
+    const int A = T * ctx->ka, U = std::min(A, ctx->Et);
     gp.xq_out = ctx->xq;
     gp.xds_out = ctx->xds;
     gp.fmt = ctx->fmt;
@@ -793,8 +850,8 @@ static int ffn_forward_body(moe_ctx *ctx, int layer, const float *d_x, int n_tok
     pp.assign = p_assign(ctx);
     pp.error = ctx->d_error;
     pp.T = T;
-    pp.k = ctx->k;
-    pp.E = ctx->E;
+    pp.k = ctx->ka;
+    pp.E = ctx->Et;
     pp.H = H;
     pp.quantize_x = small ? 1 : 0;
     rc = moe::launch_plan(pp, st);
@@ -802,7 +859,7 @@ static int ffn_forward_body(moe_ctx *ctx, int layer, const float *d_x, int n_tok
 
     if (!small && ctx->gemm_ok) {
         // prefill: grouped tensor-core GEMM over tokens sorted by expert
-        const int Umax = std::min(ctx->M * ctx->k, ctx->E);
+        const int Umax = std::min(ctx->M * ctx->ka, ctx->Et);
         moe::PrefillLaunch L{};
         L.tiling.cv = gp.cv;
         L.tiling.n_uniq = gp.n_uniq;
@@ -827,7 +884,7 @@ static int ffn_forward_body(moe_ctx *ctx, int layer, const float *d_x, int n_tok
         g.assign = gp.assign;
         g.A = A;
         g.A_pad = ctx->A_pad;
-        g.k = ctx->k;
+        g.k = ctx->ka;
         g.F_out = ctx->F;
         g.error = ctx->d_error;
         L.gu = g;
@@ -835,14 +892,14 @@ static int ffn_forward_body(moe_ctx *ctx, int layer, const float *d_x, int n_tok
         L.gu.tile_rec = L.tiling.rec_gu;
         // with pool slots lent to this prompt pass, the layer's cold expert
         // tensors are staged there once and read from HBM by the GEMMs
-        const uint64_t *rows = ctx->d_tbl + (size_t)(layer * 3) * ctx->E;
+        const uint64_t *rows = ctx->d_tbl + (size_t)(layer * 3) * ctx->Et;
         const int pb = layer & 1;
         const bool prefetched = ctx->lookahead && ctx->pf_layer[pb] == layer;
         if (prefetched) {
             // this layer's cold experts were uploaded a layer ahead: read them
             // from the prefetch buffer (entries rebuilt from the live table)
             CK(cudaStreamWaitEvent(st, ctx->ev_pf[pb], 0));
-            rc = moe::launch_prefetch_table(rows, ctx->d_pfmap[pb], ctx->pf_buf[pb], ctx->pf_cap, ctx->stride, ctx->E,
+            rc = moe::launch_prefetch_table(rows, ctx->d_pfmap[pb], ctx->pf_buf[pb], ctx->pf_cap, ctx->stride, ctx->Et,
                                             ctx->etbl, st);
             if (rc) return fail(ctx, MOE_ERR_CUDA, "prefetch table launch failed");
             rows = ctx->etbl;
@@ -859,13 +916,13 @@ static int ffn_forward_body(moe_ctx *ctx, int layer, const float *d_x, int n_tok
             sp.slot_stride = ctx->stride;
             sp.n_slots = std::min(ctx->n_lent, ctx->stage_cap);
             sp.tid0 = layer * 3;
-            sp.E = ctx->E;
+            sp.E = ctx->Et;
             rc = moe::launch_stage(sp, ctx->blob, ctx->n_sm, st);
             if (rc) return fail(ctx, MOE_ERR_CUDA, "stage launch failed");
             rows = ctx->etbl;
         }
-        L.gu.tbl[0] = rows + 0 * (size_t)ctx->E;
-        L.gu.tbl[1] = rows + 1 * (size_t)ctx->E;
+        L.gu.tbl[0] = rows + 0 * (size_t)ctx->Et;
+        L.gu.tbl[1] = rows + 1 * (size_t)ctx->Et;
         L.gu.a_scaleT = ctx->xdT;
         L.gu.rows = ctx->F;
         L.gu.K = H;
@@ -876,7 +933,7 @@ static int ffn_forward_body(moe_ctx *ctx, int layer, const float *d_x, int n_tok
         L.dn = g;
         L.dn.tile_off = L.tiling.tile_off_dn;
         L.dn.tile_rec = L.tiling.rec_dn;
-        L.dn.tbl[0] = rows + 2 * (size_t)ctx->E;
+        L.dn.tbl[0] = rows + 2 * (size_t)ctx->Et;
         L.dn.tbl[1] = nullptr;
         L.dn.a_scaleT = ctx->hdT;
         L.dn.rows = H;
@@ -891,7 +948,7 @@ static int ffn_forward_body(moe_ctx *ctx, int layer, const float *d_x, int n_tok
         L.w = d_w;
         L.y = d_y;
         L.T = T;
-        L.k = ctx->k;
+        L.k = ctx->ka;
         L.H = H;
         L.n_sm = ctx->n_sm;
         rc = moe::launch_prefill(L, st);
@@ -1270,8 +1327,11 @@ int moe_cache_reset(moe_ctx *ctx, int global_pool) {
     ctx->g_owner.assign(ctx->global_pool ? G : 0, -1);
     ctx->g_pool.assign(ctx->global_pool ? G : 0, 0);
     ctx->g_lent.assign(ctx->global_pool ? G : 0, 0);
-    std::vector<uint64_t> tbl((size_t)nt * E, 0);
-    std::vector<int32_t> dslot((size_t)nt * E, -1);
+    const int Et = ctx->Et;
+    std::vector<uint64_t> tbl((size_t)nt * Et, 0);
+    std::vector<int32_t> dslot((size_t)nt * Et, -1);
+    for (int tid = 0; tid < nt; ++tid)
+        if (ctx->sh_blob[tid]) tbl[(size_t)tid * Et + E] = (uint64_t)(uintptr_t)ctx->sh_blob[tid];
     for (int tid = 0; tid < nt; ++tid) {
         TensorState &ts = ctx->t[tid];
         if (!ts.registered) continue;
@@ -1301,8 +1361,8 @@ int moe_cache_reset(moe_ctx *ctx, int global_pool) {
             }
         }
         for (int e = 0; e < E; ++e) {
-            tbl[(size_t)tid * E + e] = ts.tbl[e];
-            dslot[(size_t)tid * E + e] = stamp_index(ctx, tid, ts.slot_of[e]);
+            tbl[(size_t)tid * Et + e] = ts.tbl[e];
+            dslot[(size_t)tid * Et + e] = stamp_index(ctx, tid, ts.slot_of[e]);
         }
     }
     CK(cudaMemcpyAsync(ctx->d_tbl, tbl.data(), sizeof(uint64_t) * tbl.size(), cudaMemcpyHostToDevice, ctx->stream));
@@ -1379,8 +1439,8 @@ int moe_set_lookahead(moe_ctx *ctx, int enable) {
         ctx->pf_cap = cap;
     }
     for (int b = 0; b < 2; ++b) {
-        if (!ctx->d_pfmap[b]) CK(cudaMalloc(&ctx->d_pfmap[b], sizeof(int32_t) * 3 * ctx->E));
-        if (!ctx->h_pfmap[b]) CK(cudaHostAlloc(&ctx->h_pfmap[b], sizeof(int32_t) * 3 * ctx->E, cudaHostAllocDefault));
+        if (!ctx->d_pfmap[b]) CK(cudaMalloc(&ctx->d_pfmap[b], sizeof(int32_t) * 3 * ctx->Et));
+        if (!ctx->h_pfmap[b]) CK(cudaHostAlloc(&ctx->h_pfmap[b], sizeof(int32_t) * 3 * ctx->Et, cudaHostAllocDefault));
         if (!ctx->ev_pf[b]) CK(cudaEventCreateWithFlags(&ctx->ev_pf[b], cudaEventDisableTiming));
         if (!ctx->ev_pf_free[b]) CK(cudaEventCreateWithFlags(&ctx->ev_pf_free[b], cudaEventDisableTiming));
     }
@@ -1398,7 +1458,8 @@ int moe_cache_snapshot(moe_ctx *ctx, int tensor_id, uint64_t *tbl, int32_t *slot
     if (rc) return rc;
     const TensorState &ts = ctx->t[tensor_id];
     const int E = ctx->E;
-    if (tbl) CK(cudaMemcpy(tbl, ctx->d_tbl + (size_t)tensor_id * E, sizeof(uint64_t) * E, cudaMemcpyDeviceToHost));
+    if (tbl)
+        CK(cudaMemcpy(tbl, ctx->d_tbl + (size_t)tensor_id * ctx->Et, sizeof(uint64_t) * E, cudaMemcpyDeviceToHost));
     if (slot_of) memcpy(slot_of, ts.slot_of.data(), sizeof(int32_t) * E);
     if (last_seen) memcpy(last_seen, ts.last_seen.data(), sizeof(int32_t) * E);
     if (ctx->global_pool) {
@@ -1457,6 +1518,9 @@ void moe_destroy(moe_ctx *ctx) {
     cudaFree(ctx->d_slot);
     cudaFree(ctx->d_stamps);
     cudaFree(ctx->d_use);
+    cudaFree(ctx->idx_a);
+    cudaFree(ctx->w_a);
+    for (uint8_t *b : ctx->sh_blob) cudaFree(b);
     cudaFree(ctx->d_bitmap);
     cudaFree(ctx->d_stepbuf);
     cudaFree(ctx->d_clock);
@@ -1500,7 +1564,7 @@ int moe_debug_block_dots(moe_ctx *ctx, int tensor_id, int expert, int row0, int 
                          int32_t *d_out) {
     if (!ctx) return fail(nullptr, MOE_ERR_ARG, "null ctx");
     if (tensor_id < 0 || tensor_id >= ctx->n_tensors || !ctx->t[tensor_id].registered || expert < 0 ||
-        expert >= ctx->E || !d_qa || !d_out)
+        expert > ctx->E || (expert == ctx->E && !ctx->sh_blob[tensor_id]) || !d_qa || !d_out)
         return fail(ctx, MOE_ERR_ARG, "block_dots: bad arguments");
     const int kind = tensor_id % 3;
     const int rows = kind == 2 ? ctx->H : ctx->F, cols = kind == 2 ? ctx->F : ctx->H;
@@ -1508,7 +1572,8 @@ int moe_debug_block_dots(moe_ctx *ctx, int tensor_id, int expert, int row0, int 
     CK(cudaSetDevice(ctx->dev));
     int rc = sync_all(ctx);
     if (rc) return rc;
-    const uint8_t *blob = (const uint8_t *)(uintptr_t)(ctx->t[tensor_id].tbl[expert] & ~1ull);
+    const uint8_t *blob = expert == ctx->E ? ctx->sh_blob[tensor_id]
+                                           : (const uint8_t *)(uintptr_t)(ctx->t[tensor_id].tbl[expert] & ~1ull);
     rc = moe::launch_block_dots(blob, ctx->fmt, rows, cols / 32, row0, n_rows, d_qa, d_out, ctx->stream);
     if (rc) return fail(ctx, MOE_ERR_CUDA, "block_dots launch failed");
     CK(cudaStreamSynchronize(ctx->stream));
@@ -1520,7 +1585,7 @@ int moe_debug_read(moe_ctx *ctx, int what, void *host_out, size_t bytes) {
     if (ctx->last_T < 0) return fail(ctx, MOE_ERR_STATE, "debug_read: no forward yet");
     CK(cudaSetDevice(ctx->dev));
     CK(cudaStreamSynchronize(ctx->stream));
-    const size_t T = ctx->last_T, A = T * ctx->k;
+    const size_t T = ctx->last_T, A = T * ctx->ka;
     size_t need = 0;
     switch (what) {
         case 0: need = T * ctx->H; break;

@@ -83,7 +83,7 @@ class Model:
 
     def __init__(self, H, F, E, k, L, capacity, max_tokens, seed=0, routing="zipf", zipf_s=1.1, window=64,
                  slots_per_tensor=None, max_swaps=0, stream=None, global_pool=False, preheat=False,
-                 weight_format=0):
+                 weight_format=0, shared=False):
         import torch
         self.torch = torch
         self.wl = synth.Workload("test", H, E, k, F, L, routing=routing, zipf_s=zipf_s, seed=seed,
@@ -95,7 +95,19 @@ class Model:
         if stream is None:
             stream = torch.cuda.current_stream().cuda_stream
         self.ctx = qec.moe_layer_init(H, F, E, k, L, self.spt, max_tokens, window_tokens=window,
-                                      max_swaps_per_step=max_swaps, stream=stream, weight_format=weight_format)
+                                      max_swaps_per_step=max_swaps, stream=stream, weight_format=weight_format,
+                                      shared_experts=int(shared))
+        self.shared = None
+        if shared:
+            # one shared expert per layer, from its own seeded stream
+            sw = synth.Workload("shared", H, 1, 1, F, L, seed=seed + 101, weight_format=weight_format)
+            self.shared = {}
+            for layer in range(L):
+                for kind in range(3):
+                    t = sw.expert_tensor(layer, kind)[0]
+                    rows, cols = sw.tensor_shapes[kind]
+                    qec.register_shared_expert(self.ctx, layer, kind, t, rows, cols)
+                    self.shared[(layer, kind)] = t
         self.tensors = {}
         self.global_pool = global_pool
         if global_pool:
@@ -159,8 +171,13 @@ class Model:
         qec.moe_ffn_forward(self.ctx, layer, x, T, idx, w, y)
         return y
 
+    @property
+    def ka(self):
+        """Assignments per token (the routed k, plus the shared expert)."""
+        return self.k + (1 if getattr(self, "shared", None) else 0)
+
     def read_debug(self, T):
-        H, F, k = self.H, self.F, self.k
+        H, F, k = self.H, self.F, self.ka
         xq = np.empty((T, H), np.int8)
         xd = np.empty((T, H // 32), np.uint16)
         hq = np.empty((T * k, F), np.int8)
@@ -193,6 +210,11 @@ def check_layer_parity(m: Model, layer, x_np, logits_np, y_gpu, idx_gpu, w_gpu):
     g = {e: m.tensor(layer, 0)[e] for e in used}
     u = {e: m.tensor(layer, 1)[e] for e in used}
     d = {e: m.tensor(layer, 2)[e] for e in used}
+    if getattr(m, "shared", None):
+        idx_o, w_o, g, u, d = oracle.with_shared(idx_o, w_o, g, u, d,
+                                                 tuple(m.shared[(layer, kd)] for kd in range(3)), e_shared=m.E)
+        # the shared expert is id E (one past the routed ids)
+        assert (idx_o[:, -1] == m.E).all()
     y_o, it = oracle.layer(x_np, idx_o, w_o, g, u, d, m.H, m.F, want_intermediates=True)
     xq, xd, hq, hd = m.read_debug(T)
     assert np.array_equal(xq, it["xq"]), "quantized x codes differ"
