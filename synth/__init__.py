@@ -281,6 +281,10 @@ WORKLOADS = {
     "decode_b1_q5_resident16": Workload("decode_b1_q5_resident16", 2048, 512, 8, 1152, 16, routing="zipf",
                                         zipf_s=1.1, capacity=[512] * 16, phases=[("decode", 1, 64)],
                                         weight_format=FMT_Q5_0),
+    # Q4 weights with a shared expert per layer: the same 16 resident layers
+    "decode_b1_shared_resident16": Workload("decode_b1_shared_resident16", 2048, 512, 8, 1152, 16,
+                                            routing="zipf", zipf_s=1.1, capacity=[512] * 16,
+                                            phases=[("decode", 1, 64)]),
     "prefill_t4096": Workload("prefill_t4096", 2048, 512, 8, 1152, 48, routing="zipf", zipf_s=1.1,
                               capacity=[384] * 48, phases=[("prefill", 4096, 1)]),
     "large_expert": Workload("large_expert", 2880, 128, 4, 2880, 36, routing="mix", zipf_s=0.8,
