@@ -5,7 +5,7 @@ with a quantized expert cache, used to check the CUDA path.  Only the tests,
 ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline leg may import
 it.  It shares no code with the CUDA library, and the library never calls it.
 
-- ``moe_oracle.c``: numerics (top-k, activation quantization, Q4, Q8_0 and Q5_0 block dots,
+- ``moe_oracle.c``: numerics (top-k, activation quantization, Q4, Q8_0, Q5_0 and Q4_K block dots,
   SwiGLU, down projection and combine), binary64 with the integer-deciding
   steps in binary32 (see the header of that file);
 - ``policy.py``: the admission / eviction policy of the expert pools.
@@ -60,6 +60,7 @@ def lib():
         L.orc_block_dot_fmt.argtypes = [vp, vp, i32]
         L.orc_row_dot_fmt.restype = ctypes.c_double
         L.orc_row_dot_fmt.argtypes = [vp, vp, vp, i32, i32, vp]
+        L.orc_k4_subdots.argtypes = [vp, vp, vp]
         L.orc_expert.argtypes = [vp, vp, vp, i32, i32, vp, vp] + [vp] * 8 + [i32]
         L.orc_down_combine.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, i32]
         L.orc_layer.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp] + [vp] * 9 + [i32]
@@ -101,11 +102,13 @@ def quantize(x: np.ndarray):
     return q, d
 
 
-BLOCK_BYTES = {18: 0, 34: 1, 22: 2}  # canonical block size -> format (0: Q4, 1: Q8_0, 2: Q5_0)
+BLOCK_BYTES = {18: 0, 34: 1, 22: 2, 144: 3}  # canonical block size -> format (0: Q4, 1: Q8_0, 2: Q5_0, 3: Q4_K)
+ELEMS = {0: 32, 1: 32, 2: 32, 3: 256}        # weights per canonical block
 
 
 def _fmt(blocks) -> int:
-    """Format of canonical blocks from their last dimension (18: Q4, 34: Q8_0, 22: Q5_0)."""
+    """Format of canonical blocks from their last dimension (18: Q4, 34: Q8_0, 22: Q5_0,
+    144: Q4_K super-blocks of 256 weights)."""
     if blocks.shape[-1] not in BLOCK_BYTES:
         raise ValueError(f"unknown block size {blocks.shape[-1]}")
     return BLOCK_BYTES[blocks.shape[-1]]
@@ -114,9 +117,20 @@ def _fmt(blocks) -> int:
 def dequant(blocks: np.ndarray) -> np.ndarray:
     """Canonical blocks [..., nb, 18 (Q4), 34 (Q8_0) or 22 (Q5_0)] -> float64 [..., nb*32]."""
     blocks = np.ascontiguousarray(blocks, np.uint8)
-    nb = blocks.size // blocks.shape[-1]
-    out = np.empty(blocks.shape[:-2] + (blocks.shape[-2] * 32,), np.float64)
-    lib().orc_dequant_fmt(_p(blocks), nb, _fmt(blocks), _p(out))
+    f = _fmt(blocks)
+    n32 = blocks.size // blocks.shape[-1] * (ELEMS[f] // 32)
+    out = np.empty(blocks.shape[:-2] + (blocks.shape[-2] * ELEMS[f],), np.float64)
+    lib().orc_dequant_fmt(_p(blocks), n32, f, _p(out))
+    return out
+
+
+def subblock_dots(superblock: np.ndarray, qa: np.ndarray) -> np.ndarray:
+    """Q4_K: raw integer dots sum q*a of the 8 sub-blocks of one super-block."""
+    sb = np.ascontiguousarray(superblock, np.uint8)
+    assert sb.size == 144 and qa.size == 256
+    qa = np.ascontiguousarray(qa, np.int8)
+    out = np.empty(8, np.int32)
+    lib().orc_k4_subdots(_p(sb), _p(qa), _p(out))
     return out
 
 
@@ -131,7 +145,8 @@ def row_dot(row: np.ndarray, qa: np.ndarray, da: np.ndarray):
     qa = np.ascontiguousarray(qa, np.int8)
     da = np.ascontiguousarray(da, np.uint16)
     a = np.zeros(1, np.float64)
-    r = lib().orc_row_dot_fmt(_p(row), _p(qa), _p(da), row.size // row.shape[-1], _fmt(row), _p(a))
+    f = _fmt(row)
+    r = lib().orc_row_dot_fmt(_p(row), _p(qa), _p(da), row.size // row.shape[-1] * (ELEMS[f] // 32), f, _p(a))
     return float(r), float(a[0])
 
 

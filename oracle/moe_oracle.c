@@ -28,7 +28,16 @@
  *  of 32 with one binary16 scale d and 5-bit codes q, w = d * (q - 16); the
  *  reading of the layout is d, then 4 bytes of high bits (bit j of the
  *  little-endian word = bit 4 of element j), then 16 bytes of low nibbles in
- *  the Q4 order (22 bytes).
+ *  the Q4 order (22 bytes).  3 = Q4_K, one of the K-quant formats those
+ *  kernels accept: super-blocks of 256 weights = 8 sub-blocks of 32 with a
+ *  binary16 scale d and min scale dmin per super-block, a 6-bit scale sc_j
+ *  and 6-bit min m_j per sub-block and 4-bit codes q, w = d*sc_j*q - dmin*m_j.
+ *  Reading of the 144-byte layout: d, dmin, 12 bytes of packed (sc, m) (for
+ *  j < 4: sc = b[j] & 63, m = b[j+4] & 63; for j >= 4: sc = (b[j+4] & 15) |
+ *  (b[j-4] >> 6) << 4, m = (b[j+4] >> 4) | (b[j] >> 6) << 4), then 128 code
+ *  bytes in 4 chunks of 32: chunk c holds sub-block 2c in its low nibbles and
+ *  sub-block 2c+1 in its high nibbles (byte i of a chunk = element i of each).
+ *  Per 32 weights that is 18 bytes, as for Q4.
  *
  * Readings where the pages are silent (each listed in the design notes):
  *  - top-k order is (logit descending, expert index ascending): ties go to
@@ -57,8 +66,40 @@
 #define ORC_Q8_BLOCK_BYTES 34
 #define ORC_Q5_BLOCK_BYTES 22
 
+#define ORC_K4_SUPER_BYTES 144
+
+/* Bytes per 32 weights (Q4_K: a 144-byte super-block holds 256). */
 static size_t orc_bbytes(int fmt) {
     return fmt == 1 ? ORC_Q8_BLOCK_BYTES : fmt == 2 ? ORC_Q5_BLOCK_BYTES : ORC_BLOCK_BYTES;
+}
+
+/* Q4_K: scale and min of sub-block j (0..7) of a super-block. */
+static void orc_k4_scale_min(const uint8_t *sb, int j, int *sc, int *m) {
+    const uint8_t *b = sb + 4;
+    if (j < 4) {
+        *sc = b[j] & 63;
+        *m = b[j + 4] & 63;
+    } else {
+        *sc = (b[j + 4] & 15) | ((b[j - 4] >> 6) << 4);
+        *m = (b[j + 4] >> 4) | ((b[j] >> 6) << 4);
+    }
+}
+
+/* Q4_K: 4-bit code of element i (0..255) of a super-block. */
+static int orc_k4_code(const uint8_t *sb, int i) {
+    const uint8_t *qs = sb + 16;
+    const int c = i / 64, r = i % 64;
+    return r < 32 ? (qs[32 * c + r] & 15) : (qs[32 * c + r - 32] >> 4);
+}
+
+/* Q4_K: raw integer dots sum_i q_i * a_i of the 8 sub-blocks against 256
+ * int8 activations (exact in int32: |sum| <= 32 * 15 * 127). */
+void orc_k4_subdots(const uint8_t *sb, const int8_t *qa, int32_t *out) {
+    for (int j = 0; j < 8; ++j) {
+        int32_t s = 0;
+        for (int i = 0; i < 32; ++i) s += (int32_t)orc_k4_code(sb, 32 * j + i) * (int32_t)qa[32 * j + i];
+        out[j] = s;
+    }
 }
 
 /* ---- binary16 <-> binary64/32 from the IEEE 754 definition ------------- */
@@ -191,6 +232,18 @@ static uint16_t orc_block_scale(const uint8_t *blk) { return (uint16_t)(blk[0] |
 /* Dequantized weights of nb blocks: w = d * (q - 8) (Q4), d * q (Q8_0) or
  * d * (q - 16) (Q5_0). */
 void orc_dequant_fmt(const uint8_t *blocks, int nb, int fmt, double *out) {
+    if (fmt == 3) { /* nb counts 32-weight blocks; super-blocks of 8 */
+        for (int s = 0; s < nb / 8; ++s) {
+            const uint8_t *sb = blocks + (size_t)s * ORC_K4_SUPER_BYTES;
+            const double d = orc_h2d(orc_block_scale(sb)), dmin = orc_h2d(orc_block_scale(sb + 2));
+            for (int i = 0; i < 256; ++i) {
+                int sc, m;
+                orc_k4_scale_min(sb, i / 32, &sc, &m);
+                out[(size_t)s * 256 + i] = d * sc * (double)orc_k4_code(sb, i) - dmin * m;
+            }
+        }
+        return;
+    }
     for (int b = 0; b < nb; ++b) {
         const uint8_t *blk = blocks + (size_t)b * orc_bbytes(fmt);
         double d = orc_h2d(orc_block_scale(blk));
@@ -216,6 +269,28 @@ int32_t orc_block_dot(const uint8_t *blk, const int8_t *qa) { return orc_block_d
  * sum_b |d_w,b * d_a,b * sumi_b| (for error bounds), if not NULL. */
 double orc_row_dot_fmt(const uint8_t *row, const int8_t *qa, const uint16_t *da, int nb, int fmt, double *abs_sum) {
     double acc = 0.0, aacc = 0.0;
+    if (fmt == 3) {
+        /* per sub-block b: d_a,b * (d * sc * sum q*a - dmin * m * sum a) */
+        for (int s = 0; s < nb / 8; ++s) {
+            const uint8_t *sb = row + (size_t)s * ORC_K4_SUPER_BYTES;
+            const double d = orc_h2d(orc_block_scale(sb)), dmin = orc_h2d(orc_block_scale(sb + 2));
+            int32_t raw[8];
+            orc_k4_subdots(sb, qa + (size_t)s * 256, raw);
+            for (int j = 0; j < 8; ++j) {
+                const int b = 8 * s + j;
+                int sc, m;
+                orc_k4_scale_min(sb, j, &sc, &m);
+                int32_t asum = 0;
+                for (int i = 0; i < 32; ++i) asum += qa[(size_t)b * 32 + i];
+                const double da_b = orc_h2d(da[b]);
+                const double p1 = d * sc * (double)raw[j], p2 = dmin * m * (double)asum;
+                acc += da_b * (p1 - p2);
+                aacc += fabs(da_b) * (fabs(p1) + fabs(p2));
+            }
+        }
+        if (abs_sum) *abs_sum = aacc;
+        return acc;
+    }
     for (int b = 0; b < nb; ++b) {
         const uint8_t *blk = row + (size_t)b * orc_bbytes(fmt);
         int32_t s = orc_block_dot_fmt(blk, qa + (size_t)b * ORC_BLOCK, fmt);

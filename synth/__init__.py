@@ -33,11 +33,15 @@ KIND_GATE, KIND_UP, KIND_DOWN = 0, 1, 2
 Q4_BLOCK_BYTES = 18
 Q8_BLOCK_BYTES = 34
 Q5_BLOCK_BYTES = 22
-FMT_Q4, FMT_Q8_0, FMT_Q5_0 = 0, 1, 2
-BLOCK_BYTES = {FMT_Q4: Q4_BLOCK_BYTES, FMT_Q8_0: Q8_BLOCK_BYTES, FMT_Q5_0: Q5_BLOCK_BYTES}
+Q4K_BLOCK_BYTES = 144  # one super-block of 256 weights
+FMT_Q4, FMT_Q8_0, FMT_Q5_0, FMT_Q4_K = 0, 1, 2, 3
+BLOCK_BYTES = {FMT_Q4: Q4_BLOCK_BYTES, FMT_Q8_0: Q8_BLOCK_BYTES, FMT_Q5_0: Q5_BLOCK_BYTES,
+               FMT_Q4_K: Q4K_BLOCK_BYTES}
+BLOCK_ELEMS = {FMT_Q4: 32, FMT_Q8_0: 32, FMT_Q5_0: 32, FMT_Q4_K: 256}
 # scale ranges: |w| <= 0.16 in every format (|q - 8| <= 8 for Q4, |q| <= 127
-# for Q8_0, |q - 16| <= 16 for Q5_0)
-D_RANGE = {FMT_Q4: (0.005, 0.02), FMT_Q8_0: (0.005 / 16, 0.02 / 16), FMT_Q5_0: (0.0025, 0.01)}
+# for Q8_0, |q - 16| <= 16 for Q5_0; Q4_K: d * 63 * 15 and dmin * 63 <= 0.16)
+D_RANGE = {FMT_Q4: (0.005, 0.02), FMT_Q8_0: (0.005 / 16, 0.02 / 16), FMT_Q5_0: (0.0025, 0.01),
+           FMT_Q4_K: (0.0000625, 0.00017)}
 
 
 def build(force: bool = False) -> str:
@@ -68,6 +72,7 @@ def lib():
         L.synth_q4_experts.argtypes = [u64, u64, i32, i32, sz, vp, dbl, dbl, i32]
         L.synth_q8_blocks.argtypes = [u64, vp, sz, dbl, dbl]
         L.synth_q5_blocks.argtypes = [u64, vp, sz, dbl, dbl]
+        L.synth_q4k_blocks.argtypes = [u64, vp, sz, dbl, dbl, dbl, dbl]
         L.synth_experts.argtypes = [u64, u64, i32, i32, sz, vp, dbl, dbl, i32, i32]
         L.synth_permutation.argtypes = [u64, vp, i32]
         L.synth_gumbel_logits.argtypes = [u64, vp, i32, i32, vp]
@@ -116,6 +121,13 @@ def q5_blocks(k: int, n_blocks: int, dlo: float = D_RANGE[FMT_Q5_0][0],
     return out
 
 
+def q4k_blocks(k: int, n_super: int, dlo: float = D_RANGE[FMT_Q4_K][0], dhi: float = D_RANGE[FMT_Q4_K][1],
+               mlo: float = 0.0006, mhi: float = 0.0025) -> np.ndarray:
+    out = np.empty((n_super, Q4K_BLOCK_BYTES), np.uint8)
+    lib().synth_q4k_blocks(k, _ptr(out), n_super, dlo, dhi, mlo, mhi)
+    return out
+
+
 def q4_experts(seed: int, tensor_tag: int, e_begin: int, e_end: int, rows: int, cols: int,
                out: np.ndarray | None = None, dlo: float | None = None, dhi: float | None = None,
                threads: int | None = None, fmt: int = FMT_Q4) -> np.ndarray:
@@ -125,14 +137,14 @@ def q4_experts(seed: int, tensor_tag: int, e_begin: int, e_end: int, rows: int, 
     Shape [n, rows, cols/32, 18, 34 or 22] uint8; expert e's bytes do not depend
     on the range it was generated in, nor on the thread count.
     """
-    assert cols % 32 == 0
-    bb = BLOCK_BYTES[fmt]
+    bb, per = BLOCK_BYTES[fmt], BLOCK_ELEMS[fmt]
+    assert cols % per == 0
     dlo = D_RANGE[fmt][0] if dlo is None else dlo
     dhi = D_RANGE[fmt][1] if dhi is None else dhi
     n = e_end - e_begin
-    nbe = rows * (cols // 32)
+    nbe = rows * (cols // per)
     if out is None:
-        out = np.empty((n, rows, cols // 32, bb), np.uint8)
+        out = np.empty((n, rows, cols // per, bb), np.uint8)
     assert out.nbytes == n * nbe * bb and out.flags["C_CONTIGUOUS"]
     if threads is None:
         threads = max(1, min(16, os.cpu_count() or 1))
@@ -252,7 +264,7 @@ class Workload:
 
     def tensor_bytes(self, kind: int) -> int:
         rows, cols = self.tensor_shapes[kind]
-        return rows * (cols // 32) * BLOCK_BYTES[self.weight_format]
+        return rows * (cols // BLOCK_ELEMS[self.weight_format]) * BLOCK_BYTES[self.weight_format]
 
 
 def _c1_capacity(L=48, E=512):

@@ -186,6 +186,30 @@ void synth_q5_blocks(uint64_t key, uint8_t *out, size_t n_blocks, double dlo, do
     }
 }
 
+/*
+ * Canonical Q4_K super-blocks of 256 weights, 144 bytes each: binary16
+ * d ~ U(dlo, dhi) and dmin ~ U(mlo, mhi) (rounded to binary16), then 140
+ * uniform bytes (12 bytes of packed 6-bit sub-block scales and mins, every
+ * pattern valid and every 6-bit value equally likely, and 128 code bytes).
+ */
+void synth_q4k_blocks(uint64_t key, uint8_t *out, size_t n_super, double dlo, double dhi, double mlo, double mhi) {
+    xo_t g;
+    xo_init(&g, key);
+    for (size_t b = 0; b < n_super; ++b) {
+        uint8_t *sb = out + b * 144;
+        uint16_t h = gen_f16_bits((float)(dlo + (dhi - dlo) * xo_unit(&g)));
+        uint16_t hm = gen_f16_bits((float)(mlo + (mhi - mlo) * xo_unit(&g)));
+        sb[0] = (uint8_t)(h & 0xff);
+        sb[1] = (uint8_t)(h >> 8);
+        sb[2] = (uint8_t)(hm & 0xff);
+        sb[3] = (uint8_t)(hm >> 8);
+        for (int w = 0; w < 140; w += 4) {
+            uint64_t v = xo_next(&g);
+            for (int j = 0; j < 4; ++j) sb[4 + w + j] = (uint8_t)(v >> (8 * j));
+        }
+    }
+}
+
 typedef struct {
     uint64_t seed, tag;
     int e0, e1, fmt;
@@ -196,11 +220,13 @@ typedef struct {
 
 static void *q4_worker(void *arg) {
     q4_job_t *j = (q4_job_t *)arg;
-    const size_t bb = j->fmt == 1 ? 34 : j->fmt == 2 ? 22 : 18;
+    const size_t bb = j->fmt == 1 ? 34 : j->fmt == 2 ? 22 : j->fmt == 3 ? 144 : 18;
     for (int e = j->e0; e < j->e1; ++e) {
         uint64_t key = synth_key(j->seed, 1, j->tag, (uint64_t)e, 0);
         uint8_t *dst = j->out + (size_t)e * j->blocks_per_expert * bb;
-        if (j->fmt == 1)
+        if (j->fmt == 3)
+            synth_q4k_blocks(key, dst, j->blocks_per_expert, j->dlo, j->dhi, 0.0006, 0.0025);
+        else if (j->fmt == 1)
             synth_q8_blocks(key, dst, j->blocks_per_expert, j->dlo, j->dhi);
         else if (j->fmt == 2)
             synth_q5_blocks(key, dst, j->blocks_per_expert, j->dlo, j->dhi);
@@ -212,14 +238,15 @@ static void *q4_worker(void *arg) {
 
 /*
  * All experts of one expert tensor, expert-major: out[e][block] (18 B each
- * for Q4, fmt 0; 34 B for Q8_0, fmt 1; 22 B for Q5_0, fmt 2).
+ * for Q4, fmt 0; 34 B for Q8_0, fmt 1; 22 B for Q5_0, fmt 2; 144-byte
+ * super-blocks of 256 weights for Q4_K, fmt 3, with dmin ~ U(0.0006, 0.0025)).
  * Expert e is drawn from its own stream keyed by (seed, 1, tensor_tag, e), so
  * the result does not depend on n_threads and any expert can be regenerated
  * alone with synth_experts(seed, tag, e, e+1, ...).
  */
 void synth_experts(uint64_t seed, uint64_t tensor_tag, int e_begin, int e_end, size_t blocks_per_expert,
                    uint8_t *out, double dlo, double dhi, int n_threads, int fmt) {
-    const size_t bb = fmt == 1 ? 34 : fmt == 2 ? 22 : 18;
+    const size_t bb = fmt == 1 ? 34 : fmt == 2 ? 22 : fmt == 3 ? 144 : 18;
     int n = e_end - e_begin;
     if (n <= 0) return;
     if (n_threads < 1) n_threads = 1;

@@ -486,3 +486,84 @@ def test_shared_expert_layer_vs_dense_fp64():
         o = Sd @ (hq.astype(np.float64) * np.repeat(hd.view(np.float16).astype(np.float64), 32))
         # y = (routed sum) + o_shared: the routed part is the plain layer
         np.testing.assert_allclose(y[t], y0[t] + o, rtol=1e-12, atol=1e-12 * np.abs(o).max())
+
+
+# ---------------------------------------------------------------- Q4_K weights
+def _np_dequant_q4k(sb):
+    """Independent Q4_K decode with numpy: [..., 144] super-blocks -> codes
+    [..., 256], per-sub-block scales and mins [..., 8], d and dmin."""
+    sb = np.asarray(sb, np.uint8)
+    d = np.ascontiguousarray(sb[..., 0:2]).view(np.float16)[..., 0].astype(np.float64)
+    dmin = np.ascontiguousarray(sb[..., 2:4]).view(np.float16)[..., 0].astype(np.float64)
+    b = sb[..., 4:16].astype(np.int64)
+    sc = np.concatenate([b[..., 0:4] & 63, (b[..., 8:12] & 15) | ((b[..., 0:4] >> 6) << 4)], axis=-1)
+    mn = np.concatenate([b[..., 4:8] & 63, (b[..., 8:12] >> 4) | ((b[..., 4:8] >> 6) << 4)], axis=-1)
+    qs = sb[..., 16:144].astype(np.int64).reshape(sb.shape[:-1] + (4, 32))
+    codes = np.stack([qs & 15, qs >> 4], axis=-2).reshape(sb.shape[:-1] + (256,))
+    return codes, sc, mn, d, dmin
+
+
+def _q4k_weights(sb):
+    codes, sc, mn, d, dmin = _np_dequant_q4k(sb)
+    scale = np.repeat(d[..., None] * sc, 32, axis=-1)
+    mins = np.repeat(dmin[..., None] * mn, 32, axis=-1)
+    return scale * codes - mins
+
+
+def test_q4k_golden(golden):
+    (d, dmin, scales, codes, over, dots, weights), = golden("q4k_superblock.txt")
+    sb = np.zeros(144, np.uint8)
+    sb[0:2] = np.array([int(d, 16) & 0xFF, int(d, 16) >> 8], np.uint8)  # little endian
+    sb[2:4] = np.array([int(dmin, 16) & 0xFF, int(dmin, 16) >> 8], np.uint8)
+    sb[4:16] = np.frombuffer(bytes.fromhex(scales.replace(" ", "")), np.uint8)
+    hexs = "".join(h * int(n) for h, n in (t.split("*") for t in codes.split()))
+    sb[16:] = np.frombuffer(bytes.fromhex(hexs), np.uint8)
+    a = np.ones(256, np.int8)
+    for kv in over.split(","):
+        i, v = kv.split("=")
+        a[int(i)] = int(v)
+    assert oracle.subblock_dots(sb, a).tolist() == [int(v) for v in dots.split(",")]
+    w = oracle.dequant(sb.reshape(1, 144))
+    for kv in weights.split(","):
+        i, v = kv.split("=")
+        assert w[int(i)] == float(v)
+
+
+def test_q4k_brute_force_vs_independent_decode():
+    sbs = synth.q4k_blocks(synth.key(7, 400), 60)
+    codes, *_ = _np_dequant_q4k(sbs)
+    acts = RNG.integers(-127, 128, (60, 256)).astype(np.int8)
+    for i in range(60):
+        ref = (codes[i].reshape(8, 32) * acts[i].astype(np.int64).reshape(8, 32)).sum(axis=1)
+        assert np.array_equal(oracle.subblock_dots(sbs[i], acts[i]), ref)
+    assert np.array_equal(oracle.dequant(sbs.reshape(3, 20, 144)), _q4k_weights(sbs).reshape(3, 20 * 256))
+    _, sc, mn, _, _ = _np_dequant_q4k(sbs)
+    assert sc.min() == 0 and sc.max() == 63 and mn.min() == 0 and mn.max() == 63
+
+
+def test_q4k_layer_vs_dense_fp64():
+    wl = synth.Workload("tiny_q4k", 512, 8, 2, 256, 1, routing="normal", weight_format=synth.FMT_Q4_K)
+    H, F, k, T = wl.hidden, wl.ffn, wl.top_k, 3
+    gate, up, down = (wl.expert_tensor(0, kd) for kd in range(3))
+    assert gate.shape == (8, F, H // 256, 144) and down.shape == (8, H, F // 256, 144)
+    x, logits = wl.x(0, 0, T), wl.logits(0, 0, T)
+    idx, w = oracle.topk(logits, k)
+    y, it = oracle.layer(x, idx, w, gate, up, down, H, F, want_intermediates=True)
+
+    def deq(t):
+        return _q4k_weights(t).reshape(t.shape[0], t.shape[1], -1)
+
+    Wg, Wu, Wd = deq(gate), deq(up), deq(down)
+    xa = it["xq"].astype(np.float64) * np.repeat(it["xd"].view(np.float16).astype(np.float64), 32, axis=1)
+    y_bf = np.zeros((T, H))
+    for t in range(T):
+        for j in range(k):
+            a, e = t * k + j, idx[t, j]
+            g, u = Wg[e] @ xa[t], Wu[e] @ xa[t]
+            np.testing.assert_allclose(it["g"][a], g, rtol=0, atol=1e-12 * np.abs(g).max())
+            h = g * u * expit(g)
+            hq, hd = oracle.quantize(h.astype(np.float32))
+            assert np.array_equal(hq, it["hq"][a]) and np.array_equal(hd, it["hd"][a])
+            ha = hq.astype(np.float64) * np.repeat(hd.view(np.float16).astype(np.float64), 32)
+            y_bf[t] += w[t, j] * (Wd[e] @ ha)
+    np.testing.assert_allclose(y, y_bf, rtol=1e-12, atol=1e-12 * np.abs(y_bf).max())
