@@ -170,7 +170,8 @@ def register_workload(qec, synth, ctx, wl, log):
             rows, cols = wl.tensor_shapes[kind]
             key = (rows, cols)
             if key not in bufs:
-                bufs[key] = np.empty((wl.n_experts, rows, cols // 32, synth.BLOCK_BYTES[wl.weight_format]),
+                bufs[key] = np.empty((wl.n_experts, rows, cols // synth.BLOCK_ELEMS[wl.weight_format],
+                                      synth.BLOCK_BYTES[wl.weight_format]),
                                      np.uint8)
             wl.expert_tensor(layer, kind, out=bufs[key])
             qec.register_expert_tensor(ctx, layer, kind, bufs[key], rows, cols, cap, order, cap)
@@ -412,6 +413,7 @@ def run_ours(args):
     if args.q8_steps > 0:
         out["formats"] = {"q8_0": run_format_leg(args, qec, synth, torch, log, "decode_b1_q8_resident16"),
                           "q5_0": run_format_leg(args, qec, synth, torch, log, "decode_b1_q5_resident16"),
+                          "q4_k": run_format_leg(args, qec, synth, torch, log, "decode_b1_q4k_resident16"),
                           "q4_shared_expert": run_format_leg(args, qec, synth, torch, log,
                                                              "decode_b1_shared_resident16", shared=True)}
     if rank == 0:
@@ -563,7 +565,8 @@ def run_format_leg(args, qec, synth, torch, log, name, shared=False):
     shared expert counts as one more) + x and y, over the step time."""
     wl = synth.WORKLOADS[name]
     L, H, E, k, F = wl.n_layers, wl.hidden, wl.n_experts, wl.top_k, wl.ffn
-    fmt_name = {synth.FMT_Q4: "Q4", synth.FMT_Q8_0: "Q8_0", synth.FMT_Q5_0: "Q5_0"}[wl.weight_format]
+    fmt_name = {synth.FMT_Q4: "Q4", synth.FMT_Q8_0: "Q8_0", synth.FMT_Q5_0: "Q5_0",
+                synth.FMT_Q4_K: "Q4_K"}[wl.weight_format]
     T = 1
     stream = torch.cuda.Stream()
     sp = stream.cuda_stream
@@ -624,7 +627,8 @@ def run_format_leg(args, qec, synth, torch, log, name, shared=False):
         f"layer, {gbs:.0f} GB/s")
     return {"workload": f"{wl.name}: {L} layers, hidden {H}, {E} experts, top-{k}"
                         f"{' + 1 shared expert' if shared else ''}, FFN {F}, {fmt_name} blocks of 32 "
-                        f"({synth.BLOCK_BYTES[wl.weight_format]} B), every expert resident, batch-1 decode, {n} timed "
+                        f"({synth.BLOCK_BYTES[wl.weight_format]} B per {synth.BLOCK_ELEMS[wl.weight_format]}), "
+                        f"every expert resident, batch-1 decode, {n} timed "
                         f"steps in a CUDA graph",
             "tokens_per_s": round(T / (ms * 1e-3), 1), "us_per_layer": round(ms * 1e3 / L, 3),
             "roofline": {"bound": "hbm",

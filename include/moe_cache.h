@@ -69,7 +69,7 @@ typedef struct moe_cfg {
     int32_t renorm_topk;        /* 1: weights = softmax over the k selected */
     int32_t poll_timeout_ms;    /* host poll limit in cache_step (0 = 10 s) */
     int32_t device;             /* CUDA device ordinal */
-    int32_t weight_format;      /* MOE_FMT_Q4_0 (0), MOE_FMT_Q8_0 (1) or MOE_FMT_Q5_0 (2), every tensor */
+    int32_t weight_format;      /* MOE_FMT_Q4_0 (0), _Q8_0 (1), _Q5_0 (2) or _Q4_K (3), every tensor */
     int32_t shared_experts;     /* 1: every layer has one shared expert (register_shared_expert), E <= 4095 */
 } moe_cfg;
 
@@ -84,11 +84,19 @@ typedef struct moe_cfg {
  *   of element j in bit j, then 16 nibble bytes in the Q4 order;
  *   w = d * (q - 16) with q in 0..31 (another of those formats; same reading
  *   of the layout).
- * Q8_0 and Q5_0 contexts run every forward through the mat-vec kernels (no
- * fused single-launch layer, no tensor-core prompt path, no lookahead). */
+ * Q4_K: super-blocks of 256 weights (8 sub-blocks of 32), 144 bytes: d, dmin
+ *   (binary16), 12 bytes of 6-bit sub-block scales sc_j and mins m_j (j < 4:
+ *   sc = b[j] & 63, m = b[j+4] & 63; j >= 4: sc = (b[j+4] & 15) |
+ *   (b[j-4] >> 6) << 4, m = (b[j+4] >> 4) | (b[j] >> 6) << 4), 128 code bytes
+ *   (chunk c of 32: sub-block 2c in the low nibbles, 2c+1 in the high);
+ *   w = d * sc_j * q - dmin * m_j (a K-quant format of those kernels; same
+ *   reading of the layout).  Needs hidden and ffn multiples of 256.
+ * Q8_0, Q5_0 and Q4_K contexts run every forward through the mat-vec kernels
+ * (no fused single-launch layer, no tensor-core prompt path, no lookahead). */
 #define MOE_FMT_Q4_0 0
 #define MOE_FMT_Q8_0 1
 #define MOE_FMT_Q5_0 2
+#define MOE_FMT_Q4_K 3
 
 typedef struct moe_stats_t {
     uint64_t steps;        /* cache_step calls */
@@ -105,7 +113,7 @@ typedef struct moe_stats_t {
  * Create a context on cfg->device.  cuda_stream (cudaStream_t; NULL is the
  * legacy default stream, as everywhere in CUDA) is the stream every forward
  * of this context runs on; the caller keeps owning it.  The library allocates and owns: the HBM
- * expert pool (3*L*slots_per_tensor slots of rows*cols/32*(18, 34 or 22) bytes), the
+ * expert pool (3*L*slots_per_tensor slots of rows*cols/32*(18, 34, 22 or 24) bytes), the
  * pointer tables, stamps, miss log, workspaces, an upload stream and the
  * pinned host copies of registered tensors.  *out receives the context.
  * Errors: MOE_ERR_ARG (sizes), MOE_ERR_OOM, MOE_ERR_CUDA.
@@ -115,7 +123,8 @@ int moe_layer_init(const moe_cfg *cfg, void *cuda_stream, moe_ctx **out);
 /*
  * Register one expert tensor (layer, kind) and seed its pool.
  * host_q4: canonical tensor [n_experts][rows][cols/32][18 B] (Q4_0),
- *   [...][34 B] (Q8_0) or [...][22 B] (Q5_0), per cfg.weight_format, any host
+ *   [...][34 B] (Q8_0), [...][22 B] (Q5_0) or [n_experts][rows][cols/256][144 B]
+ *   (Q4_K), per cfg.weight_format, any host
  *   memory; the library copies it into its own pinned, device-mapped host
  *   memory in plane layout (all codes, then all scales) and never reads
  *   host_q4 again, so the caller may free it on return.

@@ -27,13 +27,17 @@ __host__ __device__ inline size_t blob_bytes(int rows, int nb) { return (size_t)
 // bytes as Q4 plus a 32-bit word of fifth bits, w = d (q - 16)).  Blob
 // layout, N = rows x nb blocks: [codes: N x 16 or 32 B][Q5_0 only: fifth
 // bits, N x 4 B][scales: N x binary16]; code_bytes counts both code planes.
-constexpr int kFmtQ4 = 0, kFmtQ8 = 1, kFmtQ5 = 2;
+// Q4_K (256-weight super-blocks with 6-bit sub-block scales and mins) is
+// repacked per 32-weight sub-block: Q4-order nibbles, and the exact fp32 pair
+// (d * sc, dmin * m) in the scale plane (8 bytes per block instead of 2).
+constexpr int kFmtQ4 = 0, kFmtQ8 = 1, kFmtQ5 = 2, kFmtQ4K = 3;
 __host__ __device__ constexpr int code_bytes(int fmt) { return fmt == kFmtQ8 ? 32 : fmt == kFmtQ5 ? 20 : 16; }
+__host__ __device__ constexpr int scale_bytes(int fmt) { return fmt == kFmtQ4K ? 8 : 2; }
 __host__ __device__ inline size_t blob_scales_offset_fmt(int fmt, int rows, int nb) {
     return (size_t)rows * nb * code_bytes(fmt);
 }
 __host__ __device__ inline size_t blob_bytes_fmt(int fmt, int rows, int nb) {
-    return (size_t)rows * nb * (code_bytes(fmt) + 2);
+    return (size_t)rows * nb * (code_bytes(fmt) + scale_bytes(fmt));
 }
 
 // Per-activation-block data kept next to the int8 codes: the binary16 scale
@@ -150,6 +154,38 @@ struct WCodes<kFmtQ8> {
         return __dp4a((int)hi.w, a1.w, s);
     }
 };
+template <>
+struct WCodes<kFmtQ4K> {
+    uint4 c;  // Q4-order nibbles of one sub-block
+    __device__ __forceinline__ void load(const uint8_t *blob, size_t, size_t i) {
+        c = ld_weights((const uint4 *)blob + i);
+    }
+    // raw sum q_w * q_a (the sub-block's min enters through its scale term)
+    __device__ __forceinline__ int dot(const int4 &a0, const int4 &a1, int) const { return q4_dot_raw(c, a0, a1); }
+};
+
+// Scale of one weight block and its contribution to a row sum given the
+// block's integer dot and the activation block's scale and code sum:
+// d_w * d_a * dot, or for Q4_K d_a * (d*sc * dot - dmin*m * sum q_a).
+template <int FMT>
+struct WScale {
+    float s;
+    __device__ __forceinline__ void load(const uint8_t *scales, size_t i) {
+        s = ld_scale((const __half *)scales + i);
+    }
+    __device__ __forceinline__ float term(int dot, const BlockScale &a) const { return (float)dot * (s * a.d); }
+};
+template <>
+struct WScale<kFmtQ4K> {
+    float2 sm;
+    __device__ __forceinline__ void load(const uint8_t *scales, size_t i) {
+        sm = __ldcs((const float2 *)scales + i);
+    }
+    __device__ __forceinline__ float term(int dot, const BlockScale &a) const {
+        return a.d * (sm.x * (float)dot - sm.y * (float)a.s);
+    }
+};
+
 // Bits 0..3 of x moved to bit 0 of bytes 0..3 (the four shifted copies do
 // not overlap, so the product carries nothing).
 __device__ __forceinline__ uint32_t spread4(uint32_t x) { return (x * 0x00204081u) & 0x01010101u; }

@@ -269,8 +269,6 @@ __global__ void __launch_bounds__(256) gate_up_kernel(GemvParams p) {
         const uint8_t *bu = (const uint8_t *)(uintptr_t)(eu & ~1ull);
         const int r = rg * 32 + rloc;
         const size_t nblk = (size_t)p.F * nbx, rb0 = (size_t)r * nbx;
-        const __half *dg = (const __half *)(bg + scale_off) + (size_t)r * nbx;
-        const __half *du = (const __half *)(bu + scale_off) + (size_t)r * nbx;
 
         for (int c0 = a0; c0 < a1; c0 += kMaxChunk) {
             const int nt = min(kMaxChunk, a1 - c0);
@@ -282,15 +280,15 @@ __global__ void __launch_bounds__(256) gate_up_kernel(GemvParams p) {
             for (int t = 0; t < kMaxChunk; ++t) ag[t] = au[t] = 0.0f;
             for (int b0 = sub; b0 < nbx; b0 += 4 * kGULanes) {
                 WCodes<FMT> wg4[4], wu4[4];
-                float sg[4], su[4];
+                WScale<FMT> sg[4], su[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     int b = b0 + i * kGULanes;
                     if (b < nbx) {
                         wg4[i].load(bg, nblk, rb0 + b);
                         wu4[i].load(bu, nblk, rb0 + b);
-                        sg[i] = ld_scale(dg + b);
-                        su[i] = ld_scale(du + b);
+                        sg[i].load(bg + scale_off, rb0 + b);
+                        su[i].load(bu + scale_off, rb0 + b);
                     }
                 }
 #pragma unroll
@@ -305,8 +303,8 @@ __global__ void __launch_bounds__(256) gate_up_kernel(GemvParams p) {
                                 BlockScale xs = p.xds[(size_t)tok[t] * nbx + b];
                                 int ig = wg4[i].dot(x0, x1, xs.s);
                                 int iu = wu4[i].dot(x0, x1, xs.s);
-                                ag[t] += (float)ig * (sg[i] * xs.d);
-                                au[t] += (float)iu * (su[i] * xs.d);
+                                ag[t] += sg[i].term(ig, xs);
+                                au[t] += su[i].term(iu, xs);
                             }
                         }
                     }
@@ -368,7 +366,6 @@ __global__ void __launch_bounds__(256) down_kernel(GemvParams p) {
         const uint8_t *bd = (const uint8_t *)(uintptr_t)(ed & ~1ull);
         const int r = rb * ROWS + rloc;
         const size_t nblk = (size_t)p.H * nbf, rb0 = (size_t)r * nbf;
-        const __half *dd = (const __half *)(bd + scale_off) + (size_t)r * nbf;
 
         for (int c0 = a0; c0 < a1; c0 += kMaxChunk) {
             const int nt = min(kMaxChunk, a1 - c0);
@@ -380,13 +377,13 @@ __global__ void __launch_bounds__(256) down_kernel(GemvParams p) {
             for (int t = 0; t < kMaxChunk; ++t) acc[t] = 0.0f;
             for (int b0 = sub; b0 < nbf; b0 += 4 * L) {
                 WCodes<FMT> w4[4];
-                float sw[4];
+                WScale<FMT> sw[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     int b = b0 + i * L;
                     if (b < nbf) {
                         w4[i].load(bd, nblk, rb0 + b);
-                        sw[i] = ld_scale(dd + b);
+                        sw[i].load(bd + scale_off, rb0 + b);
                     }
                 }
 #pragma unroll
@@ -400,7 +397,7 @@ __global__ void __launch_bounds__(256) down_kernel(GemvParams p) {
                                 int4 h0 = __ldcg(ha), h1 = __ldcg(ha + 1);
                                 BlockScale hs = p.hds[(size_t)asg[t] * nbf + b];
                                 int id = w4[i].dot(h0, h1, hs.s);
-                                acc[t] += (float)id * (sw[i] * hs.d);
+                                acc[t] += sw[i].term(id, hs);
                             }
                         }
                     }
@@ -465,6 +462,8 @@ int launch_gemv(const GemvParams &p, int grid_gu, int grid_dn, cudaStream_t st, 
     if (ev) record(ev[0], st);
     if (p.fmt == kFmtQ8)
         launch_gemv_fmt<kFmtQ8>(p, grid_gu, grid_dn, st, ev);
+    else if (p.fmt == kFmtQ4K)
+        launch_gemv_fmt<kFmtQ4K>(p, grid_gu, grid_dn, st, ev);
     else if (p.fmt == kFmtQ5)
         launch_gemv_fmt<kFmtQ5>(p, grid_gu, grid_dn, st, ev);
     else
@@ -1666,6 +1665,8 @@ int launch_block_dots(const uint8_t *blob, int fmt, int rows, int nb, int row0, 
         block_dots_kernel<kFmtQ8><<<(n + 255) / 256, 256, 0, st>>>(blob, rows, nb, row0, n_rows, qa, out);
     else if (fmt == kFmtQ5)
         block_dots_kernel<kFmtQ5><<<(n + 255) / 256, 256, 0, st>>>(blob, rows, nb, row0, n_rows, qa, out);
+    else if (fmt == kFmtQ4K)
+        block_dots_kernel<kFmtQ4K><<<(n + 255) / 256, 256, 0, st>>>(blob, rows, nb, row0, n_rows, qa, out);
     else
         block_dots_kernel<kFmtQ4><<<(n + 255) / 256, 256, 0, st>>>(blob, rows, nb, row0, n_rows, qa, out);
     return (int)cudaGetLastError();

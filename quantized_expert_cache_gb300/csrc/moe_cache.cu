@@ -54,7 +54,7 @@ struct moe_ctx {
     int32_t *idx_a = nullptr;              // [M][ka]: routed ids + E
     float *w_a = nullptr;                  // [M][ka]: routed weights + 1
     size_t blob = 0, stride = 0;
-    int fmt = 0;  // moe::kFmtQ4, kFmtQ8 or kFmtQ5
+    int fmt = 0;  // moe::kFmtQ4, kFmtQ8, kFmtQ5 or kFmtQ4K
     cudaStream_t stream = nullptr, up = nullptr;
     cudaEvent_t ev_fwd = nullptr, ev_up = nullptr;
 
@@ -214,13 +214,53 @@ int sync_all(moe_ctx *ctx) {
     return MOE_OK;
 }
 
+// Q4_K super-block (144 bytes, 256 weights) -> 8 sub-blocks: Q4-order
+// nibbles (byte t = element t | element t + 16 << 4) and the exact fp32
+// pairs (d * sc_j, dmin * m_j) (binary16 times a 6-bit integer fits fp32).
+void repack_q4k_super(const uint8_t *sb, uint8_t *codes, float *sm) {
+    auto h2f = [](const uint8_t *p) {
+        __half h;
+        uint16_t b = (uint16_t)(p[0] | (p[1] << 8));
+        memcpy(&h, &b, 2);
+        return __half2float(h);
+    };
+    const float d = h2f(sb), dmin = h2f(sb + 2);
+    const uint8_t *sc = sb + 4, *qs = sb + 16;
+    for (int j = 0; j < 8; ++j) {
+        int s6, m6;
+        if (j < 4) {
+            s6 = sc[j] & 63;
+            m6 = sc[j + 4] & 63;
+        } else {
+            s6 = (sc[j + 4] & 15) | ((sc[j - 4] >> 6) << 4);
+            m6 = (sc[j + 4] >> 4) | ((sc[j] >> 6) << 4);
+        }
+        sm[2 * j] = d * (float)s6;
+        sm[2 * j + 1] = dmin * (float)m6;
+        const uint8_t *chunk = qs + 32 * (j / 2);
+        const int shift = (j & 1) ? 4 : 0;
+        for (int t = 0; t < 16; ++t) {
+            const int lo = (chunk[t] >> shift) & 15, hi = (chunk[t + 16] >> shift) & 15;
+            codes[16 * j + t] = (uint8_t)(lo | (hi << 4));
+        }
+    }
+}
+
 // Repack canonical blocks (binary16 d, then the code bytes: 18 bytes for
-// Q4, 34 for Q8_0; d, 4 fifth-bit bytes, 16 nibble bytes = 22 for Q5_0) of
-// n_experts experts into plane blobs.
+// Q4, 34 for Q8_0; d, 4 fifth-bit bytes, 16 nibble bytes = 22 for Q5_0;
+// 144-byte super-blocks of 8 blocks for Q4_K) of n_experts experts into
+// plane blobs.
 void repack(const uint8_t *src, uint8_t *dst, int fmt, int n_experts, int rows, int nb, size_t stride) {
     const size_t nblk = (size_t)rows * nb, cb = (size_t)moe::code_bytes(fmt), bb = cb + 2;
     auto work = [&](int e0, int e1) {
         for (int e = e0; e < e1; ++e) {
+            if (fmt == moe::kFmtQ4K) {
+                const uint8_t *s = src + (size_t)e * (nblk / 8) * 144;
+                uint8_t *q = dst + (size_t)e * stride;
+                float *sm = (float *)(q + nblk * 16);
+                for (size_t u = 0; u < nblk / 8; ++u) repack_q4k_super(s + 144 * u, q + 128 * u, sm + 16 * u);
+                continue;
+            }
             const uint8_t *s = src + (size_t)e * nblk * bb;
             uint8_t *q = dst + (size_t)e * stride;
             uint8_t *d = q + nblk * cb;
@@ -422,10 +462,13 @@ int moe_layer_init(const moe_cfg *cfg, void *cuda_stream, moe_ctx **out) {
         c.top_k < 1 || c.top_k > 32 || c.top_k > c.n_experts || c.n_layers < 1 || c.n_layers * 3 > (1 << 20) ||
         c.slots_per_tensor < 0 || c.slots_per_tensor > c.n_experts || c.max_tokens < 1 || c.window_tokens < 1 ||
         c.max_swaps_per_step < 0 || (c.shared_experts != 0 && (c.shared_experts != 1 || c.n_experts > 4095)) ||
-        (c.weight_format != MOE_FMT_Q4_0 && c.weight_format != MOE_FMT_Q8_0 && c.weight_format != MOE_FMT_Q5_0))
+        (c.weight_format != MOE_FMT_Q4_0 && c.weight_format != MOE_FMT_Q8_0 && c.weight_format != MOE_FMT_Q5_0 &&
+         c.weight_format != MOE_FMT_Q4_K) ||
+        (c.weight_format == MOE_FMT_Q4_K && (c.hidden % 256 || c.ffn % 256)))
         return fail(nullptr, MOE_ERR_ARG,
                     "bad cfg: hidden%32, ffn%32, 1<=E<=4096, 1<=k<=min(32,E), layers>=1, 0<=slots<=E, max_tokens>=1, "
-                    "weight_format Q4_0, Q8_0 or Q5_0, shared_experts 0 or 1 (then E <= 4095)");
+                    "weight_format Q4_0, Q8_0, Q5_0 or Q4_K (hidden, ffn % 256), shared_experts 0 or 1 "
+                    "(then E <= 4095)");
     int down_rows = moe::down_rows_per_item(c.ffn);
     if (c.hidden % down_rows) return fail(nullptr, MOE_ERR_ARG, "hidden must be a multiple of the down row block");
     ctx = new moe_ctx();
@@ -441,7 +484,10 @@ int moe_layer_init(const moe_cfg *cfg, void *cuda_stream, moe_ctx **out) {
     ctx->M = c.max_tokens;
     ctx->n_tensors = 3 * c.n_layers;
     ctx->spt = c.slots_per_tensor;
-    ctx->fmt = c.weight_format == MOE_FMT_Q8_0 ? moe::kFmtQ8 : c.weight_format == MOE_FMT_Q5_0 ? moe::kFmtQ5 : moe::kFmtQ4;
+    ctx->fmt = c.weight_format == MOE_FMT_Q8_0   ? moe::kFmtQ8
+               : c.weight_format == MOE_FMT_Q5_0 ? moe::kFmtQ5
+               : c.weight_format == MOE_FMT_Q4_K ? moe::kFmtQ4K
+                                                 : moe::kFmtQ4;
     ctx->blob = moe::blob_bytes_fmt(ctx->fmt, c.ffn, c.hidden / 32);
     ctx->stride = (ctx->blob + 255) / 256 * 256;
     auto cleanup_fail = [&](int rc) {

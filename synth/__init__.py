@@ -293,6 +293,11 @@ WORKLOADS = {
     "decode_b1_q5_resident16": Workload("decode_b1_q5_resident16", 2048, 512, 8, 1152, 16, routing="zipf",
                                         zipf_s=1.1, capacity=[512] * 16, phases=[("decode", 1, 64)],
                                         weight_format=FMT_Q5_0),
+    # Q4_K expert weights: 16 resident layers, FFN 1280 (the decode shape's
+    # 1152 rounded up to whole 256-weight super-blocks)
+    "decode_b1_q4k_resident16": Workload("decode_b1_q4k_resident16", 2048, 512, 8, 1280, 16, routing="zipf",
+                                         zipf_s=1.1, capacity=[512] * 16, phases=[("decode", 1, 64)],
+                                         weight_format=FMT_Q4_K),
     # Q4 weights with a shared expert per layer: the same 16 resident layers
     "decode_b1_shared_resident16": Workload("decode_b1_shared_resident16", 2048, 512, 8, 1152, 16,
                                             routing="zipf", zipf_s=1.1, capacity=[512] * 16,

@@ -121,9 +121,10 @@ def test_shared_expert_cache_steps_and_borrow():
         m.close()
 
 
-@pytest.mark.parametrize("fmt", [qec.FMT_Q8_0, qec.FMT_Q5_0])
+@pytest.mark.parametrize("fmt", [qec.FMT_Q8_0, qec.FMT_Q5_0, qec.FMT_Q4_K])
 def test_shared_expert_other_formats(fmt):
-    m = Model(H=512, F=384, E=16, k=4, L=1, capacity=8, max_tokens=40, zipf_s=0.8, shared=True, weight_format=fmt)
+    F = 512 if fmt == qec.FMT_Q4_K else 384
+    m = Model(H=512, F=F, E=16, k=4, L=1, capacity=8, max_tokens=40, zipf_s=0.8, shared=True, weight_format=fmt)
     try:
         for T in (1, 5, 40):
             x, lg = m.wl.x(0, T, T), m.wl.logits(0, T, T)
