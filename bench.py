@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--cpu-sample-steps", type=int, default=6)
     ap.add_argument("--prefill-steps", type=int, default=2)
     ap.add_argument("--prefill-workload", default="prefill_t4096")
+    ap.add_argument("--large-decode-steps", type=int, default=16,
+                    help="decode steps per batch size of the large-expert leg (0 skips the leg)")
     ap.add_argument("--q8-steps", type=int, default=64,
                     help="timed decode steps of each of the Q8_0 / Q5_0 weight-format legs (0 skips them)")
     ap.add_argument("--pool-steps", type=int, default=256,
@@ -410,6 +412,8 @@ def run_ours(args):
         out["prefill"] = run_prefill_leg(args, qec, synth, torch, log)
     if args.pool_steps > 0:
         out["pool"] = run_pool_leg(args, qec, synth, torch, log)
+    if args.large_decode_steps > 0:
+        out["large_expert"] = run_large_expert_leg(args, qec, synth, torch, log)
     if args.q8_steps > 0:
         out["formats"] = {"q8_0": run_format_leg(args, qec, synth, torch, log, "decode_b1_q8_resident16"),
                           "q5_0": run_format_leg(args, qec, synth, torch, log, "decode_b1_q5_resident16"),
@@ -636,6 +640,87 @@ def run_format_leg(args, qec, synth, torch, log, name, shared=False):
                          "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": round(gbs / peaks["hbm_gbs"], 4), "peak_source": f"{src} hbm_gbs (copy)",
                          "algorithmic_bytes_per_step": int(alg), "traffic": None}}
+
+
+def run_large_expert_leg(args, qec, synth, torch, log):
+    """The large-expert workload (hidden 2880, 128 experts, top-4, FFN 2880,
+    36 layers, 64 of 128 experts per tensor seeded, uniform + Zipf(0.8)
+    routing): 8 slots of every tensor lent to the prompt passes, prompts of
+    512, 4096 and 12288 tokens through the 36 layers (grouped GEMM; cold
+    experts uploaded a layer ahead by the lookahead prefetch), the slots given
+    back, then batch 1, 8 and 32 decode steps with a promotion pass after
+    each.  Prompt tokens/s from CUDA events around the layer loop (one warm-up
+    pass of each size first); decode tokens/s from CUDA events around
+    args.large_decode_steps steps."""
+    wl = synth.WORKLOADS["large_expert"]
+    L, H, E, k, F = wl.n_layers, wl.hidden, wl.n_experts, wl.top_k, wl.ffn
+    spt = max(wl.layer_capacity(l) for l in range(L))
+    T_max = max(T for label, T, _ in wl.phases)
+    stream = torch.cuda.Stream()
+    sp = stream.cuda_stream
+    ctx = qec.moe_layer_init(H, F, E, k, L, spt, T_max, stream=sp)
+    register_workload(qec, synth, ctx, wl, log)
+    qec.moe_set_lookahead(ctx, True)
+    idx = torch.empty((T_max, k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T_max, k), device="cuda")
+    y = torch.empty((T_max, H), device="cuda")
+    n_borrow = 3 * L * 8
+    qec.moe_pool_borrow(ctx, n_borrow)
+    out = {"workload": (f"{wl.name}: {L} layers, hidden {H}, {E} experts, top-{k}, FFN {F}, 64/128 experts per "
+                        f"tensor seeded, 0.5 uniform + 0.5 Zipf(0.8) routing; {n_borrow} pool blocks lent to the "
+                        f"prompt passes (lookahead prefetch on), returned before decode"),
+           "prefill": {}, "decode": {}}
+    peaks, _ = load_peaks()
+    for phase, (label, T, _) in enumerate(wl.phases):
+        if label != "prefill":
+            continue
+        X = [torch.from_numpy(wl.x(l, 0, T, phase)).cuda() for l in range(L)]
+        LG = [torch.from_numpy(wl.logits(l, 0, T, phase)).cuda() for l in range(L)]
+        torch.cuda.synchronize()
+        ms = []
+        for rep in range(2):  # a warm-up pass, then the timed one
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for l in range(L):
+                qec.route_topk(ctx, LG[l], T, E, k, idx, w, sp)
+                qec.moe_ffn_forward(ctx, l, X[l], T, idx, w, y, sp)
+            e1.record(stream)
+            stream.synchronize()
+            qec.miss_drain(ctx)
+            ms.append(e0.elapsed_time(e1))
+        tfl = 2.0 * T * k * 3 * H * F * L / (ms[-1] * 1e-3) / 1e12
+        out["prefill"][str(T)] = {"tokens_per_s": round(T / (ms[-1] * 1e-3), 1), "ms_per_pass": round(ms[-1], 2),
+                                  "tflops": round(tfl, 1), "frac_of_bf16_peak": round(tfl / peaks["bf16_tflops"], 4)}
+        log(f"large expert prefill {T}: {out['prefill'][str(T)]}")
+        del X, LG
+    qec.moe_pool_return(ctx)
+    n = args.large_decode_steps
+    for phase, (label, T, _) in enumerate(wl.phases):
+        if label != "decode":
+            continue
+        Xh, LGh = [], []
+        for s in range(n):
+            Xh.append(np.stack([wl.x(l, s, T, phase) for l in range(L)]))
+            LGh.append(np.stack([wl.logits(l, s, T, phase) for l in range(L)]))
+        X, LG = torch.from_numpy(np.stack(Xh)).cuda(), torch.from_numpy(np.stack(LGh)).cuda()
+        s0 = qec.moe_stats(ctx)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for s in range(n):
+            for l in range(L):
+                qec.moe_ffn_forward_routed(ctx, l, X[s, l], LG[s, l], T, idx[:T], w[:T], y[:T], sp)
+            qec.cache_step(ctx, T)
+        e1.record(stream)
+        stream.synchronize()
+        ms = e0.elapsed_time(e1)
+        s1 = qec.moe_stats(ctx)
+        hits, misses = s1["hits"] - s0["hits"], s1["misses"] - s0["misses"]
+        out["decode"][str(T)] = {"tokens_per_s": round(n * T / (ms * 1e-3), 1), "ms_per_step": round(ms / n, 4),
+                                 "hit_rate": round(hits / max(1, hits + misses), 4)}
+        log(f"large expert decode batch {T}: {out['decode'][str(T)]}")
+    qec.moe_destroy(ctx)
+    return out
 
 
 def run_prefill_leg(args, qec, synth, torch, log):
