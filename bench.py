@@ -55,9 +55,10 @@ def parse():
                     help="timed decode steps of each of the Q8_0 / Q5_0 weight-format legs (0 skips them)")
     ap.add_argument("--pool-steps", type=int, default=256,
                     help="decode tokens per run of the pool-mode / preheat leg (0 skips it)")
-    ap.add_argument("--case", default=None, choices=["decode_layer", "prefill_layer"],
+    ap.add_argument("--case", default=None, choices=["decode_layer", "decode_layer_cold", "prefill_layer"],
                     help="small profiling case: one layer (hidden 2048, 512 experts, top-8, FFN 1152, every "
-                         "expert resident), --launches forwards at batch 1 (routed) or 4096 tokens")
+                         "expert resident, or every expert in host memory for decode_layer_cold), --launches "
+                         "forwards at batch 1 (routed) or 4096 tokens")
     ap.add_argument("--launches", type=int, default=20)
     return ap.parse_args()
 
@@ -437,14 +438,16 @@ def run_case(args):
     import synth
     qec.load()
     H, F, E, k = 2048, 1152, 512, 8
-    T = 1 if args.case == "decode_layer" else 4096
+    T = 4096 if args.case == "prefill_layer" else 1
+    cap = 0 if args.case == "decode_layer_cold" else E
     n = max(3, args.launches)
-    wl = synth.Workload("case", H, E, k, F, 1, routing="zipf", zipf_s=1.1, capacity=[E])
+    wl = synth.Workload("case", H, E, k, F, 1, routing="zipf", zipf_s=1.1, capacity=[cap])
     st = torch.cuda.current_stream()
     ctx = qec.moe_layer_init(H, F, E, k, 1, E, T, stream=st.cuda_stream)
     for kind in range(3):
         rows, cols = wl.tensor_shapes[kind]
-        qec.register_expert_tensor(ctx, 0, kind, wl.expert_tensor(0, kind), rows, cols, E, wl.seed_order(0), E)
+        qec.register_expert_tensor(ctx, 0, kind, wl.expert_tensor(0, kind), rows, cols, cap, wl.seed_order(0),
+                                   cap)
     xs = [torch.from_numpy(wl.x(0, s, T)).cuda() for s in range(n)]
     lgs = [torch.from_numpy(wl.logits(0, s, T)).cuda() for s in range(n)]
     idx = torch.empty((n, T, k), dtype=torch.int32, device="cuda")
@@ -459,8 +462,12 @@ def run_case(args):
     torch.cuda.synchronize()
     ms = [a.elapsed_time(b) for a, b in evs]
     qec.moe_destroy(ctx)
-    print(json.dumps({"case": args.case, "tokens": T, "launches": n,
-                      "median_ms_per_forward": round(float(np.median(ms[2:])), 5)}), flush=True)
+    res = {"case": args.case, "tokens": T, "launches": n, "median_ms_per_forward": round(float(np.median(ms[2:])), 5)}
+    if cap == 0:
+        # every weight byte crosses the host link
+        b = float(np.median(ms[2:]))
+        res["host_link_gbs"] = round(k * 3 * wl.tensor_bytes(0) / (b * 1e-3) / 1e9, 1)
+    print(json.dumps(res), flush=True)
 
 
 def run_pool_leg(args, qec, synth, torch, log):
