@@ -67,6 +67,21 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
+def over_ranks(ms_local, units_local, world, device="cuda"):
+    """Replicas (one process per GPU, no data-path collective): the slowest
+    rank's time and the units every rank processed, so that whole-job
+    throughput = units / time.  One process: the local values."""
+    if world == 1:
+        return float(ms_local), float(units_local)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(ms_local)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    u = torch.tensor([float(units_local)], dtype=torch.float64, device=device)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -313,13 +328,8 @@ def run_ours(args):
     ms = ev0.elapsed_time(ev1)
     barrier()
     torch.cuda.synchronize()
-    ms_max = ms
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
-    tok_per_s = world * args.steps * T / (ms_max / 1e3)
+    ms_max, tokens = over_ranks(ms, args.steps * T, world)
+    tok_per_s = tokens / (ms_max / 1e3)
     st_main = qec.moe_stats(ctx)
     log(f"timed: {tok_per_s:.1f} tokens/s, {ms_max / args.steps:.4f} ms/step, clocks {clk}")
 
@@ -335,7 +345,8 @@ def run_ours(args):
     stream.synchronize()
     e2e_s = time.perf_counter() - t0
     barrier()
-    e2e_tok = world * args.steps * T / e2e_s
+    e2e_ms, e2e_tokens = over_ranks(e2e_s * 1e3, args.steps * T, world)
+    e2e_tok = e2e_tokens / (e2e_ms / 1e3)
     log(f"e2e: {e2e_tok:.1f} tokens/s")
 
     # roofline of the fused expert-FFN layer kernel (routing, gate/up, SwiGLU,
