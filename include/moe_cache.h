@@ -392,6 +392,16 @@ int moe_probe_host_read(const void *host_pinned, size_t bytes, int iters, double
 int moe_debug_fail_upload(moe_ctx *ctx, int nth);
 
 /*
+ * Failure-detection hook: enqueue on the context stream one kernel that
+ * stays busy for `microseconds` (<= 2 s, measured on the device's global
+ * timer) and then ends by itself.  A cache_step issued behind it with a
+ * shorter cfg.poll_timeout_ms returns MOE_ERR_TIMEOUT without changing any
+ * cache state; the context stays usable and the step can be retried.
+ * Errors: MOE_ERR_ARG, MOE_ERR_CUDA.
+ */
+int moe_debug_busy(moe_ctx *ctx, int microseconds);
+
+/*
  * Kernel timing (benchmark hook): when enabled, every forward records CUDA
  * events on the context stream around its gate/up mat-vec and its down
  * mat-vec launches (also inside a captured graph).  moe_debug_timing_read

@@ -71,6 +71,7 @@ SIGNATURES = {
     "moe_probe_host_read": (_i32, [_vp, _sz, _i32, ctypes.POINTER(ctypes.c_double),
                                    ctypes.POINTER(ctypes.c_double)]),
     "moe_debug_fail_upload": (_i32, [_vp, _i32]),
+    "moe_debug_busy": (_i32, [_vp, _i32]),
     "moe_debug_timing": (_i32, [_vp, _i32]),
     "moe_debug_timing_read": (_i32, [_vp, _vp, _vp]),
     "moe_expert_ffn_noalloc": (_i32, [_vp, _i32, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp]),
@@ -276,6 +277,10 @@ def moe_probe_host_read(host_pinned_addr: int, nbytes: int, iters: int = 5, with
 
 def moe_debug_fail_upload(ctx, nth):
     return _check(ctx, load().moe_debug_fail_upload(ctx, nth))
+
+
+def moe_debug_busy(ctx, microseconds):
+    return _check(ctx, load().moe_debug_busy(ctx, microseconds))
 
 
 def moe_debug_timing(ctx, enable=True):

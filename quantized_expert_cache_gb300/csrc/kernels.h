@@ -147,6 +147,7 @@ int gemm_bn(bool dual);
 int launch_step_finish(const Update *u, int n, uint64_t *tbl, int32_t *slot, uint32_t *stamps, uint32_t *clock,
                        uint32_t new_clock, uint32_t *clear_a, int n_a, uint32_t *clear_b, int n_b, cudaStream_t st);
 int launch_count_assign(const int32_t *idx, int n, int E, uint32_t *cnt, cudaStream_t st);
+int launch_busy(unsigned long long ns, cudaStream_t st);
 int launch_shared_assign(const int32_t *idx, const float *w, int T, int k, int e_shared, int32_t *idx_a, float *w_a,
                          int *error, cudaStream_t st);
 

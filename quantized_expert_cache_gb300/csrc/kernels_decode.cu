@@ -1782,4 +1782,23 @@ int launch_shared_assign(const int32_t *idx, const float *w, int T, int k, int e
     return (int)cudaGetLastError();
 }
 
+// Debug: keep one thread of the stream busy for a bounded time (global
+// timer), so that a host-side poll limit can run out without any fault or
+// hang; the wait ends by itself after min(ns, 2 s).
+__global__ void busy_kernel(unsigned long long ns) {
+    unsigned long long t0, t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+    if (ns > 2000000000ull) ns = 2000000000ull;
+    const long long c0 = clock64();
+    do {
+        __nanosleep(1000);
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    } while (t - t0 < ns && clock64() - c0 < 6000000000ll);  // the SM clock bounds it too (~3 s)
+}
+
+int launch_busy(unsigned long long ns, cudaStream_t st) {
+    busy_kernel<<<1, 1, 0, st>>>(ns);
+    return (int)cudaGetLastError();
+}
+
 }  // namespace moe

@@ -1744,4 +1744,12 @@ int moe_debug_fail_upload(moe_ctx *ctx, int nth) {
     return MOE_OK;
 }
 
+int moe_debug_busy(moe_ctx *ctx, int microseconds) {
+    if (!ctx || microseconds < 0 || microseconds > 2000000) return fail(ctx, MOE_ERR_ARG, "bad argument");
+    CK(cudaSetDevice(ctx->dev));
+    int rc = moe::launch_busy((unsigned long long)microseconds * 1000ull, ctx->stream);
+    if (rc) return fail(ctx, MOE_ERR_CUDA, "busy launch failed");
+    return MOE_OK;
+}
+
 }  // extern "C"

@@ -83,7 +83,7 @@ class Model:
 
     def __init__(self, H, F, E, k, L, capacity, max_tokens, seed=0, routing="zipf", zipf_s=1.1, window=64,
                  slots_per_tensor=None, max_swaps=0, stream=None, global_pool=False, preheat=False,
-                 weight_format=0, shared=False):
+                 weight_format=0, shared=False, poll_timeout_ms=10000):
         import torch
         self.torch = torch
         self.wl = synth.Workload("test", H, E, k, F, L, routing=routing, zipf_s=zipf_s, seed=seed,
@@ -96,7 +96,7 @@ class Model:
             stream = torch.cuda.current_stream().cuda_stream
         self.ctx = qec.moe_layer_init(H, F, E, k, L, self.spt, max_tokens, window_tokens=window,
                                       max_swaps_per_step=max_swaps, stream=stream, weight_format=weight_format,
-                                      shared_experts=int(shared))
+                                      shared_experts=int(shared), poll_timeout_ms=poll_timeout_ms)
         self.shared = None
         if shared:
             # one shared expert per layer, from its own seeded stream

@@ -277,3 +277,33 @@ def test_routed_forward_matches_route_then_forward(H, F, E, k, T):
         np.testing.assert_allclose(y.cpu().numpy(), y_ref, rtol=1e-5, atol=1e-6)
     finally:
         m.close()
+
+
+def test_cache_step_poll_timeout_keeps_the_context_usable():
+    """Failure detection without a fault: a bounded busy kernel keeps the
+    stream busy past cache_step's host poll limit; the step reports
+    MOE_ERR_TIMEOUT and changes nothing, and once the device is done the
+    retried step is exactly the oracle's."""
+    m = Model(H=256, F=256, E=16, k=2, L=1, capacity=4, max_tokens=2, window=8, poll_timeout_ms=30)
+    try:
+        for _ in _run_steps(m, 6, lambda s: 1):
+            pass
+        _assert_state(m)
+        before = qec.moe_stats(m.ctx)
+        x, lg = m.wl.x(0, 50, 1), m.wl.logits(0, 50, 1)
+        idx, w = m.route(lg)
+        m.forward(0, x, idx, w)
+        qec.moe_debug_busy(m.ctx, 400000)  # 0.4 s, far past the 30 ms poll limit
+        with pytest.raises(qec.MoeError) as ex:
+            qec.cache_step(m.ctx, 1)
+        assert ex.value.code == -5
+        torch.cuda.synchronize()  # the busy kernel ends by itself
+        assert qec.moe_stats(m.ctx) == before
+        qec.cache_step(m.ctx, 1)
+        used = idx.cpu().numpy().ravel().tolist()
+        m.policy.step(1, {kd: used for kd in range(3)})
+        _assert_state(m)
+        st = qec.moe_stats(m.ctx)
+        assert st["steps"] == before["steps"] + 1 and st["misses"] == m.policy.stats["misses"]
+    finally:
+        m.close()
