@@ -220,7 +220,13 @@ int moe_ffn_forward_routed(moe_ctx *ctx, int layer, const float *d_x, const floa
  * Uploads run on the context's
  * upload stream; the context stream waits for them before its next forward.
  * While pool slots are borrowed, nothing is admitted.  The miss log is
- * cleared.  Errors: MOE_ERR_TIMEOUT, MOE_ERR_CUDA, MOE_ERR_FAULT (injected).
+ * cleared.  Errors: MOE_ERR_TIMEOUT (nothing changed; retry), MOE_ERR_CUDA,
+ * MOE_ERR_FAULT: an injected upload failure (moe_debug_fail_upload), or a
+ * kernel reported a device error since the last step or drain (bit 0: an
+ * expert id outside [0, n_experts) was read as expert 0; other bits: a
+ * bounded wait expired and its work item was skipped) -- the step's cache
+ * update is done, the affected forwards' outputs are not valid, and the
+ * error word is cleared (moe_last_error names the bits).
  */
 int cache_step(moe_ctx *ctx, int n_tokens);
 
@@ -228,7 +234,9 @@ int cache_step(moe_ctx *ctx, int n_tokens);
  * Copy the miss keys logged since the last cache_step (or drain) to
  * host_out, sorted ascending, unique, and clear the log.  *n_out gets the
  * count even when cap is too small (then MOE_ERR_CAPACITY and the log is
- * kept).  Synchronizes with the context stream.
+ * kept).  Synchronizes with the context stream.  MOE_ERR_FAULT (after the
+ * keys are out and the log is cleared): a device error was reported, as for
+ * cache_step.
  */
 int miss_drain(moe_ctx *ctx, uint32_t *host_out, size_t cap, size_t *n_out);
 
@@ -420,8 +428,8 @@ int moe_debug_timing_read(moe_ctx *ctx, double *gate_up_ms, double *down_ms);
  * device memory is entirely reserved by another allocator).  It computes what
  * moe_ffn_forward computes for a small batch, with the caller's expert tables
  * instead of a context: d_tbl holds 3 rows of n_experts uint64 entries
- * (gate, up, down), each the device address of one expert blob in the plane
- * layout the library uses (tag bit 0 clear), or of a device-mapped pinned
+ * (gate, up, down), each the device address of one Q4_0 expert blob in the
+ * plane layout the library uses (tag bit 0 clear), or of a device-mapped pinned
  * host copy with bit 0 set, as moe_cache_snapshot reports them.  d_x, d_idx,
  * d_w, d_y as in moe_ffn_forward; `stream` is any stream (NULL = legacy
  * default stream).  No miss log, stamp or clock is kept.

@@ -104,6 +104,7 @@ struct moe_ctx {
     uint32_t *h_stamps = nullptr;    // pinned mirror, refreshed per tensor when a victim is chosen
     uint32_t *d_stepbuf = nullptr;   // [hit bitmap: hit_words][miss count][miss keys]
     uint32_t *h_step = nullptr;      // pinned: hit bitmap, miss count and the first kStepKeys keys
+    int *h_err = nullptr;            // pinned: the device error word, read with every step record
     int hit_words = 0;               // words of the hit bitmap: one bit per stamp index
     Update *h_upd = nullptr, *d_upd = nullptr;  // pinned, mapped (d_upd: its device address)
     int upd_cap = 0, n_upd = 0;
@@ -193,6 +194,19 @@ int publish(moe_ctx *ctx, cudaStream_t st, bool clear_step = false) {
     if (rc) return fail(ctx, MOE_ERR_CUDA, std::string("step finish: ") + cudaGetErrorString((cudaError_t)rc));
     ctx->n_upd = 0;
     return MOE_OK;
+}
+
+// A kernel reported a device error since the last check (bit 0: an expert id
+// outside [0, E), read as expert 0; other bits: a bounded wait expired and its
+// work item was skipped): clear the word and report it once.
+int device_fault(moe_ctx *ctx) {
+    const int bits = *ctx->h_err;
+    *ctx->h_err = 0;
+    CK(cudaMemsetAsync(ctx->d_error, 0, sizeof(int), ctx->stream));
+    char msg[160];
+    snprintf(msg, sizeof msg, "device error bits 0x%x: %s", bits,
+             (bits & 1) ? "an expert id outside [0, n_experts) (read as expert 0)" : "a bounded wait expired");
+    return fail(ctx, MOE_ERR_FAULT, msg);
 }
 
 int wait_event(moe_ctx *ctx, cudaEvent_t ev) {
@@ -618,6 +632,8 @@ int moe_layer_init(const moe_cfg *cfg, void *cuda_stream, moe_ctx **out) {
     CKI(cudaHostGetDevicePointer((void **)&ctx->d_upd, ctx->h_upd, 0));
     CKI(cudaHostAlloc(&ctx->h_step, sizeof(uint32_t) * ((size_t)ctx->hit_words + 1 + kStepKeys),
                       cudaHostAllocDefault));
+    CKI(cudaHostAlloc(&ctx->h_err, sizeof(int), cudaHostAllocDefault));
+    *ctx->h_err = 0;
     CKI(cudaDeviceSynchronize());
 #undef CKI
     ctx->t.resize(nt);
@@ -1034,6 +1050,7 @@ int cache_step(moe_ctx *ctx, int n_tokens) {
     // and the first keys (the stamps are read only for tensors that admit)
     CK(cudaMemcpyAsync(ctx->h_step, ctx->d_stepbuf, sizeof(uint32_t) * (hb + 1 + fast), cudaMemcpyDeviceToHost,
                        ctx->stream));
+    CK(cudaMemcpyAsync(ctx->h_err, ctx->d_error, sizeof(int), cudaMemcpyDeviceToHost, ctx->stream));
     CK(cudaEventRecord(ctx->ev_fwd, ctx->stream));
     int rc = wait_event(ctx, ctx->ev_fwd);
     if (rc) return rc;
@@ -1177,6 +1194,7 @@ int cache_step(moe_ctx *ctx, int n_tokens) {
     if (rc) return rc;
     ctx->stats.clock = clk;
     if (fault) return fail(ctx, MOE_ERR_FAULT, "injected upload failure (admission rolled back)");
+    if (*ctx->h_err) return device_fault(ctx);
     return MOE_OK;
 }
 
@@ -1200,7 +1218,9 @@ int miss_drain(moe_ctx *ctx, uint32_t *host_out, size_t cap, size_t *n_out) {
     CK(cudaMemsetAsync(ctx->d_bitmap, 0, sizeof(uint32_t) * (size_t)ctx->n_tensors * ctx->bitmap_words, ctx->stream));
     CK(cudaMemsetAsync(ctx->d_stepbuf, 0, sizeof(uint32_t) * ((size_t)ctx->hit_words + 1),
                        ctx->stream));
+    CK(cudaMemcpyAsync(ctx->h_err, ctx->d_error, sizeof(int), cudaMemcpyDeviceToHost, ctx->stream));
     CK(cudaStreamSynchronize(ctx->stream));
+    if (*ctx->h_err) return device_fault(ctx);
     return MOE_OK;
 }
 
@@ -1599,6 +1619,7 @@ void moe_destroy(moe_ctx *ctx) {
     if (ctx->h_stamps) cudaFreeHost(ctx->h_stamps);
     if (ctx->h_upd) cudaFreeHost(ctx->h_upd);
     if (ctx->h_step) cudaFreeHost(ctx->h_step);
+    if (ctx->h_err) cudaFreeHost(ctx->h_err);
     for (cudaEvent_t e : ctx->tev) cudaEventDestroy(e);
     if (ctx->ev_fwd) cudaEventDestroy(ctx->ev_fwd);
     if (ctx->ev_up) cudaEventDestroy(ctx->ev_up);

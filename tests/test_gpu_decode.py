@@ -307,3 +307,26 @@ def test_cache_step_poll_timeout_keeps_the_context_usable():
         assert st["steps"] == before["steps"] + 1 and st["misses"] == m.policy.stats["misses"]
     finally:
         m.close()
+
+
+@pytest.mark.parametrize("T", [1, 40])
+def test_bad_expert_id_is_reported_once_and_the_context_recovers(T):
+    """An expert id outside [0, E) is caught by the kernels' own range checks
+    (read as expert 0, error bit set); the next promotion pass reports
+    MOE_ERR_FAULT once and clears it, and later steps are normal."""
+    m = Model(H=256, F=256, E=16, k=2, L=1, capacity=4, max_tokens=40, window=8)
+    try:
+        x, lg = m.wl.x(0, 7, T), m.wl.logits(0, 7, T)
+        idx, w = m.route(lg)
+        bad = idx.clone()
+        bad[0, 1] = m.E + 3
+        m.forward(0, x, bad, w)
+        with pytest.raises(qec.MoeError) as ex:
+            qec.cache_step(m.ctx, T)
+        assert ex.value.code == -8 and "expert id" in str(ex.value)
+        y = m.forward(0, x, idx, w)
+        torch.cuda.synchronize()
+        check_layer_parity(m, 0, x, lg, y.cpu().numpy(), idx.cpu().numpy(), w.cpu().numpy())
+        qec.cache_step(m.ctx, T)  # no error left
+    finally:
+        m.close()
