@@ -372,13 +372,13 @@ int prefetch_layer(moe_ctx *ctx, int l) {
 }
 
 // Victim search of the shared pool for one promotion pass: the free pool
-// slots in arena order first, then (built at the first eviction) the
-// occupied slots stamped before this step, by (stamp, slot).  Slots filled
+// slots in arena order first, then the occupied slots stamped before this
+// step, by (stamp, slot) (both built at the step's first admission).  Slots filled
 // in this pass carry the new clock, so they never become victims, and a
 // candidate changes hands only by being taken: one sorted list serves every
 // admission of the step.
 struct GlobalPick {
-    bool stamps_read = false, free_built = false, victims_built = false;
+    bool stamps_read = false, free_built = false;
     std::vector<int> free_slots;
     size_t fpos = 0;
     std::vector<std::pair<uint32_t, int>> victims;
@@ -399,26 +399,38 @@ int admit_global(moe_ctx *ctx, GlobalPick &gs, int tid, int e, uint64_t clk, int
         gs.stamps_read = true;
     }
     if (!gs.free_built) {
-        for (int g = 0; g < G; ++g)
-            if (ctx->g_pool[g] && !ctx->g_lent[g] && ctx->g_owner[g] < 0) gs.free_slots.push_back(g);
+        // one pass over the arena: the free pool slots in order, and the
+        // n_qualified smallest (stamp, slot) pairs among the occupied slots
+        // stamped before this step (a bounded max-heap; no step can take
+        // more victims than it has qualifying misses)
+        const size_t need = (size_t)std::max(0, gs.n_qualified);
+        auto &h = gs.victims;
+        for (int v = 0; v < G; ++v) {
+            if (!ctx->g_pool[v] || ctx->g_lent[v]) continue;
+            if (ctx->g_owner[v] < 0) {
+                gs.free_slots.push_back(v);
+                continue;
+            }
+            const uint32_t st = ctx->h_stamps[v];
+            if ((uint64_t)st >= clk || need == 0) continue;
+            const std::pair<uint32_t, int> c(st, v);
+            if (h.size() < need) {
+                h.push_back(c);
+                std::push_heap(h.begin(), h.end());
+            } else if (c < h.front()) {
+                std::pop_heap(h.begin(), h.end());
+                h.back() = c;
+                std::push_heap(h.begin(), h.end());
+            }
+        }
+        std::sort_heap(h.begin(), h.end());
         gs.free_built = true;
     }
     int g = -1;
     if (gs.fpos < gs.free_slots.size()) {
         g = gs.free_slots[gs.fpos++];
-    } else {
-        if (!gs.victims_built) {
-            for (int v = 0; v < G; ++v)
-                if (ctx->g_pool[v] && !ctx->g_lent[v] && ctx->g_owner[v] >= 0 && (uint64_t)ctx->h_stamps[v] < clk)
-                    gs.victims.emplace_back(ctx->h_stamps[v], v);
-            // no more victims than admissions can be asked for this step
-            const size_t need = std::min(gs.victims.size(), (size_t)std::max(0, gs.n_qualified));
-            std::nth_element(gs.victims.begin(), gs.victims.begin() + (long)need, gs.victims.end());
-            gs.victims.resize(need);
-            std::sort(gs.victims.begin(), gs.victims.end());
-            gs.victims_built = true;
-        }
-        if (gs.vpos < gs.victims.size()) g = gs.victims[gs.vpos++].second;
+    } else if (gs.vpos < gs.victims.size()) {
+        g = gs.victims[gs.vpos++].second;
     }
     if (g < 0) return MOE_OK;  // every pool slot was used this step: skipped, the sighting stays
     const int vkey = ctx->g_owner[g];
