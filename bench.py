@@ -485,8 +485,9 @@ def run_pool_leg(args, qec, synth, torch, log):
     """Shared expert pool and prefill preheat against per-tensor pools, on
     the 25%-pool model (one registration; moe_cache_reset puts the seeded
     state back before every run).  (1) decode_b1_pool25: args.pool_steps
-    batch-1 decode tokens from the seeded state with a pool per tensor and
-    with one pool for all layers, alternated twice.  (2)
+    batch-1 decode tokens from the seeded state with a pool per tensor, with
+    one pool for all layers, and with a pool per tensor plus per-layer upload
+    overlap (moe_set_upload_overlap), alternated twice.  (2)
     prompt_then_decode_pool25 (same weights and seeding, the request's
     popularity drifted from the seeding table), one pool: half of the pool is
     lent to a 4096-token prompt pass, given back refilled by seed order or,
@@ -537,11 +538,13 @@ def run_pool_leg(args, qec, synth, torch, log):
     # (first touches of the pinned copies), whichever pool mode it uses
     qec.moe_cache_reset(ctx, False)
     decode(X[:32], LG[:32])
-    runs = {"per_tensor": [], "global": []}
-    for name in ("per_tensor", "global", "per_tensor", "global"):
+    runs = {"per_tensor": [], "global": [], "per_tensor_overlap": []}
+    for name in ("per_tensor", "global", "per_tensor_overlap", "per_tensor", "global", "per_tensor_overlap"):
         qec.moe_cache_reset(ctx, name == "global")
+        qec.moe_set_upload_overlap(ctx, name.endswith("overlap"))
         runs[name].append(decode(X, LG))
         log(f"pool leg, {wl.name}, {name} pool: {runs[name][-1]}")
+    qec.moe_set_upload_overlap(ctx, False)
     for name, r in runs.items():
         out[name] = dict(r[-1], tokens_per_s_runs=[v["tokens_per_s"] for v in r])
     del X, LG

@@ -263,6 +263,23 @@ int moe_pool_borrow(moe_ctx *ctx, int n_slots, void **d_ws, size_t *bytes);
 int moe_pool_return(moe_ctx *ctx);
 
 /*
+ * Upload overlap (eager forwards).  By default the promotion pass makes the
+ * context stream wait for all of its pool uploads before the next forward.
+ * With enable = 1 it records one event per layer after that layer's uploads
+ * instead, and a layer's next forward waits only for its own layer's event,
+ * so the first layers of the next step run while later layers' experts are
+ * still being uploaded.  Results, cache state and statistics are the same
+ * (a layer's kernels read only its own tables; an evicted expert's entry
+ * already points at its host copy).  Forwards must then be issued outside
+ * stream capture (a captured graph could not wait on the per-step events):
+ * a pending wait inside a capture fails with MOE_ERR_STATE, and a graph
+ * captured earlier must not be replayed while the overlap is on (its
+ * launches would not wait for the uploads).  Off by default.  Synchronous.
+ * Errors: MOE_ERR_CUDA.
+ */
+int moe_set_upload_overlap(moe_ctx *ctx, int enable);
+
+/*
  * One pool of expert blocks for all layers (neurall/llama.cpp, "How it
  * works", Expert cache: the per-layer reserve gave way to one pool that every
  * layer draws on; features table, global expert pool row).  With enable = 1

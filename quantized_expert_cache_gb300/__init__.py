@@ -58,6 +58,7 @@ SIGNATURES = {
     "moe_pool_return": (_i32, [_vp]),
     "moe_set_lookahead": (_i32, [_vp, _i32]),
     "moe_set_global_pool": (_i32, [_vp, _i32]),
+    "moe_set_upload_overlap": (_i32, [_vp, _i32]),
     "moe_set_preheat": (_i32, [_vp, _i32]),
     "moe_pool_snapshot": (_i32, [_vp, _vp, _vp]),
     "moe_cache_reset": (_i32, [_vp, _i32]),
@@ -200,6 +201,10 @@ def moe_pool_return(ctx):
 
 def moe_set_lookahead(ctx, enable=True):
     return _check(ctx, load().moe_set_lookahead(ctx, 1 if enable else 0))
+
+
+def moe_set_upload_overlap(ctx, enable=True):
+    return _check(ctx, load().moe_set_upload_overlap(ctx, 1 if enable else 0))
 
 
 def moe_set_global_pool(ctx, enable=True):

@@ -117,6 +117,12 @@ struct moe_ctx {
     bool global_pool = false;
     std::vector<int32_t> g_owner;  // (tid << 12 | e) or -1
     std::vector<uint8_t> g_pool, g_lent;
+    // upload overlap: a layer's next forward waits only for its own layer's
+    // uploads (one event per layer) instead of the whole promotion pass's
+    bool overlap = false;
+    std::vector<cudaEvent_t> ev_layer_up;
+    std::vector<uint8_t> layer_pending;
+    int cur_up_layer = -1;                 // layer of the last upload issued in this pass
     // prefill preheat: assignments per (layer, expert) routed while slots are lent
     bool preheat = false;
     uint32_t *d_use = nullptr;
@@ -371,6 +377,20 @@ int prefetch_layer(moe_ctx *ctx, int l) {
     return MOE_OK;
 }
 
+// Upload overlap: called before each pool upload of the promotion pass (they
+// come in ascending layer order); closes the previous layer's uploads with its
+// event.  finish = true closes the last one.
+int note_upload(moe_ctx *ctx, int layer, bool finish = false) {
+    if (!ctx->overlap) return MOE_OK;
+    const int prev = ctx->cur_up_layer;
+    if (prev >= 0 && (finish || prev != layer)) {
+        CK(cudaEventRecord(ctx->ev_layer_up[prev], ctx->up));
+        ctx->layer_pending[prev] = 1;
+    }
+    ctx->cur_up_layer = finish ? -1 : layer;
+    return MOE_OK;
+}
+
 // Victim search of the shared pool for one promotion pass: the free pool
 // slots in arena order first, then the occupied slots stamped before this
 // step, by (stamp, slot) (both built at the step's first admission).  Slots filled
@@ -451,6 +471,8 @@ int admit_global(moe_ctx *ctx, GlobalPick &gs, int tid, int e, uint64_t clk, int
     }
     TensorState &ts = ctx->t[tid];
     const uint64_t dst = slot_addr(ctx, (size_t)g);
+    int rcu = note_upload(ctx, tid / 3);
+    if (rcu) return rcu;
     CK(cudaMemcpyAsync((void *)(uintptr_t)dst, ts.home + (size_t)e * ctx->stride, ctx->blob, cudaMemcpyHostToDevice,
                        ctx->up));
     uploads++;
@@ -819,6 +841,15 @@ static int ffn_forward_body(moe_ctx *ctx, int layer, const float *d_x, int n_tok
     if (n_tokens == 0) return MOE_OK;
     if (!d_x || !d_idx || !d_w || !d_y) return fail(ctx, MOE_ERR_ARG, "forward: null pointer");
     cudaStream_t st = ctx->stream;
+    if (ctx->overlap && ctx->layer_pending[layer]) {
+        // this layer's admissions of the last promotion pass must be in
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        CK(cudaStreamIsCapturing(st, &cs));
+        if (cs != cudaStreamCaptureStatusNone)
+            return fail(ctx, MOE_ERR_STATE, "forward: upload overlap needs forwards issued outside stream capture");
+        CK(cudaStreamWaitEvent(st, ctx->ev_layer_up[layer], 0));
+        ctx->layer_pending[layer] = 0;
+    }
     if (ctx->shared) {
         // the layer's shared expert joins every token as assignment k (id E,
         // weight 1); the routed ids are checked against E here
@@ -1184,6 +1215,8 @@ int cache_step(moe_ctx *ctx, int n_tokens) {
                 continue;
             }
             const uint64_t dst = pool_addr(ctx, tid, slot);
+            rc = note_upload(ctx, tid / 3);
+            if (rc) return rc;
             CK(cudaMemcpyAsync((void *)(uintptr_t)dst, ts.home + (size_t)e * ctx->stride, ctx->blob,
                                cudaMemcpyHostToDevice, ctx->up));
             uploads++;
@@ -1196,7 +1229,11 @@ int cache_step(moe_ctx *ctx, int n_tokens) {
             ctx->stats.upload_bytes += ctx->blob;
         }
     }
-    if (uploads) {
+    if (uploads && ctx->overlap) {
+        // each layer's next forward waits for its own uploads
+        rc = note_upload(ctx, -1, true);
+        if (rc) return rc;
+    } else if (uploads) {
         // the table entries of this step's admissions flip once their uploads
         // (side stream) are in
         CK(cudaEventRecord(ctx->ev_up, ctx->up));
@@ -1353,6 +1390,21 @@ int moe_pool_return(moe_ctx *ctx) {
     if (rc) return rc;
     CK(cudaStreamSynchronize(ctx->stream));
     ctx->n_lent = 0;
+    return MOE_OK;
+}
+
+int moe_set_upload_overlap(moe_ctx *ctx, int enable) {
+    if (!ctx) return fail(nullptr, MOE_ERR_ARG, "null ctx");
+    CK(cudaSetDevice(ctx->dev));
+    int rc = sync_all(ctx);
+    if (rc) return rc;
+    if (enable && ctx->ev_layer_up.empty()) {
+        ctx->ev_layer_up.assign(ctx->cfg.n_layers, nullptr);
+        for (cudaEvent_t &e : ctx->ev_layer_up) CK(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+    }
+    ctx->layer_pending.assign(ctx->cfg.n_layers, 0);
+    ctx->cur_up_layer = -1;
+    ctx->overlap = enable != 0;
     return MOE_OK;
 }
 
@@ -1636,6 +1688,7 @@ void moe_destroy(moe_ctx *ctx) {
     if (ctx->ev_fwd) cudaEventDestroy(ctx->ev_fwd);
     if (ctx->ev_up) cudaEventDestroy(ctx->ev_up);
     if (ctx->up) cudaStreamDestroy(ctx->up);
+    for (cudaEvent_t e : ctx->ev_layer_up) cudaEventDestroy(e);
     delete ctx;
 }
 

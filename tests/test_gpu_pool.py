@@ -201,3 +201,23 @@ def test_cache_reset_switches_pool_mode_and_restarts_from_seeding():
             _stats_match(m)
     finally:
         m.close()
+
+
+@pytest.mark.parametrize("global_pool", [False, True])
+def test_upload_overlap_same_state_and_outputs(global_pool):
+    # per-layer upload events instead of one wait for the whole promotion
+    # pass: the cache state after every step and the layer outputs are the
+    # oracle's, as without the overlap
+    m = Model(H=256, F=256, E=32, k=4, L=3, capacity=[8, 4, 6], max_tokens=4, window=8, zipf_s=1.0,
+              slots_per_tensor=8, global_pool=global_pool)
+    try:
+        qec.moe_set_upload_overlap(m.ctx, True)
+        for _ in _steps(m, 40, lambda s: 1 if s % 3 else 2, check_every=7):
+            _assert_state(m)
+        st = _stats_match(m)
+        assert st["admissions"] > 0
+        qec.moe_set_upload_overlap(m.ctx, False)
+        for _ in _steps(m, 5, lambda s: 1, step0=100, check_every=2):
+            _assert_state(m)
+    finally:
+        m.close()
