@@ -670,7 +670,7 @@ def run_large_expert_leg(args, qec, synth, torch, log):
     512, 4096 and 12288 tokens through the 36 layers (grouped GEMM; cold
     experts uploaded a layer ahead by the lookahead prefetch), the slots given
     back, then batch 1, 8 and 32 decode steps with a promotion pass after
-    each.  Prompt tokens/s from CUDA events around the layer loop (one warm-up
+    each (per-layer upload overlap on: the forwards are issued eagerly).  Prompt tokens/s from CUDA events around the layer loop (one warm-up
     pass of each size first); decode tokens/s from CUDA events around
     args.large_decode_steps steps."""
     wl = synth.WORKLOADS["large_expert"]
@@ -715,6 +715,8 @@ def run_large_expert_leg(args, qec, synth, torch, log):
         log(f"large expert prefill {T}: {out['prefill'][str(T)]}")
         del X, LG
     qec.moe_pool_return(ctx)
+    # decode is issued eagerly here: each layer waits only for its own uploads
+    qec.moe_set_upload_overlap(ctx, True)
     n = args.large_decode_steps
     for phase, (label, T, _) in enumerate(wl.phases):
         if label != "decode":
