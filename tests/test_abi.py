@@ -50,3 +50,21 @@ def test_init_rejects_bad_config_without_a_device():
         qec.moe_layer_init(hidden=256, ffn=64, n_experts=5000, top_k=2, n_layers=1, slots_per_tensor=8, max_tokens=4)
     with pytest.raises(qec.MoeError):
         qec.moe_layer_init(hidden=256, ffn=64, n_experts=8, top_k=9, n_layers=1, slots_per_tensor=8, max_tokens=4)
+
+
+def test_init_rejects_bad_formats_and_shared_experts_without_a_device():
+    def bad(**kw):
+        args = dict(hidden=256, ffn=256, n_experts=8, top_k=2, n_layers=1, slots_per_tensor=8, max_tokens=4)
+        args.update(kw)
+        with pytest.raises(qec.MoeError) as ei:
+            qec.moe_layer_init(**args)
+        assert ei.value.code == -1
+        return qec.moe_last_error(None)
+
+    assert "weight_format" in bad(weight_format=7)
+    # Q4_K needs widths that are whole 256-weight super-blocks
+    bad(weight_format=qec.FMT_Q4_K, hidden=256, ffn=320)
+    bad(weight_format=qec.FMT_Q4_K, hidden=320, ffn=256)
+    # a shared expert takes table column E, so E + 1 ids must fit 12 bits
+    bad(shared_experts=1, n_experts=4096, top_k=2)
+    bad(shared_experts=2)
