@@ -55,10 +55,11 @@ def parse():
                     help="timed decode steps of each of the Q8_0 / Q5_0 weight-format legs (0 skips them)")
     ap.add_argument("--pool-steps", type=int, default=256,
                     help="decode tokens per run of the pool-mode / preheat leg (0 skips it)")
-    ap.add_argument("--case", default=None, choices=["decode_layer", "decode_layer_cold", "prefill_layer"],
+    ap.add_argument("--case", default=None,
+                    choices=["decode_layer", "decode_layer_cold", "decode_layer_q8", "prefill_layer"],
                     help="small profiling case: one layer (hidden 2048, 512 experts, top-8, FFN 1152, every "
-                         "expert resident, or every expert in host memory for decode_layer_cold), --launches "
-                         "forwards at batch 1 (routed) or 4096 tokens")
+                         "expert resident, or every expert in host memory for decode_layer_cold, Q8_0 weights "
+                         "for decode_layer_q8), --launches forwards at batch 1 (routed) or 4096 tokens")
     ap.add_argument("--launches", type=int, default=20)
     return ap.parse_args()
 
@@ -451,10 +452,11 @@ def run_case(args):
     H, F, E, k = 2048, 1152, 512, 8
     T = 4096 if args.case == "prefill_layer" else 1
     cap = 0 if args.case == "decode_layer_cold" else E
+    fmt = synth.FMT_Q8_0 if args.case == "decode_layer_q8" else synth.FMT_Q4
     n = max(3, args.launches)
-    wl = synth.Workload("case", H, E, k, F, 1, routing="zipf", zipf_s=1.1, capacity=[cap])
+    wl = synth.Workload("case", H, E, k, F, 1, routing="zipf", zipf_s=1.1, capacity=[cap], weight_format=fmt)
     st = torch.cuda.current_stream()
-    ctx = qec.moe_layer_init(H, F, E, k, 1, E, T, stream=st.cuda_stream)
+    ctx = qec.moe_layer_init(H, F, E, k, 1, E, T, stream=st.cuda_stream, weight_format=fmt)
     for kind in range(3):
         rows, cols = wl.tensor_shapes[kind]
         qec.register_expert_tensor(ctx, 0, kind, wl.expert_tensor(0, kind), rows, cols, cap, wl.seed_order(0),
