@@ -29,12 +29,39 @@ static void record(cudaEvent_t e, cudaStream_t st) {
 }
 
 
-// --------------------------------------------------------------- top-k
+// Programmatic dependent launch for the chained small kernels (top-k, plan,
+// gate/up, down): wait for the previous kernel in the stream (a no-op when
+// launched without the attribute), then let the next one be scheduled.  The
+// wait comes first, so nothing of the previous kernel's output is read early;
+// what overlaps is the next launch's latency.
+__device__ __forceinline__ void pdl_enter() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
+// --------------------------------------------------------------- top-k// --------------------------------------------------------------- top-k
 // One warp per token; lane l holds logits l, l+32, ... (V per lane).  k
 // rounds of a warp arg-max over (value desc, index asc).
 template <int V>
 __global__ void __launch_bounds__(256) topk_kernel(const float *__restrict__ logits, int T, int E, int k,
                                                    int renorm, int32_t *__restrict__ idx, float *__restrict__ w) {
+    pdl_enter();
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= T) return;
@@ -104,17 +131,18 @@ __global__ void __launch_bounds__(256) topk_kernel(const float *__restrict__ log
 int launch_topk(const float *logits, int T, int E, int k, int renorm, int32_t *idx, float *w, cudaStream_t st) {
     if (T <= 0) return 0;
     dim3 block(256), grid((T + 7) / 8);
+    cudaError_t e;
     if (E <= 32)
-        topk_kernel<1><<<grid, block, 0, st>>>(logits, T, E, k, renorm, idx, w);
+        e = launch_pdl(topk_kernel<1>, grid, block, 0, st, logits, T, E, k, renorm, idx, w);
     else if (E <= 128)
-        topk_kernel<4><<<grid, block, 0, st>>>(logits, T, E, k, renorm, idx, w);
+        e = launch_pdl(topk_kernel<4>, grid, block, 0, st, logits, T, E, k, renorm, idx, w);
     else if (E <= 512)
-        topk_kernel<16><<<grid, block, 0, st>>>(logits, T, E, k, renorm, idx, w);
+        e = launch_pdl(topk_kernel<16>, grid, block, 0, st, logits, T, E, k, renorm, idx, w);
     else if (E <= 1024)
-        topk_kernel<32><<<grid, block, 0, st>>>(logits, T, E, k, renorm, idx, w);
+        e = launch_pdl(topk_kernel<32>, grid, block, 0, st, logits, T, E, k, renorm, idx, w);
     else
-        topk_kernel<128><<<grid, block, 0, st>>>(logits, T, E, k, renorm, idx, w);
-    return (int)cudaGetLastError();
+        e = launch_pdl(topk_kernel<128>, grid, block, 0, st, logits, T, E, k, renorm, idx, w);
+    return (int)e;
 }
 
 // --------------------------------------------------------------- quantize
@@ -169,6 +197,7 @@ __device__ __forceinline__ int block_excl_scan(int v, int *warp_tot) {
 }
 
 __global__ void __launch_bounds__(1024) plan_kernel(PlanParams p) {
+    pdl_enter();
     extern __shared__ int sm[];
     int *cnt = sm;            // [E]
     int *cur = sm + p.E;      // [E]
@@ -229,8 +258,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanParams p) {
 
 int launch_plan(const PlanParams &p, cudaStream_t st) {
     size_t smem = (size_t)2 * p.E * sizeof(int);
-    plan_kernel<<<1, 1024, smem, st>>>(p);
-    return (int)cudaGetLastError();
+    return (int)launch_pdl(plan_kernel, dim3(1), dim3(1024), smem, st, p);
 }
 
 // --------------------------------------------------------------- gate/up
@@ -244,6 +272,7 @@ constexpr int kGULanes = 8;
 
 template <int FMT>
 __global__ void __launch_bounds__(256) gate_up_kernel(GemvParams p) {
+    pdl_enter();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int sub = lane % kGULanes, grp = lane / kGULanes;
     const int rloc = warp * (32 / kGULanes) + grp;  // 0..31
@@ -344,6 +373,7 @@ __global__ void __launch_bounds__(256) gate_up_kernel(GemvParams p) {
 // row block) sums y[t][rows] = sum_j w[t][j] * o[t*k+j][rows] in j order.
 template <int L, int FMT>
 __global__ void __launch_bounds__(256) down_kernel(GemvParams p) {
+    pdl_enter();
     constexpr int G = 32 / L;          // rows per warp
     constexpr int ROWS = kWarps * G;   // rows per item
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -447,29 +477,29 @@ int down_rows_per_item(int F) {
 }
 
 template <int FMT>
-void launch_gemv_fmt(const GemvParams &p, int grid_gu, int grid_dn, cudaStream_t st, cudaEvent_t const *ev) {
-    gate_up_kernel<FMT><<<grid_gu, 256, 0, st>>>(p);
+cudaError_t launch_gemv_fmt(const GemvParams &p, int grid_gu, int grid_dn, cudaStream_t st, cudaEvent_t const *ev) {
+    cudaError_t e = launch_pdl(gate_up_kernel<FMT>, dim3(grid_gu), dim3(256), 0, st, p);
+    if (e != cudaSuccess) return e;
     if (ev) record(ev[1], st);
     if (ev) record(ev[2], st);
-    if (p.F / kBlock <= 40)
-        down_kernel<4, FMT><<<grid_dn, 256, 0, st>>>(p);
-    else
-        down_kernel<8, FMT><<<grid_dn, 256, 0, st>>>(p);
+    if (p.F / kBlock <= 40) return launch_pdl(down_kernel<4, FMT>, dim3(grid_dn), dim3(256), 0, st, p);
+    return launch_pdl(down_kernel<8, FMT>, dim3(grid_dn), dim3(256), 0, st, p);
 }
 
 // ev (optional): 4 events recorded around the gate/up and the down launch.
 int launch_gemv(const GemvParams &p, int grid_gu, int grid_dn, cudaStream_t st, cudaEvent_t const *ev) {
     if (ev) record(ev[0], st);
+    cudaError_t e;
     if (p.fmt == kFmtQ8)
-        launch_gemv_fmt<kFmtQ8>(p, grid_gu, grid_dn, st, ev);
+        e = launch_gemv_fmt<kFmtQ8>(p, grid_gu, grid_dn, st, ev);
     else if (p.fmt == kFmtQ4K)
-        launch_gemv_fmt<kFmtQ4K>(p, grid_gu, grid_dn, st, ev);
+        e = launch_gemv_fmt<kFmtQ4K>(p, grid_gu, grid_dn, st, ev);
     else if (p.fmt == kFmtQ5)
-        launch_gemv_fmt<kFmtQ5>(p, grid_gu, grid_dn, st, ev);
+        e = launch_gemv_fmt<kFmtQ5>(p, grid_gu, grid_dn, st, ev);
     else
-        launch_gemv_fmt<kFmtQ4>(p, grid_gu, grid_dn, st, ev);
+        e = launch_gemv_fmt<kFmtQ4>(p, grid_gu, grid_dn, st, ev);
     if (ev) record(ev[3], st);
-    return (int)cudaGetLastError();
+    return (int)e;
 }
 
 // --------------------------------------------------------------- fused layer
@@ -1755,6 +1785,7 @@ int launch_count_assign(const int32_t *idx, int n, int E, uint32_t *cnt, cudaStr
 // bit 0 and are replaced by e_shared, which the plan then reads as valid).
 __global__ void shared_assign_kernel(const int32_t *__restrict__ idx, const float *__restrict__ w, int T, int k,
                                      int e_shared, int32_t *idx_a, float *w_a, int *error) {
+    pdl_enter();
     const int ka = k + 1;
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < T * ka; i += gridDim.x * blockDim.x) {
         const int t = i / ka, j = i - t * ka;
@@ -1778,8 +1809,8 @@ int launch_shared_assign(const int32_t *idx, const float *w, int T, int k, int e
     const int n = T * (k + 1);
     if (n <= 0) return 0;
     const int grid = (n + 255) / 256 < 152 ? (n + 255) / 256 : 152;
-    shared_assign_kernel<<<grid, 256, 0, st>>>(idx, w, T, k, e_shared, idx_a, w_a, error);
-    return (int)cudaGetLastError();
+    return (int)launch_pdl(shared_assign_kernel, dim3(grid), dim3(256), 0, st, idx, w, T, k, e_shared, idx_a, w_a,
+                           error);
 }
 
 // Debug: keep one thread of the stream busy for a bounded time (global
