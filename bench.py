@@ -147,11 +147,27 @@ class ClockSampler:
 
 
 def src_hash(paths):
+    """Hash of source text: a path (the whole file) or (path, first line,
+    end line) for the part of a file from its first marker line up to the end
+    marker (a kernel and the device helpers it uses)."""
     h = hashlib.sha256()
     for p in paths:
-        with open(os.path.join(ROOT, p), "rb") as f:
-            h.update(f.read())
+        path, a, b = (p, None, None) if isinstance(p, str) else p
+        with open(os.path.join(ROOT, path), "rb") as f:
+            txt = f.read()
+        if a is not None:
+            i = txt.index(a.encode())
+            txt = txt[i:txt.index(b.encode(), i)]
+        h.update(txt)
     return h.hexdigest()[:16]
+
+
+# the fused decode layer kernel: its section of kernels_decode.cu and the
+# shared device header (the traffic summary is valid while these are unchanged)
+DECODE_KERNEL_SRC = [("quantized_expert_cache_gb300/csrc/kernels_decode.cu",
+                      "// --------------------------------------------------------------- fused layer",
+                      "// --------------------------------------------------------------- hooks"),
+                     "quantized_expert_cache_gb300/csrc/common.cuh"]
 
 
 def read_traffic(kernel_file, key):
@@ -167,8 +183,7 @@ def read_traffic(kernel_file, key):
                 k, v = line.split(":", 1)
                 vals[k.strip()] = v.strip()
     try:
-        if vals.get("bench.source_hash") != src_hash(["quantized_expert_cache_gb300/csrc/kernels_decode.cu",
-                                                      "quantized_expert_cache_gb300/csrc/common.cuh"]):
+        if vals.get("bench.source_hash") != src_hash(DECODE_KERNEL_SRC):
             return None
         return float(vals[key])
     except (KeyError, ValueError):
