@@ -194,6 +194,16 @@ def read_traffic(kernel_file, key):
 # workload setup
 # ----------------------------------------------------------------------------
 
+def decode_workload_desc(wl):
+    """The decode workload as both arms name it in `config`."""
+    L, H, E, k, F = wl.n_layers, wl.hidden, wl.n_experts, wl.top_k, wl.ffn
+    T = wl.phases[0][1]
+    caps = [wl.layer_capacity(l) for l in range(L)]
+    return (f"{wl.name}: {L} MoE layers, hidden {H}, {E} experts, top-{k}, FFN {F} SwiGLU, Q4 blocks of 32, "
+            f"Zipf({wl.zipf_s}) routing, batch {T} decode, HBM pool {caps.count(E)} full layers + "
+            f"{min(caps)}/{E} hot set on the rest")
+
+
 def register_workload(qec, synth, ctx, wl, log):
     t0 = time.time()
     bufs = {}
@@ -413,10 +423,7 @@ def run_ours(args):
         "metric": METRIC, "value": round(tok_per_s, 2), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
-        "config": {"workload": f"{wl.name}: {L} MoE layers, hidden {H}, {E} experts, top-{k}, FFN {F} SwiGLU, "
-                               f"Q4 blocks of 32, Zipf({wl.zipf_s}) routing, batch {T} decode, HBM pool "
-                               f"{[wl.layer_capacity(l) for l in range(L)].count(E)} full layers + "
-                               f"{min(wl.layer_capacity(l) for l in range(L))}/{E} hot set on the rest",
+        "config": {"workload": decode_workload_desc(wl),
                    "l2": "inputs larger than L2: ~1.5 GB of expert weights per step vs 129 MB L2",
                    "cuda_graph": used_graph, "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "kernel": "decode_layer_kernel (fused expert FFN, resident layers)",
@@ -869,7 +876,8 @@ def cpu_baseline(wl, n_steps, T):
     for x, idx, w, (g, u, d) in work:
         oracle.layer(x, idx, w, g, u, d, wl.hidden, wl.ffn)
     dt = time.perf_counter() - t0
-    return {"value": round(n_steps * T / dt, 4), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+    return {"value": round(n_steps * T / dt, 4), "unit": "tokens/s", "cores": 1, "host_cores": os.cpu_count(),
+            "kind": "oracle",
             "sample": f"{n_steps} decode steps x {wl.n_layers} layers (batch {T}), single-threaded C oracle, "
                       f"{dt:.1f}s"}
 
@@ -902,8 +910,9 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
-        "config": {"workload": f"{wl.name} (CPU oracle)", "parallelism": "single host core"},
-        "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+        "config": {"workload": decode_workload_desc(wl), "parallelism": "single host core (the CPU oracle)"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": 1, "host_cores": os.cpu_count(),
+                         "kind": "oracle",
                          "sample": f"each step: layers {layers} of {L} for one token, scaled by {L}/{len(layers)}"},
         "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
