@@ -44,27 +44,31 @@ def build(force: bool = False) -> str:
     return _OUT
 
 
+def configure(L):
+    """Set the argument and result types of a loaded oracle library."""
+    i32, vp, f32 = ctypes.c_int, ctypes.c_void_p, ctypes.c_float
+    L.orc_h2d.restype = ctypes.c_double
+    L.orc_h2d.argtypes = [ctypes.c_uint16]
+    L.orc_f2h.restype = ctypes.c_uint16
+    L.orc_f2h.argtypes = [f32]
+    L.orc_topk.argtypes = [vp, i32, i32, i32, i32, vp, vp]
+    L.orc_quantize_blocks.argtypes = [vp, i32, vp, vp]
+    L.orc_dequant_fmt.argtypes = [vp, i32, i32, vp]
+    L.orc_block_dot_fmt.restype = ctypes.c_int32
+    L.orc_block_dot_fmt.argtypes = [vp, vp, i32]
+    L.orc_row_dot_fmt.restype = ctypes.c_double
+    L.orc_row_dot_fmt.argtypes = [vp, vp, vp, i32, i32, vp]
+    L.orc_k4_subdots.argtypes = [vp, vp, vp]
+    L.orc_expert.argtypes = [vp, vp, vp, i32, i32, vp, vp] + [vp] * 8 + [i32]
+    L.orc_down_combine.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, i32]
+    L.orc_layer.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp] + [vp] * 9 + [i32]
+    return L
+
+
 def lib():
     global _lib
     if _lib is None:
-        L = ctypes.CDLL(build())
-        i32, vp, f32 = ctypes.c_int, ctypes.c_void_p, ctypes.c_float
-        L.orc_h2d.restype = ctypes.c_double
-        L.orc_h2d.argtypes = [ctypes.c_uint16]
-        L.orc_f2h.restype = ctypes.c_uint16
-        L.orc_f2h.argtypes = [f32]
-        L.orc_topk.argtypes = [vp, i32, i32, i32, i32, vp, vp]
-        L.orc_quantize_blocks.argtypes = [vp, i32, vp, vp]
-        L.orc_dequant_fmt.argtypes = [vp, i32, i32, vp]
-        L.orc_block_dot_fmt.restype = ctypes.c_int32
-        L.orc_block_dot_fmt.argtypes = [vp, vp, i32]
-        L.orc_row_dot_fmt.restype = ctypes.c_double
-        L.orc_row_dot_fmt.argtypes = [vp, vp, vp, i32, i32, vp]
-        L.orc_k4_subdots.argtypes = [vp, vp, vp]
-        L.orc_expert.argtypes = [vp, vp, vp, i32, i32, vp, vp] + [vp] * 8 + [i32]
-        L.orc_down_combine.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, i32]
-        L.orc_layer.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp] + [vp] * 9 + [i32]
-        _lib = L
+        _lib = configure(ctypes.CDLL(build()))
     return _lib
 
 

@@ -57,6 +57,8 @@ def test_hand_traced_borrow_return(golden):
         assert ",".join(owners(int(tid))) == ob
     misses = p.step(4, {0: [0, 3], 1: [4]})
     assert misses == [0, (1 << 12) | 4]
+    # slots are lent: nothing admitted and no sighting recorded
+    assert p.snapshot(0)["last_seen"][0] == -1 and p.snapshot(1)["last_seen"][4] == -1
     for tid, _, oa, sa, *_ in rows:
         assert ",".join(owners(int(tid))) == oa
         assert p.snapshot(int(tid))["stamp"] == _ints(sa)
@@ -138,6 +140,8 @@ def test_hand_traced_global_pool(golden):
         p.borrow(2)
         assert ",".join(_owners(p.pool_snapshot()["owner"])) == own_b
         assert p.step(2, {0: [1], 1: [2]}) == _ints(miss)
+        # lent slots: nothing admitted, no sighting recorded
+        assert p.snapshot(0)["last_seen"][1] == -1 and p.snapshot(1)["last_seen"][2] == -1
         p.check_invariants()
         counts = {0: [0, 3, 7, 0, 0, 0]} if case == "preheat" else None
         p.give_back(counts)
