@@ -567,3 +567,20 @@ def test_q4k_layer_vs_dense_fp64():
             ha = hq.astype(np.float64) * np.repeat(hd.view(np.float16).astype(np.float64), 32)
             y_bf[t] += w[t, j] * (Wd[e] @ ha)
     np.testing.assert_allclose(y, y_bf, rtol=1e-12, atol=1e-12 * np.abs(y_bf).max())
+
+
+@pytest.mark.parametrize("fmt", [synth.FMT_Q8_0, synth.FMT_Q5_0, synth.FMT_Q4_K])
+def test_generators_of_every_format_are_range_and_thread_independent(fmt):
+    # the same expert's bytes whether generated alone or in a range, with any
+    # thread count (the oracle and the library register the same weights)
+    wl = synth.Workload("g", 512, 16, 2, 512, 2, weight_format=fmt)
+    a = wl.expert_tensor(1, synth.KIND_DOWN, 3, 9, threads=4)
+    b = wl.expert_tensor(1, synth.KIND_DOWN, 6, 7, threads=1)
+    assert np.array_equal(a[3], b[0])
+    assert a.shape[-1] == synth.BLOCK_BYTES[fmt] and a.shape[-2] == 512 // synth.BLOCK_ELEMS[fmt]
+    # another tensor of the same layer draws other bytes
+    c = wl.expert_tensor(1, synth.KIND_UP, 6, 7, threads=1)
+    assert not np.array_equal(c, b)
+    # every weight within the shared |w| <= 0.16 envelope
+    w = oracle.dequant(a.reshape(-1, a.shape[-2], a.shape[-1]))
+    assert np.abs(w).max() <= 0.16 * 1.01
