@@ -5,7 +5,7 @@ with a quantized expert cache, used to check the CUDA path.  Only the tests,
 ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline leg may import
 it.  It shares no code with the CUDA library, and the library never calls it.
 
-- ``moe_oracle.c``: numerics (top-k, activation quantization, Q4, Q8_0, Q5_0 and Q4_K block dots,
+- ``moe_oracle.c``: numerics (top-k, activation quantization, Q4, Q8_0, Q5_0, Q4_K and Q6_K block dots,
   SwiGLU, down projection and combine), binary64 with the integer-deciding
   steps in binary32 (see the header of that file);
 - ``policy.py``: the admission / eviction policy of the expert pools.
@@ -59,6 +59,7 @@ def configure(L):
     L.orc_row_dot_fmt.restype = ctypes.c_double
     L.orc_row_dot_fmt.argtypes = [vp, vp, vp, i32, i32, vp]
     L.orc_k4_subdots.argtypes = [vp, vp, vp]
+    L.orc_k6_blockdots.argtypes = [vp, vp, vp]
     L.orc_expert.argtypes = [vp, vp, vp, i32, i32, vp, vp] + [vp] * 8 + [i32]
     L.orc_down_combine.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, i32]
     L.orc_layer.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp] + [vp] * 9 + [i32]
@@ -106,13 +107,14 @@ def quantize(x: np.ndarray):
     return q, d
 
 
-BLOCK_BYTES = {18: 0, 34: 1, 22: 2, 144: 3}  # canonical block size -> format (0: Q4, 1: Q8_0, 2: Q5_0, 3: Q4_K)
-ELEMS = {0: 32, 1: 32, 2: 32, 3: 256}        # weights per canonical block
+# canonical block size -> format (0: Q4, 1: Q8_0, 2: Q5_0, 3: Q4_K, 4: Q6_K)
+BLOCK_BYTES = {18: 0, 34: 1, 22: 2, 144: 3, 210: 4}
+ELEMS = {0: 32, 1: 32, 2: 32, 3: 256, 4: 256}  # weights per canonical block
 
 
 def _fmt(blocks) -> int:
     """Format of canonical blocks from their last dimension (18: Q4, 34: Q8_0, 22: Q5_0,
-    144: Q4_K super-blocks of 256 weights)."""
+    144: Q4_K and 210: Q6_K super-blocks of 256 weights)."""
     if blocks.shape[-1] not in BLOCK_BYTES:
         raise ValueError(f"unknown block size {blocks.shape[-1]}")
     return BLOCK_BYTES[blocks.shape[-1]]
@@ -135,6 +137,17 @@ def subblock_dots(superblock: np.ndarray, qa: np.ndarray) -> np.ndarray:
     qa = np.ascontiguousarray(qa, np.int8)
     out = np.empty(8, np.int32)
     lib().orc_k4_subdots(_p(sb), _p(qa), _p(out))
+    return out
+
+
+def q6k_blockdots(superblock: np.ndarray, qa: np.ndarray) -> np.ndarray:
+    """Q6_K: the integer dots of the 8 32-weight blocks of one super-block
+    (each = the two 16-weight halves' sums of (q - 32) * a times their scales)."""
+    sb = np.ascontiguousarray(superblock, np.uint8)
+    assert sb.size == 210 and qa.size == 256
+    qa = np.ascontiguousarray(qa, np.int8)
+    out = np.empty(8, np.int32)
+    lib().orc_k6_blockdots(_p(sb), _p(qa), _p(out))
     return out
 
 

@@ -37,7 +37,13 @@
  *  (b[j-4] >> 6) << 4, m = (b[j+4] >> 4) | (b[j] >> 6) << 4), then 128 code
  *  bytes in 4 chunks of 32: chunk c holds sub-block 2c in its low nibbles and
  *  sub-block 2c+1 in its high nibbles (byte i of a chunk = element i of each).
- *  Per 32 weights that is 18 bytes, as for Q4.
+ *  Per 32 weights that is 18 bytes, as for Q4.  4 = Q6_K, another K-quant:
+ *  super-blocks of 256 weights = 16 sub-blocks of 16 with a signed 8-bit
+ *  scale sc_j each, one binary16 scale d and 6-bit codes q,
+ *  w = d * sc_j * (q - 32).  Reading of the 210-byte layout: 128 bytes of
+ *  low nibbles (byte t: element t in the low, element t + 128 in the high
+ *  nibble), 64 bytes of high bit pairs (byte u, bits 2m..2m+1: element
+ *  u + 64 m), the 16 scales, then d.
  *
  * Readings where the pages are silent (each listed in the design notes):
  *  - top-k order is (logit descending, expert index ascending): ties go to
@@ -67,10 +73,50 @@
 #define ORC_Q5_BLOCK_BYTES 22
 
 #define ORC_K4_SUPER_BYTES 144
+#define ORC_K6_SUPER_BYTES 210
+
+double orc_h2d(uint16_t h);
 
 /* Bytes per 32 weights (Q4_K: a 144-byte super-block holds 256). */
 static size_t orc_bbytes(int fmt) {
     return fmt == 1 ? ORC_Q8_BLOCK_BYTES : fmt == 2 ? ORC_Q5_BLOCK_BYTES : ORC_BLOCK_BYTES;
+}
+
+/* Bytes of a row of nb 32-weight blocks (super-block formats: nb / 8 of them). */
+static size_t orc_row_bytes(int fmt, int nb) {
+    if (fmt == 3) return (size_t)(nb / 8) * ORC_K4_SUPER_BYTES;
+    if (fmt == 4) return (size_t)(nb / 8) * ORC_K6_SUPER_BYTES;
+    return (size_t)nb * orc_bbytes(fmt);
+}
+
+/* Q6_K: 6-bit code of element i (0..255) of a super-block. */
+static int orc_k6_code(const uint8_t *sb, int i) {
+    const uint8_t *ql = sb, *qh = sb + 128;
+    const int lo = i < 128 ? (ql[i] & 15) : (ql[i - 128] >> 4);
+    const int hi = (qh[i % 64] >> (2 * (i / 64))) & 3;
+    return lo | (hi << 4);
+}
+
+/* Q6_K: signed scale of 16-weight sub-block j (0..15) and the super-block's d. */
+static int orc_k6_scale(const uint8_t *sb, int j) { return (int)(int8_t)sb[192 + j]; }
+static double orc_k6_d(const uint8_t *sb) { return orc_h2d((uint16_t)(sb[208] | (sb[209] << 8))); }
+
+/* Q6_K: the integer dot of each 32-weight block against 32 int8
+ * activations: sc_2b * sum_{i<16} (q-32) a + sc_2b+1 * sum_{16<=i<32} (q-32) a
+ * (exact in int32: |.| <= 2 * 128 * 16 * 32 * 127). */
+void orc_k6_blockdots(const uint8_t *sb, const int8_t *qa, int32_t *out) {
+    for (int b = 0; b < 8; ++b) {
+        int32_t s = 0;
+        for (int h = 0; h < 2; ++h) {
+            int32_t t = 0;
+            for (int i = 0; i < 16; ++i) {
+                const int e = 32 * b + 16 * h + i;
+                t += (int32_t)(orc_k6_code(sb, e) - 32) * (int32_t)qa[e];
+            }
+            s += orc_k6_scale(sb, 2 * b + h) * t;
+        }
+        out[b] = s;
+    }
 }
 
 /* Q4_K: scale and min of sub-block j (0..7) of a super-block. */
@@ -232,6 +278,15 @@ static uint16_t orc_block_scale(const uint8_t *blk) { return (uint16_t)(blk[0] |
 /* Dequantized weights of nb blocks: w = d * (q - 8) (Q4), d * q (Q8_0) or
  * d * (q - 16) (Q5_0). */
 void orc_dequant_fmt(const uint8_t *blocks, int nb, int fmt, double *out) {
+    if (fmt == 4) { /* Q6_K: w = d * sc_j * (q - 32), sub-blocks of 16 */
+        for (int s = 0; s < nb / 8; ++s) {
+            const uint8_t *sb = blocks + (size_t)s * ORC_K6_SUPER_BYTES;
+            const double d = orc_k6_d(sb);
+            for (int i = 0; i < 256; ++i)
+                out[(size_t)s * 256 + i] = d * orc_k6_scale(sb, i / 16) * (double)(orc_k6_code(sb, i) - 32);
+        }
+        return;
+    }
     if (fmt == 3) { /* nb counts 32-weight blocks; super-blocks of 8 */
         for (int s = 0; s < nb / 8; ++s) {
             const uint8_t *sb = blocks + (size_t)s * ORC_K4_SUPER_BYTES;
@@ -269,6 +324,22 @@ int32_t orc_block_dot(const uint8_t *blk, const int8_t *qa) { return orc_block_d
  * sum_b |d_w,b * d_a,b * sumi_b| (for error bounds), if not NULL. */
 double orc_row_dot_fmt(const uint8_t *row, const int8_t *qa, const uint16_t *da, int nb, int fmt, double *abs_sum) {
     double acc = 0.0, aacc = 0.0;
+    if (fmt == 4) {
+        /* per 32-weight block b: d_a,b * d * (its integer dot) */
+        for (int s = 0; s < nb / 8; ++s) {
+            const uint8_t *sb = row + (size_t)s * ORC_K6_SUPER_BYTES;
+            const double d = orc_k6_d(sb);
+            int32_t dots[8];
+            orc_k6_blockdots(sb, qa + (size_t)s * 256, dots);
+            for (int j = 0; j < 8; ++j) {
+                const double term = orc_h2d(da[8 * s + j]) * d * (double)dots[j];
+                acc += term;
+                aacc += fabs(term);
+            }
+        }
+        if (abs_sum) *abs_sum = aacc;
+        return acc;
+    }
     if (fmt == 3) {
         /* per sub-block b: d_a,b * (d * sc * sum q*a - dmin * m * sum a) */
         for (int s = 0; s < nb / 8; ++s) {
@@ -316,7 +387,7 @@ void orc_expert(const uint8_t *gate, const uint8_t *up, const uint8_t *down, int
                 const uint16_t *xd, double *g_out, double *u_out, double *gabs, double *uabs, double *h_out,
                 int8_t *hq_out, uint16_t *hd_out, double *o, int fmt) {
     int nbh = H / ORC_BLOCK, nbf = F / ORC_BLOCK;
-    size_t rowh = (size_t)nbh * orc_bbytes(fmt), rowf = (size_t)nbf * orc_bbytes(fmt);
+    size_t rowh = orc_row_bytes(fmt, nbh), rowf = orc_row_bytes(fmt, nbf);
     float h32[F > 0 ? F : 1];
     int8_t hq[F > 0 ? F : 1];
     uint16_t hd[F / ORC_BLOCK > 0 ? F / ORC_BLOCK : 1];
@@ -343,7 +414,7 @@ void orc_expert(const uint8_t *gate, const uint8_t *up, const uint8_t *down, int
 void orc_down_combine(int T, int H, int F, int k, const int32_t *idx, const double *w,
                       const uint8_t *const *down, const int8_t *hq, const uint16_t *hd, double *y, int fmt) {
     int nbf = F / ORC_BLOCK;
-    size_t rowf = (size_t)nbf * orc_bbytes(fmt);
+    size_t rowf = orc_row_bytes(fmt, nbf);
     for (int t = 0; t < T; ++t) {
         double *yt = y + (size_t)t * H;
         for (int i = 0; i < H; ++i) yt[i] = 0.0;

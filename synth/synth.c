@@ -210,6 +210,31 @@ void synth_q4k_blocks(uint64_t key, uint8_t *out, size_t n_super, double dlo, do
     }
 }
 
+/*
+ * Canonical Q6_K super-blocks of 256 weights, 210 bytes each: 192 uniform
+ * bytes of 6-bit codes (ql, qh), 16 signed scales ~ U{-64..63}, then a
+ * binary16 d ~ U(dlo, dhi).
+ */
+void synth_q6k_blocks(uint64_t key, uint8_t *out, size_t n_super, double dlo, double dhi) {
+    xo_t g;
+    xo_init(&g, key);
+    for (size_t b = 0; b < n_super; ++b) {
+        uint8_t *sb = out + b * 210;
+        for (int w = 0; w < 192; w += 8) {
+            uint64_t v = xo_next(&g);
+            for (int j = 0; j < 8; ++j) sb[w + j] = (uint8_t)(v >> (8 * j));
+        }
+        uint64_t v0 = xo_next(&g), v1 = xo_next(&g);
+        for (int j = 0; j < 16; ++j) {
+            const unsigned byte = (unsigned)(((j < 8 ? v0 : v1) >> (8 * (j & 7))) & 0xff);
+            sb[192 + j] = (uint8_t)(int8_t)((int)(byte % 128) - 64);
+        }
+        uint16_t h = gen_f16_bits((float)(dlo + (dhi - dlo) * xo_unit(&g)));
+        sb[208] = (uint8_t)(h & 0xff);
+        sb[209] = (uint8_t)(h >> 8);
+    }
+}
+
 typedef struct {
     uint64_t seed, tag;
     int e0, e1, fmt;
@@ -220,11 +245,13 @@ typedef struct {
 
 static void *q4_worker(void *arg) {
     q4_job_t *j = (q4_job_t *)arg;
-    const size_t bb = j->fmt == 1 ? 34 : j->fmt == 2 ? 22 : j->fmt == 3 ? 144 : 18;
+    const size_t bb = j->fmt == 1 ? 34 : j->fmt == 2 ? 22 : j->fmt == 3 ? 144 : j->fmt == 4 ? 210 : 18;
     for (int e = j->e0; e < j->e1; ++e) {
         uint64_t key = synth_key(j->seed, 1, j->tag, (uint64_t)e, 0);
         uint8_t *dst = j->out + (size_t)e * j->blocks_per_expert * bb;
-        if (j->fmt == 3)
+        if (j->fmt == 4)
+            synth_q6k_blocks(key, dst, j->blocks_per_expert, j->dlo, j->dhi);
+        else if (j->fmt == 3)
             synth_q4k_blocks(key, dst, j->blocks_per_expert, j->dlo, j->dhi, 0.0006, 0.0025);
         else if (j->fmt == 1)
             synth_q8_blocks(key, dst, j->blocks_per_expert, j->dlo, j->dhi);
@@ -239,14 +266,15 @@ static void *q4_worker(void *arg) {
 /*
  * All experts of one expert tensor, expert-major: out[e][block] (18 B each
  * for Q4, fmt 0; 34 B for Q8_0, fmt 1; 22 B for Q5_0, fmt 2; 144-byte
- * super-blocks of 256 weights for Q4_K, fmt 3, with dmin ~ U(0.0006, 0.0025)).
+ * super-blocks of 256 weights for Q4_K, fmt 3, with dmin ~ U(0.0006, 0.0025);
+ * 210-byte super-blocks for Q6_K, fmt 4).
  * Expert e is drawn from its own stream keyed by (seed, 1, tensor_tag, e), so
  * the result does not depend on n_threads and any expert can be regenerated
  * alone with synth_experts(seed, tag, e, e+1, ...).
  */
 void synth_experts(uint64_t seed, uint64_t tensor_tag, int e_begin, int e_end, size_t blocks_per_expert,
                    uint8_t *out, double dlo, double dhi, int n_threads, int fmt) {
-    const size_t bb = fmt == 1 ? 34 : fmt == 2 ? 22 : fmt == 3 ? 144 : 18;
+    const size_t bb = fmt == 1 ? 34 : fmt == 2 ? 22 : fmt == 3 ? 144 : fmt == 4 ? 210 : 18;
     int n = e_end - e_begin;
     if (n <= 0) return;
     if (n_threads < 1) n_threads = 1;

@@ -43,6 +43,10 @@ C_MUTANTS = [
     ("binary16 truncation", "double r = nearbyint(a / quantum); /* default rounding: ties to even */",
      "double r = floor(a / quantum);"),
     ("softmax over all logits", "if (renorm) {", "if (!renorm) {"),
+    ("q6k high pair index", "const int hi = (qh[i % 64] >> (2 * (i / 64))) & 3;",
+     "const int hi = (qh[i / 4] >> (2 * (i % 4))) & 3;"),
+    ("q6k offset 31", "t += (int32_t)(orc_k6_code(sb, e) - 32) * (int32_t)qa[e];",
+     "t += (int32_t)(orc_k6_code(sb, e) - 31) * (int32_t)qa[e];"),
 ]
 
 # oracle pins that take no fixture, and those that take the golden reader
@@ -55,9 +59,10 @@ C_PINS = [pins.test_h2d_all_bit_patterns_vs_numpy, pins.test_f2h_vs_numpy_random
           pins.test_q8_row_dot_vs_dense_fp64, pins.test_q8_layer_vs_dense_fp64_brute_force,
           pins.test_quantizer_zero_and_tiny_blocks, pins.test_q5_block_dot_brute_force_every_code,
           pins.test_q5_dequant_and_layer_vs_dense_fp64, pins.test_q4k_brute_force_vs_independent_decode,
-          pins.test_q4k_layer_vs_dense_fp64, pins.test_shared_expert_layer_vs_dense_fp64]
+          pins.test_q4k_layer_vs_dense_fp64, pins.test_shared_expert_layer_vs_dense_fp64,
+          pins.test_q6k_brute_force_vs_independent_decode, pins.test_q6k_layer_vs_dense_fp64]
 C_GOLDEN_PINS = [pins.test_h2d_golden, pins.test_block_dot_golden, pins.test_q8_block_dot_golden,
-                 pins.test_q5_block_dot_golden, pins.test_q4k_golden]
+                 pins.test_q5_block_dot_golden, pins.test_q4k_golden, pins.test_q6k_golden]
 
 
 def _failing_pins(run):

@@ -584,3 +584,80 @@ def test_generators_of_every_format_are_range_and_thread_independent(fmt):
     # every weight within the shared |w| <= 0.16 envelope
     w = oracle.dequant(a.reshape(-1, a.shape[-2], a.shape[-1]))
     assert np.abs(w).max() <= 0.16 * 1.01
+
+
+# ---------------------------------------------------------------- Q6_K weights
+def _np_q6k(sb):
+    """Independent Q6_K decode with numpy: [..., 210] -> codes q [..., 256],
+    signed scales [..., 16], d."""
+    sb = np.asarray(sb, np.uint8)
+    ql = sb[..., 0:128].astype(np.int64)
+    qh = sb[..., 128:192].astype(np.int64)
+    lo = np.concatenate([ql & 15, ql >> 4], axis=-1)                       # elements 0..127, 128..255
+    hi = np.concatenate([(qh >> (2 * m)) & 3 for m in range(4)], axis=-1)  # elements u + 64 m
+    sc = np.ascontiguousarray(sb[..., 192:208]).view(np.int8).astype(np.int64)
+    d = np.ascontiguousarray(sb[..., 208:210]).view(np.float16)[..., 0].astype(np.float64)
+    return lo | (hi << 4), sc, d
+
+
+def _q6k_weights(sb):
+    q, sc, d = _np_q6k(sb)
+    return d[..., None] * np.repeat(sc, 16, axis=-1) * (q - 32)
+
+
+def test_q6k_golden(golden):
+    (ql_over, qh_over, d, dots, weights), = golden("q6k_superblock.txt")
+    sb = np.zeros(210, np.uint8)
+    for kv in ql_over.split(","):
+        i, v = kv.split("=")
+        sb[int(i)] = int(v, 16)
+    for kv in qh_over.split(","):
+        i, v = kv.split("=")
+        sb[128 + int(i)] = int(v, 16)
+    sb[192:208] = (np.arange(16) - 8).astype(np.int8).view(np.uint8)
+    sb[208:210] = np.array([int(d, 16) & 0xFF, int(d, 16) >> 8], np.uint8)
+    a = np.ones(256, np.int8)
+    assert oracle.q6k_blockdots(sb, a).tolist() == [int(v) for v in dots.split(",")]
+    w = oracle.dequant(sb.reshape(1, 210))
+    for kv in weights.split(","):
+        i, v = kv.split("=")
+        assert w[int(i)] == float(v)
+
+
+def test_q6k_brute_force_vs_independent_decode():
+    sbs = synth.q6k_blocks(synth.key(7, 500), 60)
+    q, sc, _ = _np_q6k(sbs)
+    assert q.min() == 0 and q.max() == 63 and sc.min() == -64 and sc.max() == 63
+    acts = RNG.integers(-127, 128, (60, 256)).astype(np.int8)
+    for i in range(60):
+        t = ((q[i] - 32) * acts[i].astype(np.int64)).reshape(16, 16).sum(axis=1) * sc[i]
+        assert np.array_equal(oracle.q6k_blockdots(sbs[i], acts[i]), t.reshape(8, 2).sum(axis=1))
+    assert np.array_equal(oracle.dequant(sbs.reshape(3, 20, 210)), _q6k_weights(sbs).reshape(3, 20 * 256))
+
+
+def test_q6k_layer_vs_dense_fp64():
+    wl = synth.Workload("tiny_q6k", 512, 8, 2, 256, 1, routing="normal", weight_format=synth.FMT_Q6_K)
+    H, F, k, T = wl.hidden, wl.ffn, wl.top_k, 3
+    gate, up, down = (wl.expert_tensor(0, kd) for kd in range(3))
+    assert gate.shape == (8, F, H // 256, 210) and down.shape == (8, H, F // 256, 210)
+    x, logits = wl.x(0, 0, T), wl.logits(0, 0, T)
+    idx, w = oracle.topk(logits, k)
+    y, it = oracle.layer(x, idx, w, gate, up, down, H, F, want_intermediates=True)
+
+    def deq(t):
+        return _q6k_weights(t).reshape(t.shape[0], t.shape[1], -1)
+
+    Wg, Wu, Wd = deq(gate), deq(up), deq(down)
+    xa = it["xq"].astype(np.float64) * np.repeat(it["xd"].view(np.float16).astype(np.float64), 32, axis=1)
+    y_bf = np.zeros((T, H))
+    for t in range(T):
+        for j in range(k):
+            a, e = t * k + j, idx[t, j]
+            g, u = Wg[e] @ xa[t], Wu[e] @ xa[t]
+            np.testing.assert_allclose(it["g"][a], g, rtol=0, atol=1e-12 * np.abs(g).max())
+            h = g * u * expit(g)
+            hq, hd = oracle.quantize(h.astype(np.float32))
+            assert np.array_equal(hq, it["hq"][a]) and np.array_equal(hd, it["hd"][a])
+            ha = hq.astype(np.float64) * np.repeat(hd.view(np.float16).astype(np.float64), 32)
+            y_bf[t] += w[t, j] * (Wd[e] @ ha)
+    np.testing.assert_allclose(y, y_bf, rtol=1e-12, atol=1e-12 * np.abs(y_bf).max())
