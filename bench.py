@@ -61,6 +61,8 @@ def parse():
                          "expert resident, or every expert in host memory for decode_layer_cold, Q8_0 weights "
                          "for decode_layer_q8), --launches forwards at batch 1 (routed) or 4096 tokens")
     ap.add_argument("--launches", type=int, default=20)
+    ap.add_argument("--cold-launches", type=int, default=20,
+                    help="timed batch-1 forwards of the all-cold layer leg (0 skips it)")
     return ap.parse_args()
 
 
@@ -443,10 +445,18 @@ def run_ours(args):
     }
     qec.moe_destroy(ctx)
     del X, LG, Xp, LGp
+    link_peak = max(zc_gbs, ce_gbs)
+    out["host_link"]["peak_gbs"] = round(link_peak, 1)
+    out["host_link"]["peak_source"] = "best of the zero-copy read probe and the copy-engine H2D probe, this run"
     if args.prefill_steps > 0:
         out["prefill"] = run_prefill_leg(args, qec, synth, torch, log)
+        out["roofline_tensor"] = out["prefill"]["roofline_tensor"]
+    if args.cold_launches > 0:
+        out["cold_layer"] = run_cold_layer_leg(args, qec, synth, torch, log, link_peak)
     if args.pool_steps > 0:
-        out["pool"] = run_pool_leg(args, qec, synth, torch, log)
+        out["pool"] = run_pool_leg(args, qec, synth, torch, log, link_peak)
+        out["roofline_link"] = {"pool_per_tensor": out["pool"]["per_tensor"]["roofline_link"],
+                                "all_cold_layer": out.get("cold_layer", {}).get("roofline_link")}
     if args.large_decode_steps > 0:
         out["large_expert"] = run_large_expert_leg(args, qec, synth, torch, log)
     if args.q8_steps > 0:
@@ -505,7 +515,50 @@ def run_case(args):
     print(json.dumps(res), flush=True)
 
 
-def run_pool_leg(args, qec, synth, torch, log):
+def run_cold_layer_leg(args, qec, synth, torch, log, link_peak):
+    """One layer of the decode shape (hidden 2048, 512 experts, top-8, FFN
+    1152) with every expert in pinned host memory: each batch-1 routed
+    forward reads its 8 experts' 3 tensors zero-copy over the host link.
+    args.cold_launches forwards on fresh seeded inputs, each timed with CUDA
+    events (the first two untimed); link roofline = the weight bytes of the
+    experts each forward uses over its median time, against the link probe."""
+    H, F, E, k, T = 2048, 1152, 512, 8, 1
+    n = max(3, args.cold_launches)
+    wl = synth.Workload("cold_layer", H, E, k, F, 1, routing="zipf", zipf_s=1.1, capacity=[0])
+    stream = torch.cuda.Stream()
+    sp = stream.cuda_stream
+    ctx = qec.moe_layer_init(H, F, E, k, 1, 1, T, stream=sp)
+    for kind in range(3):
+        rows, cols = wl.tensor_shapes[kind]
+        qec.register_expert_tensor(ctx, 0, kind, wl.expert_tensor(0, kind), rows, cols, 0, wl.seed_order(0), 0)
+    xs = [torch.from_numpy(wl.x(0, s, T)).cuda() for s in range(n)]
+    lgs = [torch.from_numpy(wl.logits(0, s, T)).cuda() for s in range(n)]
+    idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, k), device="cuda")
+    y = torch.empty((T, H), device="cuda")
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for s in range(n):
+        evs[s][0].record(stream)
+        qec.moe_ffn_forward_routed(ctx, 0, xs[s], lgs[s], T, idx, w, y, sp)
+        evs[s][1].record(stream)
+    stream.synchronize()
+    qec.miss_drain(ctx)
+    qec.moe_destroy(ctx)
+    ms = float(np.median([a.elapsed_time(b) for a, b in evs[2:]]))
+    byts = k * 3 * wl.tensor_bytes(0)
+    gbs = byts / (ms * 1e-3) / 1e9
+    log(f"all-cold layer: {ms * 1e3:.1f} us per forward, {gbs:.1f} GB/s over the host link")
+    return {"workload": f"one layer, hidden {H}, {E} experts, top-{k}, FFN {F}, every expert in pinned host memory, "
+                        f"batch-1 routed forwards",
+            "us_per_forward": round(ms * 1e3, 2),
+            "roofline_link": {"bound": "host link", "achieved": round(gbs, 1), "peak": round(link_peak, 1),
+                              "unit": "GB/s", "frac": round(gbs / link_peak, 4), "bytes_per_forward": byts,
+                              "what": "weights of the 8 experts each forward reads zero-copy, over the median "
+                                      "event time of one forward"}}
+
+
+def run_pool_leg(args, qec, synth, torch, log, link_peak):
     """Shared expert pool and prefill preheat against per-tensor pools, on
     the 25%-pool model (one registration; moe_cache_reset puts the seeded
     state back before every run).  (1) decode_b1_pool25: args.pool_steps
@@ -550,9 +603,20 @@ def run_pool_leg(args, qec, synth, torch, log):
         stream.synchronize()
         ms = e0.elapsed_time(e1)
         s1 = qec.moe_stats(ctx)
-        d = {key: s1[key] - s0[key] for key in ("hits", "misses", "admissions", "evictions", "cold_bytes")}
+        d = {key: s1[key] - s0[key] for key in ("hits", "misses", "admissions", "evictions", "cold_bytes",
+                                                 "upload_bytes")}
+        # host-link roofline of the run: every byte that crossed the link
+        # (zero-copy weight reads by the kernels + promotion-pass uploads)
+        # over the run's time, against the link probe of this run
+        link_bytes = d["cold_bytes"] + d["upload_bytes"]
+        gbs = link_bytes / (ms * 1e-3) / 1e9
         return {"tokens_per_s": round(n / (ms * 1e-3), 1), "ms_per_token": round(ms / n, 4),
-                "hit_rate": round(d["hits"] / max(1, d["hits"] + d["misses"]), 4), **d}
+                "hit_rate": round(d["hits"] / max(1, d["hits"] + d["misses"]), 4), **d,
+                "roofline_link": {"bound": "host link", "achieved": round(gbs, 1), "peak": round(link_peak, 1),
+                                  "unit": "GB/s", "frac": round(gbs / link_peak, 4),
+                                  "bytes_per_token": round(link_bytes / n),
+                                  "what": "zero-copy cold weight bytes + promotion-pass upload bytes, over the "
+                                          "decode loop's event time (forwards and promotion passes)"}}
 
     out = {"workload": (f"{wl.name}: {L} layers, hidden {H}, {E} experts, top-{k}, FFN {F}, Zipf({wl.zipf_s}) "
                         f"routing, 128/512 experts per tensor seeded, {args.pool_steps} batch-1 decode tokens "
@@ -793,14 +857,16 @@ def run_prefill_leg(args, qec, synth, torch, log):
             qec.route_topk(ctx, lg[l], T, E, k, idx, w, sp)
             qec.moe_ffn_forward(ctx, l, x[l], T, idx, w, y, sp)
 
-    def timed():
+    def timed(gemm_events=False):
         pass_()
         stream.synchronize()
         qec.miss_drain(ctx)
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(L)]
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         per_layer = np.zeros(L)
+        gemm_ms = np.zeros((L, 2))
         total = 0.0
+        qec.moe_debug_timing(ctx, gemm_events)
         for s in range(args.prefill_steps):
             with torch.cuda.stream(stream):
                 e0.record()
@@ -814,18 +880,33 @@ def run_prefill_leg(args, qec, synth, torch, log):
             qec.miss_drain(ctx)
             total += e0.elapsed_time(e1)
             per_layer += np.array([a.elapsed_time(b) for a, b in ev])
-        return total / args.prefill_steps, per_layer / args.prefill_steps
+            if gemm_events:
+                gu, dn = qec.moe_debug_timing_read(ctx, L)
+                gemm_ms += np.stack([gu, dn], axis=1)
+        qec.moe_debug_timing(ctx, False)
+        n = args.prefill_steps
+        return total / n, per_layer / n, gemm_ms / n
 
     # cold experts read zero-copy by the GEMM's converters, then with the
     # lookahead prefetch (layer l + 1's cold experts uploaded by the copy
     # engine while layer l computes)
-    ms_zc, per_layer_zc = timed()
+    ms_zc, per_layer_zc, _ = timed()
     qec.moe_set_lookahead(ctx, True)
-    ms, per_layer = timed()
+    # the lookahead pass, with events around each layer's two GEMM kernels
+    # (the per-layer times then include the event records: a few us)
+    ms, per_layer, gemm_ms = timed(gemm_events=True)
     flop = 2.0 * T * k * 3 * H * F
     peaks, src = load_peaks()
     best = float(per_layer.min())
     tfl = flop / (best * 1e-3) / 1e12
+    # tensor roofline of the grouped GEMM kernels alone: 2 A (2 H F) flops of
+    # gate/up and 2 A F H of down per layer (A = T k assignments), over their
+    # own event time, summed over the pass's layers
+    gk_ms = float(gemm_ms.sum())
+    gk_tfl = L * flop / (gk_ms * 1e-3) / 1e12
+    peak_t = peaks.get("bf16_tflops_sustained") or peaks.get("bf16_tflops", 1900.0)
+    gu_tfl = L * 2.0 * T * k * 2 * H * F / (float(gemm_ms[:, 0].sum()) * 1e-3) / 1e12
+    dn_tfl = L * 2.0 * T * k * H * F / (float(gemm_ms[:, 1].sum()) * 1e-3) / 1e12
     qec.moe_destroy(ctx)
     log(f"prefill: {T / (ms * 1e-3):.0f} tokens/s through {L} layers with lookahead prefetch "
         f"({T / (ms_zc * 1e-3):.0f} with zero-copy cold reads), best layer {best:.3f} ms = {tfl:.1f} TFLOP/s")
@@ -840,7 +921,18 @@ def run_prefill_leg(args, qec, synth, torch, log):
                      "peak_tflops": peaks.get("bf16_tflops"), "unit": "TFLOP/s",
                      "frac": round(tfl / peaks.get("bf16_tflops", 1900.0), 4),
                      "note": "kind::f16 MMA on integer-valued fp16 operands (sm_103a has no tcgen05 kind::i8); "
-                             "per-layer time includes quantize, sort, gather, both GEMMs and the combine"}}
+                             "per-layer time includes quantize, sort, gather, both GEMMs and the combine"},
+            "roofline_tensor": {"bound": "tensor", "kernel": "grouped GEMM kernels (gate/up + SwiGLU + h "
+                                                             "quantization, down)",
+                                "achieved": round(gk_tfl, 1), "peak": peak_t, "unit": "TFLOP/s",
+                                "frac": round(gk_tfl / peak_t, 4),
+                                "peak_source": f"{src} bf16_tflops_sustained (the GEMMs run inside a "
+                                               f"{ms:.0f} ms pass; kind::f16 runs at the bf16 rate)",
+                                "gate_up_tflops": round(gu_tfl, 1), "down_tflops": round(dn_tfl, 1),
+                                "gemm_ms_per_layer": round(gk_ms / L, 4),
+                                "flops_per_layer": flop,
+                                "timing": "CUDA events around each GEMM launch on the context stream, all "
+                                          f"{L} layers of the lookahead pass"}}
 
 
 # ----------------------------------------------------------------------------
@@ -901,14 +993,19 @@ def run_reference(args):
             oracle.layer(x, idx, w, g, u, d, wl.hidden, wl.ffn)
         dt = time.perf_counter() - t0
         if s >= args.warmup:
-            per_step.append(dt * L / len(layers))
+            per_step.append(dt)
         if len(cache) > 3 * 8 * 64:
             cache.clear()
-    step_s = float(np.mean(per_step))
+    sample_s = float(np.mean(per_step))     # measured: the sampled layers of one step
+    step_s = sample_s * L / len(layers)     # extrapolated to all layers of the step
     value = T / step_s
     out = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 2),
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sample_s * 1e3, 2),
+        "ms_per_step_what": f"measured time of one step's sampled work ({len(layers)} of {L} layers, one token)",
+        "ms_per_step_extrapolated": round(step_s * 1e3, 2),
+        "extrapolation": f"value = tokens / (measured sample time x {L}/{len(layers)}): the oracle's layers all cost "
+                         f"the same (same shapes, 8 experts each)",
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
         "config": {"workload": decode_workload_desc(wl), "parallelism": "single host core (the CPU oracle)"},
         "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": 1, "host_cores": os.cpu_count(),

@@ -428,8 +428,10 @@ int moe_debug_busy(moe_ctx *ctx, int microseconds);
 
 /*
  * Kernel timing (benchmark hook): when enabled, every forward records CUDA
- * events on the context stream around its gate/up mat-vec and its down
- * mat-vec launches (also inside a captured graph).  moe_debug_timing_read
+ * events on the context stream around its gate/up and its down launches:
+ * the mat-vec kernels (or the single-launch layer kernel, whose time is then
+ * the gate/up figure) for small batches, the two grouped GEMM kernels for
+ * prompt batches (also inside a captured graph).  moe_debug_timing_read
  * synchronizes and writes, per layer, the device time in ms of the most
  * recent gate/up and down launch of that layer since the last read (0 when
  * the layer ran no forward); both arrays hold n_layers doubles.
@@ -458,14 +460,33 @@ int moe_debug_timing_read(moe_ctx *ctx, double *gate_up_ms, double *down_ms);
  * multiple of the down row block (64 for ffn/32 <= 40, else 32).  The first
  * call on a device looks up the array's device address and configures the
  * kernel (make it before any stream capture); later calls on that device
- * only clear the parts of the array that must start at zero and launch one
- * kernel.  All calls share the array and each leaves its contents behind, so
- * calls that overlap on the GPU (other streams, other host threads) race.
- * Errors: MOE_ERR_ARG, MOE_ERR_CAPACITY, MOE_ERR_CUDA.
+ * (and shape) only clear the parts of the array that must start at zero and
+ * launch one kernel.  All calls share the array and each leaves its contents
+ * behind, so calls that overlap on the GPU (other streams, other host
+ * threads) race.  The call returns before the kernel has run, so faults the
+ * kernel detects (an expert id outside [0, n_experts), which it reads as
+ * expert 0; a bounded wait that expired) are not in its return value: they
+ * are left in the array's error word, which moe_expert_ffn_noalloc_status
+ * reads.  Errors: MOE_ERR_ARG, MOE_ERR_CAPACITY, MOE_ERR_CUDA.
  */
 int moe_expert_ffn_noalloc(const float *d_x, int n_tokens, const int32_t *d_idx, const float *d_w,
                            const uint64_t *d_tbl, int hidden, int ffn, int n_experts, int top_k, float *d_y,
                            void *stream);
+
+/*
+ * Device-side status of the most recent moe_expert_ffn_noalloc call on the
+ * current device (no counterpart on the source pages; the companion of the
+ * allocation-free entry point).  Waits for `stream` (the stream that call
+ * used, NULL = legacy default stream), reads the kernel's error word from the
+ * first bytes of the entry point's device array and returns MOE_OK when it is
+ * zero, else MOE_ERR_FAULT with moe_last_error(NULL) naming the bits (1: an
+ * expert id outside [0, n_experts) was read as expert 0; 2, 4: a bounded wait
+ * expired and its work item was skipped; that call's output is then not
+ * valid).  The word stays until the next call on the device clears it.
+ * Allocates nothing.  MOE_OK when no call has run on the device yet.
+ * Errors: MOE_ERR_FAULT, MOE_ERR_CUDA.
+ */
+int moe_expert_ffn_noalloc_status(void *stream);
 
 #ifdef __cplusplus
 }

@@ -76,6 +76,7 @@ SIGNATURES = {
     "moe_debug_timing": (_i32, [_vp, _i32]),
     "moe_debug_timing_read": (_i32, [_vp, _vp, _vp]),
     "moe_expert_ffn_noalloc": (_i32, [_vp, _i32, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp]),
+    "moe_expert_ffn_noalloc_status": (_i32, [_vp]),
 }
 
 
@@ -303,3 +304,9 @@ def moe_expert_ffn_noalloc(x, n_tokens, idx, w, tbl, hidden, ffn, n_experts, top
     """One layer without any device allocation (scratch in a fixed device array)."""
     return _check(None, load().moe_expert_ffn_noalloc(_dev(x), n_tokens, _dev(idx), _dev(w), _dev(tbl), hidden, ffn,
                                                       n_experts, top_k, _dev(y), _stream(stream)))
+
+
+def moe_expert_ffn_noalloc_status(stream=None):
+    """Device-side status of the last allocation-free call on this device
+    (raises MoeError(MOE_ERR_FAULT) when its kernel reported an error)."""
+    return _check(None, load().moe_expert_ffn_noalloc_status(_stream(stream)))

@@ -1243,7 +1243,6 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
     const int H = g.H, F = g.F, k = g.k;
     const int nbx = H / kBlock, nbf = F / kBlock, rgs = F / kBlock;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const uint32_t step_clock = *g.cv.clock + (uint32_t)g.n_tokens;
 
     if (p.pdl) {
         // programmatic dependent launch: the previous kernel's writes are
@@ -1251,6 +1250,9 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
         asm volatile("griddepcontrol.wait;" ::: "memory");
         asm volatile("griddepcontrol.launch_dependents;");
     }
+    // the clock is read after the dependency wait: every input of this
+    // launch, the promotion pass's clock included, comes from before it
+    const uint32_t step_clock = *g.cv.clock + (uint32_t)g.n_tokens;
     constexpr int DG = 32 / LD, DROWS = kWarps * DG;
     const int n_rb_all = H / DROWS;
     const int R = p.rb_rows;
@@ -1583,13 +1585,16 @@ static const void *fused_fn(int F, int T, bool rb) { return rb ? fused_fn_t<true
 // raised, so contexts of different shapes coexist); *blocks_per_sm gets the
 // smallest resident-CTA count over the variants (a safe cooperative grid).
 static int configure_mode(int F, size_t smem, bool rb, int *blocks_per_sm) {
+    // the shared-memory opt-in is a per-device function attribute
     static std::mutex mu;
-    static std::map<const void *, size_t> opted;
+    static std::map<std::pair<int, const void *>, size_t> opted;
     std::lock_guard<std::mutex> lk(mu);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return (int)cudaErrorInvalidDevice;
     int best = 1 << 30;
     for (int T : {1, 2, 4, 8}) {
         const void *fn = fused_fn(F, T, rb);
-        size_t &cur = opted[fn];
+        size_t &cur = opted[{dev, fn}];
         if (smem > cur) {
             cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             if (e != cudaSuccess) return (int)e;

@@ -837,13 +837,29 @@ int gemm_configure() {
     return (int)(e1 != cudaSuccess ? e1 : e2);
 }
 
-int launch_prefill(const PrefillLaunch &L, cudaStream_t st) {
+// An event record that also works inside a stream capture (an external
+// event node there).
+static void record_event(cudaEvent_t e, cudaStream_t st) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaStreamIsCapturing(st, &cs);
+    if (cs == cudaStreamCaptureStatusActive)
+        cudaEventRecordWithFlags(e, st, cudaEventRecordExternal);
+    else
+        cudaEventRecord(e, st);
+}
+
+int launch_prefill(const PrefillLaunch &L, cudaStream_t st, cudaEvent_t const *ev) {
     tiling_kernel<<<1, 1024, 0, st>>>(L.tiling);
     const int A = L.gu.A;
     int g = (int)std::min<size_t>(((size_t)A * (L.H / 8) + 255) / 256, (size_t)L.n_sm * 16);
     if (g > 0) gather_kernel<<<g, 256, 0, st>>>(L.gu.assign, A, L.k, L.H, L.xq, L.xds, L.xs16, L.xdT, L.gu.A_pad);
+    // timing hook: events around each GEMM launch
+    if (ev) record_event(ev[0], st);
     gemm::grouped_gemm_kernel<true><<<L.n_sm, gemm::Cfg<true>::NTHREADS, gemm::Cfg<true>::SMEM, st>>>(L.tm_x, L.gu);
+    if (ev) record_event(ev[1], st);
+    if (ev) record_event(ev[2], st);
     gemm::grouped_gemm_kernel<false><<<L.n_sm, gemm::Cfg<false>::NTHREADS, gemm::Cfg<false>::SMEM, st>>>(L.tm_h, L.dn);
+    if (ev) record_event(ev[3], st);
     const size_t n = (size_t)L.T * L.H;
     int gc = (int)std::min<size_t>((n + 255) / 256, (size_t)L.n_sm * 16);
     combine_kernel<<<gc, 256, 0, st>>>(L.dn.o, L.w, L.y, L.T, L.k, L.H);

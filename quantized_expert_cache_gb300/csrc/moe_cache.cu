@@ -1056,7 +1056,12 @@ static int ffn_forward_body(moe_ctx *ctx, int layer, const float *d_x, int n_tok
         L.k = ctx->ka;
         L.H = H;
         L.n_sm = ctx->n_sm;
-        rc = moe::launch_prefill(L, st);
+        const cudaEvent_t *pev = nullptr;
+        if (ctx->timing) {
+            pev = ctx->tev.data() + 4 * (size_t)layer;
+            ctx->tev_used[layer] = 1;
+        }
+        rc = moe::launch_prefill(L, st, pev);
         if (rc) return fail(ctx, MOE_ERR_CUDA, std::string("prefill launch: ") + cudaGetErrorString((cudaError_t)rc));
         ctx->last_T = T;
         if (prefetched) {

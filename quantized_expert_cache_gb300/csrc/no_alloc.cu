@@ -15,6 +15,10 @@
 // cudaGetSymbolAddress (with that device current) and every later call on that
 // device reuses it.  All calls share the array, so calls that overlap on the
 // GPU (different streams, or different host threads) race on it.
+//
+// The kernel's error word sits at a fixed place, the first bytes of the
+// array, so that moe_expert_ffn_noalloc_status can read what the most recent
+// call left there without knowing that call's sizes.
 #include "../../include/moe_cache.h"
 #include "kernels.h"
 
@@ -37,10 +41,14 @@ void set_context_free_error(const std::string &msg);  // shared with moe_last_er
 
 namespace {
 
+constexpr size_t kErrWordBytes = 256;  // [0, 256): the error word of the most recent call
+
 struct DevSetup {
     bool done = false;
     unsigned char *scratch = nullptr;  // device address of g_noalloc_scratch
     int n_sm = 0;
+    // kernel configuration of the last (hidden, ffn) seen on this device
+    int cfg_h = 0, cfg_f = 0, bps = 0;
 };
 DevSetup g_dev[kMaxDevices];
 std::mutex g_mu;
@@ -82,8 +90,9 @@ int moe_expert_ffn_noalloc(const float *d_x, int n_tokens, const int32_t *d_idx,
         return fail(MOE_ERR_ARG, "noalloc: needs n_tokens <= 32, n_tokens*top_k <= 256 and hidden a multiple of " +
                                      std::to_string(down_rows));
     const int E = n_experts, H = hidden, F = ffn, n_rb = H / down_rows;
-    // scratch layout (sizes only first)
+    // scratch layout (sizes only first); the error word comes first
     Carve c;
+    c.off = kErrWordBytes;
     auto layout = [&](Carve &cv, moe::FusedParams *fp) {
         uint32_t *bitmap = cv.take<uint32_t>((size_t)3 * ((E + 31) / 32));
         uint32_t *misslog = cv.take<uint32_t>(1 + (size_t)3 * E);
@@ -92,7 +101,6 @@ int moe_expert_ffn_noalloc(const float *d_x, int n_tokens, const int32_t *d_idx,
         uint32_t *stamps = cv.take<uint32_t>(1);
         unsigned *done = cv.take<unsigned>((size_t)E + 1);
         unsigned *counters = cv.take<unsigned>((size_t)n_rb);
-        int *err = cv.take<int>(1);
         int8_t *xq = cv.take<int8_t>((size_t)n_tokens * H);
         moe::BlockScale *xds = cv.take<moe::BlockScale>((size_t)n_tokens * (H / 32));
         int8_t *hq = cv.take<int8_t>((size_t)A * F);
@@ -131,13 +139,14 @@ int moe_expert_ffn_noalloc(const float *d_x, int n_tokens, const int32_t *d_idx,
             fp->idx = d_idx;
             fp->done_gu = done;
             fp->exit_count = done + E;
-            fp->error = err;
+            fp->error = reinterpret_cast<int *>(cv.base);
         }
-        // [base, xq) holds the small tables (zeroed per call); slot is set to -1
-        return std::make_pair((size_t)((unsigned char *)slot - (unsigned char *)bitmap),
-                              (size_t)((unsigned char *)xq - (unsigned char *)bitmap));
+        // [array start, xq) holds the error word and the small tables (zeroed
+        // per call); slot is set to -1
+        return std::make_pair(cv.base ? (size_t)((unsigned char *)slot - cv.base) : (size_t)0,
+                              cv.base ? (size_t)((unsigned char *)xq - cv.base) : (size_t)0);
     };
-    const auto offs = layout(c, nullptr);
+    layout(c, nullptr);
     const size_t need = c.off;
     if (need > kNoAllocScratchBytes)
         return fail(MOE_ERR_CAPACITY, "noalloc: this call needs " + std::to_string(need) + " scratch bytes, above the " +
@@ -163,16 +172,28 @@ int moe_expert_ffn_noalloc(const float *d_x, int n_tokens, const int32_t *d_idx,
     }
     DevSetup &d = g_dev[dev];
     int bps = 0;
-    e = (cudaError_t)moe::fused_configure(F, smem, &bps);
-    if (e != cudaSuccess || bps < 1) return fail(MOE_ERR_CUDA, "noalloc: kernel configuration failed");
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (d.cfg_h != H || d.cfg_f != F) {
+            e = (cudaError_t)moe::fused_configure(F, smem, &d.bps);
+            if (e != cudaSuccess || d.bps < 1) {
+                d.cfg_h = d.cfg_f = 0;
+                return fail(MOE_ERR_CUDA, "noalloc: kernel configuration failed");
+            }
+            d.cfg_h = H;
+            d.cfg_f = F;
+        }
+        bps = d.bps;
+    }
     moe::FusedParams fp{};
     Carve cv;
     cv.base = d.scratch;
-    layout(cv, &fp);
+    cv.off = kErrWordBytes;
+    const auto offs = layout(cv, &fp);
     cudaStream_t st = (cudaStream_t)stream;
-    // the counters, the miss log, the error word and the clock must start at
-    // zero, the slot table at -1 (so no stamp is written); the large buffers
-    // are written before they are read
+    // the error word, the counters, the miss log and the clock must start
+    // at zero, the slot table at -1 (so no stamp is written); the large
+    // buffers are written before they are read
     e = cudaMemsetAsync(d.scratch, 0, offs.second, st);
     if (e == cudaSuccess) e = cudaMemsetAsync(d.scratch + offs.first, 0xff, (size_t)3 * E * sizeof(int32_t), st);
     if (e != cudaSuccess) return fail(MOE_ERR_CUDA, std::string("noalloc: memset: ") + cudaGetErrorString(e));
@@ -182,6 +203,28 @@ int moe_expert_ffn_noalloc(const float *d_x, int n_tokens, const int32_t *d_idx,
     int rc = moe::launch_fused(fp, grid, smem, st, nullptr);
     if (rc) return fail(MOE_ERR_CUDA, std::string("noalloc: launch: ") + cudaGetErrorString((cudaError_t)rc));
     return MOE_OK;
+}
+
+int moe_expert_ffn_noalloc_status(void *stream) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) return fail(MOE_ERR_CUDA, "noalloc status: no current device");
+    unsigned char *scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (g_dev[dev].done) scratch = g_dev[dev].scratch;
+    }
+    if (!scratch) return MOE_OK;  // no call has run on this device
+    cudaStream_t st = (cudaStream_t)stream;
+    int word = 0;
+    e = cudaMemcpyAsync(&word, scratch, sizeof(int), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return fail(MOE_ERR_CUDA, std::string("noalloc status: ") + cudaGetErrorString(e));
+    if (word == 0) return MOE_OK;
+    std::string m = "noalloc: the kernel reported error bits " + std::to_string(word) + ":";
+    if (word & 1) m += " an expert id outside [0, n_experts) was read as expert 0;";
+    if (word & 6) m += " a bounded wait expired and its work item was skipped;";
+    return fail(MOE_ERR_FAULT, m + " the output of that call is not valid");
 }
 
 }  // extern "C"

@@ -15,6 +15,7 @@ registered with its pool seeding):
 import numpy as np
 import pytest
 
+import oracle
 import quantized_expert_cache_gb300 as qec
 import synth
 from gpu_helpers import FullModel, check_sampled_rows
@@ -65,6 +66,90 @@ def test_decode_b1_resident_full_size():
             o = m.policy.snapshot(tid)
             assert snap["slot_of"].tolist() == o["slot_of"]
             assert np.array_equal(snap["tbl"], m.expected_tbl(tid))
+    finally:
+        m.close()
+
+
+def test_decode_b1_resident_step_graph_replay():
+    """The configuration the benchmark times: the 48 routed layer launches
+    of a decode step captured in one CUDA graph on the context's stream
+    (consecutive layers chained by programmatic dependent launch), replayed
+    step after step with each step's inputs copied in before the replay and
+    the promotion pass after it.  Every layer's top-k indices and weights of
+    every replay against the oracle (bit-exact / 1e-5); sampled layers' y
+    bit-equal to an eager forward of the same inputs issued after the replay
+    (same step clock, so the cache records are unchanged), whose x codes, h
+    codes and y are checked against the oracle; the table, slot and stamp
+    state of every tensor after every promotion pass against the policy
+    oracle; hit and miss counts at the end."""
+    wl = synth.WORKLOADS["decode_b1_resident"]
+    T, steps = 1, 8
+    stream = torch.cuda.Stream()
+    sp = stream.cuda_stream
+    m = FullModel(wl, max_tokens=T, stream=sp)
+    try:
+        L, H, E, k = m.L, m.H, m.E, m.k
+        xin = torch.empty((L, T, H), device="cuda")
+        lin = torch.empty((L, T, E), device="cuda")
+        idx = torch.empty((L, T, k), dtype=torch.int32, device="cuda")
+        w = torch.empty((L, T, k), device="cuda")
+        y = torch.empty((L, T, H), device="cuda")
+
+        def load_step(s):
+            X = np.stack([wl.x(l, s, T) for l in range(L)])
+            LG = np.stack([wl.logits(l, s, T) for l in range(L)])
+            with torch.cuda.stream(stream):
+                xin.copy_(torch.from_numpy(X).pin_memory(), non_blocking=True)
+                lin.copy_(torch.from_numpy(LG).pin_memory(), non_blocking=True)
+            return X, LG
+
+        def layers():
+            for l in range(L):
+                qec.moe_ffn_forward_routed(m.ctx, l, xin[l], lin[l], T, idx[l], w[l], y[l], sp)
+
+        # warm-up on step 0's inputs (its records are those of step 0 itself),
+        # then the capture, as the benchmark does
+        load_step(0)
+        layers()
+        stream.synchronize()
+        qec.miss_drain(m.ctx)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            layers()
+        check = {(0, 0), (1, 7), (2, 3), (3, 47), (5, 12), (7, 5), (7, 40)}
+        y_e = torch.empty((T, H), device="cuda")
+        i_e = torch.empty((T, k), dtype=torch.int32, device="cuda")
+        w_e = torch.empty((T, k), device="cuda")
+        for s in range(steps):
+            X, LG = load_step(s)
+            with torch.cuda.stream(stream):
+                graph.replay()
+            stream.synchronize()
+            idx_np, w_np, y_np = idx.cpu().numpy(), w.cpu().numpy(), y.cpu().numpy()
+            used = {}
+            for l in range(L):
+                io, wo = oracle.topk(LG[l], k)
+                assert np.array_equal(idx_np[l], io), (s, l)
+                np.testing.assert_allclose(w_np[l], wo, rtol=1e-5, atol=1e-7)
+                for kind in range(3):
+                    used[3 * l + kind] = io.ravel().tolist()
+                if (s, l) in check:
+                    qec.moe_ffn_forward_routed(m.ctx, l, xin[l], lin[l], T, i_e, w_e, y_e, sp)
+                    stream.synchronize()
+                    assert np.array_equal(y_e.cpu().numpy(), y_np[l]), (s, l)
+                    check_sampled_rows(m, l, X[l], LG[l], y_np[l], idx_np[l], w_np[l], range(T))
+            qec.cache_step(m.ctx, T)
+            m.policy.step(T, used)
+            for tid in range(3 * L):
+                snap = qec.moe_cache_snapshot(m.ctx, tid, m.E, m.spt)
+                o = m.policy.snapshot(tid)
+                assert snap["slot_of"].tolist() == o["slot_of"], (s, tid)
+                assert snap["last_seen"].tolist() == o["last_seen"], (s, tid)
+                assert snap["stamps"].tolist() == o["stamp"], (s, tid)
+                assert np.array_equal(snap["tbl"], m.expected_tbl(tid)), (s, tid)
+        st = qec.moe_stats(m.ctx)
+        assert st["hits"] == m.policy.stats["hits"] and st["misses"] == m.policy.stats["misses"]
+        assert st["misses"] > 0
     finally:
         m.close()
 
