@@ -145,7 +145,9 @@ def test_decode_b1_resident_step_graph_replay():
                 o = m.policy.snapshot(tid)
                 assert snap["slot_of"].tolist() == o["slot_of"], (s, tid)
                 assert snap["last_seen"].tolist() == o["last_seen"], (s, tid)
-                assert snap["stamps"].tolist() == o["stamp"], (s, tid)
+                # the partial layers use the first 307 of the 512 slots per tensor
+                cap = len(o["stamp"])
+                assert snap["stamps"][:cap].tolist() == o["stamp"], (s, tid)
                 assert np.array_equal(snap["tbl"], m.expected_tbl(tid)), (s, tid)
         st = qec.moe_stats(m.ctx)
         assert st["hits"] == m.policy.stats["hits"] and st["misses"] == m.policy.stats["misses"]
