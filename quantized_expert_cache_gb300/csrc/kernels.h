@@ -144,6 +144,7 @@ int launch_prefetch_table(const uint64_t *tbl_rows, const int32_t *map, const vo
                           int E, uint64_t *etbl, cudaStream_t st);
 int gemm_configure();
 int gemm_bn(bool dual);
+int gemm_rows_per_tile(bool dual);
 int launch_step_finish(const Update *u, int n, uint64_t *tbl, int32_t *slot, uint32_t *stamps, uint32_t *clock,
                        uint32_t new_clock, uint32_t *clear_a, int n_a, uint32_t *clear_b, int n_b, cudaStream_t st);
 int launch_count_assign(const int32_t *idx, int n, int E, uint32_t *cnt, cudaStream_t st);

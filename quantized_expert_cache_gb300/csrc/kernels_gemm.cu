@@ -15,17 +15,22 @@
 // sum of the 32 products of one quantization block (|sum| <= 32512) is exact.
 // Each 32-wide K block is accumulated into its own TMEM buffer, so the MMA
 // produces exactly the int32 block dots of the mat-vec path; epilogue warps
-// then add d_w * d_a * sumi in fp32 (fma.rn.f32x2), as the mat-vec does.
+// then add sum * (d_w * d_a) in fp32 (packed fp32x2 multiplies and fused
+// multiply-adds), as the mat-vec does.
 //
-// Tile: M = 128 weight rows (TMEM lanes) x N tokens (TMEM columns), K staged
-// 64 at a time (two quantization blocks = one 128-B swizzle row of fp16).
-// Warp roles (10 warps): 0 TMA producer of the token tile; 1 TMEM owner and
-// MMA issuer; 2-5 weight converters (Q4 codes read through the expert table,
-// from the HBM pool or zero-copy from pinned host memory, turned into fp16
-// and stored in the 128-B swizzled K-major layout); 6-9 epilogue (TMEM lane
-// quarter = warp % 4).  Gate/up tiles hold two A operands (gate rows and up
-// rows) so SwiGLU and the quantization of h happen in the epilogue; the 32
-// rows of one h block are the 32 lanes of one epilogue warp.
+// Tile: M = 128 weight rows (TMEM lanes) x N = 128 sorted tokens (TMEM
+// columns), K staged 64 at a time (two quantization blocks = one 128-B
+// swizzle row of fp16), four 128-column K-block buffers in TMEM (all 512
+// columns).  Gate/up tiles stack 64 gate rows over the same 64 up rows, so
+// one MMA per K step serves both tensors and the tile's SwiGLU pairs lane l of
+// TMEM quarter q with lane l of quarter q + 2.  Warp roles (24 warps): 0-3
+// weight converters (Q4 codes and scales fetched with cp.async through the
+// expert table -- HBM pool, staged slot or zero-copy host memory -- several
+// stages ahead, expanded to fp16 in the 128-B swizzled K-major layout); 4 TMA
+// producer of the token tile; 5 TMEM owner and MMA issuer; 8-23 epilogue:
+// TMEM lane quarter = warp % 4, 32 token columns per warp.  Per K
+// block an epilogue thread reads its row's 32 block sums with one TMEM load;
+// the columns' activation scales are broadcast shared-memory reads.
 //
 // Every mbarrier wait is bounded (about 2 s of SM clock): on expiry the CTA
 // sets an error bit, all roles leave their loops, in-flight copies and MMAs
@@ -40,42 +45,44 @@
 namespace moe {
 namespace gemm {
 
-constexpr int BM = 128;
-constexpr int BK = 64;
-constexpr int W_TMA = 0, W_MMA = 1, W_CONV = 2, W_EPI = 6;
+constexpr int BM = 128;   // weight rows per tile (TMEM lanes)
+constexpr int BN = 128;   // token columns per tile
+constexpr int BK = 64;    // K per pipeline stage (two quantization blocks)
+// Warp roles by warpgroup (setmaxnreg moves registers between warpgroups):
+// warpgroup 0 = the 4 converter warps, warpgroup 1 = TMA producer, MMA issuer
+// and two warps that only join the final barrier, warpgroups 2-5 = the 16
+// epilogue warps (4 lane quarters x 4 column groups).
+constexpr int W_CONV = 0, W_TMA = 4, W_MMA = 5, W_EPI = 8;
+constexpr int N_EPI = 16;
+constexpr int NTHREADS = (W_EPI + N_EPI) * 32;  // 768
+// Register split: launched with kLaunchRegs per thread (ptxas' allocation for
+// 768 threads, checked on the host before the first launch), warpgroups 0-1
+// drop to kProdRegs and warpgroups 2-5 rise to kEpiRegs; the two splits
+// move the same number of registers.
+constexpr int kLaunchRegs = 80, kProdRegs = 56, kEpiRegs = 88;
+static_assert(2 * 128 * kProdRegs + 4 * 128 * kEpiRegs <= NTHREADS * kLaunchRegs, "register split");
 constexpr long long kTimeoutCycles = 4000000000ll;
 
-template <bool DUAL>
-struct Cfg {
-    static constexpr int BN = DUAL ? 64 : 128;
-    static constexpr int NA = DUAL ? 2 : 1;
-    static constexpr int STAGES = DUAL ? 3 : 4;   // A/B pipeline slots
-    static constexpr int RR = 8;                  // raw prefetch ring (converter cp.async)
-    static constexpr int PD = RR - 1;             // prefetch distance in stages
-    static constexpr int A_BYTES = BM * BK * 2;
-    static constexpr int B_BYTES = BN * BK * 2;
-    // per-slot scales for the epilogue: weight scales [NA][BM][2] fp16 and
-    // activation scales [2][BN] fp32 of the slot's two K blocks
-    static constexpr int WS_BYTES = NA * BM * 2 * 2;
-    static constexpr int AS_BYTES = 2 * BN * 4;
-    static constexpr int SLOT_BYTES = NA * A_BYTES + B_BYTES + WS_BYTES + AS_BYTES;
-    static constexpr int SLOT_STRIDE = (SLOT_BYTES + 1023) / 1024 * 1024;
-    // raw ring entry: codes [NA][BM][32 B], weight scales, activation scales
-    static constexpr int RAW_CODES = NA * BM * 32;
-    static constexpr int RAW_BYTES = RAW_CODES + WS_BYTES + AS_BYTES;
-    static constexpr int RAW_OFF = STAGES * SLOT_STRIDE;
-    static constexpr int TBUF = NA * BN;          // TMEM columns per K-block buffer
-    static constexpr int NTBUF = 512 / TBUF;      // K-block buffers in TMEM
-    static constexpr int BAR_OFF = RAW_OFF + RR * RAW_BYTES;
-    static constexpr int NBARS = 2 * STAGES + 2 * NTBUF;
-    static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
-    static constexpr int SMEM = MISC_OFF + 16 + 1024;  // + alignment slack
-    // epilogue warps: EPI_SPLIT per TMEM lane quarter, each owning BN / EPI_SPLIT
-    // token columns (32 for gate/up with its two tensors, 64 for down)
-    static constexpr int N_EPI = 8;
-    static constexpr int EPI_SPLIT = N_EPI / 4;
-    static constexpr int NTHREADS = (W_EPI + N_EPI) * 32;
-};
+constexpr int STAGES = 4;                        // A/B pipeline slots
+constexpr int RR = 6;                            // raw prefetch ring of the converters (cp.async)
+constexpr int PD = RR - 1;                       // prefetch distance in stages
+constexpr int A_BYTES = BM * BK * 2;             // fp16 weight tile, 128-B swizzle
+constexpr int B_BYTES = BN * BK * 2;             // fp16 token tile (TMA), 128-B swizzle
+constexpr int WS_BYTES = BM * 2 * 2;             // weight scales [row][2 blocks] binary16
+constexpr int CS_BYTES = 2 * BN * 4;             // activation scales [2 blocks][column] fp32
+constexpr int SLOT_BYTES = A_BYTES + B_BYTES + WS_BYTES + CS_BYTES;
+constexpr int SLOT_STRIDE = (SLOT_BYTES + 1023) / 1024 * 1024;
+constexpr int RAW_CODES = BM * 32;               // raw ring entry: Q4 codes [row][32 B], then scales
+constexpr int RAW_BYTES = RAW_CODES + WS_BYTES + CS_BYTES;
+constexpr int RAW_OFF = STAGES * SLOT_STRIDE;
+constexpr int XCH_OFF = RAW_OFF + RR * RAW_BYTES;  // SwiGLU exchange: [8 pairs][2][16 cols][32 lanes] fp32
+constexpr int XCH_BYTES = 8 * 2 * 16 * 32 * 4;
+constexpr int NTBUF = 4;                         // K-block accumulators in TMEM (BN columns each)
+constexpr int BAR_OFF = XCH_OFF + XCH_BYTES;
+constexpr int NBARS = 2 * STAGES + 2 * NTBUF;
+constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
+constexpr int SMEM = MISC_OFF + 16 + 1024;       // + alignment slack
+static_assert(SMEM <= 227 * 1024, "shared memory of the GEMM CTA");
 
 // ---- PTX wrappers -----------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -167,26 +174,7 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                  : "memory");
 }
 
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
-    uint32_t r[16];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
-// 16 consecutive TMEM columns of this warp's 32 lanes (raw fp32 bits)
-__device__ __forceinline__ void tmem_ld16u(uint32_t taddr, uint32_t *r) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-}
 
 // 32 consecutive TMEM columns of this warp's 32 lanes (one fp32 per column)
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t *r) {
@@ -200,48 +188,9 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t *r) {
         : "r"(taddr));
 }
 
-// Packed fp32 pairs (two IEEE round-to-nearest operations per instruction).
-__device__ __forceinline__ unsigned long long pk2(uint32_t lo, uint32_t hi) {
-    unsigned long long r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
-    return r;
-}
-// acc{0,1} += sum{0,1} * (dw * da{0,1}): the scale products and the
-// accumulation as packed fp32 pairs (mul.rn.f32x2, fma.rn.f32x2).
-__device__ __forceinline__ void fma_scaled2(float &acc0, float &acc1, uint32_t sum0, uint32_t sum1, float da0, float da1,
-                                            float dw) {
-    asm("{\n.reg .b64 a, p, d, w, s;\n"
-        "mov.b64 a, {%0, %1};\nmov.b64 p, {%2, %3};\nmov.b64 d, {%4, %5};\nmov.b64 w, {%6, %6};\n"
-        "mul.rn.f32x2 s, w, d;\nfma.rn.f32x2 a, p, s, a;\nmov.b64 {%0, %1}, a;\n}"
-        : "+f"(acc0), "+f"(acc1)
-        : "r"(sum0), "r"(sum1), "f"(da0), "f"(da1), "f"(dw));
-}
-
-
-// acc{0,1} += p{0,1} * s{0,1}, two IEEE fp32 fused multiply-adds.
-__device__ __forceinline__ void fma2(float &a0, float &a1, float p0, float p1, float s0, float s1) {
-    unsigned long long acc, pp, ss;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(acc) : "f"(a0), "f"(a1));
-    asm("mov.b64 %0, {%1, %2};" : "=l"(pp) : "f"(p0), "f"(p1));
-    asm("mov.b64 %0, {%1, %2};" : "=l"(ss) : "f"(s0), "f"(s1));
-    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(pp), "l"(ss));
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(acc));
-}
-
 // Q4 codes of one row and two quantization blocks (32 B) -> 64 fp16 values
 // (q - 8) in K order, stored as 8 16-byte chunks of the row in the 128-B
 // swizzled layout (chunk c of row r of an 8-row group sits at chunk c ^ r).
-__device__ __forceinline__ uint32_t nib_pair(uint32_t w, int sel, int hi) {
-    // two bytes of w (selected) -> their low (hi=0) or high (hi=1) nibbles as
-    // the fp16 pair (1024 + n0, 1024 + n1), then minus (1032, 1032)
-    uint32_t t = __byte_perm(w, 0, sel);
-    if (hi) t >>= 4;
-    t = (t & 0x000F000Fu) | 0x64006400u;
-    __half2 h = *reinterpret_cast<__half2 *>(&t);
-    h = __hsub2(h, __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408)));
-    return *reinterpret_cast<uint32_t *>(&h);
-}
-
 // Four codes (one nibble per byte of n, values 0..15) -> two fp16 pairs
 // (q0 - 8, q1 - 8), (q2 - 8, q3 - 8): the bytes are placed under the fp16
 // exponent byte 0x64 (1024 + q, exact) and 1032 is subtracted (exact).
@@ -288,56 +237,66 @@ __device__ __forceinline__ void decode_tile(const uint2 *rec, int t, int &u, int
     ncols = (int)(r.y >> 16);
 }
 
-// Stage cursor over the flattened (tile, K stage) sequence of one CTA.
-// The tile's expert-table entries (weight blobs) and first token position
-// are looked up once per tile, not per stage.
+// A-tile row r of row tile rt: gate/up tiles hold gate rows 64 rt .. 64 rt + 63
+// in tile rows 0..63 and the same up rows in tile rows 64..127; down tiles
+// hold rows 128 rt .. 128 rt + 127.
+template <bool DUAL>
+__device__ __forceinline__ int tile_row(int rt, int r) {
+    return DUAL ? rt * 64 + (r & 63) : rt * BM + r;
+}
+
+// Stage cursor of one converter thread over the flattened (tile, K stage)
+// sequence of its CTA.  The expert-table entry of the thread's tensor and the
+// tile's first sorted position are looked up once per tile.
 struct StageCur {
-    int t, kt, u, rt, tt, nc, pos0;
-    const uint8_t *blob[2];
+    int t, kt, rt, pos0;
+    const uint8_t *blob;
     bool valid;
 };
 
-template <int BN>
-__device__ __forceinline__ void cur_tile(StageCur &c, const GemmParams &p, int n_uniq) {
-    decode_tile(p.tile_rec, c.t, c.u, c.rt, c.tt, c.nc);
-    const int e = p.uniq_e[c.u];
-    c.blob[0] = (const uint8_t *)(uintptr_t)(p.tbl[0][e] & ~1ull);
-    c.blob[1] = p.tbl[1] ? (const uint8_t *)(uintptr_t)(p.tbl[1][e] & ~1ull) : c.blob[0];
-    c.pos0 = p.uniq_off[c.u] + c.tt * BN;
+template <bool DUAL>
+__device__ __forceinline__ void cur_tile(StageCur &c, const GemmParams &p, int r) {
+    int u, tt, nc;
+    decode_tile(p.tile_rec, c.t, u, c.rt, tt, nc);
+    const int e = p.uniq_e[u];
+    const uint64_t *tb = (DUAL && r >= 64) ? p.tbl[1] : p.tbl[0];
+    c.blob = (const uint8_t *)(uintptr_t)(tb[e] & ~1ull);
+    c.pos0 = p.uniq_off[u] + tt * BN;
 }
 
-template <int BN>
-__device__ __forceinline__ void cur_init(StageCur &c, const GemmParams &p, int n_uniq, int total) {
+template <bool DUAL>
+__device__ __forceinline__ void cur_init(StageCur &c, const GemmParams &p, int total, int r) {
     c.t = blockIdx.x;
     c.kt = 0;
     c.valid = c.t < total;
-    if (c.valid) cur_tile<BN>(c, p, n_uniq);
+    if (c.valid) cur_tile<DUAL>(c, p, r);
 }
 
-template <int BN>
-__device__ __forceinline__ void cur_next(StageCur &c, const GemmParams &p, int n_uniq, int total, int nkt) {
+template <bool DUAL>
+__device__ __forceinline__ void cur_next(StageCur &c, const GemmParams &p, int total, int nkt, int r) {
     if (!c.valid) return;
     if (++c.kt == nkt) {
         c.kt = 0;
         c.t += gridDim.x;
         c.valid = c.t < total;
-        if (c.valid) cur_tile<BN>(c, p, n_uniq);
+        if (c.valid) cur_tile<DUAL>(c, p, r);
     }
 }
 
+__device__ __forceinline__ void bar_sync_named(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
 template <bool DUAL>
-__global__ void __launch_bounds__(Cfg<DUAL>::NTHREADS, 1)
+__global__ void __launch_bounds__(NTHREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmB, GemmParams p) {
-    using C = Cfg<DUAL>;
-    constexpr int BN = C::BN, NA = C::NA, NTBUF = C::NTBUF, STAGES = C::STAGES;
-    constexpr int N_EPI = C::N_EPI, EPI_SPLIT = C::EPI_SPLIT;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    uint64_t *bars = (uint64_t *)(smem + C::BAR_OFF);
+    uint64_t *bars = (uint64_t *)(smem + BAR_OFF);
     const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * STAGES, tfull0 = empty0 + 8 * STAGES,
                    tempty0 = tfull0 + 8 * NTBUF;
-    volatile uint32_t *tmem_slot = (volatile uint32_t *)(smem + C::MISC_OFF);
-    volatile int *abort_flag = (volatile int *)(smem + C::MISC_OFF + 4);
+    volatile uint32_t *tmem_slot = (volatile uint32_t *)(smem + MISC_OFF);
+    volatile int *abort_flag = (volatile int *)(smem + MISC_OFF + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -368,10 +327,13 @@ __global__ void __launch_bounds__(Cfg<DUAL>::NTHREADS, 1)
     const int nkt = p.K / BK;
     const int nbk = p.K / kBlock;
     const size_t scale_off = blob_scales_offset(p.rows, nbk);
-    auto slot_ptr = [&](int slot) { return smem + slot * C::SLOT_STRIDE; };
+    auto slot_ptr = [&](int slot) { return smem + slot * SLOT_STRIDE; };
 
-    if (warp == W_TMA) {
-        if (lane == 0) {
+    if (warp >= W_TMA && warp < W_EPI) {
+        // warpgroup 1: one setmaxnreg for all four warps, then the TMA and
+        // MMA roles (warps 6 and 7 only join the final barrier)
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProdRegs));
+        if (warp == W_TMA && lane == 0) {
             int it = 0;
             for (int t = blockIdx.x; t < total; t += gridDim.x) {
                 int u, rt, tt, nc;
@@ -381,14 +343,13 @@ __global__ void __launch_bounds__(Cfg<DUAL>::NTHREADS, 1)
                     const int slot = it % STAGES;
                     const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
                     if (!mbar_wait(empty0 + 8 * slot, ph ^ 1u, abort_flag, p.error, 2)) goto tma_done;
-                    mbar_arrive_tx(full0 + 8 * slot, C::B_BYTES);
-                    tma_load_2d(smem_u32(slot_ptr(slot) + NA * C::A_BYTES), &tmB, kt * BK, pos0, full0 + 8 * slot);
+                    mbar_arrive_tx(full0 + 8 * slot, B_BYTES);
+                    tma_load_2d(smem_u32(slot_ptr(slot) + A_BYTES), &tmB, kt * BK, pos0, full0 + 8 * slot);
                 }
             }
         tma_done:;
         }
-    } else if (warp == W_MMA) {
-        if (lane == 0) {
+        if (warp == W_MMA && lane == 0) {
             int it = 0, qc = 0;
             // the tile's MMA width: its valid token columns rounded up to 16
             // (the record of the next tile is requested a tile ahead)
@@ -404,7 +365,8 @@ __global__ void __launch_bounds__(Cfg<DUAL>::NTHREADS, 1)
                         goto mma_done;
                     tc_fence_after();
                     uint8_t *st = slot_ptr(slot);
-                    const uint64_t db = sdesc(smem_u32(st + NA * C::A_BYTES));
+                    const uint64_t da = sdesc(smem_u32(st));
+                    const uint64_t db = sdesc(smem_u32(st + A_BYTES));
                     for (int blk = 0; blk < 2; ++blk, ++qc) {
                         const int j = qc % NTBUF;
                         if (!mbar_wait(tempty0 + 8 * j, ((uint32_t)(qc / NTBUF) & 1u) ^ 1u, abort_flag, p.error, 8))
@@ -413,12 +375,7 @@ __global__ void __launch_bounds__(Cfg<DUAL>::NTHREADS, 1)
 #pragma unroll
                         for (int kk = 0; kk < 2; ++kk) {
                             const uint64_t koff = (uint64_t)((blk * 32 + kk * 16) * 2) >> 4;
-#pragma unroll
-                            for (int a = 0; a < NA; ++a) {
-                                const uint64_t da = sdesc(smem_u32(st + a * C::A_BYTES));
-                                mma_f16(tmem + (uint32_t)(j * C::TBUF + a * BN), da + koff, db + koff, idesc,
-                                        kk > 0 ? 1u : 0u);
-                            }
+                            mma_f16(tmem + (uint32_t)(j * BN), da + koff, db + koff, idesc, kk > 0 ? 1u : 0u);
                         }
                         mma_commit(tfull0 + 8 * j);
                     }
@@ -427,52 +384,50 @@ __global__ void __launch_bounds__(Cfg<DUAL>::NTHREADS, 1)
             }
         mma_done:;
         }
-    } else if (warp < W_EPI) {
-        // Converters: thread r owns row r of the A tiles.  Raw Q4 codes and
-        // both scale sets of stage s are fetched with cp.async PD stages ahead
-        // into raw ring entry s % RR; stage s is then converted into its slot.
+    } else if (warp < W_TMA) {
+        // Converters: thread r owns row r of the A tile.  Raw Q4 codes, the
+        // row's two block scales and the tile columns' activation scales of
+        // stage s are fetched with cp.async PD stages ahead into raw ring
+        // entry s % RR; stage s is then converted into its slot.
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProdRegs));
         const int r = threadIdx.x - W_CONV * 32;
-        uint8_t *raw = smem + C::RAW_OFF;
+        uint8_t *raw = smem + RAW_OFF;
         StageCur fc;  // fetch cursor; conversion only counts stages
-        cur_init<BN>(fc, p, n_uniq, total);
+        cur_init<DUAL>(fc, p, total, r);
         const int n_stages = blockIdx.x < total ? ((total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1) * nkt : 0;
         auto fetch = [&](const StageCur &c, int rs) {
-            uint8_t *ent = raw + rs * C::RAW_BYTES;
+            uint8_t *ent = raw + rs * RAW_BYTES;
             if (c.valid) {
-                const int row = c.rt * BM + r;
+                const int row = tile_row<DUAL>(c.rt, r);
                 const bool vrow = row < p.rows;
                 const int srow = vrow ? row : 0;
+                const uint8_t *src = c.blob + ((size_t)srow * nbk + 2 * c.kt) * 16;
+                const uint32_t dst = smem_u32(ent + r * 32);
+                cp_async(dst, src, 16, vrow);
+                cp_async(dst + 16, src + 16, 16, vrow);
+                const uint8_t *ssrc = c.blob + scale_off + ((size_t)srow * nbk + 2 * c.kt) * 2;
+                cp_async(smem_u32(ent + RAW_CODES + r * 4), ssrc, 4, vrow);
 #pragma unroll
-                for (int a = 0; a < NA; ++a) {
-                    const uint8_t *blob = c.blob[a];
-                    const uint8_t *src = blob + ((size_t)srow * nbk + 2 * c.kt) * 16;
-                    const uint32_t dst = smem_u32(ent + (a * BM + r) * 32);
-                    cp_async(dst, src, 16, vrow);
-                    cp_async(dst + 16, src + 16, 16, vrow);
-                    const uint8_t *ssrc = blob + scale_off + ((size_t)srow * nbk + 2 * c.kt) * 2;
-                    cp_async(smem_u32(ent + C::RAW_CODES + (a * BM + r) * 4), ssrc, 4, vrow);
-                }
-                const int pos0 = c.pos0;
-                for (int i = r; i < 2 * BN; i += 128) {
+                for (int i = r; i < 2 * BN; i += BM) {
                     const int q = i / BN, col = i - q * BN;
-                    const int pos = pos0 + col;
+                    const int pos = c.pos0 + col;
                     const bool v = pos < p.A_pad;
-                    const float *src = p.a_scaleT + (size_t)(2 * c.kt + q) * p.A_pad + (v ? pos : 0);
-                    cp_async(smem_u32(ent + C::RAW_CODES + C::WS_BYTES + i * 4), src, 4, v);
+                    const float *asrc = p.a_scaleT + (size_t)(2 * c.kt + q) * p.A_pad + (v ? pos : 0);
+                    cp_async(smem_u32(ent + RAW_CODES + WS_BYTES + i * 4), asrc, 4, v);
                 }
             }
             cp_commit();
         };
-        for (int i = 0; i < C::PD; ++i) {
-            fetch(fc, i % C::RR);
-            cur_next<BN>(fc, p, n_uniq, total, nkt);
+        for (int i = 0; i < PD; ++i) {
+            fetch(fc, i % RR);
+            cur_next<DUAL>(fc, p, total, nkt, r);
         }
         int it = 0;
         while (it < n_stages) {
-            fetch(fc, (it + C::PD) % C::RR);
-            cur_next<BN>(fc, p, n_uniq, total, nkt);
-            cp_wait<C::PD>();
-            const uint8_t *ent = raw + (it % C::RR) * C::RAW_BYTES;
+            fetch(fc, (it + PD) % RR);
+            cur_next<DUAL>(fc, p, total, nkt, r);
+            cp_wait<PD>();
+            const uint8_t *ent = raw + (it % RR) * RAW_BYTES;
             const int slot = it % STAGES;
             const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
             bool ok = true;
@@ -480,17 +435,13 @@ __global__ void __launch_bounds__(Cfg<DUAL>::NTHREADS, 1)
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
             if (!ok) break;
             uint8_t *st = slot_ptr(slot);
+            const uint4 *cs = (const uint4 *)(ent + r * 32);
+            convert_store_row(st, r, cs[0], cs[1]);
+            *(uint32_t *)(st + A_BYTES + B_BYTES + r * 4) = *(const uint32_t *)(ent + RAW_CODES + r * 4);
 #pragma unroll
-            for (int a = 0; a < NA; ++a) {
-                const uint4 *cs = (const uint4 *)(ent + (a * BM + r) * 32);
-                convert_store_row(st + a * C::A_BYTES, r, cs[0], cs[1]);
-                // this row's two weight scales of the stage
-                *(uint32_t *)(st + NA * C::A_BYTES + C::B_BYTES + (a * BM + r) * 4) =
-                    *(const uint32_t *)(ent + C::RAW_CODES + (a * BM + r) * 4);
-            }
-            for (int i = r; i < 2 * BN; i += 128)
-                *(float *)(st + NA * C::A_BYTES + C::B_BYTES + C::WS_BYTES + i * 4) =
-                    *(const float *)(ent + C::RAW_CODES + C::WS_BYTES + i * 4);
+            for (int i = r; i < 2 * BN; i += BM)
+                *(float *)(st + A_BYTES + B_BYTES + WS_BYTES + i * 4) =
+                    *(const float *)(ent + RAW_CODES + WS_BYTES + i * 4);
             fence_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(full0 + 8 * slot);
@@ -498,31 +449,26 @@ __global__ void __launch_bounds__(Cfg<DUAL>::NTHREADS, 1)
         }
         cp_wait<0>();
     } else {
-        // epilogue: TMEM lane quarter = warp % 4 (thread = weight row), half =
-        // which HC token columns this warp owns.  Per K stage: one wait (the
-        // MMA's commit after the stage's second block covers the first), the
-        // activation scales of the warp's columns read once per block, the
-        // block sums read 32 columns per TMEM load, and the scaling as packed
-        // fp32 pairs: s = d_w * d_a (mul.f32x2), acc += sum * s (fma.f32x2).
+        // Epilogue: TMEM lane quarter = warp % 4 (thread = tile row), column
+        // group = 32 token columns.  Per K block: one 32-column TMEM load,
+        // s = d_w * d_a (mul.f32x2) and acc += sum * s (fma.f32x2), the
+        // activation scales of four columns per 128-bit broadcast load.
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kEpiRegs));
+        const int e = warp - W_EPI;
         const int quarter = warp & 3;
-        const int half = (warp - W_EPI) >> 2;  // which column part this warp owns
-        constexpr int HC = BN / EPI_SPLIT;      // token columns per epilogue warp
-        static_assert(HC % 32 == 0, "32-column groups per epilogue warp");
+        const int grp = e >> 2;  // column group: columns [32 grp, 32 grp + 32)
         const int r = quarter * 32 + lane;
+        float *xch = (float *)(smem + XCH_OFF);
         int qc = 0, it = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
             int u, rt, tt, ncols;
             decode_tile(p.tile_rec, t, u, rt, tt, ncols);
-            const int ncw = ncols - half * HC;  // this warp's valid columns (may be <= 0)
-            const int row = rt * BM + r;
-            const bool vrow = row < p.rows;
-            const int pos0 = p.uniq_off[u] + tt * BN + half * HC;
+            const bool active = grp * 32 < ncols;  // warp-uniform
+            const int pos0 = p.uniq_off[u] + tt * BN + grp * 32;
             const int pos_end = p.uniq_off[u + 1];
-            float acc[NA][HC];
+            float2 acc[16];
 #pragma unroll
-            for (int a = 0; a < NA; ++a)
-#pragma unroll
-                for (int c = 0; c < HC; ++c) acc[a][c] = 0.0f;
+            for (int c = 0; c < 16; ++c) acc[c] = make_float2(0.0f, 0.0f);
             for (int kt = 0; kt < nkt; ++kt, ++it, qc += 2) {
                 const int slot = it % STAGES;
                 const uint8_t *st = slot_ptr(slot);
@@ -537,37 +483,29 @@ __global__ void __launch_bounds__(Cfg<DUAL>::NTHREADS, 1)
                 ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                 if (!ok) goto epi_done;
                 tc_fence_after();
-                uint32_t wsc[NA];
+                if (active) {
+                    const uint32_t wsc = *(const uint32_t *)(st + A_BYTES + B_BYTES + r * 4);
+                    const float4 *cs4 = (const float4 *)(st + A_BYTES + B_BYTES + WS_BYTES) + grp * 8;
 #pragma unroll
-                for (int a = 0; a < NA; ++a)
-                    wsc[a] = *(const uint32_t *)(st + NA * C::A_BYTES + C::B_BYTES + (a * BM + r) * 4);
-                const float *asc = (const float *)(st + NA * C::A_BYTES + C::B_BYTES + C::WS_BYTES) + half * HC;
+                    for (int blk = 0; blk < 2; ++blk) {
+                        const int j = blk ? j1 : j0;
+                        uint32_t sv[32];
+                        tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(j * BN + grp * 32), sv);
+                        const float dw =
+                            __half2float(__ushort_as_half((unsigned short)(blk ? (wsc >> 16) : (wsc & 0xffffu))));
+                        const float2 dw2 = make_float2(dw, dw);
+                        tmem_ld_wait();
 #pragma unroll
-                for (int blk = 0; blk < 2; ++blk) {
-                    const int j = blk ? j1 : j0;
-                    const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(j * C::TBUF + half * HC);
-                    float dw[NA];
-#pragma unroll
-                    for (int a = 0; a < NA; ++a) {
-                        const uint32_t dwb = blk ? (wsc[a] >> 16) : (wsc[a] & 0xffffu);
-                        dw[a] = __half2float(__ushort_as_half((unsigned short)dwb));
-                    }
-                    const float2 *dq2 = reinterpret_cast<const float2 *>(asc + blk * BN);
-#pragma unroll
-                    for (int cb = 0; cb < HC; cb += 16) {
-                        if (cb >= ncw) break;  // columns past the tile's tokens (warp-uniform)
-#pragma unroll
-                        for (int a = 0; a < NA; ++a) {
-                            // block sums of 16 columns of tensor a
-                            uint32_t pv[16];
-                            tmem_ld16u(tb + (uint32_t)(a * BN + cb), pv);
-                            tmem_ld_wait();
-#pragma unroll
-                            for (int c = 0; c < 8; ++c) {
-                                const float2 d2 = dq2[(cb >> 1) + c];  // activation scales: broadcast reads
-                                fma_scaled2(acc[a][cb + 2 * c], acc[a][cb + 2 * c + 1], pv[2 * c], pv[2 * c + 1], d2.x,
-                                            d2.y, dw[a]);
-                            }
+                        for (int c4 = 0; c4 < 8; ++c4) {
+                            const float4 d4 = cs4[blk * (BN / 4) + c4];  // broadcast read
+                            const float2 s01 = __fmul2_rn(dw2, make_float2(d4.x, d4.y));
+                            const float2 s23 = __fmul2_rn(dw2, make_float2(d4.z, d4.w));
+                            acc[2 * c4] = __ffma2_rn(make_float2(__uint_as_float(sv[4 * c4]),
+                                                                 __uint_as_float(sv[4 * c4 + 1])),
+                                                     s01, acc[2 * c4]);
+                            acc[2 * c4 + 1] = __ffma2_rn(make_float2(__uint_as_float(sv[4 * c4 + 2]),
+                                                                     __uint_as_float(sv[4 * c4 + 3])),
+                                                         s23, acc[2 * c4 + 1]);
                         }
                     }
                 }
@@ -579,45 +517,82 @@ __global__ void __launch_bounds__(Cfg<DUAL>::NTHREADS, 1)
                     mbar_arrive(empty0 + 8 * slot);
                 }
             }
-            // tile outputs (this warp's token columns); the assignment ids of
-            // the columns are fetched once (lane i: columns i, i + 32, ...)
-            int asg_l[HC / 32];
-#pragma unroll
-            for (int i = 0; i < HC / 32; ++i) {
-                const int pos = pos0 + i * 32 + lane;
-                asg_l[i] = pos < pos_end ? __ldg(p.assign + pos) : 0;
-            }
+            // tile outputs; the assignment id of column i of this warp's group
+            // is held by lane i
+            const int my_pos = pos0 + lane;
+            const int my_asg = my_pos < pos_end ? __ldg(p.assign + my_pos) : 0;
             if (DUAL) {
-                const int fb = (rt * BM + quarter * 32) / kBlock;  // h block index along F
-                const bool vblk = rt * BM + quarter * 32 < p.rows;
+                // SwiGLU pairs gate row f (quarter q < 2) with up row f (quarter
+                // q + 2), same lane, same column group; the gate warp finishes
+                // columns 0..15 of the group, the up warp columns 16..31, each
+                // receiving the other tensor's values through shared memory.
+                const int pair = grp * 2 + (quarter & 1);
+                const bool is_gate = quarter < 2;
+                float *to_partner = xch + ((size_t)(pair * 2 + (is_gate ? 0 : 1)) * 16) * 32;
+                const float *from_partner = xch + ((size_t)(pair * 2 + (is_gate ? 1 : 0)) * 16) * 32;
+                if (active) {
 #pragma unroll
-                for (int c = 0; c < HC; ++c) {
-                    if (c >= ncw) break;  // warp-uniform
-                    const int pos = pos0 + c;
-                    const float g = acc[0][c], uu = acc[NA - 1][c];
-                    const float h = g * uu / (1.0f + expf(-g));
-                    const float amax = warp_max(fabsf(h));
-                    const float dd = __half2float(__float2half_rn(amax / 127.0f));
-                    int qv = 0;
-                    if (dd != 0.0f) qv = (int)fminf(fmaxf(rintf(h / dd), -127.0f), 127.0f);
-                    const int s = warp_sum_i(qv);
-                    const int a = __shfl_sync(0xffffffffu, asg_l[c / 32], c % 32);
-                    if (vblk && pos < pos_end) {
-                        p.hq16[(size_t)pos * p.F_out + row] = __int2half_rn(qv);
-                        p.hq[(size_t)a * p.F_out + row] = (int8_t)qv;
-                        if (lane == 0) {
-                            p.hdT[(size_t)fb * p.A_pad + pos] = dd;
-                            p.hds[(size_t)a * (p.F_out / kBlock) + fb] = BlockScale{dd, s};
+                    for (int c = 0; c < 8; ++c) {
+                        // the gate warp sends columns 16..31, the up warp 0..15
+                        const float2 v = is_gate ? acc[8 + c] : acc[c];
+                        to_partner[(2 * c) * 32 + lane] = v.x;
+                        to_partner[(2 * c + 1) * 32 + lane] = v.y;
+                    }
+                }
+                bar_sync_named(1 + pair, 64);
+                if (active) {
+                    // this warp's 16 columns of the group (gate warp: 0..15, up warp: 16..31)
+                    float mine[16];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const float2 v = is_gate ? acc[c] : acc[8 + c];
+                        mine[2 * c] = v.x;
+                        mine[2 * c + 1] = v.y;
+                    }
+                    const int c0 = is_gate ? 0 : 16;
+                    const int fb = (rt * 64 + (quarter & 1) * 32) / kBlock;  // h block index along F
+                    const int f = rt * 64 + (quarter & 1) * 32 + lane;       // F row of this lane
+                    const int nc = min(16, ncols - grp * 32 - c0);           // valid columns (warp-uniform)
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        if (c < nc) {
+                            const float other = from_partner[c * 32 + lane];
+                            const float g = is_gate ? mine[c] : other, uu = is_gate ? other : mine[c];
+                            const float h = g * uu / (1.0f + expf(-g));
+                            const float amax =
+                                __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(h))));
+                            const float dd = __half2float(__float2half_rn(amax / 127.0f));
+                            int qv = 0;
+                            if (dd != 0.0f) qv = (int)fminf(fmaxf(rintf(h / dd), -127.0f), 127.0f);
+                            const int s = __reduce_add_sync(0xffffffffu, qv);
+                            const int col = c0 + c;
+                            const int pos = pos0 + col;
+                            const int a = __shfl_sync(0xffffffffu, my_asg, col);
+                            if (pos < pos_end) {
+                                p.hq16[(size_t)pos * p.F_out + f] = __int2half_rn(qv);
+                                p.hq[(size_t)a * p.F_out + f] = (int8_t)qv;
+                                if (lane == 0) {
+                                    p.hdT[(size_t)fb * p.A_pad + pos] = dd;
+                                    p.hds[(size_t)a * (p.F_out / kBlock) + fb] = BlockScale{dd, s};
+                                }
+                            }
                         }
                     }
                 }
-            } else {
+                // the exchange area is rewritten at the end of the next tile
+                bar_sync_named(1 + pair, 64);
+            } else if (active) {
+                const int row = rt * BM + r;
+                const bool vrow = row < p.rows;
+                const int nc = min(32, ncols - grp * 32);  // valid columns (warp-uniform)
 #pragma unroll
-                for (int c = 0; c < HC; ++c) {
-                    if (c >= ncw) break;  // warp-uniform
-                    const int pos = pos0 + c;
-                    const int a = __shfl_sync(0xffffffffu, asg_l[c / 32], c % 32);
-                    if (vrow && pos < pos_end) p.o[(size_t)a * p.rows + row] = acc[0][c];
+                for (int c = 0; c < 32; ++c) {
+                    if (c < nc) {
+                        const int pos = pos0 + c;
+                        const int a = __shfl_sync(0xffffffffu, my_asg, c);
+                        const float v = (c & 1) ? acc[c >> 1].y : acc[c >> 1].x;
+                        if (vrow && pos < pos_end) p.o[(size_t)a * p.rows + row] = v;
+                    }
                 }
             }
         }
@@ -826,14 +801,23 @@ int launch_stage(const StageParams &p, size_t blob_bytes, int n_sm, cudaStream_t
     return (int)cudaGetLastError();
 }
 
-int gemm_smem_bytes(bool dual) { return dual ? gemm::Cfg<true>::SMEM : gemm::Cfg<false>::SMEM; }
-int gemm_bn(bool dual) { return dual ? gemm::Cfg<true>::BN : gemm::Cfg<false>::BN; }
+int gemm_bn(bool) { return gemm::BN; }
+// Weight rows of the layer's tensors covered by one row tile: 64 F rows for
+// gate/up (64 gate + the same 64 up rows), 128 H rows for down.
+int gemm_rows_per_tile(bool dual) { return dual ? 64 : gemm::BM; }
 
 int gemm_configure() {
+    // the kernels' register split assumes ptxas gave them kLaunchRegs per thread
+    for (const void *fn : {(const void *)gemm::grouped_gemm_kernel<true>, (const void *)gemm::grouped_gemm_kernel<false>}) {
+        cudaFuncAttributes fa{};
+        cudaError_t e = cudaFuncGetAttributes(&fa, fn);
+        if (e != cudaSuccess) return (int)e;
+        if (fa.numRegs != gemm::kLaunchRegs) return (int)cudaErrorInvalidConfiguration;
+    }
     cudaError_t e1 = cudaFuncSetAttribute(gemm::grouped_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          gemm::Cfg<true>::SMEM);
+                                          gemm::SMEM);
     cudaError_t e2 = cudaFuncSetAttribute(gemm::grouped_gemm_kernel<false>,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize, gemm::Cfg<false>::SMEM);
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize, gemm::SMEM);
     return (int)(e1 != cudaSuccess ? e1 : e2);
 }
 
@@ -855,10 +839,10 @@ int launch_prefill(const PrefillLaunch &L, cudaStream_t st, cudaEvent_t const *e
     if (g > 0) gather_kernel<<<g, 256, 0, st>>>(L.gu.assign, A, L.k, L.H, L.xq, L.xds, L.xs16, L.xdT, L.gu.A_pad);
     // timing hook: events around each GEMM launch
     if (ev) record_event(ev[0], st);
-    gemm::grouped_gemm_kernel<true><<<L.n_sm, gemm::Cfg<true>::NTHREADS, gemm::Cfg<true>::SMEM, st>>>(L.tm_x, L.gu);
+    gemm::grouped_gemm_kernel<true><<<L.n_sm, gemm::NTHREADS, gemm::SMEM, st>>>(L.tm_x, L.gu);
     if (ev) record_event(ev[1], st);
     if (ev) record_event(ev[2], st);
-    gemm::grouped_gemm_kernel<false><<<L.n_sm, gemm::Cfg<false>::NTHREADS, gemm::Cfg<false>::SMEM, st>>>(L.tm_h, L.dn);
+    gemm::grouped_gemm_kernel<false><<<L.n_sm, gemm::NTHREADS, gemm::SMEM, st>>>(L.tm_h, L.dn);
     if (ev) record_event(ev[3], st);
     const size_t n = (size_t)L.T * L.H;
     int gc = (int)std::min<size_t>((n + 255) / 256, (size_t)L.n_sm * 16);

@@ -617,8 +617,9 @@ int moe_layer_init(const moe_cfg *cfg, void *cuda_stream, moe_ctx **out) {
         CKI(cudaMemset(ctx->hdT, 0, sizeof(float) * AP * (ctx->F / 32)));
         CKI(cudaMalloc(&ctx->tile_off, sizeof(int32_t) * 2 * (U + 1)));
         // tiles per GEMM <= row tiles x (assignments / tile width + used experts)
-        ctx->cap_gu = ((ctx->F + 127) / 128) * (int)((A + moe::gemm_bn(true) - 1) / moe::gemm_bn(true) + U);
-        ctx->cap_dn = ((ctx->H + 127) / 128) * (int)((A + moe::gemm_bn(false) - 1) / moe::gemm_bn(false) + U);
+        const int rg = moe::gemm_rows_per_tile(true), rd = moe::gemm_rows_per_tile(false);
+        ctx->cap_gu = ((ctx->F + rg - 1) / rg) * (int)((A + moe::gemm_bn(true) - 1) / moe::gemm_bn(true) + U);
+        ctx->cap_dn = ((ctx->H + rd - 1) / rd) * (int)((A + moe::gemm_bn(false) - 1) / moe::gemm_bn(false) + U);
         CKI(cudaMalloc(&ctx->tile_rec, sizeof(uint2) * ((size_t)ctx->cap_gu + ctx->cap_dn)));
         CKI(cudaMalloc(&ctx->etbl, sizeof(uint64_t) * 3 * Et));
         ctx->stage_cap = 3 * E;
@@ -978,9 +979,9 @@ static int ffn_forward_body(moe_ctx *ctx, int layer, const float *d_x, int n_tok
         L.tiling.cap_dn = ctx->cap_dn;
         L.tiling.tid0 = layer * 3;
         L.tiling.n_tokens = T;
-        L.tiling.rt_gu = (ctx->F + 127) / 128;
+        L.tiling.rt_gu = (ctx->F + moe::gemm_rows_per_tile(true) - 1) / moe::gemm_rows_per_tile(true);
         L.tiling.bn_gu = moe::gemm_bn(true);
-        L.tiling.rt_dn = (ctx->H + 127) / 128;
+        L.tiling.rt_dn = (ctx->H + moe::gemm_rows_per_tile(false) - 1) / moe::gemm_rows_per_tile(false);
         L.tiling.bn_dn = moe::gemm_bn(false);
         moe::GemmParams g{};
         g.n_uniq = gp.n_uniq;
