@@ -500,14 +500,24 @@ def run_case(args):
     y = torch.empty((T, H), device="cuda")
     torch.cuda.synchronize()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    kt = []
+    qec.moe_debug_timing(ctx, True)
     for s in range(n):
         evs[s][0].record(st)
         qec.moe_ffn_forward_routed(ctx, 0, xs[s], lgs[s], T, idx[s], w[s], y, st.cuda_stream)
         evs[s][1].record(st)
+        gu, dn = qec.moe_debug_timing_read(ctx, 1)
+        kt.append((gu[0], dn[0]))
     torch.cuda.synchronize()
     ms = [a.elapsed_time(b) for a, b in evs]
     qec.moe_destroy(ctx)
-    res = {"case": args.case, "tokens": T, "launches": n, "median_ms_per_forward": round(float(np.median(ms[2:])), 5)}
+    res = {"case": args.case, "tokens": T, "launches": n, "median_ms_per_forward": round(float(np.median(ms[2:])), 5),
+           "median_ms_gate_up_kernel": round(float(np.median([a for a, _ in kt[2:]])), 5),
+           "median_ms_down_kernel": round(float(np.median([b for _, b in kt[2:]])), 5)}
+    if T > 32:
+        flop_gu = 2.0 * T * k * 2 * H * F
+        res["gate_up_tflops"] = round(flop_gu / (res["median_ms_gate_up_kernel"] * 1e-3) / 1e12, 1)
+        res["down_tflops"] = round(flop_gu / 2 / (res["median_ms_down_kernel"] * 1e-3) / 1e12, 1)
     if cap == 0:
         # every weight byte crosses the host link
         b = float(np.median(ms[2:]))

@@ -23,11 +23,11 @@
 // swizzle row of fp16), four 128-column K-block buffers in TMEM (all 512
 // columns).  Gate/up tiles stack 64 gate rows over the same 64 up rows, so
 // one MMA per K step serves both tensors and the tile's SwiGLU pairs lane l of
-// TMEM quarter q with lane l of quarter q + 2.  Warp roles (24 warps): 0-3
+// TMEM quarter q with lane l of quarter q + 2.  Warp roles (28 warps): 0-7
 // weight converters (Q4 codes and scales fetched with cp.async through the
 // expert table -- HBM pool, staged slot or zero-copy host memory -- several
-// stages ahead, expanded to fp16 in the 128-B swizzled K-major layout); 4 TMA
-// producer of the token tile; 5 TMEM owner and MMA issuer; 8-23 epilogue:
+// stages ahead, expanded to fp16 in the 128-B swizzled K-major layout); 8 TMA
+// producer of the token tile; 9 TMEM owner and MMA issuer; 12-27 epilogue:
 // TMEM lane quarter = warp % 4, 32 token columns per warp.  Per K
 // block an epilogue thread reads its row's 32 block sums with one TMEM load;
 // the columns' activation scales are broadcast shared-memory reads.
@@ -49,37 +49,42 @@ constexpr int BM = 128;   // weight rows per tile (TMEM lanes)
 constexpr int BN = 128;   // token columns per tile
 constexpr int BK = 64;    // K per pipeline stage (two quantization blocks)
 // Warp roles by warpgroup (setmaxnreg moves registers between warpgroups):
-// warpgroup 0 = the 4 converter warps, warpgroup 1 = TMA producer, MMA issuer
-// and two warps that only join the final barrier, warpgroups 2-5 = the 16
-// epilogue warps (4 lane quarters x 4 column groups).
-constexpr int W_CONV = 0, W_TMA = 4, W_MMA = 5, W_EPI = 8;
+// warpgroups 0-1 = the 8 converter warps, warpgroup 2 = TMA producer, MMA
+// issuer and two warps that only join the final barrier, warpgroups 3-6 =
+// the 16 epilogue warps (4 lane quarters x 4 column groups).
+constexpr int W_CONV = 0, N_CONV = 8, W_TMA = 8, W_MMA = 9, W_EPI = 12;
 constexpr int N_EPI = 16;
-constexpr int NTHREADS = (W_EPI + N_EPI) * 32;  // 768
+constexpr int NTHREADS = (W_EPI + N_EPI) * 32;  // 896
 // Register split: launched with kLaunchRegs per thread (ptxas' allocation for
-// 768 threads, checked on the host before the first launch), warpgroups 0-1
-// drop to kProdRegs and warpgroups 2-5 rise to kEpiRegs; the two splits
-// move the same number of registers.
-constexpr int kLaunchRegs = 80, kProdRegs = 56, kEpiRegs = 88;
-static_assert(2 * 128 * kProdRegs + 4 * 128 * kEpiRegs <= NTHREADS * kLaunchRegs, "register split");
+// 896 threads, checked on the host before the first launch), warpgroups 0-2
+// drop to kProdRegs and warpgroups 3-6 rise to kEpiRegs.
+constexpr int kLaunchRegs = 72, kProdRegs = 48, kEpiRegs = 88;
+static_assert(3 * 128 * kProdRegs + 4 * 128 * kEpiRegs <= NTHREADS * kLaunchRegs, "register split");
 constexpr long long kTimeoutCycles = 4000000000ll;
 
-constexpr int STAGES = 4;                        // A/B pipeline slots
+// Operand ring (A and B tiles of a stage; freed by the MMA's commit alone)
+// and scale ring (the stage's weight and activation scales, freed by the
+// epilogue), so that neither the converters nor the TMA wait for the
+// epilogue's arithmetic.
+constexpr int STAGES = 4;                        // operand slots
+constexpr int SR = 8;                            // scale slots
 constexpr int RR = 6;                            // raw prefetch ring of the converters (cp.async)
 constexpr int PD = RR - 1;                       // prefetch distance in stages
 constexpr int A_BYTES = BM * BK * 2;             // fp16 weight tile, 128-B swizzle
 constexpr int B_BYTES = BN * BK * 2;             // fp16 token tile (TMA), 128-B swizzle
+constexpr int SLOT_STRIDE = A_BYTES + B_BYTES;   // 32 KB, 1024-aligned
 constexpr int WS_BYTES = BM * 2 * 2;             // weight scales [row][2 blocks] binary16
 constexpr int CS_BYTES = 2 * BN * 4;             // activation scales [2 blocks][column] fp32
-constexpr int SLOT_BYTES = A_BYTES + B_BYTES + WS_BYTES + CS_BYTES;
-constexpr int SLOT_STRIDE = (SLOT_BYTES + 1023) / 1024 * 1024;
+constexpr int SC_BYTES = WS_BYTES + CS_BYTES;
+constexpr int SC_OFF = STAGES * SLOT_STRIDE;
 constexpr int RAW_CODES = BM * 32;               // raw ring entry: Q4 codes [row][32 B], then scales
-constexpr int RAW_BYTES = RAW_CODES + WS_BYTES + CS_BYTES;
-constexpr int RAW_OFF = STAGES * SLOT_STRIDE;
+constexpr int RAW_BYTES = RAW_CODES + SC_BYTES;
+constexpr int RAW_OFF = SC_OFF + SR * SC_BYTES;
 constexpr int XCH_OFF = RAW_OFF + RR * RAW_BYTES;  // SwiGLU exchange: [8 pairs][2][16 cols][32 lanes] fp32
 constexpr int XCH_BYTES = 8 * 2 * 16 * 32 * 4;
 constexpr int NTBUF = 4;                         // K-block accumulators in TMEM (BN columns each)
 constexpr int BAR_OFF = XCH_OFF + XCH_BYTES;
-constexpr int NBARS = 2 * STAGES + 2 * NTBUF;
+constexpr int NBARS = 2 * STAGES + 2 * SR + 2 * NTBUF;
 constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
 constexpr int SMEM = MISC_OFF + 16 + 1024;       // + alignment slack
 static_assert(SMEM <= 227 * 1024, "shared memory of the GEMM CTA");
@@ -96,34 +101,36 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 __device__ __forceinline__ void mbar_arrive_tx(uint32_t bar, uint32_t tx) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(tx) : "memory");
 }
-// One try: the thread is suspended (not spinning) until the phase completes
-// or about kSuspendNs pass, so waiting warps leave their issue slots to the
-// converter and epilogue warps.
-constexpr uint32_t kSuspendNs = 20000;
+// One test of an mbarrier phase (mbarrier.try_wait: the hardware may hold the
+// thread for a short, system-dependent time while the phase is incomplete).
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
-        "{\n.reg .pred P;\nmbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2, %3;\nselp.u32 %0, 1, 0, P;\n}"
+        "{\n.reg .pred P;\nmbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2;\nselp.u32 %0, 1, 0, P;\n}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity), "r"(kSuspendNs)
+        : "r"(bar), "r"(parity)
         : "memory");
     return ok != 0;
 }
 
 // Bounded wait: false when the CTA is aborting or the wait expired (then the
-// abort flag and an error bit are set).
+// abort flag and an error bit are set).  The abort flag and the clock are
+// checked every 64 tests, so a waiting warp issues little besides the tests.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag, int *err,
                                           int code) {
+    if (mbar_try(bar, parity)) return true;
     const long long t0 = clock64();
-    while (!mbar_try(bar, parity)) {
-        if (*abort_flag) return false;
-        if (clock64() - t0 > kTimeoutCycles) {
-            *abort_flag = 1;
-            atomicOr(err, code);
-            return false;
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_try(bar, parity)) return true;
+        if ((n & 63) == 0) {
+            if (*abort_flag) return false;
+            if (clock64() - t0 > kTimeoutCycles) {
+                *abort_flag = 1;
+                atomicOr(err, code);
+                return false;
+            }
         }
     }
-    return true;
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *tm, int x, int y, uint32_t bar) {
@@ -188,9 +195,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t *r) {
         : "r"(taddr));
 }
 
-// Q4 codes of one row and two quantization blocks (32 B) -> 64 fp16 values
-// (q - 8) in K order, stored as 8 16-byte chunks of the row in the 128-B
-// swizzled layout (chunk c of row r of an 8-row group sits at chunk c ^ r).
 // Four codes (one nibble per byte of n, values 0..15) -> two fp16 pairs
 // (q0 - 8, q1 - 8), (q2 - 8, q3 - 8): the bytes are placed under the fp16
 // exponent byte 0x64 (1024 + q, exact) and 1032 is subtracted (exact).
@@ -204,25 +208,24 @@ __device__ __forceinline__ void nib4(uint32_t n, uint32_t &p01, uint32_t &p23) {
     p23 = *reinterpret_cast<uint32_t *>(&hb);
 }
 
-__device__ __forceinline__ void convert_store_row(uint8_t *tile, int r, uint4 c0, uint4 c1) {
-    const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+// Q4 codes of one row and one quantization block (16 B) -> 32 fp16 values
+// (q - 8) in K order: chunks 4 hb .. 4 hb + 3 of the row in the 128-B
+// swizzled layout (chunk c of row r of an 8-row group sits at chunk c ^ r).
+__device__ __forceinline__ void convert_store_block(uint8_t *tile, int r, int hb, uint4 c) {
+    const uint32_t q[4] = {c.x, c.y, c.z, c.w};
     uint8_t *rowbase = tile + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
-    for (int blk = 0; blk < 2; ++blk) {
-        const uint32_t *q = w + 4 * blk;  // 16 code bytes of this block
-#pragma unroll
-        for (int part = 0; part < 4; ++part) {
-            // part 0: elements 0..7 (low nibbles of bytes 0..7), 1: 8..15
-            // (low, bytes 8..15), 2: 16..23 (high, bytes 0..7), 3: 24..31
-            const uint32_t wa = q[(part & 1) * 2], wb = q[(part & 1) * 2 + 1];
-            const uint32_t na = (part >> 1) ? (wa >> 4) & 0x0F0F0F0Fu : wa & 0x0F0F0F0Fu;
-            const uint32_t nb = (part >> 1) ? (wb >> 4) & 0x0F0F0F0Fu : wb & 0x0F0F0F0Fu;
-            uint4 out;
-            nib4(na, out.x, out.y);
-            nib4(nb, out.z, out.w);
-            const int chunk = blk * 4 + part;
-            *reinterpret_cast<uint4 *>(rowbase + ((chunk ^ (r & 7)) << 4)) = out;
-        }
+    for (int part = 0; part < 4; ++part) {
+        // part 0: elements 0..7 (low nibbles of bytes 0..7), 1: 8..15
+        // (low, bytes 8..15), 2: 16..23 (high, bytes 0..7), 3: 24..31
+        const uint32_t wa = q[(part & 1) * 2], wb = q[(part & 1) * 2 + 1];
+        const uint32_t na = (part >> 1) ? (wa >> 4) & 0x0F0F0F0Fu : wa & 0x0F0F0F0Fu;
+        const uint32_t nb = (part >> 1) ? (wb >> 4) & 0x0F0F0F0Fu : wb & 0x0F0F0F0Fu;
+        uint4 out;
+        nib4(na, out.x, out.y);
+        nib4(nb, out.z, out.w);
+        const int chunk = hb * 4 + part;
+        *reinterpret_cast<uint4 *>(rowbase + ((chunk ^ (r & 7)) << 4)) = out;
     }
 }
 
@@ -293,16 +296,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint64_t *bars = (uint64_t *)(smem + BAR_OFF);
-    const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * STAGES, tfull0 = empty0 + 8 * STAGES,
-                   tempty0 = tfull0 + 8 * NTBUF;
+    const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * STAGES, sfull0 = empty0 + 8 * STAGES,
+                   sempty0 = sfull0 + 8 * SR, tfull0 = sempty0 + 8 * SR, tempty0 = tfull0 + 8 * NTBUF;
     volatile uint32_t *tmem_slot = (volatile uint32_t *)(smem + MISC_OFF);
     volatile int *abort_flag = (volatile int *)(smem + MISC_OFF + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full0 + 8 * s, 1 + 4);       // TMA expect-tx arrive + 4 converter warps
-            mbar_init(empty0 + 8 * s, 1 + N_EPI);  // MMA commit + the epilogue warps
+            mbar_init(full0 + 8 * s, 1 + N_CONV);  // TMA expect-tx arrive + the converter warps
+            mbar_init(empty0 + 8 * s, 1);          // the MMA's commit
+        }
+        for (int s = 0; s < SR; ++s) {
+            mbar_init(sfull0 + 8 * s, N_CONV);
+            mbar_init(sempty0 + 8 * s, N_EPI);
         }
         for (int j = 0; j < NTBUF; ++j) {
             mbar_init(tfull0 + 8 * j, 1);
@@ -328,10 +335,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int nbk = p.K / kBlock;
     const size_t scale_off = blob_scales_offset(p.rows, nbk);
     auto slot_ptr = [&](int slot) { return smem + slot * SLOT_STRIDE; };
+    auto sc_ptr = [&](int s) { return smem + SC_OFF + s * SC_BYTES; };
 
     if (warp >= W_TMA && warp < W_EPI) {
-        // warpgroup 1: one setmaxnreg for all four warps, then the TMA and
-        // MMA roles (warps 6 and 7 only join the final barrier)
+        // warpgroup 2: one setmaxnreg for all four warps, then the TMA and
+        // MMA roles (warps 10 and 11 only join the final barrier)
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProdRegs));
         if (warp == W_TMA && lane == 0) {
             int it = 0;
@@ -385,36 +393,37 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         mma_done:;
         }
     } else if (warp < W_TMA) {
-        // Converters: thread r owns row r of the A tile.  Raw Q4 codes, the
-        // row's two block scales and the tile columns' activation scales of
-        // stage s are fetched with cp.async PD stages ahead into raw ring
-        // entry s % RR; stage s is then converted into its slot.
+        // Converters (8 warps): thread c owns quantization block c / 128 of
+        // stage row r = c % 128 of the A tile.  Raw Q4 codes, the row's two
+        // block scales and the tile columns' activation scales of stage s are
+        // fetched with cp.async PD stages ahead into raw ring entry s % RR;
+        // stage s is then converted into operand slot s % STAGES and its
+        // scales copied into scale slot s % SR.
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProdRegs));
-        const int r = threadIdx.x - W_CONV * 32;
+        const int c = threadIdx.x - W_CONV * 32;
+        const int r = c & (BM - 1), hb = c >> 7;
         uint8_t *raw = smem + RAW_OFF;
         StageCur fc;  // fetch cursor; conversion only counts stages
         cur_init<DUAL>(fc, p, total, r);
         const int n_stages = blockIdx.x < total ? ((total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1) * nkt : 0;
-        auto fetch = [&](const StageCur &c, int rs) {
+        auto fetch = [&](const StageCur &cu, int rs) {
             uint8_t *ent = raw + rs * RAW_BYTES;
-            if (c.valid) {
-                const int row = tile_row<DUAL>(c.rt, r);
+            if (cu.valid) {
+                const int row = tile_row<DUAL>(cu.rt, r);
                 const bool vrow = row < p.rows;
                 const int srow = vrow ? row : 0;
-                const uint8_t *src = c.blob + ((size_t)srow * nbk + 2 * c.kt) * 16;
-                const uint32_t dst = smem_u32(ent + r * 32);
-                cp_async(dst, src, 16, vrow);
-                cp_async(dst + 16, src + 16, 16, vrow);
-                const uint8_t *ssrc = c.blob + scale_off + ((size_t)srow * nbk + 2 * c.kt) * 2;
-                cp_async(smem_u32(ent + RAW_CODES + r * 4), ssrc, 4, vrow);
-#pragma unroll
-                for (int i = r; i < 2 * BN; i += BM) {
-                    const int q = i / BN, col = i - q * BN;
-                    const int pos = c.pos0 + col;
-                    const bool v = pos < p.A_pad;
-                    const float *asrc = p.a_scaleT + (size_t)(2 * c.kt + q) * p.A_pad + (v ? pos : 0);
-                    cp_async(smem_u32(ent + RAW_CODES + WS_BYTES + i * 4), asrc, 4, v);
+                const uint8_t *src = cu.blob + ((size_t)srow * nbk + 2 * cu.kt + hb) * 16;
+                cp_async(smem_u32(ent + r * 32 + hb * 16), src, 16, vrow);
+                if (hb == 0) {
+                    const uint8_t *ssrc = cu.blob + scale_off + ((size_t)srow * nbk + 2 * cu.kt) * 2;
+                    cp_async(smem_u32(ent + RAW_CODES + r * 4), ssrc, 4, vrow);
                 }
+                // activation scale c of the stage: block c / BN, column c % BN
+                const int q = c / BN, col = c - q * BN;
+                const int pos = cu.pos0 + col;
+                const bool v = pos < p.A_pad;
+                const float *asrc = p.a_scaleT + (size_t)(2 * cu.kt + q) * p.A_pad + (v ? pos : 0);
+                cp_async(smem_u32(ent + RAW_CODES + WS_BYTES + c * 4), asrc, 4, v);
             }
             cp_commit();
         };
@@ -428,31 +437,32 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             cur_next<DUAL>(fc, p, total, nkt, r);
             cp_wait<PD>();
             const uint8_t *ent = raw + (it % RR) * RAW_BYTES;
-            const int slot = it % STAGES;
-            const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+            const int slot = it % STAGES, ss = it % SR;
             bool ok = true;
-            if (lane == 0) ok = mbar_wait(empty0 + 8 * slot, ph ^ 1u, abort_flag, p.error, 16);
+            if (lane == 0)
+                ok = mbar_wait(empty0 + 8 * slot, ((uint32_t)(it / STAGES) & 1u) ^ 1u, abort_flag, p.error, 16) &&
+                     mbar_wait(sempty0 + 8 * ss, ((uint32_t)(it / SR) & 1u) ^ 1u, abort_flag, p.error, 16);
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
             if (!ok) break;
-            uint8_t *st = slot_ptr(slot);
-            const uint4 *cs = (const uint4 *)(ent + r * 32);
-            convert_store_row(st, r, cs[0], cs[1]);
-            *(uint32_t *)(st + A_BYTES + B_BYTES + r * 4) = *(const uint32_t *)(ent + RAW_CODES + r * 4);
-#pragma unroll
-            for (int i = r; i < 2 * BN; i += BM)
-                *(float *)(st + A_BYTES + B_BYTES + WS_BYTES + i * 4) =
-                    *(const float *)(ent + RAW_CODES + WS_BYTES + i * 4);
+            convert_store_block(slot_ptr(slot), r, hb, *(const uint4 *)(ent + r * 32 + hb * 16));
+            uint8_t *sc = sc_ptr(ss);
+            if (hb == 0) *(uint32_t *)(sc + r * 4) = *(const uint32_t *)(ent + RAW_CODES + r * 4);
+            *(float *)(sc + WS_BYTES + c * 4) = *(const float *)(ent + RAW_CODES + WS_BYTES + c * 4);
             fence_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(full0 + 8 * slot);
+            if (lane == 0) {
+                mbar_arrive(full0 + 8 * slot);
+                mbar_arrive(sfull0 + 8 * ss);
+            }
             ++it;
         }
         cp_wait<0>();
     } else {
         // Epilogue: TMEM lane quarter = warp % 4 (thread = tile row), column
-        // group = 32 token columns.  Per K block: one 32-column TMEM load,
-        // s = d_w * d_a (mul.f32x2) and acc += sum * s (fma.f32x2), the
-        // activation scales of four columns per 128-bit broadcast load.
+        // group = 32 token columns.  Per K block: one 32-column TMEM load
+        // (the buffer is handed back to the MMA as soon as the load is
+        // complete), s = d_w * d_a (mul.f32x2) and acc += sum * s (fma.f32x2),
+        // the activation scales of four columns per 128-bit broadcast load.
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kEpiRegs));
         const int e = warp - W_EPI;
         const int quarter = warp & 3;
@@ -468,33 +478,35 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const int pos_end = p.uniq_off[u + 1];
             float2 acc[16];
 #pragma unroll
-            for (int c = 0; c < 16; ++c) acc[c] = make_float2(0.0f, 0.0f);
-            for (int kt = 0; kt < nkt; ++kt, ++it, qc += 2) {
-                const int slot = it % STAGES;
-                const uint8_t *st = slot_ptr(slot);
-                const int j0 = qc % NTBUF, j1 = (qc + 1) % NTBUF;
+            for (int cc = 0; cc < 16; ++cc) acc[cc] = make_float2(0.0f, 0.0f);
+            for (int kt = 0; kt < nkt; ++kt, ++it) {
+                const int ss = it % SR;
+                const uint8_t *sc = sc_ptr(ss);
                 bool ok = true;
-                // the slot's scales were written before its full barrier
-                // completed; the second block's commit covers both blocks
-                if (lane == 0) {
-                    ok = mbar_wait(full0 + 8 * slot, (uint32_t)(it / STAGES) & 1u, abort_flag, p.error, 64) &&
-                         mbar_wait(tfull0 + 8 * j1, (uint32_t)((qc + 1) / NTBUF) & 1u, abort_flag, p.error, 32);
-                }
+                if (lane == 0) ok = mbar_wait(sfull0 + 8 * ss, (uint32_t)(it / SR) & 1u, abort_flag, p.error, 64);
                 ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                 if (!ok) goto epi_done;
-                tc_fence_after();
-                if (active) {
-                    const uint32_t wsc = *(const uint32_t *)(st + A_BYTES + B_BYTES + r * 4);
-                    const float4 *cs4 = (const float4 *)(st + A_BYTES + B_BYTES + WS_BYTES) + grp * 8;
+                const uint32_t wsc = *(const uint32_t *)(sc + r * 4);
+                const float4 *cs4 = (const float4 *)(sc + WS_BYTES) + grp * 8;
 #pragma unroll
-                    for (int blk = 0; blk < 2; ++blk) {
-                        const int j = blk ? j1 : j0;
-                        uint32_t sv[32];
+                for (int blk = 0; blk < 2; ++blk, ++qc) {
+                    const int j = qc % NTBUF;
+                    if (lane == 0) ok = mbar_wait(tfull0 + 8 * j, (uint32_t)(qc / NTBUF) & 1u, abort_flag, p.error, 32);
+                    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                    if (!ok) goto epi_done;
+                    tc_fence_after();
+                    uint32_t sv[32];
+                    if (active) {
                         tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(j * BN + grp * 32), sv);
+                        tmem_ld_wait();
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(tempty0 + 8 * j);
+                    if (active) {
                         const float dw =
                             __half2float(__ushort_as_half((unsigned short)(blk ? (wsc >> 16) : (wsc & 0xffffu))));
                         const float2 dw2 = make_float2(dw, dw);
-                        tmem_ld_wait();
 #pragma unroll
                         for (int c4 = 0; c4 < 8; ++c4) {
                             const float4 d4 = cs4[blk * (BN / 4) + c4];  // broadcast read
@@ -509,13 +521,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         }
                     }
                 }
-                tc_fence_before();
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(tempty0 + 8 * j0);
-                    mbar_arrive(tempty0 + 8 * j1);
-                    mbar_arrive(empty0 + 8 * slot);
-                }
+                if (lane == 0) mbar_arrive(sempty0 + 8 * ss);
             }
             // tile outputs; the assignment id of column i of this warp's group
             // is held by lane i
@@ -532,11 +539,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const float *from_partner = xch + ((size_t)(pair * 2 + (is_gate ? 1 : 0)) * 16) * 32;
                 if (active) {
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
+                    for (int cc = 0; cc < 8; ++cc) {
                         // the gate warp sends columns 16..31, the up warp 0..15
-                        const float2 v = is_gate ? acc[8 + c] : acc[c];
-                        to_partner[(2 * c) * 32 + lane] = v.x;
-                        to_partner[(2 * c + 1) * 32 + lane] = v.y;
+                        const float2 v = is_gate ? acc[8 + cc] : acc[cc];
+                        to_partner[(2 * cc) * 32 + lane] = v.x;
+                        to_partner[(2 * cc + 1) * 32 + lane] = v.y;
                     }
                 }
                 bar_sync_named(1 + pair, 64);
@@ -544,28 +551,28 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     // this warp's 16 columns of the group (gate warp: 0..15, up warp: 16..31)
                     float mine[16];
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const float2 v = is_gate ? acc[c] : acc[8 + c];
-                        mine[2 * c] = v.x;
-                        mine[2 * c + 1] = v.y;
+                    for (int cc = 0; cc < 8; ++cc) {
+                        const float2 v = is_gate ? acc[cc] : acc[8 + cc];
+                        mine[2 * cc] = v.x;
+                        mine[2 * cc + 1] = v.y;
                     }
                     const int c0 = is_gate ? 0 : 16;
                     const int fb = (rt * 64 + (quarter & 1) * 32) / kBlock;  // h block index along F
                     const int f = rt * 64 + (quarter & 1) * 32 + lane;       // F row of this lane
                     const int nc = min(16, ncols - grp * 32 - c0);           // valid columns (warp-uniform)
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) {
-                        if (c < nc) {
-                            const float other = from_partner[c * 32 + lane];
-                            const float g = is_gate ? mine[c] : other, uu = is_gate ? other : mine[c];
+                    for (int cc = 0; cc < 16; ++cc) {
+                        if (cc < nc) {
+                            const float other = from_partner[cc * 32 + lane];
+                            const float g = is_gate ? mine[cc] : other, uu = is_gate ? other : mine[cc];
                             const float h = g * uu / (1.0f + expf(-g));
                             const float amax =
                                 __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(h))));
                             const float dd = __half2float(__float2half_rn(amax / 127.0f));
                             int qv = 0;
                             if (dd != 0.0f) qv = (int)fminf(fmaxf(rintf(h / dd), -127.0f), 127.0f);
-                            const int s = __reduce_add_sync(0xffffffffu, qv);
-                            const int col = c0 + c;
+                            const int sum = __reduce_add_sync(0xffffffffu, qv);
+                            const int col = c0 + cc;
                             const int pos = pos0 + col;
                             const int a = __shfl_sync(0xffffffffu, my_asg, col);
                             if (pos < pos_end) {
@@ -573,7 +580,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                                 p.hq[(size_t)a * p.F_out + f] = (int8_t)qv;
                                 if (lane == 0) {
                                     p.hdT[(size_t)fb * p.A_pad + pos] = dd;
-                                    p.hds[(size_t)a * (p.F_out / kBlock) + fb] = BlockScale{dd, s};
+                                    p.hds[(size_t)a * (p.F_out / kBlock) + fb] = BlockScale{dd, sum};
                                 }
                             }
                         }
@@ -586,11 +593,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const bool vrow = row < p.rows;
                 const int nc = min(32, ncols - grp * 32);  // valid columns (warp-uniform)
 #pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    if (c < nc) {
-                        const int pos = pos0 + c;
-                        const int a = __shfl_sync(0xffffffffu, my_asg, c);
-                        const float v = (c & 1) ? acc[c >> 1].y : acc[c >> 1].x;
+                for (int cc = 0; cc < 32; ++cc) {
+                    if (cc < nc) {
+                        const int pos = pos0 + cc;
+                        const int a = __shfl_sync(0xffffffffu, my_asg, cc);
+                        const float v = (cc & 1) ? acc[cc >> 1].y : acc[cc >> 1].x;
                         if (vrow && pos < pos_end) p.o[(size_t)a * p.rows + row] = v;
                     }
                 }
