@@ -52,14 +52,20 @@ constexpr int BK = 64;    // K per pipeline stage (two quantization blocks)
 // warpgroups 0-1 = the 8 converter warps, warpgroup 2 = TMA producer, MMA
 // issuer and two warps that only join the final barrier, warpgroups 3-6 =
 // the 16 epilogue warps (4 lane quarters x 4 column groups).
-constexpr int W_CONV = 0, N_CONV = 8, W_TMA = 8, W_MMA = 9, W_EPI = 12;
+#ifndef MOE_GEMM_CONV_WARPS
+#define MOE_GEMM_CONV_WARPS 8
+#endif
+constexpr int N_CONV = MOE_GEMM_CONV_WARPS;     // 4 (a row per thread) or 8 (a block per thread)
+static_assert(N_CONV == 4 || N_CONV == 8, "converter warps");
+constexpr int W_CONV = 0, W_TMA = N_CONV, W_MMA = N_CONV + 1, W_EPI = N_CONV + 4;
 constexpr int N_EPI = 16;
-constexpr int NTHREADS = (W_EPI + N_EPI) * 32;  // 896
+constexpr int NTHREADS = (W_EPI + N_EPI) * 32;  // 896 (768 with 4 converter warps)
+constexpr int N_PROD_WG = W_EPI / 4;            // warpgroups before the epilogue
 // Register split: launched with kLaunchRegs per thread (ptxas' allocation for
-// 896 threads, checked on the host before the first launch), warpgroups 0-2
-// drop to kProdRegs and warpgroups 3-6 rise to kEpiRegs.
-constexpr int kLaunchRegs = 72, kProdRegs = 48, kEpiRegs = 88;
-static_assert(3 * 128 * kProdRegs + 4 * 128 * kEpiRegs <= NTHREADS * kLaunchRegs, "register split");
+// NTHREADS threads, checked on the host before the first launch), the
+// producer warpgroups drop to kProdRegs and the epilogue's rise to kEpiRegs.
+constexpr int kLaunchRegs = N_CONV == 8 ? 72 : 80, kProdRegs = N_CONV == 8 ? 48 : 56, kEpiRegs = 88;
+static_assert(N_PROD_WG * 128 * kProdRegs + 4 * 128 * kEpiRegs <= NTHREADS * kLaunchRegs, "register split");
 constexpr long long kTimeoutCycles = 4000000000ll;
 
 // Operand ring (A and B tiles of a stage; freed by the MMA's commit alone)
@@ -82,9 +88,12 @@ constexpr int RAW_BYTES = RAW_CODES + SC_BYTES;
 constexpr int RAW_OFF = SC_OFF + SR * SC_BYTES;
 constexpr int XCH_OFF = RAW_OFF + RR * RAW_BYTES;  // SwiGLU exchange: [8 pairs][2][16 cols][32 lanes] fp32
 constexpr int XCH_BYTES = 8 * 2 * 16 * 32 * 4;
-constexpr int NTBUF = 4;                         // K-block accumulators in TMEM (BN columns each)
+// TMEM: a ring of 16 units of 32 columns; one K block of a tile takes 1, 2
+// or 4 consecutive units (its valid token columns rounded up), aligned to its
+// width, so narrow tiles keep up to 16 K blocks in flight.
+constexpr int NUNIT = 16;
 constexpr int BAR_OFF = XCH_OFF + XCH_BYTES;
-constexpr int NBARS = 2 * STAGES + 2 * SR + 2 * NTBUF;
+constexpr int NBARS = 2 * STAGES + 2 * SR + 2 * NUNIT;
 constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
 constexpr int SMEM = MISC_OFF + 16 + 1024;       // + alignment slack
 static_assert(SMEM <= 227 * 1024, "shared memory of the GEMM CTA");
@@ -286,6 +295,19 @@ __device__ __forceinline__ void cur_next(StageCur &c, const GemmParams &p, int t
     }
 }
 
+// TMEM units of one K block of a tile with ncols valid columns.
+__device__ __forceinline__ int block_units(int ncols) { return ncols <= 32 ? 1 : ncols <= 64 ? 2 : 4; }
+
+// Place the next K block of w units on the ring: the first unit at or after
+// pos that is a multiple of w, wrapping to unit 0 at the end of the ring.
+// Every role computes the same placements from the same tile sequence.
+__device__ __forceinline__ int ring_place(int &pos, int w) {
+    int start = (pos + w - 1) & ~(w - 1);
+    if (start + w > NUNIT) start = 0;
+    pos = start + w;
+    return start;
+}
+
 __device__ __forceinline__ void bar_sync_named(int id, int n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
@@ -297,7 +319,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint64_t *bars = (uint64_t *)(smem + BAR_OFF);
     const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * STAGES, sfull0 = empty0 + 8 * STAGES,
-                   sempty0 = sfull0 + 8 * SR, tfull0 = sempty0 + 8 * SR, tempty0 = tfull0 + 8 * NTBUF;
+                   sempty0 = sfull0 + 8 * SR, tfull0 = sempty0 + 8 * SR, tempty0 = tfull0 + 8 * NUNIT;
     volatile uint32_t *tmem_slot = (volatile uint32_t *)(smem + MISC_OFF);
     volatile int *abort_flag = (volatile int *)(smem + MISC_OFF + 4);
 
@@ -311,9 +333,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             mbar_init(sfull0 + 8 * s, N_CONV);
             mbar_init(sempty0 + 8 * s, N_EPI);
         }
-        for (int j = 0; j < NTBUF; ++j) {
+        for (int j = 0; j < NUNIT; ++j) {
             mbar_init(tfull0 + 8 * j, 1);
-            mbar_init(tempty0 + 8 * j, N_EPI);
+            mbar_init(tempty0 + 8 * j, 4);  // the four lane-quarter warps of the column group reading it
         }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -338,8 +360,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     auto sc_ptr = [&](int s) { return smem + SC_OFF + s * SC_BYTES; };
 
     if (warp >= W_TMA && warp < W_EPI) {
-        // warpgroup 2: one setmaxnreg for all four warps, then the TMA and
-        // MMA roles (warps 10 and 11 only join the final barrier)
+        // the TMA/MMA warpgroup: one setmaxnreg for all four warps, then the
+        // TMA and MMA roles (its last two warps only join the final barrier)
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProdRegs));
         if (warp == W_TMA && lane == 0) {
             int it = 0;
@@ -358,7 +380,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tma_done:;
         }
         if (warp == W_MMA && lane == 0) {
-            int it = 0, qc = 0;
+            int it = 0, pos = 0;
+            uint32_t ph = 0;  // per TMEM unit: parity of its next use
             // the tile's MMA width: its valid token columns rounded up to 16
             // (the record of the next tile is requested a tile ahead)
             uint2 rec_next = blockIdx.x < total ? __ldg(p.tile_rec + blockIdx.x) : make_uint2(0, 0);
@@ -366,6 +389,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const int ncols = (int)(rec_next.y >> 16);
                 if (t + (int)gridDim.x < total) rec_next = __ldg(p.tile_rec + t + gridDim.x);
                 const int nmma = min(BN, (ncols + 15) & ~15);
+                const int w = block_units(ncols);
                 const uint32_t idesc = idesc_f16(BM, nmma < 16 ? 16 : nmma);
                 for (int kt = 0; kt < nkt; ++kt, ++it) {
                     const int slot = it % STAGES;
@@ -375,17 +399,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     uint8_t *st = slot_ptr(slot);
                     const uint64_t da = sdesc(smem_u32(st));
                     const uint64_t db = sdesc(smem_u32(st + A_BYTES));
-                    for (int blk = 0; blk < 2; ++blk, ++qc) {
-                        const int j = qc % NTBUF;
-                        if (!mbar_wait(tempty0 + 8 * j, ((uint32_t)(qc / NTBUF) & 1u) ^ 1u, abort_flag, p.error, 8))
-                            goto mma_done;
+                    for (int blk = 0; blk < 2; ++blk) {
+                        const int u0 = ring_place(pos, w);
+                        // the units' previous readers are done with them
+                        for (int g = 0; g < w; ++g)
+                            if (!mbar_wait(tempty0 + 8 * (u0 + g), ((ph >> (u0 + g)) & 1u) ^ 1u, abort_flag, p.error, 8))
+                                goto mma_done;
                         tc_fence_after();
 #pragma unroll
                         for (int kk = 0; kk < 2; ++kk) {
                             const uint64_t koff = (uint64_t)((blk * 32 + kk * 16) * 2) >> 4;
-                            mma_f16(tmem + (uint32_t)(j * BN), da + koff, db + koff, idesc, kk > 0 ? 1u : 0u);
+                            mma_f16(tmem + (uint32_t)(u0 * 32), da + koff, db + koff, idesc, kk > 0 ? 1u : 0u);
                         }
-                        mma_commit(tfull0 + 8 * j);
+                        for (int g = 0; g < w; ++g) mma_commit(tfull0 + 8 * (u0 + g));
+                        ph ^= ((1u << w) - 1u) << u0;
                     }
                     mma_commit(empty0 + 8 * slot);
                 }
@@ -393,15 +420,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         mma_done:;
         }
     } else if (warp < W_TMA) {
-        // Converters (8 warps): thread c owns quantization block c / 128 of
-        // stage row r = c % 128 of the A tile.  Raw Q4 codes, the row's two
+        // Converters: with 8 warps thread c owns quantization block c / 128
+        // of stage row r = c % 128 of the A tile, with 4 warps both blocks.  Raw Q4 codes, the row's two
         // block scales and the tile columns' activation scales of stage s are
         // fetched with cp.async PD stages ahead into raw ring entry s % RR;
         // stage s is then converted into operand slot s % STAGES and its
         // scales copied into scale slot s % SR.
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProdRegs));
+        constexpr int NCT = N_CONV * 32;  // converter threads
         const int c = threadIdx.x - W_CONV * 32;
-        const int r = c & (BM - 1), hb = c >> 7;
+        const int r = c & (BM - 1), hb0 = c >> 7;  // with 4 warps: both blocks (hb0 = 0)
         uint8_t *raw = smem + RAW_OFF;
         StageCur fc;  // fetch cursor; conversion only counts stages
         cur_init<DUAL>(fc, p, total, r);
@@ -412,18 +440,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const int row = tile_row<DUAL>(cu.rt, r);
                 const bool vrow = row < p.rows;
                 const int srow = vrow ? row : 0;
-                const uint8_t *src = cu.blob + ((size_t)srow * nbk + 2 * cu.kt + hb) * 16;
-                cp_async(smem_u32(ent + r * 32 + hb * 16), src, 16, vrow);
-                if (hb == 0) {
+#pragma unroll
+                for (int hb = hb0; hb < 2; hb += NCT / BM) {
+                    const uint8_t *src = cu.blob + ((size_t)srow * nbk + 2 * cu.kt + hb) * 16;
+                    cp_async(smem_u32(ent + r * 32 + hb * 16), src, 16, vrow);
+                }
+                if (hb0 == 0) {
                     const uint8_t *ssrc = cu.blob + scale_off + ((size_t)srow * nbk + 2 * cu.kt) * 2;
                     cp_async(smem_u32(ent + RAW_CODES + r * 4), ssrc, 4, vrow);
                 }
-                // activation scale c of the stage: block c / BN, column c % BN
-                const int q = c / BN, col = c - q * BN;
-                const int pos = cu.pos0 + col;
-                const bool v = pos < p.A_pad;
-                const float *asrc = p.a_scaleT + (size_t)(2 * cu.kt + q) * p.A_pad + (v ? pos : 0);
-                cp_async(smem_u32(ent + RAW_CODES + WS_BYTES + c * 4), asrc, 4, v);
+                // activation scales i of the stage: block i / BN, column i % BN
+#pragma unroll
+                for (int i = c; i < 2 * BN; i += NCT) {
+                    const int q = i / BN, col = i - q * BN;
+                    const int pos = cu.pos0 + col;
+                    const bool v = pos < p.A_pad;
+                    const float *asrc = p.a_scaleT + (size_t)(2 * cu.kt + q) * p.A_pad + (v ? pos : 0);
+                    cp_async(smem_u32(ent + RAW_CODES + WS_BYTES + i * 4), asrc, 4, v);
+                }
             }
             cp_commit();
         };
@@ -444,10 +478,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                      mbar_wait(sempty0 + 8 * ss, ((uint32_t)(it / SR) & 1u) ^ 1u, abort_flag, p.error, 16);
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
             if (!ok) break;
-            convert_store_block(slot_ptr(slot), r, hb, *(const uint4 *)(ent + r * 32 + hb * 16));
+#pragma unroll
+            for (int hb = hb0; hb < 2; hb += NCT / BM)
+                convert_store_block(slot_ptr(slot), r, hb, *(const uint4 *)(ent + r * 32 + hb * 16));
             uint8_t *sc = sc_ptr(ss);
-            if (hb == 0) *(uint32_t *)(sc + r * 4) = *(const uint32_t *)(ent + RAW_CODES + r * 4);
-            *(float *)(sc + WS_BYTES + c * 4) = *(const float *)(ent + RAW_CODES + WS_BYTES + c * 4);
+            if (hb0 == 0) *(uint32_t *)(sc + r * 4) = *(const uint32_t *)(ent + RAW_CODES + r * 4);
+#pragma unroll
+            for (int i = c; i < 2 * BN; i += NCT)
+                *(float *)(sc + WS_BYTES + i * 4) = *(const float *)(ent + RAW_CODES + WS_BYTES + i * 4);
             fence_async_smem();
             __syncwarp();
             if (lane == 0) {
@@ -469,11 +507,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int grp = e >> 2;  // column group: columns [32 grp, 32 grp + 32)
         const int r = quarter * 32 + lane;
         float *xch = (float *)(smem + XCH_OFF);
-        int qc = 0, it = 0;
+        int it = 0, pos = 0;
+        uint32_t ph = 0;  // per TMEM unit: parity of its next use
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
             int u, rt, tt, ncols;
             decode_tile(p.tile_rec, t, u, rt, tt, ncols);
-            const bool active = grp * 32 < ncols;  // warp-uniform
+            const int w = block_units(ncols);
+            const bool reader = grp < w;           // this warp's group reads a unit of each K block
+            const bool active = grp * 32 < ncols;  // ... and has valid columns (warp-uniform)
             const int pos0 = p.uniq_off[u] + tt * BN + grp * 32;
             const int pos_end = p.uniq_off[u + 1];
             float2 acc[16];
@@ -489,20 +530,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const uint32_t wsc = *(const uint32_t *)(sc + r * 4);
                 const float4 *cs4 = (const float4 *)(sc + WS_BYTES) + grp * 8;
 #pragma unroll
-                for (int blk = 0; blk < 2; ++blk, ++qc) {
-                    const int j = qc % NTBUF;
-                    if (lane == 0) ok = mbar_wait(tfull0 + 8 * j, (uint32_t)(qc / NTBUF) & 1u, abort_flag, p.error, 32);
-                    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-                    if (!ok) goto epi_done;
-                    tc_fence_after();
+                for (int blk = 0; blk < 2; ++blk) {
+                    const int u0 = ring_place(pos, w);
+                    const int un = u0 + grp;  // this warp's unit (when grp < w)
                     uint32_t sv[32];
-                    if (active) {
-                        tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(j * BN + grp * 32), sv);
-                        tmem_ld_wait();
+                    if (reader) {
+                        if (lane == 0) ok = mbar_wait(tfull0 + 8 * un, (ph >> un) & 1u, abort_flag, p.error, 32);
+                        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                        if (!ok) goto epi_done;
+                        tc_fence_after();
+                        if (active) {
+                            tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(un * 32), sv);
+                            tmem_ld_wait();
+                        }
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(tempty0 + 8 * un);
                     }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(tempty0 + 8 * j);
+                    ph ^= ((1u << w) - 1u) << u0;
                     if (active) {
                         const float dw =
                             __half2float(__ushort_as_half((unsigned short)(blk ? (wsc >> 16) : (wsc & 0xffffu))));
