@@ -190,6 +190,15 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                  : "memory");
 }
 
+// 16 consecutive TMEM columns of this warp's 32 lanes (raw fp32 bits)
+__device__ __forceinline__ void tmem_ld16u(uint32_t taddr, uint32_t *r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // 32 consecutive TMEM columns of this warp's 32 lanes (one fp32 per column)
@@ -529,42 +538,45 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (!ok) goto epi_done;
                 const uint32_t wsc = *(const uint32_t *)(sc + r * 4);
                 const float4 *cs4 = (const float4 *)(sc + WS_BYTES) + grp * 8;
-#pragma unroll
+#pragma unroll 1
                 for (int blk = 0; blk < 2; ++blk) {
                     const int u0 = ring_place(pos, w);
                     const int un = u0 + grp;  // this warp's unit (when grp < w)
-                    uint32_t sv[32];
                     if (reader) {
                         if (lane == 0) ok = mbar_wait(tfull0 + 8 * un, (ph >> un) & 1u, abort_flag, p.error, 32);
                         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                         if (!ok) goto epi_done;
                         tc_fence_after();
                         if (active) {
-                            tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(un * 32), sv);
-                            tmem_ld_wait();
+                            const float dw = __half2float(
+                                __ushort_as_half((unsigned short)(blk ? (wsc >> 16) : (wsc & 0xffffu))));
+                            const float2 dw2 = make_float2(dw, dw);
+                            const float4 *c4p = cs4 + blk * (BN / 4);
+                            // the unit's 32 columns in two 16-column loads
+#pragma unroll
+                            for (int half = 0; half < 2; ++half) {
+                                uint32_t sv[16];
+                                tmem_ld16u(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(un * 32 + half * 16),
+                                           sv);
+                                tmem_ld_wait();
+#pragma unroll
+                                for (int c4 = 0; c4 < 4; ++c4) {
+                                    const float4 d4 = c4p[half * 4 + c4];  // broadcast read
+                                    const float2 s01 = __fmul2_rn(dw2, make_float2(d4.x, d4.y));
+                                    const float2 s23 = __fmul2_rn(dw2, make_float2(d4.z, d4.w));
+                                    float2 &a0 = acc[half * 8 + 2 * c4], &a1 = acc[half * 8 + 2 * c4 + 1];
+                                    a0 = __ffma2_rn(make_float2(__uint_as_float(sv[4 * c4]),
+                                                                __uint_as_float(sv[4 * c4 + 1])), s01, a0);
+                                    a1 = __ffma2_rn(make_float2(__uint_as_float(sv[4 * c4 + 2]),
+                                                                __uint_as_float(sv[4 * c4 + 3])), s23, a1);
+                                }
+                            }
                         }
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(tempty0 + 8 * un);
                     }
                     ph ^= ((1u << w) - 1u) << u0;
-                    if (active) {
-                        const float dw =
-                            __half2float(__ushort_as_half((unsigned short)(blk ? (wsc >> 16) : (wsc & 0xffffu))));
-                        const float2 dw2 = make_float2(dw, dw);
-#pragma unroll
-                        for (int c4 = 0; c4 < 8; ++c4) {
-                            const float4 d4 = cs4[blk * (BN / 4) + c4];  // broadcast read
-                            const float2 s01 = __fmul2_rn(dw2, make_float2(d4.x, d4.y));
-                            const float2 s23 = __fmul2_rn(dw2, make_float2(d4.z, d4.w));
-                            acc[2 * c4] = __ffma2_rn(make_float2(__uint_as_float(sv[4 * c4]),
-                                                                 __uint_as_float(sv[4 * c4 + 1])),
-                                                     s01, acc[2 * c4]);
-                            acc[2 * c4 + 1] = __ffma2_rn(make_float2(__uint_as_float(sv[4 * c4 + 2]),
-                                                                     __uint_as_float(sv[4 * c4 + 3])),
-                                                         s23, acc[2 * c4 + 1]);
-                        }
-                    }
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(sempty0 + 8 * ss);
