@@ -247,15 +247,23 @@ __device__ __forceinline__ void convert_store_block(uint8_t *tile, int r, int hb
     }
 }
 
-// tile index -> (used expert u, row tile, token tile, valid token columns),
-// from the per-tile records the tiling kernel writes (token tile innermost).
+// TMEM units of one K block of a tile with ncols valid columns.
+__host__ __device__ __forceinline__ int block_units(int ncols) { return ncols <= 32 ? 1 : ncols <= 64 ? 2 : 4; }
+
+// Work item ("batch") index -> (used expert u, first row tile, token tile,
+// valid token columns, row tiles in the batch), from the records the tiling
+// kernel writes.  A batch holds 4 / block_units(ncols) consecutive row tiles
+// of one expert's token tile (fewer at the end of the rows): narrow token
+// tiles are processed several row tiles at a time, their K stages
+// interleaved, so that every epilogue column group has a tile to finish.
 __device__ __forceinline__ void decode_tile(const uint2 *rec, int t, int &u, int &row_tile, int &tok_tile,
-                                            int &ncols) {
+                                            int &ncols, int &nrt) {
     const uint2 r = __ldg(rec + t);
     u = (int)(r.x & 0xffffu);
     row_tile = (int)(r.x >> 16);
     tok_tile = (int)(r.y & 0xffffu);
-    ncols = (int)(r.y >> 16);
+    ncols = (int)((r.y >> 16) & 0xffu);
+    nrt = (int)(r.y >> 24);
 }
 
 // A-tile row r of row tile rt: gate/up tiles hold gate rows 64 rt .. 64 rt + 63
@@ -270,7 +278,7 @@ __device__ __forceinline__ int tile_row(int rt, int r) {
 // sequence of its CTA.  The expert-table entry of the thread's tensor and the
 // tile's first sorted position are looked up once per tile.
 struct StageCur {
-    int t, kt, rt, pos0;
+    int t, kt, j, rt0, nrt, pos0;
     const uint8_t *blob;
     bool valid;
 };
@@ -278,7 +286,7 @@ struct StageCur {
 template <bool DUAL>
 __device__ __forceinline__ void cur_tile(StageCur &c, const GemmParams &p, int r) {
     int u, tt, nc;
-    decode_tile(p.tile_rec, c.t, u, c.rt, tt, nc);
+    decode_tile(p.tile_rec, c.t, u, c.rt0, tt, nc, c.nrt);
     const int e = p.uniq_e[u];
     const uint64_t *tb = (DUAL && r >= 64) ? p.tbl[1] : p.tbl[0];
     c.blob = (const uint8_t *)(uintptr_t)(tb[e] & ~1ull);
@@ -289,13 +297,17 @@ template <bool DUAL>
 __device__ __forceinline__ void cur_init(StageCur &c, const GemmParams &p, int total, int r) {
     c.t = blockIdx.x;
     c.kt = 0;
+    c.j = 0;
     c.valid = c.t < total;
     if (c.valid) cur_tile<DUAL>(c, p, r);
 }
 
+// stage order within a batch: K stage outer, row tile of the batch inner
 template <bool DUAL>
 __device__ __forceinline__ void cur_next(StageCur &c, const GemmParams &p, int total, int nkt, int r) {
     if (!c.valid) return;
+    if (++c.j < c.nrt) return;
+    c.j = 0;
     if (++c.kt == nkt) {
         c.kt = 0;
         c.t += gridDim.x;
@@ -303,9 +315,6 @@ __device__ __forceinline__ void cur_next(StageCur &c, const GemmParams &p, int t
         if (c.valid) cur_tile<DUAL>(c, p, r);
     }
 }
-
-// TMEM units of one K block of a tile with ncols valid columns.
-__device__ __forceinline__ int block_units(int ncols) { return ncols <= 32 ? 1 : ncols <= 64 ? 2 : 4; }
 
 // Place the next K block of w units on the ring: the first unit at or after
 // pos that is a multiple of w, wrapping to unit 0 at the end of the ring.
@@ -375,16 +384,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (warp == W_TMA && lane == 0) {
             int it = 0;
             for (int t = blockIdx.x; t < total; t += gridDim.x) {
-                int u, rt, tt, nc;
-                decode_tile(p.tile_rec, t, u, rt, tt, nc);
+                int u, rt, tt, nc, nrt;
+                decode_tile(p.tile_rec, t, u, rt, tt, nc, nrt);
                 const int pos0 = p.uniq_off[u] + tt * BN;
-                for (int kt = 0; kt < nkt; ++kt, ++it) {
-                    const int slot = it % STAGES;
-                    const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
-                    if (!mbar_wait(empty0 + 8 * slot, ph ^ 1u, abort_flag, p.error, 2)) goto tma_done;
-                    mbar_arrive_tx(full0 + 8 * slot, B_BYTES);
-                    tma_load_2d(smem_u32(slot_ptr(slot) + A_BYTES), &tmB, kt * BK, pos0, full0 + 8 * slot);
-                }
+                for (int kt = 0; kt < nkt; ++kt)
+                    for (int j = 0; j < nrt; ++j, ++it) {
+                        const int slot = it % STAGES;
+                        const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+                        if (!mbar_wait(empty0 + 8 * slot, ph ^ 1u, abort_flag, p.error, 2)) goto tma_done;
+                        mbar_arrive_tx(full0 + 8 * slot, B_BYTES);
+                        tma_load_2d(smem_u32(slot_ptr(slot) + A_BYTES), &tmB, kt * BK, pos0, full0 + 8 * slot);
+                    }
             }
         tma_done:;
         }
@@ -395,12 +405,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             // (the record of the next tile is requested a tile ahead)
             uint2 rec_next = blockIdx.x < total ? __ldg(p.tile_rec + blockIdx.x) : make_uint2(0, 0);
             for (int t = blockIdx.x; t < total; t += gridDim.x) {
-                const int ncols = (int)(rec_next.y >> 16);
+                const int ncols = (int)((rec_next.y >> 16) & 0xffu), nrt = (int)(rec_next.y >> 24);
                 if (t + (int)gridDim.x < total) rec_next = __ldg(p.tile_rec + t + gridDim.x);
                 const int nmma = min(BN, (ncols + 15) & ~15);
                 const int w = block_units(ncols);
                 const uint32_t idesc = idesc_f16(BM, nmma < 16 ? 16 : nmma);
-                for (int kt = 0; kt < nkt; ++kt, ++it) {
+                for (int ks = 0; ks < nkt * nrt; ++ks, ++it) {
                     const int slot = it % STAGES;
                     if (!mbar_wait(full0 + 8 * slot, (uint32_t)(it / STAGES) & 1u, abort_flag, p.error, 4))
                         goto mma_done;
@@ -442,11 +452,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         uint8_t *raw = smem + RAW_OFF;
         StageCur fc;  // fetch cursor; conversion only counts stages
         cur_init<DUAL>(fc, p, total, r);
-        const int n_stages = blockIdx.x < total ? ((total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1) * nkt : 0;
+        int n_stages = 0;
+        for (int t = blockIdx.x; t < total; t += gridDim.x) {
+            int u, rt, tt, nc, nrt;
+            decode_tile(p.tile_rec, t, u, rt, tt, nc, nrt);
+            n_stages += nkt * nrt;
+        }
         auto fetch = [&](const StageCur &cu, int rs) {
             uint8_t *ent = raw + rs * RAW_BYTES;
             if (cu.valid) {
-                const int row = tile_row<DUAL>(cu.rt, r);
+                const int row = tile_row<DUAL>(cu.rt0 + cu.j, r);
                 const bool vrow = row < p.rows;
                 const int srow = vrow ? row : 0;
 #pragma unroll
@@ -513,36 +528,39 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kEpiRegs));
         const int e = warp - W_EPI;
         const int quarter = warp & 3;
-        const int grp = e >> 2;  // column group: columns [32 grp, 32 grp + 32)
+        const int grp = e >> 2;  // column group: tile grp / w of the batch, its columns [32 cu, 32 cu + 32)
         const int r = quarter * 32 + lane;
         float *xch = (float *)(smem + XCH_OFF);
         int it = 0, pos = 0;
         uint32_t ph = 0;  // per TMEM unit: parity of its next use
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
-            int u, rt, tt, ncols;
-            decode_tile(p.tile_rec, t, u, rt, tt, ncols);
+            int u, rt0, tt, ncols, nrt;
+            decode_tile(p.tile_rec, t, u, rt0, tt, ncols, nrt);
             const int w = block_units(ncols);
-            const bool reader = grp < w;           // this warp's group reads a unit of each K block
-            const bool active = grp * 32 < ncols;  // ... and has valid columns (warp-uniform)
-            const int pos0 = p.uniq_off[u] + tt * BN + grp * 32;
+            const int tj = grp / w, cu = grp - tj * w;  // this group's tile in the batch and column unit
+            const int rt = rt0 + tj;
+            const bool reader = tj < nrt;                   // reads unit cu of each K block of tile tj
+            const bool active = reader && cu * 32 < ncols;  // ... and has valid columns (warp-uniform)
+            const int pos0 = p.uniq_off[u] + tt * BN + cu * 32;
             const int pos_end = p.uniq_off[u + 1];
             float2 acc[16];
 #pragma unroll
             for (int cc = 0; cc < 16; ++cc) acc[cc] = make_float2(0.0f, 0.0f);
-            for (int kt = 0; kt < nkt; ++kt, ++it) {
+            for (int ks = 0; ks < nkt * nrt; ++ks, ++it) {
                 const int ss = it % SR;
+                const bool mine = reader && ks % nrt == tj;  // this stage belongs to this group's tile
                 const uint8_t *sc = sc_ptr(ss);
                 bool ok = true;
                 if (lane == 0) ok = mbar_wait(sfull0 + 8 * ss, (uint32_t)(it / SR) & 1u, abort_flag, p.error, 64);
                 ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                 if (!ok) goto epi_done;
                 const uint32_t wsc = *(const uint32_t *)(sc + r * 4);
-                const float4 *cs4 = (const float4 *)(sc + WS_BYTES) + grp * 8;
+                const float4 *cs4 = (const float4 *)(sc + WS_BYTES) + cu * 8;
 #pragma unroll 1
                 for (int blk = 0; blk < 2; ++blk) {
                     const int u0 = ring_place(pos, w);
-                    const int un = u0 + grp;  // this warp's unit (when grp < w)
-                    if (reader) {
+                    const int un = u0 + cu;  // this warp's unit (for its own tile's stages)
+                    if (mine) {
                         if (lane == 0) ok = mbar_wait(tfull0 + 8 * un, (ph >> un) & 1u, abort_flag, p.error, 32);
                         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                         if (!ok) goto epi_done;
@@ -616,7 +634,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     const int c0 = is_gate ? 0 : 16;
                     const int fb = (rt * 64 + (quarter & 1) * 32) / kBlock;  // h block index along F
                     const int f = rt * 64 + (quarter & 1) * 32 + lane;       // F row of this lane
-                    const int nc = min(16, ncols - grp * 32 - c0);           // valid columns (warp-uniform)
+                    const int nc = min(16, ncols - cu * 32 - c0);            // valid columns (warp-uniform)
 #pragma unroll
                     for (int cc = 0; cc < 16; ++cc) {
                         if (cc < nc) {
@@ -648,7 +666,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             } else if (active) {
                 const int row = rt * BM + r;
                 const bool vrow = row < p.rows;
-                const int nc = min(32, ncols - grp * 32);  // valid columns (warp-uniform)
+                const int nc = min(32, ncols - cu * 32);  // valid columns (warp-uniform)
 #pragma unroll
                 for (int cc = 0; cc < 32; ++cc) {
                     if (cc < nc) {
@@ -681,6 +699,30 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 }  // namespace gemm
 
 // ---------------------------------------------------------------- prefill helpers
+// Work items of one expert with n tokens: per token tile of bn columns, its
+// rt row tiles in batches of 4 / block_units(valid columns).
+__device__ __forceinline__ int gemm_batches(int n, int rt, int bn) {
+    int cnt = 0;
+    for (int tt = 0; tt * bn < n; ++tt) {
+        const int per = 4 / gemm::block_units(min(bn, n - tt * bn));
+        cnt += (rt + per - 1) / per;
+    }
+    return cnt;
+}
+
+__device__ __forceinline__ void gemm_batch_records(int u, int n, int rt, int bn, uint2 *out, int cap) {
+    int i = 0;
+    for (int tt = 0; tt * bn < n; ++tt) {
+        const int nc = min(bn, n - tt * bn);
+        const int per = 4 / gemm::block_units(nc);
+        for (int r0 = 0; r0 < rt; r0 += per, ++i) {
+            if (i < cap)
+                out[i] = make_uint2((unsigned)u | ((unsigned)r0 << 16),
+                                    (unsigned)tt | ((unsigned)nc << 16) | ((unsigned)min(per, rt - r0) << 24));
+        }
+    }
+}
+
 // Per used expert: cumulative tile counts of the gate/up and down GEMMs, and
 // the miss / stamp record of the layer's three tensors.
 __global__ void tiling_kernel(TilingParams p) {
@@ -700,8 +742,8 @@ __global__ void tiling_kernel(TilingParams p) {
         int tg = 0, td = 0;
         if (u < n_uniq) {
             const int n = p.uniq_off[u + 1] - p.uniq_off[u];
-            tg = p.rt_gu * ((n + p.bn_gu - 1) / p.bn_gu);
-            td = p.rt_dn * ((n + p.bn_dn - 1) / p.bn_dn);
+            tg = gemm_batches(n, p.rt_gu, p.bn_gu);
+            td = gemm_batches(n, p.rt_dn, p.bn_dn);
         }
         // inclusive warp scans then block offsets, for both counts
         int ig = tg, id = td;
@@ -742,23 +784,12 @@ __global__ void tiling_kernel(TilingParams p) {
         __syncthreads();
     }
     __syncthreads();
-    // per-tile records: (u | row tile << 16, token tile | valid columns << 16)
+    // batch records: (u | first row tile << 16, token tile | valid columns
+    // << 16 | row tiles << 24), token tile outer, row tiles inner
     for (int u = threadIdx.x; u < n_uniq; u += blockDim.x) {
         const int n = p.uniq_off[u + 1] - p.uniq_off[u];
-        const int ng = (n + p.bn_gu - 1) / p.bn_gu, nd = (n + p.bn_dn - 1) / p.bn_dn;
-        const int bg = p.tile_off_gu[u], bd = p.tile_off_dn[u];
-        for (int i = 0; i < p.rt_gu * ng; ++i) {
-            const int rt = i / ng, tt = i - rt * ng;
-            if (bg + i < p.cap_gu)
-                p.rec_gu[bg + i] = make_uint2((unsigned)u | ((unsigned)rt << 16),
-                                              (unsigned)tt | ((unsigned)min(p.bn_gu, n - tt * p.bn_gu) << 16));
-        }
-        for (int i = 0; i < p.rt_dn * nd; ++i) {
-            const int rt = i / nd, tt = i - rt * nd;
-            if (bd + i < p.cap_dn)
-                p.rec_dn[bd + i] = make_uint2((unsigned)u | ((unsigned)rt << 16),
-                                              (unsigned)tt | ((unsigned)min(p.bn_dn, n - tt * p.bn_dn) << 16));
-        }
+        gemm_batch_records(u, n, p.rt_gu, p.bn_gu, p.rec_gu + p.tile_off_gu[u], p.cap_gu - p.tile_off_gu[u]);
+        gemm_batch_records(u, n, p.rt_dn, p.bn_dn, p.rec_dn + p.tile_off_dn[u], p.cap_dn - p.tile_off_dn[u]);
     }
     if (threadIdx.x == 0) {
         p.tile_off_gu[n_uniq] = run_gu;
