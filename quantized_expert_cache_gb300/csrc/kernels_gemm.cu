@@ -52,46 +52,46 @@ constexpr int BK = 64;    // K per pipeline stage (two quantization blocks)
 // warpgroups 0-1 = the 8 converter warps, warpgroup 2 = TMA producer, MMA
 // issuer and two warps that only join the final barrier, warpgroups 3-6 =
 // the 16 epilogue warps (4 lane quarters x 4 column groups).
-#ifndef MOE_GEMM_CONV_WARPS
-#define MOE_GEMM_CONV_WARPS 8
-#endif
-constexpr int N_CONV = MOE_GEMM_CONV_WARPS;     // 4 (a row per thread) or 8 (a block per thread)
-static_assert(N_CONV == 4 || N_CONV == 8, "converter warps");
-constexpr int W_CONV = 0, W_TMA = N_CONV, W_MMA = N_CONV + 1, W_EPI = N_CONV + 4;
+// Warp roles by warpgroup (setmaxnreg moves registers between warpgroups):
+// warpgroup 0 = the 4 converter warps (warp k writes TMEM lane quarter k),
+// warpgroup 1 = TMA producer, MMA issuer and two warps that only join the
+// final barrier, warpgroups 2-5 = the 16 epilogue warps (4 lane quarters x 4
+// column groups).
+constexpr int N_CONV = 4, W_CONV = 0, W_TMA = 4, W_MMA = 5, W_EPI = 8;
 constexpr int N_EPI = 16;
-constexpr int NTHREADS = (W_EPI + N_EPI) * 32;  // 896 (768 with 4 converter warps)
-constexpr int N_PROD_WG = W_EPI / 4;            // warpgroups before the epilogue
+constexpr int NTHREADS = (W_EPI + N_EPI) * 32;  // 768
 // Register split: launched with kLaunchRegs per thread (ptxas' allocation for
-// NTHREADS threads, checked on the host before the first launch), the
-// producer warpgroups drop to kProdRegs and the epilogue's rise to kEpiRegs.
-constexpr int kLaunchRegs = N_CONV == 8 ? 72 : 80, kProdRegs = N_CONV == 8 ? 48 : 56, kEpiRegs = 88;
-static_assert(N_PROD_WG * 128 * kProdRegs + 4 * 128 * kEpiRegs <= NTHREADS * kLaunchRegs, "register split");
+// 768 threads, checked on the host before the first launch), warpgroups 0-1
+// drop to kProdRegs and warpgroups 2-5 rise to kEpiRegs.
+constexpr int kLaunchRegs = 80, kProdRegs = 56, kEpiRegs = 88;
+static_assert(2 * 128 * kProdRegs + 4 * 128 * kEpiRegs <= NTHREADS * kLaunchRegs, "register split");
 constexpr long long kTimeoutCycles = 4000000000ll;
 
-// Operand ring (A and B tiles of a stage; freed by the MMA's commit alone)
-// and scale ring (the stage's weight and activation scales, freed by the
-// epilogue), so that neither the converters nor the TMA wait for the
-// epilogue's arithmetic.
+// Operand slots: the weight tile (A, fp16) in TMEM columns written by the
+// converters with tcgen05.st, the token tile (B) in shared memory by TMA;
+// a slot is freed by the MMA's commit alone.  Scale ring: the stage's weight
+// and activation scales, fetched by cp.async straight into their slot and
+// freed by the epilogue.
 constexpr int STAGES = 4;                        // operand slots
-constexpr int SR = 8;                            // scale slots
-constexpr int RR = 6;                            // raw prefetch ring of the converters (cp.async)
+constexpr int SR = 16;                           // scale slots
+constexpr int RR = 6;                            // raw code ring of the converters (cp.async)
 constexpr int PD = RR - 1;                       // prefetch distance in stages
-constexpr int A_BYTES = BM * BK * 2;             // fp16 weight tile, 128-B swizzle
 constexpr int B_BYTES = BN * BK * 2;             // fp16 token tile (TMA), 128-B swizzle
-constexpr int SLOT_STRIDE = A_BYTES + B_BYTES;   // 32 KB, 1024-aligned
 constexpr int WS_BYTES = BM * 2 * 2;             // weight scales [row][2 blocks] binary16
 constexpr int CS_BYTES = 2 * BN * 4;             // activation scales [2 blocks][column] fp32
 constexpr int SC_BYTES = WS_BYTES + CS_BYTES;
-constexpr int SC_OFF = STAGES * SLOT_STRIDE;
-constexpr int RAW_CODES = BM * 32;               // raw ring entry: Q4 codes [row][32 B], then scales
-constexpr int RAW_BYTES = RAW_CODES + SC_BYTES;
+constexpr int SC_OFF = STAGES * B_BYTES;
+constexpr int RAW_BYTES = BM * 32;               // raw ring entry: Q4 codes [row][32 B]
 constexpr int RAW_OFF = SC_OFF + SR * SC_BYTES;
 constexpr int XCH_OFF = RAW_OFF + RR * RAW_BYTES;  // SwiGLU exchange: [8 pairs][2][16 cols][32 lanes] fp32
 constexpr int XCH_BYTES = 8 * 2 * 16 * 32 * 4;
-// TMEM: a ring of 16 units of 32 columns; one K block of a tile takes 1, 2
-// or 4 consecutive units (its valid token columns rounded up), aligned to its
-// width, so narrow tiles keep up to 16 K blocks in flight.
-constexpr int NUNIT = 16;
+// TMEM: columns [0, 384) are a ring of 12 units of 32 columns for the K-block
+// accumulators -- one K block of a tile takes 1, 2 or 4 consecutive units
+// (its valid token columns rounded up), aligned to its width, so narrow tiles
+// keep up to 12 K blocks in flight; columns [384, 512) hold the A operand of
+// the 4 operand slots (32 columns = 64 fp16 of K per lane each).
+constexpr int NUNIT = 12;
+constexpr uint32_t A_TMEM_COL = NUNIT * 32;
 constexpr int BAR_OFF = XCH_OFF + XCH_BYTES;
 constexpr int NBARS = 2 * STAGES + 2 * SR + 2 * NUNIT;
 constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
@@ -185,6 +185,28 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b,
         : "memory");
 }
 
+// D (TMEM) [+]= A (TMEM, 128 lanes x 16 fp16 of K) x B (shared memory descriptor)
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\ntcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(
+            d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+// 32 consecutive TMEM columns of this warp's 32 lanes <- 32 registers
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t *r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]),
+        "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]),
+        "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
@@ -227,11 +249,9 @@ __device__ __forceinline__ void nib4(uint32_t n, uint32_t &p01, uint32_t &p23) {
 }
 
 // Q4 codes of one row and one quantization block (16 B) -> 32 fp16 values
-// (q - 8) in K order: chunks 4 hb .. 4 hb + 3 of the row in the 128-B
-// swizzled layout (chunk c of row r of an 8-row group sits at chunk c ^ r).
-__device__ __forceinline__ void convert_store_block(uint8_t *tile, int r, int hb, uint4 c) {
+// (q - 8) in K order as 16 words (word m = elements 2m, 2m + 1).
+__device__ __forceinline__ void convert_block(uint4 c, uint32_t *o) {
     const uint32_t q[4] = {c.x, c.y, c.z, c.w};
-    uint8_t *rowbase = tile + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
     for (int part = 0; part < 4; ++part) {
         // part 0: elements 0..7 (low nibbles of bytes 0..7), 1: 8..15
@@ -239,11 +259,8 @@ __device__ __forceinline__ void convert_store_block(uint8_t *tile, int r, int hb
         const uint32_t wa = q[(part & 1) * 2], wb = q[(part & 1) * 2 + 1];
         const uint32_t na = (part >> 1) ? (wa >> 4) & 0x0F0F0F0Fu : wa & 0x0F0F0F0Fu;
         const uint32_t nb = (part >> 1) ? (wb >> 4) & 0x0F0F0F0Fu : wb & 0x0F0F0F0Fu;
-        uint4 out;
-        nib4(na, out.x, out.y);
-        nib4(nb, out.z, out.w);
-        const int chunk = hb * 4 + part;
-        *reinterpret_cast<uint4 *>(rowbase + ((chunk ^ (r & 7)) << 4)) = out;
+        nib4(na, o[4 * part], o[4 * part + 1]);
+        nib4(nb, o[4 * part + 2], o[4 * part + 3]);
     }
 }
 
@@ -374,7 +391,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int nkt = p.K / BK;
     const int nbk = p.K / kBlock;
     const size_t scale_off = blob_scales_offset(p.rows, nbk);
-    auto slot_ptr = [&](int slot) { return smem + slot * SLOT_STRIDE; };
+    auto slot_ptr = [&](int slot) { return smem + slot * B_BYTES; };  // the slot's B tile
     auto sc_ptr = [&](int s) { return smem + SC_OFF + s * SC_BYTES; };
 
     if (warp >= W_TMA && warp < W_EPI) {
@@ -393,7 +410,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
                         if (!mbar_wait(empty0 + 8 * slot, ph ^ 1u, abort_flag, p.error, 2)) goto tma_done;
                         mbar_arrive_tx(full0 + 8 * slot, B_BYTES);
-                        tma_load_2d(smem_u32(slot_ptr(slot) + A_BYTES), &tmB, kt * BK, pos0, full0 + 8 * slot);
+                        tma_load_2d(smem_u32(slot_ptr(slot)), &tmB, kt * BK, pos0, full0 + 8 * slot);
                     }
             }
         tma_done:;
@@ -415,9 +432,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     if (!mbar_wait(full0 + 8 * slot, (uint32_t)(it / STAGES) & 1u, abort_flag, p.error, 4))
                         goto mma_done;
                     tc_fence_after();
-                    uint8_t *st = slot_ptr(slot);
-                    const uint64_t da = sdesc(smem_u32(st));
-                    const uint64_t db = sdesc(smem_u32(st + A_BYTES));
+                    const uint32_t ta = tmem + A_TMEM_COL + 32u * (uint32_t)slot;
+                    const uint64_t db = sdesc(smem_u32(slot_ptr(slot)));
                     for (int blk = 0; blk < 2; ++blk) {
                         const int u0 = ring_place(pos, w);
                         // the units' previous readers are done with them
@@ -428,7 +444,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                         for (int kk = 0; kk < 2; ++kk) {
                             const uint64_t koff = (uint64_t)((blk * 32 + kk * 16) * 2) >> 4;
-                            mma_f16(tmem + (uint32_t)(u0 * 32), da + koff, db + koff, idesc, kk > 0 ? 1u : 0u);
+                            mma_f16_ts(tmem + (uint32_t)(u0 * 32), ta + (uint32_t)(blk * 16 + kk * 8), db + koff, idesc,
+                                       kk > 0 ? 1u : 0u);
                         }
                         for (int g = 0; g < w; ++g) mma_commit(tfull0 + 8 * (u0 + g));
                         ph ^= ((1u << w) - 1u) << u0;
@@ -439,16 +456,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         mma_done:;
         }
     } else if (warp < W_TMA) {
-        // Converters: with 8 warps thread c owns quantization block c / 128
-        // of stage row r = c % 128 of the A tile, with 4 warps both blocks.  Raw Q4 codes, the row's two
-        // block scales and the tile columns' activation scales of stage s are
-        // fetched with cp.async PD stages ahead into raw ring entry s % RR;
-        // stage s is then converted into operand slot s % STAGES and its
-        // scales copied into scale slot s % SR.
+        // Converters: thread r owns row r of the A tile (TMEM lane r).  The
+        // raw Q4 codes of stage s are fetched with cp.async PD stages ahead
+        // into raw ring entry s % RR, the stage's weight and activation scales
+        // straight into scale slot s % SR (once the epilogue has freed it);
+        // stage s is then expanded to fp16 and stored into the slot's TMEM
+        // columns with one tcgen05.st per thread.
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProdRegs));
-        constexpr int NCT = N_CONV * 32;  // converter threads
-        const int c = threadIdx.x - W_CONV * 32;
-        const int r = c & (BM - 1), hb0 = c >> 7;  // with 4 warps: both blocks (hb0 = 0)
+        const int r = threadIdx.x - W_CONV * 32;
         uint8_t *raw = smem + RAW_OFF;
         StageCur fc;  // fetch cursor; conversion only counts stages
         cur_init<DUAL>(fc, p, total, r);
@@ -458,63 +473,61 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             decode_tile(p.tile_rec, t, u, rt, tt, nc, nrt);
             n_stages += nkt * nrt;
         }
-        auto fetch = [&](const StageCur &cu, int rs) {
-            uint8_t *ent = raw + rs * RAW_BYTES;
+        bool ok = true;
+        auto fetch = [&](const StageCur &cu, int q) {  // stage q
             if (cu.valid) {
+                uint8_t *ent = raw + (q % RR) * RAW_BYTES;
+                uint8_t *sc = sc_ptr(q % SR);
+                if (lane == 0)
+                    ok = ok && mbar_wait(sempty0 + 8 * (q % SR), ((uint32_t)(q / SR) & 1u) ^ 1u, abort_flag, p.error, 16);
+                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                 const int row = tile_row<DUAL>(cu.rt0 + cu.j, r);
-                const bool vrow = row < p.rows;
-                const int srow = vrow ? row : 0;
-#pragma unroll
-                for (int hb = hb0; hb < 2; hb += NCT / BM) {
-                    const uint8_t *src = cu.blob + ((size_t)srow * nbk + 2 * cu.kt + hb) * 16;
-                    cp_async(smem_u32(ent + r * 32 + hb * 16), src, 16, vrow);
-                }
-                if (hb0 == 0) {
-                    const uint8_t *ssrc = cu.blob + scale_off + ((size_t)srow * nbk + 2 * cu.kt) * 2;
-                    cp_async(smem_u32(ent + RAW_CODES + r * 4), ssrc, 4, vrow);
-                }
+                const bool vrow = ok && row < p.rows;
+                const int srow = row < p.rows ? row : 0;
+                const uint8_t *src = cu.blob + ((size_t)srow * nbk + 2 * cu.kt) * 16;
+                cp_async(smem_u32(ent + r * 32), src, 16, vrow);
+                cp_async(smem_u32(ent + r * 32 + 16), src + 16, 16, vrow);
+                const uint8_t *ssrc = cu.blob + scale_off + ((size_t)srow * nbk + 2 * cu.kt) * 2;
+                cp_async(smem_u32(sc + r * 4), ssrc, 4, vrow);
                 // activation scales i of the stage: block i / BN, column i % BN
 #pragma unroll
-                for (int i = c; i < 2 * BN; i += NCT) {
-                    const int q = i / BN, col = i - q * BN;
+                for (int i = r; i < 2 * BN; i += BM) {
+                    const int qb = i / BN, col = i - qb * BN;
                     const int pos = cu.pos0 + col;
-                    const bool v = pos < p.A_pad;
-                    const float *asrc = p.a_scaleT + (size_t)(2 * cu.kt + q) * p.A_pad + (v ? pos : 0);
-                    cp_async(smem_u32(ent + RAW_CODES + WS_BYTES + i * 4), asrc, 4, v);
+                    const bool v = ok && pos < p.A_pad;
+                    const float *asrc = p.a_scaleT + (size_t)(2 * cu.kt + qb) * p.A_pad + (pos < p.A_pad ? pos : 0);
+                    cp_async(smem_u32(sc + WS_BYTES + i * 4), asrc, 4, v);
                 }
             }
             cp_commit();
         };
         for (int i = 0; i < PD; ++i) {
-            fetch(fc, i % RR);
+            fetch(fc, i);
             cur_next<DUAL>(fc, p, total, nkt, r);
         }
+        const uint32_t ta_lane = tmem + ((uint32_t)(warp * 32) << 16) + A_TMEM_COL;  // this warp's lane quarter
         int it = 0;
-        while (it < n_stages) {
-            fetch(fc, (it + PD) % RR);
+        while (it < n_stages && ok) {
+            fetch(fc, it + PD);
             cur_next<DUAL>(fc, p, total, nkt, r);
             cp_wait<PD>();
-            const uint8_t *ent = raw + (it % RR) * RAW_BYTES;
-            const int slot = it % STAGES, ss = it % SR;
-            bool ok = true;
+            const int slot = it % STAGES;
             if (lane == 0)
-                ok = mbar_wait(empty0 + 8 * slot, ((uint32_t)(it / STAGES) & 1u) ^ 1u, abort_flag, p.error, 16) &&
-                     mbar_wait(sempty0 + 8 * ss, ((uint32_t)(it / SR) & 1u) ^ 1u, abort_flag, p.error, 16);
+                ok = mbar_wait(empty0 + 8 * slot, ((uint32_t)(it / STAGES) & 1u) ^ 1u, abort_flag, p.error, 16);
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
             if (!ok) break;
-#pragma unroll
-            for (int hb = hb0; hb < 2; hb += NCT / BM)
-                convert_store_block(slot_ptr(slot), r, hb, *(const uint4 *)(ent + r * 32 + hb * 16));
-            uint8_t *sc = sc_ptr(ss);
-            if (hb0 == 0) *(uint32_t *)(sc + r * 4) = *(const uint32_t *)(ent + RAW_CODES + r * 4);
-#pragma unroll
-            for (int i = c; i < 2 * BN; i += NCT)
-                *(float *)(sc + WS_BYTES + i * 4) = *(const float *)(ent + RAW_CODES + WS_BYTES + i * 4);
-            fence_async_smem();
+            tc_fence_after();
+            const uint8_t *ent = raw + (it % RR) * RAW_BYTES;
+            uint32_t a[32];
+            convert_block(*(const uint4 *)(ent + r * 32), a);
+            convert_block(*(const uint4 *)(ent + r * 32 + 16), a + 16);
+            tmem_st32(ta_lane + 32u * (uint32_t)slot, a);
+            tmem_st_wait();
+            tc_fence_before();
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(full0 + 8 * slot);
-                mbar_arrive(sfull0 + 8 * ss);
+                mbar_arrive(sfull0 + 8 * (it % SR));
             }
             ++it;
         }
