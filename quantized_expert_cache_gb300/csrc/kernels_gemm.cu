@@ -85,11 +85,13 @@ constexpr int RAW_BYTES = BM * 32;               // raw ring entry: Q4 codes [ro
 constexpr int RAW_OFF = SC_OFF + SR * SC_BYTES;
 constexpr int XCH_OFF = RAW_OFF + RR * RAW_BYTES;  // SwiGLU exchange: [8 pairs][2][16 cols][32 lanes] fp32
 constexpr int XCH_BYTES = 8 * 2 * 16 * 32 * 4;
-// TMEM: columns [0, 384) are a ring of 12 units of 32 columns for the K-block
-// accumulators -- one K block of a tile takes 1, 2 or 4 consecutive units
-// (its valid token columns rounded up), aligned to its width, so narrow tiles
-// keep up to 12 K blocks in flight; columns [384, 512) hold the A operand of
-// the 4 operand slots (32 columns = 64 fp16 of K per lane each).
+// TMEM: columns [0, 384) hold 12 units of 32 columns for the K-block
+// accumulators.  One K block of a tile takes w = 1, 2 or 4 units (its valid
+// token columns rounded up); tile j of a batch owns 3 block slots of w units
+// starting at unit 3 w j, used in turn by its consecutive K blocks, so every
+// tile keeps up to 3 K blocks in flight and an epilogue warp reads only its
+// own tile's units.  Columns [384, 512) hold the A operand of the 4 operand
+// slots (32 columns = 64 fp16 of K per lane each).
 constexpr int NUNIT = 12;
 constexpr uint32_t A_TMEM_COL = NUNIT * 32;
 constexpr int BAR_OFF = XCH_OFF + XCH_BYTES;
@@ -103,6 +105,9 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)_
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_n(uint32_t bar, uint32_t n) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(n) : "memory");
 }
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
@@ -333,14 +338,15 @@ __device__ __forceinline__ void cur_next(StageCur &c, const GemmParams &p, int t
     }
 }
 
-// Place the next K block of w units on the ring: the first unit at or after
-// pos that is a multiple of w, wrapping to unit 0 at the end of the ring.
-// Every role computes the same placements from the same tile sequence.
-__device__ __forceinline__ int ring_place(int &pos, int w) {
-    int start = (pos + w - 1) & ~(w - 1);
-    if (start + w > NUNIT) start = 0;
-    pos = start + w;
-    return start;
+// Parities of the TMEM units' barriers after a batch of nrt tiles, each of
+// nblk K blocks of w units: block b of tile j uses block slot b % 3, i.e.
+// units 3 w j + w (b % 3) .. + w - 1; every use flips a unit's parity.
+__device__ __forceinline__ uint32_t batch_unit_flips(int nrt, int w, int nblk) {
+    uint32_t m = 0;
+    for (int sl = 0; sl < 3; ++sl)
+        if (((nblk - sl + 2) / 3) & 1)
+            for (int j = 0; j < nrt; ++j) m |= ((1u << w) - 1u) << (3 * w * j + w * sl);
+    return m;
 }
 
 __device__ __forceinline__ void bar_sync_named(int id, int n) {
@@ -416,7 +422,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tma_done:;
         }
         if (warp == W_MMA && lane == 0) {
-            int it = 0, pos = 0;
+            int it = 0;
             uint32_t ph = 0;  // per TMEM unit: parity of its next use
             // the tile's MMA width: its valid token columns rounded up to 16
             // (the record of the next tile is requested a tile ahead)
@@ -427,7 +433,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const int nmma = min(BN, (ncols + 15) & ~15);
                 const int w = block_units(ncols);
                 const uint32_t idesc = idesc_f16(BM, nmma < 16 ? 16 : nmma);
-                for (int ks = 0; ks < nkt * nrt; ++ks, ++it) {
+                uint32_t slots = 0;  // block slot (0..2) of each tile of the batch, 2 bits per tile
+                for (int ks = 0, j = 0; ks < nkt * nrt; ++ks, ++it, j = (j + 1 == nrt) ? 0 : j + 1) {
                     const int slot = it % STAGES;
                     if (!mbar_wait(full0 + 8 * slot, (uint32_t)(it / STAGES) & 1u, abort_flag, p.error, 4))
                         goto mma_done;
@@ -435,7 +442,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     const uint32_t ta = tmem + A_TMEM_COL + 32u * (uint32_t)slot;
                     const uint64_t db = sdesc(smem_u32(slot_ptr(slot)));
                     for (int blk = 0; blk < 2; ++blk) {
-                        const int u0 = ring_place(pos, w);
+                        const int sl = (int)((slots >> (2 * j)) & 3u);
+                        slots = (slots & ~(3u << (2 * j))) | ((uint32_t)(sl == 2 ? 0 : sl + 1) << (2 * j));
+                        const int u0 = 3 * w * j + w * sl;
                         // the units' previous readers are done with them
                         for (int g = 0; g < w; ++g)
                             if (!mbar_wait(tempty0 + 8 * (u0 + g), ((ph >> (u0 + g)) & 1u) ^ 1u, abort_flag, p.error, 8))
@@ -544,24 +553,33 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int grp = e >> 2;  // column group: tile grp / w of the batch, its columns [32 cu, 32 cu + 32)
         const int r = quarter * 32 + lane;
         float *xch = (float *)(smem + XCH_OFF);
-        int it = 0, pos = 0;
-        uint32_t ph = 0;  // per TMEM unit: parity of its next use
+        int it0 = 0;      // stage index of the batch's first stage
+        uint32_t ph = 0;  // per TMEM unit: parity of its next use, at the start of the batch
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
             int u, rt0, tt, ncols, nrt;
             decode_tile(p.tile_rec, t, u, rt0, tt, ncols, nrt);
             const int w = block_units(ncols);
             const int tj = grp / w, cu = grp - tj * w;  // this group's tile in the batch and column unit
+            const uint32_t ph_next = ph ^ batch_unit_flips(nrt, w, 2 * nkt);
+            const int it_first = it0;
+            it0 += nkt * nrt;
+            if (tj >= nrt) {  // no tile of this batch for this group
+                ph = ph_next;
+                continue;
+            }
             const int rt = rt0 + tj;
-            const bool reader = tj < nrt;                   // reads unit cu of each K block of tile tj
-            const bool active = reader && cu * 32 < ncols;  // ... and has valid columns (warp-uniform)
+            const bool active = cu * 32 < ncols;  // this warp has valid columns (warp-uniform)
             const int pos0 = p.uniq_off[u] + tt * BN + cu * 32;
             const int pos_end = p.uniq_off[u + 1];
+            const uint32_t sc_weight = 4u / (uint32_t)w;  // 4 w warps read a stage's scales; 16 arrivals free it
             float2 acc[16];
 #pragma unroll
             for (int cc = 0; cc < 16; ++cc) acc[cc] = make_float2(0.0f, 0.0f);
-            for (int ks = 0; ks < nkt * nrt; ++ks, ++it) {
+            uint32_t q = ph;  // parities of this tile's units, updated as they are read
+            int sl = 0;       // block slot of the next K block
+            for (int kt = 0; kt < nkt; ++kt) {
+                const int it = it_first + kt * nrt + tj;  // this tile's stage
                 const int ss = it % SR;
-                const bool mine = reader && ks % nrt == tj;  // this stage belongs to this group's tile
                 const uint8_t *sc = sc_ptr(ss);
                 bool ok = true;
                 if (lane == 0) ok = mbar_wait(sfull0 + 8 * ss, (uint32_t)(it / SR) & 1u, abort_flag, p.error, 64);
@@ -571,10 +589,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const float4 *cs4 = (const float4 *)(sc + WS_BYTES) + cu * 8;
 #pragma unroll 1
                 for (int blk = 0; blk < 2; ++blk) {
-                    const int u0 = ring_place(pos, w);
-                    const int un = u0 + cu;  // this warp's unit (for its own tile's stages)
-                    if (mine) {
-                        if (lane == 0) ok = mbar_wait(tfull0 + 8 * un, (ph >> un) & 1u, abort_flag, p.error, 32);
+                    const int un = 3 * w * tj + w * sl + cu;  // this warp's unit of the block
+                    sl = sl == 2 ? 0 : sl + 1;
+                    {
+                        if (lane == 0) ok = mbar_wait(tfull0 + 8 * un, (q >> un) & 1u, abort_flag, p.error, 32);
                         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                         if (!ok) goto epi_done;
                         tc_fence_after();
@@ -607,11 +625,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         __syncwarp();
                         if (lane == 0) mbar_arrive(tempty0 + 8 * un);
                     }
-                    ph ^= ((1u << w) - 1u) << u0;
+                    q ^= 1u << un;
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(sempty0 + 8 * ss);
+                if (lane == 0) mbar_arrive_n(sempty0 + 8 * ss, sc_weight);
             }
+            ph = ph_next;
             // tile outputs; the assignment id of column i of this warp's group
             // is held by lane i
             const int my_pos = pos0 + lane;
