@@ -95,7 +95,7 @@ constexpr int XCH_BYTES = 8 * 2 * 16 * 32 * 4;
 constexpr int NUNIT = 12;
 constexpr uint32_t A_TMEM_COL = NUNIT * 32;
 constexpr int BAR_OFF = XCH_OFF + XCH_BYTES;
-constexpr int NBARS = 2 * STAGES + 2 * SR + 2 * NUNIT;
+constexpr int NBARS = 2 * STAGES + SR + 2 * NUNIT;
 constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
 constexpr int SMEM = MISC_OFF + 16 + 1024;       // + alignment slack
 static_assert(SMEM <= 227 * 1024, "shared memory of the GEMM CTA");
@@ -106,6 +106,35 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)_
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
+__device__ __forceinline__ void st_release_cta(uint32_t addr, uint32_t v) {
+    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_cta(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// Bounded wait until the MMA issuer has issued at least n K blocks (an
+// acquire of its release-stored count): false when the CTA is aborting or
+// the wait expired.
+__device__ __forceinline__ bool wait_issued(uint32_t issued, uint32_t n, volatile int *abort_flag, int *err) {
+    if (ld_acquire_cta(issued) >= n) return true;
+    const long long t0 = clock64();
+    for (uint32_t k = 1;; ++k) {
+        __nanosleep(32);
+        if (ld_acquire_cta(issued) >= n) return true;
+        if ((k & 63) == 0) {
+            if (*abort_flag) return false;
+            if (clock64() - t0 > kTimeoutCycles) {
+                *abort_flag = 1;
+                atomicOr(err, 128);
+                return false;
+            }
+        }
+    }
+}
+
 __device__ __forceinline__ void mbar_arrive_n(uint32_t bar, uint32_t n) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(n) : "memory");
 }
@@ -359,10 +388,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint64_t *bars = (uint64_t *)(smem + BAR_OFF);
-    const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * STAGES, sfull0 = empty0 + 8 * STAGES,
-                   sempty0 = sfull0 + 8 * SR, tfull0 = sempty0 + 8 * SR, tempty0 = tfull0 + 8 * NUNIT;
+    const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * STAGES, sempty0 = empty0 + 8 * STAGES,
+                   tfull0 = sempty0 + 8 * SR, tempty0 = tfull0 + 8 * NUNIT;
     volatile uint32_t *tmem_slot = (volatile uint32_t *)(smem + MISC_OFF);
     volatile int *abort_flag = (volatile int *)(smem + MISC_OFF + 4);
+    const uint32_t issued = smem_u32(smem + MISC_OFF + 8);  // K blocks the MMA issuer has issued
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -370,15 +400,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             mbar_init(full0 + 8 * s, 1 + N_CONV);  // TMA expect-tx arrive + the converter warps
             mbar_init(empty0 + 8 * s, 1);          // the MMA's commit
         }
-        for (int s = 0; s < SR; ++s) {
-            mbar_init(sfull0 + 8 * s, N_CONV);
-            mbar_init(sempty0 + 8 * s, N_EPI);
-        }
+        for (int s = 0; s < SR; ++s) mbar_init(sempty0 + 8 * s, N_EPI);  // 16 weighted reader arrivals
         for (int j = 0; j < NUNIT; ++j) {
             mbar_init(tfull0 + 8 * j, 1);
             mbar_init(tempty0 + 8 * j, 4);  // the four lane-quarter warps of the column group reading it
         }
         *abort_flag = 0;
+        *(volatile uint32_t *)(smem + MISC_OFF + 8) = 0u;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == W_MMA) {
@@ -458,6 +486,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         }
                         for (int g = 0; g < w; ++g) mma_commit(tfull0 + 8 * (u0 + g));
                         ph ^= ((1u << w) - 1u) << u0;
+                        // K block 2 it + blk is issued: its units' previous uses are complete
+                        // (the waits above), and the stage's scales are in place (full)
+                        st_release_cta(issued, (uint32_t)(2 * it + blk + 1));
                     }
                     mma_commit(empty0 + 8 * slot);
                 }
@@ -534,10 +565,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(full0 + 8 * slot);
-                mbar_arrive(sfull0 + 8 * (it % SR));
-            }
+            if (lane == 0) mbar_arrive(full0 + 8 * slot);
             ++it;
         }
         cp_wait<0>();
@@ -582,7 +610,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const int ss = it % SR;
                 const uint8_t *sc = sc_ptr(ss);
                 bool ok = true;
-                if (lane == 0) ok = mbar_wait(sfull0 + 8 * ss, (uint32_t)(it / SR) & 1u, abort_flag, p.error, 64);
+                // the stage's first K block is issued: its scales are in place
+                // (and no TMEM unit of the stage is more than a phase ahead)
+                if (lane == 0) ok = wait_issued(issued, (uint32_t)(2 * it + 1), abort_flag, p.error);
                 ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                 if (!ok) goto epi_done;
                 const uint32_t wsc = *(const uint32_t *)(sc + r * 4);
@@ -592,7 +622,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     const int un = 3 * w * tj + w * sl + cu;  // this warp's unit of the block
                     sl = sl == 2 ? 0 : sl + 1;
                     {
-                        if (lane == 0) ok = mbar_wait(tfull0 + 8 * un, (q >> un) & 1u, abort_flag, p.error, 32);
+                        if (lane == 0)
+                            ok = wait_issued(issued, (uint32_t)(2 * it + blk + 1), abort_flag, p.error) &&
+                                 mbar_wait(tfull0 + 8 * un, (q >> un) & 1u, abort_flag, p.error, 32);
                         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                         if (!ok) goto epi_done;
                         tc_fence_after();
