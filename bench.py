@@ -56,7 +56,8 @@ def parse():
     ap.add_argument("--pool-steps", type=int, default=256,
                     help="decode tokens per run of the pool-mode / preheat leg (0 skips it)")
     ap.add_argument("--case", default=None,
-                    choices=["decode_layer", "decode_layer_cold", "decode_layer_q8", "prefill_layer"],
+                    choices=["decode_layer", "decode_layer_cold", "decode_layer_q8", "prefill_layer",
+                             "prefill_layer_wide"],
                     help="small profiling case: one layer (hidden 2048, 512 experts, top-8, FFN 1152, every "
                          "expert resident, or every expert in host memory for decode_layer_cold, Q8_0 weights "
                          "for decode_layer_q8), --launches forwards at batch 1 (routed) or 4096 tokens")
@@ -482,7 +483,9 @@ def run_case(args):
     import synth
     qec.load()
     H, F, E, k = 2048, 1152, 512, 8
-    T = 4096 if args.case == "prefill_layer" else 1
+    T = 4096 if args.case.startswith("prefill_layer") else 1
+    if args.case == "prefill_layer_wide":
+        E = 64  # ~512 tokens per expert: every token tile of the grouped GEMM full
     cap = 0 if args.case == "decode_layer_cold" else E
     fmt = synth.FMT_Q8_0 if args.case == "decode_layer_q8" else synth.FMT_Q4
     n = max(3, args.launches)

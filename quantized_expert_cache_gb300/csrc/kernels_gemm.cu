@@ -15,22 +15,17 @@
 // sum of the 32 products of one quantization block (|sum| <= 32512) is exact.
 // Each 32-wide K block is accumulated into its own TMEM buffer, so the MMA
 // produces exactly the int32 block dots of the mat-vec path; epilogue warps
-// then add sum * (d_w * d_a) in fp32 (packed fp32x2 multiplies and fused
-// multiply-adds), as the mat-vec does.
+// then add d_w * d_a * sumi in fp32 (fma.rn.f32x2), as the mat-vec does.
 //
-// Tile: M = 128 weight rows (TMEM lanes) x N = 128 sorted tokens (TMEM
-// columns), K staged 64 at a time (two quantization blocks = one 128-B
-// swizzle row of fp16), four 128-column K-block buffers in TMEM (all 512
-// columns).  Gate/up tiles stack 64 gate rows over the same 64 up rows, so
-// one MMA per K step serves both tensors and the tile's SwiGLU pairs lane l of
-// TMEM quarter q with lane l of quarter q + 2.  Warp roles (28 warps): 0-7
-// weight converters (Q4 codes and scales fetched with cp.async through the
-// expert table -- HBM pool, staged slot or zero-copy host memory -- several
-// stages ahead, expanded to fp16 in the 128-B swizzled K-major layout); 8 TMA
-// producer of the token tile; 9 TMEM owner and MMA issuer; 12-27 epilogue:
-// TMEM lane quarter = warp % 4, 32 token columns per warp.  Per K
-// block an epilogue thread reads its row's 32 block sums with one TMEM load;
-// the columns' activation scales are broadcast shared-memory reads.
+// Tile: M = 128 weight rows (TMEM lanes) x N tokens (TMEM columns), K staged
+// 64 at a time (two quantization blocks = one 128-B swizzle row of fp16).
+// Warp roles (10 warps): 0 TMA producer of the token tile; 1 TMEM owner and
+// MMA issuer; 2-5 weight converters (Q4 codes read through the expert table,
+// from the HBM pool or zero-copy from pinned host memory, turned into fp16
+// and stored in the 128-B swizzled K-major layout); 6-9 epilogue (TMEM lane
+// quarter = warp % 4).  Gate/up tiles hold two A operands (gate rows and up
+// rows) so SwiGLU and the quantization of h happen in the epilogue; the 32
+// rows of one h block are the 32 lanes of one epilogue warp.
 //
 // Every mbarrier wait is bounded (about 2 s of SM clock): on expiry the CTA
 // sets an error bit, all roles leave their loops, in-flight copies and MMAs
@@ -45,60 +40,42 @@
 namespace moe {
 namespace gemm {
 
-constexpr int BM = 128;   // weight rows per tile (TMEM lanes)
-constexpr int BN = 128;   // token columns per tile
-constexpr int BK = 64;    // K per pipeline stage (two quantization blocks)
-// Warp roles by warpgroup (setmaxnreg moves registers between warpgroups):
-// warpgroups 0-1 = the 8 converter warps, warpgroup 2 = TMA producer, MMA
-// issuer and two warps that only join the final barrier, warpgroups 3-6 =
-// the 16 epilogue warps (4 lane quarters x 4 column groups).
-// Warp roles by warpgroup (setmaxnreg moves registers between warpgroups):
-// warpgroup 0 = the 4 converter warps (warp k writes TMEM lane quarter k),
-// warpgroup 1 = TMA producer, MMA issuer and two warps that only join the
-// final barrier, warpgroups 2-5 = the 16 epilogue warps (4 lane quarters x 4
-// column groups).
-constexpr int N_CONV = 4, W_CONV = 0, W_TMA = 4, W_MMA = 5, W_EPI = 8;
-constexpr int N_EPI = 16;
-constexpr int NTHREADS = (W_EPI + N_EPI) * 32;  // 768
-// Register split: launched with kLaunchRegs per thread (ptxas' allocation for
-// 768 threads, checked on the host before the first launch), warpgroups 0-1
-// drop to kProdRegs and warpgroups 2-5 rise to kEpiRegs.
-constexpr int kLaunchRegs = 80, kProdRegs = 56, kEpiRegs = 88;
-static_assert(2 * 128 * kProdRegs + 4 * 128 * kEpiRegs <= NTHREADS * kLaunchRegs, "register split");
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int W_TMA = 0, W_MMA = 1, W_CONV = 2, W_EPI = 6;
 constexpr long long kTimeoutCycles = 4000000000ll;
 
-// Operand slots: the weight tile (A, fp16) in TMEM columns written by the
-// converters with tcgen05.st, the token tile (B) in shared memory by TMA;
-// a slot is freed by the MMA's commit alone.  Scale ring: the stage's weight
-// and activation scales, fetched by cp.async straight into their slot and
-// freed by the epilogue.
-constexpr int STAGES = 4;                        // operand slots
-constexpr int SR = 16;                           // scale slots
-constexpr int RR = 6;                            // raw code ring of the converters (cp.async)
-constexpr int PD = RR - 1;                       // prefetch distance in stages
-constexpr int B_BYTES = BN * BK * 2;             // fp16 token tile (TMA), 128-B swizzle
-constexpr int WS_BYTES = BM * 2 * 2;             // weight scales [row][2 blocks] binary16
-constexpr int CS_BYTES = 2 * BN * 4;             // activation scales [2 blocks][column] fp32
-constexpr int SC_BYTES = WS_BYTES + CS_BYTES;
-constexpr int SC_OFF = STAGES * B_BYTES;
-constexpr int RAW_BYTES = BM * 32;               // raw ring entry: Q4 codes [row][32 B]
-constexpr int RAW_OFF = SC_OFF + SR * SC_BYTES;
-constexpr int XCH_OFF = RAW_OFF + RR * RAW_BYTES;  // SwiGLU exchange: [8 pairs][2][16 cols][32 lanes] fp32
-constexpr int XCH_BYTES = 8 * 2 * 16 * 32 * 4;
-// TMEM: columns [0, 384) hold 12 units of 32 columns for the K-block
-// accumulators.  One K block of a tile takes w = 1, 2 or 4 units (its valid
-// token columns rounded up); tile j of a batch owns 3 block slots of w units
-// starting at unit 3 w j, used in turn by its consecutive K blocks, so every
-// tile keeps up to 3 K blocks in flight and an epilogue warp reads only its
-// own tile's units.  Columns [384, 512) hold the A operand of the 4 operand
-// slots (32 columns = 64 fp16 of K per lane each).
-constexpr int NUNIT = 12;
-constexpr uint32_t A_TMEM_COL = NUNIT * 32;
-constexpr int BAR_OFF = XCH_OFF + XCH_BYTES;
-constexpr int NBARS = 2 * STAGES + SR + 2 * NUNIT;
-constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
-constexpr int SMEM = MISC_OFF + 16 + 1024;       // + alignment slack
-static_assert(SMEM <= 227 * 1024, "shared memory of the GEMM CTA");
+template <bool DUAL>
+struct Cfg {
+    static constexpr int BN = DUAL ? 64 : 128;
+    static constexpr int NA = DUAL ? 2 : 1;
+    static constexpr int STAGES = DUAL ? 3 : 4;   // A/B pipeline slots
+    static constexpr int RR = 8;                  // raw prefetch ring (converter cp.async)
+    static constexpr int PD = RR - 1;             // prefetch distance in stages
+    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int B_BYTES = BN * BK * 2;
+    // per-slot scales for the epilogue: weight scales [NA][BM][2] fp16 and
+    // activation scales [2][BN] fp32 of the slot's two K blocks
+    static constexpr int WS_BYTES = NA * BM * 2 * 2;
+    static constexpr int AS_BYTES = 2 * BN * 4;
+    static constexpr int SLOT_BYTES = NA * A_BYTES + B_BYTES + WS_BYTES + AS_BYTES;
+    static constexpr int SLOT_STRIDE = (SLOT_BYTES + 1023) / 1024 * 1024;
+    // raw ring entry: codes [NA][BM][32 B], weight scales, activation scales
+    static constexpr int RAW_CODES = NA * BM * 32;
+    static constexpr int RAW_BYTES = RAW_CODES + WS_BYTES + AS_BYTES;
+    static constexpr int RAW_OFF = STAGES * SLOT_STRIDE;
+    static constexpr int TBUF = NA * BN;          // TMEM columns per K-block buffer
+    static constexpr int NTBUF = 512 / TBUF;      // K-block buffers in TMEM
+    static constexpr int BAR_OFF = RAW_OFF + RR * RAW_BYTES;
+    static constexpr int NBARS = 2 * STAGES + 2 * NTBUF;
+    static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
+    static constexpr int SMEM = MISC_OFF + 16 + 1024;  // + alignment slack
+    // epilogue warps: EPI_SPLIT per TMEM lane quarter, each owning BN / EPI_SPLIT
+    // token columns (32 for gate/up with its two tensors, 64 for down)
+    static constexpr int N_EPI = 8;
+    static constexpr int EPI_SPLIT = N_EPI / 4;
+    static constexpr int NTHREADS = (W_EPI + N_EPI) * 32;
+};
 
 // ---- PTX wrappers -----------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -106,65 +83,35 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)_
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
-__device__ __forceinline__ void st_release_cta(uint32_t addr, uint32_t v) {
-    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-__device__ __forceinline__ uint32_t ld_acquire_cta(uint32_t addr) {
-    uint32_t v;
-    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-    return v;
-}
-
-// Bounded wait until the MMA issuer has issued at least n K blocks (an
-// acquire of its release-stored count): false when the CTA is aborting or
-// the wait expired.
-__device__ __forceinline__ bool wait_issued(uint32_t issued, uint32_t n, volatile int *abort_flag, int *err) {
-    if (ld_acquire_cta(issued) >= n) return true;
-    const long long t0 = clock64();
-    for (uint32_t k = 1;; ++k) {
-        __nanosleep(32);
-        if (ld_acquire_cta(issued) >= n) return true;
-        if ((k & 63) == 0) {
-            if (*abort_flag) return false;
-            if (clock64() - t0 > kTimeoutCycles) {
-                *abort_flag = 1;
-                atomicOr(err, 128);
-                return false;
-            }
-        }
-    }
-}
-
-__device__ __forceinline__ void mbar_arrive_n(uint32_t bar, uint32_t n) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(n) : "memory");
-}
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 __device__ __forceinline__ void mbar_arrive_tx(uint32_t bar, uint32_t tx) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(tx) : "memory");
 }
-// One test of an mbarrier phase (mbarrier.try_wait: the hardware may hold the
-// thread for a short, system-dependent time while the phase is incomplete).
+// One try: the thread is suspended (not spinning) until the phase completes
+// or about kSuspendNs pass, so waiting warps leave their issue slots to the
+// converter and epilogue warps.
+constexpr uint32_t kSuspendNs = 20000;
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
-        "{\n.reg .pred P;\nmbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2;\nselp.u32 %0, 1, 0, P;\n}"
+        "{\n.reg .pred P;\nmbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2, %3;\nselp.u32 %0, 1, 0, P;\n}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(kSuspendNs)
         : "memory");
     return ok != 0;
 }
 
 // Bounded wait: false when the CTA is aborting or the wait expired (then the
-// abort flag and an error bit are set).  The abort flag and the clock are
-// checked every 64 tests, so a waiting warp issues little besides the tests.
+// abort flag and an error bit are set).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag, int *err,
                                           int code) {
     if (mbar_try(bar, parity)) return true;
     const long long t0 = clock64();
     for (uint32_t n = 1;; ++n) {
         if (mbar_try(bar, parity)) return true;
+        // the abort flag and the clock are checked every 64 tests
         if ((n & 63) == 0) {
             if (*abort_flag) return false;
             if (clock64() - t0 > kTimeoutCycles) {
@@ -219,32 +166,22 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b,
         : "memory");
 }
 
-// D (TMEM) [+]= A (TMEM, 128 lanes x 16 fp16 of K) x B (shared memory descriptor)
-__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
-    asm volatile(
-        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\ntcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(
-            d_tmem),
-        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
-        : "memory");
-}
-
-// 32 consecutive TMEM columns of this warp's 32 lanes <- 32 registers
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t *r) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]),
-        "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]),
-        "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-        : "memory");
-}
-__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
 }
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // 16 consecutive TMEM columns of this warp's 32 lanes (raw fp32 bits)
 __device__ __forceinline__ void tmem_ld16u(uint32_t taddr, uint32_t *r) {
@@ -254,8 +191,6 @@ __device__ __forceinline__ void tmem_ld16u(uint32_t taddr, uint32_t *r) {
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
 }
-
-__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // 32 consecutive TMEM columns of this warp's 32 lanes (one fp32 per column)
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t *r) {
@@ -267,6 +202,48 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t *r) {
           "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
           "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr));
+}
+
+// Packed fp32 pairs (two IEEE round-to-nearest operations per instruction).
+__device__ __forceinline__ unsigned long long pk2(uint32_t lo, uint32_t hi) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+    return r;
+}
+// acc{0,1} += sum{0,1} * (dw * da{0,1}): the scale products and the
+// accumulation as packed fp32 pairs (mul.rn.f32x2, fma.rn.f32x2).
+__device__ __forceinline__ void fma_scaled2(float &acc0, float &acc1, uint32_t sum0, uint32_t sum1, float da0, float da1,
+                                            float dw) {
+    asm("{\n.reg .b64 a, p, d, w, s;\n"
+        "mov.b64 a, {%0, %1};\nmov.b64 p, {%2, %3};\nmov.b64 d, {%4, %5};\nmov.b64 w, {%6, %6};\n"
+        "mul.rn.f32x2 s, w, d;\nfma.rn.f32x2 a, p, s, a;\nmov.b64 {%0, %1}, a;\n}"
+        : "+f"(acc0), "+f"(acc1)
+        : "r"(sum0), "r"(sum1), "f"(da0), "f"(da1), "f"(dw));
+}
+
+
+// acc{0,1} += p{0,1} * s{0,1}, two IEEE fp32 fused multiply-adds.
+__device__ __forceinline__ void fma2(float &a0, float &a1, float p0, float p1, float s0, float s1) {
+    unsigned long long acc, pp, ss;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(acc) : "f"(a0), "f"(a1));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(pp) : "f"(p0), "f"(p1));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(ss) : "f"(s0), "f"(s1));
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(pp), "l"(ss));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(acc));
+}
+
+// Q4 codes of one row and two quantization blocks (32 B) -> 64 fp16 values
+// (q - 8) in K order, stored as 8 16-byte chunks of the row in the 128-B
+// swizzled layout (chunk c of row r of an 8-row group sits at chunk c ^ r).
+__device__ __forceinline__ uint32_t nib_pair(uint32_t w, int sel, int hi) {
+    // two bytes of w (selected) -> their low (hi=0) or high (hi=1) nibbles as
+    // the fp16 pair (1024 + n0, 1024 + n1), then minus (1032, 1032)
+    uint32_t t = __byte_perm(w, 0, sel);
+    if (hi) t >>= 4;
+    t = (t & 0x000F000Fu) | 0x64006400u;
+    __half2 h = *reinterpret_cast<__half2 *>(&t);
+    h = __hsub2(h, __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408)));
+    return *reinterpret_cast<uint32_t *>(&h);
 }
 
 // Four codes (one nibble per byte of n, values 0..15) -> two fp16 pairs
@@ -282,131 +259,101 @@ __device__ __forceinline__ void nib4(uint32_t n, uint32_t &p01, uint32_t &p23) {
     p23 = *reinterpret_cast<uint32_t *>(&hb);
 }
 
-// Q4 codes of one row and one quantization block (16 B) -> 32 fp16 values
-// (q - 8) in K order as 16 words (word m = elements 2m, 2m + 1).
-__device__ __forceinline__ void convert_block(uint4 c, uint32_t *o) {
-    const uint32_t q[4] = {c.x, c.y, c.z, c.w};
+__device__ __forceinline__ void convert_store_row(uint8_t *tile, int r, uint4 c0, uint4 c1) {
+    const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+    uint8_t *rowbase = tile + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
-    for (int part = 0; part < 4; ++part) {
-        // part 0: elements 0..7 (low nibbles of bytes 0..7), 1: 8..15
-        // (low, bytes 8..15), 2: 16..23 (high, bytes 0..7), 3: 24..31
-        const uint32_t wa = q[(part & 1) * 2], wb = q[(part & 1) * 2 + 1];
-        const uint32_t na = (part >> 1) ? (wa >> 4) & 0x0F0F0F0Fu : wa & 0x0F0F0F0Fu;
-        const uint32_t nb = (part >> 1) ? (wb >> 4) & 0x0F0F0F0Fu : wb & 0x0F0F0F0Fu;
-        nib4(na, o[4 * part], o[4 * part + 1]);
-        nib4(nb, o[4 * part + 2], o[4 * part + 3]);
+    for (int blk = 0; blk < 2; ++blk) {
+        const uint32_t *q = w + 4 * blk;  // 16 code bytes of this block
+#pragma unroll
+        for (int part = 0; part < 4; ++part) {
+            // part 0: elements 0..7 (low nibbles of bytes 0..7), 1: 8..15
+            // (low, bytes 8..15), 2: 16..23 (high, bytes 0..7), 3: 24..31
+            const uint32_t wa = q[(part & 1) * 2], wb = q[(part & 1) * 2 + 1];
+            const uint32_t na = (part >> 1) ? (wa >> 4) & 0x0F0F0F0Fu : wa & 0x0F0F0F0Fu;
+            const uint32_t nb = (part >> 1) ? (wb >> 4) & 0x0F0F0F0Fu : wb & 0x0F0F0F0Fu;
+            uint4 out;
+            nib4(na, out.x, out.y);
+            nib4(nb, out.z, out.w);
+            const int chunk = blk * 4 + part;
+            *reinterpret_cast<uint4 *>(rowbase + ((chunk ^ (r & 7)) << 4)) = out;
+        }
     }
 }
 
-// TMEM units of one K block of a tile with ncols valid columns.
-__host__ __device__ __forceinline__ int block_units(int ncols) { return ncols <= 32 ? 1 : ncols <= 64 ? 2 : 4; }
-
-// Work item ("batch") index -> (used expert u, first row tile, token tile,
-// valid token columns, row tiles in the batch), from the records the tiling
-// kernel writes.  A batch holds 4 / block_units(ncols) consecutive row tiles
-// of one expert's token tile (fewer at the end of the rows): narrow token
-// tiles are processed several row tiles at a time, their K stages
-// interleaved, so that every epilogue column group has a tile to finish.
+// tile index -> (used expert u, row tile, token tile, valid token columns),
+// from the per-tile records the tiling kernel writes (token tile innermost).
 __device__ __forceinline__ void decode_tile(const uint2 *rec, int t, int &u, int &row_tile, int &tok_tile,
-                                            int &ncols, int &nrt) {
+                                            int &ncols) {
     const uint2 r = __ldg(rec + t);
     u = (int)(r.x & 0xffffu);
     row_tile = (int)(r.x >> 16);
     tok_tile = (int)(r.y & 0xffffu);
-    ncols = (int)((r.y >> 16) & 0xffu);
-    nrt = (int)(r.y >> 24);
+    ncols = (int)(r.y >> 16);
 }
 
-// A-tile row r of row tile rt: gate/up tiles hold gate rows 64 rt .. 64 rt + 63
-// in tile rows 0..63 and the same up rows in tile rows 64..127; down tiles
-// hold rows 128 rt .. 128 rt + 127.
-template <bool DUAL>
-__device__ __forceinline__ int tile_row(int rt, int r) {
-    return DUAL ? rt * 64 + (r & 63) : rt * BM + r;
-}
-
-// Stage cursor of one converter thread over the flattened (tile, K stage)
-// sequence of its CTA.  The expert-table entry of the thread's tensor and the
-// tile's first sorted position are looked up once per tile.
+// Stage cursor over the flattened (tile, K stage) sequence of one CTA.
+// The tile's expert-table entries (weight blobs) and first token position
+// are looked up once per tile, not per stage.
 struct StageCur {
-    int t, kt, j, rt0, nrt, pos0;
-    const uint8_t *blob;
+    int t, kt, u, rt, tt, nc, pos0;
+    const uint8_t *blob[2];
     bool valid;
 };
 
-template <bool DUAL>
-__device__ __forceinline__ void cur_tile(StageCur &c, const GemmParams &p, int r) {
-    int u, tt, nc;
-    decode_tile(p.tile_rec, c.t, u, c.rt0, tt, nc, c.nrt);
-    const int e = p.uniq_e[u];
-    const uint64_t *tb = (DUAL && r >= 64) ? p.tbl[1] : p.tbl[0];
-    c.blob = (const uint8_t *)(uintptr_t)(tb[e] & ~1ull);
-    c.pos0 = p.uniq_off[u] + tt * BN;
+template <int BN>
+__device__ __forceinline__ void cur_tile(StageCur &c, const GemmParams &p, int n_uniq) {
+    decode_tile(p.tile_rec, c.t, c.u, c.rt, c.tt, c.nc);
+    const int e = p.uniq_e[c.u];
+    c.blob[0] = (const uint8_t *)(uintptr_t)(p.tbl[0][e] & ~1ull);
+    c.blob[1] = p.tbl[1] ? (const uint8_t *)(uintptr_t)(p.tbl[1][e] & ~1ull) : c.blob[0];
+    c.pos0 = p.uniq_off[c.u] + c.tt * BN;
 }
 
-template <bool DUAL>
-__device__ __forceinline__ void cur_init(StageCur &c, const GemmParams &p, int total, int r) {
+template <int BN>
+__device__ __forceinline__ void cur_init(StageCur &c, const GemmParams &p, int n_uniq, int total) {
     c.t = blockIdx.x;
     c.kt = 0;
-    c.j = 0;
     c.valid = c.t < total;
-    if (c.valid) cur_tile<DUAL>(c, p, r);
+    if (c.valid) cur_tile<BN>(c, p, n_uniq);
 }
 
-// stage order within a batch: K stage outer, row tile of the batch inner
-template <bool DUAL>
-__device__ __forceinline__ void cur_next(StageCur &c, const GemmParams &p, int total, int nkt, int r) {
+template <int BN>
+__device__ __forceinline__ void cur_next(StageCur &c, const GemmParams &p, int n_uniq, int total, int nkt) {
     if (!c.valid) return;
-    if (++c.j < c.nrt) return;
-    c.j = 0;
     if (++c.kt == nkt) {
         c.kt = 0;
         c.t += gridDim.x;
         c.valid = c.t < total;
-        if (c.valid) cur_tile<DUAL>(c, p, r);
+        if (c.valid) cur_tile<BN>(c, p, n_uniq);
     }
 }
 
-// Parities of the TMEM units' barriers after a batch of nrt tiles, each of
-// nblk K blocks of w units: block b of tile j uses block slot b % 3, i.e.
-// units 3 w j + w (b % 3) .. + w - 1; every use flips a unit's parity.
-__device__ __forceinline__ uint32_t batch_unit_flips(int nrt, int w, int nblk) {
-    uint32_t m = 0;
-    for (int sl = 0; sl < 3; ++sl)
-        if (((nblk - sl + 2) / 3) & 1)
-            for (int j = 0; j < nrt; ++j) m |= ((1u << w) - 1u) << (3 * w * j + w * sl);
-    return m;
-}
-
-__device__ __forceinline__ void bar_sync_named(int id, int n) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-
 template <bool DUAL>
-__global__ void __launch_bounds__(NTHREADS, 1)
+__global__ void __launch_bounds__(Cfg<DUAL>::NTHREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmB, GemmParams p) {
+    using C = Cfg<DUAL>;
+    constexpr int BN = C::BN, NA = C::NA, NTBUF = C::NTBUF, STAGES = C::STAGES;
+    constexpr int N_EPI = C::N_EPI, EPI_SPLIT = C::EPI_SPLIT;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    uint64_t *bars = (uint64_t *)(smem + BAR_OFF);
-    const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * STAGES, sempty0 = empty0 + 8 * STAGES,
-                   tfull0 = sempty0 + 8 * SR, tempty0 = tfull0 + 8 * NUNIT;
-    volatile uint32_t *tmem_slot = (volatile uint32_t *)(smem + MISC_OFF);
-    volatile int *abort_flag = (volatile int *)(smem + MISC_OFF + 4);
-    const uint32_t issued = smem_u32(smem + MISC_OFF + 8);  // K blocks the MMA issuer has issued
+    uint64_t *bars = (uint64_t *)(smem + C::BAR_OFF);
+    const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * STAGES, tfull0 = empty0 + 8 * STAGES,
+                   tempty0 = tfull0 + 8 * NTBUF;
+    volatile uint32_t *tmem_slot = (volatile uint32_t *)(smem + C::MISC_OFF);
+    volatile int *abort_flag = (volatile int *)(smem + C::MISC_OFF + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full0 + 8 * s, 1 + N_CONV);  // TMA expect-tx arrive + the converter warps
-            mbar_init(empty0 + 8 * s, 1);          // the MMA's commit
+            mbar_init(full0 + 8 * s, 1 + 4);       // TMA expect-tx arrive + 4 converter warps
+            mbar_init(empty0 + 8 * s, 1 + N_EPI);  // MMA commit + the epilogue warps
         }
-        for (int s = 0; s < SR; ++s) mbar_init(sempty0 + 8 * s, N_EPI);  // 16 weighted reader arrivals
-        for (int j = 0; j < NUNIT; ++j) {
+        for (int j = 0; j < NTBUF; ++j) {
             mbar_init(tfull0 + 8 * j, 1);
-            mbar_init(tempty0 + 8 * j, 4);  // the four lane-quarter warps of the column group reading it
+            mbar_init(tempty0 + 8 * j, N_EPI);
         }
         *abort_flag = 0;
-        *(volatile uint32_t *)(smem + MISC_OFF + 8) = 0u;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == W_MMA) {
@@ -425,320 +372,256 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int nkt = p.K / BK;
     const int nbk = p.K / kBlock;
     const size_t scale_off = blob_scales_offset(p.rows, nbk);
-    auto slot_ptr = [&](int slot) { return smem + slot * B_BYTES; };  // the slot's B tile
-    auto sc_ptr = [&](int s) { return smem + SC_OFF + s * SC_BYTES; };
+    auto slot_ptr = [&](int slot) { return smem + slot * C::SLOT_STRIDE; };
 
-    if (warp >= W_TMA && warp < W_EPI) {
-        // the TMA/MMA warpgroup: one setmaxnreg for all four warps, then the
-        // TMA and MMA roles (its last two warps only join the final barrier)
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProdRegs));
-        if (warp == W_TMA && lane == 0) {
+    if (warp == W_TMA) {
+        if (lane == 0) {
             int it = 0;
             for (int t = blockIdx.x; t < total; t += gridDim.x) {
-                int u, rt, tt, nc, nrt;
-                decode_tile(p.tile_rec, t, u, rt, tt, nc, nrt);
+                int u, rt, tt, nc;
+                decode_tile(p.tile_rec, t, u, rt, tt, nc);
                 const int pos0 = p.uniq_off[u] + tt * BN;
-                for (int kt = 0; kt < nkt; ++kt)
-                    for (int j = 0; j < nrt; ++j, ++it) {
-                        const int slot = it % STAGES;
-                        const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
-                        if (!mbar_wait(empty0 + 8 * slot, ph ^ 1u, abort_flag, p.error, 2)) goto tma_done;
-                        mbar_arrive_tx(full0 + 8 * slot, B_BYTES);
-                        tma_load_2d(smem_u32(slot_ptr(slot)), &tmB, kt * BK, pos0, full0 + 8 * slot);
-                    }
+                for (int kt = 0; kt < nkt; ++kt, ++it) {
+                    const int slot = it % STAGES;
+                    const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+                    if (!mbar_wait(empty0 + 8 * slot, ph ^ 1u, abort_flag, p.error, 2)) goto tma_done;
+                    mbar_arrive_tx(full0 + 8 * slot, C::B_BYTES);
+                    tma_load_2d(smem_u32(slot_ptr(slot) + NA * C::A_BYTES), &tmB, kt * BK, pos0, full0 + 8 * slot);
+                }
             }
         tma_done:;
         }
-        if (warp == W_MMA && lane == 0) {
-            int it = 0;
-            uint32_t ph = 0;  // per TMEM unit: parity of its next use
+    } else if (warp == W_MMA) {
+        if (lane == 0) {
+            int it = 0, qc = 0;
             // the tile's MMA width: its valid token columns rounded up to 16
             // (the record of the next tile is requested a tile ahead)
             uint2 rec_next = blockIdx.x < total ? __ldg(p.tile_rec + blockIdx.x) : make_uint2(0, 0);
             for (int t = blockIdx.x; t < total; t += gridDim.x) {
-                const int ncols = (int)((rec_next.y >> 16) & 0xffu), nrt = (int)(rec_next.y >> 24);
+                const int ncols = (int)(rec_next.y >> 16);
                 if (t + (int)gridDim.x < total) rec_next = __ldg(p.tile_rec + t + gridDim.x);
                 const int nmma = min(BN, (ncols + 15) & ~15);
-                const int w = block_units(ncols);
                 const uint32_t idesc = idesc_f16(BM, nmma < 16 ? 16 : nmma);
-                uint32_t slots = 0;  // block slot (0..2) of each tile of the batch, 2 bits per tile
-                for (int ks = 0, j = 0; ks < nkt * nrt; ++ks, ++it, j = (j + 1 == nrt) ? 0 : j + 1) {
+                for (int kt = 0; kt < nkt; ++kt, ++it) {
                     const int slot = it % STAGES;
                     if (!mbar_wait(full0 + 8 * slot, (uint32_t)(it / STAGES) & 1u, abort_flag, p.error, 4))
                         goto mma_done;
                     tc_fence_after();
-                    const uint32_t ta = tmem + A_TMEM_COL + 32u * (uint32_t)slot;
-                    const uint64_t db = sdesc(smem_u32(slot_ptr(slot)));
-                    for (int blk = 0; blk < 2; ++blk) {
-                        const int sl = (int)((slots >> (2 * j)) & 3u);
-                        slots = (slots & ~(3u << (2 * j))) | ((uint32_t)(sl == 2 ? 0 : sl + 1) << (2 * j));
-                        const int u0 = 3 * w * j + w * sl;
-                        // the units' previous readers are done with them
-                        for (int g = 0; g < w; ++g)
-                            if (!mbar_wait(tempty0 + 8 * (u0 + g), ((ph >> (u0 + g)) & 1u) ^ 1u, abort_flag, p.error, 8))
-                                goto mma_done;
+                    uint8_t *st = slot_ptr(slot);
+                    const uint64_t db = sdesc(smem_u32(st + NA * C::A_BYTES));
+                    for (int blk = 0; blk < 2; ++blk, ++qc) {
+                        const int j = qc % NTBUF;
+                        if (!mbar_wait(tempty0 + 8 * j, ((uint32_t)(qc / NTBUF) & 1u) ^ 1u, abort_flag, p.error, 8))
+                            goto mma_done;
                         tc_fence_after();
 #pragma unroll
                         for (int kk = 0; kk < 2; ++kk) {
                             const uint64_t koff = (uint64_t)((blk * 32 + kk * 16) * 2) >> 4;
-                            mma_f16_ts(tmem + (uint32_t)(u0 * 32), ta + (uint32_t)(blk * 16 + kk * 8), db + koff, idesc,
-                                       kk > 0 ? 1u : 0u);
+#pragma unroll
+                            for (int a = 0; a < NA; ++a) {
+                                const uint64_t da = sdesc(smem_u32(st + a * C::A_BYTES));
+                                mma_f16(tmem + (uint32_t)(j * C::TBUF + a * BN), da + koff, db + koff, idesc,
+                                        kk > 0 ? 1u : 0u);
+                            }
                         }
-                        for (int g = 0; g < w; ++g) mma_commit(tfull0 + 8 * (u0 + g));
-                        ph ^= ((1u << w) - 1u) << u0;
-                        // K block 2 it + blk is issued: its units' previous uses are complete
-                        // (the waits above), and the stage's scales are in place (full)
-                        st_release_cta(issued, (uint32_t)(2 * it + blk + 1));
+                        mma_commit(tfull0 + 8 * j);
                     }
                     mma_commit(empty0 + 8 * slot);
                 }
             }
         mma_done:;
         }
-    } else if (warp < W_TMA) {
-        // Converters: thread r owns row r of the A tile (TMEM lane r).  The
-        // raw Q4 codes of stage s are fetched with cp.async PD stages ahead
-        // into raw ring entry s % RR, the stage's weight and activation scales
-        // straight into scale slot s % SR (once the epilogue has freed it);
-        // stage s is then expanded to fp16 and stored into the slot's TMEM
-        // columns with one tcgen05.st per thread.
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProdRegs));
+    } else if (warp < W_EPI) {
+        // Converters: thread r owns row r of the A tiles.  Raw Q4 codes and
+        // both scale sets of stage s are fetched with cp.async PD stages ahead
+        // into raw ring entry s % RR; stage s is then converted into its slot.
         const int r = threadIdx.x - W_CONV * 32;
-        uint8_t *raw = smem + RAW_OFF;
+        uint8_t *raw = smem + C::RAW_OFF;
         StageCur fc;  // fetch cursor; conversion only counts stages
-        cur_init<DUAL>(fc, p, total, r);
-        int n_stages = 0;
-        for (int t = blockIdx.x; t < total; t += gridDim.x) {
-            int u, rt, tt, nc, nrt;
-            decode_tile(p.tile_rec, t, u, rt, tt, nc, nrt);
-            n_stages += nkt * nrt;
-        }
-        bool ok = true;
-        auto fetch = [&](const StageCur &cu, int q) {  // stage q
-            if (cu.valid) {
-                uint8_t *ent = raw + (q % RR) * RAW_BYTES;
-                uint8_t *sc = sc_ptr(q % SR);
-                if (lane == 0)
-                    ok = ok && mbar_wait(sempty0 + 8 * (q % SR), ((uint32_t)(q / SR) & 1u) ^ 1u, abort_flag, p.error, 16);
-                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-                const int row = tile_row<DUAL>(cu.rt0 + cu.j, r);
-                const bool vrow = ok && row < p.rows;
-                const int srow = row < p.rows ? row : 0;
-                const uint8_t *src = cu.blob + ((size_t)srow * nbk + 2 * cu.kt) * 16;
-                cp_async(smem_u32(ent + r * 32), src, 16, vrow);
-                cp_async(smem_u32(ent + r * 32 + 16), src + 16, 16, vrow);
-                const uint8_t *ssrc = cu.blob + scale_off + ((size_t)srow * nbk + 2 * cu.kt) * 2;
-                cp_async(smem_u32(sc + r * 4), ssrc, 4, vrow);
-                // activation scales i of the stage: block i / BN, column i % BN
+        cur_init<BN>(fc, p, n_uniq, total);
+        const int n_stages = blockIdx.x < total ? ((total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1) * nkt : 0;
+        auto fetch = [&](const StageCur &c, int rs) {
+            uint8_t *ent = raw + rs * C::RAW_BYTES;
+            if (c.valid) {
+                const int row = c.rt * BM + r;
+                const bool vrow = row < p.rows;
+                const int srow = vrow ? row : 0;
 #pragma unroll
-                for (int i = r; i < 2 * BN; i += BM) {
-                    const int qb = i / BN, col = i - qb * BN;
-                    const int pos = cu.pos0 + col;
-                    const bool v = ok && pos < p.A_pad;
-                    const float *asrc = p.a_scaleT + (size_t)(2 * cu.kt + qb) * p.A_pad + (pos < p.A_pad ? pos : 0);
-                    cp_async(smem_u32(sc + WS_BYTES + i * 4), asrc, 4, v);
+                for (int a = 0; a < NA; ++a) {
+                    const uint8_t *blob = c.blob[a];
+                    const uint8_t *src = blob + ((size_t)srow * nbk + 2 * c.kt) * 16;
+                    const uint32_t dst = smem_u32(ent + (a * BM + r) * 32);
+                    cp_async(dst, src, 16, vrow);
+                    cp_async(dst + 16, src + 16, 16, vrow);
+                    const uint8_t *ssrc = blob + scale_off + ((size_t)srow * nbk + 2 * c.kt) * 2;
+                    cp_async(smem_u32(ent + C::RAW_CODES + (a * BM + r) * 4), ssrc, 4, vrow);
+                }
+                const int pos0 = c.pos0;
+                for (int i = r; i < 2 * BN; i += 128) {
+                    const int q = i / BN, col = i - q * BN;
+                    const int pos = pos0 + col;
+                    const bool v = pos < p.A_pad;
+                    const float *src = p.a_scaleT + (size_t)(2 * c.kt + q) * p.A_pad + (v ? pos : 0);
+                    cp_async(smem_u32(ent + C::RAW_CODES + C::WS_BYTES + i * 4), src, 4, v);
                 }
             }
             cp_commit();
         };
-        for (int i = 0; i < PD; ++i) {
-            fetch(fc, i);
-            cur_next<DUAL>(fc, p, total, nkt, r);
+        for (int i = 0; i < C::PD; ++i) {
+            fetch(fc, i % C::RR);
+            cur_next<BN>(fc, p, n_uniq, total, nkt);
         }
-        const uint32_t ta_lane = tmem + ((uint32_t)(warp * 32) << 16) + A_TMEM_COL;  // this warp's lane quarter
         int it = 0;
-        while (it < n_stages && ok) {
-            fetch(fc, it + PD);
-            cur_next<DUAL>(fc, p, total, nkt, r);
-            cp_wait<PD>();
+        while (it < n_stages) {
+            fetch(fc, (it + C::PD) % C::RR);
+            cur_next<BN>(fc, p, n_uniq, total, nkt);
+            cp_wait<C::PD>();
+            const uint8_t *ent = raw + (it % C::RR) * C::RAW_BYTES;
             const int slot = it % STAGES;
-            if (lane == 0)
-                ok = mbar_wait(empty0 + 8 * slot, ((uint32_t)(it / STAGES) & 1u) ^ 1u, abort_flag, p.error, 16);
+            const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+            bool ok = true;
+            if (lane == 0) ok = mbar_wait(empty0 + 8 * slot, ph ^ 1u, abort_flag, p.error, 16);
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
             if (!ok) break;
-            tc_fence_after();
-            const uint8_t *ent = raw + (it % RR) * RAW_BYTES;
-            uint32_t a[32];
-            convert_block(*(const uint4 *)(ent + r * 32), a);
-            convert_block(*(const uint4 *)(ent + r * 32 + 16), a + 16);
-            tmem_st32(ta_lane + 32u * (uint32_t)slot, a);
-            tmem_st_wait();
-            tc_fence_before();
+            uint8_t *st = slot_ptr(slot);
+#pragma unroll
+            for (int a = 0; a < NA; ++a) {
+                const uint4 *cs = (const uint4 *)(ent + (a * BM + r) * 32);
+                convert_store_row(st + a * C::A_BYTES, r, cs[0], cs[1]);
+                // this row's two weight scales of the stage
+                *(uint32_t *)(st + NA * C::A_BYTES + C::B_BYTES + (a * BM + r) * 4) =
+                    *(const uint32_t *)(ent + C::RAW_CODES + (a * BM + r) * 4);
+            }
+            for (int i = r; i < 2 * BN; i += 128)
+                *(float *)(st + NA * C::A_BYTES + C::B_BYTES + C::WS_BYTES + i * 4) =
+                    *(const float *)(ent + C::RAW_CODES + C::WS_BYTES + i * 4);
+            fence_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(full0 + 8 * slot);
             ++it;
         }
         cp_wait<0>();
     } else {
-        // Epilogue: TMEM lane quarter = warp % 4 (thread = tile row), column
-        // group = 32 token columns.  Per K block: one 32-column TMEM load
-        // (the buffer is handed back to the MMA as soon as the load is
-        // complete), s = d_w * d_a (mul.f32x2) and acc += sum * s (fma.f32x2),
-        // the activation scales of four columns per 128-bit broadcast load.
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kEpiRegs));
-        const int e = warp - W_EPI;
+        // epilogue: TMEM lane quarter = warp % 4 (thread = weight row), half =
+        // which HC token columns this warp owns.  Per K stage: one wait (the
+        // MMA's commit after the stage's second block covers the first), the
+        // activation scales of the warp's columns read once per block, the
+        // block sums read 32 columns per TMEM load, and the scaling as packed
+        // fp32 pairs: s = d_w * d_a (mul.f32x2), acc += sum * s (fma.f32x2).
         const int quarter = warp & 3;
-        const int grp = e >> 2;  // column group: tile grp / w of the batch, its columns [32 cu, 32 cu + 32)
+        const int half = (warp - W_EPI) >> 2;  // which column part this warp owns
+        constexpr int HC = BN / EPI_SPLIT;      // token columns per epilogue warp
+        static_assert(HC % 32 == 0, "32-column groups per epilogue warp");
         const int r = quarter * 32 + lane;
-        float *xch = (float *)(smem + XCH_OFF);
-        int it0 = 0;      // stage index of the batch's first stage
-        uint32_t ph = 0;  // per TMEM unit: parity of its next use, at the start of the batch
+        int qc = 0, it = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
-            int u, rt0, tt, ncols, nrt;
-            decode_tile(p.tile_rec, t, u, rt0, tt, ncols, nrt);
-            const int w = block_units(ncols);
-            const int tj = grp / w, cu = grp - tj * w;  // this group's tile in the batch and column unit
-            const uint32_t ph_next = ph ^ batch_unit_flips(nrt, w, 2 * nkt);
-            const int it_first = it0;
-            it0 += nkt * nrt;
-            if (tj >= nrt) {  // no tile of this batch for this group
-                ph = ph_next;
-                continue;
-            }
-            const int rt = rt0 + tj;
-            const bool active = cu * 32 < ncols;  // this warp has valid columns (warp-uniform)
-            const int pos0 = p.uniq_off[u] + tt * BN + cu * 32;
+            int u, rt, tt, ncols;
+            decode_tile(p.tile_rec, t, u, rt, tt, ncols);
+            const int ncw = ncols - half * HC;  // this warp's valid columns (may be <= 0)
+            const int row = rt * BM + r;
+            const bool vrow = row < p.rows;
+            const int pos0 = p.uniq_off[u] + tt * BN + half * HC;
             const int pos_end = p.uniq_off[u + 1];
-            const uint32_t sc_weight = 4u / (uint32_t)w;  // 4 w warps read a stage's scales; 16 arrivals free it
-            float2 acc[16];
+            float acc[NA][HC];
 #pragma unroll
-            for (int cc = 0; cc < 16; ++cc) acc[cc] = make_float2(0.0f, 0.0f);
-            uint32_t q = ph;  // parities of this tile's units, updated as they are read
-            int sl = 0;       // block slot of the next K block
-            for (int kt = 0; kt < nkt; ++kt) {
-                const int it = it_first + kt * nrt + tj;  // this tile's stage
-                const int ss = it % SR;
-                const uint8_t *sc = sc_ptr(ss);
+            for (int a = 0; a < NA; ++a)
+#pragma unroll
+                for (int c = 0; c < HC; ++c) acc[a][c] = 0.0f;
+            for (int kt = 0; kt < nkt; ++kt, ++it, qc += 2) {
+                const int slot = it % STAGES;
+                const uint8_t *st = slot_ptr(slot);
+                const int j0 = qc % NTBUF, j1 = (qc + 1) % NTBUF;
                 bool ok = true;
-                // the stage's first K block is issued: its scales are in place
-                // (and no TMEM unit of the stage is more than a phase ahead)
-                if (lane == 0) ok = wait_issued(issued, (uint32_t)(2 * it + 1), abort_flag, p.error);
+                // the slot's scales were written before its full barrier
+                // completed; the second block's commit covers both blocks
+                if (lane == 0) {
+                    ok = mbar_wait(full0 + 8 * slot, (uint32_t)(it / STAGES) & 1u, abort_flag, p.error, 64) &&
+                         mbar_wait(tfull0 + 8 * j1, (uint32_t)((qc + 1) / NTBUF) & 1u, abort_flag, p.error, 32);
+                }
                 ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                 if (!ok) goto epi_done;
-                const uint32_t wsc = *(const uint32_t *)(sc + r * 4);
-                const float4 *cs4 = (const float4 *)(sc + WS_BYTES) + cu * 8;
-#pragma unroll 1
+                tc_fence_after();
+                uint32_t wsc[NA];
+#pragma unroll
+                for (int a = 0; a < NA; ++a)
+                    wsc[a] = *(const uint32_t *)(st + NA * C::A_BYTES + C::B_BYTES + (a * BM + r) * 4);
+                const float *asc = (const float *)(st + NA * C::A_BYTES + C::B_BYTES + C::WS_BYTES) + half * HC;
+#pragma unroll
                 for (int blk = 0; blk < 2; ++blk) {
-                    const int un = 3 * w * tj + w * sl + cu;  // this warp's unit of the block
-                    sl = sl == 2 ? 0 : sl + 1;
-                    {
-                        if (lane == 0)
-                            ok = wait_issued(issued, (uint32_t)(2 * it + blk + 1), abort_flag, p.error) &&
-                                 mbar_wait(tfull0 + 8 * un, (q >> un) & 1u, abort_flag, p.error, 32);
-                        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-                        if (!ok) goto epi_done;
-                        tc_fence_after();
-                        if (active) {
-                            const float dw = __half2float(
-                                __ushort_as_half((unsigned short)(blk ? (wsc >> 16) : (wsc & 0xffffu))));
-                            const float2 dw2 = make_float2(dw, dw);
-                            const float4 *c4p = cs4 + blk * (BN / 4);
-                            // the unit's 32 columns in two 16-column loads
+                    const int j = blk ? j1 : j0;
+                    const uint32_t tb = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(j * C::TBUF + half * HC);
+                    float dw[NA];
 #pragma unroll
-                            for (int half = 0; half < 2; ++half) {
-                                uint32_t sv[16];
-                                tmem_ld16u(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(un * 32 + half * 16),
-                                           sv);
-                                tmem_ld_wait();
+                    for (int a = 0; a < NA; ++a) {
+                        const uint32_t dwb = blk ? (wsc[a] >> 16) : (wsc[a] & 0xffffu);
+                        dw[a] = __half2float(__ushort_as_half((unsigned short)dwb));
+                    }
+                    const float2 *dq2 = reinterpret_cast<const float2 *>(asc + blk * BN);
 #pragma unroll
-                                for (int c4 = 0; c4 < 4; ++c4) {
-                                    const float4 d4 = c4p[half * 4 + c4];  // broadcast read
-                                    const float2 s01 = __fmul2_rn(dw2, make_float2(d4.x, d4.y));
-                                    const float2 s23 = __fmul2_rn(dw2, make_float2(d4.z, d4.w));
-                                    float2 &a0 = acc[half * 8 + 2 * c4], &a1 = acc[half * 8 + 2 * c4 + 1];
-                                    a0 = __ffma2_rn(make_float2(__uint_as_float(sv[4 * c4]),
-                                                                __uint_as_float(sv[4 * c4 + 1])), s01, a0);
-                                    a1 = __ffma2_rn(make_float2(__uint_as_float(sv[4 * c4 + 2]),
-                                                                __uint_as_float(sv[4 * c4 + 3])), s23, a1);
-                                }
+                    for (int cb = 0; cb < HC; cb += 16) {
+                        if (cb >= ncw) break;  // columns past the tile's tokens (warp-uniform)
+#pragma unroll
+                        for (int a = 0; a < NA; ++a) {
+                            // block sums of 16 columns of tensor a
+                            uint32_t pv[16];
+                            tmem_ld16u(tb + (uint32_t)(a * BN + cb), pv);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int c = 0; c < 8; ++c) {
+                                const float2 d2 = dq2[(cb >> 1) + c];  // activation scales: broadcast reads
+                                fma_scaled2(acc[a][cb + 2 * c], acc[a][cb + 2 * c + 1], pv[2 * c], pv[2 * c + 1], d2.x,
+                                            d2.y, dw[a]);
                             }
                         }
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(tempty0 + 8 * un);
                     }
-                    q ^= 1u << un;
                 }
+                tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive_n(sempty0 + 8 * ss, sc_weight);
-            }
-            ph = ph_next;
-            // tile outputs; the assignment id of column i of this warp's group
-            // is held by lane i
-            const int my_pos = pos0 + lane;
-            const int my_asg = my_pos < pos_end ? __ldg(p.assign + my_pos) : 0;
-            if (DUAL) {
-                // SwiGLU pairs gate row f (quarter q < 2) with up row f (quarter
-                // q + 2), same lane, same column group; the gate warp finishes
-                // columns 0..15 of the group, the up warp columns 16..31, each
-                // receiving the other tensor's values through shared memory.
-                const int pair = grp * 2 + (quarter & 1);
-                const bool is_gate = quarter < 2;
-                float *to_partner = xch + ((size_t)(pair * 2 + (is_gate ? 0 : 1)) * 16) * 32;
-                const float *from_partner = xch + ((size_t)(pair * 2 + (is_gate ? 1 : 0)) * 16) * 32;
-                if (active) {
-#pragma unroll
-                    for (int cc = 0; cc < 8; ++cc) {
-                        // the gate warp sends columns 16..31, the up warp 0..15
-                        const float2 v = is_gate ? acc[8 + cc] : acc[cc];
-                        to_partner[(2 * cc) * 32 + lane] = v.x;
-                        to_partner[(2 * cc + 1) * 32 + lane] = v.y;
-                    }
+                if (lane == 0) {
+                    mbar_arrive(tempty0 + 8 * j0);
+                    mbar_arrive(tempty0 + 8 * j1);
+                    mbar_arrive(empty0 + 8 * slot);
                 }
-                bar_sync_named(1 + pair, 64);
-                if (active) {
-                    // this warp's 16 columns of the group (gate warp: 0..15, up warp: 16..31)
-                    float mine[16];
+            }
+            // tile outputs (this warp's token columns); the assignment ids of
+            // the columns are fetched once (lane i: columns i, i + 32, ...)
+            int asg_l[HC / 32];
 #pragma unroll
-                    for (int cc = 0; cc < 8; ++cc) {
-                        const float2 v = is_gate ? acc[cc] : acc[8 + cc];
-                        mine[2 * cc] = v.x;
-                        mine[2 * cc + 1] = v.y;
-                    }
-                    const int c0 = is_gate ? 0 : 16;
-                    const int fb = (rt * 64 + (quarter & 1) * 32) / kBlock;  // h block index along F
-                    const int f = rt * 64 + (quarter & 1) * 32 + lane;       // F row of this lane
-                    const int nc = min(16, ncols - cu * 32 - c0);            // valid columns (warp-uniform)
+            for (int i = 0; i < HC / 32; ++i) {
+                const int pos = pos0 + i * 32 + lane;
+                asg_l[i] = pos < pos_end ? __ldg(p.assign + pos) : 0;
+            }
+            if (DUAL) {
+                const int fb = (rt * BM + quarter * 32) / kBlock;  // h block index along F
+                const bool vblk = rt * BM + quarter * 32 < p.rows;
 #pragma unroll
-                    for (int cc = 0; cc < 16; ++cc) {
-                        if (cc < nc) {
-                            const float other = from_partner[cc * 32 + lane];
-                            const float g = is_gate ? mine[cc] : other, uu = is_gate ? other : mine[cc];
-                            const float h = g * uu / (1.0f + expf(-g));
-                            const float amax =
-                                __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(h))));
-                            const float dd = __half2float(__float2half_rn(amax / 127.0f));
-                            int qv = 0;
-                            if (dd != 0.0f) qv = (int)fminf(fmaxf(rintf(h / dd), -127.0f), 127.0f);
-                            const int sum = __reduce_add_sync(0xffffffffu, qv);
-                            const int col = c0 + cc;
-                            const int pos = pos0 + col;
-                            const int a = __shfl_sync(0xffffffffu, my_asg, col);
-                            if (pos < pos_end) {
-                                p.hq16[(size_t)pos * p.F_out + f] = __int2half_rn(qv);
-                                p.hq[(size_t)a * p.F_out + f] = (int8_t)qv;
-                                if (lane == 0) {
-                                    p.hdT[(size_t)fb * p.A_pad + pos] = dd;
-                                    p.hds[(size_t)a * (p.F_out / kBlock) + fb] = BlockScale{dd, sum};
-                                }
-                            }
+                for (int c = 0; c < HC; ++c) {
+                    if (c >= ncw) break;  // warp-uniform
+                    const int pos = pos0 + c;
+                    const float g = acc[0][c], uu = acc[NA - 1][c];
+                    const float h = g * uu / (1.0f + expf(-g));
+                    const float amax = warp_max(fabsf(h));
+                    const float dd = __half2float(__float2half_rn(amax / 127.0f));
+                    int qv = 0;
+                    if (dd != 0.0f) qv = (int)fminf(fmaxf(rintf(h / dd), -127.0f), 127.0f);
+                    const int s = warp_sum_i(qv);
+                    const int a = __shfl_sync(0xffffffffu, asg_l[c / 32], c % 32);
+                    if (vblk && pos < pos_end) {
+                        p.hq16[(size_t)pos * p.F_out + row] = __int2half_rn(qv);
+                        p.hq[(size_t)a * p.F_out + row] = (int8_t)qv;
+                        if (lane == 0) {
+                            p.hdT[(size_t)fb * p.A_pad + pos] = dd;
+                            p.hds[(size_t)a * (p.F_out / kBlock) + fb] = BlockScale{dd, s};
                         }
                     }
                 }
-                // the exchange area is rewritten at the end of the next tile
-                bar_sync_named(1 + pair, 64);
-            } else if (active) {
-                const int row = rt * BM + r;
-                const bool vrow = row < p.rows;
-                const int nc = min(32, ncols - cu * 32);  // valid columns (warp-uniform)
+            } else {
 #pragma unroll
-                for (int cc = 0; cc < 32; ++cc) {
-                    if (cc < nc) {
-                        const int pos = pos0 + cc;
-                        const int a = __shfl_sync(0xffffffffu, my_asg, cc);
-                        const float v = (cc & 1) ? acc[cc >> 1].y : acc[cc >> 1].x;
-                        if (vrow && pos < pos_end) p.o[(size_t)a * p.rows + row] = v;
-                    }
+                for (int c = 0; c < HC; ++c) {
+                    if (c >= ncw) break;  // warp-uniform
+                    const int pos = pos0 + c;
+                    const int a = __shfl_sync(0xffffffffu, asg_l[c / 32], c % 32);
+                    if (vrow && pos < pos_end) p.o[(size_t)a * p.rows + row] = acc[0][c];
                 }
             }
         }
@@ -763,30 +646,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 }  // namespace gemm
 
 // ---------------------------------------------------------------- prefill helpers
-// Work items of one expert with n tokens: per token tile of bn columns, its
-// rt row tiles in batches of 4 / block_units(valid columns).
-__device__ __forceinline__ int gemm_batches(int n, int rt, int bn) {
-    int cnt = 0;
-    for (int tt = 0; tt * bn < n; ++tt) {
-        const int per = 4 / gemm::block_units(min(bn, n - tt * bn));
-        cnt += (rt + per - 1) / per;
-    }
-    return cnt;
-}
-
-__device__ __forceinline__ void gemm_batch_records(int u, int n, int rt, int bn, uint2 *out, int cap) {
-    int i = 0;
-    for (int tt = 0; tt * bn < n; ++tt) {
-        const int nc = min(bn, n - tt * bn);
-        const int per = 4 / gemm::block_units(nc);
-        for (int r0 = 0; r0 < rt; r0 += per, ++i) {
-            if (i < cap)
-                out[i] = make_uint2((unsigned)u | ((unsigned)r0 << 16),
-                                    (unsigned)tt | ((unsigned)nc << 16) | ((unsigned)min(per, rt - r0) << 24));
-        }
-    }
-}
-
 // Per used expert: cumulative tile counts of the gate/up and down GEMMs, and
 // the miss / stamp record of the layer's three tensors.
 __global__ void tiling_kernel(TilingParams p) {
@@ -806,8 +665,8 @@ __global__ void tiling_kernel(TilingParams p) {
         int tg = 0, td = 0;
         if (u < n_uniq) {
             const int n = p.uniq_off[u + 1] - p.uniq_off[u];
-            tg = gemm_batches(n, p.rt_gu, p.bn_gu);
-            td = gemm_batches(n, p.rt_dn, p.bn_dn);
+            tg = p.rt_gu * ((n + p.bn_gu - 1) / p.bn_gu);
+            td = p.rt_dn * ((n + p.bn_dn - 1) / p.bn_dn);
         }
         // inclusive warp scans then block offsets, for both counts
         int ig = tg, id = td;
@@ -848,12 +707,23 @@ __global__ void tiling_kernel(TilingParams p) {
         __syncthreads();
     }
     __syncthreads();
-    // batch records: (u | first row tile << 16, token tile | valid columns
-    // << 16 | row tiles << 24), token tile outer, row tiles inner
+    // per-tile records: (u | row tile << 16, token tile | valid columns << 16)
     for (int u = threadIdx.x; u < n_uniq; u += blockDim.x) {
         const int n = p.uniq_off[u + 1] - p.uniq_off[u];
-        gemm_batch_records(u, n, p.rt_gu, p.bn_gu, p.rec_gu + p.tile_off_gu[u], p.cap_gu - p.tile_off_gu[u]);
-        gemm_batch_records(u, n, p.rt_dn, p.bn_dn, p.rec_dn + p.tile_off_dn[u], p.cap_dn - p.tile_off_dn[u]);
+        const int ng = (n + p.bn_gu - 1) / p.bn_gu, nd = (n + p.bn_dn - 1) / p.bn_dn;
+        const int bg = p.tile_off_gu[u], bd = p.tile_off_dn[u];
+        for (int i = 0; i < p.rt_gu * ng; ++i) {
+            const int rt = i / ng, tt = i - rt * ng;
+            if (bg + i < p.cap_gu)
+                p.rec_gu[bg + i] = make_uint2((unsigned)u | ((unsigned)rt << 16),
+                                              (unsigned)tt | ((unsigned)min(p.bn_gu, n - tt * p.bn_gu) << 16));
+        }
+        for (int i = 0; i < p.rt_dn * nd; ++i) {
+            const int rt = i / nd, tt = i - rt * nd;
+            if (bd + i < p.cap_dn)
+                p.rec_dn[bd + i] = make_uint2((unsigned)u | ((unsigned)rt << 16),
+                                              (unsigned)tt | ((unsigned)min(p.bn_dn, n - tt * p.bn_dn) << 16));
+        }
     }
     if (threadIdx.x == 0) {
         p.tile_off_gu[n_uniq] = run_gu;
@@ -960,23 +830,16 @@ int launch_stage(const StageParams &p, size_t blob_bytes, int n_sm, cudaStream_t
     return (int)cudaGetLastError();
 }
 
-int gemm_bn(bool) { return gemm::BN; }
-// Weight rows of the layer's tensors covered by one row tile: 64 F rows for
-// gate/up (64 gate + the same 64 up rows), 128 H rows for down.
-int gemm_rows_per_tile(bool dual) { return dual ? 64 : gemm::BM; }
+int gemm_smem_bytes(bool dual) { return dual ? gemm::Cfg<true>::SMEM : gemm::Cfg<false>::SMEM; }
+int gemm_bn(bool dual) { return dual ? gemm::Cfg<true>::BN : gemm::Cfg<false>::BN; }
+// Weight rows of the layer's tensors covered by one row tile (TMEM lanes).
+int gemm_rows_per_tile(bool) { return gemm::BM; }
 
 int gemm_configure() {
-    // the kernels' register split assumes ptxas gave them kLaunchRegs per thread
-    for (const void *fn : {(const void *)gemm::grouped_gemm_kernel<true>, (const void *)gemm::grouped_gemm_kernel<false>}) {
-        cudaFuncAttributes fa{};
-        cudaError_t e = cudaFuncGetAttributes(&fa, fn);
-        if (e != cudaSuccess) return (int)e;
-        if (fa.numRegs != gemm::kLaunchRegs) return (int)cudaErrorInvalidConfiguration;
-    }
     cudaError_t e1 = cudaFuncSetAttribute(gemm::grouped_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          gemm::SMEM);
+                                          gemm::Cfg<true>::SMEM);
     cudaError_t e2 = cudaFuncSetAttribute(gemm::grouped_gemm_kernel<false>,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize, gemm::SMEM);
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize, gemm::Cfg<false>::SMEM);
     return (int)(e1 != cudaSuccess ? e1 : e2);
 }
 
@@ -998,10 +861,10 @@ int launch_prefill(const PrefillLaunch &L, cudaStream_t st, cudaEvent_t const *e
     if (g > 0) gather_kernel<<<g, 256, 0, st>>>(L.gu.assign, A, L.k, L.H, L.xq, L.xds, L.xs16, L.xdT, L.gu.A_pad);
     // timing hook: events around each GEMM launch
     if (ev) record_event(ev[0], st);
-    gemm::grouped_gemm_kernel<true><<<L.n_sm, gemm::NTHREADS, gemm::SMEM, st>>>(L.tm_x, L.gu);
+    gemm::grouped_gemm_kernel<true><<<L.n_sm, gemm::Cfg<true>::NTHREADS, gemm::Cfg<true>::SMEM, st>>>(L.tm_x, L.gu);
     if (ev) record_event(ev[1], st);
     if (ev) record_event(ev[2], st);
-    gemm::grouped_gemm_kernel<false><<<L.n_sm, gemm::NTHREADS, gemm::SMEM, st>>>(L.tm_h, L.dn);
+    gemm::grouped_gemm_kernel<false><<<L.n_sm, gemm::Cfg<false>::NTHREADS, gemm::Cfg<false>::SMEM, st>>>(L.tm_h, L.dn);
     if (ev) record_event(ev[3], st);
     const size_t n = (size_t)L.T * L.H;
     int gc = (int)std::min<size_t>((n + 255) / 256, (size_t)L.n_sm * 16);
