@@ -1192,9 +1192,6 @@ __device__ __forceinline__ void t1_route_gate_up(const FusedParams &p, int *s_e,
                     su[i] = ld_scale(du + b);
                 }
             }
-            // the CTA's down rows are requested right behind its first
-            // gate/up loads, so both weight streams are in flight together
-            if (bb == 0 && m == 0) stage_first_down();
 #pragma unroll
             for (int i = 0; i < kGURounds; ++i) {
                 const int b = sub + kGULanes * (bb * kGURounds + i);
@@ -1220,6 +1217,15 @@ __device__ __forceinline__ void t1_route_gate_up(const FusedParams &p, int *s_e,
             quantize_block_warp(hrow[lane], lane, g.hq + (size_t)u * F + (size_t)rg * kBlock, g.hds + (size_t)u * rgs + rg);
             __syncwarp();
             if (lane == 0) red_release_add(&p.done_gu[u], 1u);
+            if (m == 0) bar_arrive_n(3, 256);
+        } else if (m == 0) {
+            // the down rows are requested once this item's gate/up weights
+            // are in and its h block is out, so they compete neither with the
+            // gate/up stream nor with the publish (requesting them with the
+            // gate/up loads measured slower: the gate/up stream is the
+            // critical path to h)
+            bar_sync_n(3, 256);
+            stage_first_down();
         }
     }
     if (m == 0) stage_first_down();  // a CTA without a gate/up item
