@@ -1221,9 +1221,7 @@ __device__ __forceinline__ void t1_route_gate_up(const FusedParams &p, int *s_e,
         } else if (m == 0) {
             // the down rows are requested once this item's gate/up weights
             // are in and its h block is out, so they compete neither with the
-            // gate/up stream nor with the publish (requesting them with the
-            // gate/up loads measured slower: the gate/up stream is the
-            // critical path to h)
+            // gate/up stream nor with the publish
             bar_sync_n(3, 256);
             stage_first_down();
         }
@@ -1417,33 +1415,8 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
         if ((int)blockIdx.x < n_items) {
             constexpr int VP = 256 / LD;  // (expert, row) pairs per pass
             const int sub = threadIdx.x % LD;
-            // every used expert's gate/up items are published (bounded wait,
-            // one thread per expert), then the h codes and scales of all
-            // assignments are copied once from L2 into the staging region
-            // (free now: the CTA's gate/up items are done) for the down dots
-            const int A = g.n_tokens * k;
-            int8_t *hq_s = (int8_t *)dsm;
-            int2 *hs_s = (int2 *)(dsm + (((size_t)A * F + 15) & ~(size_t)15));
-            if ((int)threadIdx.x < nu) {
-                const long long t0 = clock64();
-                while (ld_acquire(&p.done_gu[threadIdx.x]) < (unsigned)rgs) {
-                    if (clock64() - t0 > 4000000000ll) {
-                        atomicOr(p.error, 2);
-                        break;
-                    }
-                    __nanosleep(20);
-                }
-            }
-            __syncthreads();
-            {
-                const int4 *src = reinterpret_cast<const int4 *>(g.hq);
-                int4 *dst = reinterpret_cast<int4 *>(hq_s);
-                for (int i = threadIdx.x; i < A * F / 16; i += blockDim.x) dst[i] = __ldcg(src + i);
-                const int2 *ssrc = reinterpret_cast<const int2 *>(g.hds);
-                for (int i = threadIdx.x; i < A * nbf; i += blockDim.x) hs_s[i] = __ldcg(ssrc + i);
-            }
             cp_async_wait_all();
-            __syncthreads();  // the first item's staged rows and the h copy
+            __syncthreads();  // the first item's staged rows
             for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
                 const bool first = item == (int)blockIdx.x;
                 if (!first) {
@@ -1462,6 +1435,24 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
                     const int vr = v0 + (int)threadIdx.x / LD;
                     const bool act = vr < nu * R;
                     const int u = act ? vr / R : 0, r = vr - u * R;
+                    if (first) {
+                        // bounded wait for the gate/up items of this warp's experts
+                        const int ulo = __shfl_sync(0xffffffffu, u, 0);
+                        const int uhi = __reduce_max_sync(0xffffffffu, act ? u : 0);
+                        if (lane == 0 && v0 + (int)threadIdx.x / LD < nu * R) {
+                            const long long t0 = clock64();
+                            for (int uu = ulo; uu <= uhi; ++uu) {
+                                while (ld_acquire(&p.done_gu[uu]) < (unsigned)rgs) {
+                                    if (clock64() - t0 > 4000000000ll) {
+                                        atomicOr(p.error, 2);
+                                        break;
+                                    }
+                                    __nanosleep(20);
+                                }
+                            }
+                        }
+                        __syncwarp();
+                    }
                     const int a0 = act ? s_off[u] : 0, cnt = act ? s_off[u + 1] - a0 : 0;
                     const int mc = __reduce_max_sync(0xffffffffu, cnt);
                     const uint4 *wc = wc0 + (size_t)vr * nbf;
@@ -1471,13 +1462,13 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
                         int a = 0;
                         if (sl < cnt) {
                             a = s_asg[a0 + sl];
-                            // h of assignment a, staged in shared memory above
-                            const int4 *ha = reinterpret_cast<const int4 *>(hq_s + (size_t)a * F);
-                            const int2 *hs = hs_s + (size_t)a * nbf;
+                            // h of assignment a from L2 (written by other CTAs of this launch)
+                            const int4 *ha = reinterpret_cast<const int4 *>(g.hq + (size_t)a * F);
+                            const int2 *hs = reinterpret_cast<const int2 *>(g.hds + (size_t)a * nbf);
 #pragma unroll 4
                             for (int b = sub; b < nbf; b += LD) {
-                                const int4 h0 = ha[2 * b], h1 = ha[2 * b + 1];
-                                const int2 hsc = hs[b];
+                                const int4 h0 = __ldcg(ha + 2 * b), h1 = __ldcg(ha + 2 * b + 1);
+                                const int2 hsc = __ldcg(hs + b);
                                 const uint4 w4 = wc[b];
                                 acc += (float)q4_block_dot(w4, h0, h1, hsc.y) *
                                        (__half2float(ws[b]) * __int_as_float(hsc.x));
