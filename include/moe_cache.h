@@ -107,6 +107,8 @@ typedef struct moe_stats_t {
     uint64_t upload_bytes; /* bytes copied host -> pool by cache_step / return */
     uint64_t cold_bytes;   /* weight bytes the kernels read zero-copy */
     uint64_t clock;        /* token clock */
+    uint64_t lookahead_predicted; /* decode lookahead: picks predicted a layer ahead */
+    uint64_t lookahead_hits;      /* ... of them actually picked by that layer */
 } moe_stats_t;
 
 /*
@@ -331,9 +333,10 @@ int moe_cache_reset(moe_ctx *ctx, int global_pool);
 int moe_pool_snapshot(moe_ctx *ctx, int32_t *owner_key, uint32_t *stamps);
 
 /*
- * Lookahead prefetch for prompt passes (mihailescu2m/llama.cpp, Metal
- * streaming notes: expert reads for the next layer start a layer early).
- * With enable = 1, every forward of more than 32 tokens for layer l also
+ * Lookahead prefetch (mihailescu2m/llama.cpp, Metal streaming notes: expert
+ * reads for the next layer start a layer early).  Decode: see moe_set_router
+ * (needs the routers; enabling succeeds without a prompt-pass path then).
+ * Prompt passes: with enable = 1, every forward of more than 32 tokens for layer l also
  * enqueues, on the context's upload stream, copy-engine uploads of the
  * expert tensors of layer (l + 1) mod L that are cold at that moment into
  * one of two device prefetch buffers; the prompt forward of that layer then
@@ -349,6 +352,25 @@ int moe_pool_snapshot(moe_ctx *ctx, int32_t *owner_key, uint32_t *stamps);
  * Errors: MOE_ERR_STATE (a layer not registered), MOE_ERR_CUDA (allocation).
  */
 int moe_set_lookahead(moe_ctx *ctx, int enable);
+
+/*
+ * Router of one layer, for decode lookahead (mihailescu2m/llama.cpp, MoE
+ * expert streaming, lookahead prefetch: layer L+1's router predicts its
+ * experts from layer L's input, so their reads start a layer early).
+ * host_w: fp32 [n_experts][hidden] (stored as bf16), host_b: fp32
+ * [n_experts] or NULL (zeros); the layer's logits are modelled as
+ * b + W x.  With lookahead on (moe_set_lookahead) and the router of layer
+ * l + 1 set, every batch-1 routed forward of layer l (the single-launch
+ * layer kernel, Q4 weights, no shared expert) also computes b + W x_l for
+ * layer l + 1 from its own input x_l, takes the top-k as the prediction and
+ * prefetches the predicted experts' pool-resident gate, up and down blobs
+ * into L2 (host-resident experts are not prefetched).  Outputs, cache state
+ * and statistics other than the two lookahead counters of moe_stats are the
+ * same as without it.  Allocates (on the first call) L x E x H x 2 bytes for
+ * the routers plus small buffers.  Synchronous.  Errors: MOE_ERR_ARG,
+ * MOE_ERR_OOM, MOE_ERR_CUDA.
+ */
+int moe_set_router(moe_ctx *ctx, int layer, const float *host_w, const float *host_b);
 
 /*
  * Snapshot of one tensor's cache state (synchronizes with all streams).

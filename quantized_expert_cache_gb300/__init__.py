@@ -40,7 +40,8 @@ class moe_cfg(ctypes.Structure):
 
 class moe_stats_t(ctypes.Structure):
     _fields_ = [(n, ctypes.c_uint64) for n in (
-        "steps", "hits", "misses", "admissions", "evictions", "upload_bytes", "cold_bytes", "clock")]
+        "steps", "hits", "misses", "admissions", "evictions", "upload_bytes", "cold_bytes", "clock",
+        "lookahead_predicted", "lookahead_hits")]
 
 
 # Every symbol include/moe_cache.h declares, with (restype, argtypes).
@@ -57,6 +58,7 @@ SIGNATURES = {
     "moe_pool_borrow": (_i32, [_vp, _i32, ctypes.POINTER(_vp), ctypes.POINTER(_sz)]),
     "moe_pool_return": (_i32, [_vp]),
     "moe_set_lookahead": (_i32, [_vp, _i32]),
+    "moe_set_router": (_i32, [_vp, _i32, _vp, _vp]),
     "moe_set_global_pool": (_i32, [_vp, _i32]),
     "moe_set_upload_overlap": (_i32, [_vp, _i32]),
     "moe_set_preheat": (_i32, [_vp, _i32]),
@@ -202,6 +204,13 @@ def moe_pool_return(ctx):
 
 def moe_set_lookahead(ctx, enable=True):
     return _check(ctx, load().moe_set_lookahead(ctx, 1 if enable else 0))
+
+
+def moe_set_router(ctx, layer, w, b=None):
+    """Router of a layer for decode lookahead: w fp32 [E][H], b fp32 [E] (host)."""
+    w = np.ascontiguousarray(w, np.float32)
+    bb = None if b is None else np.ascontiguousarray(b, np.float32)
+    return _check(ctx, load().moe_set_router(ctx, layer, _host(w), _host(bb)))
 
 
 def moe_set_upload_overlap(ctx, enable=True):

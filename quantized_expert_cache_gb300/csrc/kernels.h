@@ -6,6 +6,7 @@
 #include <stdint.h>
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 
 #include "common.cuh"
 
@@ -65,6 +66,18 @@ struct FusedParams {
     // One routed token in row-block mode (fused_t1_ok): shared-memory offset
     // of the layer's gate, up and down table rows (0: the general prologue).
     int tbl_off;
+    // Lookahead (one routed token, early-start path): predict the next
+    // layer's picks as the top-k of pr_b + pr_w . x and prefetch their
+    // pool-resident weights into L2 (pr_w null: off).
+    const __nv_bfloat16 *pr_w;    // [E][H] router of the next layer
+    const float *pr_b;            // [E] its bias
+    const uint64_t *pr_tbl;       // [3][E] the next layer's gate, up and down table rows
+    float *pr_z;                  // [E] scratch: predicted logits
+    unsigned *pr_count;           // [1] predicted logits written (zero between launches)
+    int32_t *pr_set;              // [k] this launch's prediction for the next layer
+    const int32_t *pr_mine;       // [k] the previous layer's prediction for this one (or null)
+    unsigned long long *pr_stats; // [2] predicted picks, of them actually picked
+    size_t pr_blob;               // bytes of one expert tensor blob
 };
 
 // One grouped GEMM launch (gate/up with SwiGLU + h quantization, or down).

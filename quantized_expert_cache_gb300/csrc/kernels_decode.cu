@@ -1008,6 +1008,73 @@ __device__ __forceinline__ void dn_chunk(const FusedParams &p, int c0, int nt, i
 __device__ __forceinline__ void bar_sync_n(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 __device__ __forceinline__ void bar_arrive_n(int id, int n) { asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 
+// Lookahead prediction (mihailescu2m/llama.cpp, MoE expert streaming,
+// lookahead prefetch: layer L+1's router predicts its experts from layer L's
+// input, so their reads start a layer early).  Warp-level dot of one router
+// row (bf16) with the layer's input x (fp32); the warp that writes the last
+// predicted logit of the launch takes their top-k and prefetches the picked
+// experts' pool-resident gate, up and down blobs into L2.
+__device__ __forceinline__ void l2_prefetch(const void *p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void lookahead_predict(const FusedParams &p, int e, int lane) {
+    const int H = p.g.H, E = p.g.cv.E, k = p.g.k;
+    const uint4 *w = reinterpret_cast<const uint4 *>(p.pr_w + (size_t)e * H);  // 8 bf16 per uint4
+    const float4 *x = reinterpret_cast<const float4 *>(p.x);
+    float acc = 0.0f;
+    for (int i = lane; i < H / 8; i += 32) {
+        const uint4 wv = __ldg(w + i);
+        const float4 x0 = __ldg(x + 2 * i), x1 = __ldg(x + 2 * i + 1);
+        const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&wv);
+        const float2 w01 = __bfloat1622float2(b2[0]), w23 = __bfloat1622float2(b2[1]);
+        const float2 w45 = __bfloat1622float2(b2[2]), w67 = __bfloat1622float2(b2[3]);
+        acc += w01.x * x0.x + w01.y * x0.y + w23.x * x0.z + w23.y * x0.w;
+        acc += w45.x * x1.x + w45.y * x1.y + w67.x * x1.z + w67.y * x1.w;
+    }
+    acc = warp_sum_f(acc);
+    unsigned last = 0;
+    if (lane == 0) {
+        p.pr_z[e] = p.pr_b[e] + acc;
+        __threadfence();
+        last = atomicAdd(p.pr_count, 1u) == (unsigned)(E - 1);
+    }
+    if (!__shfl_sync(0xffffffffu, last, 0)) return;
+    __threadfence();
+    // top-k of the predicted logits (value desc, index asc), then prefetch
+    unsigned long long prev = ~0ull;
+    int my_e = -1;
+    for (int j = 0; j < k; ++j) {
+        unsigned long long best = 0ull;
+        for (int i = lane; i < E; i += 32) {
+            const unsigned long long r = ((unsigned long long)fkey(__ldcg(p.pr_z + i)) << 32) | (unsigned)(~(unsigned)i);
+            if (r < prev && r > best) best = r;
+        }
+        const unsigned hi = __reduce_max_sync(0xffffffffu, (unsigned)(best >> 32));
+        const unsigned lo = __reduce_max_sync(0xffffffffu, (unsigned)(best >> 32) == hi ? (unsigned)best : 0u);
+        prev = ((unsigned long long)hi << 32) | lo;
+        if (lane == j) my_e = (int)(~lo);
+    }
+    if (lane < k) p.pr_set[lane] = my_e;
+    constexpr uint32_t CH = 64u << 10;
+    const size_t nch = (p.pr_blob + CH - 1) / CH;
+    for (int j = 0; j < k; ++j) {
+        const int pe = __shfl_sync(0xffffffffu, my_e, j);
+        if (pe < 0 || pe >= E) continue;
+        for (int kd = 0; kd < 3; ++kd) {
+            const uint64_t ent = p.pr_tbl[(size_t)kd * E + pe];
+            if (ent & 1ull) continue;  // cold: read zero-copy by the next layer, not prefetched
+            const uint8_t *base = (const uint8_t *)(uintptr_t)ent;
+            for (size_t c = lane; c < nch; c += 32) {
+                const size_t off = c * CH;
+                const size_t n = p.pr_blob - off < CH ? p.pr_blob - off : CH;
+                l2_prefetch(base + off, (uint32_t)n);
+            }
+        }
+    }
+    if (lane == 0) *p.pr_count = 0u;  // for the next launch
+}
+
 __device__ __forceinline__ void t1_route_gate_up(const FusedParams &p, int *s_e, float *s_w, int *s_uniq, int *s_off,
                                                  int *s_asg, int *s_nu, int *s_npick, float (*sh_h)[32], uint8_t *dsm,
                                                  uint8_t *dpre, int n_dn_items, uint32_t step_clock) {
@@ -1077,6 +1144,17 @@ __device__ __forceinline__ void t1_route_gate_up(const FusedParams &p, int *s_e,
                 p.w_out[lane] = my_w;
             }
         }
+        if (p.pr_mine && blockIdx.x == 0) {
+            // how many of this layer's picks the previous layer predicted
+            bool hit = false;
+            if (lane < k)
+                for (int j = 0; j < k; ++j) hit |= __ldcg(p.pr_mine + j) == my_e;
+            const int hits = __popc(__ballot_sync(0xffffffffu, hit));
+            if (lane == 0) {
+                atomicAdd(p.pr_stats, (unsigned long long)k);
+                atomicAdd(p.pr_stats + 1, (unsigned long long)hits);
+            }
+        }
         if (lane == 0) {
             s_off[k] = k;
             *s_nu = k;
@@ -1110,6 +1188,12 @@ __device__ __forceinline__ void t1_route_gate_up(const FusedParams &p, int *s_e,
         if (blockIdx.x == 0) {
             for (int i = threadIdx.x - 32; i < H; i += 224) g.xq_out[i] = xq_s[i];
             for (int i = threadIdx.x - 32; i < nbx; i += 224) g.xds_out[i] = xds_s[i];
+        }
+        if (p.pr_w) {
+            // the next layer's router on this layer's input: warp w of CTA c
+            // takes expert c + (w - 1) * grid
+            const int e = (int)blockIdx.x + (warp - 1) * (int)gridDim.x;
+            if (e < E) lookahead_predict(p, e, lane);
         }
     }
 

@@ -95,6 +95,17 @@ struct moe_ctx {
     cudaEvent_t ev_pf[2] = {nullptr, nullptr}, ev_pf_free[2] = {nullptr, nullptr};
     int pf_layer[2] = {-1, -1};
     bool pf_map_pending[2] = {false, false};
+    // decode lookahead (batch-1 routed forwards): the routers of the layers;
+    // layer l's kernel applies layer l + 1's router to its input and
+    // prefetches the predicted experts' pool-resident weights into L2
+    bool la_decode = false;
+    __nv_bfloat16 *d_router = nullptr;        // [L][E][H]
+    float *d_rbias = nullptr;                 // [L][E]
+    std::vector<uint8_t> has_router;          // [L]
+    float *d_prz = nullptr;                   // [E] predicted logits (scratch)
+    unsigned *d_prcount = nullptr;            // [1]
+    int32_t *d_prset = nullptr;               // [L][k]: the prediction for layer l
+    unsigned long long *d_prstats = nullptr;  // [2]: predicted picks, of them picked
     // fused small-batch layer kernel
     unsigned *done_gu = nullptr, *exit_count = nullptr;
     size_t fused_smem = 0, fused_smem_rb = 0;
@@ -929,9 +940,28 @@ static int ffn_forward_body(moe_ctx *ctx, int layer, const float *d_x, int n_tok
                 // one routed token: the gate, up and down table rows follow
                 fp.tbl_off = (int)((smem + 15) / 16 * 16);
                 smem = (size_t)fp.tbl_off + (size_t)24 * ctx->E;
+                if (ctx->la_decode && !ctx->shared) {
+                    const int L = ctx->cfg.n_layers, E = ctx->E;
+                    if (layer + 1 < L && ctx->has_router[layer + 1]) {
+                        fp.pr_w = ctx->d_router + (size_t)(layer + 1) * E * H;
+                        fp.pr_b = ctx->d_rbias + (size_t)(layer + 1) * E;
+                        fp.pr_tbl = ctx->d_tbl + (size_t)(layer + 1) * 3 * ctx->Et;
+                        fp.pr_z = ctx->d_prz;
+                        fp.pr_count = ctx->d_prcount;
+                        fp.pr_set = ctx->d_prset + (size_t)(layer + 1) * ctx->k;
+                        fp.pr_stats = ctx->d_prstats;
+                        fp.pr_blob = ctx->blob;
+                    }
+                    if (layer > 0 && ctx->has_router[layer]) {
+                        fp.pr_mine = ctx->d_prset + (size_t)layer * ctx->k;
+                        fp.pr_stats = ctx->d_prstats;
+                    }
+                }
             }
             items = std::max(U * (ctx->F / 32), H / rows);
             grid = std::min(items, ctx->fused_blocks_rb);
+            // the lookahead predictor takes up to 7 experts per CTA (warps 1..7)
+            if (fp.pr_w && 7 * grid < ctx->E) fp.pr_w = nullptr;
         }
         const cudaEvent_t *ev = nullptr;
         if (ctx->timing) {
@@ -1511,6 +1541,10 @@ int moe_cache_reset(moe_ctx *ctx, int global_pool) {
     CK(cudaMemsetAsync(ctx->d_cold, 0, sizeof(unsigned long long), ctx->stream));
     if (ctx->d_use)
         CK(cudaMemsetAsync(ctx->d_use, 0, sizeof(uint32_t) * (size_t)ctx->cfg.n_layers * E, ctx->stream));
+    if (ctx->d_prstats) {
+        CK(cudaMemsetAsync(ctx->d_prstats, 0, sizeof(unsigned long long) * 2, ctx->stream));
+        CK(cudaMemsetAsync(ctx->d_prset, 0xff, sizeof(int32_t) * (size_t)ctx->cfg.n_layers * ctx->k, ctx->stream));
+    }
     CK(cudaStreamSynchronize(ctx->stream));
     for (int b = 0; b < 2; ++b) {
         ctx->pf_layer[b] = -1;
@@ -1554,9 +1588,15 @@ int moe_set_lookahead(moe_ctx *ctx, int enable) {
     CK(cudaSetDevice(ctx->dev));
     if (!enable) {
         ctx->lookahead = false;
+        ctx->la_decode = false;
         return MOE_OK;
     }
-    if (!ctx->gemm_ok) return fail(ctx, MOE_ERR_STATE, "lookahead: no prompt-pass path in this context");
+    // decode: the layers whose routers are set are predicted a layer ahead
+    ctx->la_decode = ctx->d_router != nullptr;
+    if (!ctx->gemm_ok) {
+        if (ctx->la_decode) return MOE_OK;  // no prompt-pass path: decode lookahead only
+        return fail(ctx, MOE_ERR_STATE, "lookahead: no prompt-pass path and no router set");
+    }
     int cap = 0;
     for (int tid = 0; tid < ctx->n_tensors; ++tid) {
         const TensorState &ts = ctx->t[tid];
@@ -1581,6 +1621,52 @@ int moe_set_lookahead(moe_ctx *ctx, int enable) {
         if (!ctx->ev_pf_free[b]) CK(cudaEventCreateWithFlags(&ctx->ev_pf_free[b], cudaEventDisableTiming));
     }
     ctx->lookahead = cap > 0;
+    return MOE_OK;
+}
+
+int moe_set_router(moe_ctx *ctx, int layer, const float *host_w, const float *host_b) {
+    if (!ctx) return fail(nullptr, MOE_ERR_ARG, "null ctx");
+    if (layer < 0 || layer >= ctx->cfg.n_layers || !host_w)
+        return fail(ctx, MOE_ERR_ARG, "set_router: bad layer or null router");
+    if (ctx->H % 8) return fail(ctx, MOE_ERR_ARG, "set_router: hidden must be a multiple of 8");
+    CK(cudaSetDevice(ctx->dev));
+    const int L = ctx->cfg.n_layers, E = ctx->E, H = ctx->H;
+    if (!ctx->d_router) {
+        int rc = sync_all(ctx);
+        if (rc) return rc;
+        if (cudaMalloc(&ctx->d_router, sizeof(__nv_bfloat16) * (size_t)L * E * H) != cudaSuccess ||
+            cudaMalloc(&ctx->d_rbias, sizeof(float) * (size_t)L * E) != cudaSuccess ||
+            cudaMalloc(&ctx->d_prz, sizeof(float) * E) != cudaSuccess ||
+            cudaMalloc(&ctx->d_prcount, sizeof(unsigned)) != cudaSuccess ||
+            cudaMalloc(&ctx->d_prset, sizeof(int32_t) * (size_t)L * ctx->k) != cudaSuccess ||
+            cudaMalloc(&ctx->d_prstats, sizeof(unsigned long long) * 2) != cudaSuccess) {
+            cudaFree(ctx->d_router);
+            cudaFree(ctx->d_rbias);
+            cudaFree(ctx->d_prz);
+            cudaFree(ctx->d_prcount);
+            cudaFree(ctx->d_prset);
+            cudaFree(ctx->d_prstats);
+            ctx->d_router = nullptr;
+            ctx->d_rbias = ctx->d_prz = nullptr;
+            ctx->d_prcount = nullptr;
+            ctx->d_prset = nullptr;
+            ctx->d_prstats = nullptr;
+            return fail(ctx, MOE_ERR_OOM, "set_router: device allocation failed");
+        }
+        CK(cudaMemset(ctx->d_prcount, 0, sizeof(unsigned)));
+        CK(cudaMemset(ctx->d_prset, 0xff, sizeof(int32_t) * (size_t)L * ctx->k));
+        CK(cudaMemset(ctx->d_prstats, 0, sizeof(unsigned long long) * 2));
+        ctx->has_router.assign(L, 0);
+    }
+    std::vector<__nv_bfloat16> w((size_t)E * H);
+    for (size_t i = 0; i < w.size(); ++i) w[i] = __float2bfloat16_rn(host_w[i]);
+    std::vector<float> b(E, 0.0f);
+    if (host_b) memcpy(b.data(), host_b, sizeof(float) * E);
+    CK(cudaStreamSynchronize(ctx->stream));
+    CK(cudaMemcpy(ctx->d_router + (size_t)layer * E * H, w.data(), sizeof(__nv_bfloat16) * w.size(),
+                  cudaMemcpyHostToDevice));
+    CK(cudaMemcpy(ctx->d_rbias + (size_t)layer * E, b.data(), sizeof(float) * E, cudaMemcpyHostToDevice));
+    ctx->has_router[layer] = 1;
     return MOE_OK;
 }
 
@@ -1637,6 +1723,15 @@ int moe_stats(moe_ctx *ctx, moe_stats_t *out) {
     if (!ctx || !out) return fail(ctx, MOE_ERR_ARG, "null argument");
     *out = ctx->stats;
     out->clock = ctx->clock;
+    out->lookahead_predicted = out->lookahead_hits = 0;
+    if (ctx->d_prstats) {
+        CK(cudaSetDevice(ctx->dev));
+        CK(cudaStreamSynchronize(ctx->stream));
+        unsigned long long h[2] = {0, 0};
+        CK(cudaMemcpy(h, ctx->d_prstats, sizeof(h), cudaMemcpyDeviceToHost));
+        out->lookahead_predicted = h[0];
+        out->lookahead_hits = h[1];
+    }
     return MOE_OK;
 }
 
@@ -1677,6 +1772,12 @@ void moe_destroy(moe_ctx *ctx) {
     cudaFree(ctx->tile_rec);
     cudaFree(ctx->done_gu);
     cudaFree(ctx->etbl);
+    cudaFree(ctx->d_router);
+    cudaFree(ctx->d_rbias);
+    cudaFree(ctx->d_prz);
+    cudaFree(ctx->d_prcount);
+    cudaFree(ctx->d_prset);
+    cudaFree(ctx->d_prstats);
     cudaFree(ctx->stage_jobs);
     cudaFree(ctx->stage_n);
     for (int b = 0; b < 2; ++b) {

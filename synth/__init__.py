@@ -28,6 +28,7 @@ STREAM_X = 2
 STREAM_LOGITS = 3
 STREAM_PERM = 4
 STREAM_DRIFT = 5
+STREAM_ROUTER = 6
 
 KIND_GATE, KIND_UP, KIND_DOWN = 0, 1, 2
 Q4_BLOCK_BYTES = 18
@@ -208,6 +209,18 @@ class Workload:
     drift: float = 0.0
     # expert weight format: FMT_Q4 (canonical Q4 blocks), FMT_Q8_0 or FMT_Q5_0
     weight_format: int = FMT_Q4
+    # router model (residual_rho > 0): each step's token runs through a
+    # residual-stream stand-in, x_l = rho x_(l-1) + sqrt(1 - rho^2) xi_l with
+    # x_0, xi_l ~ N(0, I), and layer l's logits are linear in its input,
+    # bias_l + router_scale * R_l x_l (R_l: seeded rows of unit length, so
+    # R_l x_l ~ N(0, 1) per expert; bias_l = the log popularity by rank);
+    # layer l + 1's router applied to x_l then predicts its picks
+    residual_rho: float = 0.0
+    router_scale: float = math.pi / math.sqrt(6.0)
+
+    def __post_init__(self):
+        self._xcache = {}
+        self._rcache = {}
 
     @property
     def tensor_shapes(self):
@@ -260,9 +273,42 @@ class Workload:
         return int(self.capacity[layer])
 
     def x(self, layer: int, step: int, T: int, phase: int = 0) -> np.ndarray:
-        return normal(key(self.seed, STREAM_X, layer, step, phase), (T, self.hidden))
+        if self.residual_rho <= 0.0:
+            return normal(key(self.seed, STREAM_X, layer, step, phase), (T, self.hidden))
+        # residual chain, cached per (step, T, phase) from the last layer asked
+        ck = (step, T, phase)
+        l0, x = self._xcache.get(ck, (-1, None))
+        if l0 > layer:
+            l0, x = -1, None
+        rho = self.residual_rho
+        c = math.sqrt(1.0 - rho * rho)
+        for l in range(l0 + 1, layer + 1):
+            xi = normal(key(self.seed, STREAM_X, l, step, phase), (T, self.hidden))
+            x = xi if l == 0 else (rho * x + c * xi).astype(np.float32)
+        self._xcache = {ck: (layer, x)}
+        return x.copy()
+
+    def router(self, layer: int) -> np.ndarray:
+        """R_l: [E][H] fp32, seeded rows of unit length (router model only)."""
+        if layer not in self._rcache:
+            r = normal(key(self.seed, STREAM_ROUTER, layer), (self.n_experts, self.hidden)).astype(np.float64)
+            r /= np.linalg.norm(r, axis=1, keepdims=True)
+            if len(self._rcache) >= 64:
+                self._rcache.clear()
+            self._rcache[layer] = r.astype(np.float32)
+        return self._rcache[layer]
+
+    def router_bias(self, layer: int) -> np.ndarray:
+        """bias_l[e] = log popularity of e's rank in layer l (router model)."""
+        base = np.empty(self.n_experts, np.float64)
+        base[self.request_perm(layer)] = np.log(self.popularity())
+        return base.astype(np.float32)
 
     def logits(self, layer: int, step: int, T: int, phase: int = 0) -> np.ndarray:
+        if self.residual_rho > 0.0:
+            x = self.x(layer, step, T, phase).astype(np.float64)
+            z = x @ self.router(layer).astype(np.float64).T
+            return (self.router_bias(layer).astype(np.float64)[None, :] + self.router_scale * z).astype(np.float32)
         k = key(self.seed, STREAM_LOGITS, layer, step, phase)
         p = self.popularity()
         if p is None:
@@ -288,6 +334,12 @@ WORKLOADS = {
                      routing="normal", seed=0, phases=[("decode", 4, 1)]),
     "decode_b1_resident": Workload("decode_b1_resident", 2048, 512, 8, 1152, 48, routing="zipf",
                                    zipf_s=1.1, capacity=_c1_capacity(), phases=[("decode", 1, 128)]),
+    # the decode workload with the router model (residual stream, linear
+    # router, rho 0.9): layer l + 1's router on layer l's input predicts
+    # its picks, for lookahead prefetch
+    "decode_b1_resident_router": Workload("decode_b1_resident_router", 2048, 512, 8, 1152, 48, routing="zipf",
+                                          zipf_s=1.1, capacity=_c1_capacity(), phases=[("decode", 1, 128)],
+                                          residual_rho=0.9),
     "decode_b1_pool25": Workload("decode_b1_pool25", 2048, 512, 8, 1152, 48, routing="zipf",
                                  zipf_s=1.1, capacity=[128] * 48, phases=[("decode", 1, 256)]),
     # a 4096-token prompt, then decode, on the 25% pool; the request's expert
