@@ -62,6 +62,8 @@ def parse():
                          "expert resident, or every expert in host memory for decode_layer_cold, Q8_0 weights "
                          "for decode_layer_q8), --launches forwards at batch 1 (routed) or 4096 tokens")
     ap.add_argument("--launches", type=int, default=20)
+    ap.add_argument("--lookahead-steps", type=int, default=64,
+                    help="timed decode steps of each run of the decode lookahead leg (0 skips it)")
     ap.add_argument("--cold-launches", type=int, default=20,
                     help="timed batch-1 forwards of the all-cold layer leg (0 skips it)")
     return ap.parse_args()
@@ -422,6 +424,9 @@ def run_ours(args):
     zc_gbs, ce_gbs = qec.moe_probe_host_read(probe.data_ptr(), probe.numel(), iters=5)
     del probe
     log(f"host link: zero-copy read {zc_gbs:.1f} GB/s, copy engine {ce_gbs:.1f} GB/s")
+    lookahead = None
+    if args.lookahead_steps > 0 and seg is not None:
+        lookahead = run_lookahead_leg(args, qec, synth, torch, log, ctx, stream, resident, blob)
     out = {
         "metric": METRIC, "value": round(tok_per_s, 2), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4), "higher_is_better": True,
@@ -444,6 +449,8 @@ def run_ours(args):
         "clocks": clk,
         "gpu_launches": launches_per_step * args.steps,
     }
+    if lookahead is not None:
+        out["lookahead"] = lookahead
     qec.moe_destroy(ctx)
     del X, LG, Xp, LGp
     link_peak = max(zc_gbs, ce_gbs)
@@ -526,6 +533,93 @@ def run_case(args):
         b = float(np.median(ms[2:]))
         res["host_link_gbs"] = round(k * 3 * wl.tensor_bytes(0) / (b * 1e-3) / 1e9, 1)
     print(json.dumps(res), flush=True)
+
+
+def run_lookahead_leg(args, qec, synth, torch, log, ctx, stream, resident, blob):
+    """Decode lookahead prefetch on the decode model (same weights and pool
+    seeding as the headline workload) with the router model's inputs
+    (decode_b1_resident_router: residual stream x_l = 0.9 x_(l-1) + ..., logits
+    linear in x_l): the routers of all layers registered, then
+    args.lookahead_steps batch-1 decode steps (48 routed layer launches in a
+    CUDA graph + the promotion pass) from the seeded cache state, lookahead
+    off and on, alternated twice.  Tokens/s from CUDA events around the timed
+    steps, the resident layers' segment time, and the prediction hit rate."""
+    wl = synth.WORKLOADS["decode_b1_resident_router"]
+    L, H, E, k = wl.n_layers, wl.hidden, wl.n_experts, wl.top_k
+    T = 1
+    t0 = time.time()
+    for l in range(L):
+        qec.moe_set_router(ctx, l, wl.router_scale * wl.router(l), wl.router_bias(l))
+    W, n = args.warmup, args.lookahead_steps
+    Xh, LGh = make_inputs(wl, W + n, T)
+    log(f"lookahead leg: routers and {W + n} steps of inputs in {time.time() - t0:.1f}s")
+    X, LG = torch.from_numpy(Xh).cuda(), torch.from_numpy(LGh).cuda()
+    sp = stream.cuda_stream
+    xin = torch.empty((L, T, H), device="cuda")
+    lin = torch.empty((L, T, E), device="cuda")
+    idx = torch.empty((L, T, k), dtype=torch.int32, device="cuda")
+    w = torch.empty((L, T, k), device="cuda")
+    y = torch.empty((L, T, H), device="cuda")
+    seg = (torch.cuda.Event(enable_timing=True, external=True), torch.cuda.Event(enable_timing=True, external=True))
+
+    def layers(mark=False):
+        for l in range(L):
+            if mark and l == resident[0]:
+                seg[0].record(stream)
+            qec.moe_ffn_forward_routed(ctx, l, xin[l], lin[l], T, idx[l], w[l], y[l], sp)
+            if mark and l == resident[-1]:
+                seg[1].record(stream)
+
+    runs = {"off": [], "on": []}
+    for mode in ("off", "on", "off", "on"):
+        qec.moe_set_lookahead(ctx, mode == "on")
+        with torch.cuda.stream(stream):
+            xin.copy_(X[0])
+            lin.copy_(LG[0])
+        layers()
+        stream.synchronize()
+        qec.miss_drain(ctx)
+        qec.moe_cache_reset(ctx, False)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            layers(mark=True)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        seg_ms = 0.0
+        s0 = None
+        for s in range(W + n):
+            if s == W:
+                stream.synchronize()
+                s0 = qec.moe_stats(ctx)
+                e0.record(stream)
+            with torch.cuda.stream(stream):
+                xin.copy_(X[s])
+                lin.copy_(LG[s])
+                graph.replay()
+            qec.cache_step(ctx, T)
+            if s >= W:
+                seg_ms += seg[0].elapsed_time(seg[1])
+        e1.record(stream)
+        stream.synchronize()
+        ms = e0.elapsed_time(e1)
+        s1 = qec.moe_stats(ctx)
+        pred = s1["lookahead_predicted"] - s0["lookahead_predicted"]
+        hits = s1["lookahead_hits"] - s0["lookahead_hits"]
+        r = {"tokens_per_s": round(n * T / (ms * 1e-3), 1), "ms_per_step": round(ms / n, 4),
+             "resident_layer_us": round(1e3 * seg_ms / (n * len(resident)), 3),
+             "prediction_hit_rate": round(hits / pred, 4) if pred else None}
+        runs[mode].append(r)
+        log(f"lookahead leg, {mode}: {r}")
+        del graph
+    qec.moe_set_lookahead(ctx, False)
+    out = {"workload": (f"{wl.name}: the headline model's weights and pool seeding; inputs from the router model "
+                        f"(residual stream rho {wl.residual_rho}, logits = log popularity + "
+                        f"{wl.router_scale:.4f} R_l x_l); {n} timed batch-1 decode steps per run, CUDA graph, "
+                        f"promotion pass after each step, runs from the seeded state"),
+           "off": runs["off"][-1], "on": runs["on"][-1],
+           "tokens_per_s_runs": {m: [r["tokens_per_s"] for r in v] for m, v in runs.items()},
+           "prediction": f"top-{k} of layer l+1's router on layer l's input, pool-resident weights prefetched into L2"}
+    out["speedup"] = round(out["on"]["tokens_per_s"] / out["off"]["tokens_per_s"], 4)
+    return out
 
 
 def run_cold_layer_leg(args, qec, synth, torch, log, link_peak):
