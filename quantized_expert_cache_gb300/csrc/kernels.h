@@ -74,6 +74,7 @@ struct FusedParams {
     const uint64_t *pr_tbl;       // [3][E] the next layer's gate, up and down table rows
     float *pr_z;                  // [E] scratch: predicted logits
     unsigned *pr_count;           // [1] predicted logits written (zero between launches)
+    unsigned *pr_flag;            // [1] the prediction is out (zero between launches)
     int32_t *pr_set;              // [k] this launch's prediction for the next layer
     const int32_t *pr_mine;       // [k] the previous layer's prediction for this one (or null)
     unsigned long long *pr_stats; // [2] predicted picks, of them actually picked

@@ -1012,8 +1012,9 @@ __device__ __forceinline__ void bar_arrive_n(int id, int n) { asm volatile("bar.
 // lookahead prefetch: layer L+1's router predicts its experts from layer L's
 // input, so their reads start a layer early).  Warp-level dot of one router
 // row (bf16) with the layer's input x (fp32); the warp that writes the last
-// predicted logit of the launch takes their top-k and prefetches the picked
-// experts' pool-resident gate, up and down blobs into L2.
+// predicted logit of the launch takes their top-k and publishes it; every
+// CTA then prefetches a share of the picked experts' pool-resident gate, up
+// and down blobs into L2 (lookahead_prefetch).
 __device__ __forceinline__ void l2_prefetch(const void *p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
@@ -1056,23 +1057,33 @@ __device__ __forceinline__ void lookahead_predict(const FusedParams &p, int e, i
         if (lane == j) my_e = (int)(~lo);
     }
     if (lane < k) p.pr_set[lane] = my_e;
-    constexpr uint32_t CH = 64u << 10;
-    const size_t nch = (p.pr_blob + CH - 1) / CH;
-    for (int j = 0; j < k; ++j) {
-        const int pe = __shfl_sync(0xffffffffu, my_e, j);
-        if (pe < 0 || pe >= E) continue;
-        for (int kd = 0; kd < 3; ++kd) {
-            const uint64_t ent = p.pr_tbl[(size_t)kd * E + pe];
-            if (ent & 1ull) continue;  // cold: read zero-copy by the next layer, not prefetched
-            const uint8_t *base = (const uint8_t *)(uintptr_t)ent;
-            for (size_t c = lane; c < nch; c += 32) {
-                const size_t off = c * CH;
-                const size_t n = p.pr_blob - off < CH ? p.pr_blob - off : CH;
-                l2_prefetch(base + off, (uint32_t)n);
-            }
-        }
+    __syncwarp();
+    if (lane == 0) {
+        *p.pr_count = 0u;  // for the next launch
+        __threadfence();
+        atomicExch(p.pr_flag, 1u);  // the prediction is out
     }
-    if (lane == 0) *p.pr_count = 0u;  // for the next launch
+}
+
+// This CTA's share of the L2 prefetch of the predicted experts (64 KB
+// chunks of the pool-resident gate, up and down blobs, spread over every
+// thread of the grid); nothing when the prediction is not out yet.
+__device__ void lookahead_prefetch(const FusedParams &p) {
+    if (!ld_acquire(p.pr_flag)) return;
+    const int E = p.g.cv.E, k = p.g.k;
+    constexpr uint32_t CH = 64u << 10;
+    const int nch = (int)((p.pr_blob + CH - 1) / CH);
+    const int total = k * 3 * nch;
+    for (int c = (int)blockIdx.x + (int)gridDim.x * (int)threadIdx.x; c < total; c += (int)(gridDim.x * blockDim.x)) {
+        const int j = c / (3 * nch), rem = c - j * 3 * nch, kd = rem / nch, ci = rem - kd * nch;
+        const int pe = __ldcg(p.pr_set + j);
+        if (pe < 0 || pe >= E) continue;
+        const uint64_t ent = p.pr_tbl[(size_t)kd * E + pe];
+        if (ent & 1ull) continue;  // cold: read zero-copy by the next layer, not prefetched
+        const size_t off = (size_t)ci * CH;
+        const size_t n = p.pr_blob - off < CH ? p.pr_blob - off : CH;
+        l2_prefetch((const uint8_t *)(uintptr_t)ent + off, (uint32_t)n);
+    }
 }
 
 __device__ __forceinline__ void t1_route_gate_up(const FusedParams &p, int *s_e, float *s_w, int *s_uniq, int *s_off,
@@ -1488,6 +1499,7 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
     issue_prefetch();
 
     // ---------------- down items
+    if (RB && p.pr_w) lookahead_prefetch(p);  // the next layer's predicted experts into L2
     if (RB) {
         // Row-block mode: item rb = rows [rb R, rb R + R) of H for every used
         // expert, (expert, row) pairs spread over the CTA's lanes (LD lanes a
@@ -1633,6 +1645,7 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
         if (prev == gridDim.x - 1) {
             for (int u = 0; u < nu; ++u) p.done_gu[RB ? u : s_uniq[u]] = 0u;
             *p.exit_count = 0u;
+            if (p.pr_w) *p.pr_flag = 0u;  // every CTA is past its prefetch
             __threadfence();
         }
     }

@@ -103,7 +103,7 @@ struct moe_ctx {
     float *d_rbias = nullptr;                 // [L][E]
     std::vector<uint8_t> has_router;          // [L]
     float *d_prz = nullptr;                   // [E] predicted logits (scratch)
-    unsigned *d_prcount = nullptr;            // [1]
+    unsigned *d_prcount = nullptr;            // [2]: logits written, prediction out
     int32_t *d_prset = nullptr;               // [L][k]: the prediction for layer l
     unsigned long long *d_prstats = nullptr;  // [2]: predicted picks, of them picked
     // fused small-batch layer kernel
@@ -948,6 +948,7 @@ static int ffn_forward_body(moe_ctx *ctx, int layer, const float *d_x, int n_tok
                         fp.pr_tbl = ctx->d_tbl + (size_t)(layer + 1) * 3 * ctx->Et;
                         fp.pr_z = ctx->d_prz;
                         fp.pr_count = ctx->d_prcount;
+                        fp.pr_flag = ctx->d_prcount + 1;
                         fp.pr_set = ctx->d_prset + (size_t)(layer + 1) * ctx->k;
                         fp.pr_stats = ctx->d_prstats;
                         fp.pr_blob = ctx->blob;
@@ -1637,7 +1638,7 @@ int moe_set_router(moe_ctx *ctx, int layer, const float *host_w, const float *ho
         if (cudaMalloc(&ctx->d_router, sizeof(__nv_bfloat16) * (size_t)L * E * H) != cudaSuccess ||
             cudaMalloc(&ctx->d_rbias, sizeof(float) * (size_t)L * E) != cudaSuccess ||
             cudaMalloc(&ctx->d_prz, sizeof(float) * E) != cudaSuccess ||
-            cudaMalloc(&ctx->d_prcount, sizeof(unsigned)) != cudaSuccess ||
+            cudaMalloc(&ctx->d_prcount, sizeof(unsigned) * 2) != cudaSuccess ||
             cudaMalloc(&ctx->d_prset, sizeof(int32_t) * (size_t)L * ctx->k) != cudaSuccess ||
             cudaMalloc(&ctx->d_prstats, sizeof(unsigned long long) * 2) != cudaSuccess) {
             cudaFree(ctx->d_router);
@@ -1653,7 +1654,7 @@ int moe_set_router(moe_ctx *ctx, int layer, const float *host_w, const float *ho
             ctx->d_prstats = nullptr;
             return fail(ctx, MOE_ERR_OOM, "set_router: device allocation failed");
         }
-        CK(cudaMemset(ctx->d_prcount, 0, sizeof(unsigned)));
+        CK(cudaMemset(ctx->d_prcount, 0, sizeof(unsigned) * 2));
         CK(cudaMemset(ctx->d_prset, 0xff, sizeof(int32_t) * (size_t)L * ctx->k));
         CK(cudaMemset(ctx->d_prstats, 0, sizeof(unsigned long long) * 2));
         ctx->has_router.assign(L, 0);

@@ -59,6 +59,7 @@ def test_decode_lookahead_matches_plain_run(H, F, E, k, L, cap):
                     used[3 * l + kind] = ib.cpu().numpy().ravel().tolist()
             qec.cache_step(a.ctx, 1)
             qec.cache_step(b.ctx, 1)
+            a.policy.step(1, used)
             b.policy.step(1, used)
         sa, sb = qec.moe_stats(a.ctx), qec.moe_stats(b.ctx)
         for key in ("hits", "misses", "admissions", "evictions", "cold_bytes"):
@@ -70,10 +71,11 @@ def test_decode_lookahead_matches_plain_run(H, F, E, k, L, cap):
         for tid in range(3 * L):
             xa = qec.moe_cache_snapshot(a.ctx, tid, a.E, a.spt)
             xb = qec.moe_cache_snapshot(b.ctx, tid, b.E, b.spt)
-            for key in ("tbl", "slot_of", "last_seen", "owner", "stamps"):
+            for key in ("slot_of", "last_seen", "owner", "stamps"):
                 assert np.array_equal(xa[key], xb[key]), (tid, key)
             o = b.policy.snapshot(tid)
             assert xb["slot_of"].tolist() == o["slot_of"], tid
+            assert np.array_equal(xa["tbl"], a.expected_tbl(tid)) and np.array_equal(xb["tbl"], b.expected_tbl(tid))
     finally:
         a.close()
         b.close()
