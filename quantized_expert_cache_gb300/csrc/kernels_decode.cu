@@ -1042,17 +1042,26 @@ __device__ __forceinline__ void lookahead_predict(const FusedParams &p, int e, i
     }
     if (!__shfl_sync(0xffffffffu, last, 0)) return;
     __threadfence();
-    // top-k of the predicted logits (value desc, index asc), then prefetch
+    // top-k of the predicted logits (value desc, index asc): the logits are
+    // read once into registers (16 per lane; E <= 512 on this path)
+    unsigned long long rk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const int e2 = lane + 32 * i;
+        rk[i] = e2 < E ? ((unsigned long long)fkey(__ldcg(p.pr_z + e2)) << 32) | (unsigned)(~(unsigned)e2) : 0ull;
+    }
     unsigned long long prev = ~0ull;
     int my_e = -1;
     for (int j = 0; j < k; ++j) {
-        unsigned long long best = 0ull;
-        for (int i = lane; i < E; i += 32) {
-            const unsigned long long r = ((unsigned long long)fkey(__ldcg(p.pr_z + i)) << 32) | (unsigned)(~(unsigned)i);
-            if (r < prev && r > best) best = r;
-        }
-        const unsigned hi = __reduce_max_sync(0xffffffffu, (unsigned)(best >> 32));
-        const unsigned lo = __reduce_max_sync(0xffffffffu, (unsigned)(best >> 32) == hi ? (unsigned)best : 0u);
+        unsigned long long c[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) c[i] = rk[i] < prev ? rk[i] : 0ull;
+#pragma unroll
+        for (int w2 = 8; w2 > 0; w2 >>= 1)
+#pragma unroll
+            for (int i = 0; i < w2; ++i) c[i] = umax64(c[i], c[i + w2]);
+        const unsigned hi = __reduce_max_sync(0xffffffffu, (unsigned)(c[0] >> 32));
+        const unsigned lo = __reduce_max_sync(0xffffffffu, (unsigned)(c[0] >> 32) == hi ? (unsigned)c[0] : 0u);
         prev = ((unsigned long long)hi << 32) | lo;
         if (lane == j) my_e = (int)(~lo);
     }
