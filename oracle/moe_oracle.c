@@ -40,10 +40,13 @@
  *  Per 32 weights that is 18 bytes, as for Q4.  4 = Q6_K, another K-quant:
  *  super-blocks of 256 weights = 16 sub-blocks of 16 with a signed 8-bit
  *  scale sc_j each, one binary16 scale d and 6-bit codes q,
- *  w = d * sc_j * (q - 32).  Reading of the 210-byte layout: 128 bytes of
- *  low nibbles (byte t: element t in the low, element t + 128 in the high
- *  nibble), 64 bytes of high bit pairs (byte u, bits 2m..2m+1: element
- *  u + 64 m), the 16 scales, then d.
+ *  w = d * sc_j * (q - 32).  The 210-byte layout is the one the format is
+ *  published with (the pages name Q6_K but print no layout): 128 bytes of
+ *  low nibbles ql, 64 bytes of high bit pairs qh, the 16 scales, then d;
+ *  each 128-weight half n owns ql[64n .. 64n + 63] and qh[32n .. 32n + 31],
+ *  and its element 32m + l (m = 0..3, l < 32) keeps its low four bits in
+ *  ql[64n + l + 32 (m & 1)] (the low nibble for m < 2, the high one for
+ *  m >= 2) and its high two bits in bits 2m..2m+1 of qh[32n + l].
  *
  * Readings where the pages are silent (each listed in the design notes):
  *  - top-k order is (logit descending, expert index ascending): ties go to
@@ -89,11 +92,14 @@ static size_t orc_row_bytes(int fmt, int nb) {
     return (size_t)nb * orc_bbytes(fmt);
 }
 
-/* Q6_K: 6-bit code of element i (0..255) of a super-block. */
+/* Q6_K: 6-bit code of element i (0..255) of a super-block: half n = i / 128,
+ * quarter m of that half, position l in the quarter. */
 static int orc_k6_code(const uint8_t *sb, int i) {
     const uint8_t *ql = sb, *qh = sb + 128;
-    const int lo = i < 128 ? (ql[i] & 15) : (ql[i - 128] >> 4);
-    const int hi = (qh[i % 64] >> (2 * (i / 64))) & 3;
+    const int n = i / 128, m = (i % 128) / 32, l = i % 32;
+    const uint8_t lb = ql[64 * n + 32 * (m & 1) + l];
+    const int lo = m < 2 ? (lb & 15) : (lb >> 4);
+    const int hi = (qh[32 * n + l] >> (2 * m)) & 3;
     return lo | (hi << 4);
 }
 

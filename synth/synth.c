@@ -211,8 +211,9 @@ void synth_q4k_blocks(uint64_t key, uint8_t *out, size_t n_super, double dlo, do
 }
 
 /*
- * Canonical Q6_K super-blocks of 256 weights, 210 bytes each: 192 uniform
- * bytes of 6-bit codes (ql, qh), 16 signed scales ~ U{-64..63}, then a
+ * Q6_K super-blocks of 256 weights in the published block layout, 210 bytes
+ * each: 192 uniform bytes of 6-bit codes (ql, qh: every code equally likely
+ * whatever the element order), 16 signed scales ~ U{-64..63}, then a
  * binary16 d ~ U(dlo, dhi).
  */
 void synth_q6k_blocks(uint64_t key, uint8_t *out, size_t n_super, double dlo, double dhi) {

@@ -43,8 +43,10 @@ C_MUTANTS = [
     ("binary16 truncation", "double r = nearbyint(a / quantum); /* default rounding: ties to even */",
      "double r = floor(a / quantum);"),
     ("softmax over all logits", "if (renorm) {", "if (!renorm) {"),
-    ("q6k high pair index", "const int hi = (qh[i % 64] >> (2 * (i / 64))) & 3;",
-     "const int hi = (qh[i / 4] >> (2 * (i % 4))) & 3;"),
+    ("q6k high pair index", "const int hi = (qh[32 * n + l] >> (2 * m)) & 3;",
+     "const int hi = (qh[i % 64] >> (2 * (i / 64))) & 3;"),
+    ("q6k low nibble byte", "const uint8_t lb = ql[64 * n + 32 * (m & 1) + l];",
+     "const uint8_t lb = ql[64 * n + 32 * (m >> 1) + l];"),
     ("q6k offset 31", "t += (int32_t)(orc_k6_code(sb, e) - 32) * (int32_t)qa[e];",
      "t += (int32_t)(orc_k6_code(sb, e) - 31) * (int32_t)qa[e];"),
 ]

@@ -589,12 +589,19 @@ def test_generators_of_every_format_are_range_and_thread_independent(fmt):
 # ---------------------------------------------------------------- Q6_K weights
 def _np_q6k(sb):
     """Independent Q6_K decode with numpy: [..., 210] -> codes q [..., 256],
-    signed scales [..., 16], d."""
+    signed scales [..., 16], d.  Per 128-weight half: ql bytes 0..31 give the
+    low nibbles of quarter 0 (low) and 2 (high), bytes 32..63 those of
+    quarters 1 and 3; qh byte l gives the high pairs of element l of every
+    quarter (bits 0-1, 2-3, 4-5, 6-7 for quarters 0..3)."""
     sb = np.asarray(sb, np.uint8)
-    ql = sb[..., 0:128].astype(np.int64)
-    qh = sb[..., 128:192].astype(np.int64)
-    lo = np.concatenate([ql & 15, ql >> 4], axis=-1)                       # elements 0..127, 128..255
-    hi = np.concatenate([(qh >> (2 * m)) & 3 for m in range(4)], axis=-1)  # elements u + 64 m
+    lo_parts, hi_parts = [], []
+    for n in range(2):
+        ql = sb[..., 64 * n:64 * n + 64].astype(np.int64)
+        qh = sb[..., 128 + 32 * n:128 + 32 * n + 32].astype(np.int64)
+        lo_parts += [ql[..., 0:32] & 15, ql[..., 32:64] & 15, ql[..., 0:32] >> 4, ql[..., 32:64] >> 4]
+        hi_parts += [(qh >> (2 * m)) & 3 for m in range(4)]
+    lo = np.concatenate(lo_parts, axis=-1)
+    hi = np.concatenate(hi_parts, axis=-1)
     sc = np.ascontiguousarray(sb[..., 192:208]).view(np.int8).astype(np.int64)
     d = np.ascontiguousarray(sb[..., 208:210]).view(np.float16)[..., 0].astype(np.float64)
     return lo | (hi << 4), sc, d
