@@ -69,7 +69,7 @@ typedef struct moe_cfg {
     int32_t renorm_topk;        /* 1: weights = softmax over the k selected */
     int32_t poll_timeout_ms;    /* host poll limit in cache_step (0 = 10 s) */
     int32_t device;             /* CUDA device ordinal */
-    int32_t weight_format;      /* MOE_FMT_Q4_0 (0), _Q8_0 (1), _Q5_0 (2) or _Q4_K (3), every tensor */
+    int32_t weight_format;      /* MOE_FMT_Q4_0 (0), _Q8_0 (1), _Q5_0 (2), _Q4_K (3) or _Q6_K (4), every tensor */
     int32_t shared_experts;     /* 1: every layer has one shared expert (register_shared_expert), E <= 4095 */
 } moe_cfg;
 
@@ -91,12 +91,22 @@ typedef struct moe_cfg {
  *   (chunk c of 32: sub-block 2c in the low nibbles, 2c+1 in the high);
  *   w = d * sc_j * q - dmin * m_j (a K-quant format of those kernels; same
  *   reading of the layout).  Needs hidden and ffn multiples of 256.
- * Q8_0, Q5_0 and Q4_K contexts run every forward through the mat-vec kernels
- * (no fused single-launch layer, no tensor-core prompt path, no lookahead). */
+ * Q6_K: super-blocks of 256 weights (16 sub-blocks of 16), 210 bytes in the
+ *   layout the format is published with: 128 bytes ql, 64 bytes qh, 16
+ *   signed 8-bit scales sc_j, binary16 d; in 128-weight half n, element
+ *   32m + l (m = 0..3) has its low 4 bits in ql[64n + 32(m & 1) + l] (low
+ *   nibble for m < 2, high for m >= 2) and its high 2 bits in bits 2m..2m+1
+ *   of qh[32n + l]; w = d * sc_j * (q - 32), j = element / 16 (another
+ *   K-quant of those kernels; the pages print no layout).  Needs hidden and
+ *   ffn multiples of 256.
+ * Q8_0, Q5_0, Q4_K and Q6_K contexts run every forward through the mat-vec
+ * kernels (no fused single-launch layer, no tensor-core prompt path, no
+ * lookahead). */
 #define MOE_FMT_Q4_0 0
 #define MOE_FMT_Q8_0 1
 #define MOE_FMT_Q5_0 2
 #define MOE_FMT_Q4_K 3
+#define MOE_FMT_Q6_K 4
 
 typedef struct moe_stats_t {
     uint64_t steps;        /* cache_step calls */
@@ -206,6 +216,37 @@ int moe_ffn_forward(moe_ctx *ctx, int layer, const float *d_x, int n_tokens, con
  */
 int moe_ffn_forward_routed(moe_ctx *ctx, int layer, const float *d_x, const float *d_logits, int n_tokens,
                            int32_t *d_idx, float *d_w, float *d_y, void *stream);
+
+/*
+ * Expert shard (neurall/llama.cpp README, "More GPUs": every GPU keeps its
+ * own expert cache in its own memory; the pages do not say how experts are
+ * split, and this library's reading is expert parallelism: GPU r holds a
+ * contiguous range of every layer's experts, so the GPUs cache disjoint
+ * experts).  After this call the context holds experts
+ * [expert_base, expert_base + n_experts) of layers with n_route experts:
+ * its tensors are registered with those n_experts experts only (local id =
+ * global id - expert_base, which is also the expert field of its miss keys
+ * and the index of its tables and seed orders); route_topk and the routed
+ * forward take n_route logits per token and write global ids; every forward
+ * takes global ids in [0, n_route) and leaves out the assignments whose
+ * expert is outside the range: it reads, logs, stamps and counts nothing for
+ * them, and y[t] = sum over this range's j of d_w[t][j] * o (0 when none),
+ * the rank's partial sum; the sum over every shard is the layer's output.
+ * (0, n_experts) is the unsharded default.  Not with shared_experts.
+ * Errors: MOE_ERR_ARG (range), MOE_ERR_STATE (shared experts).
+ */
+int moe_set_expert_shard(moe_ctx *ctx, int expert_base, int n_route);
+
+/*
+ * moe_ffn_forward over n_rows token rows that are part of a step of
+ * step_tokens tokens (step_tokens >= n_rows): an expert-parallel rank that
+ * receives only the rows routed to its experts stamps its pool hits with the
+ * clock of the whole step (clock + step_tokens), as a rank that saw every
+ * token would, and the caller passes step_tokens to cache_step.  Otherwise
+ * as moe_ffn_forward.  Errors: as moe_ffn_forward.
+ */
+int moe_ffn_forward_rows(moe_ctx *ctx, int layer, const float *d_x, int n_rows, const int32_t *d_idx,
+                         const float *d_w, float *d_y, int step_tokens, void *stream);
 
 /*
  * Promotion pass between steps (Zapdev-labs/a6000-custom-kernels:
@@ -464,9 +505,9 @@ int moe_debug_timing_read(moe_ctx *ctx, double *gate_up_ms, double *down_ms);
 /*
  * One routed-expert FFN layer that allocates nothing (no counterpart on the
  * source pages: this entry point exists for callers that cannot allocate
- * device memory when they run a layer, such as code running while a CUDA
- * graph is captured in a mode that forbids allocation, or processes whose
- * device memory is entirely reserved by another allocator).  It computes what
+ * device memory when they run a layer, such as processes whose device memory
+ * is entirely reserved by another allocator, or hosts that forbid device
+ * allocation after start-up).  It computes what
  * moe_ffn_forward computes for a small batch, with the caller's expert tables
  * instead of a context: d_tbl holds 3 rows of n_experts uint64 entries
  * (gate, up, down), each the device address of one Q4_0 expert blob in the
@@ -481,7 +522,7 @@ int moe_debug_timing_read(moe_ctx *ctx, double *gate_up_ms, double *down_ms);
  * exceeds 8 MiB.  Limits: n_tokens <= 32, n_tokens*top_k <= 256, hidden a
  * multiple of the down row block (64 for ffn/32 <= 40, else 32).  The first
  * call on a device looks up the array's device address and configures the
- * kernel (make it before any stream capture); later calls on that device
+ * kernel; later calls on that device
  * (and shape) only clear the parts of the array that must start at zero and
  * launch one kernel.  All calls share the array and each leaves its contents
  * behind, so calls that overlap on the GPU (other streams, other host

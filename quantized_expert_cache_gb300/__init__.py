@@ -23,7 +23,7 @@ MOE_OK = 0
 ERRORS = {-1: "MOE_ERR_ARG", -2: "MOE_ERR_OOM", -3: "MOE_ERR_CUDA", -4: "MOE_ERR_NOT_PINNED",
           -5: "MOE_ERR_TIMEOUT", -6: "MOE_ERR_CAPACITY", -7: "MOE_ERR_STATE", -8: "MOE_ERR_FAULT"}
 KIND_GATE, KIND_UP, KIND_DOWN = 0, 1, 2
-FMT_Q4_0, FMT_Q8_0, FMT_Q5_0, FMT_Q4_K = 0, 1, 2, 3
+FMT_Q4_0, FMT_Q8_0, FMT_Q5_0, FMT_Q4_K, FMT_Q6_K = 0, 1, 2, 3, 4
 
 
 class MoeError(RuntimeError):
@@ -53,6 +53,8 @@ SIGNATURES = {
     "route_topk": (_i32, [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp]),
     "moe_ffn_forward": (_i32, [_vp, _i32, _vp, _i32, _vp, _vp, _vp, _vp]),
     "moe_ffn_forward_routed": (_i32, [_vp, _i32, _vp, _vp, _i32, _vp, _vp, _vp, _vp]),
+    "moe_set_expert_shard": (_i32, [_vp, _i32, _i32]),
+    "moe_ffn_forward_rows": (_i32, [_vp, _i32, _vp, _i32, _vp, _vp, _vp, _i32, _vp]),
     "cache_step": (_i32, [_vp, _i32]),
     "miss_drain": (_i32, [_vp, _vp, _sz, ctypes.POINTER(_sz)]),
     "moe_pool_borrow": (_i32, [_vp, _i32, ctypes.POINTER(_vp), ctypes.POINTER(_sz)]),
@@ -178,6 +180,15 @@ def moe_ffn_forward(ctx, layer, x, n_tokens, idx, w, y, stream=None):
 def moe_ffn_forward_routed(ctx, layer, x, logits, n_tokens, idx, w, y, stream=None):
     return _check(ctx, load().moe_ffn_forward_routed(ctx, layer, _dev(x), _dev(logits), n_tokens, _dev(idx), _dev(w),
                                                      _dev(y), _stream(stream)))
+
+
+def moe_set_expert_shard(ctx, expert_base, n_route):
+    return _check(ctx, load().moe_set_expert_shard(ctx, expert_base, n_route))
+
+
+def moe_ffn_forward_rows(ctx, layer, x, n_rows, idx, w, y, step_tokens, stream=None):
+    return _check(ctx, load().moe_ffn_forward_rows(ctx, layer, _dev(x), n_rows, _dev(idx), _dev(w), _dev(y),
+                                                   step_tokens, _stream(stream)))
 
 
 def cache_step(ctx, n_tokens):

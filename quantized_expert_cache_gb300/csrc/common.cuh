@@ -27,17 +27,29 @@ __host__ __device__ inline size_t blob_bytes(int rows, int nb) { return (size_t)
 // bytes as Q4 plus a 32-bit word of fifth bits, w = d (q - 16)).  Blob
 // layout, N = rows x nb blocks: [codes: N x 16 or 32 B][Q5_0 only: fifth
 // bits, N x 4 B][scales: N x binary16]; code_bytes counts both code planes.
-// Q4_K (256-weight super-blocks with 6-bit sub-block scales and mins) is
-// repacked per 32-weight sub-block: Q4-order nibbles, and the exact fp32 pair
-// (d * sc, dmin * m) in the scale plane (8 bytes per block instead of 2).
-constexpr int kFmtQ4 = 0, kFmtQ8 = 1, kFmtQ5 = 2, kFmtQ4K = 3;
-__host__ __device__ constexpr int code_bytes(int fmt) { return fmt == kFmtQ8 ? 32 : fmt == kFmtQ5 ? 20 : 16; }
-__host__ __device__ constexpr int scale_bytes(int fmt) { return fmt == kFmtQ4K ? 8 : 2; }
+// The K-quants keep one header per 256-weight super-block (8 blocks):
+// Q4_K (6-bit sub-block scales and mins) is repacked per 32-weight sub-block
+// into Q4-order nibbles, and its scale plane holds the super-block's 16-byte
+// header as stored (d, dmin, the 12 bytes of packed scales and mins).  Q6_K
+// (16-weight sub-blocks with signed 8-bit scales, 6-bit codes) keeps per
+// block the low nibbles in Q4 order (16 B), the high bit pairs (8 B: word h,
+// byte b, bits 2i..2i+1 = element 16h + 4i + b) and the two sub-block scales
+// (2 B) in its code planes, and the super-block's binary16 d in its scale
+// plane.  Both take the canonical bytes per weight (18 and 26.25 per 32).
+constexpr int kFmtQ4 = 0, kFmtQ8 = 1, kFmtQ5 = 2, kFmtQ4K = 3, kFmtQ6K = 4;
+__host__ __device__ constexpr int code_bytes(int fmt) {
+    return fmt == kFmtQ8 ? 32 : fmt == kFmtQ5 ? 20 : fmt == kFmtQ6K ? 26 : 16;
+}
 __host__ __device__ inline size_t blob_scales_offset_fmt(int fmt, int rows, int nb) {
     return (size_t)rows * nb * code_bytes(fmt);
 }
+// bytes of the scale plane of n blocks (n a multiple of 8 for the K-quants)
+__host__ __device__ inline size_t scale_plane_bytes(int fmt, size_t n) {
+    return fmt == kFmtQ4K ? n / 8 * 16 : fmt == kFmtQ6K ? n / 8 * 2 : n * 2;
+}
 __host__ __device__ inline size_t blob_bytes_fmt(int fmt, int rows, int nb) {
-    return (size_t)rows * nb * (code_bytes(fmt) + scale_bytes(fmt));
+    const size_t n = (size_t)rows * nb;
+    return n * code_bytes(fmt) + scale_plane_bytes(fmt, n);
 }
 
 // Per-activation-block data kept next to the int8 codes: the binary16 scale
@@ -177,12 +189,65 @@ struct WScale {
 };
 template <>
 struct WScale<kFmtQ4K> {
-    float2 sm;
+    float sc, mn;  // d * sc_j and dmin * m_j of the block's sub-block j (exact in fp32)
+    // block i is sub-block j = i mod 8 of super-block i / 8 (rows hold whole
+    // super-blocks); the 8 lanes reading one super-block share its header
     __device__ __forceinline__ void load(const uint8_t *scales, size_t i) {
-        sm = __ldcs((const float2 *)scales + i);
+        const uint4 h = __ldg((const uint4 *)scales + i / 8);
+        const int j = (int)(i & 7);
+        // the 12 packed bytes b[0..11] = header bytes 4..15
+        const unsigned long long b07 = (unsigned long long)h.y | ((unsigned long long)h.z << 32);
+        auto byte = [&](int k) { return k < 8 ? (int)((b07 >> (8 * k)) & 255u) : (int)((h.w >> (8 * (k - 8))) & 255u); };
+        int s6, m6;
+        if (j < 4) {
+            s6 = byte(j) & 63;
+            m6 = byte(j + 4) & 63;
+        } else {
+            s6 = (byte(j + 4) & 15) | ((byte(j - 4) >> 6) << 4);
+            m6 = (byte(j + 4) >> 4) | ((byte(j) >> 6) << 4);
+        }
+        sc = __half2float(__ushort_as_half((unsigned short)(h.x & 0xffffu))) * (float)s6;
+        mn = __half2float(__ushort_as_half((unsigned short)(h.x >> 16))) * (float)m6;
     }
     __device__ __forceinline__ float term(int dot, const BlockScale &a) const {
-        return a.d * (sm.x * (float)dot - sm.y * (float)a.s);
+        return a.d * (sc * (float)dot - mn * (float)a.s);
+    }
+};
+template <>
+struct WScale<kFmtQ6K> {
+    float s;  // the super-block's d
+    __device__ __forceinline__ void load(const uint8_t *scales, size_t i) { s = __half2float(__ldg((const __half *)scales + i / 8)); }
+    __device__ __forceinline__ float term(int dot, const BlockScale &a) const { return (float)dot * (s * a.d); }
+};
+template <>
+struct WCodes<kFmtQ6K> {
+    uint4 lo;      // low nibbles of the 32 codes, Q4 order
+    uint2 hi;      // high bit pairs: word h, byte b, bits 2i..2i+1 = element 16h + 4i + b
+    int sc0, sc1;  // signed scales of elements 0..15 and 16..31
+    __device__ __forceinline__ void load(const uint8_t *blob, size_t n, size_t i) {
+        lo = ld_weights((const uint4 *)blob + i);
+        hi = __ldcs((const uint2 *)(blob + 16 * n) + i);
+        const unsigned s = __ldcs((const unsigned short *)(blob + 24 * n) + i);
+        sc0 = (int)(int8_t)(s & 255u);
+        sc1 = (int)(int8_t)(s >> 8);
+    }
+    // sc0 * sum_{i<16} (q_i - 32) a_i + sc1 * sum_{i>=16} (q_i - 32) a_i, with
+    // q = low nibble + 16 * high pair (|result| < 2^24: exact in fp32 too)
+    __device__ __forceinline__ int dot(const int4 &a0, const int4 &a1, int a_sum) const {
+        const uint32_t m4 = 0x0F0F0F0Fu, m2 = 0x03030303u;
+        const uint32_t lw[4] = {lo.x, lo.y, lo.z, lo.w};
+        const int aw0[4] = {a0.x, a0.y, a0.z, a0.w}, aw1[4] = {a1.x, a1.y, a1.z, a1.w};
+        int l0 = 0, l1 = 0, h0 = 0, h1 = 0, s0 = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            l0 = __dp4a((int)(lw[k] & m4), aw0[k], l0);
+            l1 = __dp4a((int)((lw[k] >> 4) & m4), aw1[k], l1);
+            h0 = __dp4a((int)((hi.x >> (2 * k)) & m2), aw0[k], h0);
+            h1 = __dp4a((int)((hi.y >> (2 * k)) & m2), aw1[k], h1);
+            s0 = __dp4a(0x01010101, aw0[k], s0);
+        }
+        const int s1 = a_sum - s0;
+        return sc0 * (l0 + 16 * h0 - 32 * s0) + sc1 * (l1 + 16 * h1 - 32 * s1);
     }
 };
 
@@ -226,6 +291,7 @@ struct CacheView {
     unsigned long long *cold_reads;  // [1]: (tensor, expert) zero-copy passes
     uint32_t *hit_bitmap;      // [hit_words]: stamp indices hit since the last promotion pass (or null)
     int E, slots_per_tensor, bitmap_words, miss_cap, hit_words;
+    int clock_tokens;          // tokens of the step this launch belongs to: reads stamp *clock + clock_tokens
 };
 
 // Record one (tensor, expert) read: a cold read sets its bit in the miss

@@ -23,6 +23,11 @@ struct PlanParams {
     int32_t *assign;      // [T*k]: assignment ids grouped by expert
     int *error;           // [1]: bit 0 = expert id out of range
     int T, k, E, H, quantize_x;
+    // expert shard: ids are global in [0, E_route); this context holds
+    // [e_base, e_base + E) (local id = id - e_base); assignments to other
+    // experts are left out of every used-expert list (placed after them in
+    // assign) and contribute nothing
+    int e_base, E_route;
 };
 
 struct GemvParams {
@@ -41,6 +46,8 @@ struct GemvParams {
     int8_t *xq_out;       // fused path: [T][H] copy of the quantized x
     BlockScale *xds_out;  // fused path: [T][H/32]
     int fmt;              // weight format of the mat-vec kernels (kFmtQ4 / kFmtQ8)
+    const int32_t *idx;   // [T][k] global expert ids (the combine skips experts of other shards)
+    int e_base;           // first expert of this shard (local id = global id - e_base)
 };
 
 // Fused small-batch layer (cooperative launch).
@@ -48,7 +55,8 @@ struct FusedParams {
     GemvParams g;
     const float *x;          // [T][H]
     const int32_t *idx;      // [T][k] (when logits is null)
-    const float *logits;     // [T][E]: route in-kernel (top-k + softmax) when not null
+    const float *logits;     // [T][n_route]: route in-kernel (top-k + softmax) when not null
+    int n_route;             // experts of the whole layer (logit columns; global id range)
     int32_t *idx_out;        // routed: [T][k] written by CTA 0
     float *w_out;            // routed: [T][k] written by CTA 0
     int renorm;
@@ -117,6 +125,8 @@ struct PrefillLaunch {
     const float *w;
     float *y;
     int T, k, H, n_sm;
+    const int32_t *idx;         // [T][k] global expert ids (the combine skips other shards' experts)
+    int e_base, E;              // this shard's experts: global ids [e_base, e_base + E)
 };
 
 // Staging of a prefill layer's cold expert tensors into lent pool slots.
@@ -161,7 +171,7 @@ int gemm_bn(bool dual);
 int gemm_rows_per_tile(bool dual);
 int launch_step_finish(const Update *u, int n, uint64_t *tbl, int32_t *slot, uint32_t *stamps, uint32_t *clock,
                        uint32_t new_clock, uint32_t *clear_a, int n_a, uint32_t *clear_b, int n_b, cudaStream_t st);
-int launch_count_assign(const int32_t *idx, int n, int E, uint32_t *cnt, cudaStream_t st);
+int launch_count_assign(const int32_t *idx, int n, int E, int e_base, uint32_t *cnt, cudaStream_t st);
 int launch_busy(unsigned long long ns, cudaStream_t st);
 int launch_shared_assign(const int32_t *idx, const float *w, int T, int k, int e_shared, int32_t *idx_a, float *w_a,
                          int *error, cudaStream_t st);

@@ -202,6 +202,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanParams p) {
     int *cnt = sm;            // [E]
     int *cur = sm + p.E;      // [E]
     __shared__ int warp_tot[33];
+    __shared__ int s_other;   // assignments to experts of other shards
     const int A = p.T * p.k;
     const int lane = threadIdx.x & 31;
     if (p.quantize_x) {
@@ -210,14 +211,21 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanParams p) {
             quantize_block_warp(p.x[(size_t)b * kBlock + lane], lane, p.xq + (size_t)b * kBlock, p.xds + b);
     }
     for (int e = threadIdx.x; e < p.E; e += blockDim.x) cnt[e] = 0;
+    if (threadIdx.x == 0) s_other = 0;
     __syncthreads();
+    // local expert of assignment a: -1 for another shard's expert; ids outside
+    // the layer's range set error bit 0 and are read as local expert 0
+    auto local_e = [&](int a) {
+        const int g = p.idx[a];
+        if (g < 0 || g >= p.E_route) return 0;
+        const int e = g - p.e_base;
+        return e >= 0 && e < p.E ? e : -1;
+    };
     for (int a = threadIdx.x; a < A; a += blockDim.x) {
-        int e = p.idx[a];
-        if (e < 0 || e >= p.E) {
-            atomicOr(p.error, 1);
-            e = 0;
-        }
-        atomicAdd(&cnt[e], 1);
+        const int g = p.idx[a];
+        if (g < 0 || g >= p.E_route) atomicOr(p.error, 1);
+        const int e = local_e(a);
+        if (e >= 0) atomicAdd(&cnt[e], 1);
     }
     __syncthreads();
     // exclusive scans over experts of counts and of "used" flags, in
@@ -244,14 +252,14 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanParams p) {
         run_u += tot_u;
     }
     if (threadIdx.x == 0) {
-        p.uniq_off[run_u] = A;
+        p.uniq_off[run_u] = run_off;
         *p.n_uniq = run_u;
     }
     __syncthreads();
+    // other shards' assignments follow the grouped ones (in no used list)
     for (int a = threadIdx.x; a < A; a += blockDim.x) {
-        int e = p.idx[a];
-        if (e < 0 || e >= p.E) e = 0;
-        int pos = atomicAdd(&cur[e], 1);
+        const int e = local_e(a);
+        const int pos = e >= 0 ? atomicAdd(&cur[e], 1) : run_off + atomicAdd(&s_other, 1);
         p.assign[pos] = a;
     }
 }
@@ -280,7 +288,7 @@ __global__ void __launch_bounds__(256) gate_up_kernel(GemvParams p) {
     const int rgs = p.F / kBlock;
     const int n_uniq = *p.n_uniq;
     const int n_items = n_uniq * rgs;
-    const uint32_t step_clock = *p.cv.clock + (uint32_t)p.n_tokens;
+    const uint32_t step_clock = *p.cv.clock + (uint32_t)p.cv.clock_tokens;
     const size_t scale_off = blob_scales_offset_fmt(FMT, p.F, nbx);
     __shared__ float sh_h[kMaxChunk][32];
 
@@ -383,9 +391,16 @@ __global__ void __launch_bounds__(256) down_kernel(GemvParams p) {
     const int n_rb = p.H / ROWS;
     const int n_uniq = *p.n_uniq;
     const int n_items = n_uniq * n_rb;
-    const uint32_t step_clock = *p.cv.clock + (uint32_t)p.n_tokens;
+    const uint32_t step_clock = *p.cv.clock + (uint32_t)p.cv.clock_tokens;
     const size_t scale_off = blob_scales_offset_fmt(FMT, p.H, nbf);
     __shared__ int sh_last;
+    if (n_uniq == 0) {
+        // no assignment of this shard: y = 0
+        for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < (size_t)p.n_tokens * p.H;
+             i += (size_t)gridDim.x * blockDim.x)
+            p.y[i] = 0.0f;
+        return;
+    }
 
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
         const int u = item / n_rb, rb = item - u * n_rb;
@@ -460,6 +475,7 @@ __global__ void __launch_bounds__(256) down_kernel(GemvParams p) {
                 float y = 0.0f;
                 for (int j = 0; j < p.k; ++j) {
                     const size_t a = (size_t)t * p.k + j;
+                    if ((unsigned)(p.idx[a] - p.e_base) >= (unsigned)p.cv.E) continue;  // another shard's
                     y += p.w[a] * __ldcg(p.o + a * p.H + rr);
                 }
                 p.y[(size_t)t * p.H + rr] = y;
@@ -494,6 +510,8 @@ int launch_gemv(const GemvParams &p, int grid_gu, int grid_dn, cudaStream_t st, 
         e = launch_gemv_fmt<kFmtQ8>(p, grid_gu, grid_dn, st, ev);
     else if (p.fmt == kFmtQ4K)
         e = launch_gemv_fmt<kFmtQ4K>(p, grid_gu, grid_dn, st, ev);
+    else if (p.fmt == kFmtQ6K)
+        e = launch_gemv_fmt<kFmtQ6K>(p, grid_gu, grid_dn, st, ev);
     else if (p.fmt == kFmtQ5)
         e = launch_gemv_fmt<kFmtQ5>(p, grid_gu, grid_dn, st, ev);
     else
@@ -642,6 +660,21 @@ __device__ __forceinline__ void warp_topk_row(const float *l, int E, int k, int 
     my_w = ej / den;
 }
 
+// Global expert id of an assignment -> this shard's local expert, or -1 for
+// another shard's expert (ids outside the layer's range set error bit 0 and
+// are read as local expert 0).
+__device__ __forceinline__ int fused_local_e(const FusedParams &p, int g) {
+    if (g < 0 || g >= p.n_route) {
+        atomicOr(p.error, 1);
+        return 0;
+    }
+    const int e = g - p.g.e_base;
+    return e >= 0 && e < p.g.cv.E ? e : -1;
+}
+
+// The launch's plan in shared memory: s_e[a] = local expert of assignment a
+// (-1: another shard's, left out), s_uniq / s_off / s_asg = used experts
+// ascending, their assignment ranges and the assignments grouped by expert.
 __device__ void fused_plan(const FusedParams &p, int *s_e, int *s_uniq, int *s_off, int *s_asg, int *s_nu,
                            int *s_cnt, int *s_first, float *s_w) {
     const int A = p.g.n_tokens * p.g.k;
@@ -650,33 +683,35 @@ __device__ void fused_plan(const FusedParams &p, int *s_e, int *s_uniq, int *s_o
         // used experts are the positions where the expert changes
         __syncthreads();  // routing / x prologue writes
         if (p.logits && p.g.n_tokens == 1) {
-            // one routed token: its k picks are distinct experts already
-            if (threadIdx.x < p.g.k) {
-                s_asg[threadIdx.x] = threadIdx.x;
-                s_uniq[threadIdx.x] = s_e[threadIdx.x];
-                s_off[threadIdx.x] = threadIdx.x;
-            }
-            if (threadIdx.x == 0) {
-                s_off[p.g.k] = p.g.k;
-                *s_nu = p.g.k;
+            // one routed token: its k picks are distinct experts already;
+            // this shard's picks in pick order
+            if (threadIdx.x < 32) {
+                const int lane = threadIdx.x;
+                const int e = lane < p.g.k ? fused_local_e(p, s_e[lane]) : -1;
+                const unsigned mine = __ballot_sync(0xffffffffu, e >= 0);
+                const int u = __popc(mine & ((1u << lane) - 1u));
+                if (lane < p.g.k) s_e[lane] = e;
+                if (e >= 0) {
+                    s_asg[u] = lane;
+                    s_uniq[u] = e;
+                    s_off[u] = u;
+                }
+                if (lane == 0) {
+                    s_off[__popc(mine)] = __popc(mine);
+                    *s_nu = __popc(mine);
+                }
             }
         } else if (threadIdx.x < 32) {
             const int lane = threadIdx.x;
-            int e = 0x7fffffff;
+            int e = -1;
             if (lane < A) {
-                if (p.logits) {
-                    e = s_e[lane];
-                } else {
-                    e = p.idx[lane];
-                    if (e < 0 || e >= p.g.cv.E) {
-                        atomicOr(p.error, 1);
-                        e = 0;
-                    }
-                    s_e[lane] = e;
-                    s_w[lane] = p.g.w[lane];
-                }
+                e = fused_local_e(p, p.logits ? s_e[lane] : p.idx[lane]);
+                s_e[lane] = e;
+                if (!p.logits) s_w[lane] = p.g.w[lane];
             }
-            unsigned key = lane < A ? ((unsigned)e << 8) | (unsigned)lane : 0xffffffffu;
+            const unsigned mine = __ballot_sync(0xffffffffu, e >= 0);
+            const int An = __popc(mine);  // this shard's assignments (sorted first)
+            unsigned key = e >= 0 ? ((unsigned)e << 8) | (unsigned)lane : 0xffffffffu;
 #pragma unroll
             for (int size = 2; size <= 32; size <<= 1) {
 #pragma unroll
@@ -690,40 +725,34 @@ __device__ void fused_plan(const FusedParams &p, int *s_e, int *s_uniq, int *s_o
             }
             const int se = (int)(key >> 8), sa = (int)(key & 0xffu);
             const int prev = __shfl_up_sync(0xffffffffu, se, 1);
-            const bool head = lane < A && (lane == 0 || prev != se);
+            const bool head = lane < An && (lane == 0 || prev != se);
             const unsigned heads = __ballot_sync(0xffffffffu, head);
             const int u = __popc(heads & ((1u << lane) - 1u)) + (head ? 0 : -1);
-            if (lane < A) s_asg[lane] = sa;
+            if (lane < An) s_asg[lane] = sa;
             if (head) {
                 s_uniq[u] = se;
                 s_off[u] = lane;
             }
             if (lane == 0) {
                 const int nu = __popc(heads);
-                s_off[nu] = A;
+                s_off[nu] = An;
                 *s_nu = nu;
             }
         }
         __syncthreads();
         return;
     }
-    if (!p.logits) {
-        for (int a = threadIdx.x; a < A; a += blockDim.x) {
-            int e = p.idx[a];
-            if (e < 0 || e >= p.g.cv.E) {
-                atomicOr(p.error, 1);
-                e = 0;
-            }
-            s_e[a] = e;
-            s_w[a] = p.g.w[a];
-        }
+    __syncthreads();  // routing writes
+    for (int a = threadIdx.x; a < A; a += blockDim.x) {
+        s_e[a] = fused_local_e(p, p.logits ? s_e[a] : p.idx[a]);
+        if (!p.logits) s_w[a] = p.g.w[a];
     }
     __syncthreads();
     int n_first = 0;
     for (int a = threadIdx.x; a < A; a += blockDim.x) {
         const int e = s_e[a];
-        int first = 1;
-        for (int b = 0; b < a; ++b)
+        int first = e >= 0;
+        for (int b = 0; first && b < a; ++b)
             if (s_e[b] == e) {
                 first = 0;
                 break;
@@ -761,6 +790,7 @@ __device__ void fused_plan(const FusedParams &p, int *s_e, int *s_uniq, int *s_o
     // assignments grouped by expert, ascending assignment id within an expert
     for (int a = threadIdx.x; a < A; a += blockDim.x) {
         const int e = s_e[a];
+        if (e < 0) continue;  // another shard's
         int lo = 0, hi = *s_nu - 1;
         while (lo < hi) {
             const int mid = (lo + hi) >> 1;
@@ -783,7 +813,7 @@ template <int NT, class Prefetch>
 __device__ __forceinline__ void gu_chunk(const FusedParams &p, int c0, int nt, int rg, int rloc, int sub, int lane,
                                          int warp, const uint4 *qg, const uint4 *qu, const __half *dg,
                                          const __half *du, int8_t *xq_s, BlockScale *xds_s, float (*sh_h)[32],
-                                         const int *s_asg, Prefetch &&prefetch, bool xpre) {
+                                         const int *s_asg, Prefetch &&prefetch, bool xpre, const int *s_e) {
     const GemvParams &g = p.g;
     const int H = g.H, F = g.F, k = g.k;
     const int nbx = H / kBlock, rgs = F / kBlock;
@@ -847,7 +877,11 @@ __device__ __forceinline__ void gu_chunk(const FusedParams &p, int c0, int nt, i
                         const int tok = a / k;
                         quantize_block_warp(xv[i], lane, xq_s + (size_t)t * H + (size_t)b * kBlock,
                                             xds_s + (size_t)t * nbx + b);
-                        if (rg == 0 && (a % k) == 0) {
+                        // the context's copy of x: written by the token's
+                        // first assignment of this shard (s_e < 0: another's)
+                        bool first = rg == 0;
+                        for (int j = 0; first && j < a % k; ++j) first = s_e[tok * k + j] < 0;
+                        if (first) {
                             g.xq_out[(size_t)tok * H + (size_t)b * kBlock + lane] =
                                 xq_s[(size_t)t * H + (size_t)b * kBlock + lane];
                             if (lane == 0) g.xds_out[(size_t)tok * nbx + b] = xds_s[(size_t)t * nbx + b];
@@ -1356,7 +1390,7 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
     }
     // the clock is read after the dependency wait: every input of this
     // launch, the promotion pass's clock included, comes from before it
-    const uint32_t step_clock = *g.cv.clock + (uint32_t)g.n_tokens;
+    const uint32_t step_clock = *g.cv.clock + (uint32_t)g.cv.clock_tokens;
     constexpr int DG = 32 / LD, DROWS = kWarps * DG;
     const int n_rb_all = H / DROWS;
     const int R = p.rb_rows;
@@ -1376,11 +1410,11 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
     if (t1) {
         // routed and x quantized above
     } else if (p.logits && warp < n_route_warps) {
-        const int k_ = g.k, E = g.cv.E;
+        const int k_ = g.k;
         for (int t = warp; t < g.n_tokens; t += n_route_warps) {
             int me;
             float mw;
-            warp_topk_row(p.logits + (size_t)t * E, E, k_, p.renorm, lane, me, mw);
+            warp_topk_row(p.logits + (size_t)t * p.n_route, p.n_route, k_, p.renorm, lane, me, mw);
             if (lane < k_) {
                 s_e[t * k_ + lane] = me;
                 s_w[t * k_ + lane] = mw;
@@ -1497,7 +1531,7 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
             for (int c0 = a0; c0 < a1; c0 += NT) {
                 const int nt = min(NT, a1 - c0);
                 gu_chunk<NT>(p, c0, nt, rg, rloc, sub, lane, warp, qg, qu, dg, du, xq_s, xds_s, sh_h, s_asg,
-                             issue_prefetch, xpre);
+                             issue_prefetch, xpre, s_e);
             }
             // publish this row block of expert e (the writers fenced h
             // before the chunk's closing barrier)
@@ -1588,7 +1622,8 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
                 for (int i = threadIdx.x; i < g.n_tokens * R; i += blockDim.x) {
                     const int t = i / R, r = i - t * R;
                     float y = 0.0f;
-                    for (int j = 0; j < k; ++j) y += s_w[t * k + j] * s_o[(t * k + j) * R + r];
+                    for (int j = 0; j < k; ++j)
+                        if (s_e[t * k + j] >= 0) y += s_w[t * k + j] * s_o[(t * k + j) * R + r];
                     g.y[(size_t)t * H + (size_t)item * R + r] = y;
                 }
             }
@@ -1603,6 +1638,12 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
         const int n_rb = H / ROWS;
         const size_t scale_off = blob_scales_offset(H, nbf);
         const int n_items = nu * n_rb;
+        if (nu == 0) {
+            // no assignment of this shard: y = 0
+            for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < (size_t)g.n_tokens * H;
+                 i += (size_t)gridDim.x * blockDim.x)
+                g.y[i] = 0.0f;
+        }
         for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
             const int u = item / n_rb, rb = item - u * n_rb;
             const int e = s_uniq[u];
@@ -1636,7 +1677,7 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
                     float y = 0.0f;
                     for (int j = 0; j < k; ++j) {
                         const size_t a = (size_t)t * k + j;
-                        y += s_w[a] * __ldcg(g.o + a * H + rr);
+                        if (s_e[a] >= 0) y += s_w[a] * __ldcg(g.o + a * H + rr);
                     }
                     g.y[(size_t)t * H + rr] = y;
                 }
@@ -1808,6 +1849,8 @@ int launch_block_dots(const uint8_t *blob, int fmt, int rows, int nb, int row0, 
         block_dots_kernel<kFmtQ5><<<(n + 255) / 256, 256, 0, st>>>(blob, rows, nb, row0, n_rows, qa, out);
     else if (fmt == kFmtQ4K)
         block_dots_kernel<kFmtQ4K><<<(n + 255) / 256, 256, 0, st>>>(blob, rows, nb, row0, n_rows, qa, out);
+    else if (fmt == kFmtQ6K)
+        block_dots_kernel<kFmtQ6K><<<(n + 255) / 256, 256, 0, st>>>(blob, rows, nb, row0, n_rows, qa, out);
     else
         block_dots_kernel<kFmtQ4><<<(n + 255) / 256, 256, 0, st>>>(blob, rows, nb, row0, n_rows, qa, out);
     return (int)cudaGetLastError();
@@ -1870,12 +1913,12 @@ int launch_step_finish(const Update *u, int n, uint64_t *tbl, int32_t *slot, uin
 
 // Prefill preheat: the (token, expert) assignments of one layer added to the
 // layer's use counts, through a per-block histogram in shared memory.
-__global__ void count_assign_kernel(const int32_t *__restrict__ idx, int n, int E, uint32_t *cnt) {
+__global__ void count_assign_kernel(const int32_t *__restrict__ idx, int n, int E, int e_base, uint32_t *cnt) {
     extern __shared__ uint32_t hist[];
     for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0u;
     __syncthreads();
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
-        const int e = idx[i];
+        const int e = idx[i] - e_base;  // this shard's experts only
         if ((unsigned)e < (unsigned)E) atomicAdd(&hist[e], 1u);
     }
     __syncthreads();
@@ -1883,11 +1926,11 @@ __global__ void count_assign_kernel(const int32_t *__restrict__ idx, int n, int 
         if (hist[e]) atomicAdd(&cnt[e], hist[e]);
 }
 
-int launch_count_assign(const int32_t *idx, int n, int E, uint32_t *cnt, cudaStream_t st) {
+int launch_count_assign(const int32_t *idx, int n, int E, int e_base, uint32_t *cnt, cudaStream_t st) {
     if (n <= 0) return 0;
     int grid = (n + 1023) / 1024;
     grid = grid > 152 ? 152 : grid;
-    count_assign_kernel<<<grid, 256, sizeof(uint32_t) * (size_t)E, st>>>(idx, n, E, cnt);
+    count_assign_kernel<<<grid, 256, sizeof(uint32_t) * (size_t)E, st>>>(idx, n, E, e_base, cnt);
     return (int)cudaGetLastError();
 }
 

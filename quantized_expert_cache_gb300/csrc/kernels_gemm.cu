@@ -651,7 +651,7 @@ __global__ void __launch_bounds__(Cfg<DUAL>::NTHREADS, 1)
 __global__ void tiling_kernel(TilingParams p) {
     __shared__ int warp_tot[33];
     const int n_uniq = *p.n_uniq;
-    const uint32_t step_clock = *p.cv.clock + (uint32_t)p.n_tokens;
+    const uint32_t step_clock = *p.cv.clock + (uint32_t)p.cv.clock_tokens;
     for (int u = threadIdx.x; u < n_uniq; u += blockDim.x) {
         const int e = p.uniq_e[u];
         for (int kd = 0; kd < 3; ++kd) {
@@ -751,14 +751,19 @@ __global__ void gather_kernel(const int32_t *__restrict__ assign, int A, int k, 
     }
 }
 
-// y[t][i] = sum_j w[t][j] * o[t*k + j][i], j in order.
-__global__ void combine_kernel(const float *__restrict__ o, const float *__restrict__ w, float *__restrict__ y, int T,
-                               int k, int H) {
+// y[t][i] = sum_j w[t][j] * o[t*k + j][i], j in order, over this shard's
+// assignments (global id - e_base in [0, E)).
+__global__ void combine_kernel(const float *__restrict__ o, const float *__restrict__ w,
+                               const int32_t *__restrict__ idx, int e_base, int E, float *__restrict__ y, int T, int k,
+                               int H) {
     const size_t n = (size_t)T * H;
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
         const int t = (int)(i / H), c = (int)(i % H);
         float acc = 0.0f;
-        for (int j = 0; j < k; ++j) acc += w[(size_t)t * k + j] * o[((size_t)t * k + j) * H + c];
+        for (int j = 0; j < k; ++j) {
+            const size_t a = (size_t)t * k + j;
+            if ((unsigned)(idx[a] - e_base) < (unsigned)E) acc += w[a] * o[a * H + c];
+        }
         y[i] = acc;
     }
 }
@@ -868,7 +873,7 @@ int launch_prefill(const PrefillLaunch &L, cudaStream_t st, cudaEvent_t const *e
     if (ev) record_event(ev[3], st);
     const size_t n = (size_t)L.T * L.H;
     int gc = (int)std::min<size_t>((n + 255) / 256, (size_t)L.n_sm * 16);
-    combine_kernel<<<gc, 256, 0, st>>>(L.dn.o, L.w, L.y, L.T, L.k, L.H);
+    combine_kernel<<<gc, 256, 0, st>>>(L.dn.o, L.w, L.idx, L.e_base, L.E, L.y, L.T, L.k, L.H);
     return (int)cudaGetLastError();
 }
 

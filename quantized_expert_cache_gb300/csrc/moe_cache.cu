@@ -50,6 +50,13 @@ struct moe_ctx {
     // k + 1 assignments (the last = the shared expert, weight 1)
     bool shared = false;
     int Et = 0, ka = 0;                    // table row length, assignments per token
+    // expert shard (moe_set_expert_shard): this context holds experts
+    // [e_base, e_base + E) of a layer of E_route experts; forwards take
+    // global ids and skip the other shards' assignments
+    int e_base = 0, E_route = 0;
+    // tokens of the step a forward belongs to (moe_ffn_forward_rows); 0: its
+    // own token count
+    int clock_tokens = 0;
     std::vector<uint8_t *> sh_blob;        // [n_tensors]: device blob of the shared expert
     int32_t *idx_a = nullptr;              // [M][ka]: routed ids + E
     float *w_a = nullptr;                  // [M][ka]: routed weights + 1
@@ -245,29 +252,13 @@ int sync_all(moe_ctx *ctx) {
     return MOE_OK;
 }
 
-// Q4_K super-block (144 bytes, 256 weights) -> 8 sub-blocks: Q4-order
-// nibbles (byte t = element t | element t + 16 << 4) and the exact fp32
-// pairs (d * sc_j, dmin * m_j) (binary16 times a 6-bit integer fits fp32).
-void repack_q4k_super(const uint8_t *sb, uint8_t *codes, float *sm) {
-    auto h2f = [](const uint8_t *p) {
-        __half h;
-        uint16_t b = (uint16_t)(p[0] | (p[1] << 8));
-        memcpy(&h, &b, 2);
-        return __half2float(h);
-    };
-    const float d = h2f(sb), dmin = h2f(sb + 2);
-    const uint8_t *sc = sb + 4, *qs = sb + 16;
+// Q4_K super-block (144 bytes, 256 weights) -> 8 sub-blocks of Q4-order
+// nibbles (byte t = element t | element t + 16 << 4) and the 16-byte header
+// (d, dmin, packed 6-bit scales and mins) as stored.
+void repack_q4k_super(const uint8_t *sb, uint8_t *codes, uint8_t *header) {
+    memcpy(header, sb, 16);
+    const uint8_t *qs = sb + 16;
     for (int j = 0; j < 8; ++j) {
-        int s6, m6;
-        if (j < 4) {
-            s6 = sc[j] & 63;
-            m6 = sc[j + 4] & 63;
-        } else {
-            s6 = (sc[j + 4] & 15) | ((sc[j - 4] >> 6) << 4);
-            m6 = (sc[j + 4] >> 4) | ((sc[j] >> 6) << 4);
-        }
-        sm[2 * j] = d * (float)s6;
-        sm[2 * j + 1] = dmin * (float)m6;
         const uint8_t *chunk = qs + 32 * (j / 2);
         const int shift = (j & 1) ? 4 : 0;
         for (int t = 0; t < 16; ++t) {
@@ -277,10 +268,32 @@ void repack_q4k_super(const uint8_t *sb, uint8_t *codes, float *sm) {
     }
 }
 
+// Q6_K super-block (210 bytes, 256 weights, the published layout: per
+// 128-weight half n, element 32m + l has its low nibble in
+// ql[64n + 32 (m & 1) + l] (low half of the byte for m < 2) and its high pair
+// in bits 2m..2m+1 of qh[32n + l]; then 16 signed scales and d) -> 8 blocks
+// of 32: Q4-order low nibbles, packed high pairs, the two scales; and d.
+void repack_q6k_super(const uint8_t *sb, uint8_t *lo, uint32_t *hi, uint8_t *sc, uint8_t *d) {
+    memset(lo, 0, 128);
+    memset(hi, 0, 16 * sizeof(uint32_t));
+    for (int n = 0; n < 2; ++n)
+        for (int m = 0; m < 4; ++m)
+            for (int l = 0; l < 32; ++l) {
+                const uint8_t lb = sb[64 * n + 32 * (m & 1) + l];
+                const uint32_t q_lo = m < 2 ? (lb & 15u) : (uint32_t)(lb >> 4);
+                const uint32_t q_hi = (sb[128 + 32 * n + l] >> (2 * m)) & 3u;
+                const int b = 4 * n + m, j = l & 15;  // block b, element l of it
+                lo[16 * b + j] |= (uint8_t)(q_lo << (l < 16 ? 0 : 4));
+                hi[2 * b + (l >> 4)] |= q_hi << (8 * (j & 3) + 2 * (j >> 2));
+            }
+    memcpy(sc, sb + 192, 16);
+    memcpy(d, sb + 208, 2);
+}
+
 // Repack canonical blocks (binary16 d, then the code bytes: 18 bytes for
 // Q4, 34 for Q8_0; d, 4 fifth-bit bytes, 16 nibble bytes = 22 for Q5_0;
-// 144-byte super-blocks of 8 blocks for Q4_K) of n_experts experts into
-// plane blobs.
+// 144-byte super-blocks of 8 blocks for Q4_K, 210-byte ones for Q6_K) of
+// n_experts experts into plane blobs.
 void repack(const uint8_t *src, uint8_t *dst, int fmt, int n_experts, int rows, int nb, size_t stride) {
     const size_t nblk = (size_t)rows * nb, cb = (size_t)moe::code_bytes(fmt), bb = cb + 2;
     auto work = [&](int e0, int e1) {
@@ -288,8 +301,16 @@ void repack(const uint8_t *src, uint8_t *dst, int fmt, int n_experts, int rows, 
             if (fmt == moe::kFmtQ4K) {
                 const uint8_t *s = src + (size_t)e * (nblk / 8) * 144;
                 uint8_t *q = dst + (size_t)e * stride;
-                float *sm = (float *)(q + nblk * 16);
-                for (size_t u = 0; u < nblk / 8; ++u) repack_q4k_super(s + 144 * u, q + 128 * u, sm + 16 * u);
+                uint8_t *hd = q + nblk * 16;
+                for (size_t u = 0; u < nblk / 8; ++u) repack_q4k_super(s + 144 * u, q + 128 * u, hd + 16 * u);
+                continue;
+            }
+            if (fmt == moe::kFmtQ6K) {
+                const uint8_t *s = src + (size_t)e * (nblk / 8) * 210;
+                uint8_t *q = dst + (size_t)e * stride;
+                for (size_t u = 0; u < nblk / 8; ++u)
+                    repack_q6k_super(s + 210 * u, q + 128 * u, (uint32_t *)(q + 16 * nblk + 64 * u),
+                                     q + 24 * nblk + 16 * u, q + 26 * nblk + 2 * u);
                 continue;
             }
             const uint8_t *s = src + (size_t)e * nblk * bb;
@@ -522,11 +543,11 @@ int moe_layer_init(const moe_cfg *cfg, void *cuda_stream, moe_ctx **out) {
         c.slots_per_tensor < 0 || c.slots_per_tensor > c.n_experts || c.max_tokens < 1 || c.window_tokens < 1 ||
         c.max_swaps_per_step < 0 || (c.shared_experts != 0 && (c.shared_experts != 1 || c.n_experts > 4095)) ||
         (c.weight_format != MOE_FMT_Q4_0 && c.weight_format != MOE_FMT_Q8_0 && c.weight_format != MOE_FMT_Q5_0 &&
-         c.weight_format != MOE_FMT_Q4_K) ||
-        (c.weight_format == MOE_FMT_Q4_K && (c.hidden % 256 || c.ffn % 256)))
+         c.weight_format != MOE_FMT_Q4_K && c.weight_format != MOE_FMT_Q6_K) ||
+        ((c.weight_format == MOE_FMT_Q4_K || c.weight_format == MOE_FMT_Q6_K) && (c.hidden % 256 || c.ffn % 256)))
         return fail(nullptr, MOE_ERR_ARG,
                     "bad cfg: hidden%32, ffn%32, 1<=E<=4096, 1<=k<=min(32,E), layers>=1, 0<=slots<=E, max_tokens>=1, "
-                    "weight_format Q4_0, Q8_0, Q5_0 or Q4_K (hidden, ffn % 256), shared_experts 0 or 1 "
+                    "weight_format Q4_0, Q8_0, Q5_0, Q4_K or Q6_K (hidden, ffn % 256), shared_experts 0 or 1 "
                     "(then E <= 4095)");
     int down_rows = moe::down_rows_per_item(c.ffn);
     if (c.hidden % down_rows) return fail(nullptr, MOE_ERR_ARG, "hidden must be a multiple of the down row block");
@@ -539,6 +560,7 @@ int moe_layer_init(const moe_cfg *cfg, void *cuda_stream, moe_ctx **out) {
     ctx->k = c.top_k;
     ctx->shared = c.shared_experts != 0;
     ctx->Et = c.n_experts + (ctx->shared ? 1 : 0);
+    ctx->E_route = c.n_experts;
     ctx->ka = c.top_k + (ctx->shared ? 1 : 0);
     ctx->M = c.max_tokens;
     ctx->n_tensors = 3 * c.n_layers;
@@ -546,6 +568,7 @@ int moe_layer_init(const moe_cfg *cfg, void *cuda_stream, moe_ctx **out) {
     ctx->fmt = c.weight_format == MOE_FMT_Q8_0   ? moe::kFmtQ8
                : c.weight_format == MOE_FMT_Q5_0 ? moe::kFmtQ5
                : c.weight_format == MOE_FMT_Q4_K ? moe::kFmtQ4K
+               : c.weight_format == MOE_FMT_Q6_K ? moe::kFmtQ6K
                                                  : moe::kFmtQ4;
     ctx->blob = moe::blob_bytes_fmt(ctx->fmt, c.ffn, c.hidden / 32);
     ctx->stride = (ctx->blob + 255) / 256 * 256;
@@ -796,7 +819,7 @@ int register_shared_expert(moe_ctx *ctx, int layer, int kind, const void *host_w
 int route_topk(moe_ctx *ctx, const float *d_logits, int n_tokens, int n_experts, int k, int32_t *d_idx, float *d_w,
                void *stream) {
     if (!ctx) return fail(nullptr, MOE_ERR_ARG, "null ctx");
-    if (n_tokens < 0 || n_experts != ctx->E || k != ctx->k || (n_tokens > 0 && (!d_logits || !d_idx || !d_w)))
+    if (n_tokens < 0 || n_experts != ctx->E_route || k != ctx->k || (n_tokens > 0 && (!d_logits || !d_idx || !d_w)))
         return fail(ctx, MOE_ERR_ARG, "route_topk: bad sizes or pointers");
     cudaStream_t st = stream ? (cudaStream_t)stream : ctx->stream;
     int rc = moe::launch_topk(d_logits, n_tokens, n_experts, k, ctx->cfg.renorm_topk, d_idx, d_w, st);
@@ -819,9 +842,30 @@ int moe_ffn_forward_routed(moe_ctx *ctx, int layer, const float *d_x, const floa
     if (n_tokens > 0 && (!d_logits || !d_idx || !d_w)) return fail(ctx, MOE_ERR_ARG, "routed forward: null pointer");
     if (n_tokens > 0 && n_tokens <= 32 && n_tokens * ctx->k <= 256 && ctx->fused_blocks > 0)
         return ffn_forward_impl(ctx, layer, d_x, n_tokens, d_idx, d_w, d_y, stream, d_logits, d_idx, d_w);
-    int rc = route_topk(ctx, d_logits, n_tokens, ctx->E, ctx->k, d_idx, d_w, stream);
+    int rc = route_topk(ctx, d_logits, n_tokens, ctx->E_route, ctx->k, d_idx, d_w, stream);
     if (rc) return rc;
     return ffn_forward_impl(ctx, layer, d_x, n_tokens, d_idx, d_w, d_y, stream, nullptr, nullptr, nullptr);
+}
+
+int moe_set_expert_shard(moe_ctx *ctx, int expert_base, int n_route) {
+    if (!ctx) return fail(nullptr, MOE_ERR_ARG, "null ctx");
+    if (ctx->shared) return fail(ctx, MOE_ERR_STATE, "expert shard: not with shared experts");
+    if (expert_base < 0 || n_route < ctx->E || n_route > 4096 || expert_base > n_route - ctx->E)
+        return fail(ctx, MOE_ERR_ARG, "expert shard: need 0 <= expert_base <= n_route - n_experts, n_route <= 4096");
+    ctx->e_base = expert_base;
+    ctx->E_route = n_route;
+    return MOE_OK;
+}
+
+int moe_ffn_forward_rows(moe_ctx *ctx, int layer, const float *d_x, int n_rows, const int32_t *d_idx,
+                         const float *d_w, float *d_y, int step_tokens, void *stream) {
+    if (!ctx) return fail(nullptr, MOE_ERR_ARG, "null ctx");
+    if (n_rows < 0 || step_tokens < n_rows || step_tokens < 1)
+        return fail(ctx, MOE_ERR_ARG, "forward_rows: need 0 <= n_rows <= step_tokens, step_tokens >= 1");
+    ctx->clock_tokens = step_tokens;
+    const int rc = ffn_forward_impl(ctx, layer, d_x, n_rows, d_idx, d_w, d_y, stream, nullptr, nullptr, nullptr);
+    ctx->clock_tokens = 0;
+    return rc;
 }
 
 static int ffn_forward_body(moe_ctx *ctx, int layer, const float *d_x, int n_tokens, const int32_t *d_idx,
@@ -835,7 +879,8 @@ static int ffn_forward_impl(moe_ctx *ctx, int layer, const float *d_x, int n_tok
                             float *w_out) {
     int rc = ffn_forward_body(ctx, layer, d_x, n_tokens, d_idx, d_w, d_y, stream, d_logits, idx_out, w_out);
     if (rc || !ctx->preheat || !ctx->n_lent || n_tokens <= 0 || !ctx->d_use) return rc;
-    rc = moe::launch_count_assign(d_idx, n_tokens * ctx->k, ctx->E, ctx->d_use + (size_t)layer * ctx->E, ctx->stream);
+    rc = moe::launch_count_assign(d_idx, n_tokens * ctx->k, ctx->E, ctx->e_base, ctx->d_use + (size_t)layer * ctx->E,
+                                  ctx->stream);
     if (rc) return fail(ctx, MOE_ERR_CUDA, std::string("use counts: ") + cudaGetErrorString((cudaError_t)rc));
     return MOE_OK;
 }
@@ -892,6 +937,7 @@ static int ffn_forward_body(moe_ctx *ctx, int layer, const float *d_x, int n_tok
     gp.cv.miss_cap = ctx->miss_cap;
     gp.cv.hit_bitmap = ctx->d_stepbuf;
     gp.cv.hit_words = ctx->hit_words;
+    gp.cv.clock_tokens = ctx->clock_tokens > 0 ? ctx->clock_tokens : n_tokens;
     gp.tid_gate = layer * 3 + 0;
     gp.tid_up = layer * 3 + 1;
     gp.tid_down = layer * 3 + 2;
@@ -915,6 +961,9 @@ static int ffn_forward_body(moe_ctx *ctx, int layer, const float *d_x, int n_tok
     gp.xq_out = ctx->xq;
     gp.xds_out = ctx->xds;
     gp.fmt = ctx->fmt;
+    gp.idx = d_idx;
+    gp.e_base = ctx->e_base;
+    const bool sharded = ctx->e_base != 0 || ctx->E_route != ctx->E;
     if (small && A <= 256 && ctx->fused_blocks > 0) {
         moe::FusedParams fp{};
         fp.g = gp;
@@ -924,6 +973,7 @@ static int ffn_forward_body(moe_ctx *ctx, int layer, const float *d_x, int n_tok
         fp.exit_count = ctx->exit_count;
         fp.error = ctx->d_error;
         fp.logits = d_logits;
+        fp.n_route = sharded ? ctx->E_route : ctx->Et;
         fp.idx_out = idx_out;
         fp.w_out = w_out;
         fp.renorm = ctx->cfg.renorm_topk;
@@ -936,7 +986,7 @@ static int ffn_forward_body(moe_ctx *ctx, int layer, const float *d_x, int n_tok
             // row-block down mode: each down item sums y for its rows
             fp.rb_rows = rows;
             smem = moe::fused_rb_smem(H, ctx->F, T, ctx->k, ctx->E, rows, &fp.pre_off);
-            if (T == 1 && d_logits && moe::fused_t1_ok(ctx->E, ctx->k)) {
+            if (T == 1 && d_logits && moe::fused_t1_ok(ctx->E, ctx->k) && !sharded) {
                 // one routed token: the gate, up and down table rows follow
                 fp.tbl_off = (int)((smem + 15) / 16 * 16);
                 smem = (size_t)fp.tbl_off + (size_t)24 * ctx->E;
@@ -989,6 +1039,8 @@ static int ffn_forward_body(moe_ctx *ctx, int layer, const float *d_x, int n_tok
     pp.T = T;
     pp.k = ctx->ka;
     pp.E = ctx->Et;
+    pp.e_base = ctx->e_base;
+    pp.E_route = sharded ? ctx->E_route : ctx->Et;
     pp.H = H;
     pp.quantize_x = small ? 1 : 0;
     rc = moe::launch_plan(pp, st);
@@ -1085,6 +1137,9 @@ static int ffn_forward_body(moe_ctx *ctx, int layer, const float *d_x, int n_tok
         L.w = d_w;
         L.y = d_y;
         L.T = T;
+        L.idx = d_idx;
+        L.e_base = ctx->e_base;
+        L.E = ctx->Et;
         L.k = ctx->ka;
         L.H = H;
         L.n_sm = ctx->n_sm;

@@ -1,9 +1,8 @@
 // An allocation-free entry point for one routed-expert FFN layer.
 //
 // Some callers cannot allocate device memory at the point where they run a
-// layer: code that runs while a CUDA graph is being captured in a mode that
-// forbids allocation, processes whose device memory is fully reserved by an
-// outside allocator, or embedded hosts that forbid cudaMalloc after start-up.
+// layer: processes whose device memory is fully reserved by an outside
+// allocator, or embedded hosts that forbid cudaMalloc after start-up.
 // moe_expert_ffn_noalloc serves them: it takes the caller's inputs, outputs
 // and expert tables, and keeps every intermediate (quantized x and h, per-
 // assignment outputs, arrival counters, a private miss log) in one file-scope
@@ -120,6 +119,7 @@ int moe_expert_ffn_noalloc(const float *d_x, int n_tokens, const int32_t *d_idx,
             g.cv.slots_per_tensor = 1;
             g.cv.bitmap_words = (E + 31) / 32;
             g.cv.miss_cap = 3 * E;
+            g.cv.clock_tokens = n_tokens;
             g.tid_gate = 0;
             g.tid_up = 1;
             g.tid_down = 2;
@@ -135,6 +135,9 @@ int moe_expert_ffn_noalloc(const float *d_x, int n_tokens, const int32_t *d_idx,
             g.y = d_y;
             g.xq_out = xq;
             g.xds_out = xds;
+            g.idx = d_idx;
+            g.e_base = 0;
+            fp->n_route = E;
             fp->x = d_x;
             fp->idx = d_idx;
             fp->done_gu = done;

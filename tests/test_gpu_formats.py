@@ -1,7 +1,9 @@
 """GPU parity of the other expert weight formats through the C ABI, against
 the oracle: Q8_0 (blocks of 32 signed 8-bit codes and one binary16 scale,
-w = d * q), Q5_0 (5-bit codes, w = d * (q - 16)) and Q4_K (256-weight
-super-blocks, 6-bit sub-block scales and mins, w = d*sc*q - dmin*m).  Integer block dots
+w = d * q), Q5_0 (5-bit codes, w = d * (q - 16)), Q4_K (256-weight
+super-blocks, 6-bit sub-block scales and mins, w = d*sc*q - dmin*m) and Q6_K
+(256-weight super-blocks, signed 8-bit scales of 16-weight sub-blocks, 6-bit
+codes, w = d*sc*(q - 32)).  Integer block dots
 bit-exact from pool slots and from pinned host memory, whole layers (decode
 and prompt-sized batches, hot and cold experts, ragged shapes), the miss
 log, and the cache state after every promotion pass."""
@@ -16,12 +18,13 @@ from gpu_helpers import Model, check_layer_parity
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 FMTS = [pytest.param(qec.FMT_Q8_0, id="q8_0"), pytest.param(qec.FMT_Q5_0, id="q5_0"),
-        pytest.param(qec.FMT_Q4_K, id="q4_k")]
+        pytest.param(qec.FMT_Q4_K, id="q4_k"), pytest.param(qec.FMT_Q6_K, id="q6_k")]
+K_QUANTS = (qec.FMT_Q4_K, qec.FMT_Q6_K)
 
 
 def _fits(fmt, H, F):
-    """Q4_K needs hidden and FFN widths that are multiples of its 256-weight super-blocks."""
-    return fmt != qec.FMT_Q4_K or (H % 256 == 0 and F % 256 == 0)
+    """The K-quants need hidden and FFN widths that are multiples of their 256-weight super-blocks."""
+    return fmt not in K_QUANTS or (H % 256 == 0 and F % 256 == 0)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -54,6 +57,10 @@ def test_block_dots_bit_exact_hot_and_cold(fmt):
                     # raw sub-block dots: 8 per 256-weight super-block
                     ref = np.array([np.concatenate([oracle.subblock_dots(W[5 + r, u], qa[256 * u:256 * u + 256])
                                                     for u in range(cols // 256)]) for r in range(n_rows)])
+                elif fmt == qec.FMT_Q6_K:
+                    # per 32 weights: the two 16-weight sub-blocks' scaled dots
+                    ref = np.array([np.concatenate([oracle.q6k_blockdots(W[5 + r, u], qa[256 * u:256 * u + 256])
+                                                    for u in range(cols // 256)]) for r in range(n_rows)])
                 else:
                     ref = np.array([[oracle.block_dot(W[5 + r, b], qa[32 * b:32 * b + 32])
                                      for b in range(cols // 32)] for r in range(n_rows)])
@@ -69,7 +76,7 @@ def test_block_dots_bit_exact_hot_and_cold(fmt):
                                        (768, 1024, 16, 3, 40), (2048, 1536, 64, 8, 1)])
 def test_layer_parity_hot_and_cold(H, F, E, k, T, fmt):
     if not _fits(fmt, H, F):
-        pytest.skip("Q4_K needs widths that are multiples of 256")
+        pytest.skip("the K-quants need widths that are multiples of 256")
     m = Model(H=H, F=F, E=E, k=k, L=2, capacity=E // 2, max_tokens=T, zipf_s=0.6, weight_format=fmt)
     try:
         for layer in range(2):
@@ -89,7 +96,7 @@ def test_layer_parity_hot_and_cold(H, F, E, k, T, fmt):
 
 @pytest.mark.parametrize("fmt", FMTS)
 def test_routed_forward_and_cache_steps(fmt):
-    F = 512 if fmt == qec.FMT_Q4_K else 384
+    F = 512 if fmt in K_QUANTS else 384
     m = Model(H=512, F=F, E=32, k=4, L=2, capacity=8, max_tokens=4, window=8, zipf_s=1.1, weight_format=fmt)
     try:
         for step in range(30):
