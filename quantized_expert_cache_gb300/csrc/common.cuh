@@ -27,15 +27,16 @@ __host__ __device__ inline size_t blob_bytes(int rows, int nb) { return (size_t)
 // bytes as Q4 plus a 32-bit word of fifth bits, w = d (q - 16)).  Blob
 // layout, N = rows x nb blocks: [codes: N x 16 or 32 B][Q5_0 only: fifth
 // bits, N x 4 B][scales: N x binary16]; code_bytes counts both code planes.
-// The K-quants keep one header per 256-weight super-block (8 blocks):
-// Q4_K (6-bit sub-block scales and mins) is repacked per 32-weight sub-block
-// into Q4-order nibbles, and its scale plane holds the super-block's 16-byte
-// header as stored (d, dmin, the 12 bytes of packed scales and mins).  Q6_K
-// (16-weight sub-blocks with signed 8-bit scales, 6-bit codes) keeps per
-// block the low nibbles in Q4 order (16 B), the high bit pairs (8 B: word h,
-// byte b, bits 2i..2i+1 = element 16h + 4i + b) and the two sub-block scales
-// (2 B) in its code planes, and the super-block's binary16 d in its scale
-// plane.  Both take the canonical bytes per weight (18 and 26.25 per 32).
+// Q4_K (256-weight super-blocks with 6-bit sub-block scales and mins) is
+// repacked per 32-weight sub-block: Q4-order nibbles, and the exact fp32 pair
+// (d * sc, dmin * m) in the scale plane (8 bytes per block instead of the
+// canonical 2.25: decoding the packed 6-bit pairs in the kernel measured
+// slower than reading the pairs).  Q6_K (16-weight sub-blocks with signed
+// 8-bit scales, 6-bit codes) keeps per block the low nibbles in Q4 order
+// (16 B), the high bit pairs (8 B: word h, byte b, bits 2i..2i+1 = element
+// 16h + 4i + b) and the two sub-block scales (2 B) in its code planes, and
+// the super-block's binary16 d in its scale plane: the canonical 26.25 bytes
+// per 32 weights.
 constexpr int kFmtQ4 = 0, kFmtQ8 = 1, kFmtQ5 = 2, kFmtQ4K = 3, kFmtQ6K = 4;
 __host__ __device__ constexpr int code_bytes(int fmt) {
     return fmt == kFmtQ8 ? 32 : fmt == kFmtQ5 ? 20 : fmt == kFmtQ6K ? 26 : 16;
@@ -45,7 +46,7 @@ __host__ __device__ inline size_t blob_scales_offset_fmt(int fmt, int rows, int 
 }
 // bytes of the scale plane of n blocks (n a multiple of 8 for the K-quants)
 __host__ __device__ inline size_t scale_plane_bytes(int fmt, size_t n) {
-    return fmt == kFmtQ4K ? n / 8 * 16 : fmt == kFmtQ6K ? n / 8 * 2 : n * 2;
+    return fmt == kFmtQ4K ? n * 8 : fmt == kFmtQ6K ? n / 8 * 2 : n * 2;
 }
 __host__ __device__ inline size_t blob_bytes_fmt(int fmt, int rows, int nb) {
     const size_t n = (size_t)rows * nb;
@@ -189,28 +190,12 @@ struct WScale {
 };
 template <>
 struct WScale<kFmtQ4K> {
-    float sc, mn;  // d * sc_j and dmin * m_j of the block's sub-block j (exact in fp32)
-    // block i is sub-block j = i mod 8 of super-block i / 8 (rows hold whole
-    // super-blocks); the 8 lanes reading one super-block share its header
+    float2 sm;  // (d * sc_j, dmin * m_j) of the block's sub-block
     __device__ __forceinline__ void load(const uint8_t *scales, size_t i) {
-        const uint4 h = __ldg((const uint4 *)scales + i / 8);
-        const int j = (int)(i & 7);
-        // the 12 packed bytes b[0..11] = header bytes 4..15
-        const unsigned long long b07 = (unsigned long long)h.y | ((unsigned long long)h.z << 32);
-        auto byte = [&](int k) { return k < 8 ? (int)((b07 >> (8 * k)) & 255u) : (int)((h.w >> (8 * (k - 8))) & 255u); };
-        int s6, m6;
-        if (j < 4) {
-            s6 = byte(j) & 63;
-            m6 = byte(j + 4) & 63;
-        } else {
-            s6 = (byte(j + 4) & 15) | ((byte(j - 4) >> 6) << 4);
-            m6 = (byte(j + 4) >> 4) | ((byte(j) >> 6) << 4);
-        }
-        sc = __half2float(__ushort_as_half((unsigned short)(h.x & 0xffffu))) * (float)s6;
-        mn = __half2float(__ushort_as_half((unsigned short)(h.x >> 16))) * (float)m6;
+        sm = __ldcs((const float2 *)scales + i);
     }
     __device__ __forceinline__ float term(int dot, const BlockScale &a) const {
-        return a.d * (sc * (float)dot - mn * (float)a.s);
+        return a.d * (sm.x * (float)dot - sm.y * (float)a.s);
     }
 };
 template <>

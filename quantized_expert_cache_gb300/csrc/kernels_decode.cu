@@ -1252,7 +1252,8 @@ __device__ __forceinline__ void t1_route_gate_up(const FusedParams &p, int *s_e,
     }
 
     // ---- the CTA's first down item (rows [rb R, rb R + R) of every pick),
-    // staged by warps 1..7 (pick u by warp 1 + u mod 7) once the pick is out
+    // staged by warps 1..7 (pick u by warp 1 + u mod 7) once the pick is out;
+    // a cold pick's rows are left for the down item (stage_cold_down)
     auto stage_first_down = [&]() {
         if (warp == 0 || (int)blockIdx.x >= n_dn_items) return;
         const int rb = blockIdx.x;
@@ -1271,7 +1272,9 @@ __device__ __forceinline__ void t1_route_gate_up(const FusedParams &p, int *s_e,
                 __threadfence_block();
             }
             __syncwarp();
-            const uint8_t *bd = (const uint8_t *)(uintptr_t)(s_td[v_e[u]] & ~1ull);
+            const uint64_t ent = s_td[v_e[u]];
+            if (ent & 1ull) continue;  // cold
+            const uint8_t *bd = (const uint8_t *)(uintptr_t)ent;
             for (int j = lane; j < per; j += 32) {
                 if (j < nc)
                     cp_async16(dpre + ((size_t)u * nc + j) * 16, bd + ((size_t)rb * nc + j) * 16);
@@ -1366,6 +1369,64 @@ __device__ __forceinline__ void t1_route_gate_up(const FusedParams &p, int *s_e,
     }
     if (m == 0) stage_first_down();  // a CTA without a gate/up item
     __syncthreads();  // routing results for CTAs without a gate/up item
+}
+
+// One routed token: the down rows of the cold picks (read zero-copy over the
+// host link) for this CTA's first down item, requested only once every cold
+// pick's gate/up items are done.  Every down item needs the h of every pick,
+// so the link first serves the gate/up bytes that gate the whole down phase;
+// rows requested as soon as a CTA's own gate/up item was done made the last
+// gate/up items wait behind other CTAs' down rows (all-cold layer: 229 ->
+// 168 us with the register loads below).
+__device__ void stage_cold_down(const FusedParams &p, const int *s_uniq, int nu, uint8_t *dsm, uint8_t *dpre,
+                                int rgs) {
+    const GemvParams &g = p.g;
+    const int E = g.cv.E, H = g.H, nbf = g.F / kBlock, R = p.rb_rows;
+    const uint64_t *s_td = (const uint64_t *)(dsm + p.tbl_off) + 2 * E;
+    unsigned cold = 0u;  // bit u: pick u is cold
+    for (int u = 0; u < nu; ++u) cold |= (unsigned)(s_td[s_uniq[u]] & 1ull) << u;
+    if (!cold) return;
+    if (threadIdx.x == 0) {
+        const long long t0 = clock64();
+        for (int u = 0; u < nu; ++u) {
+            if (!((cold >> u) & 1u)) continue;
+            while (ld_acquire(&p.done_gu[u]) < (unsigned)rgs) {
+                if (clock64() - t0 > 4000000000ll) {
+                    atomicOr(p.error, 2);
+                    break;
+                }
+                __nanosleep(64);
+            }
+        }
+    }
+    __syncthreads();
+    const int rb = blockIdx.x;
+    const int nc = R * nbf, ns = R * nbf / 8, per = nc + ns;
+    const size_t soff = blob_scales_offset(H, nbf);
+    // the CTA's threads walk the cold picks one after the other (pick-major),
+    // so that at any moment the CTAs of the grid read neighbouring rows of
+    // the same expert: one sequential stream through each cold blob instead
+    // of a few hundred scattered ones, which host memory serves at about
+    // twice the rate
+    const int n_cold = __popc(cold);
+    for (int j = threadIdx.x; j < n_cold * per; j += blockDim.x) {
+        const int c = j / per, q = j - c * per;
+        int u = 0;  // the c-th cold pick
+        for (int left = c; u < nu; ++u)
+            if ((cold >> u) & 1u) {
+                if (left == 0) break;
+                --left;
+            }
+        const uint8_t *bd = (const uint8_t *)(uintptr_t)(s_td[s_uniq[u]] & ~1ull);
+        // register loads, not cp.async: from host memory the asynchronous
+        // copies of this pattern ran at half the link rate in this kernel
+        if (q < nc)
+            *(uint4 *)(dpre + ((size_t)u * nc + q) * 16) = ld_weights((const uint4 *)(bd + ((size_t)rb * nc + q) * 16));
+        else
+            *(uint4 *)(dpre + (size_t)nu * nc * 16 + ((size_t)u * ns + (q - nc)) * 16) =
+                ld_weights((const uint4 *)(bd + soff + (size_t)rb * nc * 2 + (size_t)(q - nc) * 16));
+    }
+    __syncthreads();
 }
 
 template <int LD, int NT, bool RB>
@@ -1556,6 +1617,7 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
             const int sub = threadIdx.x % LD;
             cp_async_wait_all();
             __syncthreads();  // the first item's staged rows
+            if (t1) stage_cold_down(p, s_uniq, nu, dsm, dpre, rgs);
             for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
                 const bool first = item == (int)blockIdx.x;
                 if (!first) {

@@ -252,13 +252,29 @@ int sync_all(moe_ctx *ctx) {
     return MOE_OK;
 }
 
-// Q4_K super-block (144 bytes, 256 weights) -> 8 sub-blocks of Q4-order
-// nibbles (byte t = element t | element t + 16 << 4) and the 16-byte header
-// (d, dmin, packed 6-bit scales and mins) as stored.
-void repack_q4k_super(const uint8_t *sb, uint8_t *codes, uint8_t *header) {
-    memcpy(header, sb, 16);
-    const uint8_t *qs = sb + 16;
+// Q4_K super-block (144 bytes, 256 weights) -> 8 sub-blocks: Q4-order
+// nibbles (byte t = element t | element t + 16 << 4) and the exact fp32
+// pairs (d * sc_j, dmin * m_j) (binary16 times a 6-bit integer fits fp32).
+void repack_q4k_super(const uint8_t *sb, uint8_t *codes, float *sm) {
+    auto h2f = [](const uint8_t *p) {
+        __half h;
+        uint16_t b = (uint16_t)(p[0] | (p[1] << 8));
+        memcpy(&h, &b, 2);
+        return __half2float(h);
+    };
+    const float d = h2f(sb), dmin = h2f(sb + 2);
+    const uint8_t *sc = sb + 4, *qs = sb + 16;
     for (int j = 0; j < 8; ++j) {
+        int s6, m6;
+        if (j < 4) {
+            s6 = sc[j] & 63;
+            m6 = sc[j + 4] & 63;
+        } else {
+            s6 = (sc[j + 4] & 15) | ((sc[j - 4] >> 6) << 4);
+            m6 = (sc[j + 4] >> 4) | ((sc[j] >> 6) << 4);
+        }
+        sm[2 * j] = d * (float)s6;
+        sm[2 * j + 1] = dmin * (float)m6;
         const uint8_t *chunk = qs + 32 * (j / 2);
         const int shift = (j & 1) ? 4 : 0;
         for (int t = 0; t < 16; ++t) {
@@ -301,8 +317,8 @@ void repack(const uint8_t *src, uint8_t *dst, int fmt, int n_experts, int rows, 
             if (fmt == moe::kFmtQ4K) {
                 const uint8_t *s = src + (size_t)e * (nblk / 8) * 144;
                 uint8_t *q = dst + (size_t)e * stride;
-                uint8_t *hd = q + nblk * 16;
-                for (size_t u = 0; u < nblk / 8; ++u) repack_q4k_super(s + 144 * u, q + 128 * u, hd + 16 * u);
+                float *sm = (float *)(q + nblk * 16);
+                for (size_t u = 0; u < nblk / 8; ++u) repack_q4k_super(s + 144 * u, q + 128 * u, sm + 16 * u);
                 continue;
             }
             if (fmt == moe::kFmtQ6K) {
