@@ -1371,18 +1371,17 @@ __device__ __forceinline__ void t1_route_gate_up(const FusedParams &p, int *s_e,
     __syncthreads();  // routing results for CTAs without a gate/up item
 }
 
-// One routed token: the down rows of the cold picks (read zero-copy over the
-// host link) for this CTA's first down item, requested only once every cold
-// pick's gate/up items are done.  Every down item needs the h of every pick,
+// Row-block mode: the down rows of the cold used experts (read zero-copy over
+// the host link) for this CTA's first down item, requested only once every
+// cold expert's gate/up items are done.  Every down item needs the h of every pick,
 // so the link first serves the gate/up bytes that gate the whole down phase;
 // rows requested as soon as a CTA's own gate/up item was done made the last
 // gate/up items wait behind other CTAs' down rows (all-cold layer: 229 ->
 // 168 us with the register loads below).
-__device__ void stage_cold_down(const FusedParams &p, const int *s_uniq, int nu, uint8_t *dsm, uint8_t *dpre,
+__device__ void stage_cold_down(const FusedParams &p, const int *s_uniq, int nu, const uint64_t *s_td, uint8_t *dpre,
                                 int rgs) {
     const GemvParams &g = p.g;
-    const int E = g.cv.E, H = g.H, nbf = g.F / kBlock, R = p.rb_rows;
-    const uint64_t *s_td = (const uint64_t *)(dsm + p.tbl_off) + 2 * E;
+    const int H = g.H, nbf = g.F / kBlock, R = p.rb_rows;
     unsigned cold = 0u;  // bit u: pick u is cold
     for (int u = 0; u < nu; ++u) cold |= (unsigned)(s_td[s_uniq[u]] & 1ull) << u;
     if (!cold) return;
@@ -1524,19 +1523,28 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
     const int n_dn_items = RB ? H / R : nu * n_rb_all;
     const bool prefetched = (int)blockIdx.x < n_dn_items;
     bool pf_issued = !prefetched || t1;  // (one routed token: staged during routing)
-    // warp w stages the rows of used experts w, w + 8, ...
-    auto stage_rb = [&](int rb) {
+    bool pf_cold = false;                // per-expert mode: the first item's expert is cold (not staged)
+    // warp w stages the rows of used experts w, w + 8, ...; a cold expert's
+    // rows (host memory) are left to stage_cold_down on the first item
+    // (early) and read with register loads on later ones (cp.async from host
+    // memory ran at half the link rate)
+    auto stage_rb = [&](int rb, bool early) {
         const int nc = R * nbf, ns = R * nbf / 8, per = nc + ns;
         const size_t soff = blob_scales_offset(H, nbf);
         for (int u = warp; u < nu; u += kWarps) {
             const uint64_t ed = g.cv.tbl[(size_t)g.tid_down * g.cv.E + s_uniq[u]];
+            const bool cold = ed & 1ull;
+            if (cold && early) continue;
             const uint8_t *bd = (const uint8_t *)(uintptr_t)(ed & ~1ull);
             for (int j = lane; j < per; j += 32) {
-                if (j < nc)
-                    cp_async16(dpre + ((size_t)u * nc + j) * 16, bd + ((size_t)rb * nc + j) * 16);
+                uint8_t *dst = j < nc ? dpre + ((size_t)u * nc + j) * 16
+                                      : dpre + (size_t)nu * nc * 16 + ((size_t)u * ns + (j - nc)) * 16;
+                const uint8_t *src = j < nc ? bd + ((size_t)rb * nc + j) * 16
+                                            : bd + soff + (size_t)rb * nc * 2 + (size_t)(j - nc) * 16;
+                if (cold)
+                    *(uint4 *)dst = ld_weights((const uint4 *)src);
                 else
-                    cp_async16(dpre + (size_t)nu * nc * 16 + ((size_t)u * ns + (j - nc)) * 16,
-                               bd + soff + (size_t)rb * nc * 2 + (size_t)(j - nc) * 16);
+                    cp_async16(dst, src);
             }
         }
         cp_async_commit();
@@ -1545,11 +1553,17 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
         if (pf_issued) return;
         pf_issued = true;
         if (RB) {
-            stage_rb(blockIdx.x);
+            stage_rb(blockIdx.x, true);
             return;
         }
         const int u = blockIdx.x / n_rb_all, rb = blockIdx.x - u * n_rb_all;
         const uint64_t ed = g.cv.tbl[(size_t)g.tid_down * g.cv.E + s_uniq[u]];
+        if (ed & 1ull) {
+            // cold: the item reads its rows itself (register loads) once the
+            // expert's h is out
+            pf_cold = true;
+            return;
+        }
         const uint8_t *bd = (const uint8_t *)(uintptr_t)(ed & ~1ull);
         const uint8_t *codes = bd + (size_t)rb * DROWS * nbf * 16;
         const uint8_t *scales = bd + blob_scales_offset(H, nbf) + (size_t)rb * DROWS * nbf * 2;
@@ -1617,12 +1631,15 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
             const int sub = threadIdx.x % LD;
             cp_async_wait_all();
             __syncthreads();  // the first item's staged rows
-            if (t1) stage_cold_down(p, s_uniq, nu, dsm, dpre, rgs);
+            stage_cold_down(p, s_uniq, nu,
+                            t1 ? (const uint64_t *)(dsm + p.tbl_off) + 2 * g.cv.E
+                               : g.cv.tbl + (size_t)g.tid_down * g.cv.E,
+                            dpre, rgs);
             for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
                 const bool first = item == (int)blockIdx.x;
                 if (!first) {
                     __syncthreads();  // the previous item's reads of the staged rows and s_o
-                    stage_rb(item);
+                    stage_rb(item, false);
                     cp_async_wait_all();
                     __syncthreads();
                 }
@@ -1717,7 +1734,7 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
             const uint4 *qd = (const uint4 *)bd + (size_t)r * nbf;
             const __half *dd = (const __half *)(bd + scale_off) + (size_t)r * nbf;
             bool waited = false;
-            const bool from_smem = prefetched && item == (int)blockIdx.x;
+            const bool from_smem = prefetched && !pf_cold && item == (int)blockIdx.x;
             for (int c0 = a0; c0 < a1; c0 += NT) {
                 const int nt = min(NT, a1 - c0);
                 dn_chunk<NT, LD>(p, c0, nt, e, r, rloc, sub, qd, dd, hq_s, hds_s, dpre, from_smem, waited, s_asg);
