@@ -60,6 +60,7 @@ def configure(L):
     L.orc_row_dot_fmt.argtypes = [vp, vp, vp, i32, i32, vp]
     L.orc_k4_subdots.argtypes = [vp, vp, vp]
     L.orc_k6_blockdots.argtypes = [vp, vp, vp]
+    L.orc_k5_subdots.argtypes = [vp, vp, vp]
     L.orc_expert.argtypes = [vp, vp, vp, i32, i32, vp, vp] + [vp] * 8 + [i32]
     L.orc_down_combine.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, i32]
     L.orc_layer.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp] + [vp] * 9 + [i32]
@@ -107,14 +108,14 @@ def quantize(x: np.ndarray):
     return q, d
 
 
-# canonical block size -> format (0: Q4, 1: Q8_0, 2: Q5_0, 3: Q4_K, 4: Q6_K)
-BLOCK_BYTES = {18: 0, 34: 1, 22: 2, 144: 3, 210: 4}
-ELEMS = {0: 32, 1: 32, 2: 32, 3: 256, 4: 256}  # weights per canonical block
+# canonical block size -> format (0: Q4, 1: Q8_0, 2: Q5_0, 3: Q4_K, 4: Q6_K, 5: Q5_K)
+BLOCK_BYTES = {18: 0, 34: 1, 22: 2, 144: 3, 210: 4, 176: 5}
+ELEMS = {0: 32, 1: 32, 2: 32, 3: 256, 4: 256, 5: 256}  # weights per canonical block
 
 
 def _fmt(blocks) -> int:
     """Format of canonical blocks from their last dimension (18: Q4, 34: Q8_0, 22: Q5_0,
-    144: Q4_K and 210: Q6_K super-blocks of 256 weights)."""
+    144: Q4_K, 210: Q6_K and 176: Q5_K super-blocks of 256 weights)."""
     if blocks.shape[-1] not in BLOCK_BYTES:
         raise ValueError(f"unknown block size {blocks.shape[-1]}")
     return BLOCK_BYTES[blocks.shape[-1]]
@@ -137,6 +138,16 @@ def subblock_dots(superblock: np.ndarray, qa: np.ndarray) -> np.ndarray:
     qa = np.ascontiguousarray(qa, np.int8)
     out = np.empty(8, np.int32)
     lib().orc_k4_subdots(_p(sb), _p(qa), _p(out))
+    return out
+
+
+def q5k_subdots(superblock: np.ndarray, qa: np.ndarray) -> np.ndarray:
+    """Q5_K: raw integer dots sum q*a (q in 0..31) of the 8 sub-blocks of one super-block."""
+    sb = np.ascontiguousarray(superblock, np.uint8)
+    assert sb.size == 176 and qa.size == 256
+    qa = np.ascontiguousarray(qa, np.int8)
+    out = np.empty(8, np.int32)
+    lib().orc_k5_subdots(_p(sb), _p(qa), _p(out))
     return out
 
 

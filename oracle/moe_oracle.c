@@ -47,6 +47,11 @@
  *  and its element 32m + l (m = 0..3, l < 32) keeps its low four bits in
  *  ql[64n + l + 32 (m & 1)] (the low nibble for m < 2, the high one for
  *  m >= 2) and its high two bits in bits 2m..2m+1 of qh[32n + l].
+ *  5 = Q5_K, another K-quant: the Q4_K super-block with a fifth code bit,
+ *  w = d*sc_j*q - dmin*m_j, q in 0..31.  The 176-byte layout is the one the
+ *  format is published with: d, dmin, the 12 scale/min bytes packed as for
+ *  Q4_K, 32 bytes qh, then 128 code bytes qs in the Q4_K chunk order; bit j
+ *  of qh[l] is the fifth bit of element l of sub-block j.
  *
  * Readings where the pages are silent (each listed in the design notes):
  *  - top-k order is (logit descending, expert index ascending): ties go to
@@ -77,6 +82,7 @@
 
 #define ORC_K4_SUPER_BYTES 144
 #define ORC_K6_SUPER_BYTES 210
+#define ORC_K5_SUPER_BYTES 176
 
 double orc_h2d(uint16_t h);
 
@@ -89,6 +95,7 @@ static size_t orc_bbytes(int fmt) {
 static size_t orc_row_bytes(int fmt, int nb) {
     if (fmt == 3) return (size_t)(nb / 8) * ORC_K4_SUPER_BYTES;
     if (fmt == 4) return (size_t)(nb / 8) * ORC_K6_SUPER_BYTES;
+    if (fmt == 5) return (size_t)(nb / 8) * ORC_K5_SUPER_BYTES;
     return (size_t)nb * orc_bbytes(fmt);
 }
 
@@ -142,6 +149,25 @@ static int orc_k4_code(const uint8_t *sb, int i) {
     const uint8_t *qs = sb + 16;
     const int c = i / 64, r = i % 64;
     return r < 32 ? (qs[32 * c + r] & 15) : (qs[32 * c + r - 32] >> 4);
+}
+
+/* Q5_K: 5-bit code of element i (0..255) of a super-block: the low four bits
+ * as in Q4_K (from the code bytes after qh), the fifth from qh. */
+static int orc_k5_code(const uint8_t *sb, int i) {
+    const uint8_t *qh = sb + 16, *qs = sb + 48;
+    const int c = i / 64, r = i % 64, j = i / 32, l = i % 32;
+    const int lo = r < 32 ? (qs[32 * c + r] & 15) : (qs[32 * c + r - 32] >> 4);
+    return lo | (((qh[l] >> j) & 1) << 4);
+}
+
+/* Q5_K: raw integer dots sum_i q_i * a_i of the 8 sub-blocks against 256
+ * int8 activations (exact in int32: |sum| <= 32 * 31 * 127). */
+void orc_k5_subdots(const uint8_t *sb, const int8_t *qa, int32_t *out) {
+    for (int j = 0; j < 8; ++j) {
+        int32_t s = 0;
+        for (int i = 0; i < 32; ++i) s += (int32_t)orc_k5_code(sb, 32 * j + i) * (int32_t)qa[32 * j + i];
+        out[j] = s;
+    }
 }
 
 /* Q4_K: raw integer dots sum_i q_i * a_i of the 8 sub-blocks against 256
@@ -293,6 +319,18 @@ void orc_dequant_fmt(const uint8_t *blocks, int nb, int fmt, double *out) {
         }
         return;
     }
+    if (fmt == 5) { /* Q5_K: w = d * sc_j * q - dmin * m_j, q in 0..31 */
+        for (int s = 0; s < nb / 8; ++s) {
+            const uint8_t *sb = blocks + (size_t)s * ORC_K5_SUPER_BYTES;
+            const double d = orc_h2d(orc_block_scale(sb)), dmin = orc_h2d(orc_block_scale(sb + 2));
+            for (int i = 0; i < 256; ++i) {
+                int sc, m;
+                orc_k4_scale_min(sb, i / 32, &sc, &m);
+                out[(size_t)s * 256 + i] = d * sc * (double)orc_k5_code(sb, i) - dmin * m;
+            }
+        }
+        return;
+    }
     if (fmt == 3) { /* nb counts 32-weight blocks; super-blocks of 8 */
         for (int s = 0; s < nb / 8; ++s) {
             const uint8_t *sb = blocks + (size_t)s * ORC_K4_SUPER_BYTES;
@@ -346,13 +384,17 @@ double orc_row_dot_fmt(const uint8_t *row, const int8_t *qa, const uint16_t *da,
         if (abs_sum) *abs_sum = aacc;
         return acc;
     }
-    if (fmt == 3) {
+    if (fmt == 3 || fmt == 5) {
         /* per sub-block b: d_a,b * (d * sc * sum q*a - dmin * m * sum a) */
+        const size_t sbytes = fmt == 3 ? ORC_K4_SUPER_BYTES : ORC_K5_SUPER_BYTES;
         for (int s = 0; s < nb / 8; ++s) {
-            const uint8_t *sb = row + (size_t)s * ORC_K4_SUPER_BYTES;
+            const uint8_t *sb = row + (size_t)s * sbytes;
             const double d = orc_h2d(orc_block_scale(sb)), dmin = orc_h2d(orc_block_scale(sb + 2));
             int32_t raw[8];
-            orc_k4_subdots(sb, qa + (size_t)s * 256, raw);
+            if (fmt == 3)
+                orc_k4_subdots(sb, qa + (size_t)s * 256, raw);
+            else
+                orc_k5_subdots(sb, qa + (size_t)s * 256, raw);
             for (int j = 0; j < 8; ++j) {
                 const int b = 8 * s + j;
                 int sc, m;

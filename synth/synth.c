@@ -192,6 +192,29 @@ void synth_q5_blocks(uint64_t key, uint8_t *out, size_t n_blocks, double dlo, do
  * uniform bytes (12 bytes of packed 6-bit sub-block scales and mins, every
  * pattern valid and every 6-bit value equally likely, and 128 code bytes).
  */
+/*
+ * Q5_K super-blocks of 256 weights in the published layout, 176 bytes each:
+ * d ~ U(dlo, dhi) and dmin ~ U(mlo, mhi) as binary16, then 172 uniform bytes
+ * (packed 6-bit scales and mins, the fifth-bit bytes qh, the code bytes).
+ */
+void synth_q5k_blocks(uint64_t key, uint8_t *out, size_t n_super, double dlo, double dhi, double mlo, double mhi) {
+    xo_t g;
+    xo_init(&g, key);
+    for (size_t b = 0; b < n_super; ++b) {
+        uint8_t *sb = out + b * 176;
+        uint16_t h = gen_f16_bits((float)(dlo + (dhi - dlo) * xo_unit(&g)));
+        uint16_t hm = gen_f16_bits((float)(mlo + (mhi - mlo) * xo_unit(&g)));
+        sb[0] = (uint8_t)(h & 0xff);
+        sb[1] = (uint8_t)(h >> 8);
+        sb[2] = (uint8_t)(hm & 0xff);
+        sb[3] = (uint8_t)(hm >> 8);
+        for (int w = 0; w < 172; w += 4) {
+            uint64_t v = xo_next(&g);
+            for (int j = 0; j < 4; ++j) sb[4 + w + j] = (uint8_t)(v >> (8 * j));
+        }
+    }
+}
+
 void synth_q4k_blocks(uint64_t key, uint8_t *out, size_t n_super, double dlo, double dhi, double mlo, double mhi) {
     xo_t g;
     xo_init(&g, key);
@@ -246,11 +269,18 @@ typedef struct {
 
 static void *q4_worker(void *arg) {
     q4_job_t *j = (q4_job_t *)arg;
-    const size_t bb = j->fmt == 1 ? 34 : j->fmt == 2 ? 22 : j->fmt == 3 ? 144 : j->fmt == 4 ? 210 : 18;
+    const size_t bb = j->fmt == 1   ? 34
+                      : j->fmt == 2 ? 22
+                      : j->fmt == 3 ? 144
+                      : j->fmt == 4 ? 210
+                      : j->fmt == 5 ? 176
+                                    : 18;
     for (int e = j->e0; e < j->e1; ++e) {
         uint64_t key = synth_key(j->seed, 1, j->tag, (uint64_t)e, 0);
         uint8_t *dst = j->out + (size_t)e * j->blocks_per_expert * bb;
-        if (j->fmt == 4)
+        if (j->fmt == 5)
+            synth_q5k_blocks(key, dst, j->blocks_per_expert, j->dlo, j->dhi, 0.0006, 0.0025);
+        else if (j->fmt == 4)
             synth_q6k_blocks(key, dst, j->blocks_per_expert, j->dlo, j->dhi);
         else if (j->fmt == 3)
             synth_q4k_blocks(key, dst, j->blocks_per_expert, j->dlo, j->dhi, 0.0006, 0.0025);
@@ -268,14 +298,15 @@ static void *q4_worker(void *arg) {
  * All experts of one expert tensor, expert-major: out[e][block] (18 B each
  * for Q4, fmt 0; 34 B for Q8_0, fmt 1; 22 B for Q5_0, fmt 2; 144-byte
  * super-blocks of 256 weights for Q4_K, fmt 3, with dmin ~ U(0.0006, 0.0025);
- * 210-byte super-blocks for Q6_K, fmt 4).
+ * 210-byte super-blocks for Q6_K, fmt 4; 176-byte super-blocks for Q5_K,
+ * fmt 5, dmin as for Q4_K).
  * Expert e is drawn from its own stream keyed by (seed, 1, tensor_tag, e), so
  * the result does not depend on n_threads and any expert can be regenerated
  * alone with synth_experts(seed, tag, e, e+1, ...).
  */
 void synth_experts(uint64_t seed, uint64_t tensor_tag, int e_begin, int e_end, size_t blocks_per_expert,
                    uint8_t *out, double dlo, double dhi, int n_threads, int fmt) {
-    const size_t bb = fmt == 1 ? 34 : fmt == 2 ? 22 : fmt == 3 ? 144 : fmt == 4 ? 210 : 18;
+    const size_t bb = fmt == 1 ? 34 : fmt == 2 ? 22 : fmt == 3 ? 144 : fmt == 4 ? 210 : fmt == 5 ? 176 : 18;
     int n = e_end - e_begin;
     if (n <= 0) return;
     if (n_threads < 1) n_threads = 1;

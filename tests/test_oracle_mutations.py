@@ -47,6 +47,8 @@ C_MUTANTS = [
      "const int hi = (qh[i % 64] >> (2 * (i / 64))) & 3;"),
     ("q6k low nibble byte", "const uint8_t lb = ql[64 * n + 32 * (m & 1) + l];",
      "const uint8_t lb = ql[64 * n + 32 * (m >> 1) + l];"),
+    ("q5k fifth bit index", "return lo | (((qh[l] >> j) & 1) << 4);", "return lo | (((qh[j] >> l) & 1) << 4);"),
+    ("q5k code bytes offset", "const uint8_t *qh = sb + 16, *qs = sb + 48;", "const uint8_t *qh = sb + 16, *qs = sb + 44;"),
     ("q6k offset 31", "t += (int32_t)(orc_k6_code(sb, e) - 32) * (int32_t)qa[e];",
      "t += (int32_t)(orc_k6_code(sb, e) - 31) * (int32_t)qa[e];"),
 ]
@@ -62,9 +64,10 @@ C_PINS = [pins.test_h2d_all_bit_patterns_vs_numpy, pins.test_f2h_vs_numpy_random
           pins.test_quantizer_zero_and_tiny_blocks, pins.test_q5_block_dot_brute_force_every_code,
           pins.test_q5_dequant_and_layer_vs_dense_fp64, pins.test_q4k_brute_force_vs_independent_decode,
           pins.test_q4k_layer_vs_dense_fp64, pins.test_shared_expert_layer_vs_dense_fp64,
-          pins.test_q6k_brute_force_vs_independent_decode, pins.test_q6k_layer_vs_dense_fp64]
+          pins.test_q6k_brute_force_vs_independent_decode, pins.test_q6k_layer_vs_dense_fp64,
+          pins.test_q5k_brute_force_vs_independent_decode, pins.test_q5k_layer_vs_dense_fp64]
 C_GOLDEN_PINS = [pins.test_h2d_golden, pins.test_block_dot_golden, pins.test_q8_block_dot_golden,
-                 pins.test_q5_block_dot_golden, pins.test_q4k_golden, pins.test_q6k_golden]
+                 pins.test_q5_block_dot_golden, pins.test_q4k_golden, pins.test_q6k_golden, pins.test_q5k_golden]
 
 
 def _failing_pins(run):

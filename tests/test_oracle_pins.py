@@ -569,7 +569,90 @@ def test_q4k_layer_vs_dense_fp64():
     np.testing.assert_allclose(y, y_bf, rtol=1e-12, atol=1e-12 * np.abs(y_bf).max())
 
 
-@pytest.mark.parametrize("fmt", [synth.FMT_Q8_0, synth.FMT_Q5_0, synth.FMT_Q4_K])
+# ---------------------------------------------------------------- Q5_K weights
+def _np_q5k(sb):
+    """Independent Q5_K decode with numpy: [..., 176] super-blocks -> codes
+    [..., 256] (0..31), per-sub-block scales and mins [..., 8], d and dmin.
+    The scale/min bytes and the code bytes decode as in Q4_K; bit j of qh[l]
+    adds 16 to element l of sub-block j."""
+    sb = np.asarray(sb, np.uint8)
+    as_q4k = np.concatenate([sb[..., 0:16], sb[..., 48:176]], axis=-1)
+    lo, sc, mn, d, dmin = _np_dequant_q4k(as_q4k)
+    qh = sb[..., 16:48].astype(np.int64)                                  # [..., 32]
+    hi = (qh[..., None, :] >> np.arange(8)[:, None]) & 1                 # [..., 8, 32]
+    codes = lo + 16 * hi.reshape(sb.shape[:-1] + (256,))
+    return codes, sc, mn, d, dmin
+
+
+def _q5k_weights(sb):
+    codes, sc, mn, d, dmin = _np_q5k(sb)
+    scale = np.repeat(d[..., None] * sc, 32, axis=-1)
+    mins = np.repeat(dmin[..., None] * mn, 32, axis=-1)
+    return scale * codes - mins
+
+
+def test_q5k_golden(golden):
+    (d, dmin, scales, qh_over, codes, over, dots, weights), = golden("q5k_superblock.txt")
+    sb = np.zeros(176, np.uint8)
+    sb[0:2] = np.array([int(d, 16) & 0xFF, int(d, 16) >> 8], np.uint8)  # little endian
+    sb[2:4] = np.array([int(dmin, 16) & 0xFF, int(dmin, 16) >> 8], np.uint8)
+    sb[4:16] = np.frombuffer(bytes.fromhex(scales.replace(" ", "")), np.uint8)
+    for kv in qh_over.split(","):
+        i, v = kv.split("=")
+        sb[16 + int(i)] = int(v, 16)
+    hexs = "".join(h * int(n) for h, n in (t.split("*") for t in codes.split()))
+    sb[48:] = np.frombuffer(bytes.fromhex(hexs), np.uint8)
+    a = np.ones(256, np.int8)
+    for kv in over.split(","):
+        i, v = kv.split("=")
+        a[int(i)] = int(v)
+    assert oracle.q5k_subdots(sb, a).tolist() == [int(v) for v in dots.split(",")]
+    w = oracle.dequant(sb.reshape(1, 176))
+    for kv in weights.split(","):
+        i, v = kv.split("=")
+        assert w[int(i)] == float(v)
+
+
+def test_q5k_brute_force_vs_independent_decode():
+    sbs = synth.q5k_blocks(synth.key(7, 600), 60)
+    codes, sc, mn, _, _ = _np_q5k(sbs)
+    assert codes.min() == 0 and codes.max() == 31 and sc.max() == 63 and mn.max() == 63
+    acts = RNG.integers(-127, 128, (60, 256)).astype(np.int8)
+    for i in range(60):
+        ref = (codes[i].reshape(8, 32) * acts[i].astype(np.int64).reshape(8, 32)).sum(axis=1)
+        assert np.array_equal(oracle.q5k_subdots(sbs[i], acts[i]), ref)
+    assert np.array_equal(oracle.dequant(sbs.reshape(3, 20, 176)), _q5k_weights(sbs).reshape(3, 20 * 256))
+
+
+def test_q5k_layer_vs_dense_fp64():
+    wl = synth.Workload("tiny_q5k", 512, 8, 2, 256, 1, routing="normal", weight_format=synth.FMT_Q5_K)
+    H, F, k, T = wl.hidden, wl.ffn, wl.top_k, 3
+    gate, up, down = (wl.expert_tensor(0, kd) for kd in range(3))
+    assert gate.shape == (8, F, H // 256, 176) and down.shape == (8, H, F // 256, 176)
+    x, logits = wl.x(0, 0, T), wl.logits(0, 0, T)
+    idx, w = oracle.topk(logits, k)
+    y, it = oracle.layer(x, idx, w, gate, up, down, H, F, want_intermediates=True)
+
+    def deq(t):
+        return _q5k_weights(t).reshape(t.shape[0], t.shape[1], -1)
+
+    Wg, Wu, Wd = deq(gate), deq(up), deq(down)
+    xa = it["xq"].astype(np.float64) * np.repeat(it["xd"].view(np.float16).astype(np.float64), 32, axis=1)
+    y_bf = np.zeros((T, H))
+    for t in range(T):
+        for j in range(k):
+            a, e = t * k + j, idx[t, j]
+            g, u = Wg[e] @ xa[t], Wu[e] @ xa[t]
+            np.testing.assert_allclose(it["g"][a], g, rtol=0, atol=1e-12 * np.abs(g).max())
+            h = g * u * expit(g)
+            hq, hd = oracle.quantize(h.astype(np.float32))
+            assert np.array_equal(hq, it["hq"][a]) and np.array_equal(hd, it["hd"][a])
+            ha = hq.astype(np.float64) * np.repeat(hd.view(np.float16).astype(np.float64), 32)
+            y_bf[t] += w[t, j] * (Wd[e] @ ha)
+    np.testing.assert_allclose(y, y_bf, rtol=1e-12, atol=1e-12 * np.abs(y_bf).max())
+
+
+@pytest.mark.parametrize("fmt", [synth.FMT_Q8_0, synth.FMT_Q5_0, synth.FMT_Q4_K, synth.FMT_Q6_K, synth.FMT_Q5_K])
 def test_generators_of_every_format_are_range_and_thread_independent(fmt):
     # the same expert's bytes whether generated alone or in a range, with any
     # thread count (the oracle and the library register the same weights)
