@@ -472,6 +472,7 @@ def run_ours(args):
                           "q5_0": run_format_leg(args, qec, synth, torch, log, "decode_b1_q5_resident16"),
                           "q4_k": run_format_leg(args, qec, synth, torch, log, "decode_b1_q4k_resident16"),
                           "q6_k": run_format_leg(args, qec, synth, torch, log, "decode_b1_q6k_resident16"),
+                          "q5_k": run_format_leg(args, qec, synth, torch, log, "decode_b1_q5k_resident16"),
                           "q4_shared_expert": run_format_leg(args, qec, synth, torch, log,
                                                              "decode_b1_shared_resident16", shared=True)}
     if rank == 0:
@@ -778,7 +779,7 @@ def run_pool_leg(args, qec, synth, torch, log, link_peak):
 
 
 def run_format_leg(args, qec, synth, torch, log, name, shared=False):
-    """Q8_0, Q5_0, Q4_K or Q6_K expert weights (or Q4 with a shared expert per layer) on
+    """Q8_0, Q5_0, Q4_K, Q6_K or Q5_K expert weights (or Q4 with a shared expert per layer) on
     16 fully resident layers of the decode shape: batch-1 decode steps
     captured in a CUDA graph (router top-k, plan, gate/up and down mat-vec
     launches per layer), timed with CUDA events on the context stream;
@@ -787,7 +788,7 @@ def run_format_leg(args, qec, synth, torch, log, name, shared=False):
     wl = synth.WORKLOADS[name]
     L, H, E, k, F = wl.n_layers, wl.hidden, wl.n_experts, wl.top_k, wl.ffn
     fmt_name = {synth.FMT_Q4: "Q4", synth.FMT_Q8_0: "Q8_0", synth.FMT_Q5_0: "Q5_0",
-                synth.FMT_Q4_K: "Q4_K", synth.FMT_Q6_K: "Q6_K"}[wl.weight_format]
+                synth.FMT_Q4_K: "Q4_K", synth.FMT_Q6_K: "Q6_K", synth.FMT_Q5_K: "Q5_K"}[wl.weight_format]
     T = 1
     stream = torch.cuda.Stream()
     sp = stream.cuda_stream

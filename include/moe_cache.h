@@ -69,7 +69,7 @@ typedef struct moe_cfg {
     int32_t renorm_topk;        /* 1: weights = softmax over the k selected */
     int32_t poll_timeout_ms;    /* host poll limit in cache_step (0 = 10 s) */
     int32_t device;             /* CUDA device ordinal */
-    int32_t weight_format;      /* MOE_FMT_Q4_0 (0), _Q8_0 (1), _Q5_0 (2), _Q4_K (3) or _Q6_K (4), every tensor */
+    int32_t weight_format;      /* MOE_FMT_Q4_0 (0), _Q8_0 (1), _Q5_0 (2), _Q4_K (3), _Q6_K (4) or _Q5_K (5) */
     int32_t shared_experts;     /* 1: every layer has one shared expert (register_shared_expert), E <= 4095 */
 } moe_cfg;
 
@@ -99,14 +99,21 @@ typedef struct moe_cfg {
  *   of qh[32n + l]; w = d * sc_j * (q - 32), j = element / 16 (another
  *   K-quant of those kernels; the pages print no layout).  Needs hidden and
  *   ffn multiples of 256.
- * Q8_0, Q5_0, Q4_K and Q6_K contexts run every forward through the mat-vec
- * kernels (no fused single-launch layer, no tensor-core prompt path, no
- * lookahead). */
+ * Q5_K: super-blocks of 256 weights (8 sub-blocks of 32), 176 bytes in the
+ *   published layout: d, dmin (binary16), the 12 packed 6-bit scale/min
+ *   bytes as in Q4_K, 32 bytes qh (bit j of qh[l] = bit 4 of element l of
+ *   sub-block j), then 128 code bytes in the Q4_K order (low four bits);
+ *   w = d * sc_j * q - dmin * m_j, q in 0..31.  Needs hidden and ffn
+ *   multiples of 256.
+ * Q8_0, Q5_0, Q4_K, Q6_K and Q5_K contexts run every forward through the
+ * mat-vec kernels (no fused single-launch layer, no tensor-core prompt path,
+ * no lookahead). */
 #define MOE_FMT_Q4_0 0
 #define MOE_FMT_Q8_0 1
 #define MOE_FMT_Q5_0 2
 #define MOE_FMT_Q4_K 3
 #define MOE_FMT_Q6_K 4
+#define MOE_FMT_Q5_K 5
 
 typedef struct moe_stats_t {
     uint64_t steps;        /* cache_step calls */

@@ -23,7 +23,7 @@ MOE_OK = 0
 ERRORS = {-1: "MOE_ERR_ARG", -2: "MOE_ERR_OOM", -3: "MOE_ERR_CUDA", -4: "MOE_ERR_NOT_PINNED",
           -5: "MOE_ERR_TIMEOUT", -6: "MOE_ERR_CAPACITY", -7: "MOE_ERR_STATE", -8: "MOE_ERR_FAULT"}
 KIND_GATE, KIND_UP, KIND_DOWN = 0, 1, 2
-FMT_Q4_0, FMT_Q8_0, FMT_Q5_0, FMT_Q4_K, FMT_Q6_K = 0, 1, 2, 3, 4
+FMT_Q4_0, FMT_Q8_0, FMT_Q5_0, FMT_Q4_K, FMT_Q6_K, FMT_Q5_K = 0, 1, 2, 3, 4, 5
 
 
 class MoeError(RuntimeError):

@@ -36,17 +36,18 @@ __host__ __device__ inline size_t blob_bytes(int rows, int nb) { return (size_t)
 // (16 B), the high bit pairs (8 B: word h, byte b, bits 2i..2i+1 = element
 // 16h + 4i + b) and the two sub-block scales (2 B) in its code planes, and
 // the super-block's binary16 d in its scale plane: the canonical 26.25 bytes
-// per 32 weights.
-constexpr int kFmtQ4 = 0, kFmtQ8 = 1, kFmtQ5 = 2, kFmtQ4K = 3, kFmtQ6K = 4;
+// per 32 weights.  Q5_K (Q4_K with a fifth code bit) is repacked like Q4_K
+// plus a plane of 32-bit fifth-bit words as for Q5_0 (28 bytes per 32).
+constexpr int kFmtQ4 = 0, kFmtQ8 = 1, kFmtQ5 = 2, kFmtQ4K = 3, kFmtQ6K = 4, kFmtQ5K = 5;
 __host__ __device__ constexpr int code_bytes(int fmt) {
-    return fmt == kFmtQ8 ? 32 : fmt == kFmtQ5 ? 20 : fmt == kFmtQ6K ? 26 : 16;
+    return fmt == kFmtQ8 ? 32 : (fmt == kFmtQ5 || fmt == kFmtQ5K) ? 20 : fmt == kFmtQ6K ? 26 : 16;
 }
 __host__ __device__ inline size_t blob_scales_offset_fmt(int fmt, int rows, int nb) {
     return (size_t)rows * nb * code_bytes(fmt);
 }
 // bytes of the scale plane of n blocks (n a multiple of 8 for the K-quants)
 __host__ __device__ inline size_t scale_plane_bytes(int fmt, size_t n) {
-    return fmt == kFmtQ4K ? n * 8 : fmt == kFmtQ6K ? n / 8 * 2 : n * 2;
+    return (fmt == kFmtQ4K || fmt == kFmtQ5K) ? n * 8 : fmt == kFmtQ6K ? n / 8 * 2 : n * 2;
 }
 __host__ __device__ inline size_t blob_bytes_fmt(int fmt, int rows, int nb) {
     const size_t n = (size_t)rows * nb;
@@ -262,6 +263,16 @@ struct WCodes<kFmtQ5> {
         return s - 16 * a_sum;
     }
 };
+// Q5_K: the codes of Q5_0 without its offset (raw sum q * a, q in 0..31); the
+// sub-block's scale and min enter through WScale<kFmtQ5K>
+template <>
+struct WCodes<kFmtQ5K> : WCodes<kFmtQ5> {
+    __device__ __forceinline__ int dot(const int4 &a0, const int4 &a1, int a_sum) const {
+        return WCodes<kFmtQ5>::dot(a0, a1, a_sum) + 16 * a_sum;
+    }
+};
+template <>
+struct WScale<kFmtQ5K> : WScale<kFmtQ4K> {};
 
 // Cache-state arrays of one forward: pointer tables, local slots, stamps and
 // the miss log (Zapdev-labs/a6000-custom-kernels, pointer-table GEMV).

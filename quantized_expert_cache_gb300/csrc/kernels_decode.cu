@@ -512,6 +512,8 @@ int launch_gemv(const GemvParams &p, int grid_gu, int grid_dn, cudaStream_t st, 
         e = launch_gemv_fmt<kFmtQ4K>(p, grid_gu, grid_dn, st, ev);
     else if (p.fmt == kFmtQ6K)
         e = launch_gemv_fmt<kFmtQ6K>(p, grid_gu, grid_dn, st, ev);
+    else if (p.fmt == kFmtQ5K)
+        e = launch_gemv_fmt<kFmtQ5K>(p, grid_gu, grid_dn, st, ev);
     else if (p.fmt == kFmtQ5)
         e = launch_gemv_fmt<kFmtQ5>(p, grid_gu, grid_dn, st, ev);
     else
@@ -1930,6 +1932,8 @@ int launch_block_dots(const uint8_t *blob, int fmt, int rows, int nb, int row0, 
         block_dots_kernel<kFmtQ4K><<<(n + 255) / 256, 256, 0, st>>>(blob, rows, nb, row0, n_rows, qa, out);
     else if (fmt == kFmtQ6K)
         block_dots_kernel<kFmtQ6K><<<(n + 255) / 256, 256, 0, st>>>(blob, rows, nb, row0, n_rows, qa, out);
+    else if (fmt == kFmtQ5K)
+        block_dots_kernel<kFmtQ5K><<<(n + 255) / 256, 256, 0, st>>>(blob, rows, nb, row0, n_rows, qa, out);
     else
         block_dots_kernel<kFmtQ4><<<(n + 255) / 256, 256, 0, st>>>(blob, rows, nb, row0, n_rows, qa, out);
     return (int)cudaGetLastError();

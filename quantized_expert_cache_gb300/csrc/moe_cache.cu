@@ -284,6 +284,24 @@ void repack_q4k_super(const uint8_t *sb, uint8_t *codes, float *sm) {
     }
 }
 
+// Q5_K super-block (176 bytes, 256 weights, the published layout: d, dmin,
+// the 12 packed scale/min bytes of Q4_K, 32 bytes qh whose byte l bit j is
+// the fifth bit of element l of sub-block j, then the Q4_K code bytes) -> 8
+// sub-blocks: Q4-order low nibbles, a fifth-bit word (bit t = element t),
+// and the exact fp32 pair (d * sc_j, dmin * m_j).
+void repack_q5k_super(const uint8_t *sb, uint8_t *codes, uint32_t *fifth, float *sm) {
+    uint8_t q4[144];
+    memcpy(q4, sb, 16);
+    memcpy(q4 + 16, sb + 48, 128);
+    repack_q4k_super(q4, codes, sm);
+    const uint8_t *qh = sb + 16;
+    for (int j = 0; j < 8; ++j) {
+        uint32_t w = 0;
+        for (int t = 0; t < 32; ++t) w |= (uint32_t)((qh[t] >> j) & 1u) << t;
+        fifth[j] = w;
+    }
+}
+
 // Q6_K super-block (210 bytes, 256 weights, the published layout: per
 // 128-weight half n, element 32m + l has its low nibble in
 // ql[64n + 32 (m & 1) + l] (low half of the byte for m < 2) and its high pair
@@ -319,6 +337,15 @@ void repack(const uint8_t *src, uint8_t *dst, int fmt, int n_experts, int rows, 
                 uint8_t *q = dst + (size_t)e * stride;
                 float *sm = (float *)(q + nblk * 16);
                 for (size_t u = 0; u < nblk / 8; ++u) repack_q4k_super(s + 144 * u, q + 128 * u, sm + 16 * u);
+                continue;
+            }
+            if (fmt == moe::kFmtQ5K) {
+                const uint8_t *s = src + (size_t)e * (nblk / 8) * 176;
+                uint8_t *q = dst + (size_t)e * stride;
+                uint32_t *fifth = (uint32_t *)(q + nblk * 16);
+                float *sm = (float *)(q + nblk * 20);
+                for (size_t u = 0; u < nblk / 8; ++u)
+                    repack_q5k_super(s + 176 * u, q + 128 * u, fifth + 8 * u, sm + 16 * u);
                 continue;
             }
             if (fmt == moe::kFmtQ6K) {
@@ -559,11 +586,12 @@ int moe_layer_init(const moe_cfg *cfg, void *cuda_stream, moe_ctx **out) {
         c.slots_per_tensor < 0 || c.slots_per_tensor > c.n_experts || c.max_tokens < 1 || c.window_tokens < 1 ||
         c.max_swaps_per_step < 0 || (c.shared_experts != 0 && (c.shared_experts != 1 || c.n_experts > 4095)) ||
         (c.weight_format != MOE_FMT_Q4_0 && c.weight_format != MOE_FMT_Q8_0 && c.weight_format != MOE_FMT_Q5_0 &&
-         c.weight_format != MOE_FMT_Q4_K && c.weight_format != MOE_FMT_Q6_K) ||
-        ((c.weight_format == MOE_FMT_Q4_K || c.weight_format == MOE_FMT_Q6_K) && (c.hidden % 256 || c.ffn % 256)))
+         c.weight_format != MOE_FMT_Q4_K && c.weight_format != MOE_FMT_Q6_K && c.weight_format != MOE_FMT_Q5_K) ||
+        ((c.weight_format == MOE_FMT_Q4_K || c.weight_format == MOE_FMT_Q6_K || c.weight_format == MOE_FMT_Q5_K) &&
+         (c.hidden % 256 || c.ffn % 256)))
         return fail(nullptr, MOE_ERR_ARG,
                     "bad cfg: hidden%32, ffn%32, 1<=E<=4096, 1<=k<=min(32,E), layers>=1, 0<=slots<=E, max_tokens>=1, "
-                    "weight_format Q4_0, Q8_0, Q5_0, Q4_K or Q6_K (hidden, ffn % 256), shared_experts 0 or 1 "
+                    "weight_format Q4_0, Q8_0, Q5_0, Q4_K, Q6_K or Q5_K (hidden, ffn % 256), shared_experts 0 or 1 "
                     "(then E <= 4095)");
     int down_rows = moe::down_rows_per_item(c.ffn);
     if (c.hidden % down_rows) return fail(nullptr, MOE_ERR_ARG, "hidden must be a multiple of the down row block");
@@ -585,6 +613,7 @@ int moe_layer_init(const moe_cfg *cfg, void *cuda_stream, moe_ctx **out) {
                : c.weight_format == MOE_FMT_Q5_0 ? moe::kFmtQ5
                : c.weight_format == MOE_FMT_Q4_K ? moe::kFmtQ4K
                : c.weight_format == MOE_FMT_Q6_K ? moe::kFmtQ6K
+               : c.weight_format == MOE_FMT_Q5_K ? moe::kFmtQ5K
                                                  : moe::kFmtQ4;
     ctx->blob = moe::blob_bytes_fmt(ctx->fmt, c.ffn, c.hidden / 32);
     ctx->stride = (ctx->blob + 255) / 256 * 256;

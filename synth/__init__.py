@@ -373,6 +373,10 @@ WORKLOADS = {
     "decode_b1_q6k_resident16": Workload("decode_b1_q6k_resident16", 2048, 512, 8, 1280, 16, routing="zipf",
                                          zipf_s=1.1, capacity=[512] * 16, phases=[("decode", 1, 64)],
                                          weight_format=FMT_Q6_K),
+    # Q5_K expert weights: the same 16 resident layers, FFN 1280
+    "decode_b1_q5k_resident16": Workload("decode_b1_q5k_resident16", 2048, 512, 8, 1280, 16, routing="zipf",
+                                         zipf_s=1.1, capacity=[512] * 16, phases=[("decode", 1, 64)],
+                                         weight_format=FMT_Q5_K),
     # Q4 weights with a shared expert per layer: the same 16 resident layers
     "decode_b1_shared_resident16": Workload("decode_b1_shared_resident16", 2048, 512, 8, 1152, 16,
                                             routing="zipf", zipf_s=1.1, capacity=[512] * 16,

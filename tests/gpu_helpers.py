@@ -221,7 +221,7 @@ def check_layer_parity(m: Model, layer, x_np, logits_np, y_gpu, idx_gpu, w_gpu):
     assert np.array_equal(xd, it["xd"]), "quantized x scales differ"
     # Q4_K's block term has two products and a difference before the scale
     # (two more roundings per block than the other formats)
-    extra = 2 if m.wl.weight_format == synth.FMT_Q4_K else 0
+    extra = 2 if m.wl.weight_format in (synth.FMT_Q4_K, synth.FMT_Q5_K) else 0
     n_alt = check_h_codes(hq, hd, it, m.H // 32 + extra)
     y_ref = oracle.down_combine(idx_o, w_o, d, hq, hd, m.H, m.F) if n_alt else y_o
     assert_close(y_gpu, y_ref)

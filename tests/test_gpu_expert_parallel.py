@@ -114,7 +114,7 @@ def _check_partial(sh, tensors, layer, x, idx, w, y_gpu):
     # h of the other rank's assignments is not computed here: take the oracle's
     other = ~mine.ravel()
     hq[other], hd[other] = it["hq"][other], it["hd"][other]
-    extra = 2 if wl.weight_format == synth.FMT_Q4_K else 0
+    extra = 2 if wl.weight_format in (synth.FMT_Q4_K, synth.FMT_Q5_K) else 0
     n_alt = check_h_codes(hq, hd, it, H // 32 + extra)
     y_ref = oracle.down_combine(idx, wm, d, hq, hd, H, F) if n_alt else y_o
     err = np.abs(y_gpu.astype(np.float64) - y_ref)

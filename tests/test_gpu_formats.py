@@ -3,7 +3,8 @@ the oracle: Q8_0 (blocks of 32 signed 8-bit codes and one binary16 scale,
 w = d * q), Q5_0 (5-bit codes, w = d * (q - 16)), Q4_K (256-weight
 super-blocks, 6-bit sub-block scales and mins, w = d*sc*q - dmin*m) and Q6_K
 (256-weight super-blocks, signed 8-bit scales of 16-weight sub-blocks, 6-bit
-codes, w = d*sc*(q - 32)).  Integer block dots
+codes, w = d*sc*(q - 32)) and Q5_K (Q4_K with a fifth code bit, q in 0..31).
+Integer block dots
 bit-exact from pool slots and from pinned host memory, whole layers (decode
 and prompt-sized batches, hot and cold experts, ragged shapes), the miss
 log, and the cache state after every promotion pass."""
@@ -18,8 +19,9 @@ from gpu_helpers import Model, check_layer_parity
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 FMTS = [pytest.param(qec.FMT_Q8_0, id="q8_0"), pytest.param(qec.FMT_Q5_0, id="q5_0"),
-        pytest.param(qec.FMT_Q4_K, id="q4_k"), pytest.param(qec.FMT_Q6_K, id="q6_k")]
-K_QUANTS = (qec.FMT_Q4_K, qec.FMT_Q6_K)
+        pytest.param(qec.FMT_Q4_K, id="q4_k"), pytest.param(qec.FMT_Q6_K, id="q6_k"),
+        pytest.param(qec.FMT_Q5_K, id="q5_k")]
+K_QUANTS = (qec.FMT_Q4_K, qec.FMT_Q6_K, qec.FMT_Q5_K)
 
 
 def _fits(fmt, H, F):
@@ -56,6 +58,10 @@ def test_block_dots_bit_exact_hot_and_cold(fmt):
                 if fmt == qec.FMT_Q4_K:
                     # raw sub-block dots: 8 per 256-weight super-block
                     ref = np.array([np.concatenate([oracle.subblock_dots(W[5 + r, u], qa[256 * u:256 * u + 256])
+                                                    for u in range(cols // 256)]) for r in range(n_rows)])
+                elif fmt == qec.FMT_Q5_K:
+                    # raw sub-block dots (q in 0..31): 8 per super-block
+                    ref = np.array([np.concatenate([oracle.q5k_subdots(W[5 + r, u], qa[256 * u:256 * u + 256])
                                                     for u in range(cols // 256)]) for r in range(n_rows)])
                 elif fmt == qec.FMT_Q6_K:
                     # per 32 weights: the two 16-weight sub-blocks' scaled dots

@@ -121,9 +121,9 @@ def test_shared_expert_cache_steps_and_borrow():
         m.close()
 
 
-@pytest.mark.parametrize("fmt", [qec.FMT_Q8_0, qec.FMT_Q5_0, qec.FMT_Q4_K])
+@pytest.mark.parametrize("fmt", [qec.FMT_Q8_0, qec.FMT_Q5_0, qec.FMT_Q4_K, qec.FMT_Q6_K, qec.FMT_Q5_K])
 def test_shared_expert_other_formats(fmt):
-    F = 512 if fmt == qec.FMT_Q4_K else 384
+    F = 512 if fmt in (qec.FMT_Q4_K, qec.FMT_Q6_K, qec.FMT_Q5_K) else 384
     m = Model(H=512, F=F, E=16, k=4, L=1, capacity=8, max_tokens=40, zipf_s=0.8, shared=True, weight_format=fmt)
     try:
         for T in (1, 5, 40):
