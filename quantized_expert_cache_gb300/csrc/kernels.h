@@ -161,6 +161,7 @@ int fused_rb_rows(int H, int F, int T, int k, int E);
 size_t fused_rb_smem(int H, int F, int T, int k, int E, int rows, int *pre_off);
 bool fused_t1_ok(int E, int k);
 int fused_configure_rb(int F, size_t smem, int *blocks_per_sm);
+int fused_configure_t1_fmt(int F, int fmt, size_t smem, int *blocks_per_sm);
 int launch_fused(const FusedParams &p, int grid, size_t smem, cudaStream_t st, cudaEvent_t const *ev);
 int launch_prefill(const PrefillLaunch &L, cudaStream_t st, cudaEvent_t const *ev = nullptr);
 int launch_stage(const StageParams &p, size_t blob_bytes, int n_sm, cudaStream_t st);

@@ -1131,6 +1131,15 @@ __device__ void lookahead_prefetch(const FusedParams &p) {
     }
 }
 
+// 128-bit loads per lane and tensor that a single-token gate/up item issues
+// together, per weight format (the wider formats hold more registers per
+// block: Q8_0 two uint4, Q6_K a uint4, a uint2 and two scales)
+template <int FMT>
+__host__ __device__ constexpr int t1_gu_rounds() {
+    return FMT == kFmtQ4 ? kGURounds : (FMT == kFmtQ5 || FMT == kFmtQ4K) ? 6 : 4;
+}
+
+template <int FMT>
 __device__ __forceinline__ void t1_route_gate_up(const FusedParams &p, int *s_e, float *s_w, int *s_uniq, int *s_off,
                                                  int *s_asg, int *s_nu, int *s_npick, float (*sh_h)[32], uint8_t *dsm,
                                                  uint8_t *dpre, int n_dn_items, uint32_t step_clock) {
@@ -1257,7 +1266,8 @@ __device__ __forceinline__ void t1_route_gate_up(const FusedParams &p, int *s_e,
     // staged by warps 1..7 (pick u by warp 1 + u mod 7) once the pick is out;
     // a cold pick's rows are left for the down item (stage_cold_down)
     auto stage_first_down = [&]() {
-        if (warp == 0 || (int)blockIdx.x >= n_dn_items) return;
+        // other formats: the down items read their rows from global memory
+        if (FMT != kFmtQ4 || warp == 0 || (int)blockIdx.x >= n_dn_items) return;
         const int rb = blockIdx.x;
         const int nc = R * nbf, ns = R * nbf / 8, per = nc + ns;
         const size_t soff = blob_scales_offset(H, nbf);
@@ -1291,7 +1301,7 @@ __device__ __forceinline__ void t1_route_gate_up(const FusedParams &p, int *s_e,
     // ---- gate/up items: (pick i mod k, row group i / k)
     const int sub = lane % kGULanes, grp = lane / kGULanes;
     const int rloc = warp == 0 ? 28 + grp : (warp - 1) * 4 + grp;
-    const size_t scale_off = blob_scales_offset(F, nbx);
+    const size_t scale_off = blob_scales_offset_fmt(FMT, F, nbx);
     const int n_items = k * rgs;
     int m = 0;
     for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++m) {
@@ -1317,33 +1327,31 @@ __device__ __forceinline__ void t1_route_gate_up(const FusedParams &p, int *s_e,
         const uint8_t *bg = (const uint8_t *)(uintptr_t)(eg & ~1ull);
         const uint8_t *bu = (const uint8_t *)(uintptr_t)(eu & ~1ull);
         const int r = rg * 32 + rloc;
-        const uint4 *qg = (const uint4 *)bg + (size_t)r * nbx;
-        const uint4 *qu = (const uint4 *)bu + (size_t)r * nbx;
-        const __half *dg = (const __half *)(bg + scale_off) + (size_t)r * nbx;
-        const __half *du = (const __half *)(bu + scale_off) + (size_t)r * nbx;
+        const size_t nblk = (size_t)F * nbx, row0 = (size_t)r * nbx;
+        constexpr int RND = t1_gu_rounds<FMT>();
         float ag = 0.0f, au = 0.0f;
-        for (int bb = 0; bb * kGULanes * kGURounds < nbx; ++bb) {
-            uint4 wg4[kGURounds], wu4[kGURounds];
-            float sg[kGURounds], su[kGURounds];
+        for (int bb = 0; bb * kGULanes * RND < nbx; ++bb) {
+            WCodes<FMT> wg[RND], wu[RND];
+            WScale<FMT> sg[RND], su[RND];
 #pragma unroll
-            for (int i = 0; i < kGURounds; ++i) {
-                const int b = sub + kGULanes * (bb * kGURounds + i);
+            for (int i = 0; i < RND; ++i) {
+                const int b = sub + kGULanes * (bb * RND + i);
                 if (b < nbx) {
-                    wg4[i] = ld_weights(qg + b);
-                    wu4[i] = ld_weights(qu + b);
-                    sg[i] = ld_scale(dg + b);
-                    su[i] = ld_scale(du + b);
+                    wg[i].load(bg, nblk, row0 + b);
+                    wu[i].load(bu, nblk, row0 + b);
+                    sg[i].load(bg + scale_off, row0 + b);
+                    su[i].load(bu + scale_off, row0 + b);
                 }
             }
 #pragma unroll
-            for (int i = 0; i < kGURounds; ++i) {
-                const int b = sub + kGULanes * (bb * kGURounds + i);
+            for (int i = 0; i < RND; ++i) {
+                const int b = sub + kGULanes * (bb * RND + i);
                 if (b < nbx) {
                     const int4 *xa = (const int4 *)(xq_s + (size_t)b * kBlock);
                     const int4 x0 = xa[0], x1 = xa[1];
                     const BlockScale xs = xds_s[b];
-                    ag += (float)q4_block_dot(wg4[i], x0, x1, xs.s) * (sg[i] * xs.d);
-                    au += (float)q4_block_dot(wu4[i], x0, x1, xs.s) * (su[i] * xs.d);
+                    ag += sg[i].term(wg[i].dot(x0, x1, xs.s), xs);
+                    au += su[i].term(wu[i].dot(x0, x1, xs.s), xs);
                 }
             }
         }
@@ -1430,7 +1438,10 @@ __device__ void stage_cold_down(const FusedParams &p, const int *s_uniq, int nu,
     __syncthreads();
 }
 
-template <int LD, int NT, bool RB>
+// FMT: the weight format.  4-bit codes (Q4) run every mode; the other
+// formats run the single-token early-start path only (row-block down items
+// then read their rows from global memory instead of a shared-memory stage).
+template <int LD, int NT, bool RB, int FMT = kFmtQ4>
 __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
     __shared__ int s_e[kMaxFusedA], s_uniq[kMaxFusedA], s_off[kMaxFusedA + 1], s_asg[kMaxFusedA],
         s_cnt[kMaxFusedA], s_first[kMaxFusedA];
@@ -1458,10 +1469,15 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
     const int R = p.rb_rows;
     uint8_t *dpre = dsm + (RB ? (size_t)p.pre_off : fused_stage_bytes(H, F));
     const bool t1 = NT == 1 && RB && p.tbl_off > 0;
+    if (FMT != kFmtQ4 && !t1) {
+        // not a launch this instantiation serves (the host never makes one)
+        if (threadIdx.x == 0) atomicOr(p.error, 8);
+        return;
+    }
     if (t1) {
         if (threadIdx.x == 0) s_npick = 0;
         __syncthreads();
-        t1_route_gate_up(p, s_e, s_w, s_uniq, s_off, s_asg, &s_nu, &s_npick, sh_h, dsm, dpre, H / R, step_clock);
+        t1_route_gate_up<FMT>(p, s_e, s_w, s_uniq, s_off, s_asg, &s_nu, &s_npick, sh_h, dsm, dpre, H / R, step_clock);
     }
     // Prologue.  Routed launches: warps 0..T-1 route the tokens (top-k over
     // the logits) while the remaining warps quantize every token's x (small
@@ -1633,10 +1649,11 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
             const int sub = threadIdx.x % LD;
             cp_async_wait_all();
             __syncthreads();  // the first item's staged rows
-            stage_cold_down(p, s_uniq, nu,
-                            t1 ? (const uint64_t *)(dsm + p.tbl_off) + 2 * g.cv.E
-                               : g.cv.tbl + (size_t)g.tid_down * g.cv.E,
-                            dpre, rgs);
+            if (FMT == kFmtQ4)
+                stage_cold_down(p, s_uniq, nu,
+                                t1 ? (const uint64_t *)(dsm + p.tbl_off) + 2 * g.cv.E
+                                   : g.cv.tbl + (size_t)g.tid_down * g.cv.E,
+                                dpre, rgs);
             for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
                 const bool first = item == (int)blockIdx.x;
                 if (!first) {
@@ -1677,6 +1694,14 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
                     const int mc = __reduce_max_sync(0xffffffffu, cnt);
                     const uint4 *wc = wc0 + (size_t)vr * nbf;
                     const __half *ws = ws0 + (size_t)vr * nbf;
+                    // other formats: row item R + r of the expert's down blob, from global memory
+                    const uint8_t *bdg = nullptr;
+                    size_t drow = 0;
+                    if (FMT != kFmtQ4 && act) {
+                        const uint64_t *s_td = (const uint64_t *)(dsm + p.tbl_off) + 2 * g.cv.E;
+                        bdg = (const uint8_t *)(uintptr_t)(s_td[s_uniq[u]] & ~1ull);
+                        drow = ((size_t)item * R + r) * nbf;
+                    }
                     for (int sl = 0; sl < mc; ++sl) {
                         float acc = 0.0f;
                         int a = 0;
@@ -1689,9 +1714,17 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
                             for (int b = sub; b < nbf; b += LD) {
                                 const int4 h0 = __ldcg(ha + 2 * b), h1 = __ldcg(ha + 2 * b + 1);
                                 const int2 hsc = __ldcg(hs + b);
-                                const uint4 w4 = wc[b];
-                                acc += (float)q4_block_dot(w4, h0, h1, hsc.y) *
-                                       (__half2float(ws[b]) * __int_as_float(hsc.x));
+                                if constexpr (FMT == kFmtQ4) {
+                                    const uint4 w4 = wc[b];
+                                    acc += (float)q4_block_dot(w4, h0, h1, hsc.y) *
+                                           (__half2float(ws[b]) * __int_as_float(hsc.x));
+                                } else {
+                                    WCodes<FMT> w;
+                                    WScale<FMT> sc;
+                                    w.load(bdg, (size_t)H * nbf, drow + b);
+                                    sc.load(bdg + blob_scales_offset_fmt(FMT, H, nbf), drow + b);
+                                    acc += sc.term(w.dot(h0, h1, hsc.y), BlockScale{__int_as_float(hsc.x), hsc.y});
+                                }
                             }
                         }
 #pragma unroll
@@ -1809,6 +1842,23 @@ static const void *fused_fn_t(int F, int T) {
 
 static const void *fused_fn(int F, int T, bool rb) { return rb ? fused_fn_t<true>(F, T) : fused_fn_t<false>(F, T); }
 
+// The single-token row-block kernel of a non-Q4 weight format.
+template <int FMT>
+static const void *fused_fn_fmt_t(int F) {
+    return fused_down_lanes(F) == 4 ? (const void *)decode_layer_kernel<4, 1, true, FMT>
+                                    : (const void *)decode_layer_kernel<8, 1, true, FMT>;
+}
+static const void *fused_fn_fmt(int F, int fmt) {
+    switch (fmt) {
+        case kFmtQ8: return fused_fn_fmt_t<kFmtQ8>(F);
+        case kFmtQ5: return fused_fn_fmt_t<kFmtQ5>(F);
+        case kFmtQ4K: return fused_fn_fmt_t<kFmtQ4K>(F);
+        case kFmtQ6K: return fused_fn_fmt_t<kFmtQ6K>(F);
+        case kFmtQ5K: return fused_fn_fmt_t<kFmtQ5K>(F);
+        default: return fused_fn(F, 1, true);
+    }
+}
+
 // Shared-memory opt-in for every token-count variant of one mode (only ever
 // raised, so contexts of different shapes coexist); *blocks_per_sm gets the
 // smallest resident-CTA count over the variants (a safe cooperative grid).
@@ -1839,6 +1889,22 @@ static int configure_mode(int F, size_t smem, bool rb, int *blocks_per_sm) {
 
 int fused_configure(int F, size_t smem, int *blocks_per_sm) { return configure_mode(F, smem, false, blocks_per_sm); }
 int fused_configure_rb(int F, size_t smem, int *blocks_per_sm) { return configure_mode(F, smem, true, blocks_per_sm); }
+
+int fused_configure_t1_fmt(int F, int fmt, size_t smem, int *blocks_per_sm) {
+    static std::mutex mu;
+    static std::map<std::pair<int, const void *>, size_t> opted;
+    std::lock_guard<std::mutex> lk(mu);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return (int)cudaErrorInvalidDevice;
+    const void *fn = fused_fn_fmt(F, fmt);
+    size_t &cur = opted[{dev, fn}];
+    if (smem > cur) {
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return (int)e;
+        cur = smem;
+    }
+    return (int)cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, fn, 256, smem);
+}
 
 // Row-block down mode: rows of H per down item for a launch of T tokens, or
 // 0 when the mode does not apply (more than kMaxRbA assignments or 8 tokens,
@@ -1892,7 +1958,8 @@ int launch_fused(const FusedParams &p, int grid, size_t smem, cudaStream_t st, c
     cfg.numAttrs = p.pdl ? 2 : 1;
     if (ev) record(ev[0], st);
     void *args[] = {(void *)&p};
-    cudaError_t e = cudaLaunchKernelExC(&cfg, fused_fn(p.g.F, p.g.n_tokens, p.rb_rows > 0), args);
+    const void *fn = p.g.fmt != kFmtQ4 ? fused_fn_fmt(p.g.F, p.g.fmt) : fused_fn(p.g.F, p.g.n_tokens, p.rb_rows > 0);
+    cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
     if (ev) {
         record(ev[1], st);
         record(ev[2], st);

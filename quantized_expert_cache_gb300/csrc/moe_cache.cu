@@ -57,6 +57,8 @@ struct moe_ctx {
     // tokens of the step a forward belongs to (moe_ffn_forward_rows); 0: its
     // own token count
     int clock_tokens = 0;
+    // a non-Q4 format with the single-launch layer for one routed token
+    bool fused_t1_fmt = false;
     std::vector<uint8_t *> sh_blob;        // [n_tensors]: device blob of the shared expert
     int32_t *idx_a = nullptr;              // [M][ka]: routed ids + E
     float *w_a = nullptr;                  // [M][ka]: routed weights + 1
@@ -732,11 +734,27 @@ int moe_layer_init(const moe_cfg *cfg, void *cuda_stream, moe_ctx **out) {
             CKI((cudaError_t)moe::fused_configure_rb(ctx->F, ctx->fused_smem_rb, &bps));
             ctx->fused_blocks_rb = bps * ctx->n_sm;
         }
-        if (ctx->fmt != moe::kFmtQ4 || ctx->shared) {
-            // the single-launch layer reads 4-bit codes and routed experts
-            // only: other formats and shared experts take the mat-vec kernels
+        if (ctx->shared) {
+            // the single-launch layer runs routed experts only: shared
+            // experts take the mat-vec kernels
             ctx->fused_blocks = 0;
             ctx->fused_blocks_rb = 0;
+        } else if (ctx->fmt != moe::kFmtQ4) {
+            // other formats: the single-launch layer for one routed token
+            // (its own instantiation), the mat-vec kernels for the rest
+            ctx->fused_blocks = 0;
+            ctx->fused_blocks_rb = 0;
+            const int rows = moe::fused_rb_rows(ctx->H, ctx->F, 1, ctx->k, E);
+            if (rows > 0 && moe::fused_t1_ok(E, ctx->k)) {
+                size_t sm = moe::fused_rb_smem(ctx->H, ctx->F, 1, ctx->k, E, rows, nullptr);
+                sm = (sm + 15) / 16 * 16 + (size_t)24 * E;
+                CKI((cudaError_t)moe::fused_configure_t1_fmt(ctx->F, ctx->fmt, sm, &bps));
+                if (bps > 0) {
+                    ctx->fused_smem_rb = sm;
+                    ctx->fused_blocks_rb = bps * ctx->n_sm;
+                    ctx->fused_t1_fmt = true;
+                }
+            }
         }
     }
 
@@ -885,7 +903,8 @@ int moe_ffn_forward_routed(moe_ctx *ctx, int layer, const float *d_x, const floa
                            int32_t *d_idx, float *d_w, float *d_y, void *stream) {
     if (!ctx) return fail(nullptr, MOE_ERR_ARG, "null ctx");
     if (n_tokens > 0 && (!d_logits || !d_idx || !d_w)) return fail(ctx, MOE_ERR_ARG, "routed forward: null pointer");
-    if (n_tokens > 0 && n_tokens <= 32 && n_tokens * ctx->k <= 256 && ctx->fused_blocks > 0)
+    if (n_tokens > 0 && n_tokens <= 32 && n_tokens * ctx->k <= 256 &&
+        (ctx->fused_blocks > 0 || (n_tokens == 1 && ctx->fused_t1_fmt && ctx->e_base == 0 && ctx->E_route == ctx->E)))
         return ffn_forward_impl(ctx, layer, d_x, n_tokens, d_idx, d_w, d_y, stream, d_logits, d_idx, d_w);
     int rc = route_topk(ctx, d_logits, n_tokens, ctx->E_route, ctx->k, d_idx, d_w, stream);
     if (rc) return rc;
@@ -1009,7 +1028,8 @@ static int ffn_forward_body(moe_ctx *ctx, int layer, const float *d_x, int n_tok
     gp.idx = d_idx;
     gp.e_base = ctx->e_base;
     const bool sharded = ctx->e_base != 0 || ctx->E_route != ctx->E;
-    if (small && A <= 256 && ctx->fused_blocks > 0) {
+    const bool t1_fmt = ctx->fused_t1_fmt && T == 1 && d_logits && !sharded;
+    if (small && A <= 256 && (ctx->fused_blocks > 0 || t1_fmt)) {
         moe::FusedParams fp{};
         fp.g = gp;
         fp.x = d_x;
