@@ -74,6 +74,10 @@ struct FusedParams {
     // One routed token in row-block mode (fused_t1_ok): shared-memory offset
     // of the layer's gate, up and down table rows (0: the general prologue).
     int tbl_off;
+    // 1: the last assignment of the token is the layer's shared expert (table
+    // column E - 1 of the launch's rows, weight 1), which the single-token
+    // path starts at kernel entry; 0: routed experts only
+    int n_shared;
     // Lookahead (one routed token, early-start path): predict the next
     // layer's picks as the top-k of pr_b + pr_w . x and prefetch their
     // pool-resident weights into L2 (pr_w null: off).

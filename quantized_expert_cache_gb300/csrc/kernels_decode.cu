@@ -541,6 +541,11 @@ constexpr int kMaxRbOut = kMaxRbA * kMaxRbRows;
 constexpr int kGURounds = 8;  // 128-bit loads per lane and tensor issued together
 constexpr int kXBatch = 8;    // x blocks per warp loaded before they are quantized
 
+__device__ __forceinline__ void cp_async8(void *smem_dst, const void *gsrc) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"((uint32_t)__cvta_generic_to_shared(smem_dst)),
+                 "l"(gsrc)
+                 : "memory");
+}
 __device__ __forceinline__ void cp_async16(void *smem_dst, const void *gsrc) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(smem_dst)),
                  "l"(gsrc)
@@ -1145,6 +1150,10 @@ __device__ __forceinline__ void t1_route_gate_up(const FusedParams &p, int *s_e,
                                                  uint8_t *dpre, int n_dn_items, uint32_t step_clock) {
     const GemvParams &g = p.g;
     const int H = g.H, F = g.F, k = g.k, E = g.cv.E;
+    // with a shared expert (n_shared = 1): kr routed picks of the Er routed
+    // experts, then the shared expert as pick kr (table column Er, weight 1),
+    // known at kernel entry
+    const int kr = k - p.n_shared, Er = E - p.n_shared;
     const int nbx = H / kBlock, nbf = F / kBlock, rgs = F / kBlock;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int R = p.rb_rows;
@@ -1161,12 +1170,12 @@ __device__ __forceinline__ void t1_route_gate_up(const FusedParams &p, int *s_e,
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             const int e = lane + 32 * i;
-            rk[i] = e < E ? ((unsigned long long)fkey(__ldg(l + e)) << 32) | (unsigned)(~(unsigned)e) : 0ull;
+            rk[i] = e < Er ? ((unsigned long long)fkey(__ldg(l + e)) << 32) | (unsigned)(~(unsigned)e) : 0ull;
         }
         unsigned long long last = ~0ull;
         int my_e = 0;
         unsigned my_key = 0u;
-        for (int j = 0; j < k; ++j) {
+        for (int j = 0; j < kr; ++j) {
             unsigned long long c[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) c[i] = rk[i] < last ? rk[i] : 0ull;
@@ -1187,19 +1196,19 @@ __device__ __forceinline__ void t1_route_gate_up(const FusedParams &p, int *s_e,
                 my_key = hi;
             }
         }
-        const float my_v = lane < k ? funkey(my_key) : -INFINITY;
+        const float my_v = lane < kr ? funkey(my_key) : -INFINITY;
         const float m = __shfl_sync(0xffffffffu, my_v, 0);
-        const float ej = lane < k ? expf(my_v - m) : 0.0f;
+        const float ej = lane < kr ? expf(my_v - m) : 0.0f;
         float den;
         if (p.renorm) {
             den = warp_sum_f(ej);
         } else {
             float sacc = 0.0f;
-            for (int e = lane; e < E; e += 32) sacc += expf(__ldg(l + e) - m);
+            for (int e = lane; e < Er; e += 32) sacc += expf(__ldg(l + e) - m);
             den = warp_sum_f(sacc);
         }
         const float my_w = ej / den;
-        if (lane < k) {
+        if (lane < kr) {
             s_w[lane] = my_w;
             s_uniq[lane] = my_e;
             s_off[lane] = lane;
@@ -1208,15 +1217,22 @@ __device__ __forceinline__ void t1_route_gate_up(const FusedParams &p, int *s_e,
                 p.idx_out[lane] = my_e;
                 p.w_out[lane] = my_w;
             }
+        } else if (lane < k) {
+            // the shared expert: assignment kr, weight 1
+            v_e[lane] = Er;
+            s_w[lane] = 1.0f;
+            s_uniq[lane] = Er;
+            s_off[lane] = lane;
+            s_asg[lane] = lane;
         }
         if (p.pr_mine && blockIdx.x == 0) {
             // how many of this layer's picks the previous layer predicted
             bool hit = false;
-            if (lane < k)
-                for (int j = 0; j < k; ++j) hit |= __ldcg(p.pr_mine + j) == my_e;
+            if (lane < kr)
+                for (int j = 0; j < kr; ++j) hit |= __ldcg(p.pr_mine + j) == my_e;
             const int hits = __popc(__ballot_sync(0xffffffffu, hit));
             if (lane == 0) {
-                atomicAdd(p.pr_stats, (unsigned long long)k);
+                atomicAdd(p.pr_stats, (unsigned long long)kr);
                 atomicAdd(p.pr_stats + 1, (unsigned long long)hits);
             }
         }
@@ -1228,9 +1244,16 @@ __device__ __forceinline__ void t1_route_gate_up(const FusedParams &p, int *s_e,
     } else {
         // ---- gate, up and down table rows (contiguous: tensor ids 3l .. 3l + 2)
         {
-            const uint4 *src = reinterpret_cast<const uint4 *>(g.cv.tbl + (size_t)g.tid_gate * E);
+            // 16-byte copies when the three rows are 16-byte aligned (E even),
+            // else 8-byte ones (an odd row length: a shared expert's column)
             uint8_t *dst = dsm + p.tbl_off;
-            for (int i = threadIdx.x - 32; i < 3 * E / 2; i += 224) cp_async16(dst + (size_t)i * 16, src + i);
+            if (E % 2 == 0) {
+                const uint4 *src = reinterpret_cast<const uint4 *>(g.cv.tbl + (size_t)g.tid_gate * E);
+                for (int i = threadIdx.x - 32; i < 3 * E / 2; i += 224) cp_async16(dst + (size_t)i * 16, src + i);
+            } else {
+                const uint64_t *src = g.cv.tbl + (size_t)g.tid_gate * E;
+                for (int i = threadIdx.x - 32; i < 3 * E; i += 224) cp_async8(dst + (size_t)i * 8, src + i);
+            }
             cp_async_commit();
         }
         // ---- x of the token, quantized into shared memory
@@ -1272,7 +1295,7 @@ __device__ __forceinline__ void t1_route_gate_up(const FusedParams &p, int *s_e,
         const int nc = R * nbf, ns = R * nbf / 8, per = nc + ns;
         const size_t soff = blob_scales_offset(H, nbf);
         for (int u = warp - 1; u < k; u += kWarps - 1) {
-            if (lane == 0) {
+            if (lane == 0 && u < kr) {
                 const long long t0 = clock64();
                 while (*v_npick <= u) {
                     if (clock64() - t0 > 4000000000ll) {
@@ -1284,7 +1307,7 @@ __device__ __forceinline__ void t1_route_gate_up(const FusedParams &p, int *s_e,
                 __threadfence_block();
             }
             __syncwarp();
-            const uint64_t ent = s_td[v_e[u]];
+            const uint64_t ent = s_td[u < kr ? v_e[u] : Er];
             if (ent & 1ull) continue;  // cold
             const uint8_t *bd = (const uint8_t *)(uintptr_t)ent;
             for (int j = lane; j < per; j += 32) {
@@ -1306,7 +1329,7 @@ __device__ __forceinline__ void t1_route_gate_up(const FusedParams &p, int *s_e,
     int m = 0;
     for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++m) {
         const int u = item % k, rg = item / k;
-        if (warp != 0 && lane == 0) {
+        if (warp != 0 && lane == 0 && u < kr) {
             const long long t0 = clock64();
             while (*v_npick <= u) {
                 if (clock64() - t0 > 4000000000ll) {
@@ -1318,7 +1341,7 @@ __device__ __forceinline__ void t1_route_gate_up(const FusedParams &p, int *s_e,
             __threadfence_block();
         }
         __syncwarp();
-        const int e = v_e[u];
+        const int e = u < kr ? v_e[u] : Er;
         const uint64_t eg = s_tg[e], eu = s_tu[e];
         if (rg == 0 && threadIdx.x == 32) {
             record_read(g.cv, g.tid_gate, e, eg, step_clock);
@@ -1658,7 +1681,7 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
                 const bool first = item == (int)blockIdx.x;
                 if (!first) {
                     __syncthreads();  // the previous item's reads of the staged rows and s_o
-                    stage_rb(item, false);
+                    if (FMT == kFmtQ4) stage_rb(item, false);
                     cp_async_wait_all();
                     __syncthreads();
                 }

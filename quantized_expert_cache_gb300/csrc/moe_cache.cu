@@ -734,20 +734,17 @@ int moe_layer_init(const moe_cfg *cfg, void *cuda_stream, moe_ctx **out) {
             CKI((cudaError_t)moe::fused_configure_rb(ctx->F, ctx->fused_smem_rb, &bps));
             ctx->fused_blocks_rb = bps * ctx->n_sm;
         }
-        if (ctx->shared) {
-            // the single-launch layer runs routed experts only: shared
-            // experts take the mat-vec kernels
+        if (ctx->shared || ctx->fmt != moe::kFmtQ4) {
+            // other formats and shared experts: the single-launch layer for
+            // one routed token only (the shared expert is its last pick, its
+            // weights requested at kernel entry), the mat-vec kernels for
+            // the rest
             ctx->fused_blocks = 0;
             ctx->fused_blocks_rb = 0;
-        } else if (ctx->fmt != moe::kFmtQ4) {
-            // other formats: the single-launch layer for one routed token
-            // (its own instantiation), the mat-vec kernels for the rest
-            ctx->fused_blocks = 0;
-            ctx->fused_blocks_rb = 0;
-            const int rows = moe::fused_rb_rows(ctx->H, ctx->F, 1, ctx->k, E);
-            if (rows > 0 && moe::fused_t1_ok(E, ctx->k)) {
-                size_t sm = moe::fused_rb_smem(ctx->H, ctx->F, 1, ctx->k, E, rows, nullptr);
-                sm = (sm + 15) / 16 * 16 + (size_t)24 * E;
+            const int rows = moe::fused_rb_rows(ctx->H, ctx->F, 1, ctx->ka, Et);
+            if (rows > 0 && moe::fused_t1_ok(E, ctx->ka)) {
+                size_t sm = moe::fused_rb_smem(ctx->H, ctx->F, 1, ctx->ka, Et, rows, nullptr);
+                sm = (sm + 15) / 16 * 16 + (size_t)24 * Et;
                 CKI((cudaError_t)moe::fused_configure_t1_fmt(ctx->F, ctx->fmt, sm, &bps));
                 if (bps > 0) {
                     ctx->fused_smem_rb = sm;
@@ -903,7 +900,7 @@ int moe_ffn_forward_routed(moe_ctx *ctx, int layer, const float *d_x, const floa
                            int32_t *d_idx, float *d_w, float *d_y, void *stream) {
     if (!ctx) return fail(nullptr, MOE_ERR_ARG, "null ctx");
     if (n_tokens > 0 && (!d_logits || !d_idx || !d_w)) return fail(ctx, MOE_ERR_ARG, "routed forward: null pointer");
-    if (n_tokens > 0 && n_tokens <= 32 && n_tokens * ctx->k <= 256 &&
+    if (n_tokens > 0 && n_tokens <= 32 && n_tokens * ctx->ka <= 256 &&
         (ctx->fused_blocks > 0 || (n_tokens == 1 && ctx->fused_t1_fmt && ctx->e_base == 0 && ctx->E_route == ctx->E)))
         return ffn_forward_impl(ctx, layer, d_x, n_tokens, d_idx, d_w, d_y, stream, d_logits, d_idx, d_w);
     int rc = route_topk(ctx, d_logits, n_tokens, ctx->E_route, ctx->k, d_idx, d_w, stream);
@@ -971,12 +968,18 @@ static int ffn_forward_body(moe_ctx *ctx, int layer, const float *d_x, int n_tok
         CK(cudaStreamWaitEvent(st, ctx->ev_layer_up[layer], 0));
         ctx->layer_pending[layer] = 0;
     }
+    const bool sharded = ctx->e_base != 0 || ctx->E_route != ctx->E;
+    // one routed token through the single-launch layer of a format or
+    // shared-expert context (which routes and adds the shared expert itself)
+    const bool t1_only = ctx->fused_t1_fmt && n_tokens == 1 && d_logits && !sharded;
     if (ctx->shared) {
-        // the layer's shared expert joins every token as assignment k (id E,
-        // weight 1); the routed ids are checked against E here
         for (int kd = 0; kd < 3; ++kd)
             if (!ctx->sh_blob[layer * 3 + kd])
                 return fail(ctx, MOE_ERR_STATE, "forward: shared expert of this layer not registered");
+    }
+    if (ctx->shared && !t1_only) {
+        // the layer's shared expert joins every token as assignment k (id E,
+        // weight 1); the routed ids are checked against E here
         int rc0 = moe::launch_shared_assign(d_idx, d_w, n_tokens, ctx->k, ctx->E, ctx->idx_a, ctx->w_a, ctx->d_error,
                                             st);
         if (rc0) return fail(ctx, MOE_ERR_CUDA, "shared-expert assignment launch failed");
@@ -1027,9 +1030,7 @@ static int ffn_forward_body(moe_ctx *ctx, int layer, const float *d_x, int n_tok
     gp.fmt = ctx->fmt;
     gp.idx = d_idx;
     gp.e_base = ctx->e_base;
-    const bool sharded = ctx->e_base != 0 || ctx->E_route != ctx->E;
-    const bool t1_fmt = ctx->fused_t1_fmt && T == 1 && d_logits && !sharded;
-    if (small && A <= 256 && (ctx->fused_blocks > 0 || t1_fmt)) {
+    if (small && A <= 256 && (ctx->fused_blocks > 0 || t1_only)) {
         moe::FusedParams fp{};
         fp.g = gp;
         fp.x = d_x;
@@ -1046,15 +1047,17 @@ static int ffn_forward_body(moe_ctx *ctx, int layer, const float *d_x, int n_tok
         int items = U * std::max(ctx->F / 32, ctx->n_counters);
         int grid = std::min(items, ctx->fused_blocks);
         size_t smem = ctx->fused_smem;
-        const int rows = ctx->fused_blocks_rb > 0 ? moe::fused_rb_rows(H, ctx->F, T, ctx->k, ctx->E) : 0;
+        const int rows = ctx->fused_blocks_rb > 0 ? moe::fused_rb_rows(H, ctx->F, T, ctx->ka, ctx->Et) : 0;
         if (rows > 0) {
             // row-block down mode: each down item sums y for its rows
             fp.rb_rows = rows;
-            smem = moe::fused_rb_smem(H, ctx->F, T, ctx->k, ctx->E, rows, &fp.pre_off);
-            if (T == 1 && d_logits && moe::fused_t1_ok(ctx->E, ctx->k) && !sharded) {
+            smem = moe::fused_rb_smem(H, ctx->F, T, ctx->ka, ctx->Et, rows, &fp.pre_off);
+            if (T == 1 && d_logits && moe::fused_t1_ok(ctx->E, ctx->ka) && !sharded) {
                 // one routed token: the gate, up and down table rows follow
+                // (with the shared expert's column last)
                 fp.tbl_off = (int)((smem + 15) / 16 * 16);
-                smem = (size_t)fp.tbl_off + (size_t)24 * ctx->E;
+                smem = (size_t)fp.tbl_off + (size_t)24 * ctx->Et;
+                fp.n_shared = ctx->shared ? 1 : 0;
                 if (ctx->la_decode && !ctx->shared) {
                     const int L = ctx->cfg.n_layers, E = ctx->E;
                     if (layer + 1 < L && ctx->has_router[layer + 1]) {

@@ -135,3 +135,45 @@ def test_shared_expert_other_formats(fmt):
             qec.miss_drain(m.ctx)
     finally:
         m.close()
+
+
+@pytest.mark.parametrize("fmt", [qec.FMT_Q4_0, qec.FMT_Q8_0, qec.FMT_Q5_0, qec.FMT_Q4_K, qec.FMT_Q6_K, qec.FMT_Q5_K])
+def test_shared_expert_routed_single_token(fmt):
+    """One routed token per layer through the single-launch layer, whose last
+    pick is the shared expert (its weights requested at kernel entry, before
+    the routing is done): ids and weights against the oracle's top-k, x and h
+    codes and y against the oracle's layer with the shared expert, the cache
+    state and counts after every promotion pass, in every weight format."""
+    F = 512 if fmt in (qec.FMT_Q4_K, qec.FMT_Q6_K, qec.FMT_Q5_K) else 384
+    m = Model(H=512, F=F, E=32, k=4, L=2, capacity=8, max_tokens=4, window=8, zipf_s=1.1, shared=True,
+              weight_format=fmt)
+    try:
+        for step in range(16):
+            used = {}
+            for layer in range(m.L):
+                x, lg = m.wl.x(layer, step, 1), m.wl.logits(layer, step, 1)
+                idx = torch.empty((1, m.k), dtype=torch.int32, device="cuda")
+                w = torch.empty((1, m.k), device="cuda")
+                y = torch.empty((1, m.H), device="cuda")
+                qec.moe_ffn_forward_routed(m.ctx, layer, m.dev(x), m.dev(lg), 1, idx, w, y)
+                torch.cuda.synchronize()
+                idx_np = idx.cpu().numpy()
+                if step % 4 == 0 or step == 15:
+                    check_layer_parity(m, layer, x, lg, y.cpu().numpy(), idx_np, w.cpu().numpy())
+                else:
+                    io, _ = oracle.topk(lg, m.k)
+                    assert np.array_equal(idx_np, io)
+                for kd in range(3):
+                    used[layer * 3 + kd] = idx_np.ravel().tolist()
+            qec.cache_step(m.ctx, 1)
+            m.policy.step(1, used)
+            for tid in range(3 * m.L):
+                snap = qec.moe_cache_snapshot(m.ctx, tid, m.E, m.spt)
+                o = m.policy.snapshot(tid)
+                assert snap["slot_of"].tolist() == o["slot_of"] and snap["last_seen"].tolist() == o["last_seen"]
+                assert np.array_equal(snap["tbl"], m.expected_tbl(tid))
+        st = qec.moe_stats(m.ctx)
+        assert st["admissions"] == m.policy.stats["admissions"] > 0
+        assert st["hits"] == m.policy.stats["hits"] and st["misses"] == m.policy.stats["misses"] > 0
+    finally:
+        m.close()
