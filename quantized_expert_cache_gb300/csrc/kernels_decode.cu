@@ -1940,9 +1940,13 @@ int fused_rb_rows(int H, int F, int T, int k, int E) {
     const int A = T * k, U = A < E ? A : E, nbf = F / kBlock, LD = fused_down_lanes(F);
     if (T < 1 || T > kMaxChunk || A > kMaxRbA) return 0;
     if ((size_t)A * F + (size_t)A * nbf * sizeof(BlockScale) + 16 > kRbStageBudget) return 0;
+    // (expert, row) pairs of an item: one pass of the CTA's lanes, or two for
+    // one token (nine experts with a shared one keep 8 rows per item, so the
+    // items still fit one grid)
+    const int max_pairs = (T == 1 ? 2 : 1) * (256 / LD);
     for (int R = kMaxRbRows; R >= 2; R >>= 1) {
         if (H % R || (R * nbf * 2) % 16) continue;
-        if (U * R > 256 / LD) continue;
+        if (U * R > max_pairs) continue;
         if ((size_t)U * R * nbf * kBlockBytes > kRbPrefetchBudget) continue;
         return R;
     }
