@@ -105,9 +105,9 @@ typedef struct moe_cfg {
  *   sub-block j), then 128 code bytes in the Q4_K order (low four bits);
  *   w = d * sc_j * q - dmin * m_j, q in 0..31.  Needs hidden and ffn
  *   multiples of 256.
- * Q8_0, Q5_0, Q4_K, Q6_K and Q5_K contexts run every forward through the
- * mat-vec kernels (no fused single-launch layer, no tensor-core prompt path,
- * no lookahead). */
+ * Q8_0, Q5_0, Q4_K, Q6_K and Q5_K contexts run batch-1 routed forwards
+ * through the single-launch layer and every other forward through the
+ * mat-vec kernels (no tensor-core prompt path, no lookahead). */
 #define MOE_FMT_Q4_0 0
 #define MOE_FMT_Q8_0 1
 #define MOE_FMT_Q5_0 2
@@ -171,8 +171,10 @@ int register_expert_tensor(moe_ctx *ctx, int layer, int kind, const void *host_q
  * in its own HBM allocation, never cold and never in the pool: its table
  * entry is column E of the tensor's row, so it runs inside the same gate/up,
  * down (and, for prompts, grouped GEMM) launches as the routed experts, as
- * assignment k of every token.  Shared-expert contexts run the mat-vec
- * kernels for small batches (no single-launch layer).  Synchronous.
+ * assignment k of every token.  Shared-expert contexts run batch-1 routed
+ * forwards through the single-launch layer (the shared expert is its last
+ * pick, started at kernel entry) and other small batches through the
+ * mat-vec kernels.  Synchronous.
  * Errors: MOE_ERR_STATE (no shared experts in cfg), MOE_ERR_ARG (shape,
  * already registered), MOE_ERR_OOM, MOE_ERR_CUDA.
  */
