@@ -1147,20 +1147,19 @@ __host__ __device__ constexpr int t1_gu_rounds() {
 template <int FMT>
 __device__ __forceinline__ void t1_route_gate_up(const FusedParams &p, int *s_e, float *s_w, int *s_uniq, int *s_off,
                                                  int *s_asg, int *s_nu, int *s_npick, float (*sh_h)[32], uint8_t *dsm,
-                                                 uint8_t *dpre, int n_dn_items, uint32_t step_clock) {
+                                                 uint32_t step_clock) {
     const GemvParams &g = p.g;
     const int H = g.H, F = g.F, k = g.k, E = g.cv.E;
     // with a shared expert (n_shared = 1): kr routed picks of the Er routed
     // experts, then the shared expert as pick kr (table column Er, weight 1),
     // known at kernel entry
     const int kr = k - p.n_shared, Er = E - p.n_shared;
-    const int nbx = H / kBlock, nbf = F / kBlock, rgs = F / kBlock;
+    const int nbx = H / kBlock, rgs = F / kBlock;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int R = p.rb_rows;
     int8_t *xq_s = (int8_t *)dsm;
     BlockScale *xds_s = (BlockScale *)(dsm + kMaxChunk * H);
     const uint64_t *s_tg = (const uint64_t *)(dsm + p.tbl_off);  // [gate row E][up row E][down row E]
-    const uint64_t *s_tu = s_tg + E, *s_td = s_tg + 2 * E;
+    const uint64_t *s_tu = s_tg + E;
     volatile int *v_npick = s_npick;
     volatile int *v_e = s_e;
     if (warp == 0) {
@@ -1285,42 +1284,6 @@ __device__ __forceinline__ void t1_route_gate_up(const FusedParams &p, int *s_e,
         }
     }
 
-    // ---- the CTA's first down item (rows [rb R, rb R + R) of every pick),
-    // staged by warps 1..7 (pick u by warp 1 + u mod 7) once the pick is out;
-    // a cold pick's rows are left for the down item (stage_cold_down)
-    auto stage_first_down = [&]() {
-        // other formats: the down items read their rows from global memory
-        if (FMT != kFmtQ4 || warp == 0 || (int)blockIdx.x >= n_dn_items) return;
-        const int rb = blockIdx.x;
-        const int nc = R * nbf, ns = R * nbf / 8, per = nc + ns;
-        const size_t soff = blob_scales_offset(H, nbf);
-        for (int u = warp - 1; u < k; u += kWarps - 1) {
-            if (lane == 0 && u < kr) {
-                const long long t0 = clock64();
-                while (*v_npick <= u) {
-                    if (clock64() - t0 > 4000000000ll) {
-                        atomicOr(p.error, 4);
-                        break;
-                    }
-                    __nanosleep(20);
-                }
-                __threadfence_block();
-            }
-            __syncwarp();
-            const uint64_t ent = s_td[u < kr ? v_e[u] : Er];
-            if (ent & 1ull) continue;  // cold
-            const uint8_t *bd = (const uint8_t *)(uintptr_t)ent;
-            for (int j = lane; j < per; j += 32) {
-                if (j < nc)
-                    cp_async16(dpre + ((size_t)u * nc + j) * 16, bd + ((size_t)rb * nc + j) * 16);
-                else
-                    cp_async16(dpre + (size_t)k * nc * 16 + ((size_t)u * ns + (j - nc)) * 16,
-                               bd + soff + (size_t)rb * nc * 2 + (size_t)(j - nc) * 16);
-            }
-        }
-        cp_async_commit();
-    };
-
     // ---- gate/up items: (pick i mod k, row group i / k)
     const int sub = lane % kGULanes, grp = lane / kGULanes;
     const int rloc = warp == 0 ? 28 + grp : (warp - 1) * 4 + grp;
@@ -1391,16 +1354,8 @@ __device__ __forceinline__ void t1_route_gate_up(const FusedParams &p, int *s_e,
             quantize_block_warp(hrow[lane], lane, g.hq + (size_t)u * F + (size_t)rg * kBlock, g.hds + (size_t)u * rgs + rg);
             __syncwarp();
             if (lane == 0) red_release_add(&p.done_gu[u], 1u);
-            if (m == 0) bar_arrive_n(3, 256);
-        } else if (m == 0) {
-            // the down rows are requested once this item's gate/up weights
-            // are in and its h block is out, so they compete neither with the
-            // gate/up stream nor with the publish
-            bar_sync_n(3, 256);
-            stage_first_down();
         }
     }
-    if (m == 0) stage_first_down();  // a CTA without a gate/up item
     __syncthreads();  // routing results for CTAs without a gate/up item
 }
 
@@ -1500,7 +1455,7 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
     if (t1) {
         if (threadIdx.x == 0) s_npick = 0;
         __syncthreads();
-        t1_route_gate_up<FMT>(p, s_e, s_w, s_uniq, s_off, s_asg, &s_nu, &s_npick, sh_h, dsm, dpre, H / R, step_clock);
+        t1_route_gate_up<FMT>(p, s_e, s_w, s_uniq, s_off, s_asg, &s_nu, &s_npick, sh_h, dsm, step_clock);
     }
     // Prologue.  Routed launches: warps 0..T-1 route the tokens (top-k over
     // the logits) while the remaining warps quantize every token's x (small
@@ -1672,16 +1627,12 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
             const int sub = threadIdx.x % LD;
             cp_async_wait_all();
             __syncthreads();  // the first item's staged rows
-            if (FMT == kFmtQ4)
-                stage_cold_down(p, s_uniq, nu,
-                                t1 ? (const uint64_t *)(dsm + p.tbl_off) + 2 * g.cv.E
-                                   : g.cv.tbl + (size_t)g.tid_down * g.cv.E,
-                                dpre, rgs);
+            if (FMT == kFmtQ4 && !t1) stage_cold_down(p, s_uniq, nu, g.cv.tbl + (size_t)g.tid_down * g.cv.E, dpre, rgs);
             for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
                 const bool first = item == (int)blockIdx.x;
                 if (!first) {
                     __syncthreads();  // the previous item's reads of the staged rows and s_o
-                    if (FMT == kFmtQ4) stage_rb(item, false);
+                    if (FMT == kFmtQ4 && !t1) stage_rb(item, false);
                     cp_async_wait_all();
                     __syncthreads();
                 }
@@ -1717,10 +1668,13 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
                     const int mc = __reduce_max_sync(0xffffffffu, cnt);
                     const uint4 *wc = wc0 + (size_t)vr * nbf;
                     const __half *ws = ws0 + (size_t)vr * nbf;
-                    // other formats: row item R + r of the expert's down blob, from global memory
+                    // one token (every format): row item R + r of the expert's
+                    // down blob, read from global memory when the dot needs it
+                    // (staging the rows in shared memory measured slower)
+                    const bool staged = FMT == kFmtQ4 && !t1;
                     const uint8_t *bdg = nullptr;
                     size_t drow = 0;
-                    if (FMT != kFmtQ4 && act) {
+                    if (!staged && act) {
                         const uint64_t *s_td = (const uint64_t *)(dsm + p.tbl_off) + 2 * g.cv.E;
                         bdg = (const uint8_t *)(uintptr_t)(s_td[s_uniq[u]] & ~1ull);
                         drow = ((size_t)item * R + r) * nbf;
@@ -1733,19 +1687,25 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
                             // h of assignment a from L2 (written by other CTAs of this launch)
                             const int4 *ha = reinterpret_cast<const int4 *>(g.hq + (size_t)a * F);
                             const int2 *hs = reinterpret_cast<const int2 *>(g.hds + (size_t)a * nbf);
+                            if (staged) {
 #pragma unroll 4
-                            for (int b = sub; b < nbf; b += LD) {
-                                const int4 h0 = __ldcg(ha + 2 * b), h1 = __ldcg(ha + 2 * b + 1);
-                                const int2 hsc = __ldcg(hs + b);
-                                if constexpr (FMT == kFmtQ4) {
+                                for (int b = sub; b < nbf; b += LD) {
+                                    const int4 h0 = __ldcg(ha + 2 * b), h1 = __ldcg(ha + 2 * b + 1);
+                                    const int2 hsc = __ldcg(hs + b);
                                     const uint4 w4 = wc[b];
                                     acc += (float)q4_block_dot(w4, h0, h1, hsc.y) *
                                            (__half2float(ws[b]) * __int_as_float(hsc.x));
-                                } else {
+                                }
+                            } else {
+                                const size_t soff = blob_scales_offset_fmt(FMT, H, nbf);
+#pragma unroll 4
+                                for (int b = sub; b < nbf; b += LD) {
+                                    const int4 h0 = __ldcg(ha + 2 * b), h1 = __ldcg(ha + 2 * b + 1);
+                                    const int2 hsc = __ldcg(hs + b);
                                     WCodes<FMT> w;
                                     WScale<FMT> sc;
                                     w.load(bdg, (size_t)H * nbf, drow + b);
-                                    sc.load(bdg + blob_scales_offset_fmt(FMT, H, nbf), drow + b);
+                                    sc.load(bdg + soff, drow + b);
                                     acc += sc.term(w.dot(h0, h1, hsc.y), BlockScale{__int_as_float(hsc.x), hsc.y});
                                 }
                             }
@@ -1767,7 +1727,6 @@ __global__ void __launch_bounds__(256, 2) decode_layer_kernel(FusedParams p) {
         }
     } else {
         constexpr int G = 32 / LD, ROWS = kWarps * G;
-        constexpr int RD = 12;  // loads per lane issued together (<= 12 rounds)
         int8_t *hq_s = (int8_t *)dsm;                                   // [chunk][F]
         BlockScale *hds_s = (BlockScale *)(dsm + kMaxChunk * F);        // [chunk][nbf]
         const int sub = lane % LD, grp = lane / LD;
