@@ -1359,13 +1359,15 @@ __device__ __forceinline__ void t1_route_gate_up(const FusedParams &p, int *s_e,
     __syncthreads();  // routing results for CTAs without a gate/up item
 }
 
-// Row-block mode: the down rows of the cold used experts (read zero-copy over
-// the host link) for this CTA's first down item, requested only once every
-// cold expert's gate/up items are done.  Every down item needs the h of every pick,
-// so the link first serves the gate/up bytes that gate the whole down phase;
-// rows requested as soon as a CTA's own gate/up item was done made the last
-// gate/up items wait behind other CTAs' down rows (all-cold layer: 229 ->
-// 168 us with the register loads below).
+// Row-block mode, 2-8 tokens: the down rows of the cold used experts (read
+// zero-copy over the host link) for this CTA's first down item, requested
+// only once every cold expert's gate/up items are done.  Every down item
+// needs the h of every used expert, so the link first serves the gate/up
+// bytes that gate the whole down phase; rows requested as soon as a CTA's
+// own gate/up item was done made the last gate/up items wait behind other
+// CTAs' down rows (measured on the one-token layer, all-cold: 229 -> 168 us
+// with this deferral and the register loads below; that layer now reads
+// every down row in its dot loop instead).
 __device__ void stage_cold_down(const FusedParams &p, const int *s_uniq, int nu, const uint64_t *s_td, uint8_t *dpre,
                                 int rgs) {
     const GemvParams &g = p.g;
