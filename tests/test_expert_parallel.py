@@ -127,7 +127,7 @@ def _worker(rank, world, port, q, case):
         dist.destroy_process_group()
 
 
-def _run(world, case):
+def _run(world, case, n_msgs):
     port = _free_port()
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
@@ -137,8 +137,7 @@ def _run(world, case):
     for p in procs:
         p.join(180)
         assert p.exitcode == 0
-    out = [q.get(timeout=10) for _ in range(q.qsize() if hasattr(q, "qsize") else world)]
-    return out
+    return [q.get(timeout=10) for _ in range(n_msgs)]
 
 
 @pytest.mark.parametrize("world", [2, 3])
@@ -146,8 +145,7 @@ def test_replicated_tokens_allreduce_of_partials_is_the_layer(world):
     # synth and the oracle are compiled once before the ranks start
     synth.build()
     oracle.build()
-    out = _run(world, "replicated")
-    assert len(out) == 2 * world
+    out = _run(world, "replicated", 2 * world)  # two token counts per rank
     for rank, case, T, err in out:
         assert err <= 0.0, (rank, T, err)
 
@@ -156,9 +154,58 @@ def test_replicated_tokens_allreduce_of_partials_is_the_layer(world):
 def test_distributed_tokens_dispatch_and_combine(world):
     synth.build()
     oracle.build()
-    out = _run(world, "distributed")
-    assert len(out) == world
+    out = _run(world, "distributed", world)
     for rank, case, steps_ok, rows_ok, err in out:
         assert steps_ok, rank
         assert rows_ok, rank
         assert err <= 0.0, (rank, err)
+
+
+def test_rows_forward_passes_rows_and_step_tokens(monkeypatch):
+    # the product wrapper around moe_ffn_forward_rows: the received rows, their
+    # count and the step's token count reach the library call unchanged
+    calls = []
+
+    def fake(ctx, layer, x, n_rows, idx, w, y, step_tokens, stream=None):
+        calls.append((ctx, layer, n_rows, step_tokens, tuple(y.shape)))
+        y.fill_(1.0)
+
+    monkeypatch.setattr(ep, "moe_ffn_forward_rows", fake)
+    run = ep.rows_forward("ctx", 3)
+    x = torch.zeros((5, H))
+    y = run(x, torch.zeros((5, K), dtype=torch.int32), torch.zeros((5, K)), 17)
+    assert calls == [("ctx", 3, 5, 17, (5, H))]
+    assert torch.equal(y, torch.ones((5, H)))
+
+
+def _single_rank(port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=0, world_size=1)
+    try:
+        wl, tensors = _model()
+        x, lg = wl.x(0, 3, 6), wl.logits(0, 3, 6)
+        idx, w = oracle.topk(lg, K)
+
+        def local(x_r, idx_r, w_r, st):
+            return torch.from_numpy(_partial(tensors, 0, E, x_r.numpy(), idx_r.numpy(), w_r.numpy()).astype(np.float32))
+
+        y, st = ep.prefill_layer(torch.from_numpy(x), torch.from_numpy(np.asarray(idx, np.int32)),
+                                 torch.from_numpy(np.asarray(w, np.float32)), E, local)
+        y_full = oracle.layer(x, idx, w, *tensors, H, F)
+        q.put((st, float((np.abs(y.numpy() - y_full) - (1e-6 + 1e-5 * np.abs(y_full))).max())))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_one_rank_is_the_plain_layer():
+    # world size 1: every row stays home, the step counts this rank's tokens
+    synth.build()
+    oracle.build()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    p = ctx.Process(target=_single_rank, args=(_free_port(), q))
+    p.start()
+    p.join(120)
+    assert p.exitcode == 0
+    st, err = q.get(timeout=10)
+    assert st == 6 and err <= 0.0
