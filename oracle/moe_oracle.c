@@ -52,6 +52,13 @@
  *  format is published with: d, dmin, the 12 scale/min bytes packed as for
  *  Q4_K, 32 bytes qh, then 128 code bytes qs in the Q4_K chunk order; bit j
  *  of qh[l] is the fifth bit of element l of sub-block j.
+ *  6 = Q2_K, the K-quant of the pages' headline model (Q2_K_S): super-blocks
+ *  of 256 weights = 16 sub-blocks of 16, each with a 4-bit scale sc_j and a
+ *  4-bit min m_j, 2-bit codes, binary16 d and dmin, w = d*sc_j*q - dmin*m_j.
+ *  The 84-byte layout is the published one: 16 bytes scales (byte j: sc_j in
+ *  the low nibble, m_j in the high one), 64 code bytes qs, then d and dmin;
+ *  element i = 128n + 32m + t (half n, quarter m, t < 32) is bits 2m..2m+1
+ *  of qs[32n + t].
  *
  * Readings where the pages are silent (each listed in the design notes):
  *  - top-k order is (logit descending, expert index ascending): ties go to
@@ -83,6 +90,7 @@
 #define ORC_K4_SUPER_BYTES 144
 #define ORC_K6_SUPER_BYTES 210
 #define ORC_K5_SUPER_BYTES 176
+#define ORC_K2_SUPER_BYTES 84
 
 double orc_h2d(uint16_t h);
 
@@ -96,6 +104,7 @@ static size_t orc_row_bytes(int fmt, int nb) {
     if (fmt == 3) return (size_t)(nb / 8) * ORC_K4_SUPER_BYTES;
     if (fmt == 4) return (size_t)(nb / 8) * ORC_K6_SUPER_BYTES;
     if (fmt == 5) return (size_t)(nb / 8) * ORC_K5_SUPER_BYTES;
+    if (fmt == 6) return (size_t)(nb / 8) * ORC_K2_SUPER_BYTES;
     return (size_t)nb * orc_bbytes(fmt);
 }
 
@@ -166,6 +175,28 @@ void orc_k5_subdots(const uint8_t *sb, const int8_t *qa, int32_t *out) {
     for (int j = 0; j < 8; ++j) {
         int32_t s = 0;
         for (int i = 0; i < 32; ++i) s += (int32_t)orc_k5_code(sb, 32 * j + i) * (int32_t)qa[32 * j + i];
+        out[j] = s;
+    }
+}
+
+/* Q2_K: 2-bit code of element i (0..255), and scale / min of its 16-weight
+ * sub-block j = i / 16. */
+static int orc_k2_code(const uint8_t *sb, int i) {
+    const uint8_t *qs = sb + 16;
+    const int n = i / 128, m = (i % 128) / 32, t = i % 32;
+    return (qs[32 * n + t] >> (2 * m)) & 3;
+}
+static void orc_k2_scale_min(const uint8_t *sb, int j, int *sc, int *m) {
+    *sc = sb[j] & 15;
+    *m = sb[j] >> 4;
+}
+
+/* Q2_K: raw integer dots sum_i q_i * a_i of the 16 sub-blocks against 256
+ * int8 activations (exact in int32: |sum| <= 16 * 3 * 127). */
+void orc_k2_subdots(const uint8_t *sb, const int8_t *qa, int32_t *out) {
+    for (int j = 0; j < 16; ++j) {
+        int32_t s = 0;
+        for (int i = 0; i < 16; ++i) s += (int32_t)orc_k2_code(sb, 16 * j + i) * (int32_t)qa[16 * j + i];
         out[j] = s;
     }
 }
@@ -319,6 +350,18 @@ void orc_dequant_fmt(const uint8_t *blocks, int nb, int fmt, double *out) {
         }
         return;
     }
+    if (fmt == 6) { /* Q2_K: w = d * sc_j * q - dmin * m_j, sub-blocks of 16 */
+        for (int s = 0; s < nb / 8; ++s) {
+            const uint8_t *sb = blocks + (size_t)s * ORC_K2_SUPER_BYTES;
+            const double d = orc_h2d(orc_block_scale(sb + 80)), dmin = orc_h2d(orc_block_scale(sb + 82));
+            for (int i = 0; i < 256; ++i) {
+                int sc, m;
+                orc_k2_scale_min(sb, i / 16, &sc, &m);
+                out[(size_t)s * 256 + i] = d * sc * (double)orc_k2_code(sb, i) - dmin * m;
+            }
+        }
+        return;
+    }
     if (fmt == 5) { /* Q5_K: w = d * sc_j * q - dmin * m_j, q in 0..31 */
         for (int s = 0; s < nb / 8; ++s) {
             const uint8_t *sb = blocks + (size_t)s * ORC_K5_SUPER_BYTES;
@@ -379,6 +422,29 @@ double orc_row_dot_fmt(const uint8_t *row, const int8_t *qa, const uint16_t *da,
                 const double term = orc_h2d(da[8 * s + j]) * d * (double)dots[j];
                 acc += term;
                 aacc += fabs(term);
+            }
+        }
+        if (abs_sum) *abs_sum = aacc;
+        return acc;
+    }
+    if (fmt == 6) {
+        /* per 16-weight sub-block j (half of 32-block b = j / 2):
+         * d_a,b * (d * sc_j * sum q*a - dmin * m_j * sum a) */
+        for (int s = 0; s < nb / 8; ++s) {
+            const uint8_t *sb = row + (size_t)s * ORC_K2_SUPER_BYTES;
+            const double d = orc_h2d(orc_block_scale(sb + 80)), dmin = orc_h2d(orc_block_scale(sb + 82));
+            int32_t raw[16];
+            orc_k2_subdots(sb, qa + (size_t)s * 256, raw);
+            for (int j = 0; j < 16; ++j) {
+                const int b = 8 * s + j / 2;
+                int sc, m;
+                orc_k2_scale_min(sb, j, &sc, &m);
+                int32_t asum16 = 0;
+                for (int i = 0; i < 16; ++i) asum16 += qa[(size_t)s * 256 + 16 * j + i];
+                const double da_s = orc_h2d(da[b]);
+                const double sq = d * sc * (double)raw[j], mq = dmin * m * (double)asum16;
+                acc += da_s * (sq - mq);
+                aacc += fabs(da_s) * (fabs(sq) + fabs(mq));
             }
         }
         if (abs_sum) *abs_sum = aacc;

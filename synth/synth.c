@@ -215,6 +215,29 @@ void synth_q5k_blocks(uint64_t key, uint8_t *out, size_t n_super, double dlo, do
     }
 }
 
+/*
+ * Q2_K super-blocks of 256 weights in the published layout, 84 bytes each:
+ * 80 uniform bytes (16 bytes of 4-bit scales and mins, 64 code bytes), then
+ * d ~ U(dlo, dhi) and dmin ~ U(mlo, mhi) as binary16.
+ */
+void synth_q2k_blocks(uint64_t key, uint8_t *out, size_t n_super, double dlo, double dhi, double mlo, double mhi) {
+    xo_t g;
+    xo_init(&g, key);
+    for (size_t b = 0; b < n_super; ++b) {
+        uint8_t *sb = out + b * 84;
+        for (int w = 0; w < 80; w += 4) {
+            uint64_t v = xo_next(&g);
+            for (int j = 0; j < 4; ++j) sb[w + j] = (uint8_t)(v >> (8 * j));
+        }
+        uint16_t h = gen_f16_bits((float)(dlo + (dhi - dlo) * xo_unit(&g)));
+        uint16_t hm = gen_f16_bits((float)(mlo + (mhi - mlo) * xo_unit(&g)));
+        sb[80] = (uint8_t)(h & 0xff);
+        sb[81] = (uint8_t)(h >> 8);
+        sb[82] = (uint8_t)(hm & 0xff);
+        sb[83] = (uint8_t)(hm >> 8);
+    }
+}
+
 void synth_q4k_blocks(uint64_t key, uint8_t *out, size_t n_super, double dlo, double dhi, double mlo, double mhi) {
     xo_t g;
     xo_init(&g, key);
@@ -274,11 +297,14 @@ static void *q4_worker(void *arg) {
                       : j->fmt == 3 ? 144
                       : j->fmt == 4 ? 210
                       : j->fmt == 5 ? 176
+                      : j->fmt == 6 ? 84
                                     : 18;
     for (int e = j->e0; e < j->e1; ++e) {
         uint64_t key = synth_key(j->seed, 1, j->tag, (uint64_t)e, 0);
         uint8_t *dst = j->out + (size_t)e * j->blocks_per_expert * bb;
-        if (j->fmt == 5)
+        if (j->fmt == 6)
+            synth_q2k_blocks(key, dst, j->blocks_per_expert, j->dlo, j->dhi, 0.002, 0.0106);
+        else if (j->fmt == 5)
             synth_q5k_blocks(key, dst, j->blocks_per_expert, j->dlo, j->dhi, 0.0006, 0.0025);
         else if (j->fmt == 4)
             synth_q6k_blocks(key, dst, j->blocks_per_expert, j->dlo, j->dhi);
@@ -299,14 +325,21 @@ static void *q4_worker(void *arg) {
  * for Q4, fmt 0; 34 B for Q8_0, fmt 1; 22 B for Q5_0, fmt 2; 144-byte
  * super-blocks of 256 weights for Q4_K, fmt 3, with dmin ~ U(0.0006, 0.0025);
  * 210-byte super-blocks for Q6_K, fmt 4; 176-byte super-blocks for Q5_K,
- * fmt 5, dmin as for Q4_K).
+ * fmt 5, dmin as for Q4_K; 84-byte super-blocks for Q2_K, fmt 6, with
+ * dmin ~ U(0.002, 0.0106)).
  * Expert e is drawn from its own stream keyed by (seed, 1, tensor_tag, e), so
  * the result does not depend on n_threads and any expert can be regenerated
  * alone with synth_experts(seed, tag, e, e+1, ...).
  */
 void synth_experts(uint64_t seed, uint64_t tensor_tag, int e_begin, int e_end, size_t blocks_per_expert,
                    uint8_t *out, double dlo, double dhi, int n_threads, int fmt) {
-    const size_t bb = fmt == 1 ? 34 : fmt == 2 ? 22 : fmt == 3 ? 144 : fmt == 4 ? 210 : fmt == 5 ? 176 : 18;
+    const size_t bb = fmt == 1   ? 34
+                      : fmt == 2 ? 22
+                      : fmt == 3 ? 144
+                      : fmt == 4 ? 210
+                      : fmt == 5 ? 176
+                      : fmt == 6 ? 84
+                                 : 18;
     int n = e_end - e_begin;
     if (n <= 0) return;
     if (n_threads < 1) n_threads = 1;

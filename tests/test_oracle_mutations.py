@@ -49,6 +49,9 @@ C_MUTANTS = [
      "const uint8_t lb = ql[64 * n + 32 * (m >> 1) + l];"),
     ("q5k fifth bit index", "return lo | (((qh[l] >> j) & 1) << 4);", "return lo | (((qh[j] >> l) & 1) << 4);"),
     ("q5k code bytes offset", "const uint8_t *qh = sb + 16, *qs = sb + 48;", "const uint8_t *qh = sb + 16, *qs = sb + 44;"),
+    ("q2k quarter shift", "return (qs[32 * n + t] >> (2 * m)) & 3;", "return (qs[32 * n + t] >> m) & 3;"),
+    ("q2k min from the low nibble", "*m = sb[j] >> 4;", "*m = sb[j] & 15;"),
+    ("q2k min added in the dot", "acc += da_s * (sq - mq);", "acc += da_s * (sq + mq);"),
     ("q6k offset 31", "t += (int32_t)(orc_k6_code(sb, e) - 32) * (int32_t)qa[e];",
      "t += (int32_t)(orc_k6_code(sb, e) - 31) * (int32_t)qa[e];"),
 ]
@@ -65,9 +68,11 @@ C_PINS = [pins.test_h2d_all_bit_patterns_vs_numpy, pins.test_f2h_vs_numpy_random
           pins.test_q5_dequant_and_layer_vs_dense_fp64, pins.test_q4k_brute_force_vs_independent_decode,
           pins.test_q4k_layer_vs_dense_fp64, pins.test_shared_expert_layer_vs_dense_fp64,
           pins.test_q6k_brute_force_vs_independent_decode, pins.test_q6k_layer_vs_dense_fp64,
-          pins.test_q5k_brute_force_vs_independent_decode, pins.test_q5k_layer_vs_dense_fp64]
+          pins.test_q5k_brute_force_vs_independent_decode, pins.test_q5k_layer_vs_dense_fp64,
+          pins.test_q2k_brute_force_vs_independent_decode, pins.test_q2k_layer_vs_dense_fp64]
 C_GOLDEN_PINS = [pins.test_h2d_golden, pins.test_block_dot_golden, pins.test_q8_block_dot_golden,
-                 pins.test_q5_block_dot_golden, pins.test_q4k_golden, pins.test_q6k_golden, pins.test_q5k_golden]
+                 pins.test_q5_block_dot_golden, pins.test_q4k_golden, pins.test_q6k_golden, pins.test_q5k_golden,
+                 pins.test_q2k_golden]
 
 
 def _failing_pins(run):

@@ -652,7 +652,91 @@ def test_q5k_layer_vs_dense_fp64():
     np.testing.assert_allclose(y, y_bf, rtol=1e-12, atol=1e-12 * np.abs(y_bf).max())
 
 
-@pytest.mark.parametrize("fmt", [synth.FMT_Q8_0, synth.FMT_Q5_0, synth.FMT_Q4_K, synth.FMT_Q6_K, synth.FMT_Q5_K])
+# ---------------------------------------------------------------- Q2_K weights
+def _np_q2k(sb):
+    """Independent Q2_K decode with numpy: [..., 84] super-blocks -> codes
+    [..., 256] (0..3), scales and mins [..., 16], d and dmin.  Per
+    128-weight half, code byte t carries element t of each 32-weight quarter
+    m in bits 2m..2m+1."""
+    sb = np.asarray(sb, np.uint8)
+    sc = (sb[..., 0:16] & 15).astype(np.int64)
+    mn = (sb[..., 0:16] >> 4).astype(np.int64)
+    parts = []
+    for n in range(2):
+        qs = sb[..., 16 + 32 * n:16 + 32 * n + 32].astype(np.int64)
+        parts += [(qs >> (2 * m)) & 3 for m in range(4)]
+    codes = np.concatenate(parts, axis=-1)
+    d = np.ascontiguousarray(sb[..., 80:82]).view(np.float16)[..., 0].astype(np.float64)
+    dmin = np.ascontiguousarray(sb[..., 82:84]).view(np.float16)[..., 0].astype(np.float64)
+    return codes, sc, mn, d, dmin
+
+
+def _q2k_weights(sb):
+    codes, sc, mn, d, dmin = _np_q2k(sb)
+    return (np.repeat(d[..., None] * sc, 16, axis=-1) * codes - np.repeat(dmin[..., None] * mn, 16, axis=-1))
+
+
+def test_q2k_golden(golden):
+    (scales, qs_over, d, dmin, over, dots, weights), = golden("q2k_superblock.txt")
+    sb = np.zeros(84, np.uint8)
+    sb[0:16] = np.frombuffer(bytes.fromhex(scales), np.uint8)
+    for kv in qs_over.split(","):
+        i, v = kv.split("=")
+        sb[16 + int(i)] = int(v, 16)
+    sb[80:82] = np.array([int(d, 16) & 0xFF, int(d, 16) >> 8], np.uint8)  # little endian
+    sb[82:84] = np.array([int(dmin, 16) & 0xFF, int(dmin, 16) >> 8], np.uint8)
+    a = np.ones(256, np.int8)
+    for kv in over.split(","):
+        i, v = kv.split("=")
+        a[int(i)] = int(v)
+    assert oracle.q2k_subdots(sb, a).tolist() == [int(v) for v in dots.split(",")]
+    w = oracle.dequant(sb.reshape(1, 84))
+    for kv in weights.split(","):
+        i, v = kv.split("=")
+        assert w[int(i)] == float(v)
+
+
+def test_q2k_brute_force_vs_independent_decode():
+    sbs = synth.q2k_blocks(synth.key(7, 700), 60)
+    codes, sc, mn, _, _ = _np_q2k(sbs)
+    assert codes.min() == 0 and codes.max() == 3 and sc.max() == 15 and mn.max() == 15
+    acts = RNG.integers(-127, 128, (60, 256)).astype(np.int8)
+    for i in range(60):
+        ref = (codes[i].reshape(16, 16) * acts[i].astype(np.int64).reshape(16, 16)).sum(axis=1)
+        assert np.array_equal(oracle.q2k_subdots(sbs[i], acts[i]), ref)
+    assert np.array_equal(oracle.dequant(sbs.reshape(3, 20, 84)), _q2k_weights(sbs).reshape(3, 20 * 256))
+
+
+def test_q2k_layer_vs_dense_fp64():
+    wl = synth.Workload("tiny_q2k", 512, 8, 2, 256, 1, routing="normal", weight_format=synth.FMT_Q2_K)
+    H, F, k, T = wl.hidden, wl.ffn, wl.top_k, 3
+    gate, up, down = (wl.expert_tensor(0, kd) for kd in range(3))
+    assert gate.shape == (8, F, H // 256, 84) and down.shape == (8, H, F // 256, 84)
+    x, logits = wl.x(0, 0, T), wl.logits(0, 0, T)
+    idx, w = oracle.topk(logits, k)
+    y, it = oracle.layer(x, idx, w, gate, up, down, H, F, want_intermediates=True)
+
+    def deq(t):
+        return _q2k_weights(t).reshape(t.shape[0], t.shape[1], -1)
+
+    Wg, Wu, Wd = deq(gate), deq(up), deq(down)
+    xa = it["xq"].astype(np.float64) * np.repeat(it["xd"].view(np.float16).astype(np.float64), 32, axis=1)
+    y_bf = np.zeros((T, H))
+    for t in range(T):
+        for j in range(k):
+            a, e = t * k + j, idx[t, j]
+            g, u = Wg[e] @ xa[t], Wu[e] @ xa[t]
+            np.testing.assert_allclose(it["g"][a], g, rtol=0, atol=1e-12 * np.abs(g).max())
+            h = g * u * expit(g)
+            hq, hd = oracle.quantize(h.astype(np.float32))
+            assert np.array_equal(hq, it["hq"][a]) and np.array_equal(hd, it["hd"][a])
+            ha = hq.astype(np.float64) * np.repeat(hd.view(np.float16).astype(np.float64), 32)
+            y_bf[t] += w[t, j] * (Wd[e] @ ha)
+    np.testing.assert_allclose(y, y_bf, rtol=1e-12, atol=1e-12 * np.abs(y_bf).max())
+
+
+@pytest.mark.parametrize("fmt", [synth.FMT_Q8_0, synth.FMT_Q5_0, synth.FMT_Q4_K, synth.FMT_Q6_K, synth.FMT_Q5_K,
+                                 synth.FMT_Q2_K])
 def test_generators_of_every_format_are_range_and_thread_independent(fmt):
     # the same expert's bytes whether generated alone or in a range, with any
     # thread count (the oracle and the library register the same weights)
