@@ -62,6 +62,7 @@ def configure(L):
     L.orc_k6_blockdots.argtypes = [vp, vp, vp]
     L.orc_k5_subdots.argtypes = [vp, vp, vp]
     L.orc_k2_subdots.argtypes = [vp, vp, vp]
+    L.orc_k3_blockdots.argtypes = [vp, vp, vp]
     L.orc_expert.argtypes = [vp, vp, vp, i32, i32, vp, vp] + [vp] * 8 + [i32]
     L.orc_down_combine.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, i32]
     L.orc_layer.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp] + [vp] * 9 + [i32]
@@ -109,14 +110,14 @@ def quantize(x: np.ndarray):
     return q, d
 
 
-# canonical block size -> format (0: Q4, 1: Q8_0, 2: Q5_0, 3: Q4_K, 4: Q6_K, 5: Q5_K, 6: Q2_K)
-BLOCK_BYTES = {18: 0, 34: 1, 22: 2, 144: 3, 210: 4, 176: 5, 84: 6}
-ELEMS = {0: 32, 1: 32, 2: 32, 3: 256, 4: 256, 5: 256, 6: 256}  # weights per canonical block
+# canonical block size -> format (0: Q4, 1: Q8_0, 2: Q5_0, 3: Q4_K, 4: Q6_K, 5: Q5_K, 6: Q2_K, 7: Q3_K)
+BLOCK_BYTES = {18: 0, 34: 1, 22: 2, 144: 3, 210: 4, 176: 5, 84: 6, 110: 7}
+ELEMS = {0: 32, 1: 32, 2: 32, 3: 256, 4: 256, 5: 256, 6: 256, 7: 256}  # weights per canonical block
 
 
 def _fmt(blocks) -> int:
     """Format of canonical blocks from their last dimension (18: Q4, 34: Q8_0, 22: Q5_0,
-    144: Q4_K, 210: Q6_K, 176: Q5_K and 84: Q2_K super-blocks of 256 weights)."""
+    144: Q4_K, 210: Q6_K, 176: Q5_K, 84: Q2_K and 110: Q3_K super-blocks of 256 weights)."""
     if blocks.shape[-1] not in BLOCK_BYTES:
         raise ValueError(f"unknown block size {blocks.shape[-1]}")
     return BLOCK_BYTES[blocks.shape[-1]]
@@ -159,6 +160,17 @@ def q2k_subdots(superblock: np.ndarray, qa: np.ndarray) -> np.ndarray:
     qa = np.ascontiguousarray(qa, np.int8)
     out = np.empty(16, np.int32)
     lib().orc_k2_subdots(_p(sb), _p(qa), _p(out))
+    return out
+
+
+def q3k_blockdots(superblock: np.ndarray, qa: np.ndarray) -> np.ndarray:
+    """Q3_K: the integer dots of the 8 32-weight blocks of one super-block
+    (each = the two 16-weight halves' sums of q * a times their scales)."""
+    sb = np.ascontiguousarray(superblock, np.uint8)
+    assert sb.size == 110 and qa.size == 256
+    qa = np.ascontiguousarray(qa, np.int8)
+    out = np.empty(8, np.int32)
+    lib().orc_k3_blockdots(_p(sb), _p(qa), _p(out))
     return out
 
 

@@ -59,6 +59,14 @@
  *  the low nibble, m_j in the high one), 64 code bytes qs, then d and dmin;
  *  element i = 128n + 32m + t (half n, quarter m, t < 32) is bits 2m..2m+1
  *  of qs[32n + t].
+ *  7 = Q3_K: super-blocks of 256 weights = 16 sub-blocks of 16 with signed
+ *  6-bit scales sc_j, binary16 d, 3-bit codes q in -4..3, w = d*sc_j*q.  The
+ *  110-byte layout is the published one: 32 bytes hmask, 64 code bytes qs,
+ *  12 scale bytes, d.  Element 128n + 32m + t has the low two bits
+ *  (qs[32n + t] >> 2m) & 3 and q = low - 4 unless bit 4n + m of hmask[t] is
+ *  set (then q = low).  Scale j: low four bits = byte j & 15 (j < 8) or byte
+ *  j - 8 >> 4 (j >= 8), high two = bits 2(j/4)..2(j/4)+1 of byte 8 + j mod 4,
+ *  sc_j = that 6-bit value - 32.
  *
  * Readings where the pages are silent (each listed in the design notes):
  *  - top-k order is (logit descending, expert index ascending): ties go to
@@ -91,6 +99,7 @@
 #define ORC_K6_SUPER_BYTES 210
 #define ORC_K5_SUPER_BYTES 176
 #define ORC_K2_SUPER_BYTES 84
+#define ORC_K3_SUPER_BYTES 110
 
 double orc_h2d(uint16_t h);
 
@@ -105,6 +114,7 @@ static size_t orc_row_bytes(int fmt, int nb) {
     if (fmt == 4) return (size_t)(nb / 8) * ORC_K6_SUPER_BYTES;
     if (fmt == 5) return (size_t)(nb / 8) * ORC_K5_SUPER_BYTES;
     if (fmt == 6) return (size_t)(nb / 8) * ORC_K2_SUPER_BYTES;
+    if (fmt == 7) return (size_t)(nb / 8) * ORC_K3_SUPER_BYTES;
     return (size_t)nb * orc_bbytes(fmt);
 }
 
@@ -176,6 +186,40 @@ void orc_k5_subdots(const uint8_t *sb, const int8_t *qa, int32_t *out) {
         int32_t s = 0;
         for (int i = 0; i < 32; ++i) s += (int32_t)orc_k5_code(sb, 32 * j + i) * (int32_t)qa[32 * j + i];
         out[j] = s;
+    }
+}
+
+/* Q3_K: signed 3-bit code of element i (0..255), signed scale of its
+ * 16-weight sub-block j = i / 16, and d. */
+static int orc_k3_code(const uint8_t *sb, int i) {
+    const uint8_t *hm = sb, *qs = sb + 32;
+    const int n = i / 128, m = (i % 128) / 32, t = i % 32;
+    const int low = (qs[32 * n + t] >> (2 * m)) & 3;
+    return ((hm[t] >> (4 * n + m)) & 1) ? low : low - 4;
+}
+static int orc_k3_scale(const uint8_t *sb, int j) {
+    const uint8_t *b = sb + 96;
+    const int low4 = j < 8 ? (b[j] & 15) : (b[j - 8] >> 4);
+    const int high2 = (b[8 + j % 4] >> (2 * (j / 4))) & 3;
+    return (low4 | (high2 << 4)) - 32;
+}
+static double orc_k3_d(const uint8_t *sb) { return orc_h2d((uint16_t)(sb[108] | (sb[109] << 8))); }
+
+/* Q3_K: the integer dot of each 32-weight block against 32 int8
+ * activations: sc_2b * sum_{i<16} q a + sc_2b+1 * sum_{16<=i<32} q a
+ * (exact in int32: |.| <= 2 * 32 * 16 * 4 * 127). */
+void orc_k3_blockdots(const uint8_t *sb, const int8_t *qa, int32_t *out) {
+    for (int b = 0; b < 8; ++b) {
+        int32_t s = 0;
+        for (int h = 0; h < 2; ++h) {
+            int32_t part = 0;
+            for (int i = 0; i < 16; ++i) {
+                const int e = 32 * b + 16 * h + i;
+                part += (int32_t)orc_k3_code(sb, e) * (int32_t)qa[e];
+            }
+            s += orc_k3_scale(sb, 2 * b + h) * part;
+        }
+        out[b] = s;
     }
 }
 
@@ -350,6 +394,15 @@ void orc_dequant_fmt(const uint8_t *blocks, int nb, int fmt, double *out) {
         }
         return;
     }
+    if (fmt == 7) { /* Q3_K: w = d * sc_j * q, sub-blocks of 16 */
+        for (int s = 0; s < nb / 8; ++s) {
+            const uint8_t *sb = blocks + (size_t)s * ORC_K3_SUPER_BYTES;
+            const double d = orc_k3_d(sb);
+            for (int i = 0; i < 256; ++i)
+                out[(size_t)s * 256 + i] = d * orc_k3_scale(sb, i / 16) * (double)orc_k3_code(sb, i);
+        }
+        return;
+    }
     if (fmt == 6) { /* Q2_K: w = d * sc_j * q - dmin * m_j, sub-blocks of 16 */
         for (int s = 0; s < nb / 8; ++s) {
             const uint8_t *sb = blocks + (size_t)s * ORC_K2_SUPER_BYTES;
@@ -422,6 +475,22 @@ double orc_row_dot_fmt(const uint8_t *row, const int8_t *qa, const uint16_t *da,
                 const double term = orc_h2d(da[8 * s + j]) * d * (double)dots[j];
                 acc += term;
                 aacc += fabs(term);
+            }
+        }
+        if (abs_sum) *abs_sum = aacc;
+        return acc;
+    }
+    if (fmt == 7) {
+        /* per 32-weight block b: d_a,b * d * (its two-scale integer dot) */
+        for (int s = 0; s < nb / 8; ++s) {
+            const uint8_t *sb = row + (size_t)s * ORC_K3_SUPER_BYTES;
+            const double d3 = orc_k3_d(sb);
+            int32_t dots3[8];
+            orc_k3_blockdots(sb, qa + (size_t)s * 256, dots3);
+            for (int j = 0; j < 8; ++j) {
+                const double t3 = orc_h2d(da[8 * s + j]) * d3 * (double)dots3[j];
+                acc += t3;
+                aacc += fabs(t3);
             }
         }
         if (abs_sum) *abs_sum = aacc;

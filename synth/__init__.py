@@ -38,19 +38,20 @@ Q4K_BLOCK_BYTES = 144  # one super-block of 256 weights
 Q6K_BLOCK_BYTES = 210  # one super-block of 256 weights
 Q5K_BLOCK_BYTES = 176  # one super-block of 256 weights
 Q2K_BLOCK_BYTES = 84   # one super-block of 256 weights
-FMT_Q4, FMT_Q8_0, FMT_Q5_0, FMT_Q4_K, FMT_Q6_K, FMT_Q5_K, FMT_Q2_K = 0, 1, 2, 3, 4, 5, 6
+Q3K_BLOCK_BYTES = 110  # one super-block of 256 weights
+FMT_Q4, FMT_Q8_0, FMT_Q5_0, FMT_Q4_K, FMT_Q6_K, FMT_Q5_K, FMT_Q2_K, FMT_Q3_K = 0, 1, 2, 3, 4, 5, 6, 7
 BLOCK_BYTES = {FMT_Q4: Q4_BLOCK_BYTES, FMT_Q8_0: Q8_BLOCK_BYTES, FMT_Q5_0: Q5_BLOCK_BYTES,
                FMT_Q4_K: Q4K_BLOCK_BYTES, FMT_Q6_K: Q6K_BLOCK_BYTES, FMT_Q5_K: Q5K_BLOCK_BYTES,
-               FMT_Q2_K: Q2K_BLOCK_BYTES}
+               FMT_Q2_K: Q2K_BLOCK_BYTES, FMT_Q3_K: Q3K_BLOCK_BYTES}
 BLOCK_ELEMS = {FMT_Q4: 32, FMT_Q8_0: 32, FMT_Q5_0: 32, FMT_Q4_K: 256, FMT_Q6_K: 256, FMT_Q5_K: 256,
-               FMT_Q2_K: 256}
+               FMT_Q2_K: 256, FMT_Q3_K: 256}
 # scale ranges: |w| <= 0.16 in every format (|q - 8| <= 8 for Q4, |q| <= 127
 # for Q8_0, |q - 16| <= 16 for Q5_0; Q4_K: d * 63 * 15 and dmin * 63 <= 0.16;
 # Q6_K: d * 64 * 32 <= 0.16; Q5_K: d * 63 * 31 <= 0.16; Q2_K: d * 15 * 3 and
-# dmin * 15 <= 0.16)
+# dmin * 15 <= 0.16; Q3_K: d * 32 * 4 <= 0.16)
 D_RANGE = {FMT_Q4: (0.005, 0.02), FMT_Q8_0: (0.005 / 16, 0.02 / 16), FMT_Q5_0: (0.0025, 0.01),
            FMT_Q4_K: (0.0000625, 0.00017), FMT_Q6_K: (0.00002, 0.000078), FMT_Q5_K: (0.00003, 0.000082),
-           FMT_Q2_K: (0.001, 0.0035)}
+           FMT_Q2_K: (0.001, 0.0035), FMT_Q3_K: (0.0004, 0.00125)}
 
 
 def build(force: bool = False) -> str:
@@ -85,6 +86,7 @@ def lib():
         L.synth_q6k_blocks.argtypes = [u64, vp, sz, dbl, dbl]
         L.synth_q5k_blocks.argtypes = [u64, vp, sz, dbl, dbl, dbl, dbl]
         L.synth_q2k_blocks.argtypes = [u64, vp, sz, dbl, dbl, dbl, dbl]
+        L.synth_q3k_blocks.argtypes = [u64, vp, sz, dbl, dbl]
         L.synth_experts.argtypes = [u64, u64, i32, i32, sz, vp, dbl, dbl, i32, i32]
         L.synth_permutation.argtypes = [u64, vp, i32]
         L.synth_gumbel_logits.argtypes = [u64, vp, i32, i32, vp]
@@ -151,6 +153,13 @@ def q2k_blocks(k: int, n_super: int, dlo: float = D_RANGE[FMT_Q2_K][0], dhi: flo
                mlo: float = 0.002, mhi: float = 0.0106) -> np.ndarray:
     out = np.empty((n_super, Q2K_BLOCK_BYTES), np.uint8)
     lib().synth_q2k_blocks(k, _ptr(out), n_super, dlo, dhi, mlo, mhi)
+    return out
+
+
+def q3k_blocks(k: int, n_super: int, dlo: float = D_RANGE[FMT_Q3_K][0],
+               dhi: float = D_RANGE[FMT_Q3_K][1]) -> np.ndarray:
+    out = np.empty((n_super, Q3K_BLOCK_BYTES), np.uint8)
+    lib().synth_q3k_blocks(k, _ptr(out), n_super, dlo, dhi)
     return out
 
 

@@ -238,6 +238,26 @@ void synth_q2k_blocks(uint64_t key, uint8_t *out, size_t n_super, double dlo, do
     }
 }
 
+/*
+ * Q3_K super-blocks of 256 weights in the published layout, 110 bytes each:
+ * 108 uniform bytes (hmask, code bytes, packed 6-bit scales), then a
+ * binary16 d ~ U(dlo, dhi).
+ */
+void synth_q3k_blocks(uint64_t key, uint8_t *out, size_t n_super, double dlo, double dhi) {
+    xo_t g;
+    xo_init(&g, key);
+    for (size_t b = 0; b < n_super; ++b) {
+        uint8_t *sb = out + b * 110;
+        for (int w = 0; w < 108; w += 4) {
+            uint64_t v = xo_next(&g);
+            for (int j = 0; j < 4; ++j) sb[w + j] = (uint8_t)(v >> (8 * j));
+        }
+        uint16_t h = gen_f16_bits((float)(dlo + (dhi - dlo) * xo_unit(&g)));
+        sb[108] = (uint8_t)(h & 0xff);
+        sb[109] = (uint8_t)(h >> 8);
+    }
+}
+
 void synth_q4k_blocks(uint64_t key, uint8_t *out, size_t n_super, double dlo, double dhi, double mlo, double mhi) {
     xo_t g;
     xo_init(&g, key);
@@ -298,11 +318,14 @@ static void *q4_worker(void *arg) {
                       : j->fmt == 4 ? 210
                       : j->fmt == 5 ? 176
                       : j->fmt == 6 ? 84
+                      : j->fmt == 7 ? 110
                                     : 18;
     for (int e = j->e0; e < j->e1; ++e) {
         uint64_t key = synth_key(j->seed, 1, j->tag, (uint64_t)e, 0);
         uint8_t *dst = j->out + (size_t)e * j->blocks_per_expert * bb;
-        if (j->fmt == 6)
+        if (j->fmt == 7)
+            synth_q3k_blocks(key, dst, j->blocks_per_expert, j->dlo, j->dhi);
+        else if (j->fmt == 6)
             synth_q2k_blocks(key, dst, j->blocks_per_expert, j->dlo, j->dhi, 0.002, 0.0106);
         else if (j->fmt == 5)
             synth_q5k_blocks(key, dst, j->blocks_per_expert, j->dlo, j->dhi, 0.0006, 0.0025);
@@ -326,7 +349,7 @@ static void *q4_worker(void *arg) {
  * super-blocks of 256 weights for Q4_K, fmt 3, with dmin ~ U(0.0006, 0.0025);
  * 210-byte super-blocks for Q6_K, fmt 4; 176-byte super-blocks for Q5_K,
  * fmt 5, dmin as for Q4_K; 84-byte super-blocks for Q2_K, fmt 6, with
- * dmin ~ U(0.002, 0.0106)).
+ * dmin ~ U(0.002, 0.0106); 110-byte super-blocks for Q3_K, fmt 7).
  * Expert e is drawn from its own stream keyed by (seed, 1, tensor_tag, e), so
  * the result does not depend on n_threads and any expert can be regenerated
  * alone with synth_experts(seed, tag, e, e+1, ...).
@@ -339,6 +362,7 @@ void synth_experts(uint64_t seed, uint64_t tensor_tag, int e_begin, int e_end, s
                       : fmt == 4 ? 210
                       : fmt == 5 ? 176
                       : fmt == 6 ? 84
+                      : fmt == 7 ? 110
                                  : 18;
     int n = e_end - e_begin;
     if (n <= 0) return;

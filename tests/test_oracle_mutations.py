@@ -52,6 +52,10 @@ C_MUTANTS = [
     ("q2k quarter shift", "return (qs[32 * n + t] >> (2 * m)) & 3;", "return (qs[32 * n + t] >> m) & 3;"),
     ("q2k min from the low nibble", "*m = sb[j] >> 4;", "*m = sb[j] & 15;"),
     ("q2k min added in the dot", "acc += da_s * (sq - mq);", "acc += da_s * (sq + mq);"),
+    ("q3k high bit sense", "return ((hm[t] >> (4 * n + m)) & 1) ? low : low - 4;",
+     "return ((hm[t] >> (4 * n + m)) & 1) ? low - 4 : low;"),
+    ("q3k scale high pair", "const int high2 = (b[8 + j % 4] >> (2 * (j / 4))) & 3;",
+     "const int high2 = (b[8 + j / 4] >> (2 * (j % 4))) & 3;"),
     ("q6k offset 31", "t += (int32_t)(orc_k6_code(sb, e) - 32) * (int32_t)qa[e];",
      "t += (int32_t)(orc_k6_code(sb, e) - 31) * (int32_t)qa[e];"),
 ]
@@ -69,10 +73,11 @@ C_PINS = [pins.test_h2d_all_bit_patterns_vs_numpy, pins.test_f2h_vs_numpy_random
           pins.test_q4k_layer_vs_dense_fp64, pins.test_shared_expert_layer_vs_dense_fp64,
           pins.test_q6k_brute_force_vs_independent_decode, pins.test_q6k_layer_vs_dense_fp64,
           pins.test_q5k_brute_force_vs_independent_decode, pins.test_q5k_layer_vs_dense_fp64,
-          pins.test_q2k_brute_force_vs_independent_decode, pins.test_q2k_layer_vs_dense_fp64]
+          pins.test_q2k_brute_force_vs_independent_decode, pins.test_q2k_layer_vs_dense_fp64,
+          pins.test_q3k_brute_force_vs_independent_decode, pins.test_q3k_layer_vs_dense_fp64]
 C_GOLDEN_PINS = [pins.test_h2d_golden, pins.test_block_dot_golden, pins.test_q8_block_dot_golden,
                  pins.test_q5_block_dot_golden, pins.test_q4k_golden, pins.test_q6k_golden, pins.test_q5k_golden,
-                 pins.test_q2k_golden]
+                 pins.test_q2k_golden, pins.test_q3k_golden]
 
 
 def _failing_pins(run):

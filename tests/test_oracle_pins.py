@@ -735,8 +735,98 @@ def test_q2k_layer_vs_dense_fp64():
     np.testing.assert_allclose(y, y_bf, rtol=1e-12, atol=1e-12 * np.abs(y_bf).max())
 
 
+# ---------------------------------------------------------------- Q3_K weights
+def _np_q3k(sb):
+    """Independent Q3_K decode with numpy: [..., 110] super-blocks -> signed
+    codes [..., 256] (-4..3), signed scales [..., 16], d.  Per 128-weight half
+    n, code byte t and hmask byte t carry element t of each quarter m (bits
+    2m..2m+1 of the code byte, bit 4n + m of the hmask byte)."""
+    sb = np.asarray(sb, np.uint8)
+    hm = sb[..., 0:32].astype(np.int64)
+    parts = []
+    for n in range(2):
+        qs = sb[..., 32 + 32 * n:32 + 32 * n + 32].astype(np.int64)
+        for m in range(4):
+            low = (qs >> (2 * m)) & 3
+            hbit = (hm >> (4 * n + m)) & 1
+            parts.append(np.where(hbit == 1, low, low - 4))
+    codes = np.concatenate(parts, axis=-1)
+    b = sb[..., 96:108].astype(np.int64)
+    low4 = np.concatenate([b[..., 0:8] & 15, b[..., 0:8] >> 4], axis=-1)          # j = 0..7, 8..15
+    high2 = np.concatenate([(b[..., 8:12] >> (2 * q)) & 3 for q in range(4)], axis=-1)  # j = 4q + r
+    sc = (low4 | (high2 << 4)) - 32
+    d = np.ascontiguousarray(sb[..., 108:110]).view(np.float16)[..., 0].astype(np.float64)
+    return codes, sc, d
+
+
+def _q3k_weights(sb):
+    codes, sc, d = _np_q3k(sb)
+    return d[..., None] * np.repeat(sc, 16, axis=-1) * codes
+
+
+def test_q3k_golden(golden):
+    (hm_over, qs_over, scales, d, over, dots, weights), = golden("q3k_superblock.txt")
+    sb = np.zeros(110, np.uint8)
+    for kv in hm_over.split(","):
+        i, v = kv.split("=")
+        sb[int(i)] = int(v, 16)
+    for kv in qs_over.split(","):
+        i, v = kv.split("=")
+        sb[32 + int(i)] = int(v, 16)
+    sb[96:108] = np.frombuffer(bytes.fromhex(scales.replace(" ", "")), np.uint8)
+    sb[108:110] = np.array([int(d, 16) & 0xFF, int(d, 16) >> 8], np.uint8)  # little endian
+    a = np.ones(256, np.int8)
+    for kv in over.split(","):
+        i, v = kv.split("=")
+        a[int(i)] = int(v)
+    assert oracle.q3k_blockdots(sb, a).tolist() == [int(v) for v in dots.split(",")]
+    w = oracle.dequant(sb.reshape(1, 110))
+    for kv in weights.split(","):
+        i, v = kv.split("=")
+        assert w[int(i)] == float(v)
+
+
+def test_q3k_brute_force_vs_independent_decode():
+    sbs = synth.q3k_blocks(synth.key(7, 800), 60)
+    codes, sc, _ = _np_q3k(sbs)
+    assert codes.min() == -4 and codes.max() == 3 and sc.min() == -32 and sc.max() == 31
+    acts = RNG.integers(-127, 128, (60, 256)).astype(np.int8)
+    for i in range(60):
+        t = (codes[i] * acts[i].astype(np.int64)).reshape(16, 16).sum(axis=1) * sc[i]
+        assert np.array_equal(oracle.q3k_blockdots(sbs[i], acts[i]), t.reshape(8, 2).sum(axis=1))
+    assert np.array_equal(oracle.dequant(sbs.reshape(3, 20, 110)), _q3k_weights(sbs).reshape(3, 20 * 256))
+
+
+def test_q3k_layer_vs_dense_fp64():
+    wl = synth.Workload("tiny_q3k", 512, 8, 2, 256, 1, routing="normal", weight_format=synth.FMT_Q3_K)
+    H, F, k, T = wl.hidden, wl.ffn, wl.top_k, 3
+    gate, up, down = (wl.expert_tensor(0, kd) for kd in range(3))
+    assert gate.shape == (8, F, H // 256, 110) and down.shape == (8, H, F // 256, 110)
+    x, logits = wl.x(0, 0, T), wl.logits(0, 0, T)
+    idx, w = oracle.topk(logits, k)
+    y, it = oracle.layer(x, idx, w, gate, up, down, H, F, want_intermediates=True)
+
+    def deq(t):
+        return _q3k_weights(t).reshape(t.shape[0], t.shape[1], -1)
+
+    Wg, Wu, Wd = deq(gate), deq(up), deq(down)
+    xa = it["xq"].astype(np.float64) * np.repeat(it["xd"].view(np.float16).astype(np.float64), 32, axis=1)
+    y_bf = np.zeros((T, H))
+    for t in range(T):
+        for j in range(k):
+            a, e = t * k + j, idx[t, j]
+            g, u = Wg[e] @ xa[t], Wu[e] @ xa[t]
+            np.testing.assert_allclose(it["g"][a], g, rtol=0, atol=1e-12 * np.abs(g).max())
+            h = g * u * expit(g)
+            hq, hd = oracle.quantize(h.astype(np.float32))
+            assert np.array_equal(hq, it["hq"][a]) and np.array_equal(hd, it["hd"][a])
+            ha = hq.astype(np.float64) * np.repeat(hd.view(np.float16).astype(np.float64), 32)
+            y_bf[t] += w[t, j] * (Wd[e] @ ha)
+    np.testing.assert_allclose(y, y_bf, rtol=1e-12, atol=1e-12 * np.abs(y_bf).max())
+
+
 @pytest.mark.parametrize("fmt", [synth.FMT_Q8_0, synth.FMT_Q5_0, synth.FMT_Q4_K, synth.FMT_Q6_K, synth.FMT_Q5_K,
-                                 synth.FMT_Q2_K])
+                                 synth.FMT_Q2_K, synth.FMT_Q3_K])
 def test_generators_of_every_format_are_range_and_thread_independent(fmt):
     # the same expert's bytes whether generated alone or in a range, with any
     # thread count (the oracle and the library register the same weights)
