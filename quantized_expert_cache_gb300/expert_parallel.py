@@ -78,6 +78,8 @@ def dispatch(x: torch.Tensor, idx: torch.Tensor, w: torch.Tensor, n_experts: int
     handle): the rows this rank received (from rank 0's tokens first, each
     source's rows in token order), and the number of tokens of the step over
     all ranks (the clock a rank's pool hits are stamped with)."""
+    if x.dtype != torch.float32 or w.dtype != torch.float32 or idx.dtype != torch.int32:
+        raise TypeError("dispatch: x and w must be float32 and idx int32 (the payload carries the ids' bits)")
     world = dist.get_world_size(group)
     T, k = idx.shape
     H = x.shape[1]

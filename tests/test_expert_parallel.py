@@ -209,3 +209,19 @@ def test_one_rank_is_the_plain_layer():
     assert p.exitcode == 0
     st, err = q.get(timeout=10)
     assert st == 6 and err <= 0.0
+
+
+
+@pytest.mark.parametrize("bad", ["idx", "x", "w"])
+def test_dispatch_rejects_other_dtypes(bad):
+    # the ids travel as their int32 bits inside one float32 payload row, so a
+    # wider id or a half-precision row is refused before any collective
+    x, idx, w = torch.zeros((2, H)), torch.zeros((2, K), dtype=torch.int32), torch.zeros((2, K))
+    if bad == "idx":
+        idx = idx.to(torch.int64)
+    elif bad == "x":
+        x = x.to(torch.float16)
+    else:
+        w = w.to(torch.float64)
+    with pytest.raises(TypeError):
+        ep.dispatch(x, idx, w, E)
