@@ -68,3 +68,42 @@ def test_init_rejects_bad_formats_and_shared_experts_without_a_device():
     # a shared expert takes table column E, so E + 1 ids must fit 12 bits
     bad(shared_experts=1, n_experts=4096, top_k=2)
     bad(shared_experts=2)
+
+
+# entry points whose first argument is the context
+_CTX_CALLS = [n for n, (_, args) in qec.SIGNATURES.items()
+              if n not in ("moe_layer_init", "moe_last_error", "moe_destroy", "moe_probe_host_read",
+                           "moe_expert_ffn_noalloc", "moe_expert_ffn_noalloc_status")]
+
+
+@pytest.mark.parametrize("name", _CTX_CALLS)
+def test_every_context_call_rejects_a_null_context(name):
+    # the header's error behaviour: a null context is MOE_ERR_ARG, checked
+    # before any other argument and before any CUDA call
+    lib = qec.load()
+    fn = getattr(lib, name)
+    args = [None if t is ctypes.c_void_p or issubclass(t, ctypes._Pointer) else 0 for t in qec.SIGNATURES[name][1]]
+    assert fn(*args) == -1
+    assert qec.moe_last_error(None)
+
+
+def test_destroy_of_a_null_context_is_a_no_op():
+    qec.load().moe_destroy(None)
+
+
+def test_noalloc_and_probe_reject_bad_arguments_without_a_device():
+    lib = qec.load()
+    p = ctypes.c_void_p(16)  # never dereferenced: every case below fails its size checks first
+
+    def call(n_tokens=1, hidden=256, ffn=256, n_experts=8, top_k=2, ptr=p):
+        return lib.moe_expert_ffn_noalloc(ptr, n_tokens, ptr, ptr, ptr, hidden, ffn, n_experts, top_k, ptr, None)
+
+    assert call(n_tokens=-1) == -1
+    assert call(hidden=100) == -1 and call(ffn=48) == -1
+    assert call(n_experts=0) == -1 and call(n_experts=4097) == -1
+    assert call(top_k=0) == -1 and call(top_k=9) == -1
+    assert call(n_tokens=33) == -1          # more tokens than the single launch holds
+    assert call(n_tokens=1, ptr=None) == -1  # a null pointer
+    assert call(n_tokens=0, ptr=None) == 0   # nothing to do: no pointer is read
+    gbs = ctypes.c_double()
+    assert lib.moe_probe_host_read(None, 1 << 20, 1, ctypes.byref(gbs), None) == -1
