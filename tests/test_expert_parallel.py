@@ -1,6 +1,6 @@
 """Expert parallelism, host logic on the CPU: the shard ranges, the owner
-map, and the two exchange patterns as gloo process groups (world sizes 2 and
-3), with each rank's experts computed by the oracle restricted to that
+map, and the two exchange patterns as gloo process groups (world sizes 2 to
+4), with each rank's experts computed by the oracle restricted to that
 rank's shard (the weights of other ranks' picks set to 0).  The sum over the
 ranks must be the whole layer's output (the oracle's, in binary64, within
 fp32 rounding of the partial sums), and each rank must receive exactly the
@@ -91,7 +91,7 @@ def _worker(rank, world, port, q, case):
                 err = np.abs(y.numpy() - y_full) - (1e-6 + 1e-5 * np.abs(y_full))
                 q.put((rank, case, T, float(err.max())))
         else:
-            counts = [6, 11] if world == 2 else [4, 0, 7]
+            counts = {2: [6, 11], 3: [4, 0, 7], 4: [3, 5, 0, 1]}[world]
             x, lg = _tokens(wl, rank, counts[rank])
             idx, w = oracle.topk(lg, K) if counts[rank] else (np.zeros((0, K), np.int32), np.zeros((0, K)))
             seen = {}
@@ -150,7 +150,7 @@ def test_replicated_tokens_allreduce_of_partials_is_the_layer(world):
         assert err <= 0.0, (rank, T, err)
 
 
-@pytest.mark.parametrize("world", [2, 3])
+@pytest.mark.parametrize("world", [2, 3, 4])
 def test_distributed_tokens_dispatch_and_combine(world):
     synth.build()
     oracle.build()
