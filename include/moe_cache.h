@@ -47,7 +47,8 @@ extern "C" {
 #define MOE_ERR_TIMEOUT (-5)    /* a host-side poll limit was exceeded */
 #define MOE_ERR_CAPACITY (-6)   /* an output buffer is too small */
 #define MOE_ERR_STATE (-7)      /* call not valid in the current state */
-#define MOE_ERR_FAULT (-8)      /* an injected (test) upload fault */
+#define MOE_ERR_FAULT (-8)      /* a kernel reported a fault (expert id out of range, expired bounded
+                                   wait), or an injected (test) upload failure */
 
 #define MOE_KIND_GATE 0
 #define MOE_KIND_UP 1
@@ -132,7 +133,9 @@ typedef struct moe_stats_t {
  * Create a context on cfg->device.  cuda_stream (cudaStream_t; NULL is the
  * legacy default stream, as everywhere in CUDA) is the stream every forward
  * of this context runs on; the caller keeps owning it.  The library allocates and owns: the HBM
- * expert pool (3*L*slots_per_tensor slots of rows*cols/32*(18, 34, 22 or 24) bytes), the
+ * expert pool (3*L*slots_per_tensor slots of one expert tensor's plane blob:
+ * 18, 34, 22, 24, 26.25 or 28 bytes per 32 weights for Q4_0, Q8_0, Q5_0,
+ * Q4_K, Q6_K or Q5_K, rounded up to 256 bytes), the
  * pointer tables, stamps, miss log, workspaces, an upload stream and the
  * pinned host copies of registered tensors.  *out receives the context.
  * Errors: MOE_ERR_ARG (sizes), MOE_ERR_OOM, MOE_ERR_CUDA.
@@ -140,10 +143,14 @@ typedef struct moe_stats_t {
 int moe_layer_init(const moe_cfg *cfg, void *cuda_stream, moe_ctx **out);
 
 /*
- * Register one expert tensor (layer, kind) and seed its pool.
+ * Register one expert tensor (layer, kind) and seed its pool
+ * (Zapdev-labs/a6000-custom-kernels, after the pointer-table diagram: every
+ * expert tensor has its own table, pool and stamps, and pools are seeded at
+ * registration from a routing-frequency table).
  * host_q4: canonical tensor [n_experts][rows][cols/32][18 B] (Q4_0),
- *   [...][34 B] (Q8_0), [...][22 B] (Q5_0) or [n_experts][rows][cols/256][144 B]
- *   (Q4_K), per cfg.weight_format, any host
+ *   [...][34 B] (Q8_0), [...][22 B] (Q5_0), or [n_experts][rows][cols/256]
+ *   super-blocks of 144 B (Q4_K), 210 B (Q6_K) or 176 B (Q5_K), per
+ *   cfg.weight_format, any host
  *   memory; the library copies it into its own pinned, device-mapped host
  *   memory in plane layout (all codes, then all scales) and never reads
  *   host_q4 again, so the caller may free it on return.
@@ -200,8 +207,9 @@ int route_topk(moe_ctx *ctx, const float *d_logits, int n_tokens, int n_experts,
  * expert e = d_idx[t][j] computes h = silu(gate_e . x_t) * (up_e . x_t)
  * from int8-quantized x (blocks of 32, binary16 scale), quantizes h the
  * same way, computes o = down_e . h, and y[t] = sum_j d_w[t][j] * o.
- * Block dots are exact int32 sums of (q_w - 8) * q_a; each block is scaled
- * by d_w * d_a in fp32.  Each expert's weights are read through the
+ * Block dots are exact int32 sums of (q_w - 8) * q_a (Q4_0; the other
+ * formats' codes and offsets as defined above); each block is scaled by
+ * d_w * d_a in fp32 (K-quants: by their sub-block scales and mins).  Each expert's weights are read through the
  * tensor's pointer table: pool slot (tag 0, HBM) or pinned host memory
  * (tag 1, read zero-copy).  Cold reads are logged once per (tensor,
  * expert) in the miss log; pool hits write the step's clock into the
@@ -217,7 +225,8 @@ int moe_ffn_forward(moe_ctx *ctx, int layer, const float *d_x, int n_tokens, con
                     const float *d_w, float *d_y, void *stream);
 
 /*
- * route_topk followed by moe_ffn_forward, as one call: same results (d_idx
+ * route_topk followed by moe_ffn_forward, as one call (the router top-k and
+ * the pointer-table mat-vec of the two calls' sources): same results (d_idx
  * and d_w are written as route_topk writes them), and for small batches
  * (n_tokens <= 32, n_tokens*k <= 256) one kernel launch in which every CTA
  * routes the tokens itself.  d_logits: fp32 [n_tokens][E] device.
@@ -247,12 +256,14 @@ int moe_ffn_forward_routed(moe_ctx *ctx, int layer, const float *d_x, const floa
 int moe_set_expert_shard(moe_ctx *ctx, int expert_base, int n_route);
 
 /*
- * moe_ffn_forward over n_rows token rows that are part of a step of
+ * Dispatched rows of an expert shard (neurall/llama.cpp README, "More GPUs";
+ * see moe_set_expert_shard): moe_ffn_forward over n_rows token rows that are part of a step of
  * step_tokens tokens (step_tokens >= n_rows): an expert-parallel rank that
  * receives only the rows routed to its experts stamps its pool hits with the
  * clock of the whole step (clock + step_tokens), as a rank that saw every
  * token would, and the caller passes step_tokens to cache_step.  Otherwise
- * as moe_ffn_forward.  Errors: as moe_ffn_forward.
+ * as moe_ffn_forward.  Errors: as moe_ffn_forward, and MOE_ERR_ARG when
+ * n_rows < 0 or step_tokens < max(n_rows, 1).
  */
 int moe_ffn_forward_rows(moe_ctx *ctx, int layer, const float *d_x, int n_rows, const int32_t *d_idx,
                          const float *d_w, float *d_y, int step_tokens, void *stream);
@@ -284,11 +295,14 @@ int cache_step(moe_ctx *ctx, int n_tokens);
 
 /*
  * Copy the miss keys logged since the last cache_step (or drain) to
- * host_out, sorted ascending, unique, and clear the log.  *n_out gets the
+ * host_out, sorted ascending, unique, and clear the log (the miss recorder
+ * of Zapdev-labs/a6000-custom-kernels, after the pointer-table diagram:
+ * (tensor_id << 12 | expert) keys in a device buffer).  *n_out gets the
  * count even when cap is too small (then MOE_ERR_CAPACITY and the log is
  * kept).  Synchronizes with the context stream.  MOE_ERR_FAULT (after the
  * keys are out and the log is cleared): a device error was reported, as for
- * cache_step.
+ * cache_step.  n_out may be NULL.  Errors: MOE_ERR_ARG (NULL host_out when
+ * there are keys to copy), MOE_ERR_CAPACITY, MOE_ERR_FAULT, MOE_ERR_CUDA.
  */
 int miss_drain(moe_ctx *ctx, uint32_t *host_out, size_t cap, size_t *n_out);
 
@@ -304,7 +318,10 @@ int miss_drain(moe_ctx *ctx, uint32_t *host_out, size_t cap, size_t *n_out);
 int moe_pool_borrow(moe_ctx *ctx, int n_slots, void **d_ws, size_t *bytes);
 
 /*
- * Give the lent slots back: each returned pool slot, in ascending global
+ * Give the lent slots back (neurall/llama.cpp, "How it works": when the
+ * prompt pass ends its space goes back to the expert cache, refilled with
+ * the hot experts and, with prefill preheat, the ones the pass used): each
+ * returned pool slot, in ascending global
  * order, is refilled (stamp = clock) with the best non-resident expert, by
  * (use count of the prompt pass, descending; rank in its tensor's seed
  * order, ascending; tensor id, ascending).  Per-tensor pools take the slot's
@@ -315,7 +332,8 @@ int moe_pool_borrow(moe_ctx *ctx, int n_slots, void **d_ws, size_t *bytes);
 int moe_pool_return(moe_ctx *ctx);
 
 /*
- * Upload overlap (eager forwards).  By default the promotion pass makes the
+ * Upload overlap (eager forwards; no counterpart on the source pages, an
+ * ordering refinement of the promotion pass's uploads).  By default the promotion pass makes the
  * context stream wait for all of its pool uploads before the next forward.
  * With enable = 1 it records one event per layer after that layer's uploads
  * instead, and a layer's next forward waits only for its own layer's event,
@@ -360,7 +378,8 @@ int moe_set_global_pool(moe_ctx *ctx, int enable);
 int moe_set_preheat(moe_ctx *ctx, int enable);
 
 /*
- * Put the cache back in its registered state, with a pool mode chosen anew
+ * Put the cache back in its registered state (no counterpart on the source
+ * pages: lets measurements start from the same seeded state), with a pool mode chosen anew
  * (global_pool = 1: one pool for all layers, as moe_set_global_pool; 0: a
  * pool per tensor).  Every tensor holds its seeded experts again (seed order
  * in local slots 0..n_seed-1; slots already holding their seed expert are
@@ -374,11 +393,13 @@ int moe_set_preheat(moe_ctx *ctx, int enable);
 int moe_cache_reset(moe_ctx *ctx, int global_pool);
 
 /*
- * Owner and stamp of every arena slot (3L x slots_per_tensor entries, global
- * slot g = local slot g / 3L of tensor g % 3L), either pool mode; synchronizes
- * with all streams.  owner_key: (tensor_id << 12 | expert), or -1 for a free,
- * lent or unused slot; stamps: the device stamp of the slot.  Either output
- * may be NULL.
+ * Owner and stamp of every arena slot (inspection, for tests of the shared
+ * pool of neurall/llama.cpp, "How it works"; 3L x slots_per_tensor entries,
+ * global slot g = local slot g / 3L of tensor g % 3L), either pool mode;
+ * synchronizes with all streams.  owner_key: (tensor_id << 12 | expert), or
+ * -1 for a free, lent or unused slot; stamps: the device stamp of the slot.
+ * Either output may be NULL; host arrays of 3L x slots_per_tensor entries.
+ * Errors: MOE_ERR_ARG (NULL context), MOE_ERR_CUDA.
  */
 int moe_pool_snapshot(moe_ctx *ctx, int32_t *owner_key, uint32_t *stamps);
 
@@ -423,34 +444,49 @@ int moe_set_lookahead(moe_ctx *ctx, int enable);
 int moe_set_router(moe_ctx *ctx, int layer, const float *host_w, const float *host_b);
 
 /*
- * Snapshot of one tensor's cache state (synchronizes with all streams).
+ * Snapshot of one tensor's cache state (inspection for tests: the table,
+ * slots and stamps of Zapdev-labs/a6000-custom-kernels' pointer-table cache;
+ * synchronizes with all streams).
  * Any output may be NULL.  tbl: uint64 [E], the device pointer table as the
  * kernels read it; slot_of: int32 [E] (-1 = cold; the local slot, or the
  * global slot with a shared pool); last_seen: int32 [E] (-1 = no sighting);
  * owner: int32 [slots_per_tensor] (-1 = free or lent; with a shared pool,
  * the expert of this tensor held in its home slot s * 3L + tensor_id, -1 if
  * another tensor's or free); stamps: uint32 [slots_per_tensor] (device stamp
- * of each of those slots).
+ * of each of those slots).  All host arrays.  Errors: MOE_ERR_ARG (NULL
+ * context, tensor_id out of range or not registered), MOE_ERR_CUDA.
  */
 int moe_cache_snapshot(moe_ctx *ctx, int tensor_id, uint64_t *tbl, int32_t *slot_of, int32_t *last_seen,
                        int32_t *owner, uint32_t *stamps);
 
-/* Base addresses used by table entries: the pool and the pinned host copy
- * of one tensor (expert e of the tensor lives at host_base + e*tensor_slot). */
+/* Base addresses used by table entries (inspection for tests): the pool and
+ * the pinned host copy of one tensor (expert e of the tensor lives at
+ * host_base + e * slot_bytes, once the tensor is registered); *n_tensors =
+ * 3L.  Any output may be NULL.  Errors: MOE_ERR_ARG (NULL context,
+ * tensor_id out of range). */
 int moe_cache_layout(moe_ctx *ctx, int tensor_id, uint64_t *pool_base, uint64_t *host_base,
                      uint64_t *slot_bytes, int32_t *n_tensors);
 
+/* Counters since init (moe_cache_reset restarts all but upload_bytes; the
+ * pages report cache hit rates: neurall/llama.cpp, features table): see
+ * moe_stats_t.  Synchronizes with the context stream when decode lookahead
+ * is set up (its two counters live on the device).  Errors: MOE_ERR_ARG
+ * (NULL context or out), MOE_ERR_CUDA. */
 int moe_stats(moe_ctx *ctx, moe_stats_t *out);
 
 /* Message of the last error on ctx (or, when ctx is NULL, of the last failed
- * call that takes no context: moe_layer_init, moe_probe_host_read,
- * moe_expert_ffn_noalloc).  Valid until the next such call. */
+ * call that takes no context or was given a NULL one: moe_layer_init,
+ * moe_probe_host_read, moe_expert_ffn_noalloc[_status]; kept per host
+ * thread).  Valid until the next such call.  Never fails; "" when there was
+ * none. */
 const char *moe_last_error(moe_ctx *ctx);
 
-/* Release everything the context owns.  Synchronizes first. */
+/* Release everything the context owns.  Synchronizes first.  NULL is a
+ * no-op.  Returns nothing. */
 void moe_destroy(moe_ctx *ctx);
 
-/* ---- inspection and measurement hooks (tests, benchmark) ---------------- */
+/* ---- inspection and measurement hooks (tests, benchmark; no counterpart
+ * on the source pages) ---------------------------------------------------- */
 
 /*
  * Integer block dots of the mat-vec kernels' block-dot routine: out[r][b] =
@@ -506,7 +542,8 @@ int moe_debug_busy(moe_ctx *ctx, int microseconds);
  * prompt batches (also inside a captured graph).  moe_debug_timing_read
  * synchronizes and writes, per layer, the device time in ms of the most
  * recent gate/up and down launch of that layer since the last read (0 when
- * the layer ran no forward); both arrays hold n_layers doubles.
+ * the layer ran no forward); both arrays hold n_layers doubles (host;
+ * either may be NULL).  Errors: MOE_ERR_ARG (NULL context), MOE_ERR_CUDA.
  */
 int moe_debug_timing(moe_ctx *ctx, int enable);
 int moe_debug_timing_read(moe_ctx *ctx, double *gate_up_ms, double *down_ms);
