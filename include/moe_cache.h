@@ -130,7 +130,9 @@ typedef struct moe_stats_t {
 } moe_stats_t;
 
 /*
- * Create a context on cfg->device.  cuda_stream (cudaStream_t; NULL is the
+ * Create a context on cfg->device (the per-tensor tables, HBM pools, stamps
+ * and miss buffer of Zapdev-labs/a6000-custom-kernels, after the
+ * pointer-table diagram, sized by the caller).  cuda_stream (cudaStream_t; NULL is the
  * legacy default stream, as everywhere in CUDA) is the stream every forward
  * of this context runs on; the caller keeps owning it.  The library allocates and owns: the HBM
  * expert pool (3*L*slots_per_tensor slots of one expert tensor's plane blob:
@@ -225,8 +227,9 @@ int moe_ffn_forward(moe_ctx *ctx, int layer, const float *d_x, int n_tokens, con
                     const float *d_w, float *d_y, void *stream);
 
 /*
- * route_topk followed by moe_ffn_forward, as one call (the router top-k and
- * the pointer-table mat-vec of the two calls' sources): same results (d_idx
+ * route_topk followed by moe_ffn_forward, as one call (the top-k of
+ * mihailescu2m/llama.cpp and the pointer-table mat-vec of
+ * Zapdev-labs/a6000-custom-kernels, as in those two calls): same results (d_idx
  * and d_w are written as route_topk writes them), and for small batches
  * (n_tokens <= 32, n_tokens*k <= 256) one kernel launch in which every CTA
  * routes the tokens itself.  d_logits: fp32 [n_tokens][E] device.
@@ -459,11 +462,12 @@ int moe_set_router(moe_ctx *ctx, int layer, const float *host_w, const float *ho
 int moe_cache_snapshot(moe_ctx *ctx, int tensor_id, uint64_t *tbl, int32_t *slot_of, int32_t *last_seen,
                        int32_t *owner, uint32_t *stamps);
 
-/* Base addresses used by table entries (inspection for tests): the pool and
- * the pinned host copy of one tensor (expert e of the tensor lives at
- * host_base + e * slot_bytes, once the tensor is registered); *n_tensors =
- * 3L.  Any output may be NULL.  Errors: MOE_ERR_ARG (NULL context,
- * tensor_id out of range). */
+/* Base addresses used by table entries (inspection for tests; the pool and
+ * host copies the pointer tables of Zapdev-labs/a6000-custom-kernels point
+ * into): the pool and the pinned host copy of one tensor (expert e of the
+ * tensor lives at host_base + e * slot_bytes, once the tensor is
+ * registered); *n_tensors = 3L.  Any output may be NULL.  Errors:
+ * MOE_ERR_ARG (NULL context, tensor_id out of range). */
 int moe_cache_layout(moe_ctx *ctx, int tensor_id, uint64_t *pool_base, uint64_t *host_base,
                      uint64_t *slot_bytes, int32_t *n_tensors);
 
@@ -474,15 +478,16 @@ int moe_cache_layout(moe_ctx *ctx, int tensor_id, uint64_t *pool_base, uint64_t 
  * (NULL context or out), MOE_ERR_CUDA. */
 int moe_stats(moe_ctx *ctx, moe_stats_t *out);
 
-/* Message of the last error on ctx (or, when ctx is NULL, of the last failed
+/* (No counterpart on the source pages.)  Message of the last error on ctx
+ * (or, when ctx is NULL, of the last failed
  * call that takes no context or was given a NULL one: moe_layer_init,
  * moe_probe_host_read, moe_expert_ffn_noalloc[_status]; kept per host
  * thread).  Valid until the next such call.  Never fails; "" when there was
  * none. */
 const char *moe_last_error(moe_ctx *ctx);
 
-/* Release everything the context owns.  Synchronizes first.  NULL is a
- * no-op.  Returns nothing. */
+/* Release everything the context owns (no counterpart on the source
+ * pages).  Synchronizes first.  NULL is a no-op.  Returns nothing. */
 void moe_destroy(moe_ctx *ctx);
 
 /* ---- inspection and measurement hooks (tests, benchmark; no counterpart
@@ -520,7 +525,7 @@ int moe_probe_host_read(const void *host_pinned, size_t bytes, int iters, double
  * Test hook: make the n-th following pool upload (1-based; 0 = off) report
  * failure; the step rolls that admission back (the expert stays cold, the
  * victim stays evicted) and returns MOE_ERR_FAULT after finishing the
- * step consistently.
+ * step consistently.  Errors: MOE_ERR_ARG (NULL context, nth < 0).
  */
 int moe_debug_fail_upload(moe_ctx *ctx, int nth);
 

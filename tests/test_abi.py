@@ -107,3 +107,31 @@ def test_noalloc_and_probe_reject_bad_arguments_without_a_device():
     assert call(n_tokens=0, ptr=None) == 0   # nothing to do: no pointer is read
     gbs = ctypes.c_double()
     assert lib.moe_probe_host_read(None, 1 << 20, 1, ctypes.byref(gbs), None) == -1
+
+
+def _declarations_with_docs():
+    """(name, the comment just before its declaration) for every function the
+    header declares; the hooks at the end share their section's note."""
+    src = open(os.path.join(ROOT, "include", "moe_cache.h")).read()
+    comments = [(m.end(), m.group(1)) for m in re.finditer(r"/\*(.*?)\*/", src, flags=re.S)]
+    hooks_at = src.index("inspection and measurement hooks")
+    out = []
+    for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\**\s*([A-Za-z_][A-Za-z0-9_]*)\s*\(",
+                         src, flags=re.M):
+        before = [c for end, c in comments if end <= m.start()]
+        assert before, m.group(1)
+        doc = before[-1]
+        if m.start() > hooks_at:
+            doc += " (no counterpart on the source pages)"
+        out.append((m.group(1), doc))
+    return out
+
+
+def test_every_declaration_cites_its_passage_and_states_its_errors():
+    docs = _declarations_with_docs()
+    assert {n for n, _ in docs} == _declared_functions()
+    pages = ("Zapdev-labs", "neurall/llama.cpp", "mihailescu2m/llama.cpp", "mx-llama.cpp", "no counterpart",
+             "No counterpart")
+    for name, doc in docs:
+        assert any(p in doc for p in pages), name
+        assert any(k in doc for k in ("Errors", "MOE_ERR_", "Never fails", "Returns nothing")), name
