@@ -2,7 +2,7 @@
 read from a committed ncu summary only while the kernel's sources match the
 capture, the source hash over a marked section of a file, the clock sampler's
 parsing of nvidia-smi samples (median SM clock, throttle reasons) and the
-fallback peaks."""
+fallback peaks, and the reference arm's JSON line (it runs on the host cores)."""
 import os
 
 import bench
@@ -80,3 +80,30 @@ def test_peaks_fall_back_without_the_measured_file(tmp_path, monkeypatch):
     (tmp_path / "MEASURED_PEAKS.json").write_text('{"hbm_gbs": 1234.0, "bf16_tflops": 1.0}')
     peaks, src = bench.load_peaks()
     assert src == "measured" and peaks["hbm_gbs"] == 1234.0
+
+
+def test_reference_arm_prints_one_contract_line():
+    # the reference arm is the oracle on the host cores: it runs here too
+    import json
+    import subprocess
+    import sys
+
+    env = dict(os.environ)
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        env.pop(k, None)
+    out = subprocess.run([sys.executable, os.path.join(bench.ROOT, "bench.py"), "--impl", "reference",
+                          "--steps", "1", "--warmup", "3"], capture_output=True, text=True, timeout=600, env=env,
+                         cwd=bench.ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [ln for ln in out.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    r = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in r, key
+    assert r["impl"] == "reference" and r["steps"] == 1 and r["warmup"] == 3 and r["n_gpus"] == 1
+    assert r["value"] > 0 and r["higher_is_better"] is True and r["unit"] == "tokens/s"
+    assert r["config"]["workload"].startswith("decode_b1_resident")
+    cb = r["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == r["value"] and cb["cores"] >= 1 and cb["sample"]
+    assert r["e2e"] == {"value": r["value"], "unit": r["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
