@@ -9,13 +9,18 @@ import pytest
 
 import quantized_expert_cache_gb300 as qec
 
+
+def _read(path):
+    with open(path) as f:
+        return f.read()
+
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 def _declared_functions():
     names = set()
     for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
-        src = open(h).read()
+        src = _read(h)
         src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
         for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\**\s*([A-Za-z_][A-Za-z0-9_]*)\s*\(",
                              src, flags=re.M):
@@ -112,7 +117,7 @@ def test_noalloc_and_probe_reject_bad_arguments_without_a_device():
 def _declarations_with_docs():
     """(name, the comment just before its declaration) for every function the
     header declares; the hooks at the end share their section's note."""
-    src = open(os.path.join(ROOT, "include", "moe_cache.h")).read()
+    src = _read(os.path.join(ROOT, "include", "moe_cache.h"))
     comments = [(m.end(), m.group(1)) for m in re.finditer(r"/\*(.*?)\*/", src, flags=re.S)]
     hooks_at = src.index("inspection and measurement hooks")
     out = []

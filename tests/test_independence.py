@@ -9,6 +9,11 @@ import os
 
 import pytest
 
+
+def _read(path):
+    with open(path) as f:
+        return f.read()
+
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
@@ -23,13 +28,13 @@ def test_product_sources_never_name_the_oracle():
     srcs = _files("quantized_expert_cache_gb300", (".py", ".cu", ".cuh", ".h", ".cpp")) + _files("include", (".h",))
     assert srcs
     for f in srcs:
-        text = open(f).read().lower()
+        text = _read(f).lower()
         assert "oracle" not in text, f
 
 
 def test_oracle_does_not_import_the_library():
     for f in _files("oracle", (".py", ".c", ".h")):
-        text = open(f).read()
+        text = _read(f)
         assert "quantized_expert_cache_gb300" not in text, f
         assert "libmoecache" not in text, f
         assert "csrc" not in text, f
@@ -37,7 +42,7 @@ def test_oracle_does_not_import_the_library():
 
 def test_generators_hold_no_library_or_oracle_code():
     for f in _files("synth", (".py", ".c", ".h")):
-        text = open(f).read()
+        text = _read(f)
         assert "quantized_expert_cache_gb300" not in text and "libmoecache" not in text, f
         for line in text.splitlines():
             s = line.strip()
@@ -48,7 +53,7 @@ def test_generators_hold_no_library_or_oracle_code():
 @pytest.mark.parametrize("script", ["bench.py", "__graft_entry__.py"])
 def test_oracle_imported_only_by_the_allowed_functions(script):
     allowed = {"bench.py": {"cpu_baseline", "run_reference"}, "__graft_entry__.py": {"build", "smoke"}}[script]
-    tree = ast.parse(open(os.path.join(ROOT, script)).read())
+    tree = ast.parse(_read(os.path.join(ROOT, script)))
     found = []
 
     def visit(node, fn):
@@ -70,7 +75,7 @@ def test_oracle_imported_only_by_the_allowed_functions(script):
 def test_library_link_line_names_no_oracle_object():
     from quantized_expert_cache_gb300 import build as b
 
-    src = open(b.__file__).read()
+    src = _read(b.__file__)
     assert "oracle" not in src.lower()
     # every translation unit and header the library compiles is in its csrc/
     for s in b.SOURCES + b.HEADERS:

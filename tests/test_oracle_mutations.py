@@ -96,7 +96,8 @@ def _failing_pins(run):
 
 
 def _build_mutant(old, new, tmp):
-    src = open(oracle._SRC).read()
+    with open(oracle._SRC) as f:
+        src = f.read()
     assert src.count(old) == 1, old
     path = os.path.join(tmp, "mutant.c")
     with open(path, "w") as f:
@@ -155,7 +156,8 @@ P_GOLDEN_PINS = [ppins.test_hand_traced_sequence, ppins.test_hand_traced_borrow_
 
 
 def _load_policy_mutant(old, new, tmp):
-    src = open(os.path.join(os.path.dirname(oracle.__file__), "policy.py")).read()
+    with open(os.path.join(os.path.dirname(oracle.__file__), "policy.py")) as f:
+        src = f.read()
     assert src.count(old) == 1, old
     path = os.path.join(tmp, "policy_mutant.py")
     with open(path, "w") as f:
