@@ -14,6 +14,7 @@ def _read(path):
     with open(path) as f:
         return f.read()
 
+
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
