@@ -216,7 +216,9 @@ int route_topk(moe_ctx *ctx, const float *d_logits, int n_tokens, int n_experts,
  * (tag 1, read zero-copy).  Cold reads are logged once per (tensor,
  * expert) in the miss log; pool hits write the step's clock into the
  * slot's stamp.  n_tokens <= 32 runs the mat-vec kernels; larger batches
- * run the grouped per-expert GEMM over tokens sorted by expert.
+ * run the grouped per-expert GEMM over tokens sorted by expert (Q4_0
+ * contexts with hidden and ffn multiples of 64; other contexts run the
+ * mat-vec kernels at every size).
  * d_x: fp32 [n_tokens][H] device; d_idx/d_w as produced by route_topk;
  * d_y: fp32 [n_tokens][H] device, written.  `stream` must be the
  * context's stream (or NULL).  Asynchronous; capturable in a CUDA graph
