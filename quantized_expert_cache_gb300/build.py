@@ -11,7 +11,7 @@ CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libmoecache.so")
 SOURCES = ["moe_cache.cu", "kernels_decode.cu", "kernels_gemm.cu", "no_alloc.cu"]
-HEADERS = ["common.cuh", "kernels.h"]
+HEADERS = ["common.cuh", "kernels.h", "repack.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
               "-I" + os.path.join(ROOT, "include"), "-I" + CSRC]
