@@ -110,6 +110,15 @@ def test_noalloc_and_probe_reject_bad_arguments_without_a_device():
     assert call(top_k=0) == -1 and call(top_k=9) == -1
     assert call(n_tokens=33) == -1          # more tokens than the single launch holds
     assert call(n_tokens=1, ptr=None) == -1  # a null pointer
+    # above the 8 MiB array: refused before any device work, and the bytes the
+    # message names follow the header's estimate T*k*(4H + F + F/4) + T*(H + H/4)
+    # plus the small tables
+    T, k, H, F, E = 32, 8, 8192, 8192, 64
+    assert call(n_tokens=T, hidden=H, ffn=F, n_experts=E, top_k=k) == -6
+    msg = qec.moe_last_error(None)
+    need = int(re.search(r"needs (\d+) scratch bytes", msg).group(1))
+    estimate = T * k * (4 * H + F + F // 4) + T * (H + H // 4)
+    assert estimate <= need <= estimate + 64 * 1024, (need, estimate)
     assert call(n_tokens=0, ptr=None) == 0   # nothing to do: no pointer is read
     gbs = ctypes.c_double()
     assert lib.moe_probe_host_read(None, 1 << 20, 1, ctypes.byref(gbs), None) == -1
