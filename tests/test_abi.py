@@ -150,3 +150,40 @@ def test_every_declaration_cites_its_passage_and_states_its_errors():
     for name, doc in docs:
         assert any(p in doc for p in pages), name
         assert any(k in doc for k in ("Errors", "MOE_ERR_", "Never fails", "Returns nothing")), name
+
+
+def test_header_is_plain_c_and_the_library_links_from_c(tmp_path):
+    # the boundary is a C ABI: the header compiles as C99 with warnings as
+    # errors, and a C program linked against the library calls it
+    import shutil
+    import subprocess
+
+    if shutil.which("gcc") is None:
+        pytest.skip("needs gcc")
+    qec.build.build()
+    lib = qec.lib_path()
+    src = tmp_path / "use_abi.c"
+    src.write_text(r"""
+#include <stdio.h>
+#include <string.h>
+#include "moe_cache.h"
+int main(void) {
+    moe_cfg cfg;
+    memset(&cfg, 0, sizeof cfg);
+    cfg.hidden = 100; /* not a multiple of 32 */
+    cfg.ffn = 64; cfg.n_experts = 8; cfg.top_k = 2; cfg.n_layers = 1;
+    cfg.slots_per_tensor = 8; cfg.max_tokens = 4; cfg.window_tokens = 64; cfg.renorm_topk = 1;
+    moe_ctx *ctx = NULL;
+    int rc = moe_layer_init(&cfg, NULL, &ctx);
+    printf("%d %s\n", rc, moe_last_error(NULL));
+    moe_destroy(NULL);
+    return rc == MOE_ERR_ARG && ctx == NULL ? 0 : 1;
+}
+""")
+    exe = tmp_path / "use_abi"
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I",
+                    os.path.join(ROOT, "include"), str(src), "-o", str(exe), lib,
+                    "-Wl,-rpath," + os.path.dirname(lib)], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert out.returncode == 0, out.stdout + out.stderr
+    assert out.stdout.startswith("-1 ") and "hidden" in out.stdout
